@@ -1,0 +1,319 @@
+// api.cu -- the C ABI declared in include/zc.h: argument checks, plan objects,
+// workspace sizing and kernel launches.  No arithmetic of the codecs lives
+// here; see zc_plan.cu, zc_codec.cu, ibp_meta.cu and ibp_codec.cu.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+#include "zc.h"
+
+struct zc_plan_s {
+  int device;
+  lbb::ZcLayout L;
+  lbb::ZcSegDev* d_segs;
+  std::vector<lbb::ZcSegDev> h_segs;
+};
+
+namespace lbb {
+
+int resident_blocks(const void* kernel, int threads, size_t smem) {
+  struct Entry {
+    const void* k;
+    int dev, threads;
+    size_t smem;
+    int blocks;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (const Entry& e : cache)
+      if (e.k == kernel && e.dev == dev && e.threads == threads && e.smem == smem) return e.blocks;
+  }
+  int sms = 1, per = 1;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, threads, smem) != cudaSuccess ||
+      per < 1)
+    per = 1;
+  const int blocks = per * sms;
+  std::lock_guard<std::mutex> g(mu);
+  cache.push_back(Entry{kernel, dev, threads, smem, blocks});
+  return blocks;
+}
+
+}  // namespace lbb
+
+namespace {
+
+using lbb::kCtrlBytes;
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? ZC_OK : ZC_ERR_CUDA; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t zc_ws_bytes(const lbb::ZcLayout& L) {
+  const unsigned long long a = L.nunits * sizeof(lbb::StatPartial);
+  const unsigned long long b = L.ntiles * 8ull;
+  return (size_t)lbb::round_up_dev(kCtrlBytes + std::max(a, b), 256);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* zc_strerror(int code) {
+  switch (code) {
+    case ZC_OK: return "ok";
+    case ZC_ERR_ARG: return "invalid argument";
+    case ZC_ERR_CAPACITY: return "output or workspace buffer too small";
+    case ZC_ERR_FORMAT: return "stream is corrupt or inconsistent";
+    case ZC_ERR_META_MISMATCH: return "stream was made with other IBP metadata";
+    case ZC_ERR_TIMEOUT: return "a bounded wait between thread blocks ran out";
+    case ZC_ERR_CUDA: return "CUDA runtime error";
+    case ZC_ERR_UNSUPPORTED: return "parameter legal in the format but not supported by the GPU path";
+    case ZC_ERR_NOMEM: return "allocation failed";
+    default: return "unknown error";
+  }
+}
+
+int zc_version(void) { return 100; }
+
+int zc_status(const void* d_ws, zc_stream_t stream, int* h_status) {
+  if (!d_ws || !h_status) return ZC_ERR_ARG;
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, d_ws, sizeof(int), cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return ZC_ERR_CUDA;
+  *h_status = v;
+  return ZC_OK;
+}
+
+// ------------------------------------------------------------------ ZipCCL
+
+int zc_plan_create(uint64_t n, const uint64_t* h_seg_off, uint32_t nseg, uint32_t C,
+                   zc_plan_t* out_plan) {
+  if (!out_plan) return ZC_ERR_ARG;
+  *out_plan = nullptr;
+  if (nseg == 0 || (!h_seg_off && nseg != 1)) return ZC_ERR_ARG;
+  if (C < 1024u || C > 65536u || (C % 1024u) != 0) return ZC_ERR_ARG;
+  if ((C & (C - 1)) != 0) return ZC_ERR_UNSUPPORTED;  // GPU tiles need a power of two
+  if (n > (1ull << 46)) return ZC_ERR_ARG;
+  if (h_seg_off) {
+    if (h_seg_off[0] != 0 || h_seg_off[nseg] != n) return ZC_ERR_ARG;
+    for (uint32_t s = 0; s < nseg; ++s)
+      if (h_seg_off[s + 1] < h_seg_off[s]) return ZC_ERR_ARG;
+  }
+  zc_plan_s* p = new (std::nothrow) zc_plan_s();
+  if (!p) return ZC_ERR_NOMEM;
+  lbb::ZcLayout& L = p->L;
+  L.n = n;
+  L.nseg = nseg;
+  L.C = C;
+  L.log2C = 0;
+  while ((1u << L.log2C) < C) ++L.log2C;
+  // statistics unit: a power of two between 4096 and 65536 elements, fixed by n
+  unsigned long long U = 4096;
+  while (U < 65536 && U * 2 <= n / 1024) U *= 2;
+  L.U = (uint32_t)U;
+  try {
+    p->h_segs.resize(nseg);
+  } catch (...) {
+    delete p;
+    return ZC_ERR_NOMEM;
+  }
+  unsigned long long chunks = 0, units = 0;
+  for (uint32_t s = 0; s < nseg; ++s) {
+    const unsigned long long b = h_seg_off ? h_seg_off[s] : 0;
+    const unsigned long long e = h_seg_off ? h_seg_off[s + 1] : n;
+    lbb::ZcSegDev& r = p->h_segs[s];
+    std::memset(&r, 0, sizeof r);
+    r.elem_start = b;
+    r.nelem = e - b;
+    r.chunk_start = chunks;
+    r.nchunks = (r.nelem + C - 1) / C;
+    r.unit_start = units;
+    chunks += r.nchunks;
+    units += (r.nelem + U - 1) / U;
+  }
+  L.nchunks = chunks;
+  L.nunits = units;
+  L.ntiles = (chunks * C + lbb::kTileLanes - 1) / lbb::kTileLanes;
+  L.slot_bytes = (unsigned long long)C * 11ull / 8ull;
+  L.off_seg = lbb::kZcHeader;
+  L.off_escoff = L.off_seg + lbb::round_up_dev((unsigned long long)lbb::kZcSegRec * nseg, lbb::kZcAlign);
+  L.off_static = L.off_escoff + lbb::round_up_dev(8ull * (chunks + 1), lbb::kZcAlign);
+  L.off_esc = L.off_static + chunks * L.slot_bytes;
+  if (units > 0x7FFFFFFFull) {
+    delete p;
+    return ZC_ERR_ARG;
+  }
+  cudaGetDevice(&p->device);
+  if (cudaMalloc(&p->d_segs, sizeof(lbb::ZcSegDev) * nseg) != cudaSuccess) {
+    delete p;
+    return ZC_ERR_NOMEM;
+  }
+  if (cudaMemcpy(p->d_segs, p->h_segs.data(), sizeof(lbb::ZcSegDev) * nseg,
+                 cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(p->d_segs);
+    delete p;
+    return ZC_ERR_CUDA;
+  }
+  *out_plan = p;
+  return ZC_OK;
+}
+
+void zc_plan_destroy(zc_plan_t p) {
+  if (!p) return;
+  cudaFree(p->d_segs);
+  delete p;
+}
+
+size_t zc_workspace_bytes(zc_plan_t p) { return p ? zc_ws_bytes(p->L) : 0; }
+
+uint64_t zc_max_compressed_bytes(zc_plan_t p) {
+  if (!p) return 0;
+  return p->L.off_esc + lbb::round_up_dev(p->L.n, lbb::kZcAlign);
+}
+
+int zc_plan(zc_plan_t p, const uint16_t* d_x, void* d_ws, size_t ws_bytes, zc_stream_t stream) {
+  if (!p || !d_ws || (!d_x && p->L.n) || !aligned(d_ws, 256) || !aligned(d_x, 2)) return ZC_ERR_ARG;
+  if (ws_bytes < zc_ws_bytes(p->L)) return ZC_ERR_CAPACITY;
+  cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = lbb::zc_launch_plan(p->L, p->d_segs, d_x, d_ws, (cudaStream_t)stream);
+  return cuda_rc(e);
+}
+
+int zc_plan_set_books(zc_plan_t p, const uint8_t* h_books) {
+  if (!p || !h_books) return ZC_ERR_ARG;
+  for (uint32_t s = 0; s < p->L.nseg; ++s)
+    for (int j = 1; j < 7; ++j)
+      if (h_books[7 * s + j] <= h_books[7 * s + j - 1]) return ZC_ERR_ARG;
+  std::vector<lbb::ZcSegDev> segs(p->L.nseg);
+  if (cudaMemcpy(segs.data(), p->d_segs, sizeof(lbb::ZcSegDev) * p->L.nseg,
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ZC_ERR_CUDA;
+  for (uint32_t s = 0; s < p->L.nseg; ++s) {
+    std::memcpy(segs[s].book, h_books + 7 * s, 7);
+    segs[s].book[7] = 0;
+  }
+  return cuda_rc(cudaMemcpy(p->d_segs, segs.data(), sizeof(lbb::ZcSegDev) * p->L.nseg,
+                            cudaMemcpyHostToDevice));
+}
+
+int zc_plan_info(zc_plan_t p, zc_stream_t stream, uint8_t* h_books, double* h_mu_sigma) {
+  if (!p) return ZC_ERR_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return ZC_ERR_CUDA;
+  std::vector<lbb::ZcSegDev> segs(p->L.nseg);
+  if (cudaMemcpy(segs.data(), p->d_segs, sizeof(lbb::ZcSegDev) * p->L.nseg,
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ZC_ERR_CUDA;
+  for (uint32_t s = 0; s < p->L.nseg; ++s) {
+    if (h_books) std::memcpy(h_books + 7 * s, segs[s].book, 7);
+    if (h_mu_sigma) {
+      h_mu_sigma[2 * s] = segs[s].mu;
+      h_mu_sigma[2 * s + 1] = segs[s].sigma;
+    }
+  }
+  return ZC_OK;
+}
+
+int zc_compress(zc_plan_t p, const uint16_t* d_x, void* d_out, uint64_t out_cap,
+                uint64_t* d_out_bytes, void* d_ws, size_t ws_bytes, zc_stream_t stream) {
+  if (!p || !d_out || !d_ws || (!d_x && p->L.n)) return ZC_ERR_ARG;
+  if (!aligned(d_out, 16) || !aligned(d_ws, 256) || !aligned(d_x, 2) || !aligned(d_out_bytes, 8))
+    return ZC_ERR_ARG;
+  if (ws_bytes < zc_ws_bytes(p->L)) return ZC_ERR_CAPACITY;
+  if (out_cap < p->L.off_esc) return ZC_ERR_CAPACITY;
+  return cuda_rc(lbb::zc_launch_compress(p->L, p->d_segs, d_x, d_out, out_cap,
+                                         reinterpret_cast<unsigned long long*>(d_out_bytes), d_ws,
+                                         (cudaStream_t)stream));
+}
+
+size_t zc_decompress_workspace_bytes(void) { return kCtrlBytes; }
+
+int zc_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_y, uint64_t y_cap_elems,
+                  void* d_ws, size_t ws_bytes, zc_stream_t stream) {
+  if (!d_in || !d_ws || (!d_y && y_cap_elems)) return ZC_ERR_ARG;
+  if (!aligned(d_in, 16) || !aligned(d_ws, 256) || !aligned(d_y, 2)) return ZC_ERR_ARG;
+  if (ws_bytes < kCtrlBytes) return ZC_ERR_CAPACITY;
+  return cuda_rc(lbb::zc_launch_decompress(d_in, in_bytes, d_y, y_cap_elems, d_ws,
+                                           (cudaStream_t)stream));
+}
+
+// ------------------------------------------------------------------ IBP
+
+uint64_t ibp_meta_bytes(uint32_t chunk_bytes) {
+  return lbb::kIbpmHeader + 2ull * chunk_bytes;
+}
+
+static bool ibp_chunk_ok(uint32_t cb) { return cb >= 16 && cb <= 4096 && (cb % 16) == 0; }
+
+size_t ibp_workspace_bytes(uint32_t cb, uint64_t n_bytes, uint64_t n_samples) {
+  if (!ibp_chunk_ok(cb)) return 0;
+  const unsigned long long nch = (n_bytes + cb - 1) / cb;
+  const unsigned long long ng = (nch + 31) / 32;
+  const unsigned long long codec = 8ull * ng;                      // look-back states
+  const unsigned long long B = 8ull * cb;
+  const unsigned long long words = (n_samples + 31) / 32;
+  const unsigned long long meta = 8ull * B + 4ull * B * words;      // counts + columns
+  return (size_t)lbb::round_up_dev(kCtrlBytes + std::max(codec, meta), 256);
+}
+
+uint64_t ibp_max_compressed_bytes(uint32_t cb, uint64_t n_bytes) {
+  if (!ibp_chunk_ok(cb)) return 0;
+  const unsigned long long nch = (n_bytes + cb - 1) / cb;
+  const unsigned long long ng = (nch + 31) / 32;
+  // every chunk raw, 4 bytes of participation bits and up to 15 bytes of
+  // padding per group
+  return lbb::kIbp1Header + lbb::round_up_dev(8ull * (ng + 1), 128) + n_bytes + 20ull * ng + 16;
+}
+
+int ibp_build_meta(const void* d_samples, uint64_t n_samples, uint32_t cb, double T, int mode,
+                   void* d_meta, void* d_ws, size_t ws_bytes, zc_stream_t stream) {
+  if (!d_samples || !d_meta || !d_ws || n_samples == 0) return ZC_ERR_ARG;
+  if (!ibp_chunk_ok(cb) || !(T > 0.5 && T <= 1.0) || (mode != 0 && mode != 1)) return ZC_ERR_ARG;
+  if (mode == 1 && cb > 2048) return ZC_ERR_UNSUPPORTED;
+  if (!aligned(d_samples, 16) || !aligned(d_meta, 16) || !aligned(d_ws, 256)) return ZC_ERR_ARG;
+  if (ws_bytes < ibp_workspace_bytes(cb, 0, n_samples)) return ZC_ERR_CAPACITY;
+  const unsigned long long k = (unsigned long long)std::ceil(T * (double)n_samples);
+  return cuda_rc(lbb::ibp_launch_build_meta(d_samples, n_samples, cb, k, T, mode, d_meta, d_ws,
+                                            (cudaStream_t)stream));
+}
+
+int ibp_compress(const void* d_meta, uint32_t cb, const void* d_x, uint64_t n_bytes, void* d_out,
+                 uint64_t out_cap, uint64_t* d_out_bytes, void* d_ws, size_t ws_bytes,
+                 zc_stream_t stream) {
+  if (!d_meta || !d_out || !d_ws || (!d_x && n_bytes) || !ibp_chunk_ok(cb) || (n_bytes % 4) != 0)
+    return ZC_ERR_ARG;
+  if (!aligned(d_meta, 16) || !aligned(d_x, 16) || !aligned(d_out, 16) || !aligned(d_ws, 256) ||
+      !aligned(d_out_bytes, 8))
+    return ZC_ERR_ARG;
+  if (ws_bytes < ibp_workspace_bytes(cb, n_bytes, 0)) return ZC_ERR_CAPACITY;
+  const unsigned long long nch = (n_bytes + cb - 1) / cb, ng = (nch + 31) / 32;
+  if (out_cap < lbb::kIbp1Header + lbb::round_up_dev(8ull * (ng + 1), 128)) return ZC_ERR_CAPACITY;
+  return cuda_rc(lbb::ibp_launch_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap,
+                                          reinterpret_cast<unsigned long long*>(d_out_bytes),
+                                          d_ws, (cudaStream_t)stream));
+}
+
+int ibp_decompress(const void* d_meta, uint32_t cb, const void* d_in, uint64_t in_bytes,
+                   void* d_y, uint64_t y_cap, void* d_ws, size_t ws_bytes, zc_stream_t stream) {
+  if (!d_meta || !d_in || !d_ws || (!d_y && y_cap) || !ibp_chunk_ok(cb)) return ZC_ERR_ARG;
+  if (!aligned(d_meta, 16) || !aligned(d_in, 16) || !aligned(d_y, 16) || !aligned(d_ws, 256))
+    return ZC_ERR_ARG;
+  if (ws_bytes < kCtrlBytes) return ZC_ERR_CAPACITY;
+  return cuda_rc(lbb::ibp_launch_decompress(d_meta, cb, d_in, in_bytes, d_y, y_cap, d_ws,
+                                            (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,185 @@
+// common.cuh -- device helpers shared by the codec kernels: the workspace
+// control block and status word, memory-order primitives, a bounded
+// decoupled look-back scan across thread blocks, and block-wide scans.
+//
+// Nothing here traps: every wait is bounded and reports ZC_ERR_TIMEOUT through
+// the status word instead.
+#pragma once
+
+#include <cstdint>
+
+#include "zc.h"
+
+namespace lbb {
+
+constexpr int kWarp = 32;
+
+__host__ __device__ __forceinline__ unsigned long long round_up_dev(unsigned long long v,
+                                                                  unsigned long long a) {
+  return (v + a - 1) / a * a;
+}
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// First 256 bytes of every workspace.
+struct Ctrl {
+  int status;          // first error of the call (0 = none)
+  int pad0;
+  unsigned long long ticket;  // dynamic tile counter (ordered tile start)
+  unsigned long long done;    // blocks finished (last one finalises)
+  unsigned long long spare[29];
+};
+static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
+constexpr size_t kCtrlBytes = 256;
+
+__device__ __forceinline__ void set_status(Ctrl* c, int code) {
+  atomicCAS(&c->status, 0, code);
+}
+__device__ __forceinline__ int get_status(const Ctrl* c) {
+  return *reinterpret_cast<const volatile int*>(&c->status);
+}
+
+// ---------------------------------------------------------------- memory ops
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p,
+                                               unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(
+    const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(
+    const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// 16-byte read-only load (data not written by this kernel).
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+// 16-byte load through L1 bypass for data other blocks of this kernel wrote.
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
+  return __byte_perm(a, b, s);
+}
+
+// ---------------------------------------------------------------- warp sums
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------- look-back
+//
+// Tile state word: bits 63..62 = flag (0 empty, 1 aggregate, 2 inclusive
+// prefix), bits 61..0 = value.  Tiles are numbered in the order blocks took
+// them from the ticket counter, so every predecessor of a waiting tile is
+// already running: the wait ends unless something is broken, and is bounded
+// anyway.
+constexpr unsigned long long kFlagAgg = 1ull << 62;
+constexpr unsigned long long kFlagInc = 2ull << 62;
+constexpr unsigned long long kValMask = (1ull << 62) - 1;
+constexpr unsigned kMaxSpins = 1u << 22;  // ~1 s with the back-off below
+
+// Called by all 32 lanes of one warp.  Publishes `aggregate` for `tile`,
+// returns the exclusive prefix over tiles 0..tile-1 and publishes the
+// inclusive value.  On a timeout sets *timed_out, publishes an inclusive
+// value of `aggregate` (so successors finish) and returns 0.
+__device__ __forceinline__ unsigned long long lookback_warp(
+    unsigned long long* states, unsigned long long tile,
+    unsigned long long aggregate, bool* timed_out) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  if (tile == 0) {
+    if (lane == 0) st_release_u64(states, kFlagInc | aggregate);
+    return 0;
+  }
+  if (lane == 0) st_release_u64(states + tile, kFlagAgg | aggregate);
+  unsigned long long excl = 0;
+  long long end = (long long)tile - 1;
+  unsigned spins = 0;
+  unsigned ns = 32;
+  bool to = false;
+  while (true) {
+    long long idx = end - lane;
+    unsigned long long s = idx >= 0 ? ld_relaxed_u64(states + idx) : kFlagInc;
+    unsigned flag = (unsigned)(s >> 62);
+    if (__any_sync(kFull, flag == 0)) {
+      if (++spins > kMaxSpins) {
+        to = true;
+        break;
+      }
+      __nanosleep(ns);
+      if (ns < 256) ns <<= 1;
+      continue;
+    }
+    unsigned inc = __ballot_sync(kFull, flag == 2);
+    unsigned long long v = s & kValMask;
+    if (inc) {
+      int first = __ffs(inc) - 1;  // nearest tile holding an inclusive prefix
+      excl += warp_sum_u64(lane <= first ? v : 0ull);
+      break;
+    }
+    excl += warp_sum_u64(v);
+    end -= kWarp;
+  }
+  if (to) {
+    *timed_out = true;
+    if (lane == 0) st_release_u64(states + tile, kFlagInc | aggregate);
+    return 0;
+  }
+  if (lane == 0) st_release_u64(states + tile, kFlagInc | ((excl + aggregate) & kValMask));
+  return excl;
+}
+
+// ---------------------------------------------------------------- block scan
+//
+// Exclusive scan of one uint32 per thread over a block of NT threads
+// (multiple of 32).  `warp_tot` is NT/32 words of shared memory.  Returns the
+// thread's exclusive prefix; *total receives the block total.  Contains one
+// __syncthreads (callers must not have warp_tot in use).
+template <int NT>
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_tot,
+                                                    uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t t = __shfl_up_sync(kFull, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  uint32_t base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    uint32_t t = warp_tot[w];
+    if (w < warp) base += t;
+    tot += t;
+  }
+  *total = tot;
+  return base + inc - v;
+}
+
+}  // namespace lbb

@@ -1,0 +1,83 @@
+// internal.h -- structures and launchers shared between the C-ABI layer
+// (api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "zc.h"
+
+namespace lbb {
+
+// ---------------------------------------------------------------- ZipCCL
+
+constexpr uint32_t kZcMagic = 0x3143435Au;  // "ZCC1"
+constexpr uint32_t kZcHeader = 128;
+constexpr uint32_t kZcSegRec = 64;
+constexpr uint32_t kZcAlign = 128;
+constexpr uint32_t kTileLanes = 4096;   // lanes (element slots) per tile
+constexpr int kThreads = 256;           // 16 lanes per thread
+
+// Per-segment record of a plan, in device memory (64 bytes).
+struct ZcSegDev {
+  unsigned long long elem_start, nelem, chunk_start, nchunks;
+  unsigned long long unit_start;  // first statistics unit of the segment
+  unsigned char book[8];          // 7 ascending exponent fields + 0
+  double mu, sigma;
+};
+static_assert(sizeof(ZcSegDev) == 64, "segment record is 64 bytes");
+
+struct ZcLayout {
+  unsigned long long n, nchunks, ntiles, nunits;
+  uint32_t nseg, C, log2C, U;  // U: elements per statistics unit
+  unsigned long long off_seg, off_escoff, off_static, off_esc;
+  unsigned long long slot_bytes;
+};
+
+// One partial of the statistics pass (one unit of U elements).
+struct StatPartial {
+  unsigned long long cnt;
+  double s1, s2;
+};
+
+inline unsigned long long round_up(unsigned long long v, unsigned long long a) {
+  return (v + a - 1) / a * a;
+}
+
+cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
+                           const uint16_t* d_x, void* d_ws, cudaStream_t s);
+cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
+                               const uint16_t* d_x, void* d_out,
+                               unsigned long long out_cap,
+                               unsigned long long* d_out_bytes, void* d_ws,
+                               cudaStream_t s);
+cudaError_t zc_launch_decompress(const void* d_in, unsigned long long in_bytes,
+                                 uint16_t* d_y, unsigned long long y_cap,
+                                 void* d_ws, cudaStream_t s);
+
+// ---------------------------------------------------------------- IBP
+
+constexpr uint32_t kIbpmMagic = 0x4D504249u;  // "IBPM"
+constexpr uint32_t kIbp1Magic = 0x31504249u;  // "IBP1"
+constexpr uint32_t kIbpmHeader = 64;
+constexpr uint32_t kIbp1Header = 128;
+
+cudaError_t ibp_launch_build_meta(const void* d_samples, unsigned long long N,
+                                  uint32_t chunk_bytes, unsigned long long k,
+                                  double T, int mode, void* d_meta, void* d_ws,
+                                  cudaStream_t s);
+cudaError_t ibp_launch_compress(const void* d_meta, uint32_t chunk_bytes,
+                                const void* d_x, unsigned long long n_bytes,
+                                void* d_out, unsigned long long out_cap,
+                                unsigned long long* d_out_bytes, void* d_ws,
+                                cudaStream_t s);
+cudaError_t ibp_launch_decompress(const void* d_meta, uint32_t chunk_bytes,
+                                  const void* d_in, unsigned long long in_bytes,
+                                  void* d_y, unsigned long long y_cap,
+                                  void* d_ws, cudaStream_t s);
+
+// Blocks of `kernel` resident per SM times SMs on the current device.
+int resident_blocks(const void* kernel, int threads, size_t smem);
+
+}  // namespace lbb

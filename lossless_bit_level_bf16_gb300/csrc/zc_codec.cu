@@ -1,0 +1,599 @@
+// zc_codec.cu -- ZipCCL exponent coding of bf16: encode and decode kernels.
+//
+// [ZipCCL] = "ZipCCL: Efficient Lossless Data Compression of Communication
+// Collectives for Accelerating LLM Training", 2. Metodologia:
+//   B  each bf16 splits into sign+mantissa (kept as one byte) and an 8-bit
+//      exponent; an exponent in the segment's 7-entry codebook becomes a 3-bit
+//      code 001..111, any other gets 000 and goes, whole, to a separate escape
+//      array;
+//   C  blocks padded to 128 bytes for full 128-bit coalesced accesses; the
+//      3-bit codes kept as three 1-bit planes;
+//   D  fixed-size parts first, variable-size parts after.
+//
+// Stream "ZCC1": header (128 B) | segment table (64 B per segment) |
+// per-chunk escape offsets (u64) | static region: one slot of 11*C/8 bytes
+// per chunk = [C sign+mantissa bytes][plane 0][plane 1][plane 2] | escape
+// bytes.  Every region starts on a 128-byte boundary.
+//
+// GPU mapping (both kernels): a tile is 4096 consecutive element slots of the
+// chunked lane space; a block of 256 threads handles a tile, 16 consecutive
+// slots per thread loaded and stored as two 16-byte vectors.  A pair of
+// threads forms one 32-bit word of each bit plane.
+//
+// Encode: persistent blocks take tiles from a ticket counter; per tile they
+// write the slots, count escapes (block scan), obtain the tile's global escape
+// offset with a decoupled look-back over tiles and write the escape bytes
+// compacted.  The last block to finish writes the header, the segment table
+// and the padding.  Bytes per element: 2 read, 11/8 + escapes written.
+//
+// Decode: blocks own decode units (a chunk, or a 4096-slot tile of small
+// chunks); per unit the escape offsets come from the stream's table, so blocks
+// are independent.  Every offset read from the stream is checked before it is
+// used as an address; a bad stream sets ZC_ERR_FORMAT and is not written past.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lbb {
+namespace {
+
+struct EncArgs {
+  const uint16_t* x;
+  uint8_t* out;
+  unsigned long long out_cap;
+  unsigned long long* out_bytes;
+  const ZcSegDev* segs;
+  ZcLayout L;
+  Ctrl* ctrl;
+  unsigned long long* states;
+  int x_al16;
+};
+
+// Largest segment index whose chunk_start <= c (segments with no chunks are
+// skipped because a later one starts at the same chunk).
+__device__ __forceinline__ int find_chunk_segment(const ZcSegDev* segs, uint32_t nseg,
+                                                  unsigned long long c) {
+  int lo = 0, hi = (int)nseg - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (segs[mid].chunk_start <= c) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Entry of the encode lookup table: bit 0/8/16 = bit 0/1/2 of the 3-bit code,
+// bit 24 = escape.  Shifting an entry left by the element's index (0..7)
+// drops its bits into four per-plane bytes.
+__device__ __forceinline__ uint32_t lut_entry(const unsigned char* book, uint32_t e) {
+  uint32_t code = 0;
+#pragma unroll
+  for (int j = 0; j < 7; ++j)
+    if (book[j] == e) code = (uint32_t)j + 1;
+  if (code == 0) return 1u << 24;
+  return (code & 1u) | (((code >> 1) & 1u) << 8) | (((code >> 2) & 1u) << 16);
+}
+
+__device__ __forceinline__ uint32_t sm4(uint32_t w0, uint32_t w1) {
+  // sign+mantissa bytes of 4 consecutive bf16 held in w0, w1
+  return (prmt(w0, w1, 0x7531) & 0x80808080u) | (prmt(w0, w1, 0x6420) & 0x7F7F7F7Fu);
+}
+
+__global__ void __launch_bounds__(kThreads) zc_encode_kernel(EncArgs A) {
+  __shared__ uint32_t s_lut[4][256];
+  __shared__ uint32_t s_wtot[kThreads / 32];
+  __shared__ unsigned long long s_tile, s_excl;
+  __shared__ unsigned long long s_elem0[4];
+  __shared__ uint32_t s_valid[4];
+  __shared__ int s_al[4];
+  __shared__ int s_seg[4], s_lut_seg[4];
+  __shared__ int s_last;
+
+  const int t = threadIdx.x;
+  const uint32_t C = A.L.C, log2C = A.L.log2C;
+  const uint32_t cpt = C >= kTileLanes ? 1u : kTileLanes / C;  // chunks per tile
+  const unsigned long long S = A.L.slot_bytes;
+  if (t < 4) s_lut_seg[t] = -1;
+
+  for (;;) {
+    if (t == 0) s_tile = atomicAdd(&A.ctrl->ticket, 1ull);
+    __syncthreads();
+    const unsigned long long tile = s_tile;
+    if (tile >= A.L.ntiles) break;
+    const unsigned long long lane0 = tile * kTileLanes;
+    if (t < (int)cpt) {
+      const unsigned long long c = (lane0 >> log2C) + t;
+      if (c < A.L.nchunks) {
+        const int sg = find_chunk_segment(A.segs, A.L.nseg, c);
+        const ZcSegDev& r = A.segs[sg];
+        const unsigned long long e0 = r.elem_start + (c - r.chunk_start) * C;
+        const unsigned long long end = r.elem_start + r.nelem;
+        s_seg[t] = sg;
+        s_elem0[t] = e0;
+        s_valid[t] = (uint32_t)((end - e0) < C ? (end - e0) : C);
+        s_al[t] = A.x_al16 && ((r.elem_start & 7ull) == 0);
+      } else {
+        s_seg[t] = s_lut_seg[t];
+        s_elem0[t] = 0;
+        s_valid[t] = 0;
+        s_al[t] = 0;
+      }
+    }
+    __syncthreads();
+    for (uint32_t k = 0; k < cpt; ++k) {
+      const int sg = s_seg[k];
+      if (sg >= 0 && s_lut_seg[k] != sg) s_lut[k][t] = lut_entry(A.segs[sg].book, (uint32_t)t);
+    }
+    __syncthreads();
+    if (t < (int)cpt) s_lut_seg[t] = s_seg[t];
+
+    // ---- this thread's 16 slots
+    const uint32_t lt = (uint32_t)t * 16u;
+    const unsigned long long lane = lane0 + lt;
+    const unsigned long long c = lane >> log2C;
+    const uint32_t i0 = (uint32_t)(lane & (C - 1));
+    const int lc = C >= kTileLanes ? 0 : (int)(lt >> log2C);
+    const bool live = c < A.L.nchunks;
+    const uint32_t vch = live ? s_valid[lc] : 0u;
+    const int valid = vch > i0 ? ((vch - i0) < 16u ? (int)(vch - i0) : 16) : 0;
+    const unsigned long long elem = s_elem0[lc] + i0;
+    uint32_t w[8];
+    if (valid == 16 && s_al[lc]) {
+      uint4 a = ld_nc_v4(A.x + elem), b = ld_nc_v4(A.x + elem + 8);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t l = (2 * j < valid) ? (uint32_t)__ldg(A.x + elem + 2 * j) : 0u;
+        uint32_t h = (2 * j + 1 < valid) ? (uint32_t)__ldg(A.x + elem + 2 * j + 1) : 0u;
+        w[j] = l | (h << 16);
+      }
+    }
+    const uint32_t* Lt = s_lut[lc];
+    uint32_t accA = 0, accB = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      accA |= Lt[(w[j] >> 7) & 0xFFu] << (2 * j);
+      accA |= Lt[(w[j] >> 23) & 0xFFu] << (2 * j + 1);
+      accB |= Lt[(w[j + 4] >> 7) & 0xFFu] << (2 * j);
+      accB |= Lt[(w[j + 4] >> 23) & 0xFFu] << (2 * j + 1);
+    }
+    if (valid < 16) {  // slots past the segment end: code 0, no escape
+      const uint32_t vA = valid >= 8 ? 0xFFu : ((1u << valid) - 1u);
+      const uint32_t vB = valid >= 16 ? 0xFFu : (valid > 8 ? ((1u << (valid - 8)) - 1u) : 0u);
+      accA &= vA * 0x01010101u;
+      accB &= vB * 0x01010101u;
+    }
+    uint8_t* slot = A.out + A.L.off_static + c * S;
+    if (live) {
+      uint4 smv;
+      smv.x = sm4(w[0], w[1]);
+      smv.y = sm4(w[2], w[3]);
+      smv.z = sm4(w[4], w[5]);
+      smv.w = sm4(w[6], w[7]);
+      st_v4(slot + i0, smv);
+    }
+    const uint32_t T0 = prmt(accA, accB, 0x5140);  // plane0 | plane1 << 16
+    const uint32_t T1 = prmt(accA, accB, 0x7362);  // plane2 | escape << 16
+    const uint32_t U0 = __shfl_xor_sync(kFull, T0, 1);
+    const uint32_t U1 = __shfl_xor_sync(kFull, T1, 1);
+    if (live) {
+      uint32_t* pw = reinterpret_cast<uint32_t*>(slot + C) + (i0 >> 5);
+      const uint32_t pwords = C >> 5;  // 32-bit words per plane
+      if ((t & 1) == 0) {
+        pw[0] = prmt(T0, U0, 0x5410);
+        pw[pwords] = prmt(T0, U0, 0x7632);
+      } else {
+        pw[2 * pwords] = prmt(U1, T1, 0x5410);
+      }
+    }
+    const uint32_t esc = T1 >> 16;
+
+    // ---- escape offsets: block scan, then look-back across tiles
+    uint32_t total;
+    const uint32_t excl = block_excl_scan<kThreads>((uint32_t)__popc(esc), s_wtot, &total);
+    if (t < 32) {
+      bool to = false;
+      const unsigned long long e = lookback_warp(A.states, tile, total, &to);
+      if (t == 0) {
+        s_excl = e;
+        if (to) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+      }
+    }
+    __syncthreads();
+    const unsigned long long base = s_excl + excl;
+    if (live && i0 == 0)
+      reinterpret_cast<unsigned long long*>(A.out + A.L.off_escoff)[c] = base;
+    if (esc) {
+      uint32_t F[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) F[q] = prmt(w[2 * q] >> 7, w[2 * q + 1] >> 7, 0x6420);
+      uint32_t m = esc;
+      unsigned long long pos = A.L.off_esc + base;
+      while (m) {
+        const int i = __ffs(m) - 1;
+        m &= m - 1;
+        const uint32_t f = i < 8 ? (i < 4 ? F[0] : F[1]) : (i < 12 ? F[2] : F[3]);
+        const uint32_t e = (f >> ((i & 3) * 8)) & 0xFFu;
+        if (pos < A.out_cap) A.out[pos] = (uint8_t)e;
+        else set_status(A.ctrl, ZC_ERR_CAPACITY);
+        ++pos;
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- the last block to finish writes the header, tables and padding
+  __syncthreads();
+  if (t == 0) {
+    __threadfence();
+    const unsigned long long d = atomicAdd(&A.ctrl->done, 1ull);
+    s_last = (d == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const ZcLayout& L = A.L;
+  unsigned long long esc_total = 0;
+  if (L.ntiles) esc_total = ld_acquire_u64(A.states + L.ntiles - 1) & kValMask;
+  const unsigned long long total = L.off_esc + round_up_dev(esc_total, kZcAlign);
+  unsigned long long* escoff = reinterpret_cast<unsigned long long*>(A.out + L.off_escoff);
+  if (t == 0) {
+    escoff[L.nchunks] = esc_total;
+    if (total > A.out_cap) set_status(A.ctrl, ZC_ERR_CAPACITY);
+    if (A.out_bytes) *A.out_bytes = total;
+  }
+  // zero padding: escape tail, segment-table tail, offset-table tail
+  const unsigned long long pad_end = total < A.out_cap ? total : A.out_cap;
+  for (unsigned long long p = L.off_esc + esc_total + t; p < pad_end; p += kThreads) A.out[p] = 0;
+  for (unsigned long long p = L.off_seg + (unsigned long long)kZcSegRec * L.nseg + t;
+       p < L.off_escoff; p += kThreads)
+    A.out[p] = 0;
+  for (unsigned long long p = L.off_escoff + 8ull * (L.nchunks + 1) + t; p < L.off_static;
+       p += kThreads)
+    A.out[p] = 0;
+  __syncthreads();  // escoff[nchunks] visible to the block
+  for (uint32_t s = t; s < L.nseg; s += kThreads) {
+    const ZcSegDev& r = A.segs[s];
+    const volatile unsigned long long* ve = escoff;
+    const unsigned long long es = ve[r.chunk_start];
+    const unsigned long long ee = ve[r.chunk_start + r.nchunks];
+    unsigned long long* rec =
+        reinterpret_cast<unsigned long long*>(A.out + L.off_seg + (unsigned long long)kZcSegRec * s);
+    unsigned long long bk = 0;
+#pragma unroll
+    for (int j = 0; j < 7; ++j) bk |= (unsigned long long)r.book[j] << (8 * j);
+    rec[0] = r.elem_start;
+    rec[1] = r.nelem;
+    rec[2] = r.chunk_start;
+    rec[3] = r.nchunks;
+    rec[4] = es;
+    rec[5] = ee - es;
+    rec[6] = bk;
+    rec[7] = 0;
+  }
+  if (t < 16) {
+    unsigned long long h = 0;
+    switch (t) {
+      case 0: h = (unsigned long long)kZcMagic | (1ull << 32) | ((unsigned long long)kZcHeader << 48); break;
+      case 1: h = (unsigned long long)C | ((unsigned long long)L.nseg << 32); break;
+      case 2: h = L.n; break;
+      case 3: h = L.nchunks; break;
+      case 4: h = esc_total; break;
+      case 5: h = L.off_seg; break;
+      case 6: h = L.off_escoff; break;
+      case 7: h = L.off_static; break;
+      case 8: h = L.off_esc; break;
+      case 9: h = total; break;
+      default: h = 0; break;
+    }
+    reinterpret_cast<unsigned long long*>(A.out)[t] = h;
+  }
+}
+
+// ------------------------------------------------------------------ decode
+
+struct DecHdr {
+  unsigned long long n, nchunks, esc_total, off_seg, off_escoff, off_static, off_esc, total;
+  uint32_t C, log2C, nseg;
+};
+
+__device__ __forceinline__ unsigned long long rd_u64(const uint8_t* p) {
+  return *reinterpret_cast<const unsigned long long*>(p);
+}
+
+// Validates the header against in_bytes and y_cap; false on any mismatch.
+__device__ bool parse_header(const uint8_t* in, unsigned long long in_bytes,
+                             unsigned long long y_cap, DecHdr& h, int& err) {
+  err = ZC_ERR_FORMAT;
+  if (in_bytes < kZcHeader) return false;
+  const unsigned long long w0 = rd_u64(in), w1 = rd_u64(in + 8);
+  if ((uint32_t)w0 != kZcMagic || ((w0 >> 32) & 0xFFFFu) != 1u || (w0 >> 48) != kZcHeader)
+    return false;
+  h.C = (uint32_t)w1;
+  h.nseg = (uint32_t)(w1 >> 32);
+  h.n = rd_u64(in + 16);
+  h.nchunks = rd_u64(in + 24);
+  h.esc_total = rd_u64(in + 32);
+  h.off_seg = rd_u64(in + 40);
+  h.off_escoff = rd_u64(in + 48);
+  h.off_static = rd_u64(in + 56);
+  h.off_esc = rd_u64(in + 64);
+  h.total = rd_u64(in + 72);
+  if (h.C < 1024u || h.C > 65536u || (h.C & (h.C - 1)) != 0 || h.nseg == 0) return false;
+  h.log2C = 31 - __clz(h.C);
+  if (h.total > in_bytes) return false;
+  const unsigned long long S = (unsigned long long)h.C * 11ull / 8ull;
+  if (h.off_seg != kZcHeader) return false;
+  if (h.nseg > h.total / kZcSegRec) return false;
+  if (h.off_escoff != h.off_seg + round_up_dev((unsigned long long)kZcSegRec * h.nseg, kZcAlign))
+    return false;
+  if (h.nchunks > h.total / 8ull) return false;
+  if (h.off_static != h.off_escoff + round_up_dev(8ull * (h.nchunks + 1), kZcAlign)) return false;
+  if (h.nchunks > h.total / S) return false;
+  if (h.off_esc != h.off_static + h.nchunks * S) return false;
+  if (h.off_esc > h.total || h.esc_total > h.total - h.off_esc) return false;
+  if (h.total != h.off_esc + round_up_dev(h.esc_total, kZcAlign)) return false;
+  if (h.n > (h.nchunks << h.log2C)) return false;
+  if (h.n > y_cap) {
+    err = ZC_ERR_CAPACITY;
+    return false;
+  }
+  return true;
+}
+
+// Segment record s of the stream, checked for consistency with the header and
+// with record s-1; false if anything is off.
+struct SegRec {
+  unsigned long long elem_start, nelem, chunk_start, nchunks;
+  uint32_t R0, R1;  // book bytes for the byte-permute lookup (code 0 -> 0)
+};
+
+__device__ bool load_seg(const uint8_t* in, const DecHdr& h, uint32_t s, SegRec& r) {
+  const uint8_t* p = in + h.off_seg + (unsigned long long)kZcSegRec * s;
+  r.elem_start = rd_u64(p);
+  r.nelem = rd_u64(p + 8);
+  r.chunk_start = rd_u64(p + 16);
+  r.nchunks = rd_u64(p + 24);
+  const unsigned long long bk = rd_u64(p + 48);
+  r.R0 = (uint32_t)(bk << 8);
+  r.R1 = (uint32_t)(bk >> 24);
+  if (r.nelem > h.n || r.elem_start > h.n - r.nelem) return false;
+  if (r.nchunks > h.nchunks || r.chunk_start > h.nchunks - r.nchunks) return false;
+  if (r.nchunks != ((r.nelem + h.C - 1) >> h.log2C)) return false;
+  if (s == 0) return r.elem_start == 0 && r.chunk_start == 0;
+  const uint8_t* q = p - kZcSegRec;
+  return rd_u64(q) + rd_u64(q + 8) == r.elem_start && rd_u64(q + 16) + rd_u64(q + 24) == r.chunk_start;
+}
+
+__device__ __forceinline__ uint32_t out_word(uint32_t S, uint32_t E, uint32_t sel) {
+  // two bf16 from (sign+mantissa byte, exponent byte) pairs
+  const uint32_t T = prmt(S, E, sel);  // [s0, e0, s1, e1]
+  return (T & 0x007F007Fu) | ((T >> 1) & 0x7F807F80u) | ((T << 8) & 0x80008000u);
+}
+
+__global__ void __launch_bounds__(kThreads) zc_decode_kernel(
+    const uint8_t* __restrict__ in, unsigned long long in_bytes, uint16_t* __restrict__ y,
+    unsigned long long y_cap, Ctrl* ctrl, int y_al16) {
+  __shared__ uint32_t s_nib[256];
+  __shared__ DecHdr s_h;
+  __shared__ int s_ok;
+  __shared__ uint32_t s_wtot[kThreads / 32];
+  __shared__ uint32_t s_excl[kThreads];
+  __shared__ unsigned long long s_elem0[4], s_elo[4], s_ehi[4];
+  __shared__ uint32_t s_valid[4], s_R0[4], s_R1[4];
+  __shared__ int s_al[4], s_bad;
+
+  const int t = threadIdx.x;
+  if (t == 0) {
+    int err;
+    s_ok = parse_header(in, in_bytes, y_cap, s_h, err);
+    if (!s_ok) set_status(ctrl, err);
+  }
+  {
+    uint32_t v = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v |= ((t >> i) & 1u) << (4 * i);
+    s_nib[t] = v;  // bit i of a plane byte -> nibble i
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  const DecHdr h = s_h;
+  const uint32_t C = h.C, log2C = h.log2C;
+  const unsigned long long S = (unsigned long long)C * 11ull / 8ull;
+  const uint8_t* escoff = in + h.off_escoff;
+
+  // whole-table checks, once (block 0): segment chain and offset-table ends
+  if (blockIdx.x == 0) {
+    for (uint32_t s = t; s < h.nseg; s += kThreads) {
+      SegRec r;
+      if (!load_seg(in, h, s, r)) set_status(ctrl, ZC_ERR_FORMAT);
+      if (s + 1 == h.nseg && (r.elem_start + r.nelem != h.n || r.chunk_start + r.nchunks != h.nchunks))
+        set_status(ctrl, ZC_ERR_FORMAT);
+    }
+    if (t == 0 && (rd_u64(escoff) != 0 || rd_u64(escoff + 8 * h.nchunks) != h.esc_total))
+      set_status(ctrl, ZC_ERR_FORMAT);
+  }
+
+  const uint32_t cpu = C >= kTileLanes ? 1u : kTileLanes / C;          // chunks per unit
+  const uint32_t steps = C >= kTileLanes ? C / kTileLanes : 1u;          // tiles per unit
+  const unsigned long long nunits = C >= kTileLanes ? h.nchunks : (h.nchunks + cpu - 1) / cpu;
+
+  if (t == 0) s_bad = 0;
+  __syncthreads();
+  for (unsigned long long u = blockIdx.x; u < nunits; u += gridDim.x) {
+    const unsigned long long c0 = u * cpu;
+    if (t < (int)cpu) {
+      const unsigned long long c = c0 + t;
+      s_valid[t] = 0;
+      s_elem0[t] = 0;
+      s_elo[t] = s_ehi[t] = 0;
+      s_R0[t] = s_R1[t] = 0;
+      s_al[t] = 0;
+      if (c < h.nchunks) {
+        int lo = 0, hi = (int)h.nseg - 1;  // largest s with chunk_start <= c
+        while (lo < hi) {
+          int mid = (lo + hi + 1) >> 1;
+          if (rd_u64(in + h.off_seg + (unsigned long long)kZcSegRec * mid + 16) <= c) lo = mid;
+          else hi = mid - 1;
+        }
+        SegRec r;
+        const unsigned long long elo = rd_u64(escoff + 8 * c), ehi = rd_u64(escoff + 8 * (c + 1));
+        if (!load_seg(in, h, (uint32_t)lo, r) || c < r.chunk_start ||
+            c >= r.chunk_start + r.nchunks || elo > ehi || ehi > h.esc_total) {
+          s_bad = 1;
+        } else {
+          const unsigned long long e0 = r.elem_start + ((c - r.chunk_start) << log2C);
+          const unsigned long long end = r.elem_start + r.nelem;
+          s_elem0[t] = e0;
+          s_valid[t] = (uint32_t)((end - e0) < C ? (end - e0) : C);
+          s_elo[t] = elo;
+          s_ehi[t] = ehi;
+          s_R0[t] = r.R0;
+          s_R1[t] = r.R1;
+          s_al[t] = y_al16 && ((r.elem_start & 7ull) == 0);
+        }
+      }
+    }
+    __syncthreads();
+    const bool bad_tables = s_bad != 0;
+    unsigned long long carry = 0;  // escapes in earlier tiles of this chunk
+    for (uint32_t st = 0; st < (bad_tables ? 0u : steps); ++st) {
+      const uint32_t lt = (uint32_t)t * 16u;
+      const int lc = C >= kTileLanes ? 0 : (int)(lt >> log2C);
+      const uint32_t i0 = C >= kTileLanes ? st * kTileLanes + lt : (lt & (C - 1));
+      const unsigned long long c = c0 + lc;
+      const bool live = c < h.nchunks;
+      const uint32_t vch = live ? s_valid[lc] : 0u;
+      const int valid = vch > i0 ? ((vch - i0) < 16u ? (int)(vch - i0) : 16) : 0;
+      uint4 smv = make_uint4(0, 0, 0, 0);
+      uint32_t p0 = 0, p1 = 0, p2 = 0;
+      const uint8_t* slot = in + h.off_static + c * S;
+      if (live) {
+        smv = ld_nc_v4(slot + i0);
+        const uint8_t* pb = slot + C + (i0 >> 3);
+        p0 = __ldg(reinterpret_cast<const unsigned short*>(pb));
+        p1 = __ldg(reinterpret_cast<const unsigned short*>(pb + (C >> 3)));
+        p2 = __ldg(reinterpret_cast<const unsigned short*>(pb + (C >> 2)));
+      }
+      const uint32_t vmask = valid >= 16 ? 0xFFFFu : ((1u << valid) - 1u);
+      const uint32_t esc = ~(p0 | p1 | p2) & vmask;
+      uint32_t total;
+      const uint32_t excl = block_excl_scan<kThreads>((uint32_t)__popc(esc), s_wtot, &total);
+      s_excl[t] = excl;
+      __syncthreads();
+      unsigned long long base;
+      if (C >= kTileLanes) {
+        base = s_elo[0] + carry + excl;
+      } else {
+        const uint32_t tfirst = (uint32_t)lc * (C >> 4);  // first thread of this chunk
+        base = s_elo[lc] + excl - s_excl[tfirst];
+        // per-chunk check: escapes counted in the chunk == table difference
+        if (live && lt == (uint32_t)lc * C) {
+          const uint32_t tnext = tfirst + (C >> 4);
+          const uint32_t cnt = (tnext < (uint32_t)kThreads ? s_excl[tnext] : total) - s_excl[tfirst];
+          if (cnt != s_ehi[lc] - s_elo[lc]) s_bad = 1;
+        }
+      }
+      const unsigned long long ehi = s_ehi[lc];
+      if (base + (unsigned long long)__popc(esc) > ehi) s_bad = 1;
+
+      const uint32_t cA = s_nib[p0 & 0xFFu] | (s_nib[p1 & 0xFFu] << 1) | (s_nib[p2 & 0xFFu] << 2);
+      const uint32_t cB = s_nib[p0 >> 8] | (s_nib[p1 >> 8] << 1) | (s_nib[p2 >> 8] << 2);
+      const uint32_t R0 = s_R0[lc], R1 = s_R1[lc];
+      uint32_t E0 = prmt(R0, R1, cA), E1 = prmt(R0, R1, cA >> 16);
+      uint32_t E2 = prmt(R0, R1, cB), E3 = prmt(R0, R1, cB >> 16);
+      if (esc && base + (unsigned long long)__popc(esc) <= ehi) {
+        uint32_t m = esc;
+        unsigned long long pos = h.off_esc + base;
+        while (m) {
+          const int i = __ffs(m) - 1;
+          m &= m - 1;
+          const uint32_t e = in[pos++];
+          const uint32_t sh = (uint32_t)(i & 3) * 8u;
+          const uint32_t keep = ~(0xFFu << sh), ins = e << sh;
+          const int q = i >> 2;
+          if (q == 0) E0 = (E0 & keep) | ins;
+          else if (q == 1) E1 = (E1 & keep) | ins;
+          else if (q == 2) E2 = (E2 & keep) | ins;
+          else E3 = (E3 & keep) | ins;
+        }
+      }
+      uint32_t o[8];
+      o[0] = out_word(smv.x, E0, 0x5140);
+      o[1] = out_word(smv.x, E0, 0x7362);
+      o[2] = out_word(smv.y, E1, 0x5140);
+      o[3] = out_word(smv.y, E1, 0x7362);
+      o[4] = out_word(smv.z, E2, 0x5140);
+      o[5] = out_word(smv.z, E2, 0x7362);
+      o[6] = out_word(smv.w, E3, 0x5140);
+      o[7] = out_word(smv.w, E3, 0x7362);
+      const unsigned long long elem = s_elem0[lc] + i0;
+      if (valid == 16 && s_al[lc]) {
+        st_v4(y + elem, make_uint4(o[0], o[1], o[2], o[3]));
+        st_v4(y + elem + 8, make_uint4(o[4], o[5], o[6], o[7]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (2 * j < valid) y[elem + 2 * j] = (uint16_t)(o[j] & 0xFFFFu);
+          if (2 * j + 1 < valid) y[elem + 2 * j + 1] = (uint16_t)(o[j] >> 16);
+        }
+      }
+      carry += total;
+      __syncthreads();  // s_excl / s_wtot reuse
+    }
+    __syncthreads();
+    if (t == 0) {
+      if (!bad_tables && C >= kTileLanes && carry != s_ehi[0] - s_elo[0]) s_bad = 1;
+      if (s_bad) set_status(ctrl, ZC_ERR_FORMAT);
+      s_bad = 0;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
+                               const uint16_t* d_x, void* d_out,
+                               unsigned long long out_cap,
+                               unsigned long long* d_out_bytes, void* d_ws,
+                               cudaStream_t s) {
+  Ctrl* ctrl = static_cast<Ctrl*>(d_ws);
+  unsigned long long* states =
+      reinterpret_cast<unsigned long long*>(static_cast<char*>(d_ws) + kCtrlBytes);
+  cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 8ull * L.ntiles, s);
+  if (e != cudaSuccess) return e;
+  EncArgs A;
+  A.x = d_x;
+  A.out = static_cast<uint8_t*>(d_out);
+  A.out_cap = out_cap;
+  A.out_bytes = d_out_bytes;
+  A.segs = d_segs;
+  A.L = L;
+  A.ctrl = ctrl;
+  A.states = states;
+  A.x_al16 = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
+  const int res = resident_blocks((const void*)zc_encode_kernel, kThreads, 0);
+  unsigned long long grid = L.ntiles < (unsigned long long)res ? L.ntiles : (unsigned long long)res;
+  if (grid == 0) grid = 1;
+  zc_encode_kernel<<<(unsigned)grid, kThreads, 0, s>>>(A);
+  return cudaGetLastError();
+}
+
+cudaError_t zc_launch_decompress(const void* d_in, unsigned long long in_bytes,
+                                 uint16_t* d_y, unsigned long long y_cap,
+                                 void* d_ws, cudaStream_t s) {
+  Ctrl* ctrl = static_cast<Ctrl*>(d_ws);
+  cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes, s);
+  if (e != cudaSuccess) return e;
+  const int res = resident_blocks((const void*)zc_decode_kernel, kThreads, 0);
+  const int y_al = (reinterpret_cast<uintptr_t>(d_y) & 15u) == 0;
+  zc_decode_kernel<<<res, kThreads, 0, s>>>(static_cast<const uint8_t*>(d_in), in_bytes, d_y,
+                                            y_cap, ctrl, y_al);
+  return cudaGetLastError();
+}
+
+}  // namespace lbb

@@ -1,0 +1,292 @@
+// zc_plan.cu -- ZipCCL codebook prediction on the GPU.
+//
+// [ZipCCL] = "ZipCCL: Efficient Lossless Data Compression of Communication
+// Collectives for Accelerating LLM Training", 2. Metodologia A: the top-7
+// bf16 exponents of a near-Gaussian tensor follow from its standard
+// deviation, so the exponent lookup table is computed in closed form instead
+// of from a histogram or a sort.
+//
+// Two kernels:
+//   zc_stats_kernel    one block per statistics unit (U elements inside one
+//                      segment): count, sum and sum of squares of the finite
+//                      values.  HBM-bound: 2 bytes read per element.
+//   zc_predict_kernel  one block per segment: adds the unit partials in a
+//                      fixed order, forms mu and sigma, evaluates the Gaussian
+//                      mass of every exponent field and keeps the 7 largest.
+//
+// Arithmetic of the statistics pass: the 16 values a thread holds are summed
+// (and their squares, exact in fp32 for bf16 inputs) as an fp32 tree (error
+// at most 4 units in the last place of the sum of magnitudes), the tree sums
+// are accumulated as unevaluated fp32 pairs (error-free two-sum), and the
+// block reduction is fp64.  A group of 16 whose fp32 sums are not finite (an
+// inf/NaN input or an fp32 overflow) is redone element by element in fp64,
+// skipping non-finite values.  The whole pass is deterministic for a given
+// plan: the partition into units and every reduction order are fixed.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lbb {
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Error-free transformation: hi + lo accumulates v exactly up to the rounding
+// of lo itself.
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float v) {
+  float s = __fadd_rn(hi, v);
+  float bb = __fsub_rn(s, hi);
+  float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(v, bb));
+  hi = s;
+  lo = __fadd_rn(lo, err);
+}
+
+__device__ __forceinline__ int find_unit_segment(const ZcSegDev* segs, uint32_t nseg,
+                                                 unsigned long long unit) {
+  // largest s with unit_start[s] <= unit
+  int lo = 0, hi = (int)nseg - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (segs[mid].unit_start <= unit) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kThreads) zc_stats_kernel(
+    const uint16_t* __restrict__ x, const ZcSegDev* __restrict__ segs, uint32_t nseg,
+    uint32_t U, StatPartial* __restrict__ parts, int x_al16) {
+  __shared__ unsigned long long s_lo, s_hi;
+  __shared__ int s_al;
+  __shared__ double s_r1[kThreads / 32], s_r2[kThreads / 32];
+  __shared__ unsigned long long s_rc[kThreads / 32];
+  const unsigned long long unit = blockIdx.x;
+  const int t = threadIdx.x;
+  if (t == 0) {
+    int s = find_unit_segment(segs, nseg, unit);
+    unsigned long long b = segs[s].elem_start + (unit - segs[s].unit_start) * U;
+    unsigned long long e = segs[s].elem_start + segs[s].nelem;
+    s_lo = b;
+    s_hi = (b + U < e) ? b + U : e;
+    s_al = x_al16 && ((segs[s].elem_start & 7ull) == 0);
+  }
+  __syncthreads();
+  const unsigned long long lo = s_lo, hi = s_hi;
+  const bool al = s_al;
+
+  float hx = 0.f, lx = 0.f, hq = 0.f, lq = 0.f;
+  double dx = 0.0, dq = 0.0;
+  unsigned long long cnt = 0;
+  for (unsigned long long e0 = lo + 16ull * t; e0 < hi; e0 += 16ull * kThreads) {
+    const unsigned long long rem = hi - e0;
+    const int valid = rem < 16 ? (int)rem : 16;
+    uint32_t w[8];
+    if (al && valid == 16) {
+      uint4 a = ld_nc_v4(x + e0), b = ld_nc_v4(x + e0 + 8);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t l = (2 * j < valid) ? (uint32_t)__ldg(x + e0 + 2 * j) : 0u;
+        uint32_t h = (2 * j + 1 < valid) ? (uint32_t)__ldg(x + e0 + 2 * j + 1) : 0u;
+        w[j] = l | (h << 16);
+      }
+    }
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[2 * j] = bf16_lo(w[j]);
+      v[2 * j + 1] = bf16_hi(w[j]);
+    }
+    float q[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) q[j] = __fmul_rn(v[j], v[j]);
+#pragma unroll
+    for (int s = 1; s < 16; s <<= 1) {
+#pragma unroll
+      for (int j = 0; j < 16; j += 2 * s) {
+        v[j] = __fadd_rn(v[j], v[j + s]);
+        q[j] = __fadd_rn(q[j], q[j + s]);
+      }
+    }
+    if (isfinite(v[0]) && isfinite(q[0])) {
+      two_sum_acc(hx, lx, v[0]);
+      two_sum_acc(hq, lq, q[0]);
+      cnt += (unsigned long long)valid;
+    } else {
+      // an inf/NaN input or an fp32 overflow: redo these values in fp64
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
+        if (j < valid && ((bits >> 7) & 0xFFu) != 0xFFu) {
+          double d = (double)__uint_as_float(bits << 16);
+          dx = __dadd_rn(dx, d);
+          dq = __dadd_rn(dq, __dmul_rn(d, d));
+          cnt += 1;
+        }
+      }
+    }
+  }
+  double t1 = __dadd_rn(__dadd_rn((double)hx, (double)lx), dx);
+  double t2 = __dadd_rn(__dadd_rn((double)hq, (double)lq), dq);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    t1 = __dadd_rn(t1, __shfl_down_sync(kFull, t1, o));
+    t2 = __dadd_rn(t2, __shfl_down_sync(kFull, t2, o));
+    cnt += __shfl_down_sync(kFull, cnt, o);
+  }
+  if ((t & 31) == 0) {
+    s_r1[t >> 5] = t1;
+    s_r2[t >> 5] = t2;
+    s_rc[t >> 5] = cnt;
+  }
+  __syncthreads();
+  if (t == 0) {
+    double a = 0.0, b = 0.0;
+    unsigned long long c = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      a = __dadd_rn(a, s_r1[w]);
+      b = __dadd_rn(b, s_r2[w]);
+      c += s_rc[w];
+    }
+    parts[unit].cnt = c;
+    parts[unit].s1 = a;
+    parts[unit].s2 = b;
+  }
+}
+
+// Gaussian mass of exponent field f: P(2^(f-127) <= |X| < 2^(f-126)),
+// X ~ N(mu, sigma), both signs, in fp64 with every operation rounded on its
+// own (no fused multiply-add) so the result does not depend on contraction.
+__device__ double field_mass(double mu, double sigma, int f) {
+  double a = ldexp(1.0, f - 127);
+  double b = ldexp(1.0, f - 126);
+  double s = __dmul_rn(sigma, 1.4142135623730951);  // sigma * sqrt(2)
+  double pos = __dmul_rn(0.5, __dsub_rn(erfc(__ddiv_rn(__dsub_rn(a, mu), s)),
+                                        erfc(__ddiv_rn(__dsub_rn(b, mu), s))));
+  double neg = __dmul_rn(0.5, __dsub_rn(erfc(__ddiv_rn(__dadd_rn(a, mu), s)),
+                                        erfc(__ddiv_rn(__dadd_rn(b, mu), s))));
+  double m = __dadd_rn(pos, neg);
+  if (!(m >= 1e-300)) m = 0.0;
+  return m;
+}
+
+__device__ int field_of(double v) {
+  double a = fabs(v);
+  if (a == 0.0 || a < 1.1754943508222875e-38 /* 2^-126 */) return 0;
+  int ex;
+  (void)frexp(a, &ex);
+  int f = ex + 126;
+  return f > 254 ? 254 : (f < 0 ? 0 : f);
+}
+
+__global__ void __launch_bounds__(kThreads) zc_predict_kernel(
+    ZcSegDev* __restrict__ segs, uint32_t nseg, unsigned long long nunits,
+    const StatPartial* __restrict__ parts) {
+  __shared__ double s_r1[kThreads / 32], s_r2[kThreads / 32];
+  __shared__ unsigned long long s_rc[kThreads / 32];
+  __shared__ double s_mu, s_sigma;
+  __shared__ double s_mass[256];
+  __shared__ int s_take[256];
+  const int t = threadIdx.x;
+  const uint32_t sg = blockIdx.x;
+  const unsigned long long u0 = segs[sg].unit_start;
+  const unsigned long long u1 = (sg + 1 < nseg) ? segs[sg + 1].unit_start : nunits;
+  double a = 0.0, b = 0.0;
+  unsigned long long c = 0;
+  for (unsigned long long u = u0 + t; u < u1; u += kThreads) {
+    a = __dadd_rn(a, parts[u].s1);
+    b = __dadd_rn(b, parts[u].s2);
+    c += parts[u].cnt;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = __dadd_rn(a, __shfl_down_sync(kFull, a, o));
+    b = __dadd_rn(b, __shfl_down_sync(kFull, b, o));
+    c += __shfl_down_sync(kFull, c, o);
+  }
+  if ((t & 31) == 0) {
+    s_r1[t >> 5] = a;
+    s_r2[t >> 5] = b;
+    s_rc[t >> 5] = c;
+  }
+  __syncthreads();
+  if (t == 0) {
+    double s1 = 0.0, s2 = 0.0;
+    unsigned long long n = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      s1 = __dadd_rn(s1, s_r1[w]);
+      s2 = __dadd_rn(s2, s_r2[w]);
+      n += s_rc[w];
+    }
+    double mu = 0.0, sigma = 0.0;
+    if (n) {
+      mu = __ddiv_rn(s1, (double)n);
+      double var = __dsub_rn(__ddiv_rn(s2, (double)n), __dmul_rn(mu, mu));
+      sigma = var > 0.0 ? __dsqrt_rn(var) : 0.0;
+    }
+    s_mu = mu;
+    s_sigma = sigma;
+  }
+  __syncthreads();
+  const double mu = s_mu, sigma = s_sigma;
+  unsigned char* book = segs[sg].book;
+  if (!(sigma > 0.0)) {
+    if (t == 0) {
+      int lo = field_of(mu) - 3;
+      lo = lo < 0 ? 0 : (lo > 248 ? 248 : lo);
+      for (int j = 0; j < 7; ++j) book[j] = (unsigned char)(lo + j);
+      book[7] = 0;
+      segs[sg].mu = mu;
+      segs[sg].sigma = sigma;
+    }
+    return;
+  }
+  // one field per thread (threads 1..254)
+  s_mass[t] = (t >= 1 && t <= 254) ? field_mass(mu, sigma, t) : -1.0;
+  __syncthreads();
+  int take = 0;
+  if (t >= 1 && t <= 254) {
+    const double m = s_mass[t];
+    int rank = 0;
+    for (int g = 1; g <= 254; ++g) {
+      const double mg = s_mass[g];
+      rank += (mg > m || (mg == m && g < t)) ? 1 : 0;
+    }
+    take = rank < 7;
+  }
+  s_take[t] = take;
+  __syncthreads();
+  if (take) {
+    int pos = 0;
+    for (int g = 1; g < t; ++g) pos += s_take[g];
+    book[pos] = (unsigned char)t;
+  }
+  if (t == 0) {
+    book[7] = 0;
+    segs[sg].mu = mu;
+    segs[sg].sigma = sigma;
+  }
+}
+
+}  // namespace
+
+cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
+                           const uint16_t* d_x, void* d_ws, cudaStream_t s) {
+  StatPartial* parts = reinterpret_cast<StatPartial*>(static_cast<char*>(d_ws) + kCtrlBytes);
+  const int al = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
+  if (L.nunits) {
+    zc_stats_kernel<<<(unsigned)L.nunits, kThreads, 0, s>>>(d_x, d_segs, L.nseg, L.U,
+                                                             parts, al);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  zc_predict_kernel<<<L.nseg, kThreads, 0, s>>>(const_cast<ZcSegDev*>(d_segs), L.nseg,
+                                                  L.nunits, parts);
+  return cudaGetLastError();
+}
+
+}  // namespace lbb

@@ -1,0 +1,256 @@
+"""GPU parity of the ZipCCL codec against the bit-serial oracle.
+
+Every test runs the CUDA path through the C ABI (liblbb16.so via ctypes) on
+seeded inputs and compares, byte for byte, with the oracle on the same input
+bytes: the compressed stream (header, tables, slots, escapes, padding) and the
+decoded tensor.  The codebooks follow the parity protocol of zc_parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from lossless_bit_level_bf16_gb300 import abi, workloads as W, zipccl as Z
+from zc_parity import check_plan, check_stream_equal, fields
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _bits_np(t):
+    return W.bf16_bits(t)
+
+
+def _roundtrip(x, seg=None, chunk=4096, books=None, fit=True):
+    """Returns (stream bytes on host, plan, decoded tensor)."""
+    plan = Z.Plan(x.numel(), seg, chunk)
+    if books is not None:
+        plan.set_books(books)
+    elif fit:
+        plan.fit(x)
+    out, nb = plan.compress(x)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    total = int(nb.item())
+    y = Z.decompress(out, n=x.numel(), in_bytes=total)
+    torch.cuda.synchronize()
+    assert abi.status(Z.decompress_workspace(out.device)) == 0
+    return out[:total].cpu().numpy(), plan, y
+
+
+def _check_full(x, seg=None, chunk=4096, books=None):
+    xb = _bits_np(x)
+    st, plan, y = _roundtrip(x, seg, chunk, books)
+    bk, mu, sg = plan.info()
+    if books is None:
+        check_plan(xb, seg, bk, mu, sg)
+    else:
+        assert np.array_equal(bk.reshape(-1), np.asarray(books, np.uint8).reshape(-1))
+    check_stream_equal(st, xb, seg, chunk, bk)
+    assert torch.equal(y.view(torch.int16), x.view(torch.int16)), "decode must be bit-exact"
+    rc, yo = O.zc_decode(st)
+    assert rc == 0 and np.array_equal(yo, xb)
+    return st, plan
+
+
+def test_gaussian_1m():
+    x = W.zc_gaussian(1 << 20, sigma=0.02, seed=0, device=DEV)
+    st, plan = _check_full(x)
+    bk, mu, sg = plan.info()
+    assert list(bk[0]) == list(range(116, 123))
+    ratio = x.numel() * 2 / st.size
+    assert ratio > 1.40
+
+
+@pytest.mark.parametrize("chunk", [1024, 2048, 4096, 8192, 65536])
+def test_every_bf16_pattern(chunk):
+    g = torch.Generator().manual_seed(chunk)
+    allv = torch.randperm(65536, generator=g).to(torch.int32)
+    allv = (allv - (allv >= 32768).to(torch.int32) * 65536).to(torch.int16)
+    for books in ([116, 117, 118, 119, 120, 121, 122], [0, 1, 2, 3, 4, 5, 6],
+                  [249, 250, 251, 252, 253, 254, 255], [0, 50, 100, 127, 128, 200, 255]):
+        for n in (1, 15, 1023, chunk + 17, 65536):
+            x = allv[:n].to(DEV).view(torch.bfloat16)
+            _check_full(x, None, chunk, books)
+
+
+def test_gradient_blocks_64m():
+    x, seg = W.zc_gradient(device=DEV)
+    st, plan = _check_full(x, seg)
+    assert x.numel() * 2 / st.size > 1.3
+
+
+def test_moe_experts():
+    x, seg, counts = W.zc_moe(device=DEV)
+    assert sum(counts) == 8192 and len(seg) == 65
+    st, plan = _check_full(x, seg)
+
+
+@pytest.mark.parametrize("chunk", [1024, 4096, 16384])
+def test_ragged_segments_and_alignment(chunk):
+    # empty segments, odd starts (no 16-byte alignment), tiny and large ones
+    lens = [0, 1, 7, 4095, 0, 4097, 12345, 3, 65536 + 5, 0]
+    seg = [0]
+    for L in lens:
+        seg.append(seg[-1] + L)
+    parts = []
+    for i, L in enumerate(lens):
+        parts.append(W.zc_gaussian(L, sigma=[0.02, 1e-3, 3.0, 1e-5][i % 4], seed=i, device=DEV))
+    x = torch.cat(parts)
+    _check_full(x, seg, chunk)
+    # a view at an odd element offset (input pointer not 16-byte aligned)
+    big = W.zc_gaussian(50001, sigma=0.5, seed=5, device=DEV)
+    _check_full(big[1:], None, chunk)
+
+
+def test_degenerate_values():
+    n = 10000
+    # constant data (sigma = 0), all zeros, NaN / inf mixes, huge and tiny values
+    cases = [
+        torch.full((n,), 1.0, device=DEV, dtype=torch.bfloat16),
+        torch.zeros(n, device=DEV, dtype=torch.bfloat16),
+        torch.full((n,), float("nan"), device=DEV, dtype=torch.bfloat16),
+        W.zc_gaussian(n, sigma=1e30, seed=1, device=DEV),
+        W.zc_gaussian(n, sigma=1e-30, seed=2, device=DEV),
+    ]
+    mix = W.zc_gaussian(n, sigma=0.02, seed=3, device=DEV)
+    mix[::17] = float("inf")
+    mix[1::17] = float("-inf")
+    mix[2::19] = float("nan")
+    mix[3::23] = 3e38
+    cases.append(mix)
+    for x in cases:
+        _check_full(x)
+
+
+def test_empty_input():
+    x = torch.empty(0, device=DEV, dtype=torch.bfloat16)
+    st, plan, y = _roundtrip(x)
+    assert st.size == 384 and y.numel() == 0
+    check_stream_equal(st, np.zeros(0, np.uint16), None, 4096, plan.info()[0])
+
+
+@pytest.mark.parametrize("mb", [1, 4, 16, 64, 256])
+def test_sweep_sizes_full(mb):
+    n = mb * (1 << 20) // 2
+    x = W.zc_gaussian(n, sigma=0.01, seed=0, device=DEV)
+    _check_full(x)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("gib", [1, 4])
+def test_sweep_sizes_sampled(gib):
+    """Full-size points: the decode must be exact everywhere (checked on the
+    device), escape offsets must be the prefix of per-chunk escape counts
+    (counted with torch), and sampled chunks must equal the oracle's."""
+    n = gib * (1 << 30) // 2
+    C = 4096
+    x = W.zc_gaussian(n, sigma=0.01, seed=0, device=DEV)
+    plan = Z.Plan(n, None, C)
+    plan.fit(x)
+    out, nb = plan.compress(x)
+    y = Z.decompress(out, n=n)
+    torch.cuda.synchronize()
+    assert plan.status() == 0 and abi.status(Z.decompress_workspace(out.device)) == 0
+    assert torch.equal(y.view(torch.int16), x.view(torch.int16))
+    del y
+    bk, mu, sg = plan.info()
+    book = torch.tensor(bk[0].astype(np.int64), device=DEV)
+    total = int(nb.item())
+    hdr = out[:128].cpu().numpy()
+    h = hdr[:80].view(np.uint64)
+    nchunks, esc_total = int(h[3]), int(h[4])
+    off_escoff, off_static, off_esc = int(h[6]), int(h[7]), int(h[8])
+    assert nchunks == n // C
+    f = ((x.view(torch.int16).to(torch.int32) >> 7) & 0xFF)
+    esc_per_chunk = (~torch.isin(f, book)).view(nchunks, C).sum(dim=1)
+    del f
+    eo = out[off_escoff:off_escoff + 8 * (nchunks + 1)].view(torch.int64)
+    want = torch.zeros(nchunks + 1, dtype=torch.int64, device=DEV)
+    want[1:] = torch.cumsum(esc_per_chunk, 0)
+    assert torch.equal(eo, want)
+    assert esc_total == int(want[-1])
+    assert total == O.zc_stream_bytes(n, None, C, esc_total)
+    S = C * 11 // 8
+    xb_dev = x.view(torch.int16)
+    rng = np.random.default_rng(gib)
+    eo_h = eo.cpu().numpy()
+    for c in list(rng.integers(0, nchunks, 24)) + [0, nchunks - 1]:
+        xc = xb_dev[c * C:(c + 1) * C].cpu().numpy().view(np.uint16)
+        slot, esc = O.zc_encode_chunk(xc, C, bk[0])
+        got = out[off_static + c * S: off_static + (c + 1) * S].cpu().numpy()
+        assert np.array_equal(got, slot), c
+        got_e = out[off_esc + int(eo_h[c]): off_esc + int(eo_h[c + 1])].cpu().numpy()
+        assert np.array_equal(got_e, esc), c
+    assert int(h[0]) & 0xFFFFFFFF == 0x3143435A
+
+
+def test_decode_rejects_corrupt_streams():
+    x = W.zc_gaussian(100000, sigma=0.02, seed=9, device=DEV)
+    plan = Z.Plan(x.numel(), None, 4096)
+    plan.fit(x)
+    out, nb = plan.compress(x)
+    torch.cuda.synchronize()
+    total = int(nb.item())
+    good = out[:total].clone()
+    ws = Z.decompress_workspace(out.device)
+
+    def run(buf, in_bytes=None, n=x.numel()):
+        y = torch.zeros(n, dtype=torch.bfloat16, device=DEV)
+        Z.decompress(buf, out=y, in_bytes=in_bytes if in_bytes is not None else buf.numel())
+        torch.cuda.synchronize()
+        return abi.status(ws)
+
+    assert run(good) == 0
+    hdr = good[:128].cpu().numpy().view(np.uint64)
+    for off in (0, 8, 16, 24, 32, 48, 56, 64, 72):
+        bad = good.clone()
+        bad[off] ^= 0x5A
+        assert run(bad) in (abi.ZC_ERR_FORMAT, abi.ZC_ERR_CAPACITY), off
+    assert run(good, in_bytes=total - 128) == abi.ZC_ERR_FORMAT
+    assert run(good, n=x.numel() - 1) == abi.ZC_ERR_CAPACITY
+    # escape-offset table entries out of range / inconsistent with the planes
+    off_escoff = int(hdr[6])
+    bad = good.clone()
+    bad[off_escoff + 8 * 5: off_escoff + 8 * 6] = torch.tensor(
+        list(np.uint64(1 << 40).tobytes()), dtype=torch.uint8, device=DEV)
+    assert run(bad) == abi.ZC_ERR_FORMAT
+    bad = good.clone()
+    bad[off_escoff + 8 * 5] ^= 1
+    assert run(bad) == abi.ZC_ERR_FORMAT
+    # eight codes of chunk 0 zeroed in all three planes: they read as escapes,
+    # so the chunk's escape count no longer matches the table
+    off_static = int(hdr[7])
+    bad = good.clone()
+    for k in range(3):
+        bad[off_static + 4096 + 512 * k + 3] = 0
+    assert run(bad) == abi.ZC_ERR_FORMAT
+
+
+def test_output_capacity_reported():
+    x = torch.full((50000,), float("nan"), dtype=torch.bfloat16, device=DEV)  # all escapes
+    plan = Z.Plan(x.numel(), None, 4096)
+    plan.fit(x)
+    fixed = plan.max_compressed_bytes - 50048
+    out = torch.zeros(fixed + 1000, dtype=torch.uint8, device=DEV)
+    plan.compress(x, out=out)
+    torch.cuda.synchronize()
+    assert plan.status() == abi.ZC_ERR_CAPACITY
+
+
+def test_plan_is_deterministic_and_reusable():
+    x = W.zc_gaussian(3 << 20, sigma=0.07, seed=4, device=DEV)
+    plan = Z.Plan(x.numel(), None, 4096)
+    plan.fit(x)
+    a, na = plan.compress(x)
+    a = a[: int(na.item())].clone()
+    plan.fit(x)
+    b, nb = plan.compress(x)
+    assert torch.equal(a, b[: int(nb.item())])
+    # reuse the plan's codebook on another tensor of the same layout
+    x2 = W.zc_gaussian(3 << 20, sigma=0.07, seed=5, device=DEV)
+    c, nc = plan.compress(x2)
+    torch.cuda.synchronize()
+    st = c[: int(nc.item())].cpu().numpy()
+    check_stream_equal(st, _bits_np(x2), None, 4096, plan.info()[0])

@@ -1,0 +1,469 @@
+"""Benchmark of the codec hot path on GB300: one JSON line on stdout.
+
+A step is one pass of every row of the hot path over one batch of synthetic
+input:
+  ZipCCL on the gradient-like bf16 buffer (64M elements, 256 layer blocks,
+  chunk 4096): zc_plan (statistics + codebooks) -> zc_compress -> zc_decompress;
+  IBP on the fp32 embedding table (1,000,000 x 128, one row per chunk, T = 0.9,
+  metadata from 10,000 seeded rows): ibp_build_meta -> ibp_compress ->
+  ibp_decompress.
+value = uncompressed bytes of both inputs / device time of the step (GB/s).
+Every op is bracketed by CUDA events on the stream it is launched on; L2 is
+flushed (a 512 MB buffer written) before every step, outside the timed
+events.  `e2e` repeats the step through host memory: pinned host inputs are
+copied in and the compressed streams copied out inside the timed region.
+
+--impl reference times the bit-serial CPU oracle (the checker; single thread)
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "encode/decode GB/s (uncompressed) and % of HBM roofline; compression ratio"
+WORKLOAD = ("zipccl gradient-like bf16 64M (256 blocks, chunk 4096) + "
+            "ibp fp32 table 1,000,000x128 (chunk 512 B, T=0.9, 10,000 samples)")
+
+# Algorithmic bytes per launch are computed from the actual stream sizes.
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _traffic_table():
+    """Measured DRAM traffic per launch from the committed ncu summaries:
+    lines 'traffic <kernel> <source sha1> <bytes>' in profiles/*.md."""
+    import glob
+    import hashlib
+    out = {}
+    for f in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        for line in open(f):
+            parts = line.strip().strip("`").split()
+            if len(parts) == 4 and parts[0] == "traffic":
+                out[parts[1]] = (parts[2], int(parts[3]))
+    srcs = {}
+    for name in ("zc_codec.cu", "zc_plan.cu", "ibp_codec.cu", "ibp_meta.cu"):
+        path = os.path.join(ROOT, "lossless_bit_level_bf16_gb300", "csrc", name)
+        srcs[name] = hashlib.sha1(open(path, "rb").read()).hexdigest()[:12]
+    return out, srcs
+
+
+KERNEL_SRC = {
+    "zc_stats": "zc_plan.cu", "zc_encode": "zc_codec.cu", "zc_decode": "zc_codec.cu",
+    "ibp_meta": "ibp_meta.cu", "ibp_encode": "ibp_codec.cu", "ibp_decode": "ibp_codec.cu",
+}
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                out, _ = self.p.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+                out, _ = self.p.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def reduce_max(x: float) -> float:
+    """Maximum of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(ms_local: float, bytes_per_rank: int, world: int):
+    """Replicas: every rank runs the whole workload on its own GPU; the job's
+    time is the slowest rank's, its throughput all ranks' bytes over that
+    time.  Returns (ms_max, GB/s)."""
+    ms = reduce_max(ms_local)
+    return ms, bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- GPU arm
+
+class Workload:
+    def __init__(self, device, scale=1.0):
+        import torch
+
+        from lossless_bit_level_bf16_gb300 import ibp as I, workloads as W, zipccl as Z
+        self.torch, self.I, self.Z = torch, I, Z
+        self.dev = device
+        nblk = max(1, int(256 * scale))
+        self.x, self.seg = W.zc_gradient(n_blocks=nblk, device=device)
+        self.n = self.x.numel()
+        self.plan = Z.Plan(self.n, self.seg, 4096, device=device)
+        self.zout = torch.empty(self.plan.max_compressed_bytes, dtype=torch.uint8, device=device)
+        self.znb = torch.zeros(1, dtype=torch.int64, device=device)
+        self.zy = torch.empty_like(self.x)
+        self.zdws = torch.empty(256, dtype=torch.uint8, device=device)
+        rows = max(1000, int(1_000_000 * scale))
+        self.table, idx = W.ibp_table(rows=rows, device=device)
+        self.samples = self.table[idx].contiguous()
+        self.cb = 512
+        self.tbytes = self.table.numel() * 4
+        self.meta = torch.empty(64 + 2 * self.cb,
+                                dtype=torch.uint8, device=device)
+        self.mws = torch.empty(I.workspace_bytes(self.cb, 0, self.samples.shape[0]),
+                               dtype=torch.uint8, device=device)
+        self.iws = torch.empty(I.workspace_bytes(self.cb, self.tbytes, 0), dtype=torch.uint8,
+                               device=device)
+        self.iout = torch.empty(I.max_compressed_bytes(self.cb, self.tbytes), dtype=torch.uint8,
+                                device=device)
+        self.inb = torch.zeros(1, dtype=torch.int64, device=device)
+        self.iy = torch.empty_like(self.table)
+        self.idws = torch.empty(256, dtype=torch.uint8, device=device)
+        self.mode = 0
+        self.unc_bytes = 2 * self.n + self.tbytes
+        self.launches_per_step = 8  # stats, predict, encode, decode, columns, meta, encode, decode
+
+    def ops(self):
+        I, Z = self.I, self.Z
+        return [
+            ("zc_plan", lambda: self.plan.fit(self.x)),
+            ("zc_compress", lambda: self.plan.compress(self.x, out=self.zout, out_bytes=self.znb)),
+            ("zc_decompress", lambda: Z.decompress(self.zout, out=self.zy, in_bytes=self.zout.numel(),
+                                                   ws=self.zdws)),
+            ("ibp_build_meta", lambda: I.build_meta(self.samples, self.cb, T=0.9, mode=self.mode,
+                                                    meta=self.meta, ws=self.mws)),
+            ("ibp_compress", lambda: I.compress(self.meta, self.table, self.cb, out=self.iout,
+                                                out_bytes=self.inb, ws=self.iws)),
+            ("ibp_decompress", lambda: I.decompress(self.meta, self.iout, self.tbytes, self.cb,
+                                                    out=self.iy, in_bytes=self.iout.numel(),
+                                                    ws=self.idws)),
+        ]
+
+    def check(self):
+        from lossless_bit_level_bf16_gb300 import abi
+        torch = self.torch
+        torch.cuda.synchronize()
+        for ws in (self.plan.ws, self.zdws, self.mws, self.iws, self.idws):
+            s = abi.status(ws)
+            if s != 0:
+                raise RuntimeError(f"device status {s}: {abi.strerror(s)}")
+        assert torch.equal(self.zy.view(torch.int16), self.x.view(torch.int16))
+        assert torch.equal(self.iy.view(torch.int32), self.table.view(torch.int32))
+
+    def sizes(self):
+        return int(self.znb.item()), int(self.inb.item())
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = Workload(dev, args.scale)
+    ops = wl.ops()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(timed):
+        flush.add_(1)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)]
+        evs[0].record(stream)
+        for i, (_, fn) in enumerate(ops):
+            fn()
+            evs[i + 1].record(stream)
+        return evs
+
+    for _ in range(args.warmup):
+        step(False)
+    wl.check()
+    zsz, isz = wl.sizes()
+    barrier()
+    torch.cuda.synchronize()
+    all_evs = []
+    with ClockSampler(local_rank) as clk:
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            all_evs.append(step(True))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier()
+    per_op = {name: [] for name, _ in ops}
+    steps_ms = []
+    for evs in all_evs:
+        steps_ms.append(evs[0].elapsed_time(evs[-1]))
+        for i, (name, _) in enumerate(ops):
+            per_op[name].append(evs[i].elapsed_time(evs[i + 1]))
+    ms = statistics.mean(steps_ms)
+    ms_max, _ = aggregate(ms, wl.unc_bytes, world)
+    wl.check()
+
+    # ---- end to end through host memory (pinned inputs in, streams out)
+    hx = torch.empty(wl.x.shape, dtype=wl.x.dtype, pin_memory=True)
+    hx.copy_(wl.x)
+    ht = torch.empty(wl.table.shape, dtype=wl.table.dtype, pin_memory=True)
+    ht.copy_(wl.table)
+    hs = torch.empty(wl.samples.shape, dtype=wl.samples.dtype, pin_memory=True)
+    hs.copy_(wl.samples)
+    hz = torch.empty(zsz, dtype=torch.uint8, pin_memory=True)
+    hi = torch.empty(isz, dtype=torch.uint8, pin_memory=True)
+    h_status = torch.empty(5 * 4, dtype=torch.uint8, pin_memory=True)
+    e2e_ms = []
+    for it in range(args.warmup + args.steps):
+        flush.add_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        wl.x.copy_(hx, non_blocking=True)
+        wl.table.copy_(ht, non_blocking=True)
+        wl.samples.copy_(hs, non_blocking=True)
+        for _, fn in ops:
+            fn()
+        hz.copy_(wl.zout[:zsz], non_blocking=True)
+        hi.copy_(wl.iout[:isz], non_blocking=True)
+        for j, ws in enumerate((wl.plan.ws, wl.zdws, wl.mws, wl.iws, wl.idws)):
+            h_status[4 * j:4 * j + 4].copy_(ws[:4], non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    wl.check()
+    e2e = statistics.mean(e2e_ms)
+    e2e_max = reduce_max(e2e)
+    h2d = hx.numel() * 2 + ht.numel() * 4 + hs.numel() * 4
+    d2h = zsz + isz + 20
+    return dict(wl=wl, per_op=per_op, ms=ms_max, ms_local=ms, wall=wall, clocks=clk.summary(),
+                e2e_ms=e2e_max, h2d=h2d, d2h=d2h, zsz=zsz, isz=isz)
+
+
+def report_gpu(args, r, world):
+    wl = r["wl"]
+    peak, peak_kind = _peaks()
+    n = wl.n
+    unc_total = wl.unc_bytes * world
+    value = unc_total / (r["ms"] * 1e-3) / 1e9
+    zsz, isz = r["zsz"], r["isz"]
+    # algorithmic bytes per launch (read + written)
+    nsamp = wl.samples.numel() * 4
+    alg = {
+        "zc_plan": 2 * n,
+        "zc_compress": 2 * n + zsz,
+        "zc_decompress": zsz + 2 * n,
+        "ibp_build_meta": nsamp,
+        "ibp_compress": wl.tbytes + isz,
+        "ibp_decompress": isz + wl.tbytes,
+    }
+    kern = {"zc_plan": "zc_stats", "zc_compress": "zc_encode", "zc_decompress": "zc_decode",
+            "ibp_build_meta": "ibp_meta", "ibp_compress": "ibp_encode",
+            "ibp_decompress": "ibp_decode"}
+    unc = {"zc_plan": 2 * n, "zc_compress": 2 * n, "zc_decompress": 2 * n,
+           "ibp_build_meta": nsamp, "ibp_compress": wl.tbytes, "ibp_decompress": wl.tbytes}
+    ops = {}
+    for name, ts in r["per_op"].items():
+        t = statistics.mean(ts)
+        ach = alg[name] / (t * 1e-3) / 1e9
+        ops[name] = {"ms": round(t, 4), "GBps_uncompressed": round(unc[name] / (t * 1e-3) / 1e9, 1),
+                     "GBps_traffic": round(ach, 1), "frac_hbm": round(ach / peak, 4)}
+    dom = max(r["per_op"], key=lambda k: statistics.mean(r["per_op"][k]))
+    t_dom = statistics.mean(r["per_op"][dom])
+    table, srcs = _traffic_table()
+    traffic = None
+    kname = kern[dom]
+    if kname in table and table[kname][0] == srcs[KERNEL_SRC[kname]]:
+        traffic = table[kname][1]
+    achieved = alg[dom] / (t_dom * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(r["ms"], 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8",
+        "data": "synthetic (seeded generators: gradient-like bf16 blocks, N(0,0.1) fp32 table)",
+        "config": {"workload": WORKLOAD, "zc_elements": n, "zc_segments": len(wl.seg) - 1,
+                   "zc_chunk": 4096, "ibp_rows": wl.table.shape[0], "ibp_chunk_bytes": wl.cb,
+                   "ibp_T": 0.9, "ibp_mode": "per-position", "ibp_samples": wl.samples.shape[0],
+                   "l2": "flushed before every step (512 MB write)",
+                   "parallelism": f"replicas x{world}"},
+        "ratio": {"zipccl": round(2 * n / zsz, 4), "ibp": round(wl.tbytes / isz, 4)},
+        "ops": ops,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "algorithmic_bytes_per_launch": alg[dom], "traffic": traffic},
+        "e2e": {"value": round(unc_total / (r["e2e_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": wl.launches_per_step * args.steps,
+        "clocks": r["clocks"],
+    }
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def cpu_baseline(seconds=15.0):
+    """The bit-serial oracle on a bounded sample of the same workload, scaled
+    to the step's byte mix (ZipCCL : IBP = 128 MiB : 512 MB)."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+    from lossless_bit_level_bf16_gb300 import workloads as W
+    O.build()
+    t_budget = max(1.0, seconds)
+    # ZipCCL sample: the first blocks of the gradient-like buffer
+    nblk = 32
+    x, seg = W.zc_gradient(n_blocks=nblk, device="cpu")
+    xb = W.bf16_bits(x)
+    t0 = time.perf_counter()
+    st, books, _, _ = O.zc_encode(xb, seg_off=seg, chunk_elems=4096)
+    rc, y = O.zc_decode(st)
+    tz = time.perf_counter() - t0
+    assert rc == 0 and np.array_equal(y, xb)
+    zc_rate = xb.size * 2 / tz  # bytes/s
+    # IBP sample: table rows
+    rows = 100_000
+    tab, idx = W.ibp_table(rows=rows, device="cpu", n_samples=10_000)
+    tb = W.f32_bytes(tab)
+    sb = W.f32_bytes(tab[idx].contiguous())
+    t0 = time.perf_counter()
+    meta = O.ibp_build_meta(sb, 512, T=0.9, mode=0)
+    tm = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    s2 = O.ibp_encode(meta, tb)
+    rc2, y2 = O.ibp_decode(meta, s2)
+    ti = time.perf_counter() - t0
+    assert rc2 == 0 and np.array_equal(y2, tb)
+    ibp_rate = tb.size / ti
+    zc_bytes, ibp_bytes = 2 * 256 * 262144, 1_000_000 * 512
+    step_s = zc_bytes / zc_rate + ibp_bytes / ibp_rate + tm
+    return {"value": round((zc_bytes + ibp_bytes) / step_s / 1e9, 4), "unit": "GB/s",
+            "cores": 1, "kind": "oracle",
+            "sample": f"ZipCCL encode+decode of {xb.size} elements (32 of the 256 blocks); "
+                      f"IBP metadata from 10,000 rows + encode+decode of {rows} rows; "
+                      f"scaled to the step's 128 MiB + 512 MB mix",
+            "sample_seconds": round(tz + tm + ti, 2)}
+
+
+def reference_arm(args):
+    steps_s = []
+    last = None
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        last = cpu_baseline(args.cpu_seconds)
+        if i >= args.warmup:
+            steps_s.append(time.perf_counter() - t0)
+    v = last["value"]
+    return {
+        "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1000 * statistics.mean(steps_s), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded generators; a bounded sample per step)",
+        "config": {"workload": WORKLOAD, "zc_chunk": 4096, "ibp_chunk_bytes": 512, "ibp_T": 0.9,
+                   "parallelism": "host cores"},
+        "impl": "reference",
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": last["sample"], "value": v},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--scale", type=float, default=1.0, help="workload scale (1 = full size)")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    args.warmup = max(args.warmup, 3)
+    r = gpu_arm(args, rank, world, local_rank)
+    if rank == 0:
+        args.cpu_baseline = args.cpu_baseline and world >= 1
+        line = report_gpu(args, r, world)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

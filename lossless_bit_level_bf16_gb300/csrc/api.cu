@@ -282,7 +282,8 @@ int ibp_build_meta(const void* d_samples, uint64_t n_samples, uint32_t cb, doubl
                    void* d_meta, void* d_ws, size_t ws_bytes, zc_stream_t stream) {
   if (!d_samples || !d_meta || !d_ws || n_samples == 0) return ZC_ERR_ARG;
   if (!ibp_chunk_ok(cb) || !(T > 0.5 && T <= 1.0) || (mode != 0 && mode != 1)) return ZC_ERR_ARG;
-  if (mode == 1 && cb > 2048) return ZC_ERR_UNSUPPORTED;
+  if (mode == 1 && (cb > 2048 || n_samples > 262144)) return ZC_ERR_UNSUPPORTED;
+  if (n_samples >= (1ull << 32)) return ZC_ERR_UNSUPPORTED;
   if (!aligned(d_samples, 16) || !aligned(d_meta, 16) || !aligned(d_ws, 256)) return ZC_ERR_ARG;
   if (ws_bytes < ibp_workspace_bytes(cb, 0, n_samples)) return ZC_ERR_CAPACITY;
   const unsigned long long k = (unsigned long long)std::ceil(T * (double)n_samples);

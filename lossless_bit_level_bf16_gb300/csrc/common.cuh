@@ -79,6 +79,18 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
                : "memory");
 }
 
+// Asynchronous global -> shared copies (cp.async, no register staging).
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
   return __byte_perm(a, b, s);
 }
@@ -130,8 +142,12 @@ __device__ __forceinline__ unsigned long long lookback_warp(
         to = true;
         break;
       }
-      __nanosleep(ns);
-      if (ns < 256) ns <<= 1;
+      // predecessors publish within a few microseconds: poll tightly first,
+      // back off only for long waits
+      if (spins > 64) {
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
+      }
       continue;
     }
     unsigned inc = __ballot_sync(kFull, flag == 2);

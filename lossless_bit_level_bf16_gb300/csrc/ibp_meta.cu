@@ -1,0 +1,241 @@
+// ibp_meta.cu -- IBP metadata: Mask and Bitval from sampled chunks.
+//
+// [IBP] = "Riepilogo Tecnico: Riduzione del Collo di Bottiglia della Memoria
+// GPU con la Compressione Lossless per il ML", Metodologia: Invariant Bit
+// Packing (IBP), Algoritmo Core, step 1 (Preprocessing): bit positions that
+// hold the same value across a high fraction T of the sampled tensors are
+// invariant; Mask marks them and Bitval keeps their values; the result is a
+// fixed-size blob kept in GPU memory and reused for the whole dataset.
+//
+// Kernels:
+//   ibp_columns_kernel  32 samples per warp: for each 32-bit word of the chunk
+//                       one ballot per bit position transposes the 32x32 bit
+//                       block, so lane b holds the column of position 32w+b
+//                       over those samples; its popcount is added to the ones
+//                       count of that position.  The columns are kept for the
+//                       joint reading.
+//   ibp_meta_kernel     one block: threshold k = ceil(T*N) on each position's
+//                       agreement max(ones, N-ones); per-position (mode 0) or
+//                       joint greedy selection (mode 1: positions sorted by
+//                       agreement, then index; a position is kept while at
+//                       least k samples still match every kept position);
+//                       writes the IBPM blob with its FNV-1a-64 hash.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lbb {
+namespace {
+
+constexpr int kMetaThreads = 1024;
+constexpr uint32_t kWordsPerWarp = 8;
+
+__global__ void __launch_bounds__(256) ibp_columns_kernel(
+    const uint32_t* __restrict__ samples, unsigned long long N, uint32_t W,
+    uint32_t* __restrict__ ones, uint32_t* __restrict__ cols, uint32_t Wn, int keep_cols) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long warp = (blockIdx.x * 256ull + threadIdx.x) >> 5;
+  const uint32_t wgroups = (W + kWordsPerWarp - 1) / kWordsPerWarp;
+  const unsigned long long sb = warp / wgroups;  // block of 32 samples
+  const uint32_t wg = (uint32_t)(warp % wgroups);
+  if (sb >= Wn) return;
+  const unsigned long long s = sb * 32ull + lane;
+  for (uint32_t w = wg * kWordsPerWarp; w < W && w < (wg + 1) * kWordsPerWarp; ++w) {
+    const uint32_t v = s < N ? __ldg(samples + s * W + w) : 0u;
+    uint32_t mine = 0;
+#pragma unroll
+    for (int b = 0; b < 32; ++b) {
+      const uint32_t r = __ballot_sync(kFull, (v >> b) & 1u);
+      if (lane == b) mine = r;
+    }
+    const uint32_t j = 32u * w + lane;  // bit position this lane now owns
+    if (mine) atomicAdd(ones + j, (uint32_t)__popc(mine));
+    if (keep_cols) cols[(unsigned long long)j * Wn + sb] = mine;
+  }
+}
+
+__device__ __forceinline__ uint32_t block_sum_1024(uint32_t v, uint32_t* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  __syncthreads();  // red reuse
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  uint32_t t = 0;
+#pragma unroll
+  for (int w = 0; w < kMetaThreads / 32; ++w) t += red[w];
+  return t;
+}
+
+// Dynamic shared memory: keys (8*Bp bytes, mode 1), alive (4*Wn), mask and
+// bitval words (4*W each).
+__global__ void __launch_bounds__(kMetaThreads) ibp_meta_kernel(
+    const uint32_t* __restrict__ ones, const uint32_t* __restrict__ cols, uint32_t Wn,
+    unsigned long long N, uint32_t chunk_bytes, unsigned long long k, double T, int mode,
+    uint32_t Bp, uint8_t* __restrict__ meta) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  __shared__ uint32_t red[kMetaThreads / 32];
+  const uint32_t B = chunk_bytes * 8u, W = chunk_bytes / 4u;
+  const int t = threadIdx.x;
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(dyn);
+  uint32_t* alive = reinterpret_cast<uint32_t*>(dyn + (mode == 1 ? 8ull * Bp : 0ull));
+  uint32_t* smask = alive + (mode == 1 ? Wn : 0u);
+  uint32_t* sbitv = smask + W;
+
+  for (uint32_t w = t; w < W; w += kMetaThreads) {
+    smask[w] = 0;
+    sbitv[w] = 0;
+  }
+  if (mode == 0) {
+    __syncthreads();
+    for (uint32_t w = t; w < W; w += kMetaThreads) {
+      uint32_t mk = 0, bv = 0;
+      for (int b = 0; b < 32; ++b) {
+        const unsigned long long o = ones[32u * w + b];
+        const unsigned long long agree = o > N - o ? o : N - o;
+        if (agree >= k) {
+          mk |= 1u << b;
+          if (o >= k) bv |= 1u << b;
+        }
+      }
+      smask[w] = mk;
+      sbitv[w] = bv;
+    }
+  } else {
+    // candidates sorted by (agreement descending, position ascending)
+    for (uint32_t j = t; j < Bp; j += kMetaThreads) {
+      unsigned long long key = ~0ull;
+      if (j < B) {
+        const unsigned long long o = ones[j];
+        const unsigned long long agree = o > N - o ? o : N - o;
+        if (agree >= k) key = ((N - agree) << 32) | j;
+      }
+      keys[j] = key;
+    }
+    for (uint32_t w = t; w < Wn; w += kMetaThreads) {
+      const unsigned long long rem = N - 32ull * w;
+      alive[w] = rem >= 32 ? 0xFFFFFFFFu : ((1u << rem) - 1u);
+    }
+    __syncthreads();
+    for (uint32_t size = 2; size <= Bp; size <<= 1) {
+      for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+        for (uint32_t i = t; i < Bp / 2; i += kMetaThreads) {
+          const uint32_t lo = 2 * i - (i & (stride - 1));
+          const uint32_t hi = lo + stride;
+          const bool up = (lo & size) == 0;
+          const unsigned long long a = keys[lo], b = keys[hi];
+          if ((a > b) == up) {
+            keys[lo] = b;
+            keys[hi] = a;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (uint32_t c = 0; c < Bp; ++c) {
+      const unsigned long long key = keys[c];
+      if (key == ~0ull) break;  // uniform: every thread reads the same key
+      const uint32_t j = (uint32_t)(key & 0xFFFFFFFFu);
+      const uint32_t v = ones[j] >= k ? 1u : 0u;
+      const uint32_t* col = cols + (unsigned long long)j * Wn;
+      uint32_t cnt = 0, keep[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const uint32_t w = t + r * kMetaThreads;
+        keep[r] = 0;
+        if (w < Wn) {
+          const uint32_t cw = col[w];
+          keep[r] = alive[w] & (v ? cw : ~cw);
+          cnt += __popc(keep[r]);
+        }
+      }
+      const uint32_t tot = block_sum_1024(cnt, red);
+      if (tot >= k) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const uint32_t w = t + r * kMetaThreads;
+          if (w < Wn) alive[w] = keep[r];
+        }
+        if (t == 0) {
+          smask[j >> 5] |= 1u << (j & 31);
+          if (v) sbitv[j >> 5] |= 1u << (j & 31);
+        }
+      }
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  // write Mask, Bitval and the header
+  uint32_t* om = reinterpret_cast<uint32_t*>(meta + kIbpmHeader);
+  uint32_t* ob = reinterpret_cast<uint32_t*>(meta + kIbpmHeader + chunk_bytes);
+  uint32_t pc = 0;
+  for (uint32_t w = t; w < W; w += kMetaThreads) {
+    om[w] = smask[w];
+    ob[w] = sbitv[w];
+    pc += __popc(smask[w]);
+  }
+  const uint32_t m = block_sum_1024(pc, red);
+  if (t == 0) {
+    unsigned long long h = 0xcbf29ce484222325ull;
+    const unsigned long long prime = 0x100000001b3ull;
+    for (int i = 0; i < 4; ++i) {
+      h ^= (chunk_bytes >> (8 * i)) & 0xFFu;
+      h *= prime;
+    }
+    for (uint32_t w = 0; w < W; ++w)
+      for (int i = 0; i < 4; ++i) {
+        h ^= (smask[w] >> (8 * i)) & 0xFFu;
+        h *= prime;
+      }
+    for (uint32_t w = 0; w < W; ++w)
+      for (int i = 0; i < 4; ++i) {
+        h ^= (sbitv[w] >> (8 * i)) & 0xFFu;
+        h *= prime;
+      }
+    unsigned long long* hd = reinterpret_cast<unsigned long long*>(meta);
+    hd[0] = (unsigned long long)kIbpmMagic | (1ull << 32) | ((unsigned long long)kIbpmHeader << 48);
+    hd[1] = (unsigned long long)chunk_bytes | ((unsigned long long)B << 32);
+    hd[2] = (unsigned long long)m | ((unsigned long long)(uint32_t)mode << 32);
+    hd[3] = N;
+    hd[4] = k;
+    hd[5] = (unsigned long long)__double_as_longlong(T);
+    hd[6] = h;
+    hd[7] = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t ibp_launch_build_meta(const void* d_samples, unsigned long long N,
+                                  uint32_t chunk_bytes, unsigned long long k, double T, int mode,
+                                  void* d_meta, void* d_ws, cudaStream_t s) {
+  const uint32_t W = chunk_bytes / 4, B = chunk_bytes * 8;
+  const uint32_t Wn = (uint32_t)((N + 31) / 32);
+  uint32_t* ones = reinterpret_cast<uint32_t*>(static_cast<char*>(d_ws) + kCtrlBytes);
+  uint32_t* cols = ones + B;
+  cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 4ull * B, s);
+  if (e != cudaSuccess) return e;
+  const uint32_t wgroups = (W + kWordsPerWarp - 1) / kWordsPerWarp;
+  const unsigned long long warps = (unsigned long long)Wn * wgroups;
+  const unsigned long long blocks = (warps + 7) / 8;
+  if (blocks > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+  ibp_columns_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint32_t*>(d_samples), N,
+                                                      W, ones, cols, Wn, mode == 1);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  uint32_t Bp = 1;
+  while (Bp < B) Bp <<= 1;
+  const size_t smem = (mode == 1 ? 8ull * Bp + 4ull * Wn : 0ull) + 8ull * W;
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(ibp_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  ibp_meta_kernel<<<1, kMetaThreads, smem, s>>>(ones, cols, Wn, N, chunk_bytes, k, T, mode, Bp,
+                                                static_cast<uint8_t*>(d_meta));
+  return cudaGetLastError();
+}
+
+}  // namespace lbb

@@ -80,149 +80,219 @@ __device__ __forceinline__ uint32_t sm4(uint32_t w0, uint32_t w1) {
   return (prmt(w0, w1, 0x7531) & 0x80808080u) | (prmt(w0, w1, 0x6420) & 0x7F7F7F7Fu);
 }
 
+constexpr int kSub = 4;                             // 4096-slot sub-tiles per ticket
+constexpr uint32_t kEncTile = kSub * kTileLanes;    // slots per ticket
+constexpr int kMaxTileChunks = kEncTile / 1024;     // chunks per ticket at C = 1024
+
+__device__ __forceinline__ void load16(const uint16_t* x, unsigned long long elem, int valid,
+                                       bool vec, uint32_t w[8]) {
+  if (valid == 16 && vec) {
+    const uint4 a = ld_nc_v4(x + elem), b = ld_nc_v4(x + elem + 8);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t l = (2 * j < valid) ? (uint32_t)__ldg(x + elem + 2 * j) : 0u;
+      const uint32_t h = (2 * j + 1 < valid) ? (uint32_t)__ldg(x + elem + 2 * j + 1) : 0u;
+      w[j] = l | (h << 16);
+    }
+  }
+}
+
+// One ticket = kSub sub-tiles of 4096 slots.  Per sub-tile: classify, write
+// the slot bytes and plane words, stage the escape bytes (compacted) in shared
+// memory.  Per ticket: one look-back for the escape offset, one copy of the
+// staged escapes.  The next sub-tile's loads are issued before the current
+// one is classified, and the next ticket is fetched one tile ahead.
 __global__ void __launch_bounds__(kThreads) zc_encode_kernel(EncArgs A) {
   __shared__ uint32_t s_lut[4][256];
+  __shared__ __align__(16) uint8_t s_esc[kEncTile];
   __shared__ uint32_t s_wtot[kThreads / 32];
-  __shared__ unsigned long long s_tile, s_excl;
-  __shared__ unsigned long long s_elem0[4];
-  __shared__ uint32_t s_valid[4];
-  __shared__ int s_al[4];
-  __shared__ int s_seg[4], s_lut_seg[4];
+  __shared__ unsigned long long s_tile, s_next, s_excl;
+  __shared__ unsigned long long s_elem0[kMaxTileChunks];
+  __shared__ uint32_t s_valid[kMaxTileChunks];
+  __shared__ int s_al[kMaxTileChunks], s_seg[kMaxTileChunks];
+  __shared__ uint32_t s_cpref[kMaxTileChunks];
+  __shared__ int s_lut_seg[4];
   __shared__ int s_last;
 
   const int t = threadIdx.x;
-  const uint32_t C = A.L.C, log2C = A.L.log2C;
-  const uint32_t cpt = C >= kTileLanes ? 1u : kTileLanes / C;  // chunks per tile
-  const unsigned long long S = A.L.slot_bytes;
+  const ZcLayout& L = A.L;
+  const uint32_t C = L.C, log2C = L.log2C;
+  const unsigned long long S = L.slot_bytes;
+  const unsigned long long lanes_total = L.nchunks << log2C;
+  const unsigned long long ntiles = (lanes_total + kEncTile - 1) / kEncTile;
+  const uint32_t nct = C >= kEncTile ? 1u : kEncTile / C;   // chunks per ticket
+  const uint32_t cps = C >= kTileLanes ? 1u : kTileLanes / C;  // chunks per sub-tile
+  int my_seg = -1;  // segment cache of threads < nct
+  unsigned long long my_c0 = 0, my_c1 = 0;
   if (t < 4) s_lut_seg[t] = -1;
+  if (t == 0) s_next = atomicAdd(&A.ctrl->ticket, 1ull);
 
   for (;;) {
-    if (t == 0) s_tile = atomicAdd(&A.ctrl->ticket, 1ull);
+    __syncthreads();
+    if (t == 0) {
+      s_tile = s_next;
+      if (s_next < ntiles) s_next = atomicAdd(&A.ctrl->ticket, 1ull);
+    }
     __syncthreads();
     const unsigned long long tile = s_tile;
-    if (tile >= A.L.ntiles) break;
-    const unsigned long long lane0 = tile * kTileLanes;
-    if (t < (int)cpt) {
-      const unsigned long long c = (lane0 >> log2C) + t;
-      if (c < A.L.nchunks) {
-        const int sg = find_chunk_segment(A.segs, A.L.nseg, c);
-        const ZcSegDev& r = A.segs[sg];
-        const unsigned long long e0 = r.elem_start + (c - r.chunk_start) * C;
+    if (tile >= ntiles) break;
+    const unsigned long long tlane0 = tile * kEncTile;
+    const unsigned long long cfirst = tlane0 >> log2C;
+    if (t < (int)nct) {
+      const unsigned long long c = cfirst + t;
+      if (c < L.nchunks) {
+        if (my_seg < 0 || c < my_c0 || c >= my_c1) {
+          my_seg = find_chunk_segment(A.segs, L.nseg, c);
+          my_c0 = A.segs[my_seg].chunk_start;
+          my_c1 = my_c0 + A.segs[my_seg].nchunks;
+        }
+        const ZcSegDev& r = A.segs[my_seg];
+        const unsigned long long e0 = r.elem_start + ((c - r.chunk_start) << log2C);
         const unsigned long long end = r.elem_start + r.nelem;
-        s_seg[t] = sg;
+        s_seg[t] = my_seg;
         s_elem0[t] = e0;
         s_valid[t] = (uint32_t)((end - e0) < C ? (end - e0) : C);
         s_al[t] = A.x_al16 && ((r.elem_start & 7ull) == 0);
       } else {
-        s_seg[t] = s_lut_seg[t];
+        s_seg[t] = -1;
         s_elem0[t] = 0;
         s_valid[t] = 0;
         s_al[t] = 0;
       }
     }
     __syncthreads();
-    for (uint32_t k = 0; k < cpt; ++k) {
-      const int sg = s_seg[k];
-      if (sg >= 0 && s_lut_seg[k] != sg) s_lut[k][t] = lut_entry(A.segs[sg].book, (uint32_t)t);
-    }
-    __syncthreads();
-    if (t < (int)cpt) s_lut_seg[t] = s_seg[t];
 
-    // ---- this thread's 16 slots
     const uint32_t lt = (uint32_t)t * 16u;
-    const unsigned long long lane = lane0 + lt;
-    const unsigned long long c = lane >> log2C;
-    const uint32_t i0 = (uint32_t)(lane & (C - 1));
-    const int lc = C >= kTileLanes ? 0 : (int)(lt >> log2C);
-    const bool live = c < A.L.nchunks;
-    const uint32_t vch = live ? s_valid[lc] : 0u;
-    const int valid = vch > i0 ? ((vch - i0) < 16u ? (int)(vch - i0) : 16) : 0;
-    const unsigned long long elem = s_elem0[lc] + i0;
-    uint32_t w[8];
-    if (valid == 16 && s_al[lc]) {
-      uint4 a = ld_nc_v4(A.x + elem), b = ld_nc_v4(A.x + elem + 8);
-      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t l = (2 * j < valid) ? (uint32_t)__ldg(A.x + elem + 2 * j) : 0u;
-        uint32_t h = (2 * j + 1 < valid) ? (uint32_t)__ldg(A.x + elem + 2 * j + 1) : 0u;
-        w[j] = l | (h << 16);
+    // slots of this thread in sub-tile `sub`
+    auto where = [&](int sub, int& lct, uint32_t& i0, int& valid, unsigned long long& elem) {
+      const uint32_t lit = (uint32_t)sub * kTileLanes + lt;  // slot index within the ticket
+      lct = C >= kEncTile ? 0 : (int)(lit >> log2C);
+      i0 = (uint32_t)((tlane0 + lit) & (C - 1));
+      const uint32_t vch = s_valid[lct];
+      valid = vch > i0 ? ((vch - i0) < 16u ? (int)(vch - i0) : 16) : 0;
+      elem = s_elem0[lct] + i0;
+    };
+    int lct;
+    uint32_t i0;
+    int valid;
+    unsigned long long elem;
+    uint32_t w[8], wn[8];
+    where(0, lct, i0, valid, elem);
+    load16(A.x, elem, valid, s_al[lct], w);
+    uint32_t running = 0;
+    for (int sub = 0; sub < kSub; ++sub) {
+      if (tlane0 + (unsigned long long)sub * kTileLanes >= lanes_total) break;  // uniform
+      int lct_n = 0, valid_n = 0;
+      uint32_t i0_n = 0;
+      unsigned long long elem_n = 0;
+      const bool more = sub + 1 < kSub && tlane0 + (unsigned long long)(sub + 1) * kTileLanes < lanes_total;
+      if (more) {
+        where(sub + 1, lct_n, i0_n, valid_n, elem_n);
+        load16(A.x, elem_n, valid_n, s_al[lct_n], wn);
       }
-    }
-    const uint32_t* Lt = s_lut[lc];
-    uint32_t accA = 0, accB = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      accA |= Lt[(w[j] >> 7) & 0xFFu] << (2 * j);
-      accA |= Lt[(w[j] >> 23) & 0xFFu] << (2 * j + 1);
-      accB |= Lt[(w[j + 4] >> 7) & 0xFFu] << (2 * j);
-      accB |= Lt[(w[j + 4] >> 23) & 0xFFu] << (2 * j + 1);
-    }
-    if (valid < 16) {  // slots past the segment end: code 0, no escape
-      const uint32_t vA = valid >= 8 ? 0xFFu : ((1u << valid) - 1u);
-      const uint32_t vB = valid >= 16 ? 0xFFu : (valid > 8 ? ((1u << (valid - 8)) - 1u) : 0u);
-      accA &= vA * 0x01010101u;
-      accB &= vB * 0x01010101u;
-    }
-    uint8_t* slot = A.out + A.L.off_static + c * S;
-    if (live) {
-      uint4 smv;
-      smv.x = sm4(w[0], w[1]);
-      smv.y = sm4(w[2], w[3]);
-      smv.z = sm4(w[4], w[5]);
-      smv.w = sm4(w[6], w[7]);
-      st_v4(slot + i0, smv);
-    }
-    const uint32_t T0 = prmt(accA, accB, 0x5140);  // plane0 | plane1 << 16
-    const uint32_t T1 = prmt(accA, accB, 0x7362);  // plane2 | escape << 16
-    const uint32_t U0 = __shfl_xor_sync(kFull, T0, 1);
-    const uint32_t U1 = __shfl_xor_sync(kFull, T1, 1);
-    if (live) {
-      uint32_t* pw = reinterpret_cast<uint32_t*>(slot + C) + (i0 >> 5);
-      const uint32_t pwords = C >> 5;  // 32-bit words per plane
-      if ((t & 1) == 0) {
-        pw[0] = prmt(T0, U0, 0x5410);
-        pw[pwords] = prmt(T0, U0, 0x7632);
-      } else {
-        pw[2 * pwords] = prmt(U1, T1, 0x5410);
+      // lookup tables of this sub-tile's chunks (slot k = chunk within the sub-tile)
+      const uint32_t cbase = ((uint32_t)sub * kTileLanes) >> log2C;
+      for (uint32_t k = 0; k < cps; ++k) {
+        const int sg = s_seg[cbase + k];
+        if (sg >= 0 && s_lut_seg[k] != sg) s_lut[k][t] = lut_entry(A.segs[sg].book, (uint32_t)t);
       }
-    }
-    const uint32_t esc = T1 >> 16;
+      __syncthreads();
+      if (t < (int)cps && s_seg[cbase + t] >= 0) s_lut_seg[t] = s_seg[cbase + t];
 
-    // ---- escape offsets: block scan, then look-back across tiles
-    uint32_t total;
-    const uint32_t excl = block_excl_scan<kThreads>((uint32_t)__popc(esc), s_wtot, &total);
+      const unsigned long long c = cfirst + lct;
+      const bool live = c < L.nchunks;
+      const uint32_t* Lt = s_lut[C >= kTileLanes ? 0 : (lt >> log2C)];
+      uint32_t accA = 0, accB = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        accA |= Lt[(w[j] >> 7) & 0xFFu] << (2 * j);
+        accA |= Lt[(w[j] >> 23) & 0xFFu] << (2 * j + 1);
+        accB |= Lt[(w[j + 4] >> 7) & 0xFFu] << (2 * j);
+        accB |= Lt[(w[j + 4] >> 23) & 0xFFu] << (2 * j + 1);
+      }
+      if (valid < 16) {  // slots past the segment end: code 0, no escape
+        const uint32_t vA = valid >= 8 ? 0xFFu : ((1u << valid) - 1u);
+        const uint32_t vB = valid >= 16 ? 0xFFu : (valid > 8 ? ((1u << (valid - 8)) - 1u) : 0u);
+        accA &= vA * 0x01010101u;
+        accB &= vB * 0x01010101u;
+      }
+      uint8_t* slot = A.out + L.off_static + c * S;
+      if (live) {
+        uint4 smv;
+        smv.x = sm4(w[0], w[1]);
+        smv.y = sm4(w[2], w[3]);
+        smv.z = sm4(w[4], w[5]);
+        smv.w = sm4(w[6], w[7]);
+        st_v4(slot + i0, smv);
+      }
+      const uint32_t T0 = prmt(accA, accB, 0x5140);  // plane0 | plane1 << 16
+      const uint32_t T1 = prmt(accA, accB, 0x7362);  // plane2 | escape << 16
+      const uint32_t U0 = __shfl_xor_sync(kFull, T0, 1);
+      const uint32_t U1 = __shfl_xor_sync(kFull, T1, 1);
+      if (live) {
+        uint32_t* pw = reinterpret_cast<uint32_t*>(slot + C) + (i0 >> 5);
+        const uint32_t pwords = C >> 5;
+        if ((t & 1) == 0) {
+          pw[0] = prmt(T0, U0, 0x5410);
+          pw[pwords] = prmt(T0, U0, 0x7632);
+        } else {
+          pw[2 * pwords] = prmt(U1, T1, 0x5410);
+        }
+      }
+      const uint32_t esc = T1 >> 16;
+      uint32_t total;
+      const uint32_t excl = block_excl_scan<kThreads>((uint32_t)__popc(esc), s_wtot, &total);
+      const uint32_t pos0 = running + excl;
+      if (live && i0 == 0) s_cpref[lct] = pos0;
+      if (esc) {
+        uint32_t F[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) F[q] = prmt(w[2 * q] >> 7, w[2 * q + 1] >> 7, 0x6420);
+        uint32_t m = esc, pos = pos0;
+        while (m) {
+          const int i = __ffs(m) - 1;
+          m &= m - 1;
+          const uint32_t f = i < 8 ? (i < 4 ? F[0] : F[1]) : (i < 12 ? F[2] : F[3]);
+          s_esc[pos++] = (uint8_t)((f >> ((i & 3) * 8)) & 0xFFu);
+        }
+      }
+      running += total;
+      __syncthreads();  // s_wtot, s_lut reuse
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = wn[j];
+      lct = lct_n;
+      i0 = i0_n;
+      valid = valid_n;
+      elem = elem_n;
+    }
+
+    // ---- one look-back per ticket, then the staged escapes go out
     if (t < 32) {
       bool to = false;
-      const unsigned long long e = lookback_warp(A.states, tile, total, &to);
+      const unsigned long long e = lookback_warp(A.states, tile, running, &to);
       if (t == 0) {
         s_excl = e;
         if (to) set_status(A.ctrl, ZC_ERR_TIMEOUT);
       }
     }
     __syncthreads();
-    const unsigned long long base = s_excl + excl;
-    if (live && i0 == 0)
-      reinterpret_cast<unsigned long long*>(A.out + A.L.off_escoff)[c] = base;
-    if (esc) {
-      uint32_t F[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) F[q] = prmt(w[2 * q] >> 7, w[2 * q + 1] >> 7, 0x6420);
-      uint32_t m = esc;
-      unsigned long long pos = A.L.off_esc + base;
-      while (m) {
-        const int i = __ffs(m) - 1;
-        m &= m - 1;
-        const uint32_t f = i < 8 ? (i < 4 ? F[0] : F[1]) : (i < 12 ? F[2] : F[3]);
-        const uint32_t e = (f >> ((i & 3) * 8)) & 0xFFu;
-        if (pos < A.out_cap) A.out[pos] = (uint8_t)e;
-        else set_status(A.ctrl, ZC_ERR_CAPACITY);
-        ++pos;
-      }
+    const unsigned long long base = s_excl;
+    const unsigned long long dst = L.off_esc + base;
+    if (dst + running <= A.out_cap) {
+      for (uint32_t i = t; i < running; i += kThreads) A.out[dst + i] = s_esc[i];
+    } else if (t == 0) {
+      set_status(A.ctrl, ZC_ERR_CAPACITY);
     }
-    __syncthreads();
+    // escape offsets of the chunks that start in this ticket
+    if (t < (int)nct) {
+      const unsigned long long c = cfirst + t;
+      const bool starts = C >= kEncTile ? ((tlane0 & (C - 1)) == 0) : true;
+      if (c < L.nchunks && starts)
+        reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = base + s_cpref[t];
+    }
   }
 
   // ---- the last block to finish writes the header, tables and padding
@@ -235,9 +305,8 @@ __global__ void __launch_bounds__(kThreads) zc_encode_kernel(EncArgs A) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const ZcLayout& L = A.L;
   unsigned long long esc_total = 0;
-  if (L.ntiles) esc_total = ld_acquire_u64(A.states + L.ntiles - 1) & kValMask;
+  if (ntiles) esc_total = ld_acquire_u64(A.states + ntiles - 1) & kValMask;
   const unsigned long long total = L.off_esc + round_up_dev(esc_total, kZcAlign);
   unsigned long long* escoff = reinterpret_cast<unsigned long long*>(A.out + L.off_escoff);
   if (t == 0) {
@@ -374,10 +443,84 @@ __device__ __forceinline__ uint32_t out_word(uint32_t S, uint32_t E, uint32_t se
   return (T & 0x007F007Fu) | ((T >> 1) & 0x7F807F80u) | ((T << 8) & 0x80008000u);
 }
 
+// Table entries of one chunk, copied to shared memory one unit ahead of use
+// (cp.async): the segment record picked by interpolation (segments of equal
+// size need no search), the end of the record before it, and the chunk's two
+// escape offsets.
+constexpr int kAheadWords = 11;
+enum { AH_ESTART, AH_NELEM, AH_CSTART, AH_NCHK, AH_BOOK, AH_PE0, AH_PE1, AH_PC0, AH_PC1, AH_ELO, AH_EHI };
+
+__device__ __forceinline__ uint32_t interp_segment(const DecHdr& h, unsigned long long c) {
+  uint32_t g = (uint32_t)(((double)c * (double)h.nseg) / (double)h.nchunks);
+  return g >= h.nseg ? h.nseg - 1 : g;
+}
+
+// Threads 0 .. kAheadWords*cpu-1 each start one 8-byte copy.
+__device__ __forceinline__ void ahead_issue(const uint8_t* in, const DecHdr& h,
+                                            unsigned long long c0, uint32_t cpu,
+                                            unsigned long long (*dst)[kAheadWords]) {
+  const int t = threadIdx.x;
+  if (t >= kAheadWords * (int)cpu) return;
+  const int k = t / kAheadWords, f = t % kAheadWords;
+  const unsigned long long c = c0 + k;
+  if (c >= h.nchunks) return;
+  const uint32_t g = interp_segment(h, c);
+  const uint8_t* rec = in + h.off_seg + (unsigned long long)kZcSegRec * g;
+  const uint8_t* src = nullptr;
+  switch (f) {
+    case AH_ESTART: src = rec; break;
+    case AH_NELEM: src = rec + 8; break;
+    case AH_CSTART: src = rec + 16; break;
+    case AH_NCHK: src = rec + 24; break;
+    case AH_BOOK: src = rec + 48; break;
+    case AH_PE0: src = g ? rec - kZcSegRec : nullptr; break;
+    case AH_PE1: src = g ? rec - kZcSegRec + 8 : nullptr; break;
+    case AH_PC0: src = g ? rec - kZcSegRec + 16 : nullptr; break;
+    case AH_PC1: src = g ? rec - kZcSegRec + 24 : nullptr; break;
+    case AH_ELO: src = in + h.off_escoff + 8 * c; break;
+    default: src = in + h.off_escoff + 8 * (c + 1); break;
+  }
+  if (src) cp_async8(&dst[k][f], src);
+}
+
+// Resolve chunk c from its read-ahead words: if the interpolated segment does
+// not hold the chunk, search the table.  False if the tables are inconsistent.
+__device__ bool ahead_resolve(const uint8_t* in, const DecHdr& h, unsigned long long c,
+                              const unsigned long long* a, SegRec& r) {
+  const uint32_t g = interp_segment(h, c);
+  if (!(c >= a[AH_CSTART] && c - a[AH_CSTART] < a[AH_NCHK])) {
+    int lo = 0, hi = (int)h.nseg - 1;  // largest s with chunk_start <= c
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (rd_u64(in + h.off_seg + (unsigned long long)kZcSegRec * mid + 16) <= c) lo = mid;
+      else hi = mid - 1;
+    }
+    if (!load_seg(in, h, (uint32_t)lo, r)) return false;
+  } else {
+    r.elem_start = a[AH_ESTART];
+    r.nelem = a[AH_NELEM];
+    r.chunk_start = a[AH_CSTART];
+    r.nchunks = a[AH_NCHK];
+    r.R0 = (uint32_t)(a[AH_BOOK] << 8);
+    r.R1 = (uint32_t)(a[AH_BOOK] >> 24);
+    if (r.nelem > h.n || r.elem_start > h.n - r.nelem) return false;
+    if (r.nchunks > h.nchunks || r.chunk_start > h.nchunks - r.nchunks) return false;
+    if (r.nchunks != ((r.nelem + h.C - 1) >> h.log2C)) return false;
+    if (g == 0 ? (r.elem_start != 0 || r.chunk_start != 0)
+               : (a[AH_PE0] + a[AH_PE1] != r.elem_start || a[AH_PC0] + a[AH_PC1] != r.chunk_start))
+      return false;
+  }
+  return c >= r.chunk_start && c < r.chunk_start + r.nchunks && a[AH_ELO] <= a[AH_EHI] &&
+         a[AH_EHI] <= h.esc_total;
+}
+
+constexpr uint32_t kEscStageBytes = 8192;  // escape bytes staged per decode unit
+
 __global__ void __launch_bounds__(kThreads) zc_decode_kernel(
     const uint8_t* __restrict__ in, unsigned long long in_bytes, uint16_t* __restrict__ y,
     unsigned long long y_cap, Ctrl* ctrl, int y_al16) {
   __shared__ uint32_t s_nib[256];
+  __shared__ __align__(16) uint32_t s_escw[kEscStageBytes / 4 + 2];
   __shared__ DecHdr s_h;
   __shared__ int s_ok;
   __shared__ uint32_t s_wtot[kThreads / 32];
@@ -385,12 +528,14 @@ __global__ void __launch_bounds__(kThreads) zc_decode_kernel(
   __shared__ unsigned long long s_elem0[4], s_elo[4], s_ehi[4];
   __shared__ uint32_t s_valid[4], s_R0[4], s_R1[4];
   __shared__ int s_al[4], s_bad;
+  __shared__ unsigned long long s_ahead[2][4][kAheadWords];
 
   const int t = threadIdx.x;
   if (t == 0) {
     int err;
     s_ok = parse_header(in, in_bytes, y_cap, s_h, err);
     if (!s_ok) set_status(ctrl, err);
+    s_bad = 0;
   }
   {
     uint32_t v = 0;
@@ -420,11 +565,16 @@ __global__ void __launch_bounds__(kThreads) zc_decode_kernel(
   const uint32_t cpu = C >= kTileLanes ? 1u : kTileLanes / C;          // chunks per unit
   const uint32_t steps = C >= kTileLanes ? C / kTileLanes : 1u;          // tiles per unit
   const unsigned long long nunits = C >= kTileLanes ? h.nchunks : (h.nchunks + cpu - 1) / cpu;
+  const uint8_t* esc_base = in + h.off_esc;
 
-  if (t == 0) s_bad = 0;
-  __syncthreads();
-  for (unsigned long long u = blockIdx.x; u < nunits; u += gridDim.x) {
+  ahead_issue(in, h, (unsigned long long)blockIdx.x * cpu, cpu, s_ahead[0]);
+  cp_async_commit();
+
+  int buf = 0;
+  for (unsigned long long u = blockIdx.x; u < nunits; u += gridDim.x, buf ^= 1) {
     const unsigned long long c0 = u * cpu;
+    cp_async_wait_all();
+    __syncthreads();
     if (t < (int)cpu) {
       const unsigned long long c = c0 + t;
       s_valid[t] = 0;
@@ -433,32 +583,42 @@ __global__ void __launch_bounds__(kThreads) zc_decode_kernel(
       s_R0[t] = s_R1[t] = 0;
       s_al[t] = 0;
       if (c < h.nchunks) {
-        int lo = 0, hi = (int)h.nseg - 1;  // largest s with chunk_start <= c
-        while (lo < hi) {
-          int mid = (lo + hi + 1) >> 1;
-          if (rd_u64(in + h.off_seg + (unsigned long long)kZcSegRec * mid + 16) <= c) lo = mid;
-          else hi = mid - 1;
-        }
         SegRec r;
-        const unsigned long long elo = rd_u64(escoff + 8 * c), ehi = rd_u64(escoff + 8 * (c + 1));
-        if (!load_seg(in, h, (uint32_t)lo, r) || c < r.chunk_start ||
-            c >= r.chunk_start + r.nchunks || elo > ehi || ehi > h.esc_total) {
+        const unsigned long long* a = s_ahead[buf][t];
+        if (!ahead_resolve(in, h, c, a, r)) {
           s_bad = 1;
         } else {
           const unsigned long long e0 = r.elem_start + ((c - r.chunk_start) << log2C);
           const unsigned long long end = r.elem_start + r.nelem;
           s_elem0[t] = e0;
           s_valid[t] = (uint32_t)((end - e0) < C ? (end - e0) : C);
-          s_elo[t] = elo;
-          s_ehi[t] = ehi;
+          s_elo[t] = a[AH_ELO];
+          s_ehi[t] = a[AH_EHI];
           s_R0[t] = r.R0;
           s_R1[t] = r.R1;
           s_al[t] = y_al16 && ((r.elem_start & 7ull) == 0);
         }
       }
     }
+    // the next unit's table entries are copied now and used one unit later
+    ahead_issue(in, h, (u + gridDim.x) * cpu, cpu, s_ahead[buf ^ 1]);
+    cp_async_commit();
     __syncthreads();
     const bool bad_tables = s_bad != 0;
+    // escape bytes of the whole unit are contiguous: [e_lo, e_hi)
+    uint32_t last = 0;
+    for (uint32_t k = 1; k < cpu; ++k)
+      if (c0 + k < h.nchunks) last = k;
+    const unsigned long long e_lo = s_elo[0], e_hi = s_ehi[last];
+    const bool staged = !bad_tables && e_hi >= e_lo && e_hi - e_lo <= kEscStageBytes;
+    const unsigned long long ew0 = e_lo >> 2;  // first escape word
+    if (staged) {
+      const uint32_t nw = (uint32_t)(((e_hi + 3) >> 2) - ew0);
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(esc_base) + ew0;
+      for (uint32_t i = t; i < nw; i += kThreads) cp_async4(&s_escw[i], src + i);
+    }
+    cp_async_commit();
+    const uint8_t* s_escb = reinterpret_cast<const uint8_t*>(s_escw);
     unsigned long long carry = 0;  // escapes in earlier tiles of this chunk
     for (uint32_t st = 0; st < (bad_tables ? 0u : steps); ++st) {
       const uint32_t lt = (uint32_t)t * 16u;
@@ -480,14 +640,15 @@ __global__ void __launch_bounds__(kThreads) zc_decode_kernel(
       }
       const uint32_t vmask = valid >= 16 ? 0xFFFFu : ((1u << valid) - 1u);
       const uint32_t esc = ~(p0 | p1 | p2) & vmask;
+      if (st == 0) cp_async_wait_all();  // staged escapes land before the barrier below
       uint32_t total;
       const uint32_t excl = block_excl_scan<kThreads>((uint32_t)__popc(esc), s_wtot, &total);
-      s_excl[t] = excl;
-      __syncthreads();
       unsigned long long base;
       if (C >= kTileLanes) {
         base = s_elo[0] + carry + excl;
       } else {
+        s_excl[t] = excl;
+        __syncthreads();
         const uint32_t tfirst = (uint32_t)lc * (C >> 4);  // first thread of this chunk
         base = s_elo[lc] + excl - s_excl[tfirst];
         // per-chunk check: escapes counted in the chunk == table difference
@@ -498,20 +659,22 @@ __global__ void __launch_bounds__(kThreads) zc_decode_kernel(
         }
       }
       const unsigned long long ehi = s_ehi[lc];
-      if (base + (unsigned long long)__popc(esc) > ehi) s_bad = 1;
+      const uint32_t ne = (uint32_t)__popc(esc);
+      if (base + ne > ehi) s_bad = 1;
 
       const uint32_t cA = s_nib[p0 & 0xFFu] | (s_nib[p1 & 0xFFu] << 1) | (s_nib[p2 & 0xFFu] << 2);
       const uint32_t cB = s_nib[p0 >> 8] | (s_nib[p1 >> 8] << 1) | (s_nib[p2 >> 8] << 2);
       const uint32_t R0 = s_R0[lc], R1 = s_R1[lc];
       uint32_t E0 = prmt(R0, R1, cA), E1 = prmt(R0, R1, cA >> 16);
       uint32_t E2 = prmt(R0, R1, cB), E3 = prmt(R0, R1, cB >> 16);
-      if (esc && base + (unsigned long long)__popc(esc) <= ehi) {
+      if (esc && base + ne <= ehi) {
         uint32_t m = esc;
-        unsigned long long pos = h.off_esc + base;
+        unsigned long long pos = base;
         while (m) {
           const int i = __ffs(m) - 1;
           m &= m - 1;
-          const uint32_t e = in[pos++];
+          const uint32_t e = staged ? s_escb[pos - (ew0 << 2)] : esc_base[pos];
+          ++pos;
           const uint32_t sh = (uint32_t)(i & 3) * 8u;
           const uint32_t keep = ~(0xFFu << sh), ins = e << sh;
           const int q = i >> 2;
@@ -542,7 +705,7 @@ __global__ void __launch_bounds__(kThreads) zc_decode_kernel(
         }
       }
       carry += total;
-      __syncthreads();  // s_excl / s_wtot reuse
+      if (st + 1 < steps) __syncthreads();  // s_wtot reuse
     }
     __syncthreads();
     if (t == 0) {
@@ -564,7 +727,8 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   Ctrl* ctrl = static_cast<Ctrl*>(d_ws);
   unsigned long long* states =
       reinterpret_cast<unsigned long long*>(static_cast<char*>(d_ws) + kCtrlBytes);
-  cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 8ull * L.ntiles, s);
+  const unsigned long long ntiles = ((L.nchunks << L.log2C) + kEncTile - 1) / kEncTile;
+  cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 8ull * ntiles, s);
   if (e != cudaSuccess) return e;
   EncArgs A;
   A.x = d_x;
@@ -577,7 +741,7 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   A.states = states;
   A.x_al16 = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
   const int res = resident_blocks((const void*)zc_encode_kernel, kThreads, 0);
-  unsigned long long grid = L.ntiles < (unsigned long long)res ? L.ntiles : (unsigned long long)res;
+  unsigned long long grid = ntiles < (unsigned long long)res ? ntiles : (unsigned long long)res;
   if (grid == 0) grid = 1;
   zc_encode_kernel<<<(unsigned)grid, kThreads, 0, s>>>(A);
   return cudaGetLastError();

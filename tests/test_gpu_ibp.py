@@ -1,0 +1,210 @@
+"""GPU parity of the IBP codec against the bit-serial oracle.
+
+The CUDA path runs through the C ABI on seeded inputs; the metadata blob, the
+compressed stream and the decoded bytes are compared byte for byte with the
+oracle on the same input bytes.  At full size (the 512 MB table, the sweep's
+largest points) the oracle checks sampled groups and the rest is checked by
+properties that hold at any size (exact decode, group offsets = prefix of the
+group lengths implied by the participation bits).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from lossless_bit_level_bf16_gb300 import abi, ibp as I, workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _ws(cb, n_bytes=0, n_samples=0):
+    return torch.empty(max(I.workspace_bytes(cb, n_bytes, n_samples), 256), dtype=torch.uint8,
+                       device=DEV)
+
+
+def _u8(t):
+    return t.detach().contiguous().view(torch.uint8).cpu().numpy().reshape(-1)
+
+
+def _gpu_roundtrip(meta_dev, x, cb):
+    n_bytes = x.numel() * x.element_size()
+    ws = _ws(cb, n_bytes)
+    st, nb = I.compress(meta_dev, x, cb, ws=ws)
+    torch.cuda.synchronize()
+    assert I.status(ws) == 0, abi.strerror(I.status(ws))
+    total = int(nb.item())
+    dws = _ws(cb)
+    y = I.decompress(meta_dev, st, n_bytes, cb, in_bytes=total, ws=dws, dtype=torch.uint8)
+    torch.cuda.synchronize()
+    assert I.status(dws) == 0, abi.strerror(I.status(dws))
+    return st[:total], y
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_meta_table_rows(mode):
+    rows, idx = W.ibp_table(rows=200_000, cols=128, std=0.1, seed=0, device=DEV)
+    samples = rows[idx].contiguous()
+    ws = _ws(512, 0, samples.shape[0])
+    meta = I.build_meta(samples, 512, T=0.9, mode=mode, ws=ws)
+    torch.cuda.synchronize()
+    assert I.status(ws) == 0
+    ref = O.ibp_build_meta(_u8(samples), 512, T=0.9, mode=mode)
+    got = _u8(meta)
+    assert np.array_equal(got, ref), np.nonzero(got != ref)[0][:10]
+    m = int(got[16:20].view(np.uint32)[0])
+    assert (mode == 0 and m >= 512) or (mode == 1 and 400 <= m <= 640)
+
+
+@pytest.mark.parametrize("cb", [16, 48, 64, 512, 1040, 2048, 4096])
+@pytest.mark.parametrize("frac", [0.0, 0.12, 0.5, 1.0])
+def test_random_masks(cb, frac):
+    rng = np.random.default_rng(cb * 10 + int(frac * 100))
+    B = cb * 8
+    mask = (rng.uniform(size=B) < frac).astype(np.uint8)
+    bitval = rng.integers(0, 2, size=B).astype(np.uint8) & mask
+    meta = O.ibp_make_meta(cb, np.packbits(mask, bitorder="little"),
+                           np.packbits(bitval, bitorder="little"))
+    nch = 97
+    bits = rng.integers(0, 2, size=(nch, B)).astype(np.uint8)
+    force = rng.uniform(size=nch) < 0.6
+    bits[force] = np.where(mask.astype(bool), bitval, bits[force])
+    x = np.packbits(bits, axis=1, bitorder="little").reshape(-1)
+    for n_bytes in (x.size, x.size - cb // 2 // 4 * 4 if cb >= 8 else x.size, 4, 0):
+        xs = np.ascontiguousarray(x[:n_bytes])
+        xd = torch.from_numpy(xs.copy()).to(DEV)
+        md = torch.from_numpy(meta).to(DEV)
+        st, y = _gpu_roundtrip(md, xd, cb)
+        ref = O.ibp_encode(meta, xs)
+        got = st.cpu().numpy()
+        assert got.size == ref.size and np.array_equal(got, ref), (n_bytes, np.nonzero(got != ref)[0][:8])
+        assert np.array_equal(y.cpu().numpy(), xs)
+
+
+def test_table_full_size_sampled():
+    """The 1,000,000 x 128 fp32 table (512 MB), metadata from 10,000 rows."""
+    rows, idx = W.ibp_table(device=DEV)
+    samples = rows[idx].contiguous()
+    cb = 512
+    for mode in (0, 1):
+        ws = _ws(cb, 0, samples.shape[0])
+        meta = I.build_meta(samples, cb, T=0.9, mode=mode, ws=ws)
+        st, y = _gpu_roundtrip(meta, rows, cb)
+        assert torch.equal(y.view(torch.int32), rows.view(-1).view(torch.int32))
+        del y
+        mh = _u8(meta)
+        m = int(mh[16:20].view(np.uint32)[0])
+        mask = torch.from_numpy(mh[64:64 + cb].view(np.int32).copy()).to(DEV)
+        bitv = torch.from_numpy(mh[64 + cb:64 + 2 * cb].view(np.int32).copy()).to(DEV)
+        xi = rows.view(torch.int32)
+        p = (((xi ^ bitv) & mask) == 0).all(dim=1) & (m > 0)
+        nch = rows.shape[0]
+        ng = (nch + 31) // 32
+        lens = torch.where(p, cb * 8 - m, cb * 8).to(torch.int64)
+        pad = torch.zeros(ng * 32, dtype=torch.int64, device=DEV)
+        pad[:nch] = lens
+        gbits = pad.view(ng, 32).sum(1) + 32
+        gbits = (gbits + 127) // 128 * 128
+        st_h = st.cpu().numpy()
+        grp = st_h[128:128 + 8 * (ng + 1)].view(np.uint64)
+        want = np.zeros(ng + 1, np.uint64)
+        want[1:] = np.cumsum(gbits.cpu().numpy())
+        assert np.array_equal(grp, want)
+        off_pay = int(st_h[56:64].view(np.uint64)[0])
+        x_h = _u8(rows)
+        rng = np.random.default_rng(mode)
+        for g in list(rng.integers(0, ng, 16)) + [0, ng - 1]:
+            n_in = min(32, nch - 32 * g)
+            gb = O.ibp_encode_group(mh, x_h[32 * g * cb:(32 * g + n_in) * cb], n_in)
+            assert np.array_equal(st_h[off_pay + int(grp[g]) // 8: off_pay + int(grp[g + 1]) // 8], gb), g
+        ratio = rows.numel() * 4 / st.numel()
+        print(f"mode {mode}: m={m} participation={p.float().mean().item():.4f} ratio={ratio:.4f}")
+
+
+@pytest.mark.parametrize("mb", [1, 4, 16])
+def test_sweep_full(mb):
+    cb = 2048
+    x = W.ibp_gaussian(mb * (1 << 20) // 4, std=0.02, seed=0, device=DEV)
+    nch = x.numel() * 4 // cb
+    idx = W.sample_rows(nch, 10_000, seed=1, device=DEV)
+    samples = x.view(nch, cb // 4)[idx].contiguous()
+    for mode in (0, 1):
+        ws = _ws(cb, 0, samples.shape[0])
+        meta = I.build_meta(samples, cb, T=0.9, mode=mode, ws=ws)
+        mref = O.ibp_build_meta(_u8(samples), cb, T=0.9, mode=mode)
+        assert np.array_equal(_u8(meta), mref)
+        st, y = _gpu_roundtrip(meta, x, cb)
+        ref = O.ibp_encode(mref, _u8(x))
+        assert np.array_equal(st.cpu().numpy(), ref)
+        assert torch.equal(y.view(torch.int32), x.view(torch.int32))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mb", [64, 256, 1024, 4096])
+def test_sweep_sampled(mb):
+    cb = 2048
+    x = W.ibp_gaussian(mb * (1 << 20) // 4, std=0.02, seed=0, device=DEV)
+    nch = x.numel() * 4 // cb
+    idx = W.sample_rows(nch, 10_000, seed=1, device=DEV)
+    samples = x.view(nch, cb // 4)[idx].contiguous()
+    meta = I.build_meta(samples, cb, T=0.9, mode=0, ws=_ws(cb, 0, samples.shape[0]))
+    st, y = _gpu_roundtrip(meta, x, cb)
+    assert torch.equal(y.view(torch.int32), x.view(torch.int32))
+    del y
+    mh = _u8(meta)
+    ng = (nch + 31) // 32
+    grp = st[128:128 + 8 * (ng + 1)].view(torch.int64).cpu().numpy()
+    off_pay = int(st[56:64].cpu().numpy().view(np.uint64)[0])
+    rng = np.random.default_rng(mb)
+    for g in list(rng.integers(0, ng, 8)) + [0, ng - 1]:
+        n_in = min(32, nch - 32 * g)
+        xg = x.view(torch.uint8)[32 * g * cb:(32 * g + n_in) * cb].cpu().numpy()
+        gb = O.ibp_encode_group(mh, xg, n_in)
+        assert np.array_equal(st[off_pay + grp[g] // 8: off_pay + grp[g + 1] // 8].cpu().numpy(), gb)
+
+
+def test_errors_reported():
+    rng = np.random.default_rng(3)
+    cb = 512
+    meta = O.ibp_make_meta(cb, np.packbits((rng.uniform(size=cb * 8) < 0.2).astype(np.uint8),
+                                           bitorder="little"), np.zeros(cb, np.uint8))
+    md = torch.from_numpy(meta).to(DEV)
+    x = torch.from_numpy(rng.integers(0, 256, size=cb * 40, dtype=np.uint8)).to(DEV)
+    st, y = _gpu_roundtrip(md, x, cb)
+    n = x.numel()
+
+    def dec(meta_dev, buf, y_bytes=n, in_bytes=None):
+        ws = _ws(cb)
+        out = torch.zeros(y_bytes, dtype=torch.uint8, device=DEV)
+        I.decompress(meta_dev, buf, y_bytes, cb, out=out, ws=ws,
+                     in_bytes=buf.numel() if in_bytes is None else in_bytes)
+        torch.cuda.synchronize()
+        return I.status(ws)
+
+    other = O.ibp_make_meta(cb, np.packbits((rng.uniform(size=cb * 8) < 0.2).astype(np.uint8),
+                                            bitorder="little"), np.zeros(cb, np.uint8))
+    assert dec(torch.from_numpy(other).to(DEV), st) == abi.ZC_ERR_META_MISMATCH
+    assert dec(md, st, y_bytes=n - 4) == abi.ZC_ERR_CAPACITY
+    assert dec(md, st, in_bytes=st.numel() - 16) == abi.ZC_ERR_FORMAT
+    bad = st.clone()
+    bad[136] ^= 0x80  # second group offset
+    assert dec(md, bad) == abi.ZC_ERR_FORMAT
+    bad = st.clone()
+    bad[0] ^= 1
+    assert dec(md, bad) == abi.ZC_ERR_FORMAT
+    # participation bit set on a chunk that does not match: lengths disagree
+    bad = st.clone()
+    off_pay = int(st[56:64].cpu().numpy().view(np.uint64)[0])
+    bad[off_pay] ^= 0xFF
+    assert dec(md, bad) in (abi.ZC_ERR_FORMAT,)
+    # compress into a buffer that is too small
+    ws = _ws(cb, n)
+    small = torch.zeros(300, dtype=torch.uint8, device=DEV)
+    I.compress(md, x, cb, out=small, ws=ws)
+    torch.cuda.synchronize()
+    assert I.status(ws) == abi.ZC_ERR_CAPACITY
+    # metadata made for another chunk size
+    ws = _ws(1024, n)
+    I.compress(md, x, 1024, ws=ws)
+    torch.cuda.synchronize()
+    assert I.status(ws) == abi.ZC_ERR_META_MISMATCH

@@ -169,6 +169,91 @@ __device__ __forceinline__ unsigned long long lookback_warp(
   return excl;
 }
 
+// Look-back with an adaptive window: the nearest 32 predecessors are read
+// first (one state per lane; usually one of them already holds an inclusive
+// prefix); if all 32 hold only aggregates the walk continues kLbDepth*32
+// states per L2 round trip.  Spinning on a predecessor that has not published
+// yet re-reads only the current window.
+constexpr int kLbDepth = 8;
+enum { kLbEmpty = 0, kLbFound = 1, kLbAllAgg = 2 };
+
+template <int D>
+__device__ __forceinline__ int lb_window(const unsigned long long* states, long long end,
+                                         unsigned long long* sum) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  unsigned long long s[D];
+#pragma unroll
+  for (int j = 0; j < D; ++j) {
+    const long long idx = end - (32 * j + lane);
+    s[j] = idx >= 0 ? ld_relaxed_u64(states + idx) : kFlagInc;
+  }
+  int jinc = D, linc = 32;
+  bool empty_before = false;
+#pragma unroll
+  for (int j = 0; j < D; ++j) {
+    const unsigned f = (unsigned)(s[j] >> 62);
+    const unsigned inc = __ballot_sync(kFull, f == 2);
+    const unsigned emp = __ballot_sync(kFull, f == 0);
+    if (jinc == D) {
+      if (inc) {
+        jinc = j;
+        linc = __ffs(inc) - 1;
+        if (emp & ((1u << linc) - 1u)) empty_before = true;
+      } else if (emp) {
+        empty_before = true;
+      }
+    }
+  }
+  if (empty_before) return kLbEmpty;
+  unsigned long long part = 0;
+#pragma unroll
+  for (int j = 0; j < D; ++j)
+    if (j < jinc || (j == jinc && lane <= linc)) part += s[j] & kValMask;
+  *sum = warp_sum_u64(part);
+  return jinc < D ? kLbFound : kLbAllAgg;
+}
+
+__device__ __forceinline__ unsigned long long lookback_warp_wide(
+    unsigned long long* states, unsigned long long tile, unsigned long long aggregate,
+    bool* timed_out) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  if (tile == 0) {
+    if (lane == 0) st_release_u64(states, kFlagInc | aggregate);
+    return 0;
+  }
+  if (lane == 0) st_release_u64(states + tile, kFlagAgg | aggregate);
+  unsigned long long excl = 0;
+  long long end = (long long)tile - 1;
+  unsigned spins = 0, ns = 32;
+  bool deep = false, to = false;
+  while (true) {
+    unsigned long long sum = 0;
+    const int r = deep ? lb_window<kLbDepth>(states, end, &sum) : lb_window<1>(states, end, &sum);
+    if (r == kLbEmpty) {
+      if (++spins > kMaxSpins) {
+        to = true;
+        break;
+      }
+      if (spins > 64) {
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
+      }
+      continue;
+    }
+    excl += sum;
+    if (r == kLbFound) break;
+    end -= deep ? 32 * kLbDepth : 32;
+    deep = true;
+  }
+  if (to) {
+    *timed_out = true;
+    if (lane == 0) st_release_u64(states + tile, kFlagInc | aggregate);
+    return 0;
+  }
+  if (lane == 0) st_release_u64(states + tile, kFlagInc | ((excl + aggregate) & kValMask));
+  return excl;
+}
+
 // ---------------------------------------------------------------- block scan
 //
 // Exclusive scan of one uint32 per thread over a block of NT threads

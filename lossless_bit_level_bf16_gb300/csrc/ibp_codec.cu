@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_encode_kernel(IbpEncArgs 
   extern __shared__ __align__(16) uint32_t dyn[];
   __shared__ uint32_t s_scr[NT / 32 + 4];
   __shared__ uint32_t s_pword;
-  __shared__ unsigned long long s_g, s_next, s_excl;
+  __shared__ unsigned long long s_g, s_excl;
   __shared__ int s_last;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t cb = A.cb, W = cb / 4, B = cb * 8;
@@ -96,13 +96,13 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_encode_kernel(IbpEncArgs 
   uint32_t* gbuf = dyn + ibp_table_words(W);
   const uint32_t m = T.m;
   const unsigned long long tail_bytes = A.n_bytes - (A.nchunks ? (A.nchunks - 1) * cb : 0ull);
+  for (uint32_t w = t; w < ibp_group_words(cb); w += NT) gbuf[w] = 0;
+  __syncthreads();
 
-  if (t == 0) s_next = ok ? atomicAdd(&A.ctrl->ticket, 1ull) : A.ngroups;
   for (;;) {
     if (t == 0) {
-      // the ticket after this one is fetched now, used one group later
-      s_g = s_next;
-      if (s_next < A.ngroups) s_next = atomicAdd(&A.ctrl->ticket, 1ull);
+      // the ticket is taken when the group starts (see the look-back notes)
+      s_g = ok ? atomicAdd(&A.ctrl->ticket, 1ull) : A.ngroups;
       s_pword = 0;
     }
     __syncthreads();
@@ -152,12 +152,9 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_encode_kernel(IbpEncArgs 
     unsigned long long bits = 32ull + (unsigned long long)nch * B - (unsigned long long)np * m;
     if (c0 + nch == A.nchunks && tail_bytes != cb) bits -= 8ull * (cb - tail_bytes);
     const unsigned long long padded = round_up_dev(bits, 128);
-    const uint32_t gwords = (uint32_t)(padded >> 5);
     // publish the aggregate now; the look-back below resolves it later
     if (t == 0 && g > 0) st_release_u64(A.states + g, kFlagAgg | padded);
-    for (uint32_t w = t; w < gwords + 1; w += NT) gbuf[w] = 0;
-    __syncthreads();
-    if (t == 0) gbuf[0] = pword;
+    if (t == 0) gbuf[0] = pword;  // the image is all zeros here (cleared at copy-out)
 
     // ---- phase 2: close up kept bits into the group image
 #pragma unroll
@@ -186,7 +183,7 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_encode_kernel(IbpEncArgs 
     // ---- look-back for the group's bit offset
     if (warp == 0) {
       bool to = false;
-      const unsigned long long e = lookback_warp(A.states, g, padded, &to);
+      const unsigned long long e = lookback_warp_wide(A.states, g, padded, &to);
       if (lane == 0) {
         s_excl = e;
         if (to) set_status(A.ctrl, ZC_ERR_TIMEOUT);
@@ -196,11 +193,15 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_encode_kernel(IbpEncArgs 
     const unsigned long long gpos = s_excl;  // bits, multiple of 128
     const unsigned long long dst = A.off_payload + (gpos >> 3);
     const unsigned long long nbytes = padded >> 3;
-    if (dst + nbytes <= A.out_cap) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(gbuf);
-      for (uint32_t v = t; v < (uint32_t)(nbytes >> 4); v += NT) st_v4(A.out + dst + 16ull * v, s4[v]);
-    } else if (t == 0) {
-      set_status(A.ctrl, ZC_ERR_CAPACITY);
+    {
+      // copy the image out and clear it for the next group in the same pass
+      uint4* s4 = reinterpret_cast<uint4*>(gbuf);
+      const bool fits = dst + nbytes <= A.out_cap;
+      for (uint32_t v = t; v < (uint32_t)(nbytes >> 4); v += NT) {
+        if (fits) st_v4(A.out + dst + 16ull * v, s4[v]);
+        s4[v] = make_uint4(0, 0, 0, 0);
+      }
+      if (!fits && t == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
     }
     if (t == 0) reinterpret_cast<unsigned long long*>(A.out + kIbp1Header)[g] = gpos;
     __syncthreads();
@@ -314,6 +315,22 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_decode_kernel(IbpDecArgs 
   const unsigned long long* grp = reinterpret_cast<const unsigned long long*>(A.in + kIbp1Header);
   const unsigned long long tail_bytes = n_bytes - (nchunks ? (nchunks - 1) * cb : 0ull);
   const uint32_t max_words = ibp_group_words(cb);
+  // small chunks: keep this lane's per-word tables in registers
+  constexpr bool kRegTab = false;  // registers per lane outweigh the saved loads at 4 blocks/SM
+  uint32_t rK[kRegTab ? WPL : 1], rV[kRegTab ? WPL : 1], rP[kRegTab ? WPL : 1];
+  uint32_t rMV[kRegTab ? WPL : 1][5];
+  if (kRegTab) {
+#pragma unroll
+    for (int j = 0; j < WPL; ++j) {
+      const uint32_t w = owned_word<VEC>(lane, j);
+      const bool in = w < W;
+      rK[j] = in ? T.K[w] : 0u;
+      rV[j] = in ? T.V[w] : 0u;
+      rP[j] = in ? T.P[w] : 0u;
+#pragma unroll
+      for (int i = 0; i < 5; ++i) rMV[j][i] = in ? T.MV[i * W + w] : 0u;
+    }
+  }
 
   for (unsigned long long g = blockIdx.x; g < ngroups; g += gridDim.x) {
     const unsigned long long g0 = grp[g], g1 = grp[g + 1];
@@ -375,10 +392,17 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_decode_kernel(IbpDecArgs 
             o[q] = 0;
             if (ww < wv) {
               if (p) {
-                const uint32_t K = T.K[ww];
-                const uint32_t k = __popc(K);
-                const uint32_t f = k ? get_bits(gbuf, off + T.P[ww], k) : 0u;
-                o[q] = hd_expand(f, K, T.MV + ww, W) | T.V[ww];
+                if (kRegTab) {  // this lane's words are the same in every chunk
+                  const uint32_t K = rK[j + q];
+                  const uint32_t k = __popc(K);
+                  const uint32_t f = k ? get_bits(gbuf, off + rP[j + q], k) : 0u;
+                  o[q] = hd_expand(f, K, rMV[j + q], 1) | rV[j + q];
+                } else {
+                  const uint32_t K = T.K[ww];
+                  const uint32_t k = __popc(K);
+                  const uint32_t f = k ? get_bits(gbuf, off + T.P[ww], k) : 0u;
+                  o[q] = hd_expand(f, K, T.MV + ww, W) | T.V[ww];
+                }
               } else {
                 o[q] = get_bits(gbuf, off + 32ull * ww, 32);
               }

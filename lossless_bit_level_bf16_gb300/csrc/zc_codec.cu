@@ -20,15 +20,14 @@
 // slots per thread loaded and stored as two 16-byte vectors.  A pair of
 // threads forms one 32-bit word of each bit plane.
 //
-// Encode: persistent blocks take tiles from a ticket counter; per tile they
-// write the slots, count escapes (block scan), obtain the tile's global escape
-// offset with a decoupled look-back over tiles and write the escape bytes
-// compacted.  The last block to finish writes the header, the segment table
+// Encode: persistent blocks take 16384-slot tiles from a ticket counter; in a
+// tile each warp classifies its slices, writes slots and planes and stages its
+// escape bytes; one decoupled look-back per tile gives the tile's escape
+// offset and the staged bytes are copied out compacted.  The last block to finish writes the header, the segment table
 // and the padding.  Bytes per element: 2 read, 11/8 + escapes written.
 //
-// Decode: blocks own decode units (a chunk, or a 4096-slot tile of small
-// chunks); per unit the escape offsets come from the stream's table, so blocks
-// are independent.  Every offset read from the stream is checked before it is
+// Decode: every warp decodes whole chunks on its own (512 slots per step);
+// the escape offsets come from the stream's table, so warps are independent.  Every offset read from the stream is checked before it is
 // used as an address; a bad stream sets ZC_ERR_FORMAT and is not written past.
 #include <cuda_runtime.h>
 
@@ -83,6 +82,8 @@ __device__ __forceinline__ uint32_t sm4(uint32_t w0, uint32_t w1) {
 constexpr int kSub = 4;                             // 4096-slot sub-tiles per ticket
 constexpr uint32_t kEncTile = kSub * kTileLanes;    // slots per ticket
 constexpr int kMaxTileChunks = kEncTile / 1024;     // chunks per ticket at C = 1024
+constexpr int kEncWarps = kThreads / 32;
+constexpr uint32_t kWarpStage = kEncTile / kEncWarps;  // escape bytes a warp can stage per ticket
 
 __device__ __forceinline__ void load16(const uint16_t* x, unsigned long long elem, int valid,
                                        bool vec, uint32_t w[8]) {
@@ -100,44 +101,42 @@ __device__ __forceinline__ void load16(const uint16_t* x, unsigned long long ele
   }
 }
 
-// One ticket = kSub sub-tiles of 4096 slots.  Per sub-tile: classify, write
-// the slot bytes and plane words, stage the escape bytes (compacted) in shared
-// memory.  Per ticket: one look-back for the escape offset, one copy of the
-// staged escapes.  The next sub-tile's loads are issued before the current
-// one is classified, and the next ticket is fetched one tile ahead.
-__global__ void __launch_bounds__(kThreads) zc_encode_kernel(EncArgs A) {
-  __shared__ uint32_t s_lut[4][256];
-  __shared__ __align__(16) uint8_t s_esc[kEncTile];
-  __shared__ uint32_t s_wtot[kThreads / 32];
-  __shared__ unsigned long long s_tile, s_next, s_excl;
+// One ticket = 16384 slots.  Inside a ticket every warp works on its own
+// 512-slot slice of each 4096-slot sub-tile (no block barrier): classify,
+// write the slot bytes and plane words, stage its escape bytes (warp scan) in
+// its own shared-memory window.  Then one warp scans the 32 per-(sub-tile,
+// warp) counts, runs the decoupled look-back for the ticket, and every warp
+// copies its staged escapes to their place in the stream.
+__global__ void __launch_bounds__(kThreads, 4) zc_encode_kernel(EncArgs A) {
+  __shared__ uint32_t s_lut[kMaxTileChunks][256];
+  __shared__ __align__(16) uint8_t s_esc[kEncWarps][kWarpStage];
+  __shared__ uint32_t s_cnt[kSub * kEncWarps];      // escapes per (sub-tile, warp)
+  __shared__ uint32_t s_off[kSub * kEncWarps];      // their exclusive prefix in the ticket
+  __shared__ unsigned long long s_tk[2], s_excl;
   __shared__ unsigned long long s_elem0[kMaxTileChunks];
   __shared__ uint32_t s_valid[kMaxTileChunks];
-  __shared__ int s_al[kMaxTileChunks], s_seg[kMaxTileChunks];
-  __shared__ uint32_t s_cpref[kMaxTileChunks];
-  __shared__ int s_lut_seg[4];
+  __shared__ int s_al[kMaxTileChunks], s_seg[kMaxTileChunks], s_lut_seg[kMaxTileChunks];
+  __shared__ uint32_t s_cs_seg[kMaxTileChunks], s_cs_pos[kMaxTileChunks];  // chunk starts
   __shared__ int s_last;
 
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const ZcLayout& L = A.L;
   const uint32_t C = L.C, log2C = L.log2C;
   const unsigned long long S = L.slot_bytes;
   const unsigned long long lanes_total = L.nchunks << log2C;
   const unsigned long long ntiles = (lanes_total + kEncTile - 1) / kEncTile;
   const uint32_t nct = C >= kEncTile ? 1u : kEncTile / C;   // chunks per ticket
-  const uint32_t cps = C >= kTileLanes ? 1u : kTileLanes / C;  // chunks per sub-tile
   int my_seg = -1;  // segment cache of threads < nct
   unsigned long long my_c0 = 0, my_c1 = 0;
-  if (t < 4) s_lut_seg[t] = -1;
-  if (t == 0) s_next = atomicAdd(&A.ctrl->ticket, 1ull);
+  if (t < kMaxTileChunks) s_lut_seg[t] = -1;
 
-  for (;;) {
+  // A ticket is taken only when the block starts the tile: every tile before
+  // it is then already being worked on, so look-backs never wait on a tile
+  // that a busy block merely reserved.
+  for (int it = 0;; ++it) {
+    if (t == 0) s_tk[it & 1] = atomicAdd(&A.ctrl->ticket, 1ull);
     __syncthreads();
-    if (t == 0) {
-      s_tile = s_next;
-      if (s_next < ntiles) s_next = atomicAdd(&A.ctrl->ticket, 1ull);
-    }
-    __syncthreads();
-    const unsigned long long tile = s_tile;
+    const unsigned long long tile = s_tk[it & 1];
     if (tile >= ntiles) break;
     const unsigned long long tlane0 = tile * kEncTile;
     const unsigned long long cfirst = tlane0 >> log2C;
@@ -164,47 +163,55 @@ __global__ void __launch_bounds__(kThreads) zc_encode_kernel(EncArgs A) {
       }
     }
     __syncthreads();
+    bool rebuilt = false;
+    for (uint32_t k = 0; k < nct; ++k) {
+      const int sg = s_seg[k];
+      if (sg >= 0 && s_lut_seg[k] != sg) {
+        s_lut[k][t] = lut_entry(A.segs[sg].book, (uint32_t)t);
+        rebuilt = true;
+      }
+    }
+    if (rebuilt) {  // uniform: every thread saw the same s_seg / s_lut_seg
+      __syncthreads();
+      if (t < (int)nct && s_seg[t] >= 0) s_lut_seg[t] = s_seg[t];
+    }
 
-    const uint32_t lt = (uint32_t)t * 16u;
-    // slots of this thread in sub-tile `sub`
-    auto where = [&](int sub, int& lct, uint32_t& i0, int& valid, unsigned long long& elem) {
-      const uint32_t lit = (uint32_t)sub * kTileLanes + lt;  // slot index within the ticket
-      lct = C >= kEncTile ? 0 : (int)(lit >> log2C);
-      i0 = (uint32_t)((tlane0 + lit) & (C - 1));
-      const uint32_t vch = s_valid[lct];
-      valid = vch > i0 ? ((vch - i0) < 16u ? (int)(vch - i0) : 16) : 0;
-      elem = s_elem0[lct] + i0;
-    };
-    int lct;
-    uint32_t i0;
-    int valid;
-    unsigned long long elem;
+    // ---- sub-tiles: warp-level work only
+    uint8_t* wst = s_esc[warp];
+    uint32_t wrun = 0;  // escapes this warp staged in this ticket
+    uint32_t lit = (uint32_t)warp * 512u + 16u * lane;  // slot within the ticket
+    int lct = C >= kEncTile ? 0 : (int)(lit >> log2C);
+    uint32_t i0 = (uint32_t)((tlane0 + lit) & (C - 1));
+    uint32_t vch = s_valid[lct];
+    int valid = vch > i0 ? ((vch - i0) < 16u ? (int)(vch - i0) : 16) : 0;
     uint32_t w[8], wn[8];
-    where(0, lct, i0, valid, elem);
-    load16(A.x, elem, valid, s_al[lct], w);
-    uint32_t running = 0;
+    load16(A.x, s_elem0[lct] + i0, valid, s_al[lct], w);
     for (int sub = 0; sub < kSub; ++sub) {
-      if (tlane0 + (unsigned long long)sub * kTileLanes >= lanes_total) break;  // uniform
+      if (tlane0 + (unsigned long long)sub * kTileLanes >= lanes_total) {  // uniform
+        if (lane == 0) s_cnt[sub * kEncWarps + warp] = 0;
+        continue;
+      }
+      // next sub-tile's loads first
+      // (positions past the last chunk read as chunk-local slots of a
+      // chunk >= nchunks: valid 0, not live)
+      const uint32_t lit_n = lit + kTileLanes;
       int lct_n = 0, valid_n = 0;
       uint32_t i0_n = 0;
-      unsigned long long elem_n = 0;
-      const bool more = sub + 1 < kSub && tlane0 + (unsigned long long)(sub + 1) * kTileLanes < lanes_total;
-      if (more) {
-        where(sub + 1, lct_n, i0_n, valid_n, elem_n);
-        load16(A.x, elem_n, valid_n, s_al[lct_n], wn);
+      if (sub + 1 < kSub) {
+        lct_n = C >= kEncTile ? 0 : (int)(lit_n >> log2C);
+        i0_n = (uint32_t)((tlane0 + lit_n) & (C - 1));
+        const uint32_t vn = s_valid[lct_n];
+        valid_n = vn > i0_n ? ((vn - i0_n) < 16u ? (int)(vn - i0_n) : 16) : 0;
+        if (valid_n) {
+          load16(A.x, s_elem0[lct_n] + i0_n, valid_n, s_al[lct_n], wn);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) wn[j] = 0;  // padding slots: byte 0
+        }
       }
-      // lookup tables of this sub-tile's chunks (slot k = chunk within the sub-tile)
-      const uint32_t cbase = ((uint32_t)sub * kTileLanes) >> log2C;
-      for (uint32_t k = 0; k < cps; ++k) {
-        const int sg = s_seg[cbase + k];
-        if (sg >= 0 && s_lut_seg[k] != sg) s_lut[k][t] = lut_entry(A.segs[sg].book, (uint32_t)t);
-      }
-      __syncthreads();
-      if (t < (int)cps && s_seg[cbase + t] >= 0) s_lut_seg[t] = s_seg[cbase + t];
-
       const unsigned long long c = cfirst + lct;
       const bool live = c < L.nchunks;
-      const uint32_t* Lt = s_lut[C >= kTileLanes ? 0 : (lt >> log2C)];
+      const uint32_t* Lt = s_lut[lct];
       uint32_t accA = 0, accB = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -235,7 +242,7 @@ __global__ void __launch_bounds__(kThreads) zc_encode_kernel(EncArgs A) {
       if (live) {
         uint32_t* pw = reinterpret_cast<uint32_t*>(slot + C) + (i0 >> 5);
         const uint32_t pwords = C >> 5;
-        if ((t & 1) == 0) {
+        if ((lane & 1) == 0) {
           pw[0] = prmt(T0, U0, 0x5410);
           pw[pwords] = prmt(T0, U0, 0x7632);
         } else {
@@ -243,56 +250,85 @@ __global__ void __launch_bounds__(kThreads) zc_encode_kernel(EncArgs A) {
         }
       }
       const uint32_t esc = T1 >> 16;
-      uint32_t total;
-      const uint32_t excl = block_excl_scan<kThreads>((uint32_t)__popc(esc), s_wtot, &total);
-      const uint32_t pos0 = running + excl;
-      if (live && i0 == 0) s_cpref[lct] = pos0;
+      const uint32_t ne = (uint32_t)__popc(esc);
+      uint32_t inc = ne;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += v;
+      }
+      const uint32_t excl = inc - ne;
+      if (live && i0 == 0) {  // a chunk starts at this thread's first slot
+        s_cs_seg[lct] = (uint32_t)(sub * kEncWarps + warp);
+        s_cs_pos[lct] = excl;
+      }
       if (esc) {
         uint32_t F[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) F[q] = prmt(w[2 * q] >> 7, w[2 * q + 1] >> 7, 0x6420);
-        uint32_t m = esc, pos = pos0;
+        uint32_t m = esc, pos = wrun + excl;
         while (m) {
           const int i = __ffs(m) - 1;
           m &= m - 1;
           const uint32_t f = i < 8 ? (i < 4 ? F[0] : F[1]) : (i < 12 ? F[2] : F[3]);
-          s_esc[pos++] = (uint8_t)((f >> ((i & 3) * 8)) & 0xFFu);
+          wst[pos++] = (uint8_t)((f >> ((i & 3) * 8)) & 0xFFu);
         }
       }
-      running += total;
-      __syncthreads();  // s_wtot, s_lut reuse
+      const uint32_t wtot = __shfl_sync(kFull, inc, 31);
+      if (lane == 0) s_cnt[sub * kEncWarps + warp] = wtot;
+      wrun += wtot;
 #pragma unroll
       for (int j = 0; j < 8; ++j) w[j] = wn[j];
+      lit = lit_n;
       lct = lct_n;
       i0 = i0_n;
       valid = valid_n;
-      elem = elem_n;
     }
+    __syncthreads();
 
-    // ---- one look-back per ticket, then the staged escapes go out
-    if (t < 32) {
+    // ---- one warp: prefix of the 32 staged counts, look-back for the ticket
+    if (warp == 0) {
+      const uint32_t cnt = s_cnt[lane];  // order: sub-tile major, warp minor = slot order
+      uint32_t inc = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += v;
+      }
+      s_off[lane] = inc - cnt;
+      const uint32_t agg = __shfl_sync(kFull, inc, 31);
       bool to = false;
-      const unsigned long long e = lookback_warp(A.states, tile, running, &to);
-      if (t == 0) {
+      const unsigned long long e = lookback_warp_wide(A.states, tile, agg, &to);
+      if (lane == 0) {
         s_excl = e;
         if (to) set_status(A.ctrl, ZC_ERR_TIMEOUT);
       }
     }
     __syncthreads();
-    const unsigned long long base = s_excl;
-    const unsigned long long dst = L.off_esc + base;
-    if (dst + running <= A.out_cap) {
-      for (uint32_t i = t; i < running; i += kThreads) A.out[dst + i] = s_esc[i];
-    } else if (t == 0) {
-      set_status(A.ctrl, ZC_ERR_CAPACITY);
+    const unsigned long long base = L.off_esc + s_excl;
+    {
+      uint32_t src = 0;
+      for (int sub = 0; sub < kSub; ++sub) {
+        const uint32_t k = (uint32_t)(sub * kEncWarps + warp);
+        const uint32_t n = s_cnt[k];
+        const unsigned long long dst = base + s_off[k];
+        if (dst + n <= A.out_cap) {
+          for (uint32_t i = lane; i < n; i += 32) A.out[dst + i] = wst[src + i];
+        } else if (lane == 0) {
+          set_status(A.ctrl, ZC_ERR_CAPACITY);
+        }
+        src += n;
+      }
     }
     // escape offsets of the chunks that start in this ticket
     if (t < (int)nct) {
       const unsigned long long c = cfirst + t;
       const bool starts = C >= kEncTile ? ((tlane0 & (C - 1)) == 0) : true;
       if (c < L.nchunks && starts)
-        reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = base + s_cpref[t];
+        reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] =
+            s_excl + s_off[s_cs_seg[t]] + s_cs_pos[t];
     }
+    __syncthreads();  // s_excl, s_off, s_cnt and the windows are reused by the next ticket
   }
 
   // ---- the last block to finish writes the header, tables and padding
@@ -443,99 +479,47 @@ __device__ __forceinline__ uint32_t out_word(uint32_t S, uint32_t E, uint32_t se
   return (T & 0x007F007Fu) | ((T >> 1) & 0x7F807F80u) | ((T << 8) & 0x80008000u);
 }
 
-// Table entries of one chunk, copied to shared memory one unit ahead of use
-// (cp.async): the segment record picked by interpolation (segments of equal
-// size need no search), the end of the record before it, and the chunk's two
-// escape offsets.
-constexpr int kAheadWords = 11;
-enum { AH_ESTART, AH_NELEM, AH_CSTART, AH_NCHK, AH_BOOK, AH_PE0, AH_PE1, AH_PC0, AH_PC1, AH_ELO, AH_EHI };
+constexpr uint32_t kWarpEscBytes = 512;  // escape bytes a warp stages per chunk
+constexpr int kDecWarps = kThreads / 32;
 
-__device__ __forceinline__ uint32_t interp_segment(const DecHdr& h, unsigned long long c) {
+// Segment record of chunk c, found by interpolation (segments of equal size
+// need no search) and checked against the header and the record before it.
+__device__ bool find_seg_checked(const uint8_t* in, const DecHdr& h, unsigned long long c,
+                                 SegRec& r) {
   uint32_t g = (uint32_t)(((double)c * (double)h.nseg) / (double)h.nchunks);
-  return g >= h.nseg ? h.nseg - 1 : g;
-}
-
-// Threads 0 .. kAheadWords*cpu-1 each start one 8-byte copy.
-__device__ __forceinline__ void ahead_issue(const uint8_t* in, const DecHdr& h,
-                                            unsigned long long c0, uint32_t cpu,
-                                            unsigned long long (*dst)[kAheadWords]) {
-  const int t = threadIdx.x;
-  if (t >= kAheadWords * (int)cpu) return;
-  const int k = t / kAheadWords, f = t % kAheadWords;
-  const unsigned long long c = c0 + k;
-  if (c >= h.nchunks) return;
-  const uint32_t g = interp_segment(h, c);
-  const uint8_t* rec = in + h.off_seg + (unsigned long long)kZcSegRec * g;
-  const uint8_t* src = nullptr;
-  switch (f) {
-    case AH_ESTART: src = rec; break;
-    case AH_NELEM: src = rec + 8; break;
-    case AH_CSTART: src = rec + 16; break;
-    case AH_NCHK: src = rec + 24; break;
-    case AH_BOOK: src = rec + 48; break;
-    case AH_PE0: src = g ? rec - kZcSegRec : nullptr; break;
-    case AH_PE1: src = g ? rec - kZcSegRec + 8 : nullptr; break;
-    case AH_PC0: src = g ? rec - kZcSegRec + 16 : nullptr; break;
-    case AH_PC1: src = g ? rec - kZcSegRec + 24 : nullptr; break;
-    case AH_ELO: src = in + h.off_escoff + 8 * c; break;
-    default: src = in + h.off_escoff + 8 * (c + 1); break;
-  }
-  if (src) cp_async8(&dst[k][f], src);
-}
-
-// Resolve chunk c from its read-ahead words: if the interpolated segment does
-// not hold the chunk, search the table.  False if the tables are inconsistent.
-__device__ bool ahead_resolve(const uint8_t* in, const DecHdr& h, unsigned long long c,
-                              const unsigned long long* a, SegRec& r) {
-  const uint32_t g = interp_segment(h, c);
-  if (!(c >= a[AH_CSTART] && c - a[AH_CSTART] < a[AH_NCHK])) {
+  if (g >= h.nseg) g = h.nseg - 1;
+  const unsigned long long cs = rd_u64(in + h.off_seg + (unsigned long long)kZcSegRec * g + 16);
+  const unsigned long long cn = rd_u64(in + h.off_seg + (unsigned long long)kZcSegRec * g + 24);
+  if (!(c >= cs && c - cs < cn)) {
     int lo = 0, hi = (int)h.nseg - 1;  // largest s with chunk_start <= c
     while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
+      const int mid = (lo + hi + 1) >> 1;
       if (rd_u64(in + h.off_seg + (unsigned long long)kZcSegRec * mid + 16) <= c) lo = mid;
       else hi = mid - 1;
     }
-    if (!load_seg(in, h, (uint32_t)lo, r)) return false;
-  } else {
-    r.elem_start = a[AH_ESTART];
-    r.nelem = a[AH_NELEM];
-    r.chunk_start = a[AH_CSTART];
-    r.nchunks = a[AH_NCHK];
-    r.R0 = (uint32_t)(a[AH_BOOK] << 8);
-    r.R1 = (uint32_t)(a[AH_BOOK] >> 24);
-    if (r.nelem > h.n || r.elem_start > h.n - r.nelem) return false;
-    if (r.nchunks > h.nchunks || r.chunk_start > h.nchunks - r.nchunks) return false;
-    if (r.nchunks != ((r.nelem + h.C - 1) >> h.log2C)) return false;
-    if (g == 0 ? (r.elem_start != 0 || r.chunk_start != 0)
-               : (a[AH_PE0] + a[AH_PE1] != r.elem_start || a[AH_PC0] + a[AH_PC1] != r.chunk_start))
-      return false;
+    g = (uint32_t)lo;
   }
-  return c >= r.chunk_start && c < r.chunk_start + r.nchunks && a[AH_ELO] <= a[AH_EHI] &&
-         a[AH_EHI] <= h.esc_total;
+  if (!load_seg(in, h, g, r)) return false;
+  return c >= r.chunk_start && c < r.chunk_start + r.nchunks;
 }
 
-constexpr uint32_t kEscStageBytes = 8192;  // escape bytes staged per decode unit
-
-__global__ void __launch_bounds__(kThreads) zc_decode_kernel(
+// Each warp decodes whole chunks on its own, 512 slots (16 per lane) per
+// step, carrying the chunk's escape count from step to step; no block
+// barrier after the header is read.  The chunk's escape bytes are staged in
+// the warp's shared-memory window when they fit (one 16-byte load per lane).
+__global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
     const uint8_t* __restrict__ in, unsigned long long in_bytes, uint16_t* __restrict__ y,
     unsigned long long y_cap, Ctrl* ctrl, int y_al16) {
   __shared__ uint32_t s_nib[256];
-  __shared__ __align__(16) uint32_t s_escw[kEscStageBytes / 4 + 2];
+  __shared__ __align__(16) uint8_t s_esc[kDecWarps][kWarpEscBytes + 16];
   __shared__ DecHdr s_h;
   __shared__ int s_ok;
-  __shared__ uint32_t s_wtot[kThreads / 32];
-  __shared__ uint32_t s_excl[kThreads];
-  __shared__ unsigned long long s_elem0[4], s_elo[4], s_ehi[4];
-  __shared__ uint32_t s_valid[4], s_R0[4], s_R1[4];
-  __shared__ int s_al[4], s_bad;
-  __shared__ unsigned long long s_ahead[2][4][kAheadWords];
 
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   if (t == 0) {
     int err;
     s_ok = parse_header(in, in_bytes, y_cap, s_h, err);
     if (!s_ok) set_status(ctrl, err);
-    s_bad = 0;
   }
   {
     uint32_t v = 0;
@@ -546,9 +530,10 @@ __global__ void __launch_bounds__(kThreads) zc_decode_kernel(
   __syncthreads();
   if (!s_ok) return;
   const DecHdr h = s_h;
-  const uint32_t C = h.C, log2C = h.log2C;
+  const uint32_t C = h.C;
   const unsigned long long S = (unsigned long long)C * 11ull / 8ull;
   const uint8_t* escoff = in + h.off_escoff;
+  const uint8_t* esc_base = in + h.off_esc;
 
   // whole-table checks, once (block 0): segment chain and offset-table ends
   if (blockIdx.x == 0) {
@@ -562,118 +547,70 @@ __global__ void __launch_bounds__(kThreads) zc_decode_kernel(
       set_status(ctrl, ZC_ERR_FORMAT);
   }
 
-  const uint32_t cpu = C >= kTileLanes ? 1u : kTileLanes / C;          // chunks per unit
-  const uint32_t steps = C >= kTileLanes ? C / kTileLanes : 1u;          // tiles per unit
-  const unsigned long long nunits = C >= kTileLanes ? h.nchunks : (h.nchunks + cpu - 1) / cpu;
-  const uint8_t* esc_base = in + h.off_esc;
-
-  ahead_issue(in, h, (unsigned long long)blockIdx.x * cpu, cpu, s_ahead[0]);
-  cp_async_commit();
-
-  int buf = 0;
-  for (unsigned long long u = blockIdx.x; u < nunits; u += gridDim.x, buf ^= 1) {
-    const unsigned long long c0 = u * cpu;
-    cp_async_wait_all();
-    __syncthreads();
-    if (t < (int)cpu) {
-      const unsigned long long c = c0 + t;
-      s_valid[t] = 0;
-      s_elem0[t] = 0;
-      s_elo[t] = s_ehi[t] = 0;
-      s_R0[t] = s_R1[t] = 0;
-      s_al[t] = 0;
-      if (c < h.nchunks) {
-        SegRec r;
-        const unsigned long long* a = s_ahead[buf][t];
-        if (!ahead_resolve(in, h, c, a, r)) {
-          s_bad = 1;
-        } else {
-          const unsigned long long e0 = r.elem_start + ((c - r.chunk_start) << log2C);
-          const unsigned long long end = r.elem_start + r.nelem;
-          s_elem0[t] = e0;
-          s_valid[t] = (uint32_t)((end - e0) < C ? (end - e0) : C);
-          s_elo[t] = a[AH_ELO];
-          s_ehi[t] = a[AH_EHI];
-          s_R0[t] = r.R0;
-          s_R1[t] = r.R1;
-          s_al[t] = y_al16 && ((r.elem_start & 7ull) == 0);
-        }
+  const unsigned long long nwarps = (unsigned long long)gridDim.x * kDecWarps;
+  const uint32_t steps = C / 512u;
+  uint8_t* wesc = s_esc[warp];
+  for (unsigned long long c = (unsigned long long)blockIdx.x * kDecWarps + warp; c < h.nchunks;
+       c += nwarps) {
+    const uint8_t* slot = in + h.off_static + c * S;
+    // step 0 data and the chunk's table entries in flight together
+    uint4 smv = ld_nc_v4(slot + 16u * lane);
+    const uint8_t* pb = slot + C + 2u * lane;
+    uint32_t p0 = __ldg(reinterpret_cast<const unsigned short*>(pb));
+    uint32_t p1 = __ldg(reinterpret_cast<const unsigned short*>(pb + (C >> 3)));
+    uint32_t p2 = __ldg(reinterpret_cast<const unsigned short*>(pb + (C >> 2)));
+    const unsigned long long elo = rd_u64(escoff + 8 * c), ehi = rd_u64(escoff + 8 * (c + 1));
+    SegRec r;
+    bool ok = find_seg_checked(in, h, c, r) && elo <= ehi && ehi <= h.esc_total;
+    if (!ok) {
+      if (lane == 0) set_status(ctrl, ZC_ERR_FORMAT);
+      continue;  // warp-uniform
+    }
+    const unsigned long long e0 = r.elem_start + ((c - r.chunk_start) << h.log2C);
+    const unsigned long long vch_ll = r.elem_start + r.nelem - e0;
+    const uint32_t vch = (uint32_t)(vch_ll < C ? vch_ll : C);
+    const bool al = y_al16 && ((r.elem_start & 7ull) == 0);
+    const unsigned long long ea = elo & ~15ull;  // staged window starts 16-byte aligned
+    const bool staged = ehi - ea <= kWarpEscBytes;
+    if (staged && ea + 16ull * lane < ehi)
+      *reinterpret_cast<uint4*>(wesc + 16 * lane) = ld_nc_v4(esc_base + ea + 16ull * lane);
+    __syncwarp();
+    unsigned long long carry = elo;
+    for (uint32_t st = 0; st < steps; ++st) {
+      const uint32_t i0 = st * 512u + 16u * lane;
+      // next step's loads go out before this step is decoded
+      uint4 smn = make_uint4(0, 0, 0, 0);
+      uint32_t q0 = 0, q1 = 0, q2 = 0;
+      if (st + 1 < steps) {
+        smn = ld_nc_v4(slot + i0 + 512u);
+        const uint8_t* qb = slot + C + ((i0 + 512u) >> 3);
+        q0 = __ldg(reinterpret_cast<const unsigned short*>(qb));
+        q1 = __ldg(reinterpret_cast<const unsigned short*>(qb + (C >> 3)));
+        q2 = __ldg(reinterpret_cast<const unsigned short*>(qb + (C >> 2)));
       }
-    }
-    // the next unit's table entries are copied now and used one unit later
-    ahead_issue(in, h, (u + gridDim.x) * cpu, cpu, s_ahead[buf ^ 1]);
-    cp_async_commit();
-    __syncthreads();
-    const bool bad_tables = s_bad != 0;
-    // escape bytes of the whole unit are contiguous: [e_lo, e_hi)
-    uint32_t last = 0;
-    for (uint32_t k = 1; k < cpu; ++k)
-      if (c0 + k < h.nchunks) last = k;
-    const unsigned long long e_lo = s_elo[0], e_hi = s_ehi[last];
-    const bool staged = !bad_tables && e_hi >= e_lo && e_hi - e_lo <= kEscStageBytes;
-    const unsigned long long ew0 = e_lo >> 2;  // first escape word
-    if (staged) {
-      const uint32_t nw = (uint32_t)(((e_hi + 3) >> 2) - ew0);
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(esc_base) + ew0;
-      for (uint32_t i = t; i < nw; i += kThreads) cp_async4(&s_escw[i], src + i);
-    }
-    cp_async_commit();
-    const uint8_t* s_escb = reinterpret_cast<const uint8_t*>(s_escw);
-    unsigned long long carry = 0;  // escapes in earlier tiles of this chunk
-    for (uint32_t st = 0; st < (bad_tables ? 0u : steps); ++st) {
-      const uint32_t lt = (uint32_t)t * 16u;
-      const int lc = C >= kTileLanes ? 0 : (int)(lt >> log2C);
-      const uint32_t i0 = C >= kTileLanes ? st * kTileLanes + lt : (lt & (C - 1));
-      const unsigned long long c = c0 + lc;
-      const bool live = c < h.nchunks;
-      const uint32_t vch = live ? s_valid[lc] : 0u;
       const int valid = vch > i0 ? ((vch - i0) < 16u ? (int)(vch - i0) : 16) : 0;
-      uint4 smv = make_uint4(0, 0, 0, 0);
-      uint32_t p0 = 0, p1 = 0, p2 = 0;
-      const uint8_t* slot = in + h.off_static + c * S;
-      if (live) {
-        smv = ld_nc_v4(slot + i0);
-        const uint8_t* pb = slot + C + (i0 >> 3);
-        p0 = __ldg(reinterpret_cast<const unsigned short*>(pb));
-        p1 = __ldg(reinterpret_cast<const unsigned short*>(pb + (C >> 3)));
-        p2 = __ldg(reinterpret_cast<const unsigned short*>(pb + (C >> 2)));
-      }
       const uint32_t vmask = valid >= 16 ? 0xFFFFu : ((1u << valid) - 1u);
       const uint32_t esc = ~(p0 | p1 | p2) & vmask;
-      if (st == 0) cp_async_wait_all();  // staged escapes land before the barrier below
-      uint32_t total;
-      const uint32_t excl = block_excl_scan<kThreads>((uint32_t)__popc(esc), s_wtot, &total);
-      unsigned long long base;
-      if (C >= kTileLanes) {
-        base = s_elo[0] + carry + excl;
-      } else {
-        s_excl[t] = excl;
-        __syncthreads();
-        const uint32_t tfirst = (uint32_t)lc * (C >> 4);  // first thread of this chunk
-        base = s_elo[lc] + excl - s_excl[tfirst];
-        // per-chunk check: escapes counted in the chunk == table difference
-        if (live && lt == (uint32_t)lc * C) {
-          const uint32_t tnext = tfirst + (C >> 4);
-          const uint32_t cnt = (tnext < (uint32_t)kThreads ? s_excl[tnext] : total) - s_excl[tfirst];
-          if (cnt != s_ehi[lc] - s_elo[lc]) s_bad = 1;
-        }
-      }
-      const unsigned long long ehi = s_ehi[lc];
       const uint32_t ne = (uint32_t)__popc(esc);
-      if (base + ne > ehi) s_bad = 1;
-
+      uint32_t inc = ne;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += v;
+      }
+      const unsigned long long base = carry + inc - ne;
+      carry += __shfl_sync(kFull, inc, 31);
       const uint32_t cA = s_nib[p0 & 0xFFu] | (s_nib[p1 & 0xFFu] << 1) | (s_nib[p2 & 0xFFu] << 2);
       const uint32_t cB = s_nib[p0 >> 8] | (s_nib[p1 >> 8] << 1) | (s_nib[p2 >> 8] << 2);
-      const uint32_t R0 = s_R0[lc], R1 = s_R1[lc];
-      uint32_t E0 = prmt(R0, R1, cA), E1 = prmt(R0, R1, cA >> 16);
-      uint32_t E2 = prmt(R0, R1, cB), E3 = prmt(R0, R1, cB >> 16);
+      uint32_t E0 = prmt(r.R0, r.R1, cA), E1 = prmt(r.R0, r.R1, cA >> 16);
+      uint32_t E2 = prmt(r.R0, r.R1, cB), E3 = prmt(r.R0, r.R1, cB >> 16);
       if (esc && base + ne <= ehi) {
         uint32_t m = esc;
         unsigned long long pos = base;
         while (m) {
           const int i = __ffs(m) - 1;
           m &= m - 1;
-          const uint32_t e = staged ? s_escb[pos - (ew0 << 2)] : esc_base[pos];
+          const uint32_t e = staged ? wesc[pos - ea] : esc_base[pos];
           ++pos;
           const uint32_t sh = (uint32_t)(i & 3) * 8u;
           const uint32_t keep = ~(0xFFu << sh), ins = e << sh;
@@ -684,36 +621,36 @@ __global__ void __launch_bounds__(kThreads) zc_decode_kernel(
           else E3 = (E3 & keep) | ins;
         }
       }
-      uint32_t o[8];
-      o[0] = out_word(smv.x, E0, 0x5140);
-      o[1] = out_word(smv.x, E0, 0x7362);
-      o[2] = out_word(smv.y, E1, 0x5140);
-      o[3] = out_word(smv.y, E1, 0x7362);
-      o[4] = out_word(smv.z, E2, 0x5140);
-      o[5] = out_word(smv.z, E2, 0x7362);
-      o[6] = out_word(smv.w, E3, 0x5140);
-      o[7] = out_word(smv.w, E3, 0x7362);
-      const unsigned long long elem = s_elem0[lc] + i0;
-      if (valid == 16 && s_al[lc]) {
-        st_v4(y + elem, make_uint4(o[0], o[1], o[2], o[3]));
-        st_v4(y + elem + 8, make_uint4(o[4], o[5], o[6], o[7]));
-      } else {
+      if (valid) {
+        uint32_t o[8];
+        o[0] = out_word(smv.x, E0, 0x5140);
+        o[1] = out_word(smv.x, E0, 0x7362);
+        o[2] = out_word(smv.y, E1, 0x5140);
+        o[3] = out_word(smv.y, E1, 0x7362);
+        o[4] = out_word(smv.z, E2, 0x5140);
+        o[5] = out_word(smv.z, E2, 0x7362);
+        o[6] = out_word(smv.w, E3, 0x5140);
+        o[7] = out_word(smv.w, E3, 0x7362);
+        const unsigned long long elem = e0 + i0;
+        if (valid == 16 && al) {
+          st_v4(y + elem, make_uint4(o[0], o[1], o[2], o[3]));
+          st_v4(y + elem + 8, make_uint4(o[4], o[5], o[6], o[7]));
+        } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (2 * j < valid) y[elem + 2 * j] = (uint16_t)(o[j] & 0xFFFFu);
-          if (2 * j + 1 < valid) y[elem + 2 * j + 1] = (uint16_t)(o[j] >> 16);
+          for (int j = 0; j < 8; ++j) {
+            if (2 * j < valid) y[elem + 2 * j] = (uint16_t)(o[j] & 0xFFFFu);
+            if (2 * j + 1 < valid) y[elem + 2 * j + 1] = (uint16_t)(o[j] >> 16);
+          }
         }
       }
-      carry += total;
-      if (st + 1 < steps) __syncthreads();  // s_wtot reuse
+      smv = smn;
+      p0 = q0;
+      p1 = q1;
+      p2 = q2;
     }
-    __syncthreads();
-    if (t == 0) {
-      if (!bad_tables && C >= kTileLanes && carry != s_ehi[0] - s_elo[0]) s_bad = 1;
-      if (s_bad) set_status(ctrl, ZC_ERR_FORMAT);
-      s_bad = 0;
-    }
-    __syncthreads();
+    // the escapes counted in the planes must be exactly the table's
+    if (lane == 0 && carry != ehi) set_status(ctrl, ZC_ERR_FORMAT);
+    __syncwarp();  // window reuse
   }
 }
 

@@ -44,6 +44,9 @@ __device__ __forceinline__ void st_release_u64(unsigned long long* p,
                                                unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(
     const unsigned long long* p) {
   unsigned long long v;
@@ -88,6 +91,14 @@ __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
 }
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
@@ -115,61 +126,8 @@ constexpr unsigned long long kFlagInc = 2ull << 62;
 constexpr unsigned long long kValMask = (1ull << 62) - 1;
 constexpr unsigned kMaxSpins = 1u << 22;  // ~1 s with the back-off below
 
-// Called by all 32 lanes of one warp.  Publishes `aggregate` for `tile`,
-// returns the exclusive prefix over tiles 0..tile-1 and publishes the
-// inclusive value.  On a timeout sets *timed_out, publishes an inclusive
-// value of `aggregate` (so successors finish) and returns 0.
-__device__ __forceinline__ unsigned long long lookback_warp(
-    unsigned long long* states, unsigned long long tile,
-    unsigned long long aggregate, bool* timed_out) {
-  const int lane = threadIdx.x & (kWarp - 1);
-  if (tile == 0) {
-    if (lane == 0) st_release_u64(states, kFlagInc | aggregate);
-    return 0;
-  }
-  if (lane == 0) st_release_u64(states + tile, kFlagAgg | aggregate);
-  unsigned long long excl = 0;
-  long long end = (long long)tile - 1;
-  unsigned spins = 0;
-  unsigned ns = 32;
-  bool to = false;
-  while (true) {
-    long long idx = end - lane;
-    unsigned long long s = idx >= 0 ? ld_relaxed_u64(states + idx) : kFlagInc;
-    unsigned flag = (unsigned)(s >> 62);
-    if (__any_sync(kFull, flag == 0)) {
-      if (++spins > kMaxSpins) {
-        to = true;
-        break;
-      }
-      // predecessors publish within a few microseconds: poll tightly first,
-      // back off only for long waits
-      if (spins > 64) {
-        __nanosleep(ns);
-        if (ns < 256) ns <<= 1;
-      }
-      continue;
-    }
-    unsigned inc = __ballot_sync(kFull, flag == 2);
-    unsigned long long v = s & kValMask;
-    if (inc) {
-      int first = __ffs(inc) - 1;  // nearest tile holding an inclusive prefix
-      excl += warp_sum_u64(lane <= first ? v : 0ull);
-      break;
-    }
-    excl += warp_sum_u64(v);
-    end -= kWarp;
-  }
-  if (to) {
-    *timed_out = true;
-    if (lane == 0) st_release_u64(states + tile, kFlagInc | aggregate);
-    return 0;
-  }
-  if (lane == 0) st_release_u64(states + tile, kFlagInc | ((excl + aggregate) & kValMask));
-  return excl;
-}
-
-// Look-back with an adaptive window: the nearest 32 predecessors are read
+// Look-back with an adaptive window (states are published with relaxed
+// stores: they carry counts only, nothing else is read through them): the nearest 32 predecessors are read
 // first (one state per lane; usually one of them already holds an inclusive
 // prefix); if all 32 hold only aggregates the walk continues kLbDepth*32
 // states per L2 round trip.  Spinning on a predecessor that has not published
@@ -218,10 +176,10 @@ __device__ __forceinline__ unsigned long long lookback_warp_wide(
     bool* timed_out) {
   const int lane = threadIdx.x & (kWarp - 1);
   if (tile == 0) {
-    if (lane == 0) st_release_u64(states, kFlagInc | aggregate);
+    if (lane == 0) st_relaxed_u64(states, kFlagInc | aggregate);
     return 0;
   }
-  if (lane == 0) st_release_u64(states + tile, kFlagAgg | aggregate);
+  if (lane == 0) st_relaxed_u64(states + tile, kFlagAgg | aggregate);
   unsigned long long excl = 0;
   long long end = (long long)tile - 1;
   unsigned spins = 0, ns = 32;
@@ -247,10 +205,10 @@ __device__ __forceinline__ unsigned long long lookback_warp_wide(
   }
   if (to) {
     *timed_out = true;
-    if (lane == 0) st_release_u64(states + tile, kFlagInc | aggregate);
+    if (lane == 0) st_relaxed_u64(states + tile, kFlagInc | aggregate);
     return 0;
   }
-  if (lane == 0) st_release_u64(states + tile, kFlagInc | ((excl + aggregate) & kValMask));
+  if (lane == 0) st_relaxed_u64(states + tile, kFlagInc | ((excl + aggregate) & kValMask));
   return excl;
 }
 

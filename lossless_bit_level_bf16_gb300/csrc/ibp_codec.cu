@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_encode_kernel(IbpEncArgs 
     if (c0 + nch == A.nchunks && tail_bytes != cb) bits -= 8ull * (cb - tail_bytes);
     const unsigned long long padded = round_up_dev(bits, 128);
     // publish the aggregate now; the look-back below resolves it later
-    if (t == 0 && g > 0) st_release_u64(A.states + g, kFlagAgg | padded);
+    if (t == 0 && g > 0) st_relaxed_u64(A.states + g, kFlagAgg | padded);
     if (t == 0) gbuf[0] = pword;  // the image is all zeros here (cleared at copy-out)
 
     // ---- phase 2: close up kept bits into the group image

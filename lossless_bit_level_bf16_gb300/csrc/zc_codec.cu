@@ -79,69 +79,60 @@ __device__ __forceinline__ uint32_t sm4(uint32_t w0, uint32_t w1) {
   return (prmt(w0, w1, 0x7531) & 0x80808080u) | (prmt(w0, w1, 0x6420) & 0x7F7F7F7Fu);
 }
 
-constexpr int kSub = 4;                             // 4096-slot sub-tiles per ticket
-constexpr uint32_t kEncTile = kSub * kTileLanes;    // slots per ticket
-constexpr int kMaxTileChunks = kEncTile / 1024;     // chunks per ticket at C = 1024
+constexpr uint32_t kWTile = 4096;                   // slots per warp ticket
 constexpr int kEncWarps = kThreads / 32;
-constexpr uint32_t kWarpStage = kEncTile / kEncWarps;  // escape bytes a warp can stage per ticket
+constexpr int kMaxLutSlots = kWTile / 1024;          // chunks per ticket at C = 1024
+constexpr uint32_t kStages = 3, kAhead = 2;          // input ring: 2 KB steps, copied 2 ahead
+constexpr uint32_t kEscCap = 512;                    // escape bytes a warp stages per ticket
 
-__device__ __forceinline__ void load16(const uint16_t* x, unsigned long long elem, int valid,
-                                       bool vec, uint32_t w[8]) {
-  if (valid == 16 && vec) {
-    const uint4 a = ld_nc_v4(x + elem), b = ld_nc_v4(x + elem + 8);
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t l = (2 * j < valid) ? (uint32_t)__ldg(x + elem + 2 * j) : 0u;
-      const uint32_t h = (2 * j + 1 < valid) ? (uint32_t)__ldg(x + elem + 2 * j + 1) : 0u;
-      w[j] = l | (h << 16);
-    }
-  }
-}
-
-// One ticket = 16384 slots.  Inside a ticket every warp works on its own
-// 512-slot slice of each 4096-slot sub-tile (no block barrier): classify,
-// write the slot bytes and plane words, stage its escape bytes (warp scan) in
-// its own shared-memory window.  Then one warp scans the 32 per-(sub-tile,
-// warp) counts, runs the decoupled look-back for the ticket, and every warp
-// copies its staged escapes to their place in the stream.
-__global__ void __launch_bounds__(kThreads, 4) zc_encode_kernel(EncArgs A) {
-  __shared__ uint32_t s_lut[kMaxTileChunks][256];
-  __shared__ __align__(16) uint8_t s_esc[kEncWarps][kWarpStage];
-  __shared__ uint32_t s_cnt[kSub * kEncWarps];      // escapes per (sub-tile, warp)
-  __shared__ uint32_t s_off[kSub * kEncWarps];      // their exclusive prefix in the ticket
-  __shared__ unsigned long long s_tk[2], s_excl;
-  __shared__ unsigned long long s_elem0[kMaxTileChunks];
-  __shared__ uint32_t s_valid[kMaxTileChunks];
-  __shared__ int s_al[kMaxTileChunks], s_seg[kMaxTileChunks], s_lut_seg[kMaxTileChunks];
-  __shared__ uint32_t s_cs_seg[kMaxTileChunks], s_cs_pos[kMaxTileChunks];  // chunk starts
-  __shared__ int s_last;
-
+// Warp-level encoder.  A ticket is 4096 slots and belongs to one warp: it
+// classifies them 1024 at a time (32 per lane), writes the slot bytes and plane
+// words, stages its escape bytes in its own shared-memory window, then runs
+// the decoupled look-back for its ticket and copies the escapes to their place.
+// Warps never wait for each other inside a block, so one warp's look-back is
+// covered by the other warps' loads.
+// Dynamic shared memory per warp: the input ring (kStages x 2 KB), one
+// 256-word lookup table per chunk of a ticket, kEscCap staged escape bytes.
+__global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  __shared__ int s_lseg[kEncWarps][kMaxLutSlots];
+  __shared__ uint32_t s_cs[kEncWarps][kMaxLutSlots];  // escape position where a chunk starts
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const ZcLayout& L = A.L;
   const uint32_t C = L.C, log2C = L.log2C;
   const unsigned long long S = L.slot_bytes;
   const unsigned long long lanes_total = L.nchunks << log2C;
-  const unsigned long long ntiles = (lanes_total + kEncTile - 1) / kEncTile;
-  const uint32_t nct = C >= kEncTile ? 1u : kEncTile / C;   // chunks per ticket
-  int my_seg = -1;  // segment cache of threads < nct
+  const unsigned long long ntiles = (lanes_total + kWTile - 1) / kWTile;
+  const uint32_t nct = C >= kWTile ? 1u : kWTile / C;  // chunks per ticket
+  uint8_t* wring = dyn + (size_t)warp * (kStages * 2048u + nct * 1024u + kEscCap);  // input steps
+  uint32_t* wlut = reinterpret_cast<uint32_t*>(wring + kStages * 2048u);
+  uint8_t* wst = wring + kStages * 2048u + nct * 1024u;  // staged escape bytes
+  if (lane < kMaxLutSlots) s_lseg[warp][lane] = -1;
+  // ring offsets of this lane: it copies pieces lane + 32j, reads pieces 4*lane + k
+  uint32_t cp_dst[4], rd_src[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t q = (uint32_t)lane + 32u * j, r = 4u * lane + j;
+    cp_dst[j] = 16u * (q ^ ((q >> 3) & 3u));
+    rd_src[j] = 16u * (r ^ ((r >> 3) & 3u));
+  }
+  __syncwarp();
+  int my_seg = -1;  // segment cache of lanes < nct
   unsigned long long my_c0 = 0, my_c1 = 0;
-  if (t < kMaxTileChunks) s_lut_seg[t] = -1;
 
-  // A ticket is taken only when the block starts the tile: every tile before
-  // it is then already being worked on, so look-backs never wait on a tile
-  // that a busy block merely reserved.
-  for (int it = 0;; ++it) {
-    if (t == 0) s_tk[it & 1] = atomicAdd(&A.ctrl->ticket, 1ull);
-    __syncthreads();
-    const unsigned long long tile = s_tk[it & 1];
+  for (;;) {
+    unsigned long long tile = 0;
+    if (lane == 0) tile = atomicAdd(&A.ctrl->ticket, 1ull);
+    tile = __shfl_sync(kFull, tile, 0);
     if (tile >= ntiles) break;
-    const unsigned long long tlane0 = tile * kEncTile;
+    const unsigned long long tlane0 = tile * kWTile;
     const unsigned long long cfirst = tlane0 >> log2C;
-    if (t < (int)nct) {
-      const unsigned long long c = cfirst + t;
+    // chunk information, held by lane k for the ticket's chunk k
+    unsigned long long ce0 = 0;
+    uint32_t cval = 0;
+    int cal = 0, cseg = -1;
+    if (lane < (int)nct) {
+      const unsigned long long c = cfirst + lane;
       if (c < L.nchunks) {
         if (my_seg < 0 || c < my_c0 || c >= my_c1) {
           my_seg = find_chunk_segment(A.segs, L.nseg, c);
@@ -149,218 +140,265 @@ __global__ void __launch_bounds__(kThreads, 4) zc_encode_kernel(EncArgs A) {
           my_c1 = my_c0 + A.segs[my_seg].nchunks;
         }
         const ZcSegDev& r = A.segs[my_seg];
-        const unsigned long long e0 = r.elem_start + ((c - r.chunk_start) << log2C);
+        ce0 = r.elem_start + ((c - r.chunk_start) << log2C);
         const unsigned long long end = r.elem_start + r.nelem;
-        s_seg[t] = my_seg;
-        s_elem0[t] = e0;
-        s_valid[t] = (uint32_t)((end - e0) < C ? (end - e0) : C);
-        s_al[t] = A.x_al16 && ((r.elem_start & 7ull) == 0);
-      } else {
-        s_seg[t] = -1;
-        s_elem0[t] = 0;
-        s_valid[t] = 0;
-        s_al[t] = 0;
+        cval = (uint32_t)((end - ce0) < C ? (end - ce0) : C);
+        cal = A.x_al16 && ((r.elem_start & 7ull) == 0);
+        cseg = my_seg;
       }
     }
-    __syncthreads();
-    bool rebuilt = false;
+    const unsigned long long t_e0 = __shfl_sync(kFull, ce0, 0);
+    const uint32_t t_val = __shfl_sync(kFull, cval, 0);
+    const bool t_al = __shfl_sync(kFull, cal, 0) != 0;
+    // lookup tables of the ticket's chunks (rebuilt only when the segment changes)
     for (uint32_t k = 0; k < nct; ++k) {
-      const int sg = s_seg[k];
-      if (sg >= 0 && s_lut_seg[k] != sg) {
-        s_lut[k][t] = lut_entry(A.segs[sg].book, (uint32_t)t);
-        rebuilt = true;
+      const int sg = __shfl_sync(kFull, cseg, (int)k);
+      if (sg >= 0 && s_lseg[warp][k] != sg) {
+        for (uint32_t e = lane; e < 256u; e += 32u) wlut[k * 256u + e] = lut_entry(A.segs[sg].book, e);
+        __syncwarp();
+        if (lane == 0) s_lseg[warp][k] = sg;
       }
     }
-    if (rebuilt) {  // uniform: every thread saw the same s_seg / s_lut_seg
-      __syncthreads();
-      if (t < (int)nct && s_seg[t] >= 0) s_lut_seg[t] = s_seg[t];
-    }
+    __syncwarp();
 
-    // ---- sub-tiles: warp-level work only
-    uint8_t* wst = s_esc[warp];
-    uint32_t wrun = 0;  // escapes this warp staged in this ticket
-    uint32_t lit = (uint32_t)warp * 512u + 16u * lane;  // slot within the ticket
-    int lct = C >= kEncTile ? 0 : (int)(lit >> log2C);
-    uint32_t i0 = (uint32_t)((tlane0 + lit) & (C - 1));
-    uint32_t vch = s_valid[lct];
-    int valid = vch > i0 ? ((vch - i0) < 16u ? (int)(vch - i0) : 16) : 0;
-    uint32_t w[8], wn[8];
-    load16(A.x, s_elem0[lct] + i0, valid, s_al[lct], w);
-    for (int sub = 0; sub < kSub; ++sub) {
-      if (tlane0 + (unsigned long long)sub * kTileLanes >= lanes_total) {  // uniform
-        if (lane == 0) s_cnt[sub * kEncWarps + warp] = 0;
-        continue;
+    // ---- steps of 1024 slots, 32 consecutive slots per lane: a lane builds whole
+    // 32-bit plane words; a step lies inside one chunk (C is a multiple of 1024)
+    uint32_t run = 0, cs_pos = 0;  // escapes staged so far; chunk-start position (lane k)
+    const uint32_t steps =
+        (uint32_t)((lanes_total - tlane0) < kWTile ? (lanes_total - tlane0) : kWTile) / 1024u;
+    // Step input: a full, 16-byte aligned step is copied into the warp's ring
+    // with coalesced cp.async pieces (lane l copies 16-byte pieces l, l+32,
+    // l+64, l+96), kAhead steps before it is used; each lane then reads its own
+    // 64 contiguous bytes.  Piece q sits at q ^ ((q >> 3) & 3) so those reads
+    // are free of bank conflicts.  Other steps use plain per-lane loads.
+    // With C >= 4096 the whole ticket lies in one chunk and the step's chunk
+    // data need no shuffles.
+    const bool one = C >= kWTile;
+    auto info = [&](uint32_t st, int& lct, unsigned long long& e0, uint32_t& vch, bool& al) {
+      if (one) {
+        lct = 0;
+        e0 = t_e0;
+        vch = t_val;
+        al = t_al;
+      } else {
+        lct = (int)((st * 1024u) >> log2C);
+        e0 = __shfl_sync(kFull, ce0, lct);
+        vch = __shfl_sync(kFull, cval, lct);
+        al = __shfl_sync(kFull, cal, lct) != 0;
       }
-      // next sub-tile's loads first
-      // (positions past the last chunk read as chunk-local slots of a
-      // chunk >= nchunks: valid 0, not live)
-      const uint32_t lit_n = lit + kTileLanes;
-      int lct_n = 0, valid_n = 0;
-      uint32_t i0_n = 0;
-      if (sub + 1 < kSub) {
-        lct_n = C >= kEncTile ? 0 : (int)(lit_n >> log2C);
-        i0_n = (uint32_t)((tlane0 + lit_n) & (C - 1));
-        const uint32_t vn = s_valid[lct_n];
-        valid_n = vn > i0_n ? ((vn - i0_n) < 16u ? (int)(vn - i0_n) : 16) : 0;
-        if (valid_n) {
-          load16(A.x, s_elem0[lct_n] + i0_n, valid_n, s_al[lct_n], wn);
-        } else {
+    };
+    auto issue = [&](uint32_t st) {
+      if (st < steps) {
+        int l_;
+        unsigned long long e_;
+        uint32_t v_;
+        bool a_;
+        info(st, l_, e_, v_, a_);
+        const uint32_t s0 = (uint32_t)((tlane0 + st * 1024u) & (C - 1));
+        if (a_ && v_ >= s0 + 1024u) {
+          uint8_t* slotbuf = wring + (st % kStages) * 2048u;
+          const uint16_t* src = A.x + e_ + s0;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) wn[j] = 0;  // padding slots: byte 0
+          for (int j = 0; j < 4; ++j) cp_async16(slotbuf + cp_dst[j], src + 8u * lane + 256u * j);
         }
       }
-      const unsigned long long c = cfirst + lct;
-      const bool live = c < L.nchunks;
-      const uint32_t* Lt = s_lut[lct];
-      uint32_t accA = 0, accB = 0;
+      cp_async_commit();
+    };
+    auto lane_load = [&](const uint16_t* src, int valid, uint32_t(&w)[16]) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        accA |= Lt[(w[j] >> 7) & 0xFFu] << (2 * j);
-        accA |= Lt[(w[j] >> 23) & 0xFFu] << (2 * j + 1);
-        accB |= Lt[(w[j + 4] >> 7) & 0xFFu] << (2 * j);
-        accB |= Lt[(w[j + 4] >> 23) & 0xFFu] << (2 * j + 1);
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t lo = (2 * j < valid) ? (uint32_t)__ldg(src + 2 * j) : 0u;
+        const uint32_t hi = (2 * j + 1 < valid) ? (uint32_t)__ldg(src + 2 * j + 1) : 0u;
+        w[j] = lo | (hi << 16);
       }
-      if (valid < 16) {  // slots past the segment end: code 0, no escape
-        const uint32_t vA = valid >= 8 ? 0xFFu : ((1u << valid) - 1u);
-        const uint32_t vB = valid >= 16 ? 0xFFu : (valid > 8 ? ((1u << (valid - 8)) - 1u) : 0u);
-        accA &= vA * 0x01010101u;
-        accB &= vB * 0x01010101u;
-      }
-      uint8_t* slot = A.out + L.off_static + c * S;
-      if (live) {
-        uint4 smv;
-        smv.x = sm4(w[0], w[1]);
-        smv.y = sm4(w[2], w[3]);
-        smv.z = sm4(w[4], w[5]);
-        smv.w = sm4(w[6], w[7]);
-        st_v4(slot + i0, smv);
-      }
-      const uint32_t T0 = prmt(accA, accB, 0x5140);  // plane0 | plane1 << 16
-      const uint32_t T1 = prmt(accA, accB, 0x7362);  // plane2 | escape << 16
-      const uint32_t U0 = __shfl_xor_sync(kFull, T0, 1);
-      const uint32_t U1 = __shfl_xor_sync(kFull, T1, 1);
-      if (live) {
-        uint32_t* pw = reinterpret_cast<uint32_t*>(slot + C) + (i0 >> 5);
-        const uint32_t pwords = C >> 5;
-        if ((lane & 1) == 0) {
-          pw[0] = prmt(T0, U0, 0x5410);
-          pw[pwords] = prmt(T0, U0, 0x7632);
-        } else {
-          pw[2 * pwords] = prmt(U1, T1, 0x5410);
+    };
+    // byte k of acc[q] = plane k bits of slots 8q..8q+7 (k = 3: escapes); the
+    // entries' bits never overlap, so shifting and adding (one LEA) is an OR
+    auto classify = [&](const uint32_t(&w)[16], const uint32_t* Lt, int valid, uint32_t(&acc)[4]) {
+      const char* Lb = reinterpret_cast<const char*>(Lt);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t a = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t x = w[4 * q + j];
+          a += *reinterpret_cast<const uint32_t*>(Lb + ((x >> 5) & 0x3FCu)) << (2 * j);
+          a += *reinterpret_cast<const uint32_t*>(Lb + ((x >> 21) & 0x3FCu)) << (2 * j + 1);
         }
+        if (valid < 32) {  // slots past the segment end: code 0, no escape
+          const int vq = valid - 8 * q;
+          const uint32_t m = vq >= 8 ? 0xFFu : (vq <= 0 ? 0u : ((1u << vq) - 1u));
+          a &= m * 0x01010101u;
+        }
+        acc[q] = a;
       }
-      const uint32_t esc = T1 >> 16;
-      const uint32_t ne = (uint32_t)__popc(esc);
+    };
+    auto warp_excl = [&](uint32_t ne, uint32_t& total) {
       uint32_t inc = ne;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t v = __shfl_up_sync(kFull, inc, o);
         if (lane >= o) inc += v;
       }
-      const uint32_t excl = inc - ne;
-      if (live && i0 == 0) {  // a chunk starts at this thread's first slot
-        s_cs_seg[lct] = (uint32_t)(sub * kEncWarps + warp);
-        s_cs_pos[lct] = excl;
+      total = __shfl_sync(kFull, inc, 31);
+      return inc - ne;
+    };
+    // escaped exponent fields, in slot order, from the lane's 16 words
+    // (the stash is the step's ring slot, free once every lane has read it)
+    auto put_escapes = [&](const uint32_t(&w)[16], uint32_t esc, uint32_t pos, uint8_t* dst,
+                           uint32_t cap, uint8_t* slotbuf) {
+      __syncwarp();
+      uint4* stash = reinterpret_cast<uint4*>(slotbuf + 64u * lane);
+      stash[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      stash[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      stash[2] = make_uint4(w[8], w[9], w[10], w[11]);
+      stash[3] = make_uint4(w[12], w[13], w[14], w[15]);
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(stash);
+      while (esc) {
+        const int i = __ffs(esc) - 1;
+        esc &= esc - 1;
+        if (pos < cap) dst[pos] = (uint8_t)((h[i] >> 7) & 0xFFu);
+        ++pos;
       }
-      if (esc) {
-        uint32_t F[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) F[q] = prmt(w[2 * q] >> 7, w[2 * q + 1] >> 7, 0x6420);
-        uint32_t m = esc, pos = wrun + excl;
-        while (m) {
-          const int i = __ffs(m) - 1;
-          m &= m - 1;
-          const uint32_t f = i < 8 ? (i < 4 ? F[0] : F[1]) : (i < 12 ? F[2] : F[3]);
-          wst[pos++] = (uint8_t)((f >> ((i & 3) * 8)) & 0xFFu);
-        }
-      }
-      const uint32_t wtot = __shfl_sync(kFull, inc, 31);
-      if (lane == 0) s_cnt[sub * kEncWarps + warp] = wtot;
-      wrun += wtot;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) w[j] = wn[j];
-      lit = lit_n;
-      lct = lct_n;
-      i0 = i0_n;
-      valid = valid_n;
-    }
-    __syncthreads();
+    };
 
-    // ---- one warp: prefix of the 32 staged counts, look-back for the ticket
-    if (warp == 0) {
-      const uint32_t cnt = s_cnt[lane];  // order: sub-tile major, warp minor = slot order
-      uint32_t inc = cnt;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(kFull, inc, o);
-        if (lane >= o) inc += v;
-      }
-      s_off[lane] = inc - cnt;
-      const uint32_t agg = __shfl_sync(kFull, inc, 31);
-      bool to = false;
-      const unsigned long long e = lookback_warp_wide(A.states, tile, agg, &to);
-      if (lane == 0) {
-        s_excl = e;
-        if (to) set_status(A.ctrl, ZC_ERR_TIMEOUT);
-      }
-    }
-    __syncthreads();
-    const unsigned long long base = L.off_esc + s_excl;
-    {
-      uint32_t src = 0;
-      for (int sub = 0; sub < kSub; ++sub) {
-        const uint32_t k = (uint32_t)(sub * kEncWarps + warp);
-        const uint32_t n = s_cnt[k];
-        const unsigned long long dst = base + s_off[k];
-        if (dst + n <= A.out_cap) {
-          for (uint32_t i = lane; i < n; i += 32) A.out[dst + i] = wst[src + i];
-        } else if (lane == 0) {
-          set_status(A.ctrl, ZC_ERR_CAPACITY);
+    for (uint32_t k = 0; k < kAhead; ++k) issue(k);
+    for (uint32_t st = 0; st < steps; ++st) {
+      issue(st + kAhead);
+      int lct;
+      unsigned long long e0;
+      uint32_t vch;
+      bool al;
+      info(st, lct, e0, vch, al);
+      const uint32_t s0 = (uint32_t)((tlane0 + st * 1024u) & (C - 1));
+      const uint32_t i0 = s0 + 32u * lane;
+      const int valid = vch > i0 ? ((vch - i0) < 32u ? (int)(vch - i0) : 32) : 0;
+      uint32_t w[16];
+      if (al && vch >= s0 + 1024u) {  // the ring holds this step
+        cp_async_wait_group<kAhead>();
+        __syncwarp();
+        const uint8_t* slotbuf = wring + (st % kStages) * 2048u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(slotbuf + rd_src[k]);
+          w[4 * k] = v.x;
+          w[4 * k + 1] = v.y;
+          w[4 * k + 2] = v.z;
+          w[4 * k + 3] = v.w;
         }
-        src += n;
+        __syncwarp();  // every lane has its bytes before the slot is refilled
+      } else {  // unaligned segment or a ragged end; padding slots read as 0
+        lane_load(A.x + e0 + i0, valid, w);
+      }
+      const unsigned long long c = cfirst + lct;
+      uint32_t acc[4];
+      classify(w, wlut + (uint32_t)lct * 256u, valid, acc);
+      uint8_t* slot = A.out + L.off_static + c * S;
+      uint4 s0v, s1v;
+      s0v.x = sm4(w[0], w[1]);
+      s0v.y = sm4(w[2], w[3]);
+      s0v.z = sm4(w[4], w[5]);
+      s0v.w = sm4(w[6], w[7]);
+      s1v.x = sm4(w[8], w[9]);
+      s1v.y = sm4(w[10], w[11]);
+      s1v.z = sm4(w[12], w[13]);
+      s1v.w = sm4(w[14], w[15]);
+      st_v4(slot + i0, s0v);
+      st_v4(slot + i0 + 16, s1v);
+      const uint32_t tA = prmt(acc[0], acc[1], 0x5140), tB = prmt(acc[2], acc[3], 0x5140);
+      const uint32_t tC = prmt(acc[0], acc[1], 0x7362), tD = prmt(acc[2], acc[3], 0x7362);
+      uint32_t* pw = reinterpret_cast<uint32_t*>(slot + C + (i0 >> 3));
+      const uint32_t pwords = C >> 5;
+      pw[0] = prmt(tA, tB, 0x5410);
+      pw[pwords] = prmt(tA, tB, 0x7632);
+      pw[2 * pwords] = prmt(tC, tD, 0x5410);
+      const uint32_t esc = prmt(tC, tD, 0x7632);
+      uint32_t tot;
+      const uint32_t pos0 = run + warp_excl((uint32_t)__popc(esc), tot);
+      if (s0 == 0 && lane == 0) s_cs[warp][lct] = pos0;  // a chunk starts at this step
+      if (__any_sync(kFull, esc != 0 && pos0 < kEscCap))
+      {
+        put_escapes(w, (esc != 0 && pos0 < kEscCap) ? esc : 0u, pos0, wst, kEscCap,
+                    wring + (st % kStages) * 2048u);
+        __syncwarp();  // the stash is read before the next copy lands in the ring
+      }
+      run += tot;
+    }
+    __syncwarp();
+    if (lane < (int)nct) cs_pos = s_cs[warp][lane];
+
+    // ---- the warp's own decoupled look-back, then its escapes go out
+    bool to = false;
+    const unsigned long long excl = lookback_warp_wide(A.states, tile, run, &to);
+    if (to && lane == 0) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+    const unsigned long long dst = L.off_esc + excl;
+    if (dst + run > A.out_cap) {
+      if (lane == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
+    } else if (run <= kEscCap) {
+      for (uint32_t i = lane; i < run; i += 32) A.out[dst + i] = wst[i];
+    } else {
+      // more escapes than the window holds: classify the ticket again and
+      // write its escape bytes straight to their place
+      uint32_t r2 = 0;
+      for (uint32_t st = 0; st < steps; ++st) {
+        int lct;
+        unsigned long long e0;
+        uint32_t vch;
+        bool al;
+        info(st, lct, e0, vch, al);
+        const uint32_t i0 = (uint32_t)((tlane0 + st * 1024u) & (C - 1)) + 32u * lane;
+        const int valid = vch > i0 ? ((vch - i0) < 32u ? (int)(vch - i0) : 32) : 0;
+        uint32_t w[16];
+        lane_load(A.x + e0 + i0, valid, w);
+        uint32_t acc[4];
+        classify(w, wlut + (uint32_t)lct * 256u, valid, acc);
+        const uint32_t esc = prmt(prmt(acc[0], acc[1], 0x7362), prmt(acc[2], acc[3], 0x7362), 0x7632);
+        uint32_t tot;
+        const uint32_t pos = r2 + warp_excl((uint32_t)__popc(esc), tot);
+        put_escapes(w, esc, pos, A.out + dst, 0xFFFFFFFFu, wring);
+        __syncwarp();
+        r2 += tot;
       }
     }
-    // escape offsets of the chunks that start in this ticket
-    if (t < (int)nct) {
-      const unsigned long long c = cfirst + t;
-      const bool starts = C >= kEncTile ? ((tlane0 & (C - 1)) == 0) : true;
+    if (lane < (int)nct) {
+      const unsigned long long c = cfirst + lane;
+      const bool starts = C >= kWTile ? ((tlane0 & (C - 1)) == 0) : true;
       if (c < L.nchunks && starts)
-        reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] =
-            s_excl + s_off[s_cs_seg[t]] + s_cs_pos[t];
+        reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = excl + cs_pos;
     }
-    __syncthreads();  // s_excl, s_off, s_cnt and the windows are reused by the next ticket
+    __syncwarp();  // the window is reused by the next ticket
   }
 
-  // ---- the last block to finish writes the header, tables and padding
-  __syncthreads();
-  if (t == 0) {
+  // ---- the last warp to finish writes the header, tables and padding
+  unsigned last = 0;
+  if (lane == 0) {
     __threadfence();
     const unsigned long long d = atomicAdd(&A.ctrl->done, 1ull);
-    s_last = (d == gridDim.x - 1);
+    last = (d == (unsigned long long)gridDim.x * kEncWarps - 1) ? 1u : 0u;
   }
-  __syncthreads();
-  if (!s_last) return;
+  if (!__shfl_sync(kFull, last, 0)) return;
   __threadfence();
   unsigned long long esc_total = 0;
   if (ntiles) esc_total = ld_acquire_u64(A.states + ntiles - 1) & kValMask;
   const unsigned long long total = L.off_esc + round_up_dev(esc_total, kZcAlign);
   unsigned long long* escoff = reinterpret_cast<unsigned long long*>(A.out + L.off_escoff);
-  if (t == 0) {
+  if (lane == 0) {
     escoff[L.nchunks] = esc_total;
     if (total > A.out_cap) set_status(A.ctrl, ZC_ERR_CAPACITY);
     if (A.out_bytes) *A.out_bytes = total;
   }
   // zero padding: escape tail, segment-table tail, offset-table tail
   const unsigned long long pad_end = total < A.out_cap ? total : A.out_cap;
-  for (unsigned long long p = L.off_esc + esc_total + t; p < pad_end; p += kThreads) A.out[p] = 0;
-  for (unsigned long long p = L.off_seg + (unsigned long long)kZcSegRec * L.nseg + t;
-       p < L.off_escoff; p += kThreads)
+  for (unsigned long long p = L.off_esc + esc_total + lane; p < pad_end; p += 32) A.out[p] = 0;
+  for (unsigned long long p = L.off_seg + (unsigned long long)kZcSegRec * L.nseg + lane;
+       p < L.off_escoff; p += 32)
     A.out[p] = 0;
-  for (unsigned long long p = L.off_escoff + 8ull * (L.nchunks + 1) + t; p < L.off_static;
-       p += kThreads)
+  for (unsigned long long p = L.off_escoff + 8ull * (L.nchunks + 1) + lane; p < L.off_static;
+       p += 32)
     A.out[p] = 0;
-  __syncthreads();  // escoff[nchunks] visible to the block
-  for (uint32_t s = t; s < L.nseg; s += kThreads) {
+  __syncwarp();
+  for (uint32_t s = lane; s < L.nseg; s += 32) {
     const ZcSegDev& r = A.segs[s];
     const volatile unsigned long long* ve = escoff;
     const unsigned long long es = ve[r.chunk_start];
@@ -379,9 +417,9 @@ __global__ void __launch_bounds__(kThreads, 4) zc_encode_kernel(EncArgs A) {
     rec[6] = bk;
     rec[7] = 0;
   }
-  if (t < 16) {
+  if (lane < 16) {
     unsigned long long h = 0;
-    switch (t) {
+    switch (lane) {
       case 0: h = (unsigned long long)kZcMagic | (1ull << 32) | ((unsigned long long)kZcHeader << 48); break;
       case 1: h = (unsigned long long)C | ((unsigned long long)L.nseg << 32); break;
       case 2: h = L.n; break;
@@ -394,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 4) zc_encode_kernel(EncArgs A) {
       case 9: h = total; break;
       default: h = 0; break;
     }
-    reinterpret_cast<unsigned long long*>(A.out)[t] = h;
+    reinterpret_cast<unsigned long long*>(A.out)[lane] = h;
   }
 }
 
@@ -664,7 +702,7 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   Ctrl* ctrl = static_cast<Ctrl*>(d_ws);
   unsigned long long* states =
       reinterpret_cast<unsigned long long*>(static_cast<char*>(d_ws) + kCtrlBytes);
-  const unsigned long long ntiles = ((L.nchunks << L.log2C) + kEncTile - 1) / kEncTile;
+  const unsigned long long ntiles = ((L.nchunks << L.log2C) + kWTile - 1) / kWTile;
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 8ull * ntiles, s);
   if (e != cudaSuccess) return e;
   EncArgs A;
@@ -677,10 +715,17 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   A.ctrl = ctrl;
   A.states = states;
   A.x_al16 = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
-  const int res = resident_blocks((const void*)zc_encode_kernel, kThreads, 0);
-  unsigned long long grid = ntiles < (unsigned long long)res ? ntiles : (unsigned long long)res;
+  const uint32_t nct = L.C >= kWTile ? 1u : kWTile / L.C;
+  const size_t smem = (size_t)kEncWarps * (kStages * 2048u + nct * 1024u + kEscCap);
+  e = cudaFuncSetAttribute(zc_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(zc_encode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  const int res = resident_blocks((const void*)zc_encode_kernel, kThreads, smem);
+  const unsigned long long need = (ntiles + kEncWarps - 1) / kEncWarps;
+  unsigned long long grid = need < (unsigned long long)res ? need : (unsigned long long)res;
   if (grid == 0) grid = 1;
-  zc_encode_kernel<<<(unsigned)grid, kThreads, 0, s>>>(A);
+  zc_encode_kernel<<<(unsigned)grid, kThreads, smem, s>>>(A);
   return cudaGetLastError();
 }
 

@@ -30,6 +30,11 @@
 namespace lbb {
 namespace {
 
+#ifndef LBB_STAT_BATCH
+#define LBB_STAT_BATCH 4
+#endif
+constexpr int kStatBatch = LBB_STAT_BATCH;  // groups loaded before summing
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -79,53 +84,71 @@ __global__ void __launch_bounds__(kThreads) zc_stats_kernel(
   float hx = 0.f, lx = 0.f, hq = 0.f, lq = 0.f;
   double dx = 0.0, dq = 0.0;
   unsigned long long cnt = 0;
-  for (unsigned long long e0 = lo + 16ull * t; e0 < hi; e0 += 16ull * kThreads) {
-    const unsigned long long rem = hi - e0;
-    const int valid = rem < 16 ? (int)rem : 16;
-    uint32_t w[8];
-    if (al && valid == 16) {
-      uint4 a = ld_nc_v4(x + e0), b = ld_nc_v4(x + e0 + 8);
-      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-    } else {
+  // A group is 16 * kThreads values; a thread takes 8 at base + 8t and 8 at
+  // base + 8 * (kThreads + t), so every 16-byte load instruction of a warp
+  // reads 512 contiguous bytes.  kBatch groups are loaded before any is
+  // summed (more bytes in flight per thread); they are summed in order.
+  const unsigned long long gstride = 16ull * kThreads;
+  for (unsigned long long base0 = lo; base0 < hi; base0 += kStatBatch * gstride) {
+    uint32_t w[kStatBatch][8];
+    int vh[kStatBatch][2];
+#pragma unroll
+    for (int g = 0; g < kStatBatch; ++g) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const unsigned long long e0 = base0 + g * gstride + 8ull * ((unsigned long long)h * kThreads + t);
+        const unsigned long long rem = e0 < hi ? hi - e0 : 0ull;
+        const int v = rem < 8 ? (int)rem : 8;
+        vh[g][h] = v;
+        if (v == 8 && al) {
+          const uint4 a = ld_nc_v4(x + e0);
+          w[g][4 * h] = a.x; w[g][4 * h + 1] = a.y; w[g][4 * h + 2] = a.z; w[g][4 * h + 3] = a.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t l = (2 * j < v) ? (uint32_t)__ldg(x + e0 + 2 * j) : 0u;
+            const uint32_t hh = (2 * j + 1 < v) ? (uint32_t)__ldg(x + e0 + 2 * j + 1) : 0u;
+            w[g][4 * h + j] = l | (hh << 16);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < kStatBatch; ++g) {
+      const int valid = vh[g][0] + vh[g][1];
+      if (valid == 0) continue;
+      float v[16];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        uint32_t l = (2 * j < valid) ? (uint32_t)__ldg(x + e0 + 2 * j) : 0u;
-        uint32_t h = (2 * j + 1 < valid) ? (uint32_t)__ldg(x + e0 + 2 * j + 1) : 0u;
-        w[j] = l | (h << 16);
+        v[2 * j] = bf16_lo(w[g][j]);
+        v[2 * j + 1] = bf16_hi(w[g][j]);
       }
-    }
-    float v[16];
+      float q[16];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      v[2 * j] = bf16_lo(w[j]);
-      v[2 * j + 1] = bf16_hi(w[j]);
-    }
-    float q[16];
+      for (int j = 0; j < 16; ++j) q[j] = __fmul_rn(v[j], v[j]);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) q[j] = __fmul_rn(v[j], v[j]);
+      for (int s = 1; s < 16; s <<= 1) {
 #pragma unroll
-    for (int s = 1; s < 16; s <<= 1) {
-#pragma unroll
-      for (int j = 0; j < 16; j += 2 * s) {
-        v[j] = __fadd_rn(v[j], v[j + s]);
-        q[j] = __fadd_rn(q[j], q[j + s]);
+        for (int j = 0; j < 16; j += 2 * s) {
+          v[j] = __fadd_rn(v[j], v[j + s]);
+          q[j] = __fadd_rn(q[j], q[j + s]);
+        }
       }
-    }
-    if (isfinite(v[0]) && isfinite(q[0])) {
-      two_sum_acc(hx, lx, v[0]);
-      two_sum_acc(hq, lq, q[0]);
-      cnt += (unsigned long long)valid;
-    } else {
-      // an inf/NaN input or an fp32 overflow: redo these values in fp64
+      if (isfinite(v[0]) && isfinite(q[0])) {
+        two_sum_acc(hx, lx, v[0]);
+        two_sum_acc(hq, lq, q[0]);
+        cnt += (unsigned long long)valid;
+      } else {
+        // an inf/NaN input or an fp32 overflow: redo these values in fp64
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
-        if (j < valid && ((bits >> 7) & 0xFFu) != 0xFFu) {
-          double d = (double)__uint_as_float(bits << 16);
-          dx = __dadd_rn(dx, d);
-          dq = __dadd_rn(dq, __dmul_rn(d, d));
-          cnt += 1;
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t bits = (j & 1) ? (w[g][j >> 1] >> 16) : (w[g][j >> 1] & 0xFFFFu);
+          if ((j & 7) < vh[g][j >> 3] && ((bits >> 7) & 0xFFu) != 0xFFu) {
+            const double d = (double)__uint_as_float(bits << 16);
+            dx = __dadd_rn(dx, d);
+            dq = __dadd_rn(dq, __dmul_rn(d, d));
+            cnt += 1;
+          }
         }
       }
     }

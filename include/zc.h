@@ -135,6 +135,32 @@ int zc_compress(zc_plan_t plan, const uint16_t* d_x, void* d_out,
                 uint64_t out_cap, uint64_t* d_out_bytes, void* d_ws,
                 size_t ws_bytes, zc_stream_t stream);
 
+/* zc_compress without a workspace.  The ZipCCL pages have no counterpart:
+ * this is an interface for callers that cannot allocate at the point where
+ * they compress -- e.g. a communication library's progress thread, where a
+ * cudaMalloc would synchronise the device and stall transfers in flight, or
+ * a program whose device memory is all held by a pool it cannot reach from
+ * here -- and so cannot size or keep a workspace.  The encoder's scratch
+ * (status block and look-back words) is instead a fixed 1 MiB array in
+ * device memory owned by the library, which limits the plan to 131,040 tiles
+ * of 4096 slots (536,739,840 slots, chunk padding included); a larger plan
+ * returns ZC_ERR_CAPACITY.  Nothing is allocated by this call (the plan
+ * itself was allocated by zc_plan_create).
+ *
+ * Arguments, layout and the stream bytes are those of zc_compress.  d_status
+ * (device, 4-byte aligned, may be NULL) receives the status word
+ * (ZC_OK or a ZC_ERR_* code) once the kernel is done.  Enqueues one memset,
+ * the encode kernel and a 4-byte device copy on `stream`.
+ *
+ * The first call on each device looks up the array's address (with that
+ * device current); make it before any stream capture.  All calls on a device
+ * share the one array: calls whose GPU work overlaps (other streams, other
+ * threads) race and corrupt each other's streams, so order them on one
+ * stream or with events. */
+int zc_compress_static(zc_plan_t plan, const uint16_t* d_x, void* d_out,
+                       uint64_t out_cap, uint64_t* d_out_bytes, int* d_status,
+                       zc_stream_t stream);
+
 /* Workspace bytes zc_decompress needs (a constant). */
 size_t zc_decompress_workspace_bytes(void);
 

@@ -14,13 +14,6 @@
 #include "internal.h"
 #include "zc.h"
 
-struct zc_plan_s {
-  int device;
-  lbb::ZcLayout L;
-  lbb::ZcSegDev* d_segs;
-  std::vector<lbb::ZcSegDev> h_segs;
-};
-
 namespace lbb {
 
 int resident_blocks(const void* kernel, int threads, size_t smem) {

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <vector>
 
 #include "zc.h"
 
@@ -81,3 +82,12 @@ cudaError_t ibp_launch_decompress(const void* d_meta, uint32_t chunk_bytes,
 int resident_blocks(const void* kernel, int threads, size_t smem);
 
 }  // namespace lbb
+
+// A ZipCCL plan (the opaque zc_plan_t of zc.h): layout, the device segment
+// table the kernels read, and its host copy.
+struct zc_plan_s {
+  int device;
+  lbb::ZcLayout L;
+  lbb::ZcSegDev* d_segs;
+  std::vector<lbb::ZcSegDev> h_segs;
+};

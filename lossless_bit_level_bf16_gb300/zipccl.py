@@ -110,6 +110,18 @@ class Plan:
                                        abi.stream_handle(stream)), "zc_compress")
         return out, out_bytes
 
+    def compress_static(self, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
+                        status: torch.Tensor | None = None, stream=None):
+        """zc_compress_static: the caller passes every buffer (out, out_bytes
+        int64[1], status int32[1] or None); nothing is allocated or synchronised."""
+        x = _bits(x)
+        if x.numel() != self.n:
+            raise ValueError(f"plan is for {self.n} elements, tensor has {x.numel()}")
+        abi.check(self.lib.zc_compress_static(self._h, abi.ptr(x), abi.ptr(out), out.numel(),
+                                              abi.ptr(out_bytes), abi.ptr(status),
+                                              abi.stream_handle(stream)), "zc_compress_static")
+        return out, out_bytes
+
     def status(self, stream=None) -> int:
         return abi.status(self.ws, stream)
 

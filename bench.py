@@ -363,6 +363,145 @@ def report_gpu(args, r, world):
     return line
 
 
+# ---------------------------------------------------------------- size sweep
+
+SWEEP_OPS = {"zipccl": ("zc_plan", "zc_compress", "zc_decompress"),
+             "ibp": ("ibp_build_meta", "ibp_compress", "ibp_decompress")}
+
+
+def _time_ops(ops, flush, stream, warmup, steps):
+    """Median CUDA-event time (ms) of each op over `steps` launches after
+    `warmup` untimed ones; L2 is flushed before every launch."""
+    import torch
+    per = {name: [] for name, _ in ops}
+    for it in range(warmup + steps):
+        for name, fn in ops:
+            flush.add_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            if it >= warmup:
+                per[name].append((a, b))
+    torch.cuda.synchronize()
+    return {name: statistics.median(a.elapsed_time(b) for a, b in v) for name, v in per.items()}
+
+
+def _case(kind, nbytes, dev, ibp_mode):
+    """One codec workload on the device: (ops, workspaces, uncompressed bytes,
+    bytes of the metadata samples, round-trip check, output-size tensor, chunk)."""
+    import torch
+
+    from lossless_bit_level_bf16_gb300 import ibp as I, workloads as W, zipccl as Z
+    if kind in ("zipccl", "gradient", "moe"):
+        if kind == "zipccl":
+            n = nbytes // 2
+            x, seg = W.zc_gaussian(n, sigma=0.01, seed=0, device=dev), None
+        elif kind == "gradient":
+            x, seg = W.zc_gradient(device=dev)
+        else:
+            x, seg, _ = W.zc_moe(device=dev)
+        n = x.numel()
+        plan = Z.Plan(n, seg, 4096, device=dev)
+        out = torch.empty(plan.max_compressed_bytes, dtype=torch.uint8, device=dev)
+        nb = torch.zeros(1, dtype=torch.int64, device=dev)
+        y = torch.empty_like(x)
+        dws = torch.empty(256, dtype=torch.uint8, device=dev)
+        ops = [("zc_plan", lambda: plan.fit(x)),
+               ("zc_compress", lambda: plan.compress(x, out=out, out_bytes=nb)),
+               ("zc_decompress", lambda: Z.decompress(out, out=y, in_bytes=out.numel(), ws=dws))]
+        check = lambda: torch.equal(y.view(torch.int16), x.view(torch.int16))  # noqa: E731
+        return ops, (plan.ws, dws), 2 * n, 0, check, nb, 4096
+    if kind == "ibp":
+        cb = 2048
+        n = nbytes // 4
+        x = W.ibp_gaussian(n, std=0.02, seed=0, device=dev)
+        idx = W.sample_rows(4 * n // cb, 10_000, seed=1, device=dev)
+        samples = x.view(-1, cb // 4)[idx].contiguous()
+    else:  # the embedding table, one 128-value row per chunk
+        cb = 512
+        x, idx = W.ibp_table(device=dev)
+        samples = x[idx].contiguous()
+        x = x.view(-1)
+        n = x.numel()
+    ns = samples.shape[0]
+    meta = torch.empty(64 + 2 * cb, dtype=torch.uint8, device=dev)
+    mws = torch.empty(I.workspace_bytes(cb, 0, ns), dtype=torch.uint8, device=dev)
+    iws = torch.empty(I.workspace_bytes(cb, 4 * n, 0), dtype=torch.uint8, device=dev)
+    out = torch.empty(I.max_compressed_bytes(cb, 4 * n), dtype=torch.uint8, device=dev)
+    nb = torch.zeros(1, dtype=torch.int64, device=dev)
+    y = torch.empty_like(x)
+    dws = torch.empty(256, dtype=torch.uint8, device=dev)
+    ops = [("ibp_build_meta", lambda: I.build_meta(samples, cb, T=0.9, mode=ibp_mode, meta=meta,
+                                                   ws=mws)),
+           ("ibp_compress", lambda: I.compress(meta, x, cb, out=out, out_bytes=nb, ws=iws)),
+           ("ibp_decompress", lambda: I.decompress(meta, out, 4 * n, cb, out=y, in_bytes=out.numel(),
+                                                   ws=dws))]
+    check = lambda: torch.equal(y.view(torch.int32), x.view(torch.int32))  # noqa: E731
+    return ops, (mws, iws, dws), 4 * n, ns * cb, check, nb, cb
+
+
+def sweep_arm(args):
+    """Per-op throughput, one JSON line per workload and size.
+
+    --codec zipccl / ibp: the size sweep (1 MiB .. 4 GiB in x4 steps, or
+    --sizes in MiB): ZipCCL on bf16 N(0, 0.01), one segment, chunk 4096; IBP on
+    fp32 N(0, 0.02) weights, 2048-byte chunks (512 values), T = 0.9, metadata
+    from 10,000 seeded sample chunks.  --codec table / gradient / moe: the
+    full-size embedding table, gradient-like buffer and MoE activations.
+    --only limits the timed ops (the ops before them run once, untimed)."""
+    import torch
+
+    from lossless_bit_level_bf16_gb300 import abi, workloads as W
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    peak, peak_kind = _peaks()
+    sizes = [int(float(v) * (1 << 20)) for v in args.sizes.split(",")] if args.sizes \
+        else list(W.SWEEP_BYTES)
+    kinds = {"both": ["zipccl", "ibp"]}.get(args.codec, [args.codec])
+    for kind in kinds:
+        for nbytes in (sizes if kind in ("zipccl", "ibp") else [0]):
+            ops, wss, unc, sbytes, check, nb, cb = _case(kind, nbytes, dev, args.ibp_mode)
+            if args.only:
+                names = args.only.split(",")
+                first = min(i for i, o in enumerate(ops) if o[0] in names)
+                for _, fn in ops[:first]:
+                    fn()
+                ops = [o for o in ops if o[0] in names]
+            ms = _time_ops(ops, flush, stream, args.warmup, args.steps)
+            for ws in wss:
+                st = abi.status(ws)
+                if st != 0:
+                    raise RuntimeError(f"device status {st}: {abi.strerror(st)}")
+            comp = int(nb.item())
+            if not args.only and not check():
+                raise RuntimeError(f"{kind} round trip differs at {unc} bytes")
+            res = {}
+            for name, t in ms.items():
+                if name == "ibp_build_meta":
+                    alg = unc_op = sbytes
+                elif name == "zc_plan":
+                    alg = unc_op = unc
+                else:
+                    alg, unc_op = unc + comp, unc
+                gbs = alg / (t * 1e-3) / 1e9
+                res[name] = {"ms": round(t, 4),
+                             "GBps_uncompressed": round(unc_op / (t * 1e-3) / 1e9, 1),
+                             "GBps_traffic": round(gbs, 1), "frac_hbm": round(gbs / peak, 4)}
+            line = {"sweep": kind, "bytes": unc, "ratio": round(unc / comp, 4) if comp else None,
+                    "l2_resident": unc <= 128 << 20, "peak_GBps": peak, "peak_kind": peak_kind,
+                    "ops": res,
+                    "config": {"chunk": cb, "ibp_mode": args.ibp_mode if cb != 4096 else None,
+                               "warmup": args.warmup, "steps": args.steps,
+                               "l2": "flushed before every launch"}}
+            print(json.dumps(line), flush=True)
+            del ops, wss, check
+            torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------- oracle arm
 
 def cpu_baseline(seconds=15.0):
@@ -440,11 +579,22 @@ def main():
     ap.add_argument("--scale", type=float, default=1.0, help="workload scale (1 = full size)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="size sweep of both codecs instead of the step (one line per size)")
+    ap.add_argument("--codec", default="both",
+                    choices=["both", "zipccl", "ibp", "table", "gradient", "moe"])
+    ap.add_argument("--sizes", default="", help="sweep sizes in MiB, comma separated")
+    ap.add_argument("--ibp-mode", type=int, default=0, choices=[0, 1])
+    ap.add_argument("--only", default="", help="sweep: time only these ops (comma separated)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.sweep:
+        args.warmup = max(args.warmup, 3)
+        sweep_arm(args)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(reference_arm(args)), flush=True)

@@ -114,9 +114,10 @@ int zc_plan_create(uint64_t n, const uint64_t* h_seg_off, uint32_t nseg, uint32_
   L.C = C;
   L.log2C = 0;
   while ((1u << L.log2C) < C) ++L.log2C;
-  // statistics unit: a power of two between 4096 and 65536 elements, fixed by n
+  // statistics unit: a power of two between 4096 and 16384 elements, fixed by n
+  // (one block of the statistics kernel; small units keep its tail wave short)
   unsigned long long U = 4096;
-  while (U < 65536 && U * 2 <= n / 1024) U *= 2;
+  while (U < 16384 && U * 2 <= n / 1024) U *= 2;
   L.U = (uint32_t)U;
   try {
     p->h_segs.resize(nseg);
@@ -255,7 +256,9 @@ size_t ibp_workspace_bytes(uint32_t cb, uint64_t n_bytes, uint64_t n_samples) {
   if (!ibp_chunk_ok(cb)) return 0;
   const unsigned long long nch = (n_bytes + cb - 1) / cb;
   const unsigned long long ng = (nch + 31) / 32;
-  const unsigned long long codec = 8ull * ng;                      // look-back states
+  // look-back states per group (chunks above 2048 bytes), or the encode's
+  // offsets-pass states and one participation word per group
+  const unsigned long long codec = 8ull * ng + 512;
   const unsigned long long B = 8ull * cb;
   const unsigned long long words = (n_samples + 31) / 32;
   const unsigned long long meta = 8ull * B + 4ull * B * words;      // counts + columns

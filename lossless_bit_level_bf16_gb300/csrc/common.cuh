@@ -102,6 +102,73 @@ __device__ __forceinline__ void cp_async_wait_group() {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// ---------------------------------------------------------------- TMA bulk copies
+//
+// One thread copies a contiguous global range into shared memory with
+// cp.async.bulk (16-byte aligned addresses, size a multiple of 16); an
+// mbarrier with one arrival counts the bytes in and flips its phase when all
+// have landed.  Waits are bounded: they report failure instead of spinning on.
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// True once the phase with the given parity has completed; false if the
+// bounded wait ran out.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < (1u << 20); ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Barrier `id` (1..15) over `count` threads (a multiple of 32) of the block.
+__device__ __forceinline__ void named_bar(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// True if the phase with the given parity has completed (does not wait).
+__device__ __forceinline__ bool mbar_test(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Orders this thread's earlier shared-memory accesses before later
+// asynchronous-proxy (bulk copy) writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
   return __byte_perm(a, b, s);
 }
@@ -171,6 +238,10 @@ __device__ __forceinline__ int lb_window(const unsigned long long* states, long 
   return jinc < D ? kLbFound : kLbAllAgg;
 }
 
+// D0 * 32 predecessors are read in the first round trip and D1 * 32 in each
+// further one; after FREE spins on a predecessor that has not published, the
+// warp sleeps between re-reads (doubling up to 512 ns) to spare L2 bandwidth.
+template <int D0 = 1, int D1 = kLbDepth, unsigned FREE = 64>
 __device__ __forceinline__ unsigned long long lookback_warp_wide(
     unsigned long long* states, unsigned long long tile, unsigned long long aggregate,
     bool* timed_out) {
@@ -186,21 +257,115 @@ __device__ __forceinline__ unsigned long long lookback_warp_wide(
   bool deep = false, to = false;
   while (true) {
     unsigned long long sum = 0;
-    const int r = deep ? lb_window<kLbDepth>(states, end, &sum) : lb_window<1>(states, end, &sum);
+    const int r = deep ? lb_window<D1>(states, end, &sum) : lb_window<D0>(states, end, &sum);
     if (r == kLbEmpty) {
       if (++spins > kMaxSpins) {
         to = true;
         break;
       }
-      if (spins > 64) {
+      if (spins > FREE) {
         __nanosleep(ns);
-        if (ns < 256) ns <<= 1;
+        if (ns < 512) ns <<= 1;
       }
       continue;
     }
     excl += sum;
     if (r == kLbFound) break;
-    end -= deep ? 32 * kLbDepth : 32;
+    end -= deep ? 32 * D1 : 32 * D0;
+    deep = true;
+  }
+  if (to) {
+    *timed_out = true;
+    if (lane == 0) st_relaxed_u64(states + tile, kFlagInc | aggregate);
+    return 0;
+  }
+  if (lane == 0) st_relaxed_u64(states + tile, kFlagInc | ((excl + aggregate) & kValMask));
+  return excl;
+}
+
+// Look-back for kernels whose tiles take microseconds to publish: while a
+// predecessor has not published, one lane polls that single state, sleeping
+// between reads (128 ns doubling to 1 us), instead of the whole warp
+// re-reading the window; the window is read again once it has published.
+// D0 * 32 states are read in the first round trip, D1 * 32 in each further
+// one.  Bounded like lookback_warp_wide.
+template <int D>
+__device__ __forceinline__ int lb_window_pos(const unsigned long long* states, long long end,
+                                             unsigned long long* sum, long long* empty_at) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  unsigned long long s[D];
+#pragma unroll
+  for (int j = 0; j < D; ++j) {
+    const long long idx = end - (32 * j + lane);
+    s[j] = idx >= 0 ? ld_relaxed_u64(states + idx) : kFlagInc;
+  }
+  int jinc = D, linc = 32, jemp = D, lemp = 32;
+#pragma unroll
+  for (int j = 0; j < D; ++j) {
+    const unsigned f = (unsigned)(s[j] >> 62);
+    const unsigned inc = __ballot_sync(kFull, f == 2);
+    const unsigned emp = __ballot_sync(kFull, f == 0);
+    if (jemp == D && emp) {
+      jemp = j;
+      lemp = __ffs(emp) - 1;
+    }
+    if (jinc == D && inc) {
+      jinc = j;
+      linc = __ffs(inc) - 1;
+    }
+  }
+  // an empty state closer than the nearest inclusive one
+  if (jemp < jinc || (jemp == jinc && jemp < D && lemp < linc)) {
+    *empty_at = end - (32 * jemp + lemp);
+    return kLbEmpty;
+  }
+  unsigned long long part = 0;
+#pragma unroll
+  for (int j = 0; j < D; ++j)
+    if (j < jinc || (j == jinc && lane <= linc)) part += s[j] & kValMask;
+  *sum = warp_sum_u64(part);
+  return jinc < D ? kLbFound : kLbAllAgg;
+}
+
+template <int D0, int D1>
+__device__ __forceinline__ unsigned long long lookback_poll(unsigned long long* states,
+                                                            unsigned long long tile,
+                                                            unsigned long long aggregate,
+                                                            bool* timed_out) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  if (tile == 0) {
+    if (lane == 0) st_relaxed_u64(states, kFlagInc | aggregate);
+    return 0;
+  }
+  if (lane == 0) st_relaxed_u64(states + tile, kFlagAgg | aggregate);
+  unsigned long long excl = 0;
+  long long end = (long long)tile - 1;
+  unsigned spins = 0;
+  bool deep = false, to = false;
+  while (!to) {
+    unsigned long long sum = 0;
+    long long at = 0;
+    const int r = deep ? lb_window_pos<D1>(states, end, &sum, &at)
+                       : lb_window_pos<D0>(states, end, &sum, &at);
+    if (r == kLbEmpty) {
+      unsigned bad = 0;
+      if (lane == 0) {
+        unsigned ns = 128;
+        while ((ld_relaxed_u64(states + at) >> 62) == 0) {
+          if (++spins > kMaxSpins) {
+            bad = 1;
+            break;
+          }
+          __nanosleep(ns);
+          if (ns < 1024) ns <<= 1;
+        }
+      }
+      to = __shfl_sync(kFull, bad, 0) != 0;
+      continue;
+    }
+    excl += sum;
+    if (r == kLbFound) break;
+    end -= deep ? 32 * D1 : 32 * D0;
     deep = true;
   }
   if (to) {

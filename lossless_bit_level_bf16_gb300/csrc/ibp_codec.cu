@@ -219,33 +219,8 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_encode_kernel(IbpEncArgs 
   __threadfence();
   unsigned long long pay = 0;
   if (A.ngroups) pay = ld_acquire_u64(A.states + A.ngroups - 1) & kValMask;
-  const unsigned long long total = A.off_payload + (pay >> 3);
-  unsigned long long* grp = reinterpret_cast<unsigned long long*>(A.out + kIbp1Header);
-  if (t == 0) {
-    grp[A.ngroups] = pay;
-    if (A.out_bytes) *A.out_bytes = total;
-    if (total > A.out_cap) set_status(A.ctrl, ZC_ERR_CAPACITY);
-  }
-  for (unsigned long long p = kIbp1Header + 8ull * (A.ngroups + 1) + t; p < A.off_payload; p += NT)
-    A.out[p] = 0;
-  if (t < 16) {
-    const unsigned long long* mh = reinterpret_cast<const unsigned long long*>(A.meta);
-    unsigned long long h = 0;
-    switch (t) {
-      case 0: h = (unsigned long long)kIbp1Magic | (1ull << 32) | ((unsigned long long)kIbp1Header << 48); break;
-      case 1: h = (unsigned long long)cb | ((unsigned long long)m << 32); break;
-      case 2: h = A.n_bytes; break;
-      case 3: h = A.nchunks; break;
-      case 4: h = A.ngroups; break;
-      case 5: h = mh[6]; break;  // metadata hash
-      case 6: h = kIbp1Header; break;
-      case 7: h = A.off_payload; break;
-      case 8: h = pay; break;
-      case 9: h = total; break;
-      default: h = 0; break;
-    }
-    reinterpret_cast<unsigned long long*>(A.out)[t] = h;
-  }
+  ibp_write_tail(A.meta, cb, m, A.n_bytes, A.nchunks, A.ngroups, A.out, A.out_cap,
+                 A.off_payload, A.out_bytes, A.ctrl, pay, t, NT);
 }
 
 // ------------------------------------------------------------------ decode
@@ -277,33 +252,8 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_decode_kernel(IbpDecArgs 
   uint32_t* gbuf = dyn + ibp_table_words(W);
   const uint32_t m = T.m;
   if (t == 0) {
-    int err = 0;
-    const uint8_t* in = A.in;
-    const unsigned long long* hd = reinterpret_cast<const unsigned long long*>(in);
-    if (!meta_ok) err = ZC_ERR_META_MISMATCH;
-    else if (A.in_bytes < kIbp1Header) err = ZC_ERR_FORMAT;
-    else {
-      for (int i = 0; i < 10; ++i) s_h[i] = hd[i];
-      const unsigned long long h0 = s_h[0], h1 = s_h[1];
-      const unsigned long long n_bytes = s_h[2], nch = s_h[3], ng = s_h[4];
-      const unsigned long long mh = reinterpret_cast<const unsigned long long*>(A.meta)[6];
-      if ((uint32_t)h0 != kIbp1Magic || ((h0 >> 32) & 0xFFFF) != 1 || (h0 >> 48) != kIbp1Header)
-        err = ZC_ERR_FORMAT;
-      else if ((uint32_t)h1 != cb || (uint32_t)(h1 >> 32) != m || s_h[5] != mh)
-        err = ZC_ERR_META_MISMATCH;
-      else if ((n_bytes & 3) || nch != (n_bytes + cb - 1) / cb || ng != (nch + 31) / 32 ||
-               s_h[6] != kIbp1Header || ng > A.in_bytes / 8 ||
-               s_h[7] != kIbp1Header + round_up_dev(8ull * (ng + 1), 128) ||
-               s_h[9] > A.in_bytes || s_h[7] > s_h[9] || (s_h[8] & 127) ||
-               (s_h[8] >> 3) != s_h[9] - s_h[7])
-        err = ZC_ERR_FORMAT;
-      else if (n_bytes > A.y_cap)
-        err = ZC_ERR_CAPACITY;
-      else if (blockIdx.x == 0) {
-        const unsigned long long* grp = reinterpret_cast<const unsigned long long*>(in + kIbp1Header);
-        if (grp[0] != 0 || grp[ng] != s_h[8]) err = ZC_ERR_FORMAT;
-      }
-    }
+    const int err = ibp_check_stream(A.meta, meta_ok, cb, m, A.in, A.in_bytes, A.y_cap,
+                                     blockIdx.x == 0, s_h);
     if (err) set_status(A.ctrl, err);
     s_ok = err == 0;
     s_bad = 0;
@@ -496,6 +446,8 @@ cudaError_t ibp_launch_compress(const void* d_meta, uint32_t cb, const void* d_x
   A.states = reinterpret_cast<unsigned long long*>(static_cast<char*>(d_ws) + kCtrlBytes);
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 8ull * A.ngroups, s);
   if (e != cudaSuccess) return e;
+  if (ibp_pipe_supported(cb, true))
+    return ibp_pipe_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap, d_out_bytes, d_ws, s);
   const bool vec = (cb % 512) == 0;
   switch (wpl_for(cb)) {
     case 4: return vec ? launch_enc<4, 4>(A, s) : launch_enc<1, 4>(A, s);
@@ -518,6 +470,8 @@ cudaError_t ibp_launch_decompress(const void* d_meta, uint32_t cb, const void* d
   A.ctrl = static_cast<Ctrl*>(d_ws);
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes, s);
   if (e != cudaSuccess) return e;
+  if (ibp_pipe_supported(cb, false))
+    return ibp_pipe_decompress(d_meta, cb, d_in, in_bytes, d_y, y_cap, d_ws, s);
   const bool vec = (cb % 512) == 0;
   switch (wpl_for(cb)) {
     case 4: return vec ? launch_dec<4, 4>(A, s) : launch_dec<1, 4>(A, s);

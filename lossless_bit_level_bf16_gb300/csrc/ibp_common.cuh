@@ -136,4 +136,76 @@ __device__ bool ibp_load_tables(const uint8_t* meta, uint32_t chunk_bytes, uint3
   return hdr_ok && T.m == hdr[4];
 }
 
+// Closing step of an IBP encode, run by every thread of the last block to
+// finish once `pay` (payload bits, the scan total) is known: the end of the
+// group-offset table, the output size, zero padding and the 128-byte header.
+__device__ __forceinline__ void ibp_write_tail(const uint8_t* meta, uint32_t cb, uint32_t m,
+                                               unsigned long long n_bytes,
+                                               unsigned long long nchunks,
+                                               unsigned long long ngroups, uint8_t* out,
+                                               unsigned long long out_cap,
+                                               unsigned long long off_payload,
+                                               unsigned long long* out_bytes, Ctrl* ctrl,
+                                               unsigned long long pay, int t, int nt) {
+  const unsigned long long total = off_payload + (pay >> 3);
+  unsigned long long* grp = reinterpret_cast<unsigned long long*>(out + kIbp1Header);
+  if (t == 0) {
+    grp[ngroups] = pay;
+    if (out_bytes) *out_bytes = total;
+    if (total > out_cap) set_status(ctrl, ZC_ERR_CAPACITY);
+  }
+  for (unsigned long long p = kIbp1Header + 8ull * (ngroups + 1) + t; p < off_payload; p += nt)
+    out[p] = 0;
+  if (t < 16) {
+    const unsigned long long* mh = reinterpret_cast<const unsigned long long*>(meta);
+    unsigned long long h = 0;
+    switch (t) {
+      case 0: h = (unsigned long long)kIbp1Magic | (1ull << 32) | ((unsigned long long)kIbp1Header << 48); break;
+      case 1: h = (unsigned long long)cb | ((unsigned long long)m << 32); break;
+      case 2: h = n_bytes; break;
+      case 3: h = nchunks; break;
+      case 4: h = ngroups; break;
+      case 5: h = mh[6]; break;  // metadata hash
+      case 6: h = kIbp1Header; break;
+      case 7: h = off_payload; break;
+      case 8: h = pay; break;
+      case 9: h = total; break;
+      default: h = 0; break;
+    }
+    reinterpret_cast<unsigned long long*>(out)[t] = h;
+  }
+}
+
+// Checks an IBP1 stream header against the metadata (its chunk size, m and
+// hash), the stream length and the output capacity; copies the first ten
+// header words to h.  With check_table the group-offset table's two ends are
+// checked too.  Returns 0 or the error code.  One thread.
+__device__ __forceinline__ int ibp_check_stream(const uint8_t* meta, bool meta_ok, uint32_t cb,
+                                                uint32_t m, const uint8_t* in,
+                                                unsigned long long in_bytes,
+                                                unsigned long long y_cap, bool check_table,
+                                                unsigned long long* h) {
+  if (!meta_ok) return ZC_ERR_META_MISMATCH;
+  if (in_bytes < kIbp1Header) return ZC_ERR_FORMAT;
+  const unsigned long long* hd = reinterpret_cast<const unsigned long long*>(in);
+  for (int i = 0; i < 10; ++i) h[i] = hd[i];
+  const unsigned long long h0 = h[0], h1 = h[1];
+  const unsigned long long n_bytes = h[2], nch = h[3], ng = h[4];
+  const unsigned long long mh = reinterpret_cast<const unsigned long long*>(meta)[6];
+  if ((uint32_t)h0 != kIbp1Magic || ((h0 >> 32) & 0xFFFF) != 1 || (h0 >> 48) != kIbp1Header)
+    return ZC_ERR_FORMAT;
+  if ((uint32_t)h1 != cb || (uint32_t)(h1 >> 32) != m || h[5] != mh) return ZC_ERR_META_MISMATCH;
+  if ((n_bytes & 3) || nch != (n_bytes + cb - 1) / cb || ng != (nch + 31) / 32 ||
+      h[6] != kIbp1Header || ng > in_bytes / 8 ||
+      h[7] != kIbp1Header + round_up_dev(8ull * (ng + 1), 128) || h[9] > in_bytes ||
+      h[7] > h[9] || (h[8] & 127) || (h[8] >> 3) != h[9] - h[7])
+    return ZC_ERR_FORMAT;
+  if (n_bytes > y_cap) return ZC_ERR_CAPACITY;
+  if (check_table) {
+    const unsigned long long* grp = reinterpret_cast<const unsigned long long*>(in + kIbp1Header);
+    if (grp[0] != 0 || grp[ng] != h[8]) return ZC_ERR_FORMAT;
+  }
+  return 0;
+}
+
 }  // namespace lbb

@@ -1,0 +1,971 @@
+// ibp_pipe.cu -- IBP encode and decode for chunks of up to 2048 bytes, with
+// tiles of the input staged into shared memory by TMA bulk copies several
+// tiles ahead of the threads that work on them.
+//
+// [IBP] = "Riepilogo Tecnico: Riduzione del Collo di Bottiglia della Memoria
+// GPU con la Compressione Lossless per il ML", Metodologia: Invariant Bit
+// Packing (IBP), Algoritmo Core, steps 2 (Compressione) and 3
+// (Decompressione).  The stream is the same "IBP1" stream ibp_codec.cu writes
+// and reads (groups of 32 chunks: 32 participation bits, the bodies, zero bits
+// up to a multiple of 128).
+//
+// Tile = Q consecutive groups (Q = 512 / chunk_bytes below 512-byte chunks,
+// else 1), so a tile is about 16 KB of input or more.  A block owns a ring of
+// S shared-memory stages; one thread keeps up to S tiles in flight with
+// cp.async.bulk, each completing on its stage's mbarrier.
+//
+// A thread owns 16-byte vectors of the tile: 4 consecutive words, which never
+// straddle a chunk because chunk_bytes is a multiple of 16.  When the number
+// of vectors per chunk is a power of two dividing the block size, a thread's
+// vectors all sit at the same position r in their chunks, so the Mask tables
+// of its 4 words (keep masks, Bitval, compress/expand move masks) live in
+// registers for the whole kernel (REG); otherwise they are read from shared
+// memory per vector.
+//
+// Encode: three launches (match -> offsets -> pack, described at the encode
+// kernels below).  Packing closes up the kept bits of a vector's 4 words into
+// one run of at most 128 bits and puts it into a shared-memory image of the
+// tile's stream (plain stores for the words the run covers alone, atomicOr
+// for a shared first or last word), which is then copied out with 16-byte
+// stores; a tile in which no chunk participates is copied straight from the
+// stage.  The image holds stream word j at image word j + 3: chunk bodies
+// start 32 bits after a 128-bit aligned group start, so a raw chunk that
+// follows raw chunks lands 16-byte aligned.
+//
+// Decode, per tile: the tile's compressed bytes (its span taken from the
+// stream's group-offset table, checked first) are staged; one warp per group
+// scans the 32 chunk lengths; every thread then reads the <= 128 bits of each
+// of its vectors with two 16-byte shared loads, splits them into the 4 words'
+// fields, expands them, ORs in Bitval and stores 16 bytes.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "ibp_common.cuh"
+#include "internal.h"
+
+namespace lbb {
+namespace {
+
+constexpr uint32_t kMaxStages = 6;
+constexpr uint32_t kMaxQ = 32;
+constexpr uint32_t kStageSlack = 128;  // bytes readable past a stage's data
+
+struct PipeArgs {
+  const uint8_t* meta;
+  const uint32_t* pw;             // encode: participation word of every group
+  const uint8_t* src;             // encode: raw input; decode: the stream
+  unsigned long long src_bytes;   // decode: stream bytes
+  uint8_t* dst;                   // encode: the stream; decode: the output
+  unsigned long long dst_cap;
+  unsigned long long n_bytes, nchunks, ngroups, ntiles, off_payload;
+  unsigned long long* out_bytes;
+  Ctrl* ctrl;
+  unsigned long long* states;
+  uint32_t cb, vpc, lvpc;  // chunk bytes, 16-byte vectors per chunk, log2 (REG)
+  uint32_t Q, S, stage_bytes, img_words;
+};
+
+// Mask tables of the 4 words at vector position r of a chunk.
+struct VecTab {
+  uint32_t K[4], V[4], MV[5][4];
+  uint32_t Pr;  // kept bits of the chunk before this vector
+};
+
+// Kept bits per word of the vector (recomputed: cheaper than registers).
+__device__ __forceinline__ void kept_bits(const VecTab& v, uint32_t k[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) k[j] = __popc(v.K[j]);
+}
+
+__device__ __forceinline__ void load_vectab(const IbpTables& T, uint32_t r, VecTab& v) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w = 4 * r + j;
+    v.K[j] = T.K[w];
+    v.V[j] = T.V[w];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) v.MV[i][j] = T.MV[i * T.W + w];
+  }
+  v.Pr = T.P[4 * r];
+}
+
+// Fields f[0..3] (f[j] has k[j] <= 32 bits) laid end to end, LSB first.
+__device__ __forceinline__ void cat4(const uint32_t f[4], const uint32_t k[4], uint32_t o[4]) {
+  const unsigned long long a = (unsigned long long)f[0] | ((unsigned long long)f[1] << k[0]);
+  const unsigned long long b = (unsigned long long)f[2] | ((unsigned long long)f[3] << k[2]);
+  const uint32_t s = k[0] + k[1];
+  unsigned long long lo, hi;
+  if (s == 0) {
+    lo = b;
+    hi = 0;
+  } else if (s >= 64) {
+    lo = a;
+    hi = b;
+  } else {
+    lo = a | (b << s);
+    hi = b >> (64 - s);
+  }
+  o[0] = (uint32_t)lo;
+  o[1] = (uint32_t)(lo >> 32);
+  o[2] = (uint32_t)hi;
+  o[3] = (uint32_t)(hi >> 32);
+}
+
+// Inverse of cat4: the fields of lengths k[0..3] from the 128 bits u.
+__device__ __forceinline__ void split4(const uint32_t u[4], const uint32_t k[4], uint32_t f[4]) {
+  const unsigned long long lo = (unsigned long long)u[0] | ((unsigned long long)u[1] << 32);
+  const unsigned long long hi = (unsigned long long)u[2] | ((unsigned long long)u[3] << 32);
+  const uint32_t s = k[0] + k[1];
+  f[0] = (uint32_t)(lo & ((1ull << k[0]) - 1ull));
+  f[1] = (uint32_t)((lo >> k[0]) & ((1ull << k[1]) - 1ull));
+  unsigned long long b;
+  if (s == 0) b = lo;
+  else if (s >= 64) b = hi;
+  else b = (lo >> s) | (hi << (64 - s));
+  f[2] = (uint32_t)(b & ((1ull << k[2]) - 1ull));
+  f[3] = (uint32_t)((b >> k[2]) & ((1ull << k[3]) - 1ull));
+}
+
+// OR the run o[0..3] (n <= 128 bits, LSB first, zero above n) into the image
+// at bit pos.  Words the run covers entirely belong to it alone.
+__device__ __forceinline__ void img_put(uint32_t* img, uint32_t pos, const uint32_t o[4],
+                                        uint32_t n) {
+  if (n == 0) return;
+  const uint32_t b = pos >> 5, sh = pos & 31;
+  if (sh == 0 && n == 128 && (b & 3) == 0) {
+    *reinterpret_cast<uint4*>(img + b) = make_uint4(o[0], o[1], o[2], o[3]);
+    return;
+  }
+  uint32_t w[5];
+  w[0] = o[0] << sh;
+  w[1] = __funnelshift_l(o[0], o[1], sh);
+  w[2] = __funnelshift_l(o[1], o[2], sh);
+  w[3] = __funnelshift_l(o[2], o[3], sh);
+  w[4] = sh ? (o[3] >> (32 - sh)) : 0u;
+  const uint32_t end = sh + n, nw = (end + 31) >> 5;
+  const bool tail_part = (end & 31) != 0;
+#pragma unroll
+  for (uint32_t j = 0; j < 5; ++j) {
+    if (j < nw) {
+      const bool part = (j == 0 && sh != 0) || (j == nw - 1 && tail_part);
+      if (part) atomicOr(img + b + j, w[j]);
+      else img[b + j] = w[j];
+    }
+  }
+}
+
+// The 128 bits at bit position pos of a shared-memory bit string, read with
+// two 16-byte loads (the string must be readable 32 bytes past pos / 8).
+__device__ __forceinline__ void win128(const uint32_t* buf, uint32_t pos, uint32_t u[4]) {
+  const uint32_t a = pos >> 5, a4 = a & ~3u, d = a - a4, sh = pos & 31;
+  const uint4 x = *reinterpret_cast<const uint4*>(buf + a4);
+  const uint4 y = *reinterpret_cast<const uint4*>(buf + a4 + 4);
+  const uint32_t q[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+  uint32_t s[5];
+#pragma unroll
+  for (int j = 0; j < 5; ++j) s[j] = d == 0 ? q[j] : (d == 1 ? q[j + 1] : (d == 2 ? q[j + 2] : q[j + 3]));
+#pragma unroll
+  for (int j = 0; j < 4; ++j) u[j] = __funnelshift_r(s[j], s[j + 1], sh);
+}
+
+__host__ __device__ __forceinline__ bool pow2_dev(uint32_t v) { return v && !(v & (v - 1)); }
+inline bool pow2(uint32_t v) { return pow2_dev(v); }
+
+// Tile-local chunk and vector position of vector v.
+template <bool REG>
+__device__ __forceinline__ void vec_pos(const PipeArgs& A, uint32_t v, uint32_t& c, uint32_t& r) {
+  if (REG) {
+    c = v >> A.lvpc;
+    r = v & (A.vpc - 1);
+  } else {
+    c = v / A.vpc;
+    r = v - c * A.vpc;
+  }
+}
+
+// ------------------------------------------------------------------ encode
+//
+// Three launches, none of which waits on another block's progress:
+//   match    reads the input once and writes each group's participation
+//            word (its full chunks whose Mask bits all equal Bitval);
+//   offsets  scans the groups' padded bit lengths into the stream's
+//            group-offset table (tiles of 4096 groups chained by decoupled
+//            look-back: a handful of tiles, so the chain is short);
+//   pack     stages tiles of the input with TMA bulk copies, packs each group
+//            at its now-known offset and writes the header.
+// The match pass costs one extra read of the input; in exchange no tile ever
+// holds its data while it waits for its predecessors' lengths.
+
+struct MatchArgs {
+  const uint8_t* meta;
+  const uint32_t* x;
+  unsigned long long n_bytes, nchunks, ngroups;
+  uint32_t cb, vpc, lvpc;
+  uint32_t* pw;  // out: one participation word per group
+  Ctrl* ctrl;
+};
+
+// MODE 0: vpc <= 32, a power of two: a lane's vectors all sit at position
+//         lane % vpc of their chunks.
+// MODE 1, 2, 4: vpc = 32 * MODE: row i of a step of 8 rows is at positions
+//         lane + 32 * (i % MODE).
+// MODE 3: any other vpc: the tables are read per vector.
+template <int MODE>
+__global__ void __launch_bounds__(256) ibp_match_kernel(MatchArgs A) {
+  extern __shared__ __align__(128) uint8_t dyn[];
+  __shared__ uint32_t s_scr[256 / 32 + 4];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  IbpTables T;
+  const bool ok = ibp_load_tables<256>(A.meta, A.cb, reinterpret_cast<uint32_t*>(dyn), T, s_scr);
+  if (!ok) {
+    if (t == 0) set_status(A.ctrl, ZC_ERR_META_MISMATCH);
+    return;
+  }
+  const uint32_t cb = A.cb, W = cb / 4, vpc = A.vpc, m = T.m;
+  constexpr int NR = (MODE == 1 || MODE == 2 || MODE == 4) ? MODE : 1;
+  uint32_t rK[NR][4], rV[NR][4];
+  if (MODE != 3) {
+#pragma unroll
+    for (int k = 0; k < NR; ++k) {
+      const uint32_t r0 = MODE == 0 ? ((uint32_t)lane & (vpc - 1)) : (uint32_t)lane + 32u * k;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        rK[k][j] = T.K[4 * r0 + j];
+        rV[k][j] = T.V[4 * r0 + j];
+      }
+    }
+  }
+  const unsigned long long total_words = A.n_bytes / 4;
+  const unsigned long long tail_bytes = A.n_bytes - (A.nchunks ? (A.nchunks - 1) * cb : 0ull);
+  const bool short_tail = A.nchunks && tail_bytes != cb;
+  const unsigned long long nwarps = (unsigned long long)gridDim.x * 8;
+  for (unsigned long long g = (unsigned long long)blockIdx.x * 8 + warp; g < A.ngroups; g += nwarps) {
+    const unsigned long long c0 = 32ull * g;
+    const uint32_t nch = (uint32_t)((A.nchunks - c0) < 32 ? (A.nchunks - c0) : 32);
+    const uint32_t* xg = A.x + c0 * W;
+    const uint32_t gwords =
+        (uint32_t)((total_words - c0 * W) < 32ull * W ? (total_words - c0 * W) : 32ull * W);
+    const uint32_t nvec = (gwords + 3) / 4;
+    uint32_t lw = 0;  // bad bits of this lane's vectors, per chunk of the group
+    for (uint32_t v0 = 0; v0 < nvec; v0 += 256) {
+      uint4 d[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t v = v0 + 32 * i + lane;
+        if (4 * v + 3 < gwords) {
+          d[i] = ld_nc_v4(xg + 4 * v);
+        } else {
+          uint32_t w[4];
+#pragma unroll
+          for (uint32_t k = 0; k < 4; ++k) w[k] = 4 * v + k < gwords ? __ldg(xg + 4 * v + k) : 0u;
+          d[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t v = v0 + 32 * i + lane;
+        if (v >= nvec) continue;
+        uint32_t K[4], V[4];
+        if (MODE == 3) {
+          const uint32_t r = v % vpc;
+          const uint4 k4 = *reinterpret_cast<const uint4*>(T.K + 4 * r);
+          const uint4 v4 = *reinterpret_cast<const uint4*>(T.V + 4 * r);
+          K[0] = k4.x; K[1] = k4.y; K[2] = k4.z; K[3] = k4.w;
+          V[0] = v4.x; V[1] = v4.y; V[2] = v4.z; V[3] = v4.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            K[q] = rK[i % NR][q];
+            V[q] = rV[i % NR][q];
+          }
+        }
+        const uint32_t dw[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
+        const uint32_t wv = (gwords - 4 * v) < 4u ? (gwords - 4 * v) : 4u;
+        uint32_t x = 0;
+#pragma unroll
+        for (uint32_t q = 0; q < 4; ++q)
+          if (q < wv) x |= (dw[q] ^ V[q]) & ~K[q];
+        const uint32_t c = MODE == 3 ? v / vpc : v >> A.lvpc;
+        if (x) lw |= 1u << (c & 31);
+      }
+    }
+    const uint32_t bad = __reduce_or_sync(kFull, lw);
+    if (lane == 0) {
+      uint32_t valid = nch >= 32 ? kFull : ((1u << nch) - 1u);
+      if (short_tail && c0 + nch == A.nchunks) valid &= ~(1u << (nch - 1));
+      A.pw[g] = m ? (~bad & valid) : 0u;
+    }
+  }
+}
+
+// Padded bit length of group g with participation word pw.
+__device__ __forceinline__ unsigned long long ibp_group_bits(unsigned long long g, uint32_t pw,
+                                                             unsigned long long nchunks,
+                                                             unsigned long long tail_bytes,
+                                                             uint32_t cb, uint32_t m) {
+  const unsigned long long c0 = 32ull * g;
+  const uint32_t nch = (uint32_t)((nchunks - c0) < 32 ? (nchunks - c0) : 32);
+  unsigned long long bits = 32ull + (unsigned long long)nch * 8ull * cb - (unsigned long long)__popc(pw) * m;
+  if (c0 + nch == nchunks && tail_bytes != cb) bits -= 8ull * (cb - tail_bytes);
+  return round_up_dev(bits, 128);
+}
+
+constexpr int kOffNT = 512, kOffIPT = 8;  // 4096 groups per offsets tile
+
+struct OffArgs {
+  const uint32_t* pw;
+  const uint8_t* meta;
+  unsigned long long n_bytes, nchunks, ngroups, ntiles;
+  uint32_t cb;
+  unsigned long long* grp;  // the stream's group-offset table (ngroups + 1 entries)
+  Ctrl* ctrl;
+  unsigned long long* states;
+};
+
+__global__ void __launch_bounds__(kOffNT) ibp_offsets_kernel(OffArgs A) {
+  __shared__ uint32_t s_wt[kOffNT / 32];
+  __shared__ unsigned long long s_tile, s_excl;
+  const int t = threadIdx.x, warp = t >> 5;
+  const uint32_t m = reinterpret_cast<const uint32_t*>(A.meta)[4];
+  const unsigned long long tail_bytes = A.n_bytes - (A.nchunks ? (A.nchunks - 1) * A.cb : 0ull);
+  if (t == 0) s_tile = atomicAdd(&A.ctrl->ticket, 1ull);
+  __syncthreads();
+  const unsigned long long tile = s_tile;
+  if (tile >= A.ntiles) return;
+  const unsigned long long g0 = tile * (kOffNT * kOffIPT) + (unsigned long long)t * kOffIPT;
+  uint32_t len[kOffIPT];  // group lengths fit 32 bits (chunks of at most 2048 bytes)
+  uint32_t local = 0;
+#pragma unroll
+  for (int i = 0; i < kOffIPT; ++i) {
+    const unsigned long long g = g0 + i;
+    len[i] = g < A.ngroups ? (uint32_t)ibp_group_bits(g, A.pw[g], A.nchunks, tail_bytes, A.cb, m) : 0u;
+    local += len[i];
+  }
+  uint32_t total;
+  const uint32_t excl_local = block_excl_scan<kOffNT>(local, s_wt, &total);
+  if (warp == 0) {
+    bool to = false;
+    const unsigned long long ex = lookback_warp_wide(A.states, tile, total, &to);
+    if (t == 0) {
+      s_excl = ex;
+      if (to) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+    }
+  }
+  __syncthreads();
+  unsigned long long run = s_excl + excl_local;
+#pragma unroll
+  for (int i = 0; i < kOffIPT; ++i) {
+    const unsigned long long g = g0 + i;
+    if (g < A.ngroups) A.grp[g] = run;
+    run += len[i];
+    if (g + 1 == A.ngroups) A.grp[A.ngroups] = run;
+  }
+}
+
+template <int NT, bool REG>
+__global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
+  constexpr int NW = NT / 32;
+  extern __shared__ __align__(128) uint8_t dyn[];
+  __shared__ uint32_t s_scr[NW + 4];
+  __shared__ unsigned long long s_tile[kMaxStages];
+  __shared__ uint32_t s_pw[kMaxQ], s_gex[kMaxQ];
+  __shared__ unsigned long long s_base;
+  __shared__ uint32_t s_agg;
+  __shared__ int s_raw, s_last;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t cb = A.cb, W = cb / 4, B = 8 * cb, Q = A.Q, S = A.S;
+
+  uint32_t* tab = reinterpret_cast<uint32_t*>(dyn);
+  uint8_t* stages = dyn + 4 * ibp_table_words(W);
+  uint32_t* img = reinterpret_cast<uint32_t*>(stages + (size_t)S * A.stage_bytes);
+  uint4* img4 = reinterpret_cast<uint4*>(img);
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(img + A.img_words);
+  const unsigned long long* grp = reinterpret_cast<const unsigned long long*>(A.dst + kIbp1Header);
+
+  IbpTables T;
+  const bool ok = ibp_load_tables<NT>(A.meta, cb, tab, T, s_scr);
+  const uint32_t m = T.m;
+  const unsigned long long tile_raw = 32ull * Q * cb;
+  const uint32_t gvec = 8 * W + 1;  // 16-byte vectors of a full group stored raw
+
+  VecTab vt;
+  if (REG) load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
+  for (uint32_t i = t; i < A.img_words / 4; i += NT) img4[i] = make_uint4(0, 0, 0, 0);
+
+  // thread 0: start the copy of this block's kk-th tile into stage s
+  auto issue = [&](unsigned long long kk, uint32_t s) {
+    const unsigned long long tile = ok ? blockIdx.x + kk * gridDim.x : A.ntiles;
+    s_tile[s] = tile;
+    if (tile >= A.ntiles) return;
+    const unsigned long long b0 = tile * tile_raw;
+    const unsigned long long tb = (A.n_bytes - b0) < tile_raw ? (A.n_bytes - b0) : tile_raw;
+    const uint32_t b16 = (uint32_t)(tb & ~15ull);
+    uint8_t* st = stages + (size_t)s * A.stage_bytes;
+    for (uint32_t w = b16 / 4; w < (uint32_t)(tb / 4); ++w)  // the last 4..12 bytes
+      reinterpret_cast<uint32_t*>(st)[w] = __ldg(reinterpret_cast<const uint32_t*>(A.src + b0) + w);
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bars + s, b16);
+    if (b16) bulk_g2s(st, A.src + b0, b16, bars + s);
+  };
+  if (t == 0) {
+    for (uint32_t s = 0; s < S; ++s) mbar_init(bars + s, 1);
+    for (uint32_t s = 0; s < S; ++s) issue(s, s);
+  }
+  __syncthreads();
+
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t s = k % S;
+    const unsigned long long tile = s_tile[s];
+    if (tile >= A.ntiles) break;
+    if (!mbar_wait(bars + s, (k / S) & 1)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+    const uint32_t* sd = reinterpret_cast<const uint32_t*>(stages + (size_t)s * A.stage_bytes);
+    const unsigned long long g0 = tile * Q, b0 = tile * tile_raw;
+    const uint32_t nq = (uint32_t)((A.ngroups - g0) < Q ? (A.ngroups - g0) : Q);
+    const uint32_t tb = (uint32_t)((A.n_bytes - b0) < tile_raw ? (A.n_bytes - b0) : tile_raw);
+    const uint32_t twords = tb / 4, nvec = (tb + 15) / 16;
+    if (warp == 0) {
+      const uint32_t pw = (uint32_t)lane < nq ? A.pw[g0 + lane] : 0u;
+      const unsigned long long go = (uint32_t)lane < nq ? grp[g0 + lane] : 0ull;
+      const unsigned long long base = __shfl_sync(kFull, go, 0);
+      const bool raw = __ballot_sync(kFull, pw != 0) == 0;
+      if ((uint32_t)lane < nq) {
+        s_pw[lane] = pw;
+        s_gex[lane] = (uint32_t)(go - base);
+      }
+      if (lane == 0) {
+        s_base = base;
+        s_agg = (uint32_t)(grp[g0 + nq] - base);
+        s_raw = raw;
+      }
+    }
+    __syncthreads();
+    const bool raw = s_raw != 0;
+    const unsigned long long dst = A.off_payload + (s_base >> 3);
+    const uint32_t nv = s_agg >> 7;  // 16-byte vectors of the tile's stream
+    const bool fits = dst + 16ull * nv <= A.dst_cap;
+    if (!fits && t == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
+    if (raw) {
+      // [0][input words][zero padding] per group, straight from the stage
+      for (uint32_t u0 = t; u0 < nv; u0 += 4 * NT) {
+        uint4 o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t u = u0 + e * NT;
+          if (u >= nv) continue;
+          const uint32_t q = Q == 1 ? 0u : u / gvec, lu = u - q * gvec;
+          const uint32_t ib = q * 32u * W;  // group's first input word in the stage
+          const uint32_t bw = (q + 1 == nq) ? twords - ib : 32u * W;
+          if (lu > 0 && 4 * lu + 3 <= bw) {
+            const uint4 x = *reinterpret_cast<const uint4*>(sd + ib + 4 * lu);
+            o[e] = make_uint4(sd[ib + 4 * lu - 1], x.x, x.y, x.z);
+          } else {
+            uint32_t w[4];
+#pragma unroll
+            for (uint32_t kk = 0; kk < 4; ++kk) {
+              const uint32_t ow = 4 * lu + kk;  // word of the group's stream
+              w[kk] = (ow >= 1 && ow - 1 < bw) ? sd[ib + ow - 1] : 0u;
+            }
+            o[e] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        if (fits) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t u = u0 + e * NT;
+            if (u < nv) st_v4(A.dst + dst + 16ull * u, o[e]);
+          }
+        }
+      }
+    } else {
+      if ((uint32_t)t < nq) img[3 + (s_gex[t] >> 5)] = s_pw[t];
+      for (uint32_t v = t; v < nvec; v += NT) {
+        uint32_t c, r;
+        vec_pos<REG>(A, v, c, r);
+        const uint32_t q = c >> 5, i = c & 31;
+        const uint32_t pwq = s_pw[q];
+        if (!REG) load_vectab(T, r, vt);
+        const uint4 d = *reinterpret_cast<const uint4*>(sd + 4 * v);
+        const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+        const uint32_t off = s_gex[q] + 32u + i * B - (uint32_t)__popc(pwq & ((1u << i) - 1u)) * m;
+        uint32_t o[4], n, pos;
+        if ((pwq >> i) & 1u) {
+          uint32_t f[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) f[w] = hd_compress(dw[w], vt.K[w], &vt.MV[0][w], 4);
+          uint32_t kk[4];
+          kept_bits(vt, kk);
+          cat4(f, kk, o);
+          n = kk[0] + kk[1] + kk[2] + kk[3];
+          pos = off + vt.Pr;
+        } else {
+          const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
+#pragma unroll
+          for (uint32_t w = 0; w < 4; ++w) o[w] = w < wv ? dw[w] : 0u;
+          n = 32u * wv;
+          pos = off + 128u * r;
+        }
+        img_put(img, 96u + pos, o, n);
+      }
+      __syncthreads();
+      if (fits) {
+        for (uint32_t u0 = t; u0 < nv; u0 += 4 * NT) {
+          uint4 o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t u = u0 + e * NT;
+            if (u < nv) {
+              const uint4 x = img4[u + 1];
+              o[e] = make_uint4(img[4 * u + 3], x.x, x.y, x.z);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t u = u0 + e * NT;
+            if (u < nv) st_v4(A.dst + dst + 16ull * u, o[e]);
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (t == 0) issue(k + S, s);
+    if (!raw)  // ordered before the next tile's packing by its first barrier
+      for (uint32_t u = t; u <= nv; u += NT) img4[u] = make_uint4(0, 0, 0, 0);
+  }
+
+  // ---- last block: header and table end
+  __syncthreads();
+  if (t == 0) {
+    __threadfence();
+    const unsigned long long dn = atomicAdd(&A.ctrl->done, 1ull);
+    s_last = (dn == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const unsigned long long pay = A.ngroups ? grp[A.ngroups] : 0ull;
+  ibp_write_tail(A.meta, cb, m, A.n_bytes, A.nchunks, A.ngroups, A.dst, A.dst_cap, A.off_payload,
+                 A.out_bytes, A.ctrl, pay, t, NT);
+}
+
+template <int NT, bool REG>
+__global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs A) {
+  constexpr int NW = NT / 32;
+  extern __shared__ __align__(128) uint8_t dyn[];
+  __shared__ uint32_t s_scr[NW + 4];
+  __shared__ unsigned long long s_h[10];
+  __shared__ int s_ok;
+  __shared__ unsigned long long s_tile[kMaxStages];
+  __shared__ unsigned long long s_goff[kMaxStages][kMaxQ + 1];
+  __shared__ int s_sbad[kMaxStages];
+  __shared__ uint32_t s_pw[kMaxQ];
+  __shared__ int s_gbad[kMaxQ];
+  __shared__ uint32_t s_off[kMaxQ][32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t cb = A.cb, W = cb / 4, B = 8 * cb, Q = A.Q, S = A.S;
+
+  uint32_t* tab = reinterpret_cast<uint32_t*>(dyn);
+  uint8_t* stages = dyn + 4 * ibp_table_words(W);
+  unsigned long long* bars =
+      reinterpret_cast<unsigned long long*>(stages + (size_t)S * A.stage_bytes);
+
+  IbpTables T;
+  const bool meta_ok = ibp_load_tables<NT>(A.meta, cb, tab, T, s_scr);
+  const uint32_t m = T.m;
+  if (t == 0) {
+    const int err = ibp_check_stream(A.meta, meta_ok, cb, m, A.src, A.src_bytes, A.dst_cap,
+                                     blockIdx.x == 0, s_h);
+    if (err) set_status(A.ctrl, err);
+    s_ok = err == 0;
+    for (uint32_t s = 0; s < S; ++s) mbar_init(bars + s, 1);
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  const unsigned long long n_bytes = s_h[2], nchunks = s_h[3], ngroups = s_h[4];
+  const unsigned long long off_payload = s_h[7], pay_bits = s_h[8];
+  const unsigned long long ntiles = (ngroups + Q - 1) / Q;
+  const unsigned long long tail_bytes = n_bytes - (nchunks ? (nchunks - 1) * cb : 0ull);
+  const unsigned long long tile_raw = 32ull * Q * cb;
+  const unsigned long long* grp = reinterpret_cast<const unsigned long long*>(A.src + kIbp1Header);
+  const uint32_t cap = A.stage_bytes - kStageSlack;
+
+  VecTab vt;
+  if (REG) load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
+
+  // warp 0: the span of this block's kk-th tile, checked, then its copy
+  auto issue = [&](unsigned long long kk, uint32_t s) {
+    const unsigned long long tile = blockIdx.x + kk * gridDim.x;
+    if (tile >= ntiles) {
+      if (lane == 0) s_tile[s] = tile;
+      return;
+    }
+    const unsigned long long g0 = tile * Q;
+    const uint32_t nq = (uint32_t)((ngroups - g0) < Q ? (ngroups - g0) : Q);
+    const unsigned long long gend = grp[g0 + nq];
+    const unsigned long long go = (uint32_t)lane < nq ? grp[g0 + lane] : gend;
+    const unsigned long long nx0 = __shfl_down_sync(kFull, go, 1);
+    const unsigned long long nx = (uint32_t)lane + 1 < nq ? nx0 : gend;
+    bool bad = false;
+    if ((uint32_t)lane < nq) bad = (go & 127) != 0 || nx < go + 128 || nx > pay_bits;
+    const unsigned long long first = __shfl_sync(kFull, go, 0);
+    bad = __any_sync(kFull, bad) || ((gend - first) >> 3) > cap;
+    if ((uint32_t)lane < nq) s_goff[s][lane] = go;
+    if (lane == 0) {
+      s_goff[s][nq] = gend;
+      s_tile[s] = tile;
+      s_sbad[s] = bad;
+      fence_proxy_async_smem();
+      if (bad) {
+        mbar_arrive_expect_tx(bars + s, 0);  // nothing to copy: the phase completes now
+      } else {
+        const uint32_t bytes = (uint32_t)((gend - first) >> 3);
+        mbar_arrive_expect_tx(bars + s, bytes);
+        bulk_g2s(stages + (size_t)s * A.stage_bytes, A.src + off_payload + (first >> 3), bytes,
+                 bars + s);
+      }
+    }
+  };
+  if (warp == 0)
+    for (uint32_t s = 0; s < S; ++s) issue(s, s);
+  __syncthreads();
+
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t s = k % S;
+    const unsigned long long tile = s_tile[s];
+    if (tile >= ntiles) break;
+    const bool waited = mbar_wait(bars + s, (k / S) & 1);
+    if (!waited) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+    const uint32_t* sd = reinterpret_cast<const uint32_t*>(stages + (size_t)s * A.stage_bytes);
+    const unsigned long long g0 = tile * Q, b0 = tile * tile_raw;
+    const uint32_t nq = (uint32_t)((ngroups - g0) < Q ? (ngroups - g0) : Q);
+    const uint32_t tb = (uint32_t)((n_bytes - b0) < tile_raw ? (n_bytes - b0) : tile_raw);
+    const uint32_t twords = tb / 4, nvec = (tb + 15) / 16;
+    const bool sbad = s_sbad[s] != 0 || !waited;
+    const unsigned long long base = s_goff[s][0];
+    for (uint32_t q = warp; q < nq; q += NW) {
+      const uint32_t gs = (uint32_t)(s_goff[s][q] - base), ge = (uint32_t)(s_goff[s][q + 1] - base);
+      const uint32_t pw = sbad ? 0u : sd[gs >> 5];
+      const unsigned long long c = (g0 + q) * 32ull + lane;
+      const bool present = c < nchunks;
+      const bool full = present && (c + 1 < nchunks || tail_bytes == cb);
+      const bool p = (pw >> lane) & 1u;
+      bool bad = sbad || (p && (!full || m == 0));
+      const uint32_t len = !present ? 0u : (p ? B - m : (full ? B : 8u * (uint32_t)tail_bytes));
+      uint32_t inc = len;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += u;
+      }
+      s_off[q][lane] = gs + 32u + inc - len;
+      const uint32_t tot = __shfl_sync(kFull, inc, 31);
+      if (round_up_dev(32ull + tot, 128) != (unsigned long long)(ge - gs)) bad = true;
+      bad = __any_sync(kFull, bad);
+      if (lane == 0) {
+        s_pw[q] = pw;
+        s_gbad[q] = bad;
+      }
+    }
+    __syncthreads();
+    uint32_t* yt = reinterpret_cast<uint32_t*>(A.dst + b0);
+    for (uint32_t v = t; v < nvec; v += NT) {
+      uint32_t c, r;
+      vec_pos<REG>(A, v, c, r);
+      const uint32_t q = c >> 5, i = c & 31;
+      if (s_gbad[q]) continue;
+      if (!REG) load_vectab(T, r, vt);
+      const uint32_t off = s_off[q][i];
+      uint32_t u[4], o[4];
+      if ((s_pw[q] >> i) & 1u) {
+        win128(sd, off + vt.Pr, u);
+        uint32_t f[4];
+        uint32_t kk[4];
+        kept_bits(vt, kk);
+        split4(u, kk, f);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) o[w] = hd_expand(f[w], vt.K[w], &vt.MV[0][w], 4) | vt.V[w];
+      } else {
+        win128(sd, off + 128u * r, u);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) o[w] = u[w];
+      }
+      const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
+      if (wv == 4) {
+        st_v4(yt + 4 * v, make_uint4(o[0], o[1], o[2], o[3]));
+      } else {
+#pragma unroll
+        for (uint32_t w = 0; w < 4; ++w)
+          if (w < wv) yt[4 * v + w] = o[w];
+      }
+    }
+    if ((uint32_t)t < nq && s_gbad[t]) set_status(A.ctrl, ZC_ERR_FORMAT);
+    __syncthreads();
+    if (warp == 0) issue(k + S, s);
+  }
+}
+
+// ------------------------------------------------------------------ launch
+
+struct Geo {
+  bool ok;
+  int nt;   // decode: threads per block; encode: packer warps
+  bool reg;
+  uint32_t Q, S, stage_bytes, img_words;
+  size_t smem;
+};
+
+constexpr size_t kSmemPerSm = 233472;     // shared memory per SM
+constexpr size_t kSmemPerBlock = 232448;  // most one block may use
+constexpr size_t kSmemReserved = 1024;    // the system's share per resident block
+
+template <typename K>
+void attrs(K k, size_t* stat, int* regs) {
+  cudaFuncAttributes a{};
+  cudaFuncGetAttributes(&a, k);
+  *stat = a.sharedSizeBytes;
+  *regs = a.numRegs;
+}
+
+void tile_shape(uint32_t cb, bool enc, Geo& g) {
+  g.Q = cb >= 512 ? 1u : std::min<uint32_t>(kMaxQ, 512u / cb);
+  const uint64_t raw = 32ull * g.Q * cb;
+  const uint64_t maxc = (uint64_t)g.Q * (32ull * cb + 16ull);  // largest compressed tile
+  g.stage_bytes = (uint32_t)(round_up(enc ? raw : maxc, 128) + kStageSlack);
+  g.img_words = enc ? (uint32_t)round_up(raw / 4 + 4ull * g.Q + 16, 4) : 0u;
+}
+
+// Stages that fit `blocks` resident blocks per SM (0 if fewer than 2).
+uint32_t stages_for(int blocks, size_t stat, size_t fixed, uint32_t stage_bytes) {
+  const size_t per = std::min(kSmemPerSm / blocks - kSmemReserved, kSmemPerBlock);
+  if (per <= stat + fixed) return 0;
+  const size_t st = std::min<size_t>((per - stat - fixed) / stage_bytes, kMaxStages);
+  return st >= 2 ? (uint32_t)st : 0u;
+}
+
+// Encode (the pack kernel): the smallest block (most blocks per SM, each with
+// its own pipeline) whose shared memory holds the image and at least 2 stages.
+Geo pick_enc(uint32_t cb) {
+  Geo g{};
+  tile_shape(cb, true, g);
+  const uint32_t vpc = cb / 16;
+  const size_t fixed = 4 * ibp_table_words(cb / 4) + 4ull * g.img_words + 8 * kMaxStages;
+  for (int nt : {128, 256, 512}) {
+    size_t stat = 0, s2 = 0;
+    int regs = 0, r2 = 0;
+    if (nt == 128) {
+      attrs(ibp_pack_kernel<128, true>, &stat, &regs);
+      attrs(ibp_pack_kernel<128, false>, &s2, &r2);
+    } else if (nt == 256) {
+      attrs(ibp_pack_kernel<256, true>, &stat, &regs);
+      attrs(ibp_pack_kernel<256, false>, &s2, &r2);
+    } else {
+      attrs(ibp_pack_kernel<512, true>, &stat, &regs);
+      attrs(ibp_pack_kernel<512, false>, &s2, &r2);
+    }
+    const uint32_t st = stages_for(512 / nt, std::max(stat, s2), fixed, g.stage_bytes);
+    if (st) {
+      g.ok = true;
+      g.nt = nt;
+      g.reg = pow2(vpc) && (uint32_t)nt % vpc == 0;
+      g.S = st;
+      g.smem = fixed + st * g.stage_bytes;
+      return g;
+    }
+  }
+  return g;
+}
+
+// Decode: the smallest block (most blocks per SM, each with its own
+// pipeline) whose shared memory holds at least 2 stages.
+Geo pick_dec(uint32_t cb) {
+  Geo g{};
+  tile_shape(cb, false, g);
+  const uint32_t vpc = cb / 16;
+  const size_t fixed = 4 * ibp_table_words(cb / 4) + 8 * kMaxStages;
+  for (int nt : {128, 256, 512}) {
+    size_t stat = 0, s2 = 0;
+    int regs = 0, r2 = 0;
+    if (nt == 128) {
+      attrs(ibp_decode_pipe_kernel<128, true>, &stat, &regs);
+      attrs(ibp_decode_pipe_kernel<128, false>, &s2, &r2);
+    } else if (nt == 256) {
+      attrs(ibp_decode_pipe_kernel<256, true>, &stat, &regs);
+      attrs(ibp_decode_pipe_kernel<256, false>, &s2, &r2);
+    } else {
+      attrs(ibp_decode_pipe_kernel<512, true>, &stat, &regs);
+      attrs(ibp_decode_pipe_kernel<512, false>, &s2, &r2);
+    }
+    const uint32_t st = stages_for(512 / nt, std::max(stat, s2), fixed, g.stage_bytes);
+    if (st) {
+      g.ok = true;
+      g.nt = nt;
+      g.reg = pow2(vpc) && (uint32_t)nt % vpc == 0;
+      g.S = st;
+      g.smem = fixed + st * g.stage_bytes;
+      return g;
+    }
+  }
+  return g;
+}
+
+Geo pick(uint32_t cb, bool enc) {
+  static std::mutex mu;
+  static Geo cache[2][2048 / 16 + 1];
+  static bool have[2][2048 / 16 + 1];
+  if (cb == 0 || cb > 2048 || cb % 16) return Geo{};
+  std::lock_guard<std::mutex> lk(mu);
+  const int e = enc ? 1 : 0, i = (int)(cb / 16);
+  if (!have[e][i]) {
+    cache[e][i] = enc ? pick_enc(cb) : pick_dec(cb);
+    have[e][i] = true;
+  }
+  return cache[e][i];
+}
+
+template <typename K, typename Args>
+cudaError_t launch(K k, int nt, const Args& A, size_t smem, unsigned long long work,
+                   cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int res = resident_blocks((const void*)k, nt, smem);
+  unsigned long long grid = work < (unsigned long long)res ? work : (unsigned long long)res;
+  if (grid == 0) grid = 1;
+  k<<<(unsigned)grid, nt, smem, s>>>(A);
+  return cudaGetLastError();
+}
+
+template <typename K>
+cudaError_t launch(K k, int nt, const PipeArgs& A, const Geo& g, unsigned long long work,
+                   cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
+  if (e != cudaSuccess) return e;
+  const int res = resident_blocks((const void*)k, nt, g.smem);
+  unsigned long long grid = work < (unsigned long long)res ? work : (unsigned long long)res;
+  if (grid == 0) grid = 1;
+  k<<<(unsigned)grid, nt, g.smem, s>>>(A);
+  return cudaGetLastError();
+}
+
+void fill_shape(PipeArgs& A, const Geo& g) {
+  A.vpc = A.cb / 16;
+  A.lvpc = 0;
+  while ((1u << A.lvpc) < A.vpc) ++A.lvpc;
+  A.Q = g.Q;
+  A.S = g.S;
+  A.stage_bytes = g.stage_bytes;
+  A.img_words = g.img_words;
+}
+
+}  // namespace
+
+bool ibp_pipe_supported(uint32_t cb, bool encode) { return cb <= 2048 && pick(cb, encode).ok; }
+
+cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t cb, const void* d_x,
+                              unsigned long long n_bytes, void* d_out, unsigned long long out_cap,
+                              unsigned long long* d_out_bytes, void* d_ws, cudaStream_t s) {
+  const Geo g = pick(cb, true);
+  const unsigned long long nchunks = (n_bytes + cb - 1) / cb, ngroups = (nchunks + 31) / 32;
+  const unsigned long long ntiles2 = (ngroups + kOffNT * kOffIPT - 1) / (kOffNT * kOffIPT);
+  // workspace: control block | offsets-pass look-back states | participation words
+  char* ws = static_cast<char*>(d_ws);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws);
+  unsigned long long* states = reinterpret_cast<unsigned long long*>(ws + kCtrlBytes);
+  uint32_t* pw = reinterpret_cast<uint32_t*>(ws + kCtrlBytes + round_up(8ull * ntiles2, 256));
+  cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 8ull * ntiles2, s);
+  if (e != cudaSuccess) return e;
+  unsigned long long* grp =
+      reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(d_out) + kIbp1Header);
+  if (ngroups) {
+    MatchArgs M{};
+    M.meta = static_cast<const uint8_t*>(d_meta);
+    M.x = static_cast<const uint32_t*>(d_x);
+    M.n_bytes = n_bytes;
+    M.nchunks = nchunks;
+    M.ngroups = ngroups;
+    M.cb = cb;
+    M.vpc = cb / 16;
+    M.lvpc = 0;
+    while ((1u << M.lvpc) < M.vpc) ++M.lvpc;
+    M.pw = pw;
+    M.ctrl = ctrl;
+    const size_t msmem = 4 * ibp_table_words(cb / 4);
+    const unsigned long long mwork = (ngroups + 7) / 8;
+    const int mode = !pow2(M.vpc) ? 3 : (M.vpc <= 32 ? 0 : (int)(M.vpc / 32));
+    switch (mode) {
+      case 0: e = launch(ibp_match_kernel<0>, 256, M, msmem, mwork, s); break;
+      case 2: e = launch(ibp_match_kernel<2>, 256, M, msmem, mwork, s); break;
+      case 4: e = launch(ibp_match_kernel<4>, 256, M, msmem, mwork, s); break;
+      default: e = launch(ibp_match_kernel<3>, 256, M, msmem, mwork, s); break;
+    }
+    if (e != cudaSuccess) return e;
+    OffArgs O{};
+    O.pw = pw;
+    O.meta = static_cast<const uint8_t*>(d_meta);
+    O.n_bytes = n_bytes;
+    O.nchunks = nchunks;
+    O.ngroups = ngroups;
+    O.ntiles = ntiles2;
+    O.cb = cb;
+    O.grp = grp;
+    O.ctrl = ctrl;
+    O.states = states;
+    ibp_offsets_kernel<<<(unsigned)ntiles2, kOffNT, 0, s>>>(O);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  PipeArgs A{};
+  A.meta = static_cast<const uint8_t*>(d_meta);
+  A.pw = pw;
+  A.src = static_cast<const uint8_t*>(d_x);
+  A.dst = static_cast<uint8_t*>(d_out);
+  A.dst_cap = out_cap;
+  A.n_bytes = n_bytes;
+  A.cb = cb;
+  A.nchunks = nchunks;
+  A.ngroups = ngroups;
+  A.ntiles = (ngroups + g.Q - 1) / g.Q;
+  A.off_payload = kIbp1Header + round_up(8ull * (ngroups + 1), 128);
+  A.out_bytes = d_out_bytes;
+  A.ctrl = ctrl;
+  fill_shape(A, g);
+  const unsigned long long w = A.ntiles;
+  if (g.nt == 128)
+    return g.reg ? launch(ibp_pack_kernel<128, true>, 128, A, g, w, s)
+                 : launch(ibp_pack_kernel<128, false>, 128, A, g, w, s);
+  if (g.nt == 256)
+    return g.reg ? launch(ibp_pack_kernel<256, true>, 256, A, g, w, s)
+                 : launch(ibp_pack_kernel<256, false>, 256, A, g, w, s);
+  return g.reg ? launch(ibp_pack_kernel<512, true>, 512, A, g, w, s)
+               : launch(ibp_pack_kernel<512, false>, 512, A, g, w, s);
+}
+
+cudaError_t ibp_pipe_decompress(const void* d_meta, uint32_t cb, const void* d_in,
+                                unsigned long long in_bytes, void* d_y, unsigned long long y_cap,
+                                void* d_ws, cudaStream_t s) {
+  const Geo g = pick(cb, false);
+  PipeArgs A{};
+  A.meta = static_cast<const uint8_t*>(d_meta);
+  A.src = static_cast<const uint8_t*>(d_in);
+  A.src_bytes = in_bytes;
+  A.dst = static_cast<uint8_t*>(d_y);
+  A.dst_cap = y_cap;
+  A.cb = cb;
+  A.ctrl = static_cast<Ctrl*>(d_ws);
+  // the tile count is only known once the header is read on the device: the
+  // grid is sized for the largest stream that fits y_cap
+  const unsigned long long nch = (y_cap + cb - 1) / cb, ng = (nch + 31) / 32;
+  const unsigned long long w = (ng + g.Q - 1) / g.Q;
+  fill_shape(A, g);
+  if (g.nt == 128)
+    return g.reg ? launch(ibp_decode_pipe_kernel<128, true>, 128, A, g, w, s)
+                 : launch(ibp_decode_pipe_kernel<128, false>, 128, A, g, w, s);
+  if (g.nt == 256)
+    return g.reg ? launch(ibp_decode_pipe_kernel<256, true>, 256, A, g, w, s)
+                 : launch(ibp_decode_pipe_kernel<256, false>, 256, A, g, w, s);
+  return g.reg ? launch(ibp_decode_pipe_kernel<512, true>, 512, A, g, w, s)
+               : launch(ibp_decode_pipe_kernel<512, false>, 512, A, g, w, s);
+}
+
+}  // namespace lbb

@@ -78,6 +78,17 @@ cudaError_t ibp_launch_decompress(const void* d_meta, uint32_t chunk_bytes,
                                   void* d_y, unsigned long long y_cap,
                                   void* d_ws, cudaStream_t s);
 
+// TMA-pipelined IBP kernels (ibp_pipe.cu) for chunks of up to 2048 bytes;
+// the launchers above use them whenever ibp_pipe_supported says so.
+bool ibp_pipe_supported(uint32_t chunk_bytes, bool encode);
+cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t chunk_bytes, const void* d_x,
+                              unsigned long long n_bytes, void* d_out,
+                              unsigned long long out_cap, unsigned long long* d_out_bytes,
+                              void* d_ws, cudaStream_t s);
+cudaError_t ibp_pipe_decompress(const void* d_meta, uint32_t chunk_bytes, const void* d_in,
+                                unsigned long long in_bytes, void* d_y,
+                                unsigned long long y_cap, void* d_ws, cudaStream_t s);
+
 // Blocks of `kernel` resident per SM times SMs on the current device.
 int resident_blocks(const void* kernel, int threads, size_t smem);
 

@@ -13,6 +13,9 @@
 //   zc_predict_kernel  one block per segment: adds the unit partials in a
 //                      fixed order, forms mu and sigma, evaluates the Gaussian
 //                      mass of every exponent field and keeps the 7 largest.
+//                      fp64 is slow on this part, so each field edge's erfc
+//                      pair is computed once and the masses are ranked as
+//                      integers (their fp64 bit patterns).
 //
 // Arithmetic of the statistics pass: the 16 values a thread holds are summed
 // (and their squares, exact in fp32 for bf16 inputs) as an fp32 tree (error
@@ -181,17 +184,24 @@ __global__ void __launch_bounds__(kThreads) zc_stats_kernel(
   }
 }
 
-// Gaussian mass of exponent field f: P(2^(f-127) <= |X| < 2^(f-126)),
-// X ~ N(mu, sigma), both signs, in fp64 with every operation rounded on its
-// own (no fused multiply-add) so the result does not depend on contraction.
-__device__ double field_mass(double mu, double sigma, int f) {
-  double a = ldexp(1.0, f - 127);
-  double b = ldexp(1.0, f - 126);
-  double s = __dmul_rn(sigma, 1.4142135623730951);  // sigma * sqrt(2)
-  double pos = __dmul_rn(0.5, __dsub_rn(erfc(__ddiv_rn(__dsub_rn(a, mu), s)),
-                                        erfc(__ddiv_rn(__dsub_rn(b, mu), s))));
-  double neg = __dmul_rn(0.5, __dsub_rn(erfc(__ddiv_rn(__dadd_rn(a, mu), s)),
-                                        erfc(__ddiv_rn(__dadd_rn(b, mu), s))));
+// Gaussian mass of exponent field f, P(2^(f-127) <= |X| < 2^(f-126)) for
+// X ~ N(mu, sigma), is a difference of complementary error functions at the
+// field's two edges, for both signs.  Field f's upper edge is field f+1's
+// lower edge, so the erfc terms are evaluated once per edge e = 2^(k-127),
+// k = 1..255:  em = erfc((e - mu)/s),  ep = erfc((e + mu)/s),  s = sigma*sqrt(2).
+// fp64, every operation rounded on its own (no fused multiply-add), so the
+// result does not depend on contraction.
+__device__ void edge_erfc(double mu, double sigma, int k, double* em, double* ep) {
+  const double e = ldexp(1.0, k - 127);
+  const double s = __dmul_rn(sigma, 1.4142135623730951);  // sigma * sqrt(2)
+  *em = erfc(__ddiv_rn(__dsub_rn(e, mu), s));
+  *ep = erfc(__ddiv_rn(__dadd_rn(e, mu), s));
+}
+
+// mass(f) from the edge terms of edges f and f+1; masses below 1e-300 read as 0.
+__device__ double field_mass(const double* em, const double* ep, int f) {
+  const double pos = __dmul_rn(0.5, __dsub_rn(em[f], em[f + 1]));
+  const double neg = __dmul_rn(0.5, __dsub_rn(ep[f], ep[f + 1]));
   double m = __dadd_rn(pos, neg);
   if (!(m >= 1e-300)) m = 0.0;
   return m;
@@ -212,7 +222,8 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
   __shared__ double s_r1[kThreads / 32], s_r2[kThreads / 32];
   __shared__ unsigned long long s_rc[kThreads / 32];
   __shared__ double s_mu, s_sigma;
-  __shared__ double s_mass[256];
+  __shared__ double s_em[256], s_ep[256];
+  __shared__ unsigned long long s_key[256];
   __shared__ int s_take[256];
   const int t = threadIdx.x;
   const uint32_t sg = blockIdx.x;
@@ -268,15 +279,19 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
     }
     return;
   }
-  // one field per thread (threads 1..254)
-  s_mass[t] = (t >= 1 && t <= 254) ? field_mass(mu, sigma, t) : -1.0;
+  // edge terms, one edge per thread (threads 1..255)
+  if (t >= 1 && t <= 255) edge_erfc(mu, sigma, t, &s_em[t], &s_ep[t]);
+  __syncthreads();
+  // Masses are finite and >= 0 (+0 below the cut-off), so their fp64 bit
+  // patterns order like the values: the ranking compares 64-bit integers.
+  s_key[t] = (t >= 1 && t <= 254) ? (unsigned long long)__double_as_longlong(field_mass(s_em, s_ep, t)) : 0ull;
   __syncthreads();
   int take = 0;
   if (t >= 1 && t <= 254) {
-    const double m = s_mass[t];
+    const unsigned long long m = s_key[t];
     int rank = 0;
     for (int g = 1; g <= 254; ++g) {
-      const double mg = s_mass[g];
+      const unsigned long long mg = s_key[g];
       rank += (mg > m || (mg == m && g < t)) ? 1 : 0;
     }
     take = rank < 7;

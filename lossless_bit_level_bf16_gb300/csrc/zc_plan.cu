@@ -7,7 +7,7 @@
 // of from a histogram or a sort.
 //
 // Two kernels:
-//   zc_stats_kernel    one block per statistics unit (U elements inside one
+//   zc_stats_kernel    one warp per statistics unit (U elements inside one
 //                      segment): count, sum and sum of squares of the finite
 //                      values.  HBM-bound: 2 bytes read per element.
 //   zc_predict_kernel  one block per segment: adds the unit partials in a
@@ -21,7 +21,7 @@
 // (and their squares, exact in fp32 for bf16 inputs) as an fp32 tree (error
 // at most 4 units in the last place of the sum of magnitudes), the tree sums
 // are accumulated as unevaluated fp32 pairs (error-free two-sum), and the
-// block reduction is fp64.  A group of 16 whose fp32 sums are not finite (an
+// warp reduction is fp64.  A group of 16 whose fp32 sums are not finite (an
 // inf/NaN input or an fp32 overflow) is redone element by element in fp64,
 // skipping non-finite values.  The whole pass is deterministic for a given
 // plan: the partition into units and every reduction order are fixed.
@@ -63,124 +63,114 @@ __device__ __forceinline__ int find_unit_segment(const ZcSegDev* segs, uint32_t 
   return lo;
 }
 
-__global__ void __launch_bounds__(kThreads) zc_stats_kernel(
-    const uint16_t* __restrict__ x, const ZcSegDev* __restrict__ segs, uint32_t nseg,
-    uint32_t U, StatPartial* __restrict__ parts, int x_al16) {
-  __shared__ unsigned long long s_lo, s_hi;
-  __shared__ int s_al;
-  __shared__ double s_r1[kThreads / 32], s_r2[kThreads / 32];
-  __shared__ unsigned long long s_rc[kThreads / 32];
-  const unsigned long long unit = blockIdx.x;
-  const int t = threadIdx.x;
-  if (t == 0) {
-    int s = find_unit_segment(segs, nseg, unit);
-    unsigned long long b = segs[s].elem_start + (unit - segs[s].unit_start) * U;
-    unsigned long long e = segs[s].elem_start + segs[s].nelem;
-    s_lo = b;
-    s_hi = (b + U < e) ? b + U : e;
-    s_al = x_al16 && ((segs[s].elem_start & 7ull) == 0);
-  }
-  __syncthreads();
-  const unsigned long long lo = s_lo, hi = s_hi;
-  const bool al = s_al;
+// One warp per statistics unit (grid-stride over units, so the partition and
+// every reduction order depend only on the plan).  A step is 512 values: lane
+// l takes 8 at base + 8l and 8 at base + 256 + 8l, so each 16-byte load
+// instruction of the warp reads 512 contiguous bytes; kStatBatch steps are
+// loaded before any is summed.  No block barriers: a warp's loads overlap
+// other warps' sums.
+constexpr int kStatWarps = kThreads / 32;
 
-  float hx = 0.f, lx = 0.f, hq = 0.f, lq = 0.f;
-  double dx = 0.0, dq = 0.0;
-  unsigned long long cnt = 0;
-  // A group is 16 * kThreads values; a thread takes 8 at base + 8t and 8 at
-  // base + 8 * (kThreads + t), so every 16-byte load instruction of a warp
-  // reads 512 contiguous bytes.  kBatch groups are loaded before any is
-  // summed (more bytes in flight per thread); they are summed in order.
-  const unsigned long long gstride = 16ull * kThreads;
-  for (unsigned long long base0 = lo; base0 < hi; base0 += kStatBatch * gstride) {
-    uint32_t w[kStatBatch][8];
-    int vh[kStatBatch][2];
+__global__ void __launch_bounds__(kThreads, 3) zc_stats_kernel(
+    const uint16_t* __restrict__ x, const ZcSegDev* __restrict__ segs, uint32_t nseg,
+    uint32_t U, unsigned long long nunits, StatPartial* __restrict__ parts, int x_al16) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long nwarps = (unsigned long long)gridDim.x * kStatWarps;
+  for (unsigned long long unit = (unsigned long long)blockIdx.x * kStatWarps + (threadIdx.x >> 5);
+       unit < nunits; unit += nwarps) {
+    unsigned long long lo = 0, hi = 0;
+    int al = 0;
+    if (lane == 0) {
+      const int s = find_unit_segment(segs, nseg, unit);
+      lo = segs[s].elem_start + (unit - segs[s].unit_start) * U;
+      const unsigned long long e = segs[s].elem_start + segs[s].nelem;
+      hi = (lo + U < e) ? lo + U : e;
+      al = x_al16 && ((segs[s].elem_start & 7ull) == 0);
+    }
+    lo = __shfl_sync(kFull, lo, 0);
+    hi = __shfl_sync(kFull, hi, 0);
+    al = __shfl_sync(kFull, al, 0);
+
+    float hx = 0.f, lx = 0.f, hq = 0.f, lq = 0.f;
+    double dx = 0.0, dq = 0.0;
+    unsigned long long cnt = 0;
+    for (unsigned long long base0 = lo; base0 < hi; base0 += kStatBatch * 512ull) {
+      uint32_t w[kStatBatch][8];
+      int vh[kStatBatch][2];
 #pragma unroll
-    for (int g = 0; g < kStatBatch; ++g) {
+      for (int g = 0; g < kStatBatch; ++g) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const unsigned long long e0 = base0 + g * gstride + 8ull * ((unsigned long long)h * kThreads + t);
-        const unsigned long long rem = e0 < hi ? hi - e0 : 0ull;
-        const int v = rem < 8 ? (int)rem : 8;
-        vh[g][h] = v;
-        if (v == 8 && al) {
-          const uint4 a = ld_nc_v4(x + e0);
-          w[g][4 * h] = a.x; w[g][4 * h + 1] = a.y; w[g][4 * h + 2] = a.z; w[g][4 * h + 3] = a.w;
+        for (int h = 0; h < 2; ++h) {
+          const unsigned long long e0 = base0 + g * 512ull + 256ull * h + 8ull * lane;
+          const unsigned long long rem = e0 < hi ? hi - e0 : 0ull;
+          const int v = rem < 8 ? (int)rem : 8;
+          vh[g][h] = v;
+          if (v == 8 && al) {
+            const uint4 a4 = ld_nc_v4(x + e0);
+            w[g][4 * h] = a4.x; w[g][4 * h + 1] = a4.y; w[g][4 * h + 2] = a4.z; w[g][4 * h + 3] = a4.w;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t l = (2 * j < v) ? (uint32_t)__ldg(x + e0 + 2 * j) : 0u;
+              const uint32_t hh = (2 * j + 1 < v) ? (uint32_t)__ldg(x + e0 + 2 * j + 1) : 0u;
+              w[g][4 * h + j] = l | (hh << 16);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kStatBatch; ++g) {
+        const int valid = vh[g][0] + vh[g][1];
+        if (valid == 0) continue;
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[2 * j] = bf16_lo(w[g][j]);
+          v[2 * j + 1] = bf16_hi(w[g][j]);
+        }
+        float q[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) q[j] = __fmul_rn(v[j], v[j]);
+#pragma unroll
+        for (int st = 1; st < 16; st <<= 1) {
+#pragma unroll
+          for (int j = 0; j < 16; j += 2 * st) {
+            v[j] = __fadd_rn(v[j], v[j + st]);
+            q[j] = __fadd_rn(q[j], q[j + st]);
+          }
+        }
+        if (isfinite(v[0]) && isfinite(q[0])) {
+          two_sum_acc(hx, lx, v[0]);
+          two_sum_acc(hq, lq, q[0]);
+          cnt += (unsigned long long)valid;
         } else {
+          // an inf/NaN input or an fp32 overflow: redo these values in fp64
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t l = (2 * j < v) ? (uint32_t)__ldg(x + e0 + 2 * j) : 0u;
-            const uint32_t hh = (2 * j + 1 < v) ? (uint32_t)__ldg(x + e0 + 2 * j + 1) : 0u;
-            w[g][4 * h + j] = l | (hh << 16);
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t bits = (j & 1) ? (w[g][j >> 1] >> 16) : (w[g][j >> 1] & 0xFFFFu);
+            if ((j & 7) < vh[g][j >> 3] && ((bits >> 7) & 0xFFu) != 0xFFu) {
+              const double d = (double)__uint_as_float(bits << 16);
+              dx = __dadd_rn(dx, d);
+              dq = __dadd_rn(dq, __dmul_rn(d, d));
+              cnt += 1;
+            }
           }
         }
       }
     }
+    double t1 = __dadd_rn(__dadd_rn((double)hx, (double)lx), dx);
+    double t2 = __dadd_rn(__dadd_rn((double)hq, (double)lq), dq);
 #pragma unroll
-    for (int g = 0; g < kStatBatch; ++g) {
-      const int valid = vh[g][0] + vh[g][1];
-      if (valid == 0) continue;
-      float v[16];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        v[2 * j] = bf16_lo(w[g][j]);
-        v[2 * j + 1] = bf16_hi(w[g][j]);
-      }
-      float q[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) q[j] = __fmul_rn(v[j], v[j]);
-#pragma unroll
-      for (int s = 1; s < 16; s <<= 1) {
-#pragma unroll
-        for (int j = 0; j < 16; j += 2 * s) {
-          v[j] = __fadd_rn(v[j], v[j + s]);
-          q[j] = __fadd_rn(q[j], q[j + s]);
-        }
-      }
-      if (isfinite(v[0]) && isfinite(q[0])) {
-        two_sum_acc(hx, lx, v[0]);
-        two_sum_acc(hq, lq, q[0]);
-        cnt += (unsigned long long)valid;
-      } else {
-        // an inf/NaN input or an fp32 overflow: redo these values in fp64
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t bits = (j & 1) ? (w[g][j >> 1] >> 16) : (w[g][j >> 1] & 0xFFFFu);
-          if ((j & 7) < vh[g][j >> 3] && ((bits >> 7) & 0xFFu) != 0xFFu) {
-            const double d = (double)__uint_as_float(bits << 16);
-            dx = __dadd_rn(dx, d);
-            dq = __dadd_rn(dq, __dmul_rn(d, d));
-            cnt += 1;
-          }
-        }
-      }
+    for (int o = 16; o > 0; o >>= 1) {
+      t1 = __dadd_rn(t1, __shfl_down_sync(kFull, t1, o));
+      t2 = __dadd_rn(t2, __shfl_down_sync(kFull, t2, o));
+      cnt += __shfl_down_sync(kFull, cnt, o);
     }
-  }
-  double t1 = __dadd_rn(__dadd_rn((double)hx, (double)lx), dx);
-  double t2 = __dadd_rn(__dadd_rn((double)hq, (double)lq), dq);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    t1 = __dadd_rn(t1, __shfl_down_sync(kFull, t1, o));
-    t2 = __dadd_rn(t2, __shfl_down_sync(kFull, t2, o));
-    cnt += __shfl_down_sync(kFull, cnt, o);
-  }
-  if ((t & 31) == 0) {
-    s_r1[t >> 5] = t1;
-    s_r2[t >> 5] = t2;
-    s_rc[t >> 5] = cnt;
-  }
-  __syncthreads();
-  if (t == 0) {
-    double a = 0.0, b = 0.0;
-    unsigned long long c = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
-      a = __dadd_rn(a, s_r1[w]);
-      b = __dadd_rn(b, s_r2[w]);
-      c += s_rc[w];
+    if (lane == 0) {
+      parts[unit].cnt = cnt;
+      parts[unit].s1 = t1;
+      parts[unit].s2 = t2;
     }
-    parts[unit].cnt = c;
-    parts[unit].s1 = a;
-    parts[unit].s2 = b;
   }
 }
 
@@ -317,8 +307,10 @@ cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
   StatPartial* parts = reinterpret_cast<StatPartial*>(static_cast<char*>(d_ws) + kCtrlBytes);
   const int al = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
   if (L.nunits) {
-    zc_stats_kernel<<<(unsigned)L.nunits, kThreads, 0, s>>>(d_x, d_segs, L.nseg, L.U,
-                                                             parts, al);
+    const int res = resident_blocks((const void*)zc_stats_kernel, kThreads, 0);
+    const unsigned long long need = (L.nunits + kStatWarps - 1) / kStatWarps;
+    const unsigned grid = (unsigned)(need < (unsigned long long)res ? need : (unsigned long long)res);
+    zc_stats_kernel<<<grid, kThreads, 0, s>>>(d_x, d_segs, L.nseg, L.U, L.nunits, parts, al);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -104,9 +104,38 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   const unsigned long long lanes_total = L.nchunks << log2C;
   const unsigned long long ntiles = (lanes_total + kWTile - 1) / kWTile;
   const uint32_t nct = C >= kWTile ? 1u : kWTile / C;  // chunks per ticket
-  uint8_t* wring = dyn + (size_t)warp * (kStages * 2048u + nct * 1024u + kEscCap);  // input steps
+  uint8_t* wring = dyn + (size_t)warp * (kStages * 2048u + nct * 1024u + 2 * kEscCap);  // input steps
   uint32_t* wlut = reinterpret_cast<uint32_t*>(wring + kStages * 2048u);
-  uint8_t* wst = wring + kStages * 2048u + nct * 1024u;  // staged escape bytes
+  uint8_t* const wst_base = wring + kStages * 2048u + nct * 1024u;  // two escape staging windows
+  uint32_t buf = 0;                 // the window the current ticket stages into
+  uint8_t* wst = wst_base;
+  // The previous ticket: its escape count is published, its offset is
+  // resolved after the next ticket is classified (by then its predecessors
+  // have published), so the warp never waits on the look-back with its
+  // slots still to write.
+  bool p_has = false;
+  unsigned long long p_tile = 0, p_tlane0 = 0, p_cfirst = 0;
+  uint32_t p_run = 0, p_cs = 0, p_buf = 0;
+  auto resolve = [&]() {
+    bool to = false;
+    const unsigned long long excl = lookback_warp_wide<8, 8, 0>(A.states, p_tile, p_run, &to);
+    if (to && lane == 0) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+    const unsigned long long dst = L.off_esc + excl;
+    const uint8_t* pst = wst_base + p_buf * kEscCap;
+    if (dst + p_run > A.out_cap) {
+      if (lane == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
+    } else {
+      for (uint32_t i = lane; i < p_run; i += 32) A.out[dst + i] = pst[i];
+    }
+    if (lane < (int)nct) {
+      const unsigned long long c = p_cfirst + lane;
+      const bool starts = C >= kWTile ? ((p_tlane0 & (C - 1)) == 0) : true;
+      if (c < L.nchunks && starts)
+        reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = excl + p_cs;
+    }
+    __syncwarp();
+    p_has = false;
+  };
   if (lane < kMaxLutSlots) s_lseg[warp][lane] = -1;
   // ring offsets of this lane: it copies pieces lane + 32j, reads pieces 4*lane + k
   uint32_t cp_dst[4], rd_src[4];
@@ -124,7 +153,10 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     unsigned long long tile = 0;
     if (lane == 0) tile = atomicAdd(&A.ctrl->ticket, 1ull);
     tile = __shfl_sync(kFull, tile, 0);
-    if (tile >= ntiles) break;
+    if (tile >= ntiles) {
+      if (p_has) resolve();
+      break;
+    }
     const unsigned long long tlane0 = tile * kWTile;
     const unsigned long long cfirst = tlane0 >> log2C;
     // chunk information, held by lane k for the ticket's chunk k
@@ -328,15 +360,31 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     __syncwarp();
     if (lane < (int)nct) cs_pos = s_cs[warp][lane];
 
-    // ---- the warp's own decoupled look-back, then its escapes go out
+    if (run <= kEscCap) {
+      // publish this ticket's escape count now, resolve the previous ticket,
+      // and keep this one pending in its window
+      if (lane == 0) st_relaxed_u64(A.states + tile, (tile == 0 ? kFlagInc : kFlagAgg) | run);
+      if (p_has) resolve();
+      p_has = true;
+      p_tile = tile;
+      p_tlane0 = tlane0;
+      p_cfirst = cfirst;
+      p_run = run;
+      p_cs = cs_pos;
+      p_buf = buf;
+      buf ^= 1u;
+      wst = wst_base + buf * kEscCap;
+      continue;
+    }
+    if (p_has) resolve();
+    // ---- more escapes than a window holds: the look-back now, then the
+    // ticket is classified again and its escapes written straight out
     bool to = false;
-    const unsigned long long excl = lookback_warp_wide(A.states, tile, run, &to);
+    const unsigned long long excl = lookback_warp_wide<8, 8, 0>(A.states, tile, run, &to);
     if (to && lane == 0) set_status(A.ctrl, ZC_ERR_TIMEOUT);
     const unsigned long long dst = L.off_esc + excl;
     if (dst + run > A.out_cap) {
       if (lane == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
-    } else if (run <= kEscCap) {
-      for (uint32_t i = lane; i < run; i += 32) A.out[dst + i] = wst[i];
     } else {
       // more escapes than the window holds: classify the ticket again and
       // write its escape bytes straight to their place
@@ -716,7 +764,7 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   A.states = states;
   A.x_al16 = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
   const uint32_t nct = L.C >= kWTile ? 1u : kWTile / L.C;
-  const size_t smem = (size_t)kEncWarps * (kStages * 2048u + nct * 1024u + kEscCap);
+  const size_t smem = (size_t)kEncWarps * (kStages * 2048u + nct * 1024u + 2 * kEscCap);
   e = cudaFuncSetAttribute(zc_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(zc_encode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);

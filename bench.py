@@ -11,7 +11,8 @@ value = uncompressed bytes of both inputs / device time of the step (GB/s).
 Every op is bracketed by CUDA events on the stream it is launched on; L2 is
 flushed (a 512 MB buffer written) before every step, outside the timed
 events.  `e2e` repeats the step through host memory: pinned host inputs are
-copied in and the compressed streams copied out inside the timed region.
+copied in and the compressed streams copied out inside the timed region, the
+ZipCCL and IBP chains on two streams so that copies overlap kernels.
 
 --impl reference times the bit-serial CPU oracle (the checker; single thread)
 on a bounded sample of the same workload.
@@ -44,47 +45,64 @@ def _peaks():
     return 6800.0, "fallback"
 
 
-def _traffic_table():
-    """Measured DRAM traffic per launch from the committed ncu summaries:
-    lines 'traffic <kernel> <source sha1> <bytes>' in profiles/*.md."""
+def csrc_hash():
+    """sha1 (12 hex digits) over every file of the CUDA sources: a committed
+    traffic figure is used only while the kernels are the ones it measured."""
     import glob
     import hashlib
+    h = hashlib.sha1()
+    for path in sorted(glob.glob(os.path.join(ROOT, "lossless_bit_level_bf16_gb300", "csrc", "*"))):
+        h.update(os.path.basename(path).encode())
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:12]
+
+
+def _traffic_table():
+    """Measured DRAM traffic per launch from the committed ncu summaries:
+    lines 'traffic <kernel> <sources sha1> <bytes per launch>' in profiles/*.md."""
+    import glob
     out = {}
     for f in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
         for line in open(f):
             parts = line.strip().strip("`").split()
             if len(parts) == 4 and parts[0] == "traffic":
                 out[parts[1]] = (parts[2], int(parts[3]))
-    srcs = {}
-    for name in ("zc_codec.cu", "zc_plan.cu", "ibp_codec.cu", "ibp_meta.cu"):
-        path = os.path.join(ROOT, "lossless_bit_level_bf16_gb300", "csrc", name)
-        srcs[name] = hashlib.sha1(open(path, "rb").read()).hexdigest()[:12]
-    return out, srcs
-
-
-KERNEL_SRC = {
-    "zc_stats": "zc_plan.cu", "zc_encode": "zc_codec.cu", "zc_decode": "zc_codec.cu",
-    "ibp_meta": "ibp_meta.cu", "ibp_encode": "ibp_codec.cu", "ibp_decode": "ibp_codec.cu",
-}
+    return out
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    """nvidia-smi samples (every 20 ms) while the timed region runs.  The GPU is
+    named by its UUID (CUDA ordinals and nvidia-smi indices can differ); the
+    sampler's first line, taken before the timed region, is dropped."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
-        self.index = index
+    def __init__(self, device_index):
+        self.gid = str(device_index)
+        try:
+            import torch
+            u = getattr(torch.cuda.get_device_properties(device_index), "uuid", None)
+            if u is not None:
+                u = str(u)
+                self.gid = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
         self.p = None
 
     def __enter__(self):
+        import select
         try:
             self.p = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                ["nvidia-smi", f"--id={self.gid}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            # wait (at most 5 s) for the first sample, so sampling covers the
+            # whole timed region; that sample is taken before it and dropped
+            r, _, _ = select.select([self.p.stdout], [], [], 5.0)
+            if r:
+                self.p.stdout.readline()
         except (OSError, ValueError):
             self.p = None
         return self
@@ -180,7 +198,15 @@ class Workload:
         self.idws = torch.empty(256, dtype=torch.uint8, device=device)
         self.mode = 0
         self.unc_bytes = 2 * self.n + self.tbytes
-        self.launches_per_step = 8  # stats, predict, encode, decode, columns, meta, encode, decode
+        # kernels each op launches (cudaMemsetAsync of a control block aside)
+        self.kernels = {"zc_plan": ["zc_stats_kernel", "zc_predict_kernel"],
+                        "zc_compress": ["zc_encode_kernel"],
+                        "zc_decompress": ["zc_decode_kernel"],
+                        "ibp_build_meta": ["ibp_columns_kernel", "ibp_meta_kernel"],
+                        "ibp_compress": ["ibp_match_kernel", "ibp_offsets_kernel",
+                                         "ibp_pack_kernel"],
+                        "ibp_decompress": ["ibp_decode_pipe_kernel"]}
+        self.launches_per_step = sum(len(v) for v in self.kernels.values())
 
     def ops(self):
         I, Z = self.I, self.Z
@@ -265,25 +291,40 @@ def gpu_arm(args, rank, world, local_rank):
     hz = torch.empty(zsz, dtype=torch.uint8, pin_memory=True)
     hi = torch.empty(isz, dtype=torch.uint8, pin_memory=True)
     h_status = torch.empty(5 * 4, dtype=torch.uint8, pin_memory=True)
+    # the two codecs' chains (copy in, plan/meta, encode, decode, copy out)
+    # run on two streams, so one codec's copies overlap the other's kernels
+    zs, ist = torch.cuda.Stream(), torch.cuda.Stream()
+    zops, iops = ops[:3], ops[3:]
     e2e_ms = []
     for it in range(args.warmup + args.steps):
         flush.add_(1)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        wl.x.copy_(hx, non_blocking=True)
-        wl.table.copy_(ht, non_blocking=True)
-        wl.samples.copy_(hs, non_blocking=True)
-        for _, fn in ops:
-            fn()
-        hz.copy_(wl.zout[:zsz], non_blocking=True)
-        hi.copy_(wl.iout[:isz], non_blocking=True)
-        for j, ws in enumerate((wl.plan.ws, wl.zdws, wl.mws, wl.iws, wl.idws)):
-            h_status[4 * j:4 * j + 4].copy_(ws[:4], non_blocking=True)
+        zs.wait_event(a)
+        ist.wait_event(a)
+        with torch.cuda.stream(zs):
+            wl.x.copy_(hx, non_blocking=True)
+            for _, fn in zops:
+                fn()
+            hz.copy_(wl.zout[:zsz], non_blocking=True)
+            for j, ws in enumerate((wl.plan.ws, wl.zdws)):
+                h_status[4 * j:4 * j + 4].copy_(ws[:4], non_blocking=True)
+        with torch.cuda.stream(ist):
+            wl.table.copy_(ht, non_blocking=True)
+            wl.samples.copy_(hs, non_blocking=True)
+            for _, fn in iops:
+                fn()
+            hi.copy_(wl.iout[:isz], non_blocking=True)
+            for j, ws in enumerate((wl.mws, wl.iws, wl.idws)):
+                h_status[8 + 4 * j:12 + 4 * j].copy_(ws[:4], non_blocking=True)
+        stream.wait_stream(zs)
+        stream.wait_stream(ist)
         b.record(stream)
         b.synchronize()
         if it >= args.warmup:
             e2e_ms.append(a.elapsed_time(b))
+    torch.cuda.synchronize()
     wl.check()
     e2e = statistics.mean(e2e_ms)
     e2e_max = reduce_max(e2e)
@@ -310,9 +351,6 @@ def report_gpu(args, r, world):
         "ibp_compress": wl.tbytes + isz,
         "ibp_decompress": isz + wl.tbytes,
     }
-    kern = {"zc_plan": "zc_stats", "zc_compress": "zc_encode", "zc_decompress": "zc_decode",
-            "ibp_build_meta": "ibp_meta", "ibp_compress": "ibp_encode",
-            "ibp_decompress": "ibp_decode"}
     unc = {"zc_plan": 2 * n, "zc_compress": 2 * n, "zc_decompress": 2 * n,
            "ibp_build_meta": nsamp, "ibp_compress": wl.tbytes, "ibp_decompress": wl.tbytes}
     ops = {}
@@ -320,13 +358,17 @@ def report_gpu(args, r, world):
         t = statistics.mean(ts)
         ach = alg[name] / (t * 1e-3) / 1e9
         ops[name] = {"ms": round(t, 4), "GBps_uncompressed": round(unc[name] / (t * 1e-3) / 1e9, 1),
-                     "GBps_traffic": round(ach, 1), "frac_hbm": round(ach / peak, 4)}
-    dom = max(r["per_op"], key=lambda k: statistics.mean(r["per_op"][k]))
+                     "GBps_traffic": round(ach, 1), "frac_hbm": round(ach / peak, 4),
+                     "kernels": wl.kernels[name]}
+    # the dominant kernel: the longest op that is a single kernel (ops of
+    # several kernels are timed as a whole and listed under "ops")
+    single = [k for k in r["per_op"] if len(wl.kernels[k]) == 1]
+    dom = max(single, key=lambda k: statistics.mean(r["per_op"][k]))
     t_dom = statistics.mean(r["per_op"][dom])
-    table, srcs = _traffic_table()
+    table = _traffic_table()
     traffic = None
-    kname = kern[dom]
-    if kname in table and table[kname][0] == srcs[KERNEL_SRC[kname]]:
+    kname = wl.kernels[dom][0]
+    if kname in table and table[kname][0] == csrc_hash():
         traffic = table[kname][1]
     achieved = alg[dom] / (t_dom * 1e-3) / 1e9
     line = {
@@ -349,7 +391,7 @@ def report_gpu(args, r, world):
                    "parallelism": f"replicas x{world}"},
         "ratio": {"zipccl": round(2 * n / zsz, 4), "ibp": round(wl.tbytes / isz, 4)},
         "ops": ops,
-        "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": kname, "op": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "algorithmic_bytes_per_launch": alg[dom], "traffic": traffic},
@@ -573,7 +615,7 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--scale", type=float, default=1.0, help="workload scale (1 = full size)")

@@ -205,7 +205,12 @@ int ibp_build_meta(const void* d_samples, uint64_t n_samples,
 /* [IBP] step 2: encode n_bytes (multiple of 4) at d_x into an IBP1 stream at
  * d_out using the metadata at d_meta (its chunk size must be chunk_bytes;
  * checked on the device).  *d_out_bytes (device, may be NULL) receives the
- * stream size; escapes past out_cap set ZC_ERR_CAPACITY. */
+ * stream size; a stream larger than out_cap sets ZC_ERR_CAPACITY and nothing
+ * is written past out_cap.  For chunk_bytes <= 2048: one memset and three
+ * kernels (a read-only pass that decides every chunk's participation bit, a
+ * scan of the group lengths into the stream's group-offset table, the packing
+ * pass); the workspace holds one participation word per group between them.
+ * Larger chunks: one memset and one kernel. */
 int ibp_compress(const void* d_meta, uint32_t chunk_bytes, const void* d_x,
                  uint64_t n_bytes, void* d_out, uint64_t out_cap,
                  uint64_t* d_out_bytes, void* d_ws, size_t ws_bytes,

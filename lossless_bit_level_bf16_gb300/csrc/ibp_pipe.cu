@@ -371,10 +371,12 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
   extern __shared__ __align__(128) uint8_t dyn[];
   __shared__ uint32_t s_scr[NW + 4];
   __shared__ unsigned long long s_tile[kMaxStages];
-  __shared__ uint32_t s_pw[kMaxQ], s_gex[kMaxQ];
-  __shared__ unsigned long long s_base;
-  __shared__ uint32_t s_agg;
-  __shared__ int s_raw, s_last;
+  // per stage, read when its copy is issued: participation words, group bit
+  // offsets in the tile's stream, the tile's stream offset and bits
+  __shared__ uint32_t s_pw[kMaxStages][kMaxQ], s_gex[kMaxStages][kMaxQ];
+  __shared__ unsigned long long s_base[kMaxStages];
+  __shared__ uint32_t s_agg[kMaxStages];
+  __shared__ int s_raw[kMaxStages], s_last;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t cb = A.cb, W = cb / 4, B = 8 * cb, Q = A.Q, S = A.S;
 
@@ -395,56 +397,74 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
   if (REG) load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
   for (uint32_t i = t; i < A.img_words / 4; i += NT) img4[i] = make_uint4(0, 0, 0, 0);
 
-  // thread 0: start the copy of this block's kk-th tile into stage s
+  // warp 0: prefetch() loads the participation words and group offsets of
+  // this block's kk-th tile into registers (their latency overlaps the
+  // current tile's work); issue() files them per stage and starts the copy of
+  // the tile's input into stage s.
+  uint32_t pf_pw = 0;
+  unsigned long long pf_go = 0, pf_gend = 0;
+  auto prefetch = [&](unsigned long long kk) {
+    const unsigned long long tile = ok ? blockIdx.x + kk * gridDim.x : A.ntiles;
+    if (tile >= A.ntiles) return;
+    const unsigned long long g0 = tile * Q;
+    const uint32_t nq = (uint32_t)((A.ngroups - g0) < Q ? (A.ngroups - g0) : Q);
+    pf_pw = (uint32_t)lane < nq ? A.pw[g0 + lane] : 0u;
+    pf_go = (uint32_t)lane < nq ? grp[g0 + lane] : 0ull;
+    pf_gend = grp[g0 + nq];
+  };
   auto issue = [&](unsigned long long kk, uint32_t s) {
     const unsigned long long tile = ok ? blockIdx.x + kk * gridDim.x : A.ntiles;
-    s_tile[s] = tile;
+    if (lane == 0) s_tile[s] = tile;
     if (tile >= A.ntiles) return;
-    const unsigned long long b0 = tile * tile_raw;
-    const unsigned long long tb = (A.n_bytes - b0) < tile_raw ? (A.n_bytes - b0) : tile_raw;
-    const uint32_t b16 = (uint32_t)(tb & ~15ull);
-    uint8_t* st = stages + (size_t)s * A.stage_bytes;
-    for (uint32_t w = b16 / 4; w < (uint32_t)(tb / 4); ++w)  // the last 4..12 bytes
-      reinterpret_cast<uint32_t*>(st)[w] = __ldg(reinterpret_cast<const uint32_t*>(A.src + b0) + w);
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bars + s, b16);
-    if (b16) bulk_g2s(st, A.src + b0, b16, bars + s);
+    const unsigned long long g0 = tile * Q;
+    const uint32_t nq = (uint32_t)((A.ngroups - g0) < Q ? (A.ngroups - g0) : Q);
+    const uint32_t pw = pf_pw;
+    const unsigned long long go = pf_go;
+    const unsigned long long base = __shfl_sync(kFull, go, 0);
+    const bool raw = __ballot_sync(kFull, pw != 0) == 0;
+    if ((uint32_t)lane < nq) {
+      s_pw[s][lane] = pw;
+      s_gex[s][lane] = (uint32_t)(go - base);
+    }
+    if (lane == 0) {
+      s_base[s] = base;
+      s_agg[s] = (uint32_t)(pf_gend - base);
+      s_raw[s] = raw;
+      const unsigned long long b0 = tile * tile_raw;
+      const unsigned long long tb = (A.n_bytes - b0) < tile_raw ? (A.n_bytes - b0) : tile_raw;
+      const uint32_t b16 = (uint32_t)(tb & ~15ull);
+      uint8_t* st = stages + (size_t)s * A.stage_bytes;
+      for (uint32_t w = b16 / 4; w < (uint32_t)(tb / 4); ++w)  // the last 4..12 bytes
+        reinterpret_cast<uint32_t*>(st)[w] = __ldg(reinterpret_cast<const uint32_t*>(A.src + b0) + w);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bars + s, b16);
+      if (b16) bulk_g2s(st, A.src + b0, b16, bars + s);
+    }
   };
-  if (t == 0) {
+  if (t == 0)
     for (uint32_t s = 0; s < S; ++s) mbar_init(bars + s, 1);
-    for (uint32_t s = 0; s < S; ++s) issue(s, s);
-  }
+  __syncthreads();
+  if (warp == 0)
+    for (uint32_t s = 0; s < S; ++s) {
+      prefetch(s);
+      issue(s, s);
+    }
   __syncthreads();
 
   for (uint32_t k = 0;; ++k) {
     const uint32_t s = k % S;
     const unsigned long long tile = s_tile[s];
     if (tile >= A.ntiles) break;
+    if (warp == 0) prefetch(k + S);
     if (!mbar_wait(bars + s, (k / S) & 1)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
     const uint32_t* sd = reinterpret_cast<const uint32_t*>(stages + (size_t)s * A.stage_bytes);
     const unsigned long long g0 = tile * Q, b0 = tile * tile_raw;
     const uint32_t nq = (uint32_t)((A.ngroups - g0) < Q ? (A.ngroups - g0) : Q);
     const uint32_t tb = (uint32_t)((A.n_bytes - b0) < tile_raw ? (A.n_bytes - b0) : tile_raw);
     const uint32_t twords = tb / 4, nvec = (tb + 15) / 16;
-    if (warp == 0) {
-      const uint32_t pw = (uint32_t)lane < nq ? A.pw[g0 + lane] : 0u;
-      const unsigned long long go = (uint32_t)lane < nq ? grp[g0 + lane] : 0ull;
-      const unsigned long long base = __shfl_sync(kFull, go, 0);
-      const bool raw = __ballot_sync(kFull, pw != 0) == 0;
-      if ((uint32_t)lane < nq) {
-        s_pw[lane] = pw;
-        s_gex[lane] = (uint32_t)(go - base);
-      }
-      if (lane == 0) {
-        s_base = base;
-        s_agg = (uint32_t)(grp[g0 + nq] - base);
-        s_raw = raw;
-      }
-    }
-    __syncthreads();
-    const bool raw = s_raw != 0;
-    const unsigned long long dst = A.off_payload + (s_base >> 3);
-    const uint32_t nv = s_agg >> 7;  // 16-byte vectors of the tile's stream
+    const bool raw = s_raw[s] != 0;
+    const unsigned long long dst = A.off_payload + (s_base[s] >> 3);
+    const uint32_t nv = s_agg[s] >> 7;  // 16-byte vectors of the tile's stream
     const bool fits = dst + 16ull * nv <= A.dst_cap;
     if (!fits && t == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
     if (raw) {
@@ -480,34 +500,41 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
         }
       }
     } else {
-      if ((uint32_t)t < nq) img[3 + (s_gex[t] >> 5)] = s_pw[t];
-      for (uint32_t v = t; v < nvec; v += NT) {
-        uint32_t c, r;
-        vec_pos<REG>(A, v, c, r);
-        const uint32_t q = c >> 5, i = c & 31;
-        const uint32_t pwq = s_pw[q];
-        if (!REG) load_vectab(T, r, vt);
-        const uint4 d = *reinterpret_cast<const uint4*>(sd + 4 * v);
-        const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
-        const uint32_t off = s_gex[q] + 32u + i * B - (uint32_t)__popc(pwq & ((1u << i) - 1u)) * m;
-        uint32_t o[4], n, pos;
-        if ((pwq >> i) & 1u) {
-          uint32_t f[4];
+      if ((uint32_t)t < nq) img[3 + (s_gex[s][t] >> 5)] = s_pw[s][t];
+      // two vectors per thread per step: independent chains to interleave
+      for (uint32_t v0 = t; v0 < nvec; v0 += 2 * NT) {
 #pragma unroll
-          for (int w = 0; w < 4; ++w) f[w] = hd_compress(dw[w], vt.K[w], &vt.MV[0][w], 4);
-          uint32_t kk[4];
-          kept_bits(vt, kk);
-          cat4(f, kk, o);
-          n = kk[0] + kk[1] + kk[2] + kk[3];
-          pos = off + vt.Pr;
-        } else {
-          const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t v = v0 + e * NT;
+          if (v >= nvec) continue;
+          uint32_t c, r;
+          vec_pos<REG>(A, v, c, r);
+          const uint32_t q = c >> 5, i = c & 31;
+          const uint32_t pwq = s_pw[s][q];
+          if (!REG) load_vectab(T, r, vt);
+          const uint4 d = *reinterpret_cast<const uint4*>(sd + 4 * v);
+          const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+          const uint32_t off =
+              s_gex[s][q] + 32u + i * B - (uint32_t)__popc(pwq & ((1u << i) - 1u)) * m;
+          uint32_t o[4], n, pos;
+          if ((pwq >> i) & 1u) {
+            uint32_t f[4];
 #pragma unroll
-          for (uint32_t w = 0; w < 4; ++w) o[w] = w < wv ? dw[w] : 0u;
-          n = 32u * wv;
-          pos = off + 128u * r;
+            for (int w = 0; w < 4; ++w) f[w] = hd_compress(dw[w], vt.K[w], &vt.MV[0][w], 4);
+            uint32_t kk[4];
+            kept_bits(vt, kk);
+            cat4(f, kk, o);
+            n = kk[0] + kk[1] + kk[2] + kk[3];
+            pos = off + vt.Pr;
+          } else {
+            const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
+#pragma unroll
+            for (uint32_t w = 0; w < 4; ++w) o[w] = w < wv ? dw[w] : 0u;
+            n = 32u * wv;
+            pos = off + 128u * r;
+          }
+          img_put(img, 96u + pos, o, n);
         }
-        img_put(img, 96u + pos, o, n);
       }
       __syncthreads();
       if (fits) {
@@ -529,10 +556,12 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
         }
       }
     }
-    __syncthreads();
-    if (t == 0) issue(k + S, s);
-    if (!raw)  // ordered before the next tile's packing by its first barrier
+    __syncthreads();  // the stage (and the image) have been read
+    if (warp == 0) issue(k + S, s);
+    if (!raw) {
       for (uint32_t u = t; u <= nv; u += NT) img4[u] = make_uint4(0, 0, 0, 0);
+      __syncthreads();  // cleared before the next tile packs into it
+    }
   }
 
   // ---- last block: header and table end
@@ -560,9 +589,9 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
   __shared__ unsigned long long s_tile[kMaxStages];
   __shared__ unsigned long long s_goff[kMaxStages][kMaxQ + 1];
   __shared__ int s_sbad[kMaxStages];
-  __shared__ uint32_t s_pw[kMaxQ];
-  __shared__ int s_gbad[kMaxQ];
-  __shared__ uint32_t s_off[kMaxQ][32];
+  __shared__ uint32_t s_pw[2][kMaxQ];
+  __shared__ int s_gbad[2][kMaxQ];
+  __shared__ uint32_t s_off[2][kMaxQ][32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t cb = A.cb, W = cb / 4, B = 8 * cb, Q = A.Q, S = A.S;
 
@@ -594,7 +623,18 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
   VecTab vt;
   if (REG) load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
 
-  // warp 0: the span of this block's kk-th tile, checked, then its copy
+  // warp 0: the span of this block's kk-th tile.  prefetch() loads its
+  // group-table entries into registers (their latency overlaps the current
+  // tile's work); issue() checks them and starts the copy into stage s.
+  unsigned long long pf_go = 0, pf_gend = 0;
+  auto prefetch = [&](unsigned long long kk) {
+    const unsigned long long tile = blockIdx.x + kk * gridDim.x;
+    if (tile >= ntiles) return;
+    const unsigned long long g0 = tile * Q;
+    const uint32_t nq = (uint32_t)((ngroups - g0) < Q ? (ngroups - g0) : Q);
+    pf_gend = grp[g0 + nq];
+    pf_go = (uint32_t)lane < nq ? grp[g0 + lane] : 0ull;
+  };
   auto issue = [&](unsigned long long kk, uint32_t s) {
     const unsigned long long tile = blockIdx.x + kk * gridDim.x;
     if (tile >= ntiles) {
@@ -603,8 +643,8 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
     }
     const unsigned long long g0 = tile * Q;
     const uint32_t nq = (uint32_t)((ngroups - g0) < Q ? (ngroups - g0) : Q);
-    const unsigned long long gend = grp[g0 + nq];
-    const unsigned long long go = (uint32_t)lane < nq ? grp[g0 + lane] : gend;
+    const unsigned long long gend = pf_gend;
+    const unsigned long long go = (uint32_t)lane < nq ? pf_go : gend;
     const unsigned long long nx0 = __shfl_down_sync(kFull, go, 1);
     const unsigned long long nx = (uint32_t)lane + 1 < nq ? nx0 : gend;
     bool bad = false;
@@ -627,24 +667,21 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
       }
     }
   };
-  if (warp == 0)
-    for (uint32_t s = 0; s < S; ++s) issue(s, s);
-  __syncthreads();
-
-  for (uint32_t k = 0;; ++k) {
-    const uint32_t s = k % S;
+  // The scan of the kk-th tile (in stage s) into buffer bf: the chunk bit
+  // offsets of its groups (one warp per group, from the last warp down).
+  auto scan = [&](uint32_t kk, uint32_t s, uint32_t bf) {
     const unsigned long long tile = s_tile[s];
-    if (tile >= ntiles) break;
-    const bool waited = mbar_wait(bars + s, (k / S) & 1);
+    if (tile >= ntiles) return;
+    const unsigned long long g0 = tile * Q;
+    const uint32_t nq = (uint32_t)((ngroups - g0) < Q ? (ngroups - g0) : Q);
+    const uint32_t qw = (uint32_t)(NW - 1 - warp);  // the last warp takes group 0
+    if (qw >= nq) return;
+    const bool waited = mbar_wait(bars + s, (kk / S) & 1);
     if (!waited) set_status(A.ctrl, ZC_ERR_TIMEOUT);
     const uint32_t* sd = reinterpret_cast<const uint32_t*>(stages + (size_t)s * A.stage_bytes);
-    const unsigned long long g0 = tile * Q, b0 = tile * tile_raw;
-    const uint32_t nq = (uint32_t)((ngroups - g0) < Q ? (ngroups - g0) : Q);
-    const uint32_t tb = (uint32_t)((n_bytes - b0) < tile_raw ? (n_bytes - b0) : tile_raw);
-    const uint32_t twords = tb / 4, nvec = (tb + 15) / 16;
     const bool sbad = s_sbad[s] != 0 || !waited;
     const unsigned long long base = s_goff[s][0];
-    for (uint32_t q = warp; q < nq; q += NW) {
+    for (uint32_t q = qw; q < nq; q += NW) {
       const uint32_t gs = (uint32_t)(s_goff[s][q] - base), ge = (uint32_t)(s_goff[s][q + 1] - base);
       const uint32_t pw = sbad ? 0u : sd[gs >> 5];
       const unsigned long long c = (g0 + q) * 32ull + lane;
@@ -659,49 +696,90 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
         const uint32_t u = __shfl_up_sync(kFull, inc, o);
         if (lane >= o) inc += u;
       }
-      s_off[q][lane] = gs + 32u + inc - len;
+      s_off[bf][q][lane] = gs + 32u + inc - len;
       const uint32_t tot = __shfl_sync(kFull, inc, 31);
       if (round_up_dev(32ull + tot, 128) != (unsigned long long)(ge - gs)) bad = true;
       bad = __any_sync(kFull, bad);
       if (lane == 0) {
-        s_pw[q] = pw;
-        s_gbad[q] = bad;
+        s_pw[bf][q] = pw;
+        s_gbad[bf][q] = bad;
       }
     }
-    __syncthreads();
+  };
+  if (warp == 0)
+    for (uint32_t s = 0; s < S; ++s) {
+      prefetch(s);
+      issue(s, s);
+    }
+  __syncthreads();
+  scan(0, 0, 0);
+  __syncthreads();
+
+  // Tile k is expanded, then tile k + 1 scanned; one barrier per tile.
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t s = k % S, bf = k & 1;
+    const unsigned long long tile = s_tile[s];
+    if (tile >= ntiles) break;
+    if (warp == 0) prefetch(k + S);
+    const bool waited = mbar_wait(bars + s, (k / S) & 1);
+    if (!waited) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+    const uint32_t* sd = reinterpret_cast<const uint32_t*>(stages + (size_t)s * A.stage_bytes);
+    const unsigned long long b0 = tile * tile_raw, g0 = tile * Q;
+    const uint32_t nq = (uint32_t)((ngroups - g0) < Q ? (ngroups - g0) : Q);
+    const uint32_t tb = (uint32_t)((n_bytes - b0) < tile_raw ? (n_bytes - b0) : tile_raw);
+    const uint32_t twords = tb / 4, nvec = (tb + 15) / 16;
     uint32_t* yt = reinterpret_cast<uint32_t*>(A.dst + b0);
-    for (uint32_t v = t; v < nvec; v += NT) {
-      uint32_t c, r;
-      vec_pos<REG>(A, v, c, r);
-      const uint32_t q = c >> 5, i = c & 31;
-      if (s_gbad[q]) continue;
-      if (!REG) load_vectab(T, r, vt);
-      const uint32_t off = s_off[q][i];
-      uint32_t u[4], o[4];
-      if ((s_pw[q] >> i) & 1u) {
-        win128(sd, off + vt.Pr, u);
-        uint32_t f[4];
-        uint32_t kk[4];
-        kept_bits(vt, kk);
-        split4(u, kk, f);
+    // two vectors per thread per step (same chunk position, so the same
+    // register tables): two independent dependency chains to interleave
+    for (uint32_t v0 = t; v0 < nvec; v0 += 2 * NT) {
+      uint32_t o[2][4];
+      bool live[2];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) o[w] = hd_expand(f[w], vt.K[w], &vt.MV[0][w], 4) | vt.V[w];
-      } else {
-        win128(sd, off + 128u * r, u);
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t v = v0 + e * NT;
+        live[e] = false;
+        if (v >= nvec) continue;
+        uint32_t c, r;
+        vec_pos<REG>(A, v, c, r);
+        const uint32_t q = c >> 5, i = c & 31;
+        if (s_gbad[bf][q]) continue;
+        live[e] = true;
+        if (!REG) load_vectab(T, r, vt);
+        const uint32_t off = s_off[bf][q][i];
+        uint32_t u[4];
+        if ((s_pw[bf][q] >> i) & 1u) {
+          win128(sd, off + vt.Pr, u);
+          uint32_t f[4];
+          uint32_t kk[4];
+          kept_bits(vt, kk);
+          split4(u, kk, f);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) o[w] = u[w];
+          for (int w = 0; w < 4; ++w) o[e][w] = hd_expand(f[w], vt.K[w], &vt.MV[0][w], 4) | vt.V[w];
+        } else {
+          win128(sd, off + 128u * r, u);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) o[e][w] = u[w];
+        }
       }
-      const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
-      if (wv == 4) {
-        st_v4(yt + 4 * v, make_uint4(o[0], o[1], o[2], o[3]));
-      } else {
 #pragma unroll
-        for (uint32_t w = 0; w < 4; ++w)
-          if (w < wv) yt[4 * v + w] = o[w];
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t v = v0 + e * NT;
+        if (!live[e]) continue;
+        const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
+        if (wv == 4) {
+          st_v4(yt + 4 * v, make_uint4(o[e][0], o[e][1], o[e][2], o[e][3]));
+        } else {
+#pragma unroll
+          for (uint32_t w = 0; w < 4; ++w)
+            if (w < wv) yt[4 * v + w] = o[e][w];
+        }
       }
     }
-    if ((uint32_t)t < nq && s_gbad[t]) set_status(A.ctrl, ZC_ERR_FORMAT);
-    __syncthreads();
+    if ((uint32_t)t < nq && s_gbad[bf][t]) set_status(A.ctrl, ZC_ERR_FORMAT);
+    // after this warp's share, so that waiting for the next tile to land
+    // overlaps the expansion
+    scan(k + 1, (k + 1) % S, bf ^ 1);
+    __syncthreads();  // stage s read; the next tile's scan written
     if (warp == 0) issue(k + S, s);
   }
 }

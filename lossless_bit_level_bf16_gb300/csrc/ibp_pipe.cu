@@ -68,11 +68,62 @@ struct PipeArgs {
   uint32_t Q, S, stage_bytes, img_words;
 };
 
-// Mask tables of the 4 words at vector position r of a chunk.
+// Mask tables of the 4 words at vector position r of a chunk.  When every
+// keep mask of the 4 words is at most two runs of ones (fast), MV holds the
+// runs instead of the move masks: MV[0] = first run's start a0, MV[1] = its
+// mask m0, MV[2] = second run's start a1, MV[3] = its mask m1, MV[4] = the
+// first run's length l0 (0 when there is no second run).
 struct VecTab {
   uint32_t K[4], V[4], MV[5][4];
   uint32_t Pr;  // kept bits of the chunk before this vector
+  bool fast;
 };
+
+// Switch vt to the two-run form if every word allows it (called once, on
+// the tables in registers).
+__device__ __forceinline__ void make_runs(VecTab& v) {
+  bool ok = true;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) ok = ok && __popc(v.K[j] & ~(v.K[j] << 1)) <= 2;
+  v.fast = ok;
+  if (!ok) return;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t k = v.K[j];
+    uint32_t a0 = 0, m0 = 0, a1 = 0, m1 = 0, l0 = 0;
+    if (k) {
+      a0 = __ffs(k) - 1;
+      const uint32_t y = k >> a0;
+      const uint32_t len0 = (y == 0xFFFFFFFFu) ? 32u : (uint32_t)(__ffs(~y) - 1);
+      m0 = len0 >= 32 ? 0xFFFFFFFFu : ((1u << len0) - 1u);
+      const uint32_t k1 = k & ~(m0 << a0);
+      if (k1) {
+        a1 = __ffs(k1) - 1;
+        m1 = (1u << __popc(k1)) - 1u;  // the second run is shorter than 32
+        l0 = len0;
+      }
+    }
+    v.MV[0][j] = a0;
+    v.MV[1][j] = m0;
+    v.MV[2][j] = a1;
+    v.MV[3][j] = m1;
+    v.MV[4][j] = l0;
+  }
+}
+
+// Kept bits of word w of x closed up toward bit 0 (the keep mask's runs, or
+// the general method).
+__device__ __forceinline__ uint32_t vt_compress(const VecTab& v, uint32_t x, int w) {
+  if (v.fast)
+    return ((x >> v.MV[0][w]) & v.MV[1][w]) | (((x >> v.MV[2][w]) & v.MV[3][w]) << v.MV[4][w]);
+  return hd_compress(x, v.K[w], &v.MV[0][w], 4);
+}
+// Inverse: the low kept-bit count of f spread out to the kept positions.
+__device__ __forceinline__ uint32_t vt_expand(const VecTab& v, uint32_t f, int w) {
+  if (v.fast)
+    return ((f & v.MV[1][w]) << v.MV[0][w]) | (((f >> v.MV[4][w]) & v.MV[3][w]) << v.MV[2][w]);
+  return hd_expand(f, v.K[w], &v.MV[0][w], 4);
+}
 
 // Kept bits per word of the vector (recomputed: cheaper than registers).
 __device__ __forceinline__ void kept_bits(const VecTab& v, uint32_t k[4]) {
@@ -90,6 +141,7 @@ __device__ __forceinline__ void load_vectab(const IbpTables& T, uint32_t r, VecT
     for (int i = 0; i < 5; ++i) v.MV[i][j] = T.MV[i * T.W + w];
   }
   v.Pr = T.P[4 * r];
+  v.fast = false;
 }
 
 // Fields f[0..3] (f[j] has k[j] <= 32 bits) laid end to end, LSB first.
@@ -394,7 +446,10 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
   const uint32_t gvec = 8 * W + 1;  // 16-byte vectors of a full group stored raw
 
   VecTab vt;
-  if (REG) load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
+  if (REG) {
+    load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
+    make_runs(vt);
+  }
   for (uint32_t i = t; i < A.img_words / 4; i += NT) img4[i] = make_uint4(0, 0, 0, 0);
 
   // warp 0: prefetch() loads the participation words and group offsets of
@@ -520,7 +575,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
           if ((pwq >> i) & 1u) {
             uint32_t f[4];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) f[w] = hd_compress(dw[w], vt.K[w], &vt.MV[0][w], 4);
+            for (int w = 0; w < 4; ++w) f[w] = vt_compress(vt, dw[w], w);
             uint32_t kk[4];
             kept_bits(vt, kk);
             cat4(f, kk, o);
@@ -621,7 +676,10 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
   const uint32_t cap = A.stage_bytes - kStageSlack;
 
   VecTab vt;
-  if (REG) load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
+  if (REG) {
+    load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
+    // (decode keeps the move masks)
+  }
 
   // warp 0: the span of this block's kk-th tile.  prefetch() loads its
   // group-table entries into registers (their latency overlaps the current

@@ -17,8 +17,9 @@
 //   ibp_meta_kernel     one block: threshold k = ceil(T*N) on each position's
 //                       agreement max(ones, N-ones); per-position (mode 0) or
 //                       joint greedy selection (mode 1: positions sorted by
-//                       agreement, then index; a position is kept while at
-//                       least k samples still match every kept position);
+//                       agreement, then index, with a block-wide bitonic
+//                       sort; one warp then keeps a position while at least
+//                       k samples still match every kept position);
 //                       writes the IBPM blob with its FNV-1a-64 hash.
 #include <cuda_runtime.h>
 
@@ -68,8 +69,101 @@ __device__ __forceinline__ uint32_t block_sum_1024(uint32_t v, uint32_t* red) {
   return t;
 }
 
+// Joint reading, greedy pass over the sorted candidates (one warp): a
+// candidate is kept when at least k samples still match every kept position
+// and it.
+constexpr int kGreedyRegs = 12;
+constexpr uint32_t kRing = 8;  // candidate columns in flight
+
+__device__ __forceinline__ void greedy_warp(const unsigned long long* keys, uint32_t Bp,
+                                            const uint32_t* __restrict__ ones,
+                                            const uint32_t* __restrict__ cols, uint32_t Wn,
+                                            unsigned long long k, uint32_t* alive,
+                                            uint32_t* smask, uint32_t* sbitv, uint32_t* ring) {
+  const int lane = threadIdx.x & 31;
+  if (Wn <= 32u * kGreedyRegs) {
+    // columns of the next kRing candidates in flight (cp.async into a ring in
+    // shared memory; each lane copies and reads only its own words)
+    uint32_t al[kGreedyRegs];
+#pragma unroll
+    for (int r = 0; r < kGreedyRegs; ++r) {
+      const uint32_t w = lane + 32u * r;
+      al[r] = w < Wn ? alive[w] : 0u;
+    }
+    auto fetch = [&](uint32_t c) {
+      const unsigned long long key = c < Bp ? keys[c] : ~0ull;
+      if (key != ~0ull) {
+        const uint32_t* col = cols + (unsigned long long)((uint32_t)key >> 1) * Wn;
+        uint32_t* slot = ring + (c % kRing) * (32u * kGreedyRegs);
+#pragma unroll
+        for (int r = 0; r < kGreedyRegs; ++r) {
+          const uint32_t w = lane + 32u * r;
+          if (w < Wn) cp_async4(slot + w, col + w);
+        }
+      }
+      cp_async_commit();  // (possibly empty) group per candidate
+    };
+#pragma unroll 1
+    for (uint32_t d = 0; d < kRing; ++d) fetch(d);
+    for (uint32_t c = 0; c < Bp; ++c) {
+      const unsigned long long key = keys[c];
+      if (key == ~0ull) break;
+      const uint32_t j = (uint32_t)(key & 0xFFFFFFFFu) >> 1;
+      cp_async_wait_group<kRing - 1>();  // this candidate's column has landed
+      const uint32_t* slot = ring + (c % kRing) * (32u * kGreedyRegs);
+      const bool v = (key & 1u) != 0;
+      uint32_t keep[kGreedyRegs], cnt = 0;
+#pragma unroll
+      for (int r = 0; r < kGreedyRegs; ++r) {
+        const uint32_t w = lane + 32u * r;
+        const uint32_t cw = w < Wn ? slot[w] : 0u;
+        keep[r] = al[r] & (v ? cw : ~cw);
+        cnt += __popc(keep[r]);
+      }
+      fetch(c + kRing);  // the slot just read is refilled
+      cnt = __reduce_add_sync(kFull, cnt);
+      if (cnt >= k) {
+#pragma unroll
+        for (int r = 0; r < kGreedyRegs; ++r) al[r] = keep[r];
+        if (lane == 0) {
+          smask[j >> 5] |= 1u << (j & 31);
+          if (v) sbitv[j >> 5] |= 1u << (j & 31);
+        }
+      }
+    }
+    cp_async_wait_all();
+    return;
+  }
+  // many samples: the mask stays in shared memory, two passes per candidate
+  for (uint32_t c = 0; c < Bp; ++c) {
+    const unsigned long long key = keys[c];
+    if (key == ~0ull) break;
+    const uint32_t j = (uint32_t)(key & 0xFFFFFFFFu) >> 1;
+    const bool v = (key & 1u) != 0;
+    const uint32_t* col = cols + (unsigned long long)j * Wn;
+    uint32_t cnt = 0;
+    for (uint32_t w = lane; w < Wn; w += 32) {
+      const uint32_t cw = __ldg(col + w);
+      cnt += __popc(alive[w] & (v ? cw : ~cw));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
+    if (cnt >= k) {
+      for (uint32_t w = lane; w < Wn; w += 32) {
+        const uint32_t cw = __ldg(col + w);
+        alive[w] &= v ? cw : ~cw;
+      }
+      if (lane == 0) {
+        smask[j >> 5] |= 1u << (j & 31);
+        if (v) sbitv[j >> 5] |= 1u << (j & 31);
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // Dynamic shared memory: keys (8*Bp bytes, mode 1), alive (4*Wn), mask and
-// bitval words (4*W each).
+// bitval words (4*W each), the greedy pass's column ring (mode 1).
 __global__ void __launch_bounds__(kMetaThreads) ibp_meta_kernel(
     const uint32_t* __restrict__ ones, const uint32_t* __restrict__ cols, uint32_t Wn,
     unsigned long long N, uint32_t chunk_bytes, unsigned long long k, double T, int mode,
@@ -109,7 +203,8 @@ __global__ void __launch_bounds__(kMetaThreads) ibp_meta_kernel(
       if (j < B) {
         const unsigned long long o = ones[j];
         const unsigned long long agree = o > N - o ? o : N - o;
-        if (agree >= k) key = ((N - agree) << 32) | j;
+        // low word: position, then its majority value (ties stay by position)
+        if (agree >= k) key = ((N - agree) << 32) | ((unsigned long long)j << 1) | (o >= k ? 1u : 0u);
       }
       keys[j] = key;
     }
@@ -133,37 +228,12 @@ __global__ void __launch_bounds__(kMetaThreads) ibp_meta_kernel(
         __syncthreads();
       }
     }
-    for (uint32_t c = 0; c < Bp; ++c) {
-      const unsigned long long key = keys[c];
-      if (key == ~0ull) break;  // uniform: every thread reads the same key
-      const uint32_t j = (uint32_t)(key & 0xFFFFFFFFu);
-      const uint32_t v = ones[j] >= k ? 1u : 0u;
-      const uint32_t* col = cols + (unsigned long long)j * Wn;
-      uint32_t cnt = 0, keep[8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const uint32_t w = t + r * kMetaThreads;
-        keep[r] = 0;
-        if (w < Wn) {
-          const uint32_t cw = col[w];
-          keep[r] = alive[w] & (v ? cw : ~cw);
-          cnt += __popc(keep[r]);
-        }
-      }
-      const uint32_t tot = block_sum_1024(cnt, red);
-      if (tot >= k) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const uint32_t w = t + r * kMetaThreads;
-          if (w < Wn) alive[w] = keep[r];
-        }
-        if (t == 0) {
-          smask[j >> 5] |= 1u << (j & 31);
-          if (v) sbitv[j >> 5] |= 1u << (j & 31);
-        }
-      }
-      __syncthreads();
-    }
+    // The greedy pass is sequential over candidates: one warp runs it, with
+    // no block barrier per candidate.  Lane l owns words l, l + 32, ... of the
+    // surviving-sample mask; for up to 32 * kGreedyRegs words those stay in
+    // registers and the next candidate's column is loaded while the current
+    // one is decided.
+    if (t < 32) greedy_warp(keys, Bp, ones, cols, Wn, k, alive, smask, sbitv, sbitv + W);
   }
   __syncthreads();
   // write Mask, Bitval and the header
@@ -226,7 +296,8 @@ cudaError_t ibp_launch_build_meta(const void* d_samples, unsigned long long N,
   if (e != cudaSuccess) return e;
   uint32_t Bp = 1;
   while (Bp < B) Bp <<= 1;
-  const size_t smem = (mode == 1 ? 8ull * Bp + 4ull * Wn : 0ull) + 8ull * W;
+  const size_t smem = (mode == 1 ? 8ull * Bp + 4ull * Wn + 4ull * kRing * 32 * kGreedyRegs : 0ull) +
+                      8ull * W;
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(ibp_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

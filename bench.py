@@ -467,6 +467,29 @@ def _case(kind, nbytes, dev, ibp_mode):
         samples = x[idx].contiguous()
         x = x.view(-1)
         n = x.numel()
+    if kind == "table_host":
+        # the table and its stream stay in pinned host memory: the kernels read
+        # them in place over the host link (the output of each op is on the GPU)
+        xd = x
+        xh = xd.cpu().pin_memory()
+        meta = I.build_meta(samples, cb, T=0.9, mode=ibp_mode)
+        st, stn = I.compress(meta, xd, cb)
+        torch.cuda.synchronize()
+        sh = st[: int(stn.item())].cpu().pin_memory()
+        mws = torch.empty(I.workspace_bytes(cb, 0, samples.shape[0]), dtype=torch.uint8, device=dev)
+        iws = torch.empty(I.workspace_bytes(cb, 4 * n, 0), dtype=torch.uint8, device=dev)
+        out = torch.empty(I.max_compressed_bytes(cb, 4 * n), dtype=torch.uint8, device=dev)
+        nb = torch.zeros(1, dtype=torch.int64, device=dev)
+        y = torch.empty_like(xd)
+        dws = torch.empty(256, dtype=torch.uint8, device=dev)
+        ops = [("ibp_build_meta", lambda: I.build_meta(samples, cb, T=0.9, mode=ibp_mode,
+                                                       meta=meta, ws=mws)),
+               ("ibp_compress", lambda: I.compress(meta, xh, cb, out=out, out_bytes=nb, ws=iws)),
+               ("ibp_decompress", lambda: I.decompress(meta, sh, 4 * n, cb, out=y,
+                                                       in_bytes=sh.numel(), ws=dws))]
+        check = lambda: torch.equal(y.view(torch.int32), xd.view(torch.int32)) and torch.equal(  # noqa: E731
+            out[: sh.numel()].cpu(), sh)
+        return ops, (mws, iws, dws), 4 * n, samples.shape[0] * cb, check, nb, cb
     ns = samples.shape[0]
     meta = torch.empty(64 + 2 * cb, dtype=torch.uint8, device=dev)
     mws = torch.empty(I.workspace_bytes(cb, 0, ns), dtype=torch.uint8, device=dev)
@@ -491,7 +514,8 @@ def sweep_arm(args):
     --sizes in MiB): ZipCCL on bf16 N(0, 0.01), one segment, chunk 4096; IBP on
     fp32 N(0, 0.02) weights, 2048-byte chunks (512 values), T = 0.9, metadata
     from 10,000 seeded sample chunks.  --codec table / gradient / moe: the
-    full-size embedding table, gradient-like buffer and MoE activations.
+    full-size embedding table, gradient-like buffer and MoE activations;
+    table_host: the table and its stream in pinned host memory, read in place.
     --only limits the timed ops (the ops before them run once, untimed)."""
     import torch
 
@@ -624,7 +648,7 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="size sweep of both codecs instead of the step (one line per size)")
     ap.add_argument("--codec", default="both",
-                    choices=["both", "zipccl", "ibp", "table", "gradient", "moe"])
+                    choices=["both", "zipccl", "ibp", "table", "table_host", "gradient", "moe"])
     ap.add_argument("--sizes", default="", help="sweep sizes in MiB, comma separated")
     ap.add_argument("--ibp-mode", type=int, default=0, choices=[0, 1])
     ap.add_argument("--only", default="", help="sweep: time only these ops (comma separated)")

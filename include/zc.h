@@ -210,14 +210,23 @@ int ibp_build_meta(const void* d_samples, uint64_t n_samples,
  * kernels (a read-only pass that decides every chunk's participation bit, a
  * scan of the group lengths into the stream's group-offset table, the packing
  * pass); the workspace holds one participation word per group between them.
- * Larger chunks: one memset and one kernel. */
+ * Larger chunks: one memset and one kernel.  d_x and d_out may be pinned host
+ * memory ([IBP] Algoritmo Core step 2: the GPU compresses through zero-copy
+ * unified memory); a host-resident d_x is read with plain loads by the
+ * single-kernel encoder.  Other host memory returns ZC_ERR_ARG. */
 int ibp_compress(const void* d_meta, uint32_t chunk_bytes, const void* d_x,
                  uint64_t n_bytes, void* d_out, uint64_t out_cap,
                  uint64_t* d_out_bytes, void* d_ws, size_t ws_bytes,
                  zc_stream_t stream);
 
 /* [IBP] step 3: decode the IBP1 stream at d_in into d_y (y_cap bytes).  A
- * stream made with other metadata sets ZC_ERR_META_MISMATCH. */
+ * stream made with other metadata sets ZC_ERR_META_MISMATCH.  d_in may be
+ * device memory or pinned host memory (cudaHostAlloc / cudaHostRegister): a
+ * host-resident stream is read in place over the host link, as in [IBP]
+ * Algoritmo Core step 3 (warps read the compressed segment from CPU memory)
+ * and Integrazione del Sistema (tensors kept compressed in CPU memory), with
+ * no separate copy.  d_y may be pinned host memory too.  Other host memory
+ * returns ZC_ERR_ARG.  d_meta and d_ws are device memory. */
 int ibp_decompress(const void* d_meta, uint32_t chunk_bytes, const void* d_in,
                    uint64_t in_bytes, void* d_y, uint64_t y_cap, void* d_ws,
                    size_t ws_bytes, zc_stream_t stream);

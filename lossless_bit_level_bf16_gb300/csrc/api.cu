@@ -53,6 +53,25 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? ZC_OK : ZC_ERR_CUDA; }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Whether the GPU can reach *p: device memory, or pinned host memory (then
+// *host is set and *p becomes its device-side address).  Unregistered host
+// memory is not reachable.
+bool reachable(const void** p, bool* host) {
+  *host = false;
+  if (!*p) return true;
+  cudaPointerAttributes pa{};
+  if (cudaPointerGetAttributes(&pa, *p) != cudaSuccess) {
+    cudaGetLastError();  // clear the lookup's error; treat as device memory
+    return true;
+  }
+  if (pa.type == cudaMemoryTypeUnregistered) return false;
+  if (pa.type == cudaMemoryTypeHost) {
+    *host = true;
+    if (pa.devicePointer) *p = pa.devicePointer;
+  }
+  return true;
+}
+
 size_t zc_ws_bytes(const lbb::ZcLayout& L) {
   const unsigned long long a = L.nunits * sizeof(lbb::StatPartial);
   const unsigned long long b = L.ntiles * 8ull;
@@ -298,9 +317,14 @@ int ibp_compress(const void* d_meta, uint32_t cb, const void* d_x, uint64_t n_by
   if (ws_bytes < ibp_workspace_bytes(cb, n_bytes, 0)) return ZC_ERR_CAPACITY;
   const unsigned long long nch = (n_bytes + cb - 1) / cb, ng = (nch + 31) / 32;
   if (out_cap < lbb::kIbp1Header + lbb::round_up_dev(8ull * (ng + 1), 128)) return ZC_ERR_CAPACITY;
+  // input and stream may be pinned host memory (zero-copy)
+  bool x_host = false, out_host = false;
+  const void* o = d_out;
+  if (!reachable(&d_x, &x_host) || !reachable(&o, &out_host)) return ZC_ERR_ARG;
+  d_out = const_cast<void*>(o);
   return cuda_rc(lbb::ibp_launch_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap,
                                           reinterpret_cast<unsigned long long*>(d_out_bytes),
-                                          d_ws, (cudaStream_t)stream));
+                                          d_ws, (cudaStream_t)stream, x_host));
 }
 
 int ibp_decompress(const void* d_meta, uint32_t cb, const void* d_in, uint64_t in_bytes,
@@ -309,8 +333,13 @@ int ibp_decompress(const void* d_meta, uint32_t cb, const void* d_in, uint64_t i
   if (!aligned(d_meta, 16) || !aligned(d_in, 16) || !aligned(d_y, 16) || !aligned(d_ws, 256))
     return ZC_ERR_ARG;
   if (ws_bytes < kCtrlBytes) return ZC_ERR_CAPACITY;
+  // the stream may stay in pinned host memory: it is then read in place
+  bool in_host = false, out_host = false;
+  const void* yo = d_y;
+  if (!reachable(&d_in, &in_host) || !reachable(&yo, &out_host)) return ZC_ERR_ARG;
+  d_y = const_cast<void*>(yo);
   return cuda_rc(lbb::ibp_launch_decompress(d_meta, cb, d_in, in_bytes, d_y, y_cap, d_ws,
-                                            (cudaStream_t)stream));
+                                            (cudaStream_t)stream, in_host));
 }
 
 }  // extern "C"

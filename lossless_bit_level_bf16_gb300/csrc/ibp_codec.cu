@@ -430,7 +430,7 @@ int wpl_for(uint32_t cb) {
 cudaError_t ibp_launch_compress(const void* d_meta, uint32_t cb, const void* d_x,
                                 unsigned long long n_bytes, void* d_out,
                                 unsigned long long out_cap, unsigned long long* d_out_bytes,
-                                void* d_ws, cudaStream_t s) {
+                                void* d_ws, cudaStream_t s, bool x_host) {
   IbpEncArgs A;
   A.meta = static_cast<const uint8_t*>(d_meta);
   A.x = static_cast<const uint32_t*>(d_x);
@@ -446,7 +446,7 @@ cudaError_t ibp_launch_compress(const void* d_meta, uint32_t cb, const void* d_x
   A.states = reinterpret_cast<unsigned long long*>(static_cast<char*>(d_ws) + kCtrlBytes);
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 8ull * A.ngroups, s);
   if (e != cudaSuccess) return e;
-  if (ibp_pipe_supported(cb, true))
+  if (!x_host && ibp_pipe_supported(cb, true))
     return ibp_pipe_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap, d_out_bytes, d_ws, s);
   const bool vec = (cb % 512) == 0;
   switch (wpl_for(cb)) {
@@ -459,7 +459,8 @@ cudaError_t ibp_launch_compress(const void* d_meta, uint32_t cb, const void* d_x
 
 cudaError_t ibp_launch_decompress(const void* d_meta, uint32_t cb, const void* d_in,
                                   unsigned long long in_bytes, void* d_y,
-                                  unsigned long long y_cap, void* d_ws, cudaStream_t s) {
+                                  unsigned long long y_cap, void* d_ws, cudaStream_t s,
+                                  bool in_host) {
   IbpDecArgs A;
   A.meta = static_cast<const uint8_t*>(d_meta);
   A.in = static_cast<const uint8_t*>(d_in);
@@ -470,7 +471,7 @@ cudaError_t ibp_launch_decompress(const void* d_meta, uint32_t cb, const void* d
   A.ctrl = static_cast<Ctrl*>(d_ws);
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes, s);
   if (e != cudaSuccess) return e;
-  if (ibp_pipe_supported(cb, false))
+  if (!in_host && ibp_pipe_supported(cb, false))
     return ibp_pipe_decompress(d_meta, cb, d_in, in_bytes, d_y, y_cap, d_ws, s);
   const bool vec = (cb % 512) == 0;
   switch (wpl_for(cb)) {

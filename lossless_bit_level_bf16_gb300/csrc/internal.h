@@ -68,15 +68,19 @@ cudaError_t ibp_launch_build_meta(const void* d_samples, unsigned long long N,
                                   uint32_t chunk_bytes, unsigned long long k,
                                   double T, int mode, void* d_meta, void* d_ws,
                                   cudaStream_t s);
+// x_host: d_x is pinned host memory, read with plain loads by the
+// single-kernel encoder (no bulk copies from system memory).
 cudaError_t ibp_launch_compress(const void* d_meta, uint32_t chunk_bytes,
                                 const void* d_x, unsigned long long n_bytes,
                                 void* d_out, unsigned long long out_cap,
                                 unsigned long long* d_out_bytes, void* d_ws,
-                                cudaStream_t s);
+                                cudaStream_t s, bool x_host);
+// in_host: d_in is pinned host memory, read in place over the host link by
+// the plain-load decoder (no bulk copies from system memory).
 cudaError_t ibp_launch_decompress(const void* d_meta, uint32_t chunk_bytes,
                                   const void* d_in, unsigned long long in_bytes,
                                   void* d_y, unsigned long long y_cap,
-                                  void* d_ws, cudaStream_t s);
+                                  void* d_ws, cudaStream_t s, bool in_host);
 
 // TMA-pipelined IBP kernels (ibp_pipe.cu) for chunks of up to 2048 bytes;
 // the launchers above use them whenever ibp_pipe_supported says so.

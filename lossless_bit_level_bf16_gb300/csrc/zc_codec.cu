@@ -277,19 +277,24 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     };
     // escaped exponent fields, in slot order, from the lane's 16 words
     // (the stash is the step's ring slot, free once every lane has read it)
+    // (each lane's 64 bytes go to the slot as four 16-byte pieces, piece j at
+    // 4 * lane + (j ^ ((lane >> 1) & 3)), so each store instruction of the warp
+    // spreads over all eight 16-byte bank groups)
     auto put_escapes = [&](const uint32_t(&w)[16], uint32_t esc, uint32_t pos, uint8_t* dst,
                            uint32_t cap, uint8_t* slotbuf) {
       __syncwarp();
-      uint4* stash = reinterpret_cast<uint4*>(slotbuf + 64u * lane);
-      stash[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      stash[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      stash[2] = make_uint4(w[8], w[9], w[10], w[11]);
-      stash[3] = make_uint4(w[12], w[13], w[14], w[15]);
-      const uint16_t* h = reinterpret_cast<const uint16_t*>(stash);
+      uint4* st4 = reinterpret_cast<uint4*>(slotbuf);
+      const uint32_t sw = ((uint32_t)lane >> 1) & 3u, b4 = 4u * lane;
+      st4[b4 + (0u ^ sw)] = make_uint4(w[0], w[1], w[2], w[3]);
+      st4[b4 + (1u ^ sw)] = make_uint4(w[4], w[5], w[6], w[7]);
+      st4[b4 + (2u ^ sw)] = make_uint4(w[8], w[9], w[10], w[11]);
+      st4[b4 + (3u ^ sw)] = make_uint4(w[12], w[13], w[14], w[15]);
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(slotbuf);
       while (esc) {
-        const int i = __ffs(esc) - 1;
+        const uint32_t i = (uint32_t)__ffs(esc) - 1u;
         esc &= esc - 1;
-        if (pos < cap) dst[pos] = (uint8_t)((h[i] >> 7) & 0xFFu);
+        const uint32_t hv = h[(b4 + ((i >> 3) ^ sw)) * 8u + (i & 7u)];
+        if (pos < cap) dst[pos] = (uint8_t)((hv >> 7) & 0xFFu);
         ++pos;
       }
     };

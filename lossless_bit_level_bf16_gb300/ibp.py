@@ -53,21 +53,34 @@ def build_meta(samples: torch.Tensor, chunk_bytes: int, T: float = 0.9, mode: in
     return meta
 
 
+def _reachable(x: torch.Tensor, name: str):
+    """A CUDA tensor, or a pinned host tensor the GPU reads in place."""
+    if not (x.is_cuda or x.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return x
+
+
 def compress(meta: torch.Tensor, x: torch.Tensor, chunk_bytes: int, out: torch.Tensor | None = None,
              out_bytes: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None):
     """ibp_compress: returns (stream uint8 tensor, out_bytes int64[1] tensor)
-    on the device; nothing is synchronised."""
+    on the device; nothing is synchronised.  ``x`` and ``out`` may be pinned
+    host tensors (read and written in place over the host link)."""
     lib = abi.load()
-    x = _dev_tensor(x, "x")
+    x = _reachable(x, "x")
+    if out is not None:
+        _reachable(out, "out")
+    dev = meta.device  # workspace and size word live on the metadata's GPU
     n_bytes = x.numel() * x.element_size()
     if out is None:
         out = torch.empty(max_compressed_bytes(chunk_bytes, n_bytes), dtype=torch.uint8,
-                          device=x.device)
+                          device=dev)
     if out_bytes is None:
-        out_bytes = torch.zeros(1, dtype=torch.int64, device=x.device)
+        out_bytes = torch.zeros(1, dtype=torch.int64, device=dev)
     if ws is None:
         ws = torch.empty(max(workspace_bytes(chunk_bytes, n_bytes, 0), 256), dtype=torch.uint8,
-                         device=x.device)
+                         device=dev)
     abi.check(lib.ibp_compress(abi.ptr(meta), chunk_bytes, abi.ptr(x), n_bytes, abi.ptr(out),
                                out.numel(), abi.ptr(out_bytes), abi.ptr(ws), ws.numel(),
                                abi.stream_handle(stream)), "ibp_compress")
@@ -79,13 +92,20 @@ def decompress(meta: torch.Tensor, stream_bytes: torch.Tensor, n_bytes: int, chu
                out: torch.Tensor | None = None, in_bytes: int | None = None,
                ws: torch.Tensor | None = None, stream=None, dtype=torch.float32):
     """ibp_decompress: decode into a new tensor of ``n_bytes`` bytes viewed as
-    ``dtype`` (or into ``out``)."""
+    ``dtype`` (or into ``out``).  ``stream_bytes`` may be a pinned host tensor:
+    the kernel then reads the stream in place over the host link."""
     lib = abi.load()
+    _reachable(stream_bytes, "stream_bytes")
+    if out is not None:
+        _reachable(out, "out")
+    # a pinned host stream is decoded in place; by default the output lives
+    # on the metadata's GPU
+    dev = meta.device
     if out is None:
         esize = torch.empty(0, dtype=dtype).element_size()
-        out = torch.empty(n_bytes // esize, dtype=dtype, device=stream_bytes.device)
+        out = torch.empty(n_bytes // esize, dtype=dtype, device=dev)
     if ws is None:
-        ws = torch.empty(256, dtype=torch.uint8, device=stream_bytes.device)
+        ws = torch.empty(256, dtype=torch.uint8, device=dev)
     if in_bytes is None:
         in_bytes = stream_bytes.numel()
     abi.check(lib.ibp_decompress(abi.ptr(meta), chunk_bytes, abi.ptr(stream_bytes), in_bytes,

@@ -208,3 +208,48 @@ def test_errors_reported():
     I.compress(md, x, 1024, ws=ws)
     torch.cuda.synchronize()
     assert I.status(ws) == abi.ZC_ERR_META_MISMATCH
+
+
+@pytest.mark.parametrize("cb", [512, 2048])
+def test_host_resident_input_and_streams(cb):
+    """Pinned host tensors as encode input, encode output, decode input and
+    decode output (read and written in place by the kernels) give the same
+    bytes as the all-device path; pageable host memory is refused."""
+    import ctypes as C
+
+    rows = 3000 if cb == 512 else 1500
+    x, idx = W.ibp_table(rows=rows, cols=cb // 4, std=0.1, seed=5, device=DEV, n_samples=400)
+    x = x.reshape(-1)
+    meta = I.build_meta(x.view(-1, cb // 4)[idx].contiguous(), cb, T=0.9, mode=1)
+    n = x.numel() * 4
+    ref, nb = I.compress(meta, x, cb)
+    torch.cuda.synchronize()
+    total = int(nb.item())
+    ref = ref[:total].clone()
+    # host input
+    xh = x.cpu().pin_memory()
+    st, nb2 = I.compress(meta, xh, cb)
+    torch.cuda.synchronize()
+    assert int(nb2.item()) == total and torch.equal(st[:total], ref)
+    # host output
+    oh = torch.full((I.max_compressed_bytes(cb, n),), 0xA5, dtype=torch.uint8, pin_memory=True)
+    nb3 = torch.zeros(1, dtype=torch.int64, device=DEV)
+    I.compress(meta, x, cb, out=oh, out_bytes=nb3)
+    torch.cuda.synchronize()
+    assert int(nb3.item()) == total and torch.equal(oh[:total], ref.cpu())
+    # host stream in, device out; device stream in, host out
+    sh = ref.cpu().pin_memory()
+    y = I.decompress(meta, sh, n, cb, in_bytes=total)
+    yh = torch.empty(x.numel(), dtype=torch.float32, pin_memory=True)
+    I.decompress(meta, ref, n, cb, out=yh, in_bytes=total)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), x.view(torch.int32))
+    assert torch.equal(yh.view(torch.int32), x.cpu().view(torch.int32))
+    # pageable host memory: refused by the host checks, nothing reaches the GPU
+    page = ref.cpu()
+    assert not page.is_pinned()
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+    out = torch.empty(x.numel(), dtype=torch.float32, device=DEV)
+    rc = abi.load().ibp_decompress(abi.ptr(meta), cb, C.c_void_p(page.data_ptr()), total,
+                                   abi.ptr(out), n, abi.ptr(ws), 256, abi.stream_handle(None))
+    assert rc == abi.ZC_ERR_ARG

@@ -455,7 +455,16 @@ def _case(kind, nbytes, dev, ibp_mode):
                ("zc_decompress", lambda: Z.decompress(out, out=y, in_bytes=out.numel(), ws=dws))]
         check = lambda: torch.equal(y.view(torch.int16), x.view(torch.int16))  # noqa: E731
         return ops, (plan.ws, dws), 2 * n, 0, check, nb, 4096
-    if kind == "ibp":
+    if kind == "ibp16":
+        # 16-bit weights: bf16 N(0, 0.02), 512-byte chunks (256 values); the
+        # codec sees bytes, so the tensor is handled as 32-bit words
+        cb = 512
+        x16 = W.zc_gaussian(nbytes // 2, sigma=0.02, seed=0, device=dev)
+        x = x16.view(torch.int32).view(torch.float32)
+        n = x.numel()
+        idx = W.sample_rows(4 * n // cb, 10_000, seed=1, device=dev)
+        samples = x.view(-1, cb // 4)[idx].contiguous()
+    elif kind == "ibp":
         cb = 2048
         n = nbytes // 4
         x = W.ibp_gaussian(n, std=0.02, seed=0, device=dev)
@@ -515,7 +524,8 @@ def sweep_arm(args):
     fp32 N(0, 0.02) weights, 2048-byte chunks (512 values), T = 0.9, metadata
     from 10,000 seeded sample chunks.  --codec table / gradient / moe: the
     full-size embedding table, gradient-like buffer and MoE activations;
-    table_host: the table and its stream in pinned host memory, read in place.
+    table_host: the table and its stream in pinned host memory, read in place;
+    ibp16: IBP on bf16 N(0, 0.02) weights in 512-byte chunks (size sweep).
     --only limits the timed ops (the ops before them run once, untimed)."""
     import torch
 
@@ -529,7 +539,7 @@ def sweep_arm(args):
         else list(W.SWEEP_BYTES)
     kinds = {"both": ["zipccl", "ibp"]}.get(args.codec, [args.codec])
     for kind in kinds:
-        for nbytes in (sizes if kind in ("zipccl", "ibp") else [0]):
+        for nbytes in (sizes if kind in ("zipccl", "ibp", "ibp16") else [0]):
             ops, wss, unc, sbytes, check, nb, cb = _case(kind, nbytes, dev, args.ibp_mode)
             if args.only:
                 names = args.only.split(",")
@@ -648,7 +658,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="size sweep of both codecs instead of the step (one line per size)")
     ap.add_argument("--codec", default="both",
-                    choices=["both", "zipccl", "ibp", "table", "table_host", "gradient", "moe"])
+                    choices=["both", "zipccl", "ibp", "ibp16", "table", "table_host", "gradient",
+                             "moe"])
     ap.add_argument("--sizes", default="", help="sweep sizes in MiB, comma separated")
     ap.add_argument("--ibp-mode", type=int, default=0, choices=[0, 1])
     ap.add_argument("--only", default="", help="sweep: time only these ops (comma separated)")

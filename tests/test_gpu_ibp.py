@@ -253,3 +253,29 @@ def test_host_resident_input_and_streams(cb):
     rc = abi.load().ibp_decompress(abi.ptr(meta), cb, C.c_void_p(page.data_ptr()), total,
                                    abi.ptr(out), n, abi.ptr(ws), 256, abi.stream_handle(None))
     assert rc == abi.ZC_ERR_ARG
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_bf16_weights(mode):
+    """IBP on 16-bit data: bf16 N(0, 0.02) weights in 512-byte chunks (256
+    values).  The codec sees bytes; metadata and stream must equal the
+    oracle's, the round trip must be exact, and the sign/exponent bits that
+    the weights share make the stream smaller than the input."""
+    cb = 512
+    x16 = W.zc_gaussian(256 * 1000 + 128, sigma=0.02, seed=21, device=DEV)  # ragged last chunk
+    xb = W.bf16_bits(x16).view("uint8")
+    x32 = x16.view(torch.int32).view(torch.float32)
+    idx = W.sample_rows(x32.numel() * 4 // cb, 600, seed=2, device=DEV)
+    samples = x32[: (x32.numel() * 4 // cb) * (cb // 4)].view(-1, cb // 4)[idx].contiguous()
+    meta = I.build_meta(samples, cb, T=0.9, mode=mode)
+    st, nb = I.compress(meta, x32, cb)
+    torch.cuda.synchronize()
+    total = int(nb.item())
+    m_ref = O.ibp_build_meta(W.f32_bytes(samples), cb, T=0.9, mode=mode)
+    assert np.array_equal(meta.cpu().numpy(), m_ref)
+    s_ref = O.ibp_encode(m_ref, xb)
+    assert np.array_equal(st[:total].cpu().numpy(), s_ref)
+    y = I.decompress(meta, st, x32.numel() * 4, cb, in_bytes=total)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), x32.view(torch.int32))
+    assert total < xb.size

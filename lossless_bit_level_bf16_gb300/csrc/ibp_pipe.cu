@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
   VecTab vt;
   if (REG) {
     load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
-    // (decode keeps the move masks)
+    make_runs(vt);
   }
 
   // warp 0: the span of this block's kk-th tile.  prefetch() loads its
@@ -806,13 +806,27 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
         const uint32_t off = s_off[bf][q][i];
         uint32_t u[4];
         if ((s_pw[bf][q] >> i) & 1u) {
-          win128(sd, off + vt.Pr, u);
-          uint32_t f[4];
-          uint32_t kk[4];
-          kept_bits(vt, kk);
-          split4(u, kk, f);
+          if (REG && vt.fast) {
+            // each word's field read at its own bit offset, expanded from runs
+            uint32_t pos = off + vt.Pr;
 #pragma unroll
-          for (int w = 0; w < 4; ++w) o[e][w] = hd_expand(f[w], vt.K[w], &vt.MV[0][w], 4) | vt.V[w];
+            for (int w = 0; w < 4; ++w) {
+              const uint32_t kw = __popc(vt.K[w]);
+              const uint32_t a = pos >> 5, sh = pos & 31;
+              uint32_t f = __funnelshift_r(sd[a], sd[a + 1], sh);
+              f &= kw >= 32 ? 0xFFFFFFFFu : ((1u << kw) - 1u);
+              o[e][w] = vt_expand(vt, f, w) | vt.V[w];
+              pos += kw;
+            }
+          } else {
+            win128(sd, off + vt.Pr, u);
+            uint32_t f[4];
+            uint32_t kk[4];
+            kept_bits(vt, kk);
+            split4(u, kk, f);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) o[e][w] = hd_expand(f[w], vt.K[w], &vt.MV[0][w], 4) | vt.V[w];
+          }
         } else {
           win128(sd, off + 128u * r, u);
 #pragma unroll

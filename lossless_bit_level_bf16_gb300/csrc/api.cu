@@ -133,10 +133,11 @@ int zc_plan_create(uint64_t n, const uint64_t* h_seg_off, uint32_t nseg, uint32_
   L.C = C;
   L.log2C = 0;
   while ((1u << L.log2C) < C) ++L.log2C;
-  // statistics unit: a power of two between 4096 and 16384 elements, fixed by n
-  // (one block of the statistics kernel; small units keep its tail wave short)
+  // statistics unit: a power of two between 4096 and 16384 elements, fixed by
+  // n (one warp of the statistics kernel; small units keep its tail short:
+  // 16384 units or more once they are 16384 elements)
   unsigned long long U = 4096;
-  while (U < 16384 && U * 2 <= n / 1024) U *= 2;
+  while (U < 16384 && U * 2 <= n / 16384) U *= 2;
   L.U = (uint32_t)U;
   try {
     p->h_segs.resize(nseg);

@@ -169,6 +169,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launches
+//
+// A kernel launched with programmatic stream serialization (launch_dependent
+// in internal.h) may start while the kernel before it on the stream is still
+// finishing: it does its set-up, then grid_dep_wait() returns once that kernel
+// has completed and its writes are visible.  grid_dep_launch() lets the next
+// such kernel start.  Both do nothing in a kernel launched the ordinary way.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
   return __byte_perm(a, b, s);
 }

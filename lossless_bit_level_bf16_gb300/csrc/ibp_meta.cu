@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(256) ibp_columns_kernel(
     const uint32_t* __restrict__ samples, unsigned long long N, uint32_t W,
     uint32_t* __restrict__ ones, uint32_t* __restrict__ cols, uint32_t Wn, int keep_cols) {
   const int lane = threadIdx.x & 31;
+  grid_dep_launch();  // the metadata kernel may be scheduled as blocks finish
   const unsigned long long warp = (blockIdx.x * 256ull + threadIdx.x) >> 5;
   const uint32_t wgroups = (W + kWordsPerWarp - 1) / kWordsPerWarp;
   const unsigned long long sb = warp / wgroups;  // block of 32 samples
@@ -176,6 +177,7 @@ __global__ void __launch_bounds__(kMetaThreads) ibp_meta_kernel(
   uint32_t* alive = reinterpret_cast<uint32_t*>(dyn + (mode == 1 ? 8ull * Bp : 0ull));
   uint32_t* smask = alive + (mode == 1 ? Wn : 0u);
   uint32_t* sbitv = smask + W;
+  grid_dep_wait();  // the ones counts and bit columns
 
   for (uint32_t w = t; w < W; w += kMetaThreads) {
     smask[w] = 0;
@@ -304,9 +306,9 @@ cudaError_t ibp_launch_build_meta(const void* d_samples, unsigned long long N,
                              (int)smem);
     if (e != cudaSuccess) return e;
   }
-  ibp_meta_kernel<<<1, kMetaThreads, smem, s>>>(ones, cols, Wn, N, chunk_bytes, k, T, mode, Bp,
-                                                static_cast<uint8_t*>(d_meta));
-  return cudaGetLastError();
+  return launch_dependent(ibp_meta_kernel, 1u, (unsigned)kMetaThreads, smem, s,
+                          static_cast<const uint32_t*>(ones), static_cast<const uint32_t*>(cols),
+                          Wn, N, chunk_bytes, k, T, mode, Bp, static_cast<uint8_t*>(d_meta));
 }
 
 }  // namespace lbb

@@ -270,6 +270,7 @@ __global__ void __launch_bounds__(256) ibp_match_kernel(MatchArgs A) {
   extern __shared__ __align__(128) uint8_t dyn[];
   __shared__ uint32_t s_scr[256 / 32 + 4];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  grid_dep_launch();  // the offsets kernel may be scheduled as blocks finish
   IbpTables T;
   const bool ok = ibp_load_tables<256>(A.meta, A.cb, reinterpret_cast<uint32_t*>(dyn), T, s_scr);
   if (!ok) {
@@ -383,6 +384,8 @@ __global__ void __launch_bounds__(kOffNT) ibp_offsets_kernel(OffArgs A) {
   const int t = threadIdx.x, warp = t >> 5;
   const uint32_t m = reinterpret_cast<const uint32_t*>(A.meta)[4];
   const unsigned long long tail_bytes = A.n_bytes - (A.nchunks ? (A.nchunks - 1) * A.cb : 0ull);
+  grid_dep_wait();    // the match kernel's participation words
+  grid_dep_launch();  // the pack kernel may start its set-up
   if (t == 0) s_tile = atomicAdd(&A.ctrl->ticket, 1ull);
   __syncthreads();
   const unsigned long long tile = s_tile;
@@ -498,6 +501,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
   };
   if (t == 0)
     for (uint32_t s = 0; s < S; ++s) mbar_init(bars + s, 1);
+  grid_dep_wait();  // the participation words and the group-offset table
   __syncthreads();
   if (warp == 0)
     for (uint32_t s = 0; s < S; ++s) {
@@ -986,14 +990,16 @@ cudaError_t launch(K k, int nt, const Args& A, size_t smem, unsigned long long w
   return cudaGetLastError();
 }
 
+// dep: launched with launch_dependent (the kernel calls grid_dep_wait()).
 template <typename K>
 cudaError_t launch(K k, int nt, const PipeArgs& A, const Geo& g, unsigned long long work,
-                   cudaStream_t s) {
+                   cudaStream_t s, bool dep = false) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
   if (e != cudaSuccess) return e;
   const int res = resident_blocks((const void*)k, nt, g.smem);
   unsigned long long grid = work < (unsigned long long)res ? work : (unsigned long long)res;
   if (grid == 0) grid = 1;
+  if (dep) return launch_dependent(k, (unsigned)grid, (unsigned)nt, g.smem, s, A);
   k<<<(unsigned)grid, nt, g.smem, s>>>(A);
   return cudaGetLastError();
 }
@@ -1061,8 +1067,7 @@ cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t cb, const void* d_x,
     O.grp = grp;
     O.ctrl = ctrl;
     O.states = states;
-    ibp_offsets_kernel<<<(unsigned)ntiles2, kOffNT, 0, s>>>(O);
-    e = cudaGetLastError();
+    e = launch_dependent(ibp_offsets_kernel, (unsigned)ntiles2, kOffNT, 0, s, O);
     if (e != cudaSuccess) return e;
   }
   PipeArgs A{};
@@ -1081,14 +1086,15 @@ cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t cb, const void* d_x,
   A.ctrl = ctrl;
   fill_shape(A, g);
   const unsigned long long w = A.ntiles;
+  const bool dep = ngroups != 0;  // after the offsets kernel
   if (g.nt == 128)
-    return g.reg ? launch(ibp_pack_kernel<128, true>, 128, A, g, w, s)
-                 : launch(ibp_pack_kernel<128, false>, 128, A, g, w, s);
+    return g.reg ? launch(ibp_pack_kernel<128, true>, 128, A, g, w, s, dep)
+                 : launch(ibp_pack_kernel<128, false>, 128, A, g, w, s, dep);
   if (g.nt == 256)
-    return g.reg ? launch(ibp_pack_kernel<256, true>, 256, A, g, w, s)
-                 : launch(ibp_pack_kernel<256, false>, 256, A, g, w, s);
-  return g.reg ? launch(ibp_pack_kernel<512, true>, 512, A, g, w, s)
-               : launch(ibp_pack_kernel<512, false>, 512, A, g, w, s);
+    return g.reg ? launch(ibp_pack_kernel<256, true>, 256, A, g, w, s, dep)
+                 : launch(ibp_pack_kernel<256, false>, 256, A, g, w, s, dep);
+  return g.reg ? launch(ibp_pack_kernel<512, true>, 512, A, g, w, s, dep)
+               : launch(ibp_pack_kernel<512, false>, 512, A, g, w, s, dep);
 }
 
 cudaError_t ibp_pipe_decompress(const void* d_meta, uint32_t cb, const void* d_in,

@@ -96,6 +96,26 @@ cudaError_t ibp_pipe_decompress(const void* d_meta, uint32_t chunk_bytes, const 
 // Blocks of `kernel` resident per SM times SMs on the current device.
 int resident_blocks(const void* kernel, int threads, size_t smem);
 
+// Launches a kernel that depends on the kernel launched just before it on the
+// same stream with programmatic stream serialization: its blocks may start
+// while that kernel finishes, and must call grid_dep_wait() (common.cuh)
+// before reading what it wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*k)(KArgs...), unsigned grid, unsigned threads, size_t smem,
+                             cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 }  // namespace lbb
 
 // A ZipCCL plan (the opaque zc_plan_t of zc.h): layout, the device segment

@@ -12,16 +12,22 @@
 //                      values.  HBM-bound: 2 bytes read per element.
 //   zc_predict_kernel  one block per segment: adds the unit partials in a
 //                      fixed order, forms mu and sigma, evaluates the Gaussian
-//                      mass of every exponent field and keeps the 7 largest.
+//                      mass of the exponent fields and keeps the 7 largest.
 //                      fp64 is slow on this part, so each field edge's erfc
-//                      pair is computed once and the masses are ranked as
-//                      integers (their fp64 bit patterns).
+//                      ranking is done in fp32 unless the 7th and 8th masses
+//                      are too close for fp32 to tell apart; then each field
+//                      edge's erfc pair is computed once in fp64, only around
+//                      the distribution's scale when bounds show that no
+//                      other field can be among the 7, and the masses are
+//                      ranked as integers (their fp64 bit patterns).
 //
 // Arithmetic of the statistics pass: the 16 values a thread holds are summed
 // (and their squares, exact in fp32 for bf16 inputs) as an fp32 tree (error
 // at most 4 units in the last place of the sum of magnitudes), the tree sums
-// are accumulated as unevaluated fp32 pairs (error-free two-sum), and the
-// warp reduction is fp64.  A group of 16 whose fp32 sums are not finite (an
+// are accumulated as unevaluated fp32 pairs (error-free two-sum), the pairs
+// of a unit's lanes are added as pairs too, and only the unit's total is
+// formed in fp64 (an fp64 tree when a pair overflows fp32).  A
+// group of 16 whose fp32 sums are not finite (an
 // inf/NaN input or an fp32 overflow) is redone element by element in fp64,
 // skipping non-finite values.  The whole pass is deterministic for a given
 // plan: the partition into units and every reduction order are fixed.
@@ -63,25 +69,50 @@ __device__ __forceinline__ int find_unit_segment(const ZcSegDev* segs, uint32_t 
   return lo;
 }
 
-// One warp per statistics unit (grid-stride over units, so the partition and
-// every reduction order depend only on the plan).  A step is 512 values: lane
-// l takes 8 at base + 8l and 8 at base + 256 + 8l, so each 16-byte load
-// instruction of the warp reads 512 contiguous bytes; kStatBatch steps are
-// loaded before any is summed.  No block barriers: a warp's loads overlap
-// other warps' sums.
+// One warp per statistics unit; warp w of the grid takes a contiguous range
+// of units, the same number (to one) as every other warp, and follows the
+// segments along it after one search.  A step is 512 values: lane l takes 8
+// at base + 8l and 8 at base + 256 + 8l, so each 16-byte load instruction of
+// the warp reads 512 contiguous bytes; kStatBatch steps are loaded before any
+// is summed.  No block barriers: a warp's loads overlap other warps' sums.
+// The lanes' sums are added as fp32 (sum, error) pairs in a fixed tree order
+// and only the unit's total goes to fp64 (fp64 is slow on this part); a pair
+// that overflows fp32, or values already summed in fp64, take an fp64 tree of
+// the same shape.  A unit's sums do not depend on which warp computes them:
+// the partition into units and every order of addition depend only on the
+// plan.
 constexpr int kStatWarps = kThreads / 32;
+
+// (a, b) += (a2, b2) for fp32 (sum, error) pairs: a takes the rounded sum of
+// the sums, b the error of that addition and the errors so far.
+__device__ __forceinline__ void pair_add(float& a, float& b, float a2, float b2) {
+  two_sum_acc(a, b, a2);
+  b = __fadd_rn(b, b2);
+}
 
 __global__ void __launch_bounds__(kThreads, 3) zc_stats_kernel(
     const uint16_t* __restrict__ x, const ZcSegDev* __restrict__ segs, uint32_t nseg,
     uint32_t U, unsigned long long nunits, StatPartial* __restrict__ parts, int x_al16) {
   const int lane = threadIdx.x & 31;
-  const unsigned long long nwarps = (unsigned long long)gridDim.x * kStatWarps;
-  for (unsigned long long unit = (unsigned long long)blockIdx.x * kStatWarps + (threadIdx.x >> 5);
-       unit < nunits; unit += nwarps) {
+  grid_dep_launch();  // the predictor may be scheduled as blocks finish
+  unsigned long long ub;
+  uint32_t nu;  // this warp's units: ub .. ub + nu - 1
+  {
+    const unsigned long long nwarps = (unsigned long long)gridDim.x * kStatWarps;
+    const unsigned long long gw = (unsigned long long)blockIdx.x * kStatWarps + (threadIdx.x >> 5);
+    const unsigned long long q = nunits / nwarps, r = nunits % nwarps;
+    ub = gw * q + (gw < r ? gw : r);
+    nu = (uint32_t)(q + (gw < r ? 1 : 0));
+  }
+  int sc = -1;  // lane 0: segment of the current unit
+  for (uint32_t k = 0; k < nu; ++k) {
+    const unsigned long long unit = ub + k;
     unsigned long long lo = 0, hi = 0;
     int al = 0;
     if (lane == 0) {
-      const int s = find_unit_segment(segs, nseg, unit);
+      if (sc < 0) sc = find_unit_segment(segs, nseg, unit);
+      while (sc + 1 < (int)nseg && segs[sc + 1].unit_start <= unit) ++sc;
+      const int s = sc;
       lo = segs[s].elem_start + (unit - segs[s].unit_start) * U;
       const unsigned long long e = segs[s].elem_start + segs[s].nelem;
       hi = (lo + U < e) ? lo + U : e;
@@ -158,13 +189,29 @@ __global__ void __launch_bounds__(kThreads, 3) zc_stats_kernel(
         }
       }
     }
-    double t1 = __dadd_rn(__dadd_rn((double)hx, (double)lx), dx);
-    double t2 = __dadd_rn(__dadd_rn((double)hq, (double)lq), dq);
+    // lanes: fp32 pairs, fp64 if a pair overflows or fp64 sums exist
+    float ax = hx, bx = lx, aq = hq, bq = lq;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      t1 = __dadd_rn(t1, __shfl_down_sync(kFull, t1, o));
-      t2 = __dadd_rn(t2, __shfl_down_sync(kFull, t2, o));
+      const float ax2 = __shfl_down_sync(kFull, ax, o), bx2 = __shfl_down_sync(kFull, bx, o);
+      const float aq2 = __shfl_down_sync(kFull, aq, o), bq2 = __shfl_down_sync(kFull, bq, o);
+      pair_add(ax, bx, ax2, bx2);
+      pair_add(aq, bq, aq2, bq2);
       cnt += __shfl_down_sync(kFull, cnt, o);
+    }
+    const bool fin = __shfl_sync(kFull, isfinite(ax) && isfinite(bx) && isfinite(aq) && isfinite(bq), 0);
+    double t1, t2;
+    if (!fin || __any_sync(kFull, dx != 0.0 || dq != 0.0)) {
+      t1 = __dadd_rn(__dadd_rn((double)hx, (double)lx), dx);
+      t2 = __dadd_rn(__dadd_rn((double)hq, (double)lq), dq);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        t1 = __dadd_rn(t1, __shfl_down_sync(kFull, t1, o));
+        t2 = __dadd_rn(t2, __shfl_down_sync(kFull, t2, o));
+      }
+    } else {
+      t1 = __dadd_rn((double)ax, (double)bx);
+      t2 = __dadd_rn((double)aq, (double)bq);
     }
     if (lane == 0) {
       parts[unit].cnt = cnt;
@@ -215,8 +262,13 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
   __shared__ double s_em[256], s_ep[256];
   __shared__ unsigned long long s_key[256];
   __shared__ int s_take[256];
+  __shared__ double s_m7, s_hb, s_is;
+  __shared__ int s_ok;
+  __shared__ float s_emf[256], s_epf[256], s_m7f, s_m8f;
+  __shared__ uint32_t s_keyf[256];
   const int t = threadIdx.x;
   const uint32_t sg = blockIdx.x;
+  grid_dep_wait();  // the statistics partials
   const unsigned long long u0 = segs[sg].unit_start;
   const unsigned long long u1 = (sg + 1 < nseg) ? segs[sg + 1].unit_start : nunits;
   double a = 0.0, b = 0.0;
@@ -254,6 +306,7 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
     }
     s_mu = mu;
     s_sigma = sigma;
+    s_is = sigma > 0.0 ? __drcp_rn(__dmul_rn(sigma, 1.4142135623730951)) : 0.0;  // 1/(sigma sqrt 2)
   }
   __syncthreads();
   const double mu = s_mu, sigma = s_sigma;
@@ -269,25 +322,100 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
     }
     return;
   }
-  // edge terms, one edge per thread (threads 1..255)
-  if (t >= 1 && t <= 255) edge_erfc(mu, sigma, t, &s_em[t], &s_ep[t]);
-  __syncthreads();
-  // Masses are finite and >= 0 (+0 below the cut-off), so their fp64 bit
-  // patterns order like the values: the ranking compares 64-bit integers.
-  s_key[t] = (t >= 1 && t <= 254) ? (unsigned long long)__double_as_longlong(field_mass(s_em, s_ep, t)) : 0ull;
-  __syncthreads();
-  int take = 0;
-  if (t >= 1 && t <= 254) {
-    const unsigned long long m = s_key[t];
-    int rank = 0;
-    for (int g = 1; g <= 254; ++g) {
-      const unsigned long long mg = s_key[g];
-      rank += (mg > m || (mg == m && g < t)) ? 1 : 0;
-    }
-    take = rank < 7;
+  // Fast ranking in fp32.  Edge terms with erfcf of the fp64 argument rounded
+  // to fp32: each term is within EPS_TERM = 1e-6 of the exact erfc (erfcf's
+  // error of a few units of 2^-23 on values <= 2, plus the argument's
+  // rounding, which moves erfc by at most 2^-24 max|x erfc'(x)| < 3e-8), so
+  // every fp32 mass (half the sum of two differences, each rounded once) is
+  // within 2.5e-6 of the exact mass.  Taking a margin of 1e-5 per mass: when
+  // the 7th largest fp32 mass exceeds the 8th by more than 2e-5, the 7 fields
+  // whose exact masses are largest are the fp32 top 7, whatever the rounding
+  // of an fp64 evaluation; the book is their set, in ascending order.
+  if (t >= 1 && t <= 255) {
+    const double e = ldexp(1.0, t - 127), is = s_is;
+    s_emf[t] = erfcf((float)__dmul_rn(__dsub_rn(e, mu), is));
+    s_epf[t] = erfcf((float)__dmul_rn(__dadd_rn(e, mu), is));
   }
-  s_take[t] = take;
   __syncthreads();
+  {
+    float mf = 0.f;
+    if (t >= 1 && t <= 254) {
+      mf = 0.5f * (s_emf[t] - s_emf[t + 1]) + 0.5f * (s_epf[t] - s_epf[t + 1]);
+      if (!(mf > 0.f)) mf = 0.f;
+    }
+    s_keyf[t] = __float_as_uint(mf);  // non-negative floats order like their bits
+  }
+  __syncthreads();
+  {
+    int rank = 256;
+    if (t >= 1 && t <= 254) {
+      const uint32_t m = s_keyf[t];
+      rank = 0;
+      for (int g = 1; g <= 254; ++g) {
+        const uint32_t mg = s_keyf[g];
+        rank += (mg > m || (mg == m && g < t)) ? 1 : 0;
+      }
+    }
+    s_take[t] = rank < 7;
+    if (rank == 6) s_m7f = __uint_as_float(s_keyf[t]);
+    if (rank == 7) s_m8f = __uint_as_float(s_keyf[t]);
+  }
+  __syncthreads();
+  if (!(s_m7f - s_m8f > 2e-5f)) {
+    // A near-tie at the 7th place: rank the exact fp64 masses.
+    // The 7 largest masses among fields lo..hi (edge terms of edges lo..hi+1,
+    // one edge per thread); s_take marks them, s_m7 gets the 7th largest.
+    // Masses are finite and >= 0 (+0 below the cut-off), so their fp64 bit
+    // patterns order like the values: the ranking compares 64-bit integers.
+    auto rank_fields = [&](int lo, int hi) {
+      if (t >= lo && t <= hi + 1) edge_erfc(mu, sigma, t, &s_em[t], &s_ep[t]);
+      __syncthreads();
+      s_key[t] = (t >= lo && t <= hi)
+                     ? (unsigned long long)__double_as_longlong(field_mass(s_em, s_ep, t))
+                     : 0ull;
+      __syncthreads();
+      int rank = 256;
+      if (t >= lo && t <= hi) {
+        const unsigned long long m = s_key[t];
+        rank = 0;
+        for (int g = lo; g <= hi; ++g) {
+          const unsigned long long mg = s_key[g];
+          rank += (mg > m || (mg == m && g < t)) ? 1 : 0;
+        }
+      }
+      s_take[t] = rank < 7;
+      if (rank == 6) s_m7 = __longlong_as_double((long long)s_key[t]);
+      __syncthreads();
+    };
+    // First only a window of fields around the field of max(sigma, |mu|),
+    // where the largest masses lie.  Every field below the window has mass at
+    // most its width times the largest density of |X|, 2^(lo-128) * 2/(sigma
+    // sqrt(2 pi)); every field above it at most P(|X| >= 2^(hi-126)) <=
+    // erfc((2^(hi-126) - |mu|)/s).  When both bounds (plus 1e-15 for the
+    // rounding of a mass computed as a difference of erfc values near 1) are
+    // under half the window's 7th largest mass, no field outside the window
+    // can be among the 7 largest, whichever way the masses are rounded, and
+    // the window's 7 are the answer; otherwise all 254 fields are ranked.
+    const int fc = field_of(fmax(sigma, fabs(mu)));
+    const int lo = fc - 24 < 1 ? 1 : fc - 24, hi = fc + 8 > 254 ? 254 : fc + 8;
+    if (t == 255) {  // the upper bound, next to the window's edge terms
+      double hb = 0.0;
+      if (hi < 254) {
+        const double a = ldexp(1.0, hi - 126), am = fabs(mu);
+        hb = a > am ? erfc((a - am) / __dmul_rn(sigma, 1.4142135623730951)) : 2.0;
+      }
+      s_hb = hb;
+    }
+    rank_fields(lo, hi);
+    if (t == 0) {
+      const double lb = lo > 1 ? ldexp(1.0, lo - 128) * 2.0 / (sigma * 2.5066282746310002) : 0.0;
+      const double lim = 0.5 * s_m7;
+      s_ok = (lb + 1e-15 < lim) && (s_hb + 1e-15 < lim);
+    }
+    __syncthreads();
+    if (!s_ok) rank_fields(1, 254);
+  }
+  const int take = s_take[t];
   if (take) {
     int pos = 0;
     for (int g = 1; g < t; ++g) pos += s_take[g];
@@ -314,9 +442,9 @@ cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  zc_predict_kernel<<<L.nseg, kThreads, 0, s>>>(const_cast<ZcSegDev*>(d_segs), L.nseg,
-                                                  L.nunits, parts);
-  return cudaGetLastError();
+  return launch_dependent(zc_predict_kernel, L.nseg, kThreads, 0, s,
+                          const_cast<ZcSegDev*>(d_segs), L.nseg, L.nunits,
+                          static_cast<const StatPartial*>(parts));
 }
 
 }  // namespace lbb

@@ -87,6 +87,37 @@ def test_moe_experts():
     st, plan = _check_full(x, seg)
 
 
+def test_predictor_scales_and_near_ties():
+    """Codebooks of many tiny segments with chosen statistics.
+
+    {+a, -a} has mean 0 and sigma a exactly; {+a, -a, +b, -b} has mean 0 and
+    sigma sqrt((a^2 + b^2)/2), which lands within 4e-5 (relative) of the
+    mantissa 1.6467... where the 7th and 8th field masses of a zero-mean
+    Gaussian swap places, so close that the predictor must fall back from its
+    fp32 ranking to exact fp64 masses; {a, b} gives mean (a + b)/2.  Every
+    book must equal the oracle's for the GPU's own mean and sigma.
+    """
+    segs = []
+    for E in range(-40, 20, 3):
+        for m in (1.0, 1.25, 1.5, 1.6328125, 1.640625, 1.6484375, 1.65625, 1.75, 1.9921875):
+            a = m * 2.0 ** E
+            segs.append([a, -a])
+    for E in range(-30, 20, 5):
+        for a, b in ((1.1171875, 0.328125), (1.21875, 1.984375), (1.1015625, 9.25),
+                     (1.15625, 0.1376953125), (1.078125, 4.53125)):
+            segs.append([x * 2.0 ** E for x in (a, -a, b, -b)])
+    rng = np.random.default_rng(0)
+    for _ in range(150):
+        a = float(rng.standard_normal()) * 2.0 ** int(rng.integers(-30, 10))
+        b = float(rng.standard_normal()) * 2.0 ** int(rng.integers(-30, 10))
+        segs.append([a, b])
+    seg = [0]
+    for v in segs:
+        seg.append(seg[-1] + len(v))
+    x = torch.tensor([v for vs in segs for v in vs], dtype=torch.float32).to(torch.bfloat16).to(DEV)
+    _check_full(x, seg, 1024)
+
+
 @pytest.mark.parametrize("chunk", [1024, 4096, 16384])
 def test_ragged_segments_and_alignment(chunk):
     # empty segments, odd starts (no 16-byte alignment), tiny and large ones

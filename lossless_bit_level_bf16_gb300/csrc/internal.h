@@ -17,7 +17,7 @@ constexpr uint32_t kZcMagic = 0x3143435Au;  // "ZCC1"
 constexpr uint32_t kZcHeader = 128;
 constexpr uint32_t kZcSegRec = 64;
 constexpr uint32_t kZcAlign = 128;
-constexpr uint32_t kTileLanes = 4096;   // lanes (element slots) per tile
+constexpr uint32_t kTileLanes = 8192;   // lanes (element slots) per encoder tile
 constexpr int kThreads = 256;           // 16 lanes per thread
 
 // Per-segment record of a plan, in device memory (64 bytes).

@@ -15,19 +15,19 @@
 // per chunk = [C sign+mantissa bytes][plane 0][plane 1][plane 2] | escape
 // bytes.  Every region starts on a 128-byte boundary.
 //
-// GPU mapping (both kernels): a tile is 4096 consecutive element slots of the
-// chunked lane space; a block of 256 threads handles a tile, 16 consecutive
-// slots per thread loaded and stored as two 16-byte vectors.  A pair of
-// threads forms one 32-bit word of each bit plane.
+// Encode: every warp takes 8192-slot tickets of the chunked slot space from a
+// ticket counter and classifies a ticket 1024 slots at a time, 32 consecutive
+// slots per lane (so a lane builds whole 32-bit words of each bit plane); it
+// writes the slot bytes and plane words with plain stores and stages its
+// escape bytes in shared memory.  One decoupled look-back per ticket, resolved
+// after the warp's next ticket, gives the ticket's escape offset, and the
+// staged bytes are copied out compacted.  The last warp to finish writes the
+// header, the segment table and the padding.  Bytes per element: 2 read,
+// 11/8 + escapes written.
 //
-// Encode: persistent blocks take 16384-slot tiles from a ticket counter; in a
-// tile each warp classifies its slices, writes slots and planes and stages its
-// escape bytes; one decoupled look-back per tile gives the tile's escape
-// offset and the staged bytes are copied out compacted.  The last block to finish writes the header, the segment table
-// and the padding.  Bytes per element: 2 read, 11/8 + escapes written.
-//
-// Decode: every warp decodes whole chunks on its own (512 slots per step);
-// the escape offsets come from the stream's table, so warps are independent.  Every offset read from the stream is checked before it is
+// Decode: every warp decodes whole chunks on its own (512 slots per step, 16
+// per lane); the escape offsets come from the stream's table, so warps are
+// independent.  Every offset read from the stream is checked before it is
 // used as an address; a bad stream sets ZC_ERR_FORMAT and is not written past.
 #include <cuda_runtime.h>
 
@@ -52,7 +52,11 @@ struct EncArgs {
 // Largest segment index whose chunk_start <= c (segments with no chunks are
 // skipped because a later one starts at the same chunk).
 __device__ __forceinline__ int find_chunk_segment(const ZcSegDev* segs, uint32_t nseg,
-                                                  unsigned long long c) {
+                                                  unsigned long long c, unsigned long long nchunks) {
+  // segments of equal size: the proportional guess is the answer (one load)
+  uint32_t g = (uint32_t)(((double)c * (double)nseg) / (double)nchunks);
+  if (g >= nseg) g = nseg - 1;
+  if (segs[g].chunk_start <= c && c - segs[g].chunk_start < segs[g].nchunks) return (int)g;
   int lo = 0, hi = (int)nseg - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
@@ -79,13 +83,13 @@ __device__ __forceinline__ uint32_t sm4(uint32_t w0, uint32_t w1) {
   return (prmt(w0, w1, 0x7531) & 0x80808080u) | (prmt(w0, w1, 0x6420) & 0x7F7F7F7Fu);
 }
 
-constexpr uint32_t kWTile = 4096;                   // slots per warp ticket
+constexpr uint32_t kWTile = kTileLanes;             // slots per warp ticket
 constexpr int kEncWarps = kThreads / 32;
 constexpr int kMaxLutSlots = kWTile / 1024;          // chunks per ticket at C = 1024
-constexpr uint32_t kStages = 3, kAhead = 2;          // input ring: 2 KB steps, copied 2 ahead
-constexpr uint32_t kEscCap = 512;                    // escape bytes a warp stages per ticket
+constexpr uint32_t kStages = 2, kAhead = 1;          // input ring: 2 KB steps, copied 1 ahead
+constexpr uint32_t kEscCap = 1024;                   // escape bytes a warp stages per ticket
 
-// Warp-level encoder.  A ticket is 4096 slots and belongs to one warp: it
+// Warp-level encoder.  A ticket is 8192 slots and belongs to one warp: it
 // classifies them 1024 at a time (32 per lane), writes the slot bytes and plane
 // words, stages its escape bytes in its own shared-memory window, then runs
 // the decoupled look-back for its ticket and copies the escapes to their place.
@@ -149,6 +153,9 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   int my_seg = -1;  // segment cache of lanes < nct
   unsigned long long my_c0 = 0, my_c1 = 0;
 
+  // A ticket is taken only when the warp is ready to work on it: taking the
+  // next one early delays its published escape count, which other warps'
+  // look-backs wait for (measured slower).
   for (;;) {
     unsigned long long tile = 0;
     if (lane == 0) tile = atomicAdd(&A.ctrl->ticket, 1ull);
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
       const unsigned long long c = cfirst + lane;
       if (c < L.nchunks) {
         if (my_seg < 0 || c < my_c0 || c >= my_c1) {
-          my_seg = find_chunk_segment(A.segs, L.nseg, c);
+          my_seg = find_chunk_segment(A.segs, L.nseg, c, L.nchunks);
           my_c0 = A.segs[my_seg].chunk_start;
           my_c1 = my_c0 + A.segs[my_seg].nchunks;
         }

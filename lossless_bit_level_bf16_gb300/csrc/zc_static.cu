@@ -1,6 +1,6 @@
 // zc_static.cu -- zc_compress_static: ZipCCL encoding without a caller
 // workspace.  The encoder's scratch (its status/ticket block and one
-// look-back word per 4096-slot tile) lives in a fixed array in device memory
+// look-back word per 8192-slot tile) lives in a fixed array in device memory
 // that belongs to the library, so this entry point allocates nothing and
 // needs no workspace from the caller.  The encoding itself is the one
 // zc_compress runs (same launcher, same kernel, same stream bytes).
@@ -15,7 +15,7 @@
 namespace {
 
 // 1 MiB: the 256-byte control block, then 131,040 look-back words, enough for
-// plans of up to 131,040 tiles of 4096 slots (536,739,840 slots).
+// plans of up to 131,040 tiles of 8192 slots (1,073,479,680 slots).
 constexpr size_t kStaticScratchBytes = 1u << 20;
 constexpr unsigned long long kStaticMaxTiles = (kStaticScratchBytes - lbb::kCtrlBytes) / 8;
 constexpr int kMaxDevices = 64;

@@ -601,8 +601,9 @@ __device__ bool find_seg_checked(const uint8_t* in, const DecHdr& h, unsigned lo
   return c >= r.chunk_start && c < r.chunk_start + r.nchunks;
 }
 
-// Each warp decodes whole chunks on its own, 512 slots (16 per lane) per
-// step, carrying the chunk's escape count from step to step; no block
+// Each warp decodes a contiguous range of whole chunks on its own, 512 slots
+// (16 per lane) per step, carrying the chunk's escape count from step to
+// step; no block
 // barrier after the header is read.  The chunk's escape bytes are staged in
 // the warp's shared-memory window when they fit (one 16-byte load per lane).
 __global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
@@ -648,8 +649,26 @@ __global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
   const unsigned long long nwarps = (unsigned long long)gridDim.x * kDecWarps;
   const uint32_t steps = C / 512u;
   uint8_t* wesc = s_esc[warp];
-  for (unsigned long long c = (unsigned long long)blockIdx.x * kDecWarps + warp; c < h.nchunks;
-       c += nwarps) {
+  // The checked record of the last segment used (chunks of one segment take
+  // it without reading the table again) and the next chunk's escape offsets,
+  // read one chunk ahead.
+  // Warp w takes a contiguous range of chunks, as many (to one) as every
+  // other warp, so consecutive chunks mostly share a segment.
+  SegRec r;
+  bool have_r = false;
+  unsigned long long c, c_end;
+  {
+    const unsigned long long gw = (unsigned long long)blockIdx.x * kDecWarps + warp;
+    const unsigned long long q = h.nchunks / nwarps, rem = h.nchunks % nwarps;
+    c = gw * q + (gw < rem ? gw : rem);
+    c_end = c + q + (gw < rem ? 1 : 0);
+  }
+  unsigned long long n_lo = 0, n_hi = 0;
+  if (c < c_end) {
+    n_lo = rd_u64(escoff + 8 * c);
+    n_hi = rd_u64(escoff + 8 * (c + 1));
+  }
+  for (; c < c_end; ++c) {
     const uint8_t* slot = in + h.off_static + c * S;
     // step 0 data and the chunk's table entries in flight together
     uint4 smv = ld_nc_v4(slot + 16u * lane);
@@ -657,9 +676,15 @@ __global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
     uint32_t p0 = __ldg(reinterpret_cast<const unsigned short*>(pb));
     uint32_t p1 = __ldg(reinterpret_cast<const unsigned short*>(pb + (C >> 3)));
     uint32_t p2 = __ldg(reinterpret_cast<const unsigned short*>(pb + (C >> 2)));
-    const unsigned long long elo = rd_u64(escoff + 8 * c), ehi = rd_u64(escoff + 8 * (c + 1));
-    SegRec r;
-    bool ok = find_seg_checked(in, h, c, r) && elo <= ehi && ehi <= h.esc_total;
+    const unsigned long long elo = n_lo, ehi = n_hi;
+    const unsigned long long cn = c + 1;
+    if (cn < c_end) {
+      n_lo = rd_u64(escoff + 8 * cn);
+      n_hi = rd_u64(escoff + 8 * (cn + 1));
+    }
+    if (!(have_r && c >= r.chunk_start && c - r.chunk_start < r.nchunks))
+      have_r = find_seg_checked(in, h, c, r);
+    bool ok = have_r && elo <= ehi && ehi <= h.esc_total;
     if (!ok) {
       if (lane == 0) set_status(ctrl, ZC_ERR_FORMAT);
       continue;  // warp-uniform

@@ -203,8 +203,10 @@ class Workload:
                         "zc_compress": ["zc_encode_kernel"],
                         "zc_decompress": ["zc_decode_kernel"],
                         "ibp_build_meta": ["ibp_columns_kernel", "ibp_meta_kernel"],
-                        "ibp_compress": ["ibp_match_kernel", "ibp_offsets_kernel",
-                                         "ibp_pack_kernel"],
+                        # one single-pass kernel for chunks of up to 512 bytes
+                        "ibp_compress": (["ibp_encode_ws_kernel"] if self.cb <= 512 else
+                                         ["ibp_match_kernel", "ibp_offsets_kernel",
+                                          "ibp_pack_kernel"]),
                         "ibp_decompress": ["ibp_decode_pipe_kernel"]}
         self.launches_per_step = sum(len(v) for v in self.kernels.values())
 

@@ -169,6 +169,33 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// L2 eviction policy for data read again soon (the cache-hinted prefetch below).
+__device__ __forceinline__ unsigned long long l2_policy_keep() {
+  unsigned long long p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// Asks L2 to fetch a contiguous range (16-byte aligned, size a multiple of
+// 16); nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes,
+                                                 unsigned long long pol) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+               "r"(bytes), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// 16-byte relaxed load of words other blocks publish while this one runs.
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+
 // ---------------------------------------------------------------- dependent launches
 //
 // A kernel launched with programmatic stream serialization (launch_dependent

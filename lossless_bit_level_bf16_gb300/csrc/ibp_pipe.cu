@@ -22,8 +22,11 @@
 // registers for the whole kernel (REG); otherwise they are read from shared
 // memory per vector.
 //
-// Encode: three launches (match -> offsets -> pack, described at the encode
-// kernels below).  Packing closes up the kept bits of a vector's 4 words into
+// Encode: for chunks of up to 512 bytes, one launch that reads the input from
+// DRAM once (a control warp matches and resolves offsets, four pack warps
+// pack; described at ibp_encode_ws_kernel); for larger chunks three launches
+// (match -> offsets -> pack, described at the encode kernels below), which
+// read the input twice.  Packing closes up the kept bits of a vector's 4 words into
 // one run of at most 128 bits and puts it into a shared-memory image of the
 // tile's stream (plain stores for the words the run covers alone, atomicOr
 // for a shared first or last word), which is then copied out with 16-byte
@@ -66,6 +69,7 @@ struct PipeArgs {
   unsigned long long* states;
   uint32_t cb, vpc, lvpc;  // chunk bytes, 16-byte vectors per chunk, log2 (REG)
   uint32_t Q, S, stage_bytes, img_words;
+  uint32_t* lens;  // single-pass encode: every tile's published stream length
 };
 
 // Mask tables of the 4 words at vector position r of a chunk.  When every
@@ -638,6 +642,452 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
                  A.out_bytes, A.ctrl, pay, t, NT);
 }
 
+// -------------------------------------------------------- single-pass encode
+//
+// For chunks of up to 512 bytes (tiles of at most 16 KB) the input is read
+// from DRAM once.  A block has four pack warps and one control warp; block b
+// owns tiles b, b + G, b + 2G, ... (G = the grid; wave i = tiles iG .. iG+G-1).
+//   The control warp, in its iteration i, asks L2 to prefetch its tile of
+//   wave i + 2, matches its tile of wave i from its own TMA stage (the first
+//   read of that tile) and publishes the tile's stream length in lens[tile]
+//   (bit 31 | length in 128-bit units).  It then resolves its tile of wave
+//   i - D: the tile's stream offset is the length of the waves before it,
+//   which the warp carries from wave to wave, plus the lengths of the tiles
+//   before it in its wave, copied into shared memory one iteration earlier.
+//   It writes the tile's entries of the group-offset table and hands the
+//   participation words and offsets to the pack warps through a two-entry
+//   ring of mbarrier-guarded slots.
+//   The pack warps run the pack kernel's pipeline: two TMA stages of input,
+//   read again right after the match read, while it is still in L2.
+// The pack warps wait only for their staged input and the handed-over slot.
+// The control warp waits for other blocks only in the resolve, D waves after
+// they published: a block that is behind never waits for one that is ahead
+// (every wave it needs was matched before the others went on), and the grid
+// is no larger than the blocks resident at once, so the waits end; each is
+// bounded all the same.
+constexpr int kWsPack = 128, kWsThreads = kWsPack + 32;
+constexpr uint32_t kWsLag = 3, kWsInfo = 2, kWsStages = 2;  // D = 3 waves (measured best)
+constexpr uint32_t kWsLensBytes = 2048;                  // a wave's lengths, padded
+constexpr unsigned kWsMaxGrid = kWsLensBytes / 4 - 8;    // 504 tiles per wave
+
+struct WsInfo {
+  unsigned long long base;  // the tile's first stream bit, from the payload start
+  uint32_t pw[kMaxQ], gex[kMaxQ];
+  uint32_t agg;             // the tile's stream bits
+  int raw;
+};
+
+// Dynamic shared memory of the single-pass encoder.
+__host__ __device__ inline size_t ws_smem_bytes(uint32_t cb, uint32_t stage_bytes,
+                                                uint32_t img_words) {
+  return 4 * ibp_table_words(cb / 4) + (size_t)(kWsStages + 1) * stage_bytes +
+         4ull * img_words + 2ull * kWsLensBytes + 8ull * (kWsStages + 1 + 2 * kWsInfo);
+}
+
+template <bool REG>
+__global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A) {
+  extern __shared__ __align__(128) uint8_t dyn[];
+  __shared__ uint32_t s_scr[kWsThreads / 32 + 4];
+  __shared__ WsInfo s_info[kWsInfo];
+  __shared__ uint32_t s_cpw[kWsLag + 1][kMaxQ];  // control warp: matched tiles' words
+  __shared__ int s_last;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t cb = A.cb, W = cb / 4, B = 8 * cb, Q = A.Q;
+  const unsigned long long G = gridDim.x, bid = blockIdx.x;
+
+  uint32_t* tab = reinterpret_cast<uint32_t*>(dyn);
+  uint8_t* stages = dyn + 4 * ibp_table_words(W);
+  uint8_t* mstage = stages + (size_t)kWsStages * A.stage_bytes;
+  uint32_t* img = reinterpret_cast<uint32_t*>(mstage + A.stage_bytes);
+  uint4* img4 = reinterpret_cast<uint4*>(img);
+  uint8_t* lensbuf = reinterpret_cast<uint8_t*>(img + A.img_words);
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(lensbuf + 2 * kWsLensBytes);
+  unsigned long long* b_sfull = bars;                    // pack stages landed
+  unsigned long long* b_mfull = bars + kWsStages;        // match stage landed
+  unsigned long long* b_ifull = b_mfull + 1;             // slot handed over
+  unsigned long long* b_iempty = b_ifull + kWsInfo;      // slot read
+  unsigned long long* grp = reinterpret_cast<unsigned long long*>(A.dst + kIbp1Header);
+
+  IbpTables T;
+  if (!ibp_load_tables<kWsThreads>(A.meta, cb, tab, T, s_scr)) {  // the same in every block
+    if (t == 0) set_status(A.ctrl, ZC_ERR_META_MISMATCH);
+    return;
+  }
+  const uint32_t m = T.m;
+  const unsigned long long tile_raw = 32ull * Q * cb;
+  const unsigned long long tail_bytes = A.n_bytes - (A.nchunks ? (A.nchunks - 1) * cb : 0ull);
+  const bool short_tail = A.nchunks && tail_bytes != cb;
+  const uint32_t mine = bid < A.ntiles ? (uint32_t)((A.ntiles - bid + G - 1) / G) : 0u;
+  auto tile_bytes = [&](unsigned long long tile) -> uint32_t {
+    const unsigned long long b0 = tile * tile_raw;
+    return (uint32_t)((A.n_bytes - b0) < tile_raw ? (A.n_bytes - b0) : tile_raw);
+  };
+  // one thread: copy a tile's input into a stage (its last 4..12 bytes with
+  // plain loads), completing on the stage's mbarrier
+  auto stage_in = [&](unsigned long long tile, uint8_t* st, unsigned long long* bar) {
+    const unsigned long long b0 = tile * tile_raw;
+    const uint32_t tb = tile_bytes(tile), b16 = tb & ~15u;
+    for (uint32_t w = b16 / 4; w < tb / 4; ++w)
+      reinterpret_cast<uint32_t*>(st)[w] = __ldg(reinterpret_cast<const uint32_t*>(A.src + b0) + w);
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, b16);
+    if (b16) bulk_g2s(st, A.src + b0, b16, bar);
+  };
+  if (t == 0) {
+    for (uint32_t s = 0; s < kWsStages; ++s) mbar_init(b_sfull + s, 1);
+    mbar_init(b_mfull, 1);
+    for (uint32_t k = 0; k < kWsInfo; ++k) {
+      mbar_init(b_ifull + k, 1);
+      mbar_init(b_iempty + k, 1);
+    }
+  }
+  for (uint32_t i = t; i < A.img_words / 4; i += kWsThreads) img4[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+
+  if (warp == kWsPack / 32) {
+    // ================================================= control warp
+    uint32_t cK[4] = {0, 0, 0, 0}, cV[4] = {0, 0, 0, 0};
+    if (REG) {
+      const uint32_t r = (uint32_t)lane & (A.vpc - 1);  // every vector of this lane
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        cK[q] = T.K[4 * r + q];
+        cV[q] = T.V[4 * r + q];
+      }
+    }
+    auto prefetch_l2 = [&](uint32_t k) {
+      if (k >= mine) return;
+      const unsigned long long tile = bid + k * G;
+      const uint32_t b16 = tile_bytes(tile) & ~15u;
+      if (b16) bulk_prefetch_l2(A.src + tile * tile_raw, b16, l2_policy_keep());
+    };
+    // lengths of the tiles of wave w (as 16-byte vectors from the tile index
+    // rounded down to 4) into lens buffer w & 1
+    auto lens_fetch = [&](uint32_t w) {
+      if (w < mine) {
+        const unsigned long long wf = (unsigned long long)w * G, la0 = wf & ~3ull;
+        const uint32_t nw = (uint32_t)((A.ntiles - wf) < G ? (A.ntiles - wf) : G);
+        const uint32_t nv4 = (uint32_t)((wf + nw - la0 + 3) / 4);
+        uint8_t* lb = lensbuf + (w & 1u) * kWsLensBytes;
+        for (uint32_t vi = lane; vi < nv4; vi += 32) cp_async16(lb + 16u * vi, A.lens + la0 + 4ull * vi);
+      }
+      cp_async_commit();
+    };
+    if (lane == 0) {
+      prefetch_l2(0);
+      prefetch_l2(1);
+      if (mine) stage_in(bid, mstage, b_mfull);
+    }
+    unsigned long long wave_base = 0;  // 128-bit units of the waves resolved so far
+    for (uint32_t i = 0; i < mine + kWsLag; ++i) {
+      if (i < mine) {
+        // ---- match the tile of wave i
+        const unsigned long long tile = bid + (unsigned long long)i * G, g0 = tile * Q;
+        if (lane == 0) prefetch_l2(i + 2);
+        if (!mbar_wait(b_mfull, i & 1u)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+        const uint32_t tb = tile_bytes(tile), twords = tb / 4, nvec = (tb + 15) / 16;
+        const uint32_t* sd = reinterpret_cast<const uint32_t*>(mstage);
+        uint32_t bad = 0;  // lane q: chunks of the tile's group q that differ
+        if (REG && A.vpc == 32) {
+          // a 512-byte chunk per step of 32 vectors: one vote per chunk, four
+          // chunks at a time (lane l's vector sits at position l of its chunk)
+          const uint32_t nfull = twords / 128;  // chunks wholly in the tile
+          uint32_t c0 = 0;
+          for (; c0 + 4 <= nfull; c0 += 4) {
+            uint32_t any4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint4 d = *reinterpret_cast<const uint4*>(sd + 128 * (c0 + u) + 4 * lane);
+              const uint32_t x = ((d.x ^ cV[0]) & ~cK[0]) | ((d.y ^ cV[1]) & ~cK[1]) |
+                                 ((d.z ^ cV[2]) & ~cK[2]) | ((d.w ^ cV[3]) & ~cK[3]);
+              any4[u] = __any_sync(kFull, x != 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t c = c0 + u;
+              if (any4[u] && (uint32_t)lane == (c >> 5)) bad |= 1u << (c & 31);
+            }
+          }
+          for (; c0 < nfull; ++c0) {
+            const uint4 d = *reinterpret_cast<const uint4*>(sd + 128 * c0 + 4 * lane);
+            const uint32_t x = ((d.x ^ cV[0]) & ~cK[0]) | ((d.y ^ cV[1]) & ~cK[1]) |
+                               ((d.z ^ cV[2]) & ~cK[2]) | ((d.w ^ cV[3]) & ~cK[3]);
+            if (__any_sync(kFull, x != 0) && (uint32_t)lane == (c0 >> 5)) bad |= 1u << (c0 & 31);
+          }
+          // a short last chunk never participates: its bits are not needed
+        } else
+        for (uint32_t v0 = 0; v0 < nvec; v0 += 32) {
+          const uint32_t v = v0 + lane;
+          uint32_t bits = 0, qq = 0xFFFFFFFFu;
+          if (v < nvec) {
+            uint32_t c, r;
+            vec_pos<REG>(A, v, c, r);
+            uint32_t K[4], V[4];
+            if (REG) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                K[q] = cK[q];
+                V[q] = cV[q];
+              }
+            } else {
+              const uint4 k4 = *reinterpret_cast<const uint4*>(T.K + 4 * r);
+              const uint4 v4 = *reinterpret_cast<const uint4*>(T.V + 4 * r);
+              K[0] = k4.x; K[1] = k4.y; K[2] = k4.z; K[3] = k4.w;
+              V[0] = v4.x; V[1] = v4.y; V[2] = v4.z; V[3] = v4.w;
+            }
+            const uint4 d = *reinterpret_cast<const uint4*>(sd + 4 * v);
+            const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+            const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
+            uint32_t x = 0;
+#pragma unroll
+            for (uint32_t q = 0; q < 4; ++q)
+              if (q < wv) x |= (dw[q] ^ V[q]) & ~K[q];
+            qq = c >> 5;
+            bits = x ? 1u << (c & 31) : 0u;
+          }
+          // the warp's 32 consecutive vectors touch at most two groups
+          const uint32_t q0 = __shfl_sync(kFull, qq, 0);
+          const uint32_t r0 = __reduce_or_sync(kFull, qq == q0 ? bits : 0u);
+          const uint32_t r1 = __reduce_or_sync(kFull, qq != q0 ? bits : 0u);
+          if ((uint32_t)lane == q0) bad |= r0;
+          if ((uint32_t)lane == q0 + 1) bad |= r1;
+        }
+        __syncwarp();  // the match stage has been read
+        if (lane == 0 && i + 1 < mine) stage_in(tile + G, mstage, b_mfull);
+        const uint32_t nq = (uint32_t)((A.ngroups - g0) < Q ? (A.ngroups - g0) : Q);
+        uint32_t pw = 0, units = 0;
+        if ((uint32_t)lane < nq) {
+          const unsigned long long g = g0 + lane, c0 = 32ull * g;
+          const uint32_t nch = (uint32_t)((A.nchunks - c0) < 32 ? (A.nchunks - c0) : 32);
+          uint32_t valid = nch >= 32 ? kFull : ((1u << nch) - 1u);
+          if (short_tail && c0 + nch == A.nchunks) valid &= ~(1u << (nch - 1));
+          pw = m ? (~bad & valid) : 0u;
+          units = (uint32_t)(ibp_group_bits(g, pw, A.nchunks, tail_bytes, cb, m) >> 7);
+        }
+        s_cpw[i % (kWsLag + 1)][lane] = pw;
+        units = __reduce_add_sync(kFull, units);
+        if (lane == 0) st_relaxed_u32(A.lens + tile, 0x80000000u | units);
+      }
+      if (i + 1 == kWsLag) lens_fetch(0);
+      if (i >= kWsLag) {
+        // ---- resolve the tile of wave j = i - D and hand it over
+        const uint32_t j = i - kWsLag;
+        const unsigned long long wf = (unsigned long long)j * G, la0 = wf & ~3ull;
+        const uint32_t nw = (uint32_t)((A.ntiles - wf) < G ? (A.ntiles - wf) : G);
+        const uint32_t nv4 = (uint32_t)((wf + nw - la0 + 3) / 4);
+        uint4* lb = reinterpret_cast<uint4*>(lensbuf + (j & 1u) * kWsLensBytes);
+        cp_async_wait_all();
+        __syncwarp();
+        uint32_t pre = 0, tot = 0;
+        for (unsigned spins = 0;; ++spins) {
+          bool all = true;
+          pre = 0;
+          tot = 0;
+          for (uint32_t vi = lane; vi < nv4; vi += 32) {
+            const uint4 e4 = lb[vi];
+            const uint32_t e[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+            for (uint32_t q = 0; q < 4; ++q) {
+              const unsigned long long idx = la0 + 4ull * vi + q;  // tile index
+              if (idx >= wf && idx < wf + nw) {
+                if (!(e[q] >> 31)) all = false;
+                const uint32_t u = e[q] & 0x7FFFFFFFu;
+                tot += u;
+                if (idx < wf + bid) pre += u;
+              }
+            }
+          }
+          if (__all_sync(kFull, all)) break;
+          if (spins >= kMaxSpins) {
+            if (lane == 0) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+            break;
+          }
+          if (get_status(A.ctrl) != 0) break;  // the call has failed: no more waiting
+          __nanosleep(spins < 64 ? 32 : 256);
+          for (uint32_t vi = lane; vi < nv4; vi += 32) lb[vi] = ld_relaxed_v4(A.lens + la0 + 4ull * vi);
+          __syncwarp();
+        }
+        __syncwarp();  // lens buffer j & 1 has been read
+        lens_fetch(j + 1);
+        pre = __reduce_add_sync(kFull, pre);
+        tot = __reduce_add_sync(kFull, tot);
+        const unsigned long long base = (wave_base + pre) * 128ull;
+        wave_base += tot;
+        const unsigned long long tile = bid + wf, g0 = tile * Q;
+        const uint32_t nq = (uint32_t)((A.ngroups - g0) < Q ? (A.ngroups - g0) : Q);
+        const uint32_t pw = (uint32_t)lane < nq ? s_cpw[j % (kWsLag + 1)][lane] : 0u;
+        const uint32_t gb =
+            (uint32_t)lane < nq ? (uint32_t)ibp_group_bits(g0 + lane, pw, A.nchunks, tail_bytes, cb, m)
+                                : 0u;
+        uint32_t inc = gb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(kFull, inc, o);
+          if (lane >= o) inc += y;
+        }
+        const uint32_t agg = __shfl_sync(kFull, inc, 31);
+        const bool raw = __ballot_sync(kFull, pw != 0) == 0;
+        if ((uint32_t)lane < nq) grp[g0 + lane] = base + (inc - gb);
+        if (lane == 0 && tile + 1 == A.ntiles) grp[A.ngroups] = base + agg;
+        // slot j % R, once the pack warps have read its previous contents
+        const uint32_t k = j % kWsInfo, f = j / kWsInfo;
+        if (f > 0 && !mbar_wait(b_iempty + k, (f - 1) & 1u)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+        WsInfo& si = s_info[k];
+        si.pw[lane] = pw;
+        si.gex[lane] = inc - gb;
+        if (lane == 0) {
+          si.base = base;
+          si.agg = agg;
+          si.raw = raw;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_ifull + k);
+      }
+    }
+    cp_async_wait_all();
+  } else {
+    // ================================================= pack warps
+    const uint32_t gvec = 8 * W + 1;  // 16-byte vectors of a full group stored raw
+    VecTab vt;
+    if (REG) {
+      load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
+      make_runs(vt);
+    }
+    if (t == 0)
+      for (uint32_t s = 0; s < kWsStages && s < mine; ++s)
+        stage_in(bid + s * G, stages + (size_t)s * A.stage_bytes, b_sfull + s);
+    for (uint32_t j = 0; j < mine; ++j) {
+      const uint32_t s = j % kWsStages, k = j % kWsInfo;
+      bool ok = mbar_wait(b_sfull + s, (j / kWsStages) & 1u);
+      ok = mbar_wait(b_ifull + k, (j / kWsInfo) & 1u) && ok;
+      if (!ok) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+      named_bar(1, kWsPack);  // the previous tile's image is cleared
+      const WsInfo& si = s_info[k];
+      const uint32_t* sd = reinterpret_cast<const uint32_t*>(stages + (size_t)s * A.stage_bytes);
+      const unsigned long long tile = bid + (unsigned long long)j * G, g0 = tile * Q;
+      const uint32_t nq = (uint32_t)((A.ngroups - g0) < Q ? (A.ngroups - g0) : Q);
+      const uint32_t tb = tile_bytes(tile);
+      const uint32_t twords = tb / 4, nvec = (tb + 15) / 16;
+      const bool raw = si.raw != 0;
+      const unsigned long long dst = A.off_payload + (si.base >> 3);
+      const uint32_t nv = si.agg >> 7;  // 16-byte vectors of the tile's stream
+      const bool fits = dst + 16ull * nv <= A.dst_cap;
+      if (!fits && t == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
+      if (raw) {
+        // [0][input words][zero padding] per group, straight from the stage
+        for (uint32_t u0 = t; u0 < nv; u0 += 4 * kWsPack) {
+          uint4 o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t u = u0 + e * kWsPack;
+            if (u >= nv) continue;
+            const uint32_t q = Q == 1 ? 0u : u / gvec, lu = u - q * gvec;
+            const uint32_t ib = q * 32u * W;  // group's first input word in the stage
+            const uint32_t bw = (q + 1 == nq) ? twords - ib : 32u * W;
+            if (lu > 0 && 4 * lu + 3 <= bw) {
+              const uint4 x = *reinterpret_cast<const uint4*>(sd + ib + 4 * lu);
+              o[e] = make_uint4(sd[ib + 4 * lu - 1], x.x, x.y, x.z);
+            } else {
+              uint32_t w[4];
+#pragma unroll
+              for (uint32_t kk = 0; kk < 4; ++kk) {
+                const uint32_t ow = 4 * lu + kk;  // word of the group's stream
+                w[kk] = (ow >= 1 && ow - 1 < bw) ? sd[ib + ow - 1] : 0u;
+              }
+              o[e] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          if (fits) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t u = u0 + e * kWsPack;
+              if (u < nv) st_v4(A.dst + dst + 16ull * u, o[e]);
+            }
+          }
+        }
+      } else {
+        if ((uint32_t)t < nq) img[3 + (si.gex[t] >> 5)] = si.pw[t];
+        // two vectors per thread per step: independent chains to interleave
+        for (uint32_t v0 = t; v0 < nvec; v0 += 2 * kWsPack) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t v = v0 + e * kWsPack;
+            if (v >= nvec) continue;
+            uint32_t c, r;
+            vec_pos<REG>(A, v, c, r);
+            const uint32_t q = c >> 5, i5 = c & 31;
+            const uint32_t pwq = si.pw[q];
+            if (!REG) load_vectab(T, r, vt);
+            const uint4 d = *reinterpret_cast<const uint4*>(sd + 4 * v);
+            const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+            const uint32_t off =
+                si.gex[q] + 32u + i5 * B - (uint32_t)__popc(pwq & ((1u << i5) - 1u)) * m;
+            uint32_t o[4], n, pos;
+            if ((pwq >> i5) & 1u) {
+              uint32_t f[4];
+#pragma unroll
+              for (int w = 0; w < 4; ++w) f[w] = vt_compress(vt, dw[w], w);
+              uint32_t kk[4];
+              kept_bits(vt, kk);
+              cat4(f, kk, o);
+              n = kk[0] + kk[1] + kk[2] + kk[3];
+              pos = off + vt.Pr;
+            } else {
+              const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
+#pragma unroll
+              for (uint32_t w = 0; w < 4; ++w) o[w] = w < wv ? dw[w] : 0u;
+              n = 32u * wv;
+              pos = off + 128u * r;
+            }
+            img_put(img, 96u + pos, o, n);
+          }
+        }
+        named_bar(1, kWsPack);
+        if (fits) {
+          for (uint32_t u0 = t; u0 < nv; u0 += 4 * kWsPack) {
+            uint4 o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t u = u0 + e * kWsPack;
+              if (u < nv) {
+                const uint4 x = img4[u + 1];
+                o[e] = make_uint4(img[4 * u + 3], x.x, x.y, x.z);
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t u = u0 + e * kWsPack;
+              if (u < nv) st_v4(A.dst + dst + 16ull * u, o[e]);
+            }
+          }
+        }
+      }
+      named_bar(1, kWsPack);  // the stage, the image and the slot have been read
+      if (t == 0) {
+        mbar_arrive(b_iempty + k);
+        if (j + kWsStages < mine)
+          stage_in(tile + kWsStages * G, stages + (size_t)s * A.stage_bytes, b_sfull + s);
+      }
+      if (!raw)  // cleared before the next tile (the barrier at its top)
+        for (uint32_t u = t; u <= nv; u += kWsPack) img4[u] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  // ---- last block: header and table end
+  __syncthreads();
+  if (t == 0) {
+    __threadfence();
+    const unsigned long long dn = atomicAdd(&A.ctrl->done, 1ull);
+    s_last = (dn == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const unsigned long long pay = A.ngroups ? grp[A.ngroups] : 0ull;
+  ibp_write_tail(A.meta, cb, m, A.n_bytes, A.nchunks, A.ngroups, A.dst, A.dst_cap, A.off_payload,
+                 A.out_bytes, A.ctrl, pay, t, kWsThreads);
+}
+
 template <int NT, bool REG>
 __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs A) {
   constexpr int NW = NT / 32;
@@ -1014,6 +1464,46 @@ void fill_shape(PipeArgs& A, const Geo& g) {
   A.img_words = g.img_words;
 }
 
+// The single-pass encoder for chunks of up to 512 bytes (one group of 16 KB
+// per tile, or several groups of smaller chunks).
+cudaError_t ibp_ws_compress(const void* d_meta, uint32_t cb, const void* d_x,
+                            unsigned long long n_bytes, void* d_out, unsigned long long out_cap,
+                            unsigned long long* d_out_bytes, void* d_ws, cudaStream_t s) {
+  Geo g{};
+  tile_shape(cb, true, g);
+  const unsigned long long nchunks = (n_bytes + cb - 1) / cb, ngroups = (nchunks + 31) / 32;
+  PipeArgs A{};
+  A.meta = static_cast<const uint8_t*>(d_meta);
+  A.src = static_cast<const uint8_t*>(d_x);
+  A.dst = static_cast<uint8_t*>(d_out);
+  A.dst_cap = out_cap;
+  A.n_bytes = n_bytes;
+  A.cb = cb;
+  A.nchunks = nchunks;
+  A.ngroups = ngroups;
+  A.ntiles = (ngroups + g.Q - 1) / g.Q;
+  A.off_payload = kIbp1Header + round_up(8ull * (ngroups + 1), 128);
+  A.out_bytes = d_out_bytes;
+  A.ctrl = static_cast<Ctrl*>(d_ws);
+  A.lens = reinterpret_cast<uint32_t*>(static_cast<char*>(d_ws) + kCtrlBytes);
+  g.S = kWsStages;
+  fill_shape(A, g);
+  const bool reg = pow2(A.vpc) && A.vpc <= 32;
+  const size_t smem = ws_smem_bytes(cb, g.stage_bytes, g.img_words);
+  auto k = reg ? ibp_encode_ws_kernel<true> : ibp_encode_ws_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  unsigned long long grid = (unsigned long long)resident_blocks((const void*)k, kWsThreads, smem);
+  if (grid > kWsMaxGrid) grid = kWsMaxGrid;
+  if (grid > A.ntiles) grid = A.ntiles;
+  if (grid == 0) grid = 1;
+  // workspace: control block | one length word per tile (+ one vector of slack)
+  e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 4ull * A.ntiles + 16, s);
+  if (e != cudaSuccess) return e;
+  k<<<(unsigned)grid, kWsThreads, smem, s>>>(A);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool ibp_pipe_supported(uint32_t cb, bool encode) { return cb <= 2048 && pick(cb, encode).ok; }
@@ -1021,6 +1511,7 @@ bool ibp_pipe_supported(uint32_t cb, bool encode) { return cb <= 2048 && pick(cb
 cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t cb, const void* d_x,
                               unsigned long long n_bytes, void* d_out, unsigned long long out_cap,
                               unsigned long long* d_out_bytes, void* d_ws, cudaStream_t s) {
+  if (cb <= 512) return ibp_ws_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap, d_out_bytes, d_ws, s);
   const Geo g = pick(cb, true);
   const unsigned long long nchunks = (n_bytes + cb - 1) / cb, ngroups = (nchunks + 31) / 32;
   const unsigned long long ntiles2 = (ngroups + kOffNT * kOffIPT - 1) / (kOffNT * kOffIPT);

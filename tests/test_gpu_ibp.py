@@ -279,3 +279,41 @@ def test_bf16_weights(mode):
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int32), x32.view(torch.int32))
     assert total < xb.size
+
+
+def test_encode_next_to_another_stream():
+    """The single-pass encoder's blocks wait for lengths that other blocks of
+    the same launch publish.  Here its launches share the GPU with ZipCCL
+    kernels on a second stream, so some of its blocks start only when those
+    finish; every stream must still equal the one encoded alone."""
+    from lossless_bit_level_bf16_gb300 import zipccl as Z
+    cb = 512
+    rows, idx = W.ibp_table(rows=200_000, cols=128, std=0.1, seed=3, device=DEV, n_samples=2000)
+    meta = I.build_meta(rows[idx].contiguous(), cb, T=0.9, mode=1, ws=_ws(cb, 0, 2000))
+    n_bytes = rows.numel() * 4
+    ws0 = _ws(cb, n_bytes)
+    ref, nb = I.compress(meta, rows, cb, ws=ws0)
+    torch.cuda.synchronize()
+    assert I.status(ws0) == 0
+    ref = ref[:int(nb.item())].clone()
+    x, seg = W.zc_gradient(n_blocks=64, device=DEV)
+    plan = Z.Plan(x.numel(), seg, 4096)
+    plan.fit(x)
+    zref, znb = plan.compress(x)
+    torch.cuda.synchronize()
+    zref = zref[:int(znb.item())].clone()
+    s_ibp, s_zc = torch.cuda.Stream(), torch.cuda.Stream()
+    for order in range(4):
+        ws = _ws(cb, n_bytes)
+        with torch.cuda.stream(s_zc):
+            zs = [plan.compress(x) for _ in range(1 + order)]
+        with torch.cuda.stream(s_ibp):
+            st, nb = I.compress(meta, rows, cb, ws=ws)
+        with torch.cuda.stream(s_zc):
+            zs.append(plan.compress(x))
+        torch.cuda.synchronize()
+        assert I.status(ws) == 0, abi.strerror(I.status(ws))
+        assert plan.status() == 0
+        assert int(nb.item()) == ref.numel() and torch.equal(st[:ref.numel()], ref), order
+        for zo, zn in zs:
+            assert int(zn.item()) == zref.numel() and torch.equal(zo[:zref.numel()], zref), order

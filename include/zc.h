@@ -206,11 +206,17 @@ int ibp_build_meta(const void* d_samples, uint64_t n_samples,
  * d_out using the metadata at d_meta (its chunk size must be chunk_bytes;
  * checked on the device).  *d_out_bytes (device, may be NULL) receives the
  * stream size; a stream larger than out_cap sets ZC_ERR_CAPACITY and nothing
- * is written past out_cap.  For chunk_bytes <= 2048: one memset and three
- * kernels (a read-only pass that decides every chunk's participation bit, a
- * scan of the group lengths into the stream's group-offset table, the packing
- * pass); the workspace holds one participation word per group between them.
- * Larger chunks: one memset and one kernel.  d_x and d_out may be pinned host
+ * is written past out_cap.  For chunk_bytes <= 512: one memset and one
+ * kernel that reads the input from device memory once (tiles are matched,
+ * their stream lengths published in the workspace and their offsets resolved
+ * a few tiles later, while the input is still in L2).  For chunk_bytes <=
+ * 2048: one memset and three kernels (a read-only pass that decides every
+ * chunk's participation bit, a scan of the group lengths into the stream's
+ * group-offset table, the packing pass); the workspace holds one
+ * participation word per group between them.  Larger chunks: one memset and
+ * one kernel.  The workspace size is ibp_workspace_bytes().  With a
+ * host-resident d_x or d_out (see below) the single-kernel encoder runs.
+ * d_x and d_out may be pinned host
  * memory ([IBP] Algoritmo Core step 2: the GPU compresses through zero-copy
  * unified memory); a host-resident d_x is read with plain loads by the
  * single-kernel encoder.  Other host memory returns ZC_ERR_ARG. */

@@ -40,10 +40,6 @@ __device__ __forceinline__ int get_status(const Ctrl* c) {
 
 // ---------------------------------------------------------------- memory ops
 
-__device__ __forceinline__ void st_release_u64(unsigned long long* p,
-                                               unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
@@ -68,14 +64,6 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
                : "l"(p));
   return r;
 }
-// 16-byte load through L1 bypass for data other blocks of this kernel wrote.
-__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
                "r"(v.y), "r"(v.z), "r"(v.w)
@@ -83,10 +71,6 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
 }
 
 // Asynchronous global -> shared copies (cp.async, no register staging).
-__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(sa), "l"(gmem) : "memory");
-}
 __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
@@ -143,17 +127,6 @@ __device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
 // Barrier `id` (1..15) over `count` threads (a multiple of 32) of the block.
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// True if the phase with the given parity has completed (does not wait).
-__device__ __forceinline__ bool mbar_test(unsigned long long* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 // Orders this thread's earlier shared-memory accesses before later
 // asynchronous-proxy (bulk copy) writes to the same memory.
@@ -306,100 +279,6 @@ __device__ __forceinline__ unsigned long long lookback_warp_wide(
         __nanosleep(ns);
         if (ns < 512) ns <<= 1;
       }
-      continue;
-    }
-    excl += sum;
-    if (r == kLbFound) break;
-    end -= deep ? 32 * D1 : 32 * D0;
-    deep = true;
-  }
-  if (to) {
-    *timed_out = true;
-    if (lane == 0) st_relaxed_u64(states + tile, kFlagInc | aggregate);
-    return 0;
-  }
-  if (lane == 0) st_relaxed_u64(states + tile, kFlagInc | ((excl + aggregate) & kValMask));
-  return excl;
-}
-
-// Look-back for kernels whose tiles take microseconds to publish: while a
-// predecessor has not published, one lane polls that single state, sleeping
-// between reads (128 ns doubling to 1 us), instead of the whole warp
-// re-reading the window; the window is read again once it has published.
-// D0 * 32 states are read in the first round trip, D1 * 32 in each further
-// one.  Bounded like lookback_warp_wide.
-template <int D>
-__device__ __forceinline__ int lb_window_pos(const unsigned long long* states, long long end,
-                                             unsigned long long* sum, long long* empty_at) {
-  const int lane = threadIdx.x & (kWarp - 1);
-  unsigned long long s[D];
-#pragma unroll
-  for (int j = 0; j < D; ++j) {
-    const long long idx = end - (32 * j + lane);
-    s[j] = idx >= 0 ? ld_relaxed_u64(states + idx) : kFlagInc;
-  }
-  int jinc = D, linc = 32, jemp = D, lemp = 32;
-#pragma unroll
-  for (int j = 0; j < D; ++j) {
-    const unsigned f = (unsigned)(s[j] >> 62);
-    const unsigned inc = __ballot_sync(kFull, f == 2);
-    const unsigned emp = __ballot_sync(kFull, f == 0);
-    if (jemp == D && emp) {
-      jemp = j;
-      lemp = __ffs(emp) - 1;
-    }
-    if (jinc == D && inc) {
-      jinc = j;
-      linc = __ffs(inc) - 1;
-    }
-  }
-  // an empty state closer than the nearest inclusive one
-  if (jemp < jinc || (jemp == jinc && jemp < D && lemp < linc)) {
-    *empty_at = end - (32 * jemp + lemp);
-    return kLbEmpty;
-  }
-  unsigned long long part = 0;
-#pragma unroll
-  for (int j = 0; j < D; ++j)
-    if (j < jinc || (j == jinc && lane <= linc)) part += s[j] & kValMask;
-  *sum = warp_sum_u64(part);
-  return jinc < D ? kLbFound : kLbAllAgg;
-}
-
-template <int D0, int D1>
-__device__ __forceinline__ unsigned long long lookback_poll(unsigned long long* states,
-                                                            unsigned long long tile,
-                                                            unsigned long long aggregate,
-                                                            bool* timed_out) {
-  const int lane = threadIdx.x & (kWarp - 1);
-  if (tile == 0) {
-    if (lane == 0) st_relaxed_u64(states, kFlagInc | aggregate);
-    return 0;
-  }
-  if (lane == 0) st_relaxed_u64(states + tile, kFlagAgg | aggregate);
-  unsigned long long excl = 0;
-  long long end = (long long)tile - 1;
-  unsigned spins = 0;
-  bool deep = false, to = false;
-  while (!to) {
-    unsigned long long sum = 0;
-    long long at = 0;
-    const int r = deep ? lb_window_pos<D1>(states, end, &sum, &at)
-                       : lb_window_pos<D0>(states, end, &sum, &at);
-    if (r == kLbEmpty) {
-      unsigned bad = 0;
-      if (lane == 0) {
-        unsigned ns = 128;
-        while ((ld_relaxed_u64(states + at) >> 62) == 0) {
-          if (++spins > kMaxSpins) {
-            bad = 1;
-            break;
-          }
-          __nanosleep(ns);
-          if (ns < 1024) ns <<= 1;
-        }
-      }
-      to = __shfl_sync(kFull, bad, 0) != 0;
       continue;
     }
     excl += sum;

@@ -44,6 +44,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "ibp_common.cuh"
@@ -79,8 +80,9 @@ struct PipeArgs {
 // first run's length l0 (0 when there is no second run).
 struct VecTab {
   uint32_t K[4], V[4], MV[5][4];
-  uint32_t Pr;  // kept bits of the chunk before this vector
-  bool fast;
+  uint32_t R3[3][4];  // three-run form (decoder): third run's start a2, mask m2, field offset l01
+  uint32_t Pr;        // kept bits of the chunk before this vector
+  bool fast, fast3;
 };
 
 // Switch vt to the two-run form if every word allows it (called once, on
@@ -115,6 +117,47 @@ __device__ __forceinline__ void make_runs(VecTab& v) {
   }
 }
 
+// The decoder's three-run form, for tables whose keep masks are three runs
+// of ones in some word (16-bit values: a sign run and a low run per half) and
+// at most three in every word: MV[0..4] as in the two-run form, R3 the third
+// run.  fast3 is set only when the two-run form does not apply.
+__device__ __forceinline__ void make_runs3(VecTab& v) {
+  v.fast3 = false;
+  if (v.fast) {  // no third run: the three-run form reduces to the two-run one
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v.R3[0][j] = v.R3[1][j] = v.R3[2][j] = 0;
+    return;
+  }
+  bool ok = true;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) ok = ok && __popc(v.K[j] & ~(v.K[j] << 1)) <= 3;
+  if (!ok) return;
+  v.fast3 = true;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t k = v.K[j];
+    uint32_t a[3] = {0, 0, 0}, mk[3] = {0, 0, 0}, len[3] = {0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      if (k) {
+        a[i] = __ffs(k) - 1;
+        const uint32_t y = k >> a[i];
+        len[i] = (y == 0xFFFFFFFFu) ? 32u : (uint32_t)(__ffs(~y) - 1);
+        mk[i] = len[i] >= 32 ? 0xFFFFFFFFu : ((1u << len[i]) - 1u);
+        k &= ~(mk[i] << a[i]);
+      }
+    }
+    v.MV[0][j] = a[0];
+    v.MV[1][j] = mk[0];
+    v.MV[2][j] = a[1];
+    v.MV[3][j] = mk[1];
+    v.MV[4][j] = mk[1] ? len[0] : 0u;
+    v.R3[0][j] = a[2];
+    v.R3[1][j] = mk[2];
+    v.R3[2][j] = mk[2] ? len[0] + len[1] : 0u;
+  }
+}
+
 // Kept bits of word w of x closed up toward bit 0 (the keep mask's runs, or
 // the general method).
 __device__ __forceinline__ uint32_t vt_compress(const VecTab& v, uint32_t x, int w) {
@@ -127,6 +170,12 @@ __device__ __forceinline__ uint32_t vt_expand(const VecTab& v, uint32_t f, int w
   if (v.fast)
     return ((f & v.MV[1][w]) << v.MV[0][w]) | (((f >> v.MV[4][w]) & v.MV[3][w]) << v.MV[2][w]);
   return hd_expand(f, v.K[w], &v.MV[0][w], 4);
+}
+
+// vt_expand for the three-run form.
+__device__ __forceinline__ uint32_t vt_expand3(const VecTab& v, uint32_t f, int w) {
+  return ((f & v.MV[1][w]) << v.MV[0][w]) | (((f >> v.MV[4][w]) & v.MV[3][w]) << v.MV[2][w]) |
+         (((f >> v.R3[2][w]) & v.R3[1][w]) << v.R3[0][w]);
 }
 
 // Kept bits per word of the vector (recomputed: cheaper than registers).
@@ -146,6 +195,7 @@ __device__ __forceinline__ void load_vectab(const IbpTables& T, uint32_t r, VecT
   }
   v.Pr = T.P[4 * r];
   v.fast = false;
+  v.fast3 = false;
 }
 
 // Fields f[0..3] (f[j] has k[j] <= 32 bits) laid end to end, LSB first.
@@ -1133,6 +1183,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
   if (REG) {
     load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
     make_runs(vt);
+    make_runs3(vt);
   }
 
   // warp 0: the span of this block's kk-th tile.  prefetch() loads its
@@ -1227,7 +1278,12 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
   scan(0, 0, 0);
   __syncthreads();
 
-  // Tile k is expanded, then tile k + 1 scanned; one barrier per tile.
+  // Tile k is expanded, then tile k + 1 scanned; one barrier per tile.  The
+  // loop is compiled for two-run and for three-run tables; a block whose
+  // threads all have two-run tables takes the first (the choice is the same
+  // for every thread of the block, so all take the same barriers).
+  auto tiles = [&](auto three_runs) {
+  constexpr bool THREE = decltype(three_runs)::value;
   for (uint32_t k = 0;; ++k) {
     const uint32_t s = k % S, bf = k & 1;
     const unsigned long long tile = s_tile[s];
@@ -1260,7 +1316,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
         const uint32_t off = s_off[bf][q][i];
         uint32_t u[4];
         if ((s_pw[bf][q] >> i) & 1u) {
-          if (REG && vt.fast) {
+          if (REG && (THREE ? (vt.fast || vt.fast3) : vt.fast)) {
             // each word's field read at its own bit offset, expanded from runs
             uint32_t pos = off + vt.Pr;
 #pragma unroll
@@ -1269,7 +1325,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
               const uint32_t a = pos >> 5, sh = pos & 31;
               uint32_t f = __funnelshift_r(sd[a], sd[a + 1], sh);
               f &= kw >= 32 ? 0xFFFFFFFFu : ((1u << kw) - 1u);
-              o[e][w] = vt_expand(vt, f, w) | vt.V[w];
+              o[e][w] = (THREE ? vt_expand3(vt, f, w) : vt_expand(vt, f, w)) | vt.V[w];
               pos += kw;
             }
           } else {
@@ -1308,6 +1364,9 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
     __syncthreads();  // stage s read; the next tile's scan written
     if (warp == 0) issue(k + S, s);
   }
+  };
+  if (__syncthreads_or(REG && vt.fast3 ? 1 : 0)) tiles(std::true_type{});
+  else tiles(std::false_type{});
 }
 
 // ------------------------------------------------------------------ launch

@@ -8,12 +8,12 @@
 // fixed-size blob kept in GPU memory and reused for the whole dataset.
 //
 // Kernels:
-//   ibp_columns_kernel  32 samples per warp: for each 32-bit word of the chunk
-//                       one ballot per bit position transposes the 32x32 bit
-//                       block, so lane b holds the column of position 32w+b
-//                       over those samples; its popcount is added to the ones
-//                       count of that position.  The columns are kept for the
-//                       joint reading.
+//   ibp_columns_kernel  a warp per 8 words of the chunk and 4 blocks of 32
+//                       samples: a shuffle butterfly transposes each 32x32
+//                       bit block, so lane b holds the column of position
+//                       32w+b over those samples; its popcounts are summed
+//                       and added to the ones count of that position.  The
+//                       columns are kept for the joint reading.
 //   ibp_meta_kernel     one block: threshold k = ceil(T*N) on each position's
 //                       agreement max(ones, N-ones); per-position (mode 0) or
 //                       joint greedy selection (mode 1: positions sorted by
@@ -31,7 +31,32 @@ namespace {
 
 constexpr int kMetaThreads = 1024;
 constexpr uint32_t kWordsPerWarp = 8;
+constexpr uint32_t kBlocksPerWarp = 4;  // blocks of 32 samples a warp takes
 
+// 32x32 bit transpose across a warp: lane i holds row i on entry; lane b
+// returns column b (bit i = bit b of row i).  Five butterfly levels, each
+// swapping the off-diagonal j x j sub-blocks of lane pairs (i, i ^ j).
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+  uint32_t m = 0x0000FFFFu;
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const uint32_t other = __shfl_xor_sync(kFull, x, j);
+    const bool up = (lane & j) != 0;
+    const uint32_t lo = up ? other : x, hi = up ? x : other;
+    const uint32_t t = ((lo >> j) ^ hi) & m;
+    x = up ? (hi ^ t) : (lo ^ (t << j));
+    m ^= m << (j >> 1);
+  }
+  return x;
+}
+
+// A warp takes 8 words of the chunk for kBlocksPerWarp blocks of 32 samples:
+// lane l loads words w0..w0+7 of sample 32*sb + l (two 16-byte loads, all
+// blocks' loads issued before any is used), each word's 32x32 bit block is
+// transposed so that lane b holds the column of position 32w+b over the 32
+// samples, and the columns' popcounts are summed in registers; one atomic
+// per position and warp adds them to the ones counts.  The columns are kept
+// for the joint reading.
 __global__ void __launch_bounds__(256) ibp_columns_kernel(
     const uint32_t* __restrict__ samples, unsigned long long N, uint32_t W,
     uint32_t* __restrict__ ones, uint32_t* __restrict__ cols, uint32_t Wn, int keep_cols) {
@@ -39,22 +64,43 @@ __global__ void __launch_bounds__(256) ibp_columns_kernel(
   grid_dep_launch();  // the metadata kernel may be scheduled as blocks finish
   const unsigned long long warp = (blockIdx.x * 256ull + threadIdx.x) >> 5;
   const uint32_t wgroups = (W + kWordsPerWarp - 1) / kWordsPerWarp;
-  const unsigned long long sb = warp / wgroups;  // block of 32 samples
-  const uint32_t wg = (uint32_t)(warp % wgroups);
-  if (sb >= Wn) return;
-  const unsigned long long s = sb * 32ull + lane;
-  for (uint32_t w = wg * kWordsPerWarp; w < W && w < (wg + 1) * kWordsPerWarp; ++w) {
-    const uint32_t v = s < N ? __ldg(samples + s * W + w) : 0u;
-    uint32_t mine = 0;
+  const unsigned long long sbq = warp / wgroups;  // group of kBlocksPerWarp sample blocks
+  const uint32_t w0 = (uint32_t)(warp % wgroups) * kWordsPerWarp;
+  if (sbq * kBlocksPerWarp >= Wn) return;
+  const uint32_t nw = (W - w0) < kWordsPerWarp ? (W - w0) : kWordsPerWarp;
+  uint32_t v[kBlocksPerWarp][kWordsPerWarp];
 #pragma unroll
-    for (int b = 0; b < 32; ++b) {
-      const uint32_t r = __ballot_sync(kFull, (v >> b) & 1u);
-      if (lane == b) mine = r;
+  for (uint32_t bi = 0; bi < kBlocksPerWarp; ++bi) {
+    const unsigned long long sb = sbq * kBlocksPerWarp + bi;
+    const unsigned long long s = sb * 32ull + lane;
+    const bool have = sb < Wn && s < N;
+    if (have && nw == kWordsPerWarp) {  // 16-byte aligned: W and w0 are multiples of 4
+      const uint4 a = ld_nc_v4(samples + s * W + w0), b = ld_nc_v4(samples + s * W + w0 + 4);
+      v[bi][0] = a.x; v[bi][1] = a.y; v[bi][2] = a.z; v[bi][3] = a.w;
+      v[bi][4] = b.x; v[bi][5] = b.y; v[bi][6] = b.z; v[bi][7] = b.w;
+    } else {
+#pragma unroll
+      for (uint32_t k = 0; k < kWordsPerWarp; ++k)
+        v[bi][k] = (have && k < nw) ? __ldg(samples + s * W + w0 + k) : 0u;
     }
-    const uint32_t j = 32u * w + lane;  // bit position this lane now owns
-    if (mine) atomicAdd(ones + j, (uint32_t)__popc(mine));
-    if (keep_cols) cols[(unsigned long long)j * Wn + sb] = mine;
   }
+  uint32_t cnt[kWordsPerWarp];
+#pragma unroll
+  for (uint32_t k = 0; k < kWordsPerWarp; ++k) cnt[k] = 0;
+#pragma unroll
+  for (uint32_t bi = 0; bi < kBlocksPerWarp; ++bi) {
+    const unsigned long long sb = sbq * kBlocksPerWarp + bi;
+    if (sb >= Wn) break;  // warp-uniform
+#pragma unroll
+    for (uint32_t k = 0; k < kWordsPerWarp; ++k) {
+      const uint32_t col = warp_transpose32(v[bi][k], lane);
+      cnt[k] += (uint32_t)__popc(col);
+      if (keep_cols && k < nw) cols[(32ull * (w0 + k) + lane) * Wn + sb] = col;
+    }
+  }
+#pragma unroll
+  for (uint32_t k = 0; k < kWordsPerWarp; ++k)
+    if (k < nw && cnt[k]) atomicAdd(ones + 32u * (w0 + k) + lane, cnt[k]);
 }
 
 __device__ __forceinline__ uint32_t block_sum_1024(uint32_t v, uint32_t* red) {
@@ -289,7 +335,8 @@ cudaError_t ibp_launch_build_meta(const void* d_samples, unsigned long long N,
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 4ull * B, s);
   if (e != cudaSuccess) return e;
   const uint32_t wgroups = (W + kWordsPerWarp - 1) / kWordsPerWarp;
-  const unsigned long long warps = (unsigned long long)Wn * wgroups;
+  const unsigned long long warps =
+      (unsigned long long)((Wn + kBlocksPerWarp - 1) / kBlocksPerWarp) * wgroups;
   const unsigned long long blocks = (warps + 7) / 8;
   if (blocks > 0x7FFFFFFFull) return cudaErrorInvalidValue;
   ibp_columns_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint32_t*>(d_samples), N,

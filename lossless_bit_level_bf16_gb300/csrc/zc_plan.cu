@@ -90,7 +90,7 @@ __device__ __forceinline__ void pair_add(float& a, float& b, float a2, float b2)
   b = __fadd_rn(b, b2);
 }
 
-__global__ void __launch_bounds__(kThreads, 3) zc_stats_kernel(
+__global__ void __launch_bounds__(kThreads, 2) zc_stats_kernel(
     const uint16_t* __restrict__ x, const ZcSegDev* __restrict__ segs, uint32_t nseg,
     uint32_t U, unsigned long long nunits, StatPartial* __restrict__ parts, int x_al16) {
   const int lane = threadIdx.x & 31;

@@ -142,8 +142,8 @@ int zc_compress(zc_plan_t plan, const uint16_t* d_x, void* d_out,
  * a program whose device memory is all held by a pool it cannot reach from
  * here -- and so cannot size or keep a workspace.  The encoder's scratch
  * (status block and look-back words) is instead a fixed 1 MiB array in
- * device memory owned by the library, which limits the plan to 131,040 tiles
- * of 8192 slots (1,073,479,680 slots, chunk padding included); a larger plan
+ * device memory owned by the library, which limits the plan to 130,024 tiles
+ * of 8192 slots (1,065,156,608 slots, chunk padding included); a larger plan
  * returns ZC_ERR_CAPACITY.  Nothing is allocated by this call (the plan
  * itself was allocated by zc_plan_create).
  *

@@ -74,7 +74,7 @@ bool reachable(const void** p, bool* host) {
 
 size_t zc_ws_bytes(const lbb::ZcLayout& L) {
   const unsigned long long a = L.nunits * sizeof(lbb::StatPartial);
-  const unsigned long long b = L.ntiles * 8ull;
+  const unsigned long long b = lbb::zc_enc_scratch_bytes(L.ntiles);
   return (size_t)lbb::round_up_dev(kCtrlBytes + std::max(a, b), 256);
 }
 

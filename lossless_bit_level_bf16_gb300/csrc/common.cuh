@@ -295,6 +295,138 @@ __device__ __forceinline__ unsigned long long lookback_warp_wide(
   return excl;
 }
 
+// ---------------------------------------------------------------- two-level look-back
+//
+// For kernels with many tickets in flight (every warp holds one), where the
+// plain look-back would read back over all of them.  Tickets are grouped in
+// blocks of kLbBlock, and each block has one word that only atomics change:
+// bit 63 is the inclusive flag (kFlagInc), bits 61:52 count the tickets whose
+// aggregate is in, bits 51:0 hold the value.  Every ticket adds (1 << 52) +
+// its aggregate; the block's first ticket, once it knows its exclusive
+// prefix, adds the flag + that prefix.  A word is read only as a whole: while its
+// count is short of kLbBlock the block is incomplete whatever else is in it;
+// once full it holds the block's sum, or with the flag the inclusive prefix
+// through the block.  So no ordering between locations is needed.
+// A look-back reads the tickets of its own block (one window), then the
+// words of the blocks before it (32 * D per window), and reads a block's
+// tickets only while that block is incomplete.
+constexpr unsigned kLbBlock = 128;  // equal to kZcLbBlock (internal.h)
+constexpr unsigned long long kBlkOne = 1ull << 52;
+constexpr unsigned long long kBlkValMask = kBlkOne - 1;
+static_assert(kLbBlock < 1024, "the count field holds a block's tickets");
+
+// Lane 0, once ticket t's aggregate is known (values below 2^52).
+__device__ __forceinline__ void lb2_publish_agg(unsigned long long* states,
+                                                unsigned long long* bwords,
+                                                unsigned long long t, unsigned long long agg) {
+  atomicAdd(bwords + t / kLbBlock, kBlkOne + agg);
+  st_relaxed_u64(states + t, (t == 0 ? kFlagInc : kFlagAgg) | agg);
+}
+
+// Lane 0, once ticket t's exclusive prefix is known: the ticket's inclusive
+// state, and for a block's first ticket the block's exclusive prefix.
+__device__ __forceinline__ void lb2_publish_inc(unsigned long long* states,
+                                                unsigned long long* bwords,
+                                                unsigned long long t, unsigned long long excl,
+                                                unsigned long long agg) {
+  st_relaxed_u64(states + t, kFlagInc | ((excl + agg) & kValMask));
+  if (t % kLbBlock == 0) atomicAdd(bwords + t / kLbBlock, kFlagInc + excl);
+}
+
+// A window of 32 * D entries below `end`, down to `lo` (indices below lo
+// are outside the range, except that with lo == 0 those below 0 read as an
+// inclusive zero); BLK selects block words over ticket states.  Returns
+// kLbFound (an inclusive entry in range; *sum = the values from end down to
+// it), kLbAllAgg (none; *sum = every value in range) or kLbEmpty (an empty
+// entry before any inclusive one; *empty_at = the nearest such index, *sum =
+// the values above it).
+template <int D, bool BLK>
+__device__ __forceinline__ int lb2_window(const unsigned long long* words, long long end,
+                                          long long lo, unsigned long long* sum,
+                                          long long* empty_at) {
+  const int lane = threadIdx.x & (kWarp - 1);
+  constexpr unsigned long long kZeroInc = BLK ? (kFlagInc | ((unsigned long long)kLbBlock << 52))
+                                              : kFlagInc;
+  unsigned long long s[D];
+#pragma unroll
+  for (int j = 0; j < D; ++j) {
+    const long long idx = end - (32 * j + lane);
+    s[j] = idx < lo ? (idx < 0 && lo == 0 ? kZeroInc : 0ull) : ld_relaxed_u64(words + idx);
+  }
+  // nearest first: values count up to the first empty entry (excluded) or
+  // the first inclusive one (included)
+  unsigned long long part = 0;
+  int res = kLbAllAgg;
+#pragma unroll
+  for (int j = 0; j < D; ++j) {
+    const long long idx = end - (32 * j + lane);
+    const bool in = idx >= lo || (idx < 0 && lo == 0);
+    unsigned f = (unsigned)(s[j] >> 62);  // 0 empty, 1 aggregate, 2 inclusive
+    if (BLK) f = ((s[j] >> 52) & 1023u) == kLbBlock ? 1u + (unsigned)(s[j] >> 63) : 0u;
+    if (res == kLbAllAgg) {
+      const unsigned emp = __ballot_sync(kFull, in && f == 0);
+      const unsigned cut = emp | __ballot_sync(kFull, in && f == 2);
+      const int lc = cut ? __ffs(cut) - 1 : 32;
+      const bool e = (emp >> (lc & 31)) & (cut != 0);
+      if (in && (lane < lc || (lane == lc && !e))) part += s[j] & (BLK ? kBlkValMask : kValMask);
+      if (cut) {
+        res = e ? kLbEmpty : kLbFound;
+        if (e) *empty_at = end - (32 * j + lc);
+      }
+    }
+  }
+  *sum = warp_sum_u64(part);
+  return res;
+}
+
+// The exclusive prefix of ticket t (whose aggregate is published), with the
+// two-level look-back; bounded like lookback_warp_wide.  The caller then
+// publishes with lb2_publish_inc (after a timeout: the ticket's own count
+// as its inclusive state and nothing for the block, so that no one waits).
+template <int D>
+__device__ __forceinline__ unsigned long long lb2_lookback(const unsigned long long* states,
+                                                           const unsigned long long* bwords,
+                                                           unsigned long long t,
+                                                           bool* timed_out) {
+  static_assert(32 * D >= (int)kLbBlock, "a window covers a block's tickets");
+  if (t == 0) return 0;
+  unsigned long long excl = 0, sum = 0;
+  unsigned spins = 0;
+  long long at = 0;
+  // the tickets of t's own block below t, then of any incomplete block below
+  long long blk = (long long)(t / kLbBlock);
+  long long tend = (long long)t - 1;
+  for (;;) {
+    int r;
+    while ((r = lb2_window<D, false>(states, tend, blk * (long long)kLbBlock, &sum, &at)) ==
+           kLbEmpty) {
+      if (++spins > kMaxSpins) {
+        *timed_out = true;
+        return excl;
+      }
+      if (spins > 64) __nanosleep(256);
+    }
+    excl += sum;
+    if (r == kLbFound) return excl;
+    // block words below blk, until an inclusive one or an incomplete block
+    long long bend = blk - 1;
+    for (;;) {
+      if (bend < 0) return excl;
+      const int q = lb2_window<D, true>(bwords, bend, 0, &sum, &at);
+      excl += sum;
+      if (q == kLbFound) return excl;
+      if (q == kLbEmpty) {
+        // the blocks above `at` are complete and counted; read block `at`
+        // ticket by ticket
+        blk = at;
+        tend = at * (long long)kLbBlock + kLbBlock - 1;
+        break;
+      }
+      bend -= 32 * D;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- block scan
 //
 // Exclusive scan of one uint32 per thread over a block of NT threads

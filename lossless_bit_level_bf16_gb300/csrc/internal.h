@@ -18,6 +18,16 @@ constexpr uint32_t kZcHeader = 128;
 constexpr uint32_t kZcSegRec = 64;
 constexpr uint32_t kZcAlign = 128;
 constexpr uint32_t kTileLanes = 8192;   // lanes (element slots) per encoder tile
+constexpr unsigned long long kZcLbBlock = 128;  // tiles per look-back block
+
+// ZipCCL encoder scratch after the control block: one look-back state per
+// tile, then one look-back word per block of kZcLbBlock tiles.
+constexpr unsigned long long zc_enc_blocks(unsigned long long ntiles) {
+  return (ntiles + kZcLbBlock - 1) / kZcLbBlock;
+}
+constexpr unsigned long long zc_enc_scratch_bytes(unsigned long long ntiles) {
+  return (8 * ntiles + 15) / 16 * 16 + (8 * zc_enc_blocks(ntiles) + 15) / 16 * 16;
+}
 constexpr int kThreads = 256;           // 16 lanes per thread
 
 // Per-segment record of a plan, in device memory (64 bytes).

@@ -45,7 +45,8 @@ struct EncArgs {
   const ZcSegDev* segs;
   ZcLayout L;
   Ctrl* ctrl;
-  unsigned long long* states;
+  unsigned long long* states;  // look-back state per tile
+  unsigned long long* bwords;  // look-back word per block of kLbBlock tiles
   int x_al16;
 };
 
@@ -97,6 +98,8 @@ constexpr uint32_t kEscCap = 1024;                   // escape bytes a warp stag
 // covered by the other warps' loads.
 // Dynamic shared memory per warp: the input ring (kStages x 2 KB), one
 // 256-word lookup table per chunk of a ticket, kEscCap staged escape bytes.
+static_assert(kLbBlock == kZcLbBlock, "the scratch layout and the look-back agree");
+
 __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ int s_lseg[kEncWarps][kMaxLutSlots];
@@ -120,10 +123,23 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   bool p_has = false;
   unsigned long long p_tile = 0, p_tlane0 = 0, p_cfirst = 0;
   uint32_t p_run = 0, p_cs = 0, p_buf = 0;
+  // a ticket's inclusive prefix (after a timeout: its own count, and nothing
+  // for its block, so that no one waits)
+  auto publish_inc = [&](unsigned long long tl, unsigned long long excl, unsigned long long agg,
+                         bool to) {
+    if (lane == 0) {
+      if (to) {
+        set_status(A.ctrl, ZC_ERR_TIMEOUT);
+        st_relaxed_u64(A.states + tl, kFlagInc | agg);
+      } else {
+        lb2_publish_inc(A.states, A.bwords, tl, excl, agg);
+      }
+    }
+  };
   auto resolve = [&]() {
     bool to = false;
-    const unsigned long long excl = lookback_warp_wide<8, 8, 0>(A.states, p_tile, p_run, &to);
-    if (to && lane == 0) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+    const unsigned long long excl = lb2_lookback<4>(A.states, A.bwords, p_tile, &to);
+    publish_inc(p_tile, excl, p_run, to);
     const unsigned long long dst = L.off_esc + excl;
     const uint8_t* pst = wst_base + p_buf * kEscCap;
     if (dst + p_run > A.out_cap) {
@@ -375,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     if (run <= kEscCap) {
       // publish this ticket's escape count now, resolve the previous ticket,
       // and keep this one pending in its window
-      if (lane == 0) st_relaxed_u64(A.states + tile, (tile == 0 ? kFlagInc : kFlagAgg) | run);
+      if (lane == 0) lb2_publish_agg(A.states, A.bwords, tile, run);
       if (p_has) resolve();
       p_has = true;
       p_tile = tile;
@@ -392,8 +408,10 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     // ---- more escapes than a window holds: the look-back now, then the
     // ticket is classified again and its escapes written straight out
     bool to = false;
-    const unsigned long long excl = lookback_warp_wide<8, 8, 0>(A.states, tile, run, &to);
-    if (to && lane == 0) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+    if (lane == 0) lb2_publish_agg(A.states, A.bwords, tile, run);
+    __syncwarp();
+    const unsigned long long excl = lb2_lookback<4>(A.states, A.bwords, tile, &to);
+    publish_inc(tile, excl, run, to);
     const unsigned long long dst = L.off_esc + excl;
     if (dst + run > A.out_cap) {
       if (lane == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
@@ -788,7 +806,8 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   unsigned long long* states =
       reinterpret_cast<unsigned long long*>(static_cast<char*>(d_ws) + kCtrlBytes);
   const unsigned long long ntiles = ((L.nchunks << L.log2C) + kWTile - 1) / kWTile;
-  cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 8ull * ntiles, s);
+  char* lb = static_cast<char*>(d_ws) + kCtrlBytes;
+  cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + zc_enc_scratch_bytes(ntiles), s);
   if (e != cudaSuccess) return e;
   EncArgs A;
   A.x = d_x;
@@ -799,6 +818,7 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   A.L = L;
   A.ctrl = ctrl;
   A.states = states;
+  A.bwords = reinterpret_cast<unsigned long long*>(lb + (8 * ntiles + 15) / 16 * 16);
   A.x_al16 = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
   const uint32_t nct = L.C >= kWTile ? 1u : kWTile / L.C;
   const size_t smem = (size_t)kEncWarps * (kStages * 2048u + nct * 1024u + 2 * kEscCap);

@@ -1,6 +1,7 @@
 // zc_static.cu -- zc_compress_static: ZipCCL encoding without a caller
 // workspace.  The encoder's scratch (its status/ticket block and one
-// look-back word per 8192-slot tile) lives in a fixed array in device memory
+// look-back word per 8192-slot tile and per block of 128 tiles) lives in a
+// fixed array in device memory
 // that belongs to the library, so this entry point allocates nothing and
 // needs no workspace from the caller.  The encoding itself is the one
 // zc_compress runs (same launcher, same kernel, same stream bytes).
@@ -14,10 +15,13 @@
 
 namespace {
 
-// 1 MiB: the 256-byte control block, then 131,040 look-back words, enough for
-// plans of up to 131,040 tiles of 8192 slots (1,073,479,680 slots).
+// 1 MiB: the 256-byte control block, then the encoder's look-back states,
+// enough for plans of up to 130,024 tiles of 8192 slots (1,065,156,608 slots).
 constexpr size_t kStaticScratchBytes = 1u << 20;
-constexpr unsigned long long kStaticMaxTiles = (kStaticScratchBytes - lbb::kCtrlBytes) / 8;
+constexpr unsigned long long kStaticMaxTiles = 130024;
+static_assert(lbb::kCtrlBytes + lbb::zc_enc_scratch_bytes(kStaticMaxTiles) <= kStaticScratchBytes &&
+                  lbb::kCtrlBytes + lbb::zc_enc_scratch_bytes(kStaticMaxTiles + 1) > kStaticScratchBytes,
+              "the largest plan the fixed scratch holds");
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_zc_scratch[kStaticScratchBytes];

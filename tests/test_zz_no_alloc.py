@@ -74,7 +74,7 @@ def test_static_status_reports_capacity():
 
 def test_static_rejects_plans_beyond_its_scratch():
     lib = abi.load()
-    n = 131040 * 8192 + 1  # one slot more than the fixed scratch covers
+    n = 130024 * 8192 + 1  # one slot more than the fixed scratch covers
     x = torch.zeros(16, dtype=torch.bfloat16, device=DEV)  # never read: the call refuses
     out = torch.zeros(1 << 10, dtype=torch.uint8, device=DEV)
     nb = torch.zeros(1, dtype=torch.int64, device=DEV)

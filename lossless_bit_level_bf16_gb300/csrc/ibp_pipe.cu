@@ -548,7 +548,9 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
       uint8_t* st = stages + (size_t)s * A.stage_bytes;
       for (uint32_t w = b16 / 4; w < (uint32_t)(tb / 4); ++w)  // the last 4..12 bytes
         reinterpret_cast<uint32_t*>(st)[w] = __ldg(reinterpret_cast<const uint32_t*>(A.src + b0) + w);
-      fence_proxy_async_smem();
+      // Only the last tile has words written through the generic proxy; the
+      // stage's earlier reads are ordered by the barrier, as with any TMA ring.
+      if (b16 != tb) fence_proxy_async_smem();
       mbar_arrive_expect_tx(bars + s, b16);
       if (b16) bulk_g2s(st, A.src + b0, b16, bars + s);
     }
@@ -779,7 +781,10 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
     const uint32_t tb = tile_bytes(tile), b16 = tb & ~15u;
     for (uint32_t w = b16 / 4; w < tb / 4; ++w)
       reinterpret_cast<uint32_t*>(st)[w] = __ldg(reinterpret_cast<const uint32_t*>(A.src + b0) + w);
-    fence_proxy_async_smem();
+    // Only the last tile has words written through the generic proxy (a fence
+    // here would also wait for the thread's outstanding global stores); the
+    // stage's earlier reads are ordered by the barrier, as with any TMA ring.
+    if (b16 != tb) fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar, b16);
     if (b16) bulk_g2s(st, A.src + b0, b16, bar);
   };
@@ -1219,7 +1224,6 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
       s_goff[s][nq] = gend;
       s_tile[s] = tile;
       s_sbad[s] = bad;
-      fence_proxy_async_smem();
       if (bad) {
         mbar_arrive_expect_tx(bars + s, 0);  // nothing to copy: the phase completes now
       } else {

@@ -1029,28 +1029,34 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
       const bool fits = dst + 16ull * nv <= A.dst_cap;
       if (!fits && t == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
       if (raw) {
-        // [0][input words][zero padding] per group, straight from the stage
-        for (uint32_t u0 = t; u0 < nv; u0 += 4 * kWsPack) {
+        // [0][input words][zero padding] per group, straight from the stage:
+        // stream vector lu of group q is input words 4 lu - 1 .. 4 lu + 2; a
+        // lane loads words 4 lu .. 4 lu + 3 and takes word 4 lu - 1 from the
+        // lane before it (lane 0 reads it), which keeps the loads 16-byte;
+        // the loop runs while the warp's first vector is in (the shuffles
+        // take every lane)
+        for (uint32_t u0 = t; u0 - lane < nv; u0 += 4 * kWsPack) {
           uint4 o[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const uint32_t u = u0 + e * kWsPack;
-            if (u >= nv) continue;
             const uint32_t q = Q == 1 ? 0u : u / gvec, lu = u - q * gvec;
             const uint32_t ib = q * 32u * W;  // group's first input word in the stage
             const uint32_t bw = (q + 1 == nq) ? twords - ib : 32u * W;
-            if (lu > 0 && 4 * lu + 3 <= bw) {
-              const uint4 x = *reinterpret_cast<const uint4*>(sd + ib + 4 * lu);
-              o[e] = make_uint4(sd[ib + 4 * lu - 1], x.x, x.y, x.z);
-            } else {
-              uint32_t w[4];
-#pragma unroll
-              for (uint32_t kk = 0; kk < 4; ++kk) {
-                const uint32_t ow = 4 * lu + kk;  // word of the group's stream
-                w[kk] = (ow >= 1 && ow - 1 < bw) ? sd[ib + ow - 1] : 0u;
+            uint4 x = make_uint4(0, 0, 0, 0);
+            if (u < nv) {
+              if (4 * lu + 3 < bw) {
+                x = *reinterpret_cast<const uint4*>(sd + ib + 4 * lu);
+              } else {
+                x.x = 4 * lu < bw ? sd[ib + 4 * lu] : 0u;
+                x.y = 4 * lu + 1 < bw ? sd[ib + 4 * lu + 1] : 0u;
+                x.z = 4 * lu + 2 < bw ? sd[ib + 4 * lu + 2] : 0u;
               }
-              o[e] = make_uint4(w[0], w[1], w[2], w[3]);
             }
+            uint32_t prev = __shfl_up_sync(kFull, x.w, 1);
+            if (lu == 0) prev = 0u;  // the group's participation word: none
+            else if (lane == 0) prev = (u < nv && 4 * lu - 1 < bw) ? sd[ib + 4 * lu - 1] : 0u;
+            o[e] = make_uint4(prev, x.x, x.y, x.z);
           }
           if (fits) {
 #pragma unroll
@@ -1099,15 +1105,17 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
         }
         named_bar(1, kWsPack);
         if (fits) {
-          for (uint32_t u0 = t; u0 < nv; u0 += 4 * kWsPack) {
+          // stream vector u is image words 4 u + 3 .. 4 u + 6: a lane loads
+          // image vector u + 1 and takes word 4 u + 3 from the lane before it
+          for (uint32_t u0 = t; u0 - lane < nv; u0 += 4 * kWsPack) {
             uint4 o[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const uint32_t u = u0 + e * kWsPack;
-              if (u < nv) {
-                const uint4 x = img4[u + 1];
-                o[e] = make_uint4(img[4 * u + 3], x.x, x.y, x.z);
-              }
+              const uint4 x = u < nv ? img4[u + 1] : make_uint4(0, 0, 0, 0);
+              uint32_t prev = __shfl_up_sync(kFull, x.w, 1);
+              if (lane == 0) prev = u < nv ? img[4 * u + 3] : 0u;
+              o[e] = make_uint4(prev, x.x, x.y, x.z);
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {

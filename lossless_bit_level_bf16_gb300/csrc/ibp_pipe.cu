@@ -165,6 +165,12 @@ __device__ __forceinline__ uint32_t vt_compress(const VecTab& v, uint32_t x, int
     return ((x >> v.MV[0][w]) & v.MV[1][w]) | (((x >> v.MV[2][w]) & v.MV[3][w]) << v.MV[4][w]);
   return hd_compress(x, v.K[w], &v.MV[0][w], 4);
 }
+// vt_compress for the three-run form (equal to the two-run form when the
+// keep masks have at most two runs: the third run's mask is then zero).
+__device__ __forceinline__ uint32_t vt_compress3(const VecTab& v, uint32_t x, int w) {
+  return ((x >> v.MV[0][w]) & v.MV[1][w]) | (((x >> v.MV[2][w]) & v.MV[3][w]) << v.MV[4][w]) |
+         (((x >> v.R3[0][w]) & v.R3[1][w]) << v.R3[2][w]);
+}
 // Inverse: the low kept-bit count of f spread out to the kept positions.
 __device__ __forceinline__ uint32_t vt_expand(const VecTab& v, uint32_t f, int w) {
   if (v.fast)
@@ -1007,6 +1013,7 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
     if (REG) {
       load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
       make_runs(vt);
+      make_runs3(vt);
     }
     if (t == 0)
       for (uint32_t s = 0; s < kWsStages && s < mine; ++s)
@@ -1068,6 +1075,11 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
         }
       } else {
         if ((uint32_t)t < nq) img[3 + (si.gex[t] >> 5)] = si.pw[t];
+        // Compiled for the general keep masks and for masks of at most three
+        // runs per word (16-bit data); a thread takes the one its vector
+        // position allows (the loop has no warp-wide operation).
+        auto pack_vectors = [&](auto three) {
+        constexpr bool THREE = decltype(three)::value;
         // two vectors per thread per step: independent chains to interleave
         for (uint32_t v0 = t; v0 < nvec; v0 += 2 * kWsPack) {
 #pragma unroll
@@ -1087,7 +1099,7 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
             if ((pwq >> i5) & 1u) {
               uint32_t f[4];
 #pragma unroll
-              for (int w = 0; w < 4; ++w) f[w] = vt_compress(vt, dw[w], w);
+              for (int w = 0; w < 4; ++w) f[w] = THREE ? vt_compress3(vt, dw[w], w) : vt_compress(vt, dw[w], w);
               uint32_t kk[4];
               kept_bits(vt, kk);
               cat4(f, kk, o);
@@ -1103,6 +1115,9 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
             img_put(img, 96u + pos, o, n);
           }
         }
+        };
+        if (REG && vt.fast3) pack_vectors(std::true_type{});
+        else pack_vectors(std::false_type{});
         named_bar(1, kWsPack);
         if (fits) {
           // stream vector u is image words 4 u + 3 .. 4 u + 6: a lane loads

@@ -451,7 +451,7 @@ def _case(kind, nbytes, dev, ibp_mode):
         out = torch.empty(plan.max_compressed_bytes, dtype=torch.uint8, device=dev)
         nb = torch.zeros(1, dtype=torch.int64, device=dev)
         y = torch.empty_like(x)
-        dws = torch.empty(256, dtype=torch.uint8, device=dev)
+        dws = torch.zeros(256, dtype=torch.uint8, device=dev)
         ops = [("zc_plan", lambda: plan.fit(x)),
                ("zc_compress", lambda: plan.compress(x, out=out, out_bytes=nb)),
                ("zc_decompress", lambda: Z.decompress(out, out=y, in_bytes=out.numel(), ws=dws))]
@@ -487,12 +487,12 @@ def _case(kind, nbytes, dev, ibp_mode):
         st, stn = I.compress(meta, xd, cb)
         torch.cuda.synchronize()
         sh = st[: int(stn.item())].cpu().pin_memory()
-        mws = torch.empty(I.workspace_bytes(cb, 0, samples.shape[0]), dtype=torch.uint8, device=dev)
-        iws = torch.empty(I.workspace_bytes(cb, 4 * n, 0), dtype=torch.uint8, device=dev)
+        mws = torch.zeros(I.workspace_bytes(cb, 0, samples.shape[0]), dtype=torch.uint8, device=dev)
+        iws = torch.zeros(I.workspace_bytes(cb, 4 * n, 0), dtype=torch.uint8, device=dev)
         out = torch.empty(I.max_compressed_bytes(cb, 4 * n), dtype=torch.uint8, device=dev)
         nb = torch.zeros(1, dtype=torch.int64, device=dev)
         y = torch.empty_like(xd)
-        dws = torch.empty(256, dtype=torch.uint8, device=dev)
+        dws = torch.zeros(256, dtype=torch.uint8, device=dev)
         ops = [("ibp_build_meta", lambda: I.build_meta(samples, cb, T=0.9, mode=ibp_mode,
                                                        meta=meta, ws=mws)),
                ("ibp_compress", lambda: I.compress(meta, xh, cb, out=out, out_bytes=nb, ws=iws)),
@@ -503,12 +503,12 @@ def _case(kind, nbytes, dev, ibp_mode):
         return ops, (mws, iws, dws), 4 * n, samples.shape[0] * cb, check, nb, cb
     ns = samples.shape[0]
     meta = torch.empty(64 + 2 * cb, dtype=torch.uint8, device=dev)
-    mws = torch.empty(I.workspace_bytes(cb, 0, ns), dtype=torch.uint8, device=dev)
-    iws = torch.empty(I.workspace_bytes(cb, 4 * n, 0), dtype=torch.uint8, device=dev)
+    mws = torch.zeros(I.workspace_bytes(cb, 0, ns), dtype=torch.uint8, device=dev)
+    iws = torch.zeros(I.workspace_bytes(cb, 4 * n, 0), dtype=torch.uint8, device=dev)
     out = torch.empty(I.max_compressed_bytes(cb, 4 * n), dtype=torch.uint8, device=dev)
     nb = torch.zeros(1, dtype=torch.int64, device=dev)
     y = torch.empty_like(x)
-    dws = torch.empty(256, dtype=torch.uint8, device=dev)
+    dws = torch.zeros(256, dtype=torch.uint8, device=dev)
     ops = [("ibp_build_meta", lambda: I.build_meta(samples, cb, T=0.9, mode=ibp_mode, meta=meta,
                                                    ws=mws)),
            ("ibp_compress", lambda: I.compress(meta, x, cb, out=out, out_bytes=nb, ws=iws)),

@@ -90,10 +90,21 @@ __device__ __forceinline__ void pair_add(float& a, float& b, float a2, float b2)
   b = __fadd_rn(b, b2);
 }
 
+// The warp's loads run ahead of its sums through a ring of kStatRing batches
+// in shared memory (cp.async: each lane copies the 16-byte pieces it will sum
+// itself, so the warp needs no synchronization), over its whole range of
+// units.  Units of a segment that does not start 16-byte aligned, and the
+// pieces at a unit's ragged end, are read with per-element loads when summed.
+constexpr int kStatRing = 3;
+constexpr uint32_t kStatSlotVecs = kStatBatch * 2 * 32;  // 16-byte pieces per batch
+constexpr size_t kStatSmem = (size_t)kStatWarps * kStatRing * kStatSlotVecs * 16;
+
 __global__ void __launch_bounds__(kThreads, 2) zc_stats_kernel(
     const uint16_t* __restrict__ x, const ZcSegDev* __restrict__ segs, uint32_t nseg,
     uint32_t U, unsigned long long nunits, StatPartial* __restrict__ parts, int x_al16) {
+  extern __shared__ uint4 s_ring[];
   const int lane = threadIdx.x & 31;
+  uint4* ring = s_ring + (size_t)(threadIdx.x >> 5) * kStatRing * kStatSlotVecs;
   grid_dep_launch();  // the predictor may be scheduled as blocks finish
   unsigned long long ub;
   uint32_t nu;  // this warp's units: ub .. ub + nu - 1
@@ -104,121 +115,179 @@ __global__ void __launch_bounds__(kThreads, 2) zc_stats_kernel(
     ub = gw * q + (gw < r ? gw : r);
     nu = (uint32_t)(q + (gw < r ? 1 : 0));
   }
-  int sc = -1;  // lane 0: segment of the current unit
-  for (uint32_t k = 0; k < nu; ++k) {
-    const unsigned long long unit = ub + k;
+  // A position in the warp's sequence of (unit, batch): the unit's element
+  // range, whether it is 16-byte aligned, and the batch's first element.
+  struct Cursor {
+    uint32_t k;
+    int sc;  // lane 0: segment of unit k
+    unsigned long long lo, hi, base;
+    int al;
+  };
+  auto load_unit = [&](Cursor& c) {  // the whole warp
+    const unsigned long long unit = ub + c.k;
     unsigned long long lo = 0, hi = 0;
     int al = 0;
     if (lane == 0) {
-      if (sc < 0) sc = find_unit_segment(segs, nseg, unit);
-      while (sc + 1 < (int)nseg && segs[sc + 1].unit_start <= unit) ++sc;
-      const int s = sc;
-      lo = segs[s].elem_start + (unit - segs[s].unit_start) * U;
-      const unsigned long long e = segs[s].elem_start + segs[s].nelem;
+      if (c.sc < 0) c.sc = find_unit_segment(segs, nseg, unit);
+      while (c.sc + 1 < (int)nseg && segs[c.sc + 1].unit_start <= unit) ++c.sc;
+      const int sg = c.sc;
+      lo = segs[sg].elem_start + (unit - segs[sg].unit_start) * U;
+      const unsigned long long e = segs[sg].elem_start + segs[sg].nelem;
       hi = (lo + U < e) ? lo + U : e;
-      al = x_al16 && ((segs[s].elem_start & 7ull) == 0);
+      al = x_al16 && ((segs[sg].elem_start & 7ull) == 0);
     }
-    lo = __shfl_sync(kFull, lo, 0);
-    hi = __shfl_sync(kFull, hi, 0);
-    al = __shfl_sync(kFull, al, 0);
+    c.lo = __shfl_sync(kFull, lo, 0);
+    c.hi = __shfl_sync(kFull, hi, 0);
+    c.al = __shfl_sync(kFull, al, 0);
+    c.base = c.lo;
+  };
+  auto advance = [&](Cursor& c) -> bool {  // to the next batch; false past the last
+    c.base += kStatBatch * 512ull;
+    if (c.base < c.hi) return true;
+    if (++c.k >= nu) return false;
+    load_unit(c);
+    return true;
+  };
+  auto issue = [&](const Cursor& c, int slot) {
+    if (!c.al) return;
+#pragma unroll
+    for (int g = 0; g < kStatBatch; ++g)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const unsigned long long e0 = c.base + g * 512ull + 256ull * h + 8ull * lane;
+        if (e0 + 8 <= c.hi)
+          cp_async16(ring + (size_t)slot * kStatSlotVecs + (2 * g + h) * 32 + lane, x + e0);
+      }
+  };
 
-    float hx = 0.f, lx = 0.f, hq = 0.f, lq = 0.f;
-    double dx = 0.0, dq = 0.0;
-    unsigned long long cnt = 0;
-    for (unsigned long long base0 = lo; base0 < hi; base0 += kStatBatch * 512ull) {
-      uint32_t w[kStatBatch][8];
-      int vh[kStatBatch][2];
+  Cursor ci{0, -1, 0, 0, 0, 0};
+  bool more = nu > 0;  // the issue cursor has a batch
+  if (more) load_unit(ci);
+  Cursor cc = ci;      // the sum cursor, kStatRing - 1 batches behind
+  int islot = 0, cslot = 0;
 #pragma unroll
-      for (int g = 0; g < kStatBatch; ++g) {
+  for (int p = 0; p < kStatRing - 1; ++p) {
+    if (more) {
+      issue(ci, islot);
+      more = advance(ci);
+    }
+    cp_async_commit();
+    islot = islot + 1 == kStatRing ? 0 : islot + 1;
+  }
+  float hx = 0.f, lx = 0.f, hq = 0.f, lq = 0.f;
+  double dx = 0.0, dq = 0.0;
+  unsigned long long cnt = 0;
+  bool have = nu > 0;  // the sum cursor has a batch
+  while (have) {
+    if (more) {
+      issue(ci, islot);
+      more = advance(ci);
+    }
+    cp_async_commit();
+    islot = islot + 1 == kStatRing ? 0 : islot + 1;
+    cp_async_wait_group<kStatRing - 1>();  // this lane's pieces of the batch
+    uint32_t w[kStatBatch][8];
+    int vh[kStatBatch][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const unsigned long long e0 = base0 + g * 512ull + 256ull * h + 8ull * lane;
-          const unsigned long long rem = e0 < hi ? hi - e0 : 0ull;
-          const int v = rem < 8 ? (int)rem : 8;
-          vh[g][h] = v;
-          if (v == 8 && al) {
-            const uint4 a4 = ld_nc_v4(x + e0);
-            w[g][4 * h] = a4.x; w[g][4 * h + 1] = a4.y; w[g][4 * h + 2] = a4.z; w[g][4 * h + 3] = a4.w;
-          } else {
+    for (int g = 0; g < kStatBatch; ++g) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t l = (2 * j < v) ? (uint32_t)__ldg(x + e0 + 2 * j) : 0u;
-              const uint32_t hh = (2 * j + 1 < v) ? (uint32_t)__ldg(x + e0 + 2 * j + 1) : 0u;
-              w[g][4 * h + j] = l | (hh << 16);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < kStatBatch; ++g) {
-        const int valid = vh[g][0] + vh[g][1];
-        if (valid == 0) continue;
-        float v[16];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          v[2 * j] = bf16_lo(w[g][j]);
-          v[2 * j + 1] = bf16_hi(w[g][j]);
-        }
-        float q[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) q[j] = __fmul_rn(v[j], v[j]);
-#pragma unroll
-        for (int st = 1; st < 16; st <<= 1) {
-#pragma unroll
-          for (int j = 0; j < 16; j += 2 * st) {
-            v[j] = __fadd_rn(v[j], v[j + st]);
-            q[j] = __fadd_rn(q[j], q[j + st]);
-          }
-        }
-        if (isfinite(v[0]) && isfinite(q[0])) {
-          two_sum_acc(hx, lx, v[0]);
-          two_sum_acc(hq, lq, q[0]);
-          cnt += (unsigned long long)valid;
+      for (int h = 0; h < 2; ++h) {
+        const unsigned long long e0 = cc.base + g * 512ull + 256ull * h + 8ull * lane;
+        const unsigned long long rem = e0 < cc.hi ? cc.hi - e0 : 0ull;
+        const int v = rem < 8 ? (int)rem : 8;
+        vh[g][h] = v;
+        if (v == 8 && cc.al) {
+          const uint4 a4 = ring[(size_t)cslot * kStatSlotVecs + (2 * g + h) * 32 + lane];
+          w[g][4 * h] = a4.x; w[g][4 * h + 1] = a4.y; w[g][4 * h + 2] = a4.z; w[g][4 * h + 3] = a4.w;
         } else {
-          // an inf/NaN input or an fp32 overflow: redo these values in fp64
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint32_t bits = (j & 1) ? (w[g][j >> 1] >> 16) : (w[g][j >> 1] & 0xFFFFu);
-            if ((j & 7) < vh[g][j >> 3] && ((bits >> 7) & 0xFFu) != 0xFFu) {
-              const double d = (double)__uint_as_float(bits << 16);
-              dx = __dadd_rn(dx, d);
-              dq = __dadd_rn(dq, __dmul_rn(d, d));
-              cnt += 1;
-            }
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t l = (2 * j < v) ? (uint32_t)__ldg(x + e0 + 2 * j) : 0u;
+            const uint32_t hh = (2 * j + 1 < v) ? (uint32_t)__ldg(x + e0 + 2 * j + 1) : 0u;
+            w[g][4 * h + j] = l | (hh << 16);
           }
         }
       }
     }
-    // lanes: fp32 pairs, fp64 if a pair overflows or fp64 sums exist
-    float ax = hx, bx = lx, aq = hq, bq = lq;
+    cslot = cslot + 1 == kStatRing ? 0 : cslot + 1;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ax2 = __shfl_down_sync(kFull, ax, o), bx2 = __shfl_down_sync(kFull, bx, o);
-      const float aq2 = __shfl_down_sync(kFull, aq, o), bq2 = __shfl_down_sync(kFull, bq, o);
-      pair_add(ax, bx, ax2, bx2);
-      pair_add(aq, bq, aq2, bq2);
-      cnt += __shfl_down_sync(kFull, cnt, o);
+    for (int g = 0; g < kStatBatch; ++g) {
+      const int valid = vh[g][0] + vh[g][1];
+      if (valid == 0) continue;
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[2 * j] = bf16_lo(w[g][j]);
+        v[2 * j + 1] = bf16_hi(w[g][j]);
+      }
+      float q[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) q[j] = __fmul_rn(v[j], v[j]);
+#pragma unroll
+      for (int st = 1; st < 16; st <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 16; j += 2 * st) {
+          v[j] = __fadd_rn(v[j], v[j + st]);
+          q[j] = __fadd_rn(q[j], q[j + st]);
+        }
+      }
+      if (isfinite(v[0]) && isfinite(q[0])) {
+        two_sum_acc(hx, lx, v[0]);
+        two_sum_acc(hq, lq, q[0]);
+        cnt += (unsigned long long)valid;
+      } else {
+        // an inf/NaN input or an fp32 overflow: redo these values in fp64
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t bits = (j & 1) ? (w[g][j >> 1] >> 16) : (w[g][j >> 1] & 0xFFFFu);
+          if ((j & 7) < vh[g][j >> 3] && ((bits >> 7) & 0xFFu) != 0xFFu) {
+            const double d = (double)__uint_as_float(bits << 16);
+            dx = __dadd_rn(dx, d);
+            dq = __dadd_rn(dq, __dmul_rn(d, d));
+            cnt += 1;
+          }
+        }
+      }
     }
-    const bool fin = __shfl_sync(kFull, isfinite(ax) && isfinite(bx) && isfinite(aq) && isfinite(bq), 0);
-    double t1, t2;
-    if (!fin || __any_sync(kFull, dx != 0.0 || dq != 0.0)) {
-      t1 = __dadd_rn(__dadd_rn((double)hx, (double)lx), dx);
-      t2 = __dadd_rn(__dadd_rn((double)hq, (double)lq), dq);
+    if (cc.base + kStatBatch * 512ull >= cc.hi) {
+      // the unit's last batch: lanes' fp32 pairs, fp64 if a pair overflows or
+      // fp64 sums exist
+      float ax = hx, bx = lx, aq = hq, bq = lq;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        t1 = __dadd_rn(t1, __shfl_down_sync(kFull, t1, o));
-        t2 = __dadd_rn(t2, __shfl_down_sync(kFull, t2, o));
+        const float ax2 = __shfl_down_sync(kFull, ax, o), bx2 = __shfl_down_sync(kFull, bx, o);
+        const float aq2 = __shfl_down_sync(kFull, aq, o), bq2 = __shfl_down_sync(kFull, bq, o);
+        pair_add(ax, bx, ax2, bx2);
+        pair_add(aq, bq, aq2, bq2);
+        cnt += __shfl_down_sync(kFull, cnt, o);
       }
-    } else {
-      t1 = __dadd_rn((double)ax, (double)bx);
-      t2 = __dadd_rn((double)aq, (double)bq);
+      const bool fin = __shfl_sync(kFull, isfinite(ax) && isfinite(bx) && isfinite(aq) && isfinite(bq), 0);
+      double t1, t2;
+      if (!fin || __any_sync(kFull, dx != 0.0 || dq != 0.0)) {
+        t1 = __dadd_rn(__dadd_rn((double)hx, (double)lx), dx);
+        t2 = __dadd_rn(__dadd_rn((double)hq, (double)lq), dq);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          t1 = __dadd_rn(t1, __shfl_down_sync(kFull, t1, o));
+          t2 = __dadd_rn(t2, __shfl_down_sync(kFull, t2, o));
+        }
+      } else {
+        t1 = __dadd_rn((double)ax, (double)bx);
+        t2 = __dadd_rn((double)aq, (double)bq);
+      }
+      if (lane == 0) {
+        const unsigned long long unit = ub + cc.k;
+        parts[unit].cnt = cnt;
+        parts[unit].s1 = t1;
+        parts[unit].s2 = t2;
+      }
+      hx = lx = hq = lq = 0.f;
+      dx = dq = 0.0;
+      cnt = 0;
     }
-    if (lane == 0) {
-      parts[unit].cnt = cnt;
-      parts[unit].s1 = t1;
-      parts[unit].s2 = t2;
-    }
+    have = advance(cc);
   }
+  cp_async_wait_all();
 }
 
 // Gaussian mass of exponent field f, P(2^(f-127) <= |X| < 2^(f-126)) for
@@ -435,11 +504,14 @@ cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
   StatPartial* parts = reinterpret_cast<StatPartial*>(static_cast<char*>(d_ws) + kCtrlBytes);
   const int al = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
   if (L.nunits) {
-    const int res = resident_blocks((const void*)zc_stats_kernel, kThreads, 0);
+    cudaError_t e = cudaFuncSetAttribute(zc_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kStatSmem);
+    if (e != cudaSuccess) return e;
+    const int res = resident_blocks((const void*)zc_stats_kernel, kThreads, kStatSmem);
     const unsigned long long need = (L.nunits + kStatWarps - 1) / kStatWarps;
     const unsigned grid = (unsigned)(need < (unsigned long long)res ? need : (unsigned long long)res);
-    zc_stats_kernel<<<grid, kThreads, 0, s>>>(d_x, d_segs, L.nseg, L.U, L.nunits, parts, al);
-    cudaError_t e = cudaGetLastError();
+    zc_stats_kernel<<<grid, kThreads, kStatSmem, s>>>(d_x, d_segs, L.nseg, L.U, L.nunits, parts, al);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return launch_dependent(zc_predict_kernel, L.nseg, kThreads, 0, s,

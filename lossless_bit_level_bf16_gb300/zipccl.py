@@ -54,7 +54,8 @@ class Plan:
         self._h = h
         self.workspace_bytes = int(self.lib.zc_workspace_bytes(h))
         self.max_compressed_bytes = int(self.lib.zc_max_compressed_bytes(h))
-        self.ws = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=self.device)
+        # zeroed once: the status word reads 0 until an op reports an error
+        self.ws = torch.zeros(self.workspace_bytes, dtype=torch.uint8, device=self.device)
 
     def __del__(self):
         h = getattr(self, "_h", None)

@@ -75,6 +75,23 @@ def test_every_bf16_pattern(chunk):
             _check_full(x, None, chunk, books)
 
 
+@pytest.mark.parametrize("ntiles", [127, 128, 129, 257])
+def test_escape_overflow_across_lookback_blocks(ntiles):
+    """The encoder groups its 8192-slot tickets in blocks of 128 for the
+    look-back.  Every third ticket here holds random bit patterns (almost
+    every value an escape, more than a ticket stages, so the ticket resolves
+    its offset at once); the others N(0, 0.01) (about 2 % escapes, resolved a
+    ticket later); across block boundaries, with a ragged last ticket."""
+    n = ntiles * 8192 - 5
+    x = W.zc_gaussian(n, sigma=0.01, seed=ntiles)
+    xb = x.view(torch.int16)
+    g = torch.Generator().manual_seed(1000 + ntiles)
+    for t in range(0, ntiles, 3):
+        lo, hi = t * 8192, min(n, (t + 1) * 8192)
+        xb[lo:hi] = torch.randint(-32768, 32768, (hi - lo,), generator=g, dtype=torch.int32).to(torch.int16)
+    _check_full(x.to(DEV), None, 4096, [116, 117, 118, 119, 120, 121, 122])
+
+
 def test_gradient_blocks_64m():
     x, seg = W.zc_gradient(device=DEV)
     st, plan = _check_full(x, seg)

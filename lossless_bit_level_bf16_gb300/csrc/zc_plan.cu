@@ -415,19 +415,34 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
     s_keyf[t] = __float_as_uint(mf);  // non-negative floats order like their bits
   }
   __syncthreads();
-  {
-    int rank = 256;
-    if (t >= 1 && t <= 254) {
-      const uint32_t m = s_keyf[t];
-      rank = 0;
-      for (int g = 1; g <= 254; ++g) {
-        const uint32_t mg = s_keyf[g];
-        rank += (mg > m || (mg == m && g < t)) ? 1 : 0;
+  if (t < 32) {
+    // The 8 largest masses of fields 1..254 (ties to the lower field) by
+    // eight rounds of a warp argmax, lane l holding fields 8l .. 8l + 7: the
+    // first 7 are taken, the 7th and 8th masses decide the margin.
+    const int f0 = 8 * t;
+    uint32_t taken = 0;
+    for (int r = 0; r < 8; ++r) {
+      unsigned long long best = 0;  // (mass bits << 32) | (255 - field); 0 = none
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int f = f0 + i;
+        if (f >= 1 && f <= 254 && !((taken >> i) & 1u)) {
+          const unsigned long long cand = ((unsigned long long)s_keyf[f] << 32) | (unsigned)(255 - f);
+          best = cand > best ? cand : best;
+        }
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(kFull, best, o);
+        best = y > best ? y : best;
+      }
+      const int fs = 255 - (int)(best & 0xFFFFFFFFull);
+      if (r < 7 && fs >= f0 && fs < f0 + 8) taken |= 1u << (fs - f0);
+      if (t == 0 && r == 6) s_m7f = __uint_as_float((uint32_t)(best >> 32));
+      if (t == 0 && r == 7) s_m8f = __uint_as_float((uint32_t)(best >> 32));
     }
-    s_take[t] = rank < 7;
-    if (rank == 6) s_m7f = __uint_as_float(s_keyf[t]);
-    if (rank == 7) s_m8f = __uint_as_float(s_keyf[t]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s_take[f0 + i] = (taken >> i) & 1u;
   }
   __syncthreads();
   if (!(s_m7f - s_m8f > 2e-5f)) {

@@ -1324,6 +1324,32 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
     const uint32_t tb = (uint32_t)((n_bytes - b0) < tile_raw ? (n_bytes - b0) : tile_raw);
     const uint32_t twords = tb / 4, nvec = (tb + 15) / 16;
     uint32_t* yt = reinterpret_cast<uint32_t*>(A.dst + b0);
+    if (Q == 1 && s_pw[bf][0] == 0 && !s_gbad[bf][0]) {
+      // A tile of one group in which no chunk participates: output word j is
+      // stream word 1 + j.  A lane loads stage vector v (words 4v .. 4v + 3)
+      // and takes word 4v + 4 from the lane above (lane 31 reads it), so the
+      // lane just past the last vector loads too (inside the stage: a stage
+      // holds 16 bytes more than a tile's vectors); the loop runs while the
+      // warp's first vector is in (the shuffle takes every lane).  The same
+      // for every thread of the block.
+      const uint4* sd4 = reinterpret_cast<const uint4*>(sd);
+      for (uint32_t v = t; v - lane < nvec; v += NT) {
+        const uint4 x = v <= nvec ? sd4[v] : make_uint4(0, 0, 0, 0);
+        uint32_t nx = __shfl_down_sync(kFull, x.x, 1);
+        if (lane == 31) nx = v < nvec ? sd[4 * v + 4] : 0u;
+        if (v < nvec) {
+          const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
+          if (wv == 4) {
+            st_v4(yt + 4 * v, make_uint4(x.y, x.z, x.w, nx));
+          } else {
+            const uint32_t o[3] = {x.y, x.z, x.w};
+#pragma unroll
+            for (uint32_t w = 0; w < 3; ++w)
+              if (w < wv) yt[4 * v + w] = o[w];
+          }
+        }
+      }
+    } else
     // two vectors per thread per step (same chunk position, so the same
     // register tables): two independent dependency chains to interleave
     for (uint32_t v0 = t; v0 < nvec; v0 += 2 * NT) {

@@ -59,15 +59,24 @@ def csrc_hash():
 
 def _traffic_table():
     """Measured DRAM traffic per launch from the committed ncu summaries:
-    lines 'traffic <kernel> <sources sha1> <bytes per launch>' in profiles/*.md."""
+    lines 'traffic <kernel> <sources sha1> <bytes per launch>' in profiles/*.md,
+    as {kernel: {sha1: bytes}} (a kernel may have lines from several captures)."""
     import glob
     out = {}
-    for f in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+    for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         for line in open(f):
             parts = line.strip().strip("`").split()
-            if len(parts) == 4 and parts[0] == "traffic":
-                out[parts[1]] = (parts[2], int(parts[3]))
+            if len(parts) == 4 and parts[0] == "traffic" and parts[3].isdigit():
+                out.setdefault(parts[1], {})[parts[2]] = int(parts[3])
     return out
+
+
+def measured_traffic(kernel, table=None, sha=None):
+    """The kernel's DRAM bytes per launch measured on the current sources, or
+    None when no capture matches them."""
+    table = _traffic_table() if table is None else table
+    sha = csrc_hash() if sha is None else sha
+    return table.get(kernel, {}).get(sha)
 
 
 class ClockSampler:
@@ -367,11 +376,8 @@ def report_gpu(args, r, world):
     single = [k for k in r["per_op"] if len(wl.kernels[k]) == 1]
     dom = max(single, key=lambda k: statistics.mean(r["per_op"][k]))
     t_dom = statistics.mean(r["per_op"][dom])
-    table = _traffic_table()
-    traffic = None
     kname = wl.kernels[dom][0]
-    if kname in table and table[kname][0] == csrc_hash():
-        traffic = table[kname][1]
+    traffic = measured_traffic(kname)
     achieved = alg[dom] / (t_dom * 1e-3) / 1e9
     line = {
         "metric": METRIC,

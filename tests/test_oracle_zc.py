@@ -124,9 +124,15 @@ def test_multisegment_layout_and_books():
     nseg = len(lens)
     recs = st[128:128 + 64 * nseg].reshape(nseg, 64)
     esc_start = 0
+    chunk_start = 0
     for s in range(nseg):
         r = recs[s, :48].view(np.uint64)
         assert int(r[0]) == seg[s] and int(r[1]) == lens[s]
+        # each segment is chunked on its own: ceil(len / C) chunks, numbered
+        # after the chunks of the segments before it
+        assert int(r[2]) == chunk_start
+        assert int(r[3]) == -(-lens[s] // 2048)
+        chunk_start += -(-lens[s] // 2048)
         assert int(r[4]) == esc_start
         xs = x[seg[s]:seg[s + 1]]
         # the book of each segment comes from that segment's own values
@@ -142,6 +148,7 @@ def test_multisegment_layout_and_books():
         assert int(r[5]) == n_esc
         esc_start += n_esc
     assert st.size == O.zc_stream_bytes(x.size, seg, 2048, esc_start)
+    assert int(st[24:32].view(np.uint64)[0]) == chunk_start == 5 + 0 + 2 + 7 + 1
 
 
 def test_empty_input():
@@ -278,3 +285,51 @@ def test_mass_sums_to_one():
     for mu, s in [(0.0, 0.02), (0.5, 0.1), (-2.0, 3.0)]:
         tot = sum(O.zc_mass(mu, s, f) for f in range(1, 255))
         assert tot == pytest.approx(1.0, abs=1e-12)
+
+
+def _norm_mass(mu, sigma, f):
+    """P(2^(f-127) <= |X| < 2^(f-126)) for X ~ N(mu, sigma), from scipy's
+    normal distribution: the positive interval [a, 2a) plus the negative one
+    (-2a, -a], each as a difference of upper tails (or of lower tails when
+    the interval lies below the mean), which keeps the difference accurate."""
+    from scipy.stats import norm
+    a = 2.0 ** (f - 127)
+
+    def interval(lo, hi):  # P(lo <= X < hi)
+        if lo >= mu:
+            return norm.sf(lo, mu, sigma) - norm.sf(hi, mu, sigma)
+        if hi <= mu:
+            return norm.cdf(hi, mu, sigma) - norm.cdf(lo, mu, sigma)
+        return 1.0 - norm.cdf(lo, mu, sigma) - norm.sf(hi, mu, sigma)
+    return interval(a, 2 * a) + interval(-2 * a, -a)
+
+
+@pytest.mark.parametrize("mu,sigma", [(0.0, 0.02), (0.013, 0.013), (-0.05, 0.02), (3.0, 1.0),
+                                      (-7.5e-4, 1e-3), (1e5, 2e3), (-0.2, 0.9)])
+def test_mass_matches_scipy_normal(mu, sigma):
+    """Every field mass for a nonzero mean against scipy: a wrong sign of mu in
+    either the positive or the negative interval, or a swapped edge, moves the
+    masses by far more than the tolerance."""
+    checked = 0
+    for f in range(1, 255):
+        want = _norm_mass(mu, sigma, f)
+        got = O.zc_mass(mu, sigma, f)
+        if want < 1e-250:
+            assert got < 1e-15  # rounding noise of CDF differences at most
+            continue
+        # absolute 1e-15: both sides take differences of normal CDF values
+        # near 1/2 for bins far inside the bulk, each rounded to ~1e-16
+        assert got == pytest.approx(want, rel=2e-9, abs=1e-15), (f, got, want)
+        checked += want > 1e-6
+    assert checked >= 1
+
+
+@pytest.mark.parametrize("mu,sigma", [(0.013, 0.013), (-0.05, 0.02), (3.0, 1.0), (-0.2, 0.9),
+                                      (0.02, 0.004), (-1e-3, 0.02)])
+def test_nonzero_mean_book_is_top7_of_scipy_masses(mu, sigma):
+    m = np.array([_norm_mass(mu, sigma, f) for f in range(1, 255)])
+    order = np.argsort(-m, kind="stable")  # ties toward the smaller field
+    gap = (m[order[6]] - m[order[7]]) / m[order[6]]
+    assert gap > 1e-6, "case chosen away from a tie"
+    want = np.sort(order[:7] + 1).astype(np.uint8)
+    assert np.array_equal(O.zc_predict(mu, sigma), want)

@@ -27,8 +27,9 @@
 // are accumulated as unevaluated fp32 pairs (error-free two-sum), the pairs
 // of a unit's lanes are added as pairs too, and only the unit's total is
 // formed in fp64 (an fp64 tree when a pair overflows fp32).  A
-// group of 16 whose fp32 sums are not finite (an
-// inf/NaN input or an fp32 overflow) is redone element by element in fp64,
+// group of 16 whose fp32 sums are not finite (an inf/NaN input or an fp32
+// overflow), or whose squares may have underflowed (sum of squares below
+// 2^-96 with a nonzero value), is redone element by element in fp64,
 // skipping non-finite values.  The whole pass is deterministic for a given
 // plan: the partition into units and every reduction order are fixed.
 #include <cuda_runtime.h>
@@ -231,12 +232,24 @@ __global__ void __launch_bounds__(kThreads, 2) zc_stats_kernel(
           q[j] = __fadd_rn(q[j], q[j + st]);
         }
       }
-      if (isfinite(v[0]) && isfinite(q[0])) {
+      // Squares below 2^-126 lose bits in fp32 (below 2^-149 they vanish):
+      // when the group's sum of squares is under 2^-96 and a value is not
+      // zero, the loss could exceed the fp32 rounding bound, so the group
+      // goes to fp64 like a non-finite one.
+      bool fast = isfinite(v[0]) && isfinite(q[0]);
+      if (fast && q[0] < 0x1p-96f) {
+        uint32_t nz = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) nz |= w[g][j] & 0x7FFF7FFFu;
+        fast = nz == 0;
+      }
+      if (fast) {
         two_sum_acc(hx, lx, v[0]);
         two_sum_acc(hq, lq, q[0]);
         cnt += (unsigned long long)valid;
       } else {
-        // an inf/NaN input or an fp32 overflow: redo these values in fp64
+        // an inf/NaN input, an fp32 overflow or underflow: redo these values
+        // in fp64
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const uint32_t bits = (j & 1) ? (w[g][j >> 1] >> 16) : (w[g][j >> 1] & 0xFFFFu);

@@ -3,9 +3,9 @@
 The CUDA path runs through the C ABI on seeded inputs; the metadata blob, the
 compressed stream and the decoded bytes are compared byte for byte with the
 oracle on the same input bytes.  At full size (the 512 MB table, the sweep's
-largest points) the oracle checks sampled groups and the rest is checked by
-properties that hold at any size (exact decode, group offsets = prefix of the
-group lengths implied by the participation bits).
+points up to 4 GiB) the whole stream is compared too: the oracle encodes the
+input in pieces of whole groups, one oracle call per piece on all host cores,
+and every byte of the GPU stream is checked against them (oracle_split.py).
 """
 import numpy as np
 import pytest
@@ -13,6 +13,7 @@ import torch
 
 import oracle as O
 from lossless_bit_level_bf16_gb300 import abi, ibp as I, workloads as W
+from oracle_split import ibp_stream_equal
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -81,44 +82,28 @@ def test_random_masks(cb, frac):
         assert np.array_equal(y.cpu().numpy(), xs)
 
 
-def test_table_full_size_sampled():
-    """The 1,000,000 x 128 fp32 table (512 MB), metadata from 10,000 rows."""
+@pytest.mark.parametrize("mode", [0, 1])
+def test_table_full_size(mode):
+    """The 1,000,000 x 128 fp32 table (512 MB): metadata from its own 10,000
+    seeded sample rows equal to the oracle's, the whole stream equal to the
+    oracle's, exact decode."""
     rows, idx = W.ibp_table(device=DEV)
     samples = rows[idx].contiguous()
+    assert samples.shape[0] == 10_000
     cb = 512
-    for mode in (0, 1):
-        ws = _ws(cb, 0, samples.shape[0])
-        meta = I.build_meta(samples, cb, T=0.9, mode=mode, ws=ws)
-        st, y = _gpu_roundtrip(meta, rows, cb)
-        assert torch.equal(y.view(torch.int32), rows.view(-1).view(torch.int32))
-        del y
-        mh = _u8(meta)
-        m = int(mh[16:20].view(np.uint32)[0])
-        mask = torch.from_numpy(mh[64:64 + cb].view(np.int32).copy()).to(DEV)
-        bitv = torch.from_numpy(mh[64 + cb:64 + 2 * cb].view(np.int32).copy()).to(DEV)
-        xi = rows.view(torch.int32)
-        p = (((xi ^ bitv) & mask) == 0).all(dim=1) & (m > 0)
-        nch = rows.shape[0]
-        ng = (nch + 31) // 32
-        lens = torch.where(p, cb * 8 - m, cb * 8).to(torch.int64)
-        pad = torch.zeros(ng * 32, dtype=torch.int64, device=DEV)
-        pad[:nch] = lens
-        gbits = pad.view(ng, 32).sum(1) + 32
-        gbits = (gbits + 127) // 128 * 128
-        st_h = st.cpu().numpy()
-        grp = st_h[128:128 + 8 * (ng + 1)].view(np.uint64)
-        want = np.zeros(ng + 1, np.uint64)
-        want[1:] = np.cumsum(gbits.cpu().numpy())
-        assert np.array_equal(grp, want)
-        off_pay = int(st_h[56:64].view(np.uint64)[0])
-        x_h = _u8(rows)
-        rng = np.random.default_rng(mode)
-        for g in list(rng.integers(0, ng, 16)) + [0, ng - 1]:
-            n_in = min(32, nch - 32 * g)
-            gb = O.ibp_encode_group(mh, x_h[32 * g * cb:(32 * g + n_in) * cb], n_in)
-            assert np.array_equal(st_h[off_pay + int(grp[g]) // 8: off_pay + int(grp[g + 1]) // 8], gb), g
-        ratio = rows.numel() * 4 / st.numel()
-        print(f"mode {mode}: m={m} participation={p.float().mean().item():.4f} ratio={ratio:.4f}")
+    ws = _ws(cb, 0, samples.shape[0])
+    meta = I.build_meta(samples, cb, T=0.9, mode=mode, ws=ws)
+    torch.cuda.synchronize()
+    assert I.status(ws) == 0
+    mh = _u8(meta)
+    mref = O.ibp_build_meta(_u8(samples), cb, T=0.9, mode=mode)
+    assert np.array_equal(mh, mref), np.nonzero(mh != mref)[0][:10]
+    st, y = _gpu_roundtrip(meta, rows, cb)
+    assert torch.equal(y.view(torch.int32), rows.view(-1).view(torch.int32))
+    del y
+    ibp_stream_equal(st.cpu().numpy(), mref, _u8(rows))
+    m = int(mh[16:20].view(np.uint32)[0])
+    print(f"mode {mode}: m={m} ratio={rows.numel() * 4 / st.numel():.4f}")
 
 
 @pytest.mark.parametrize("mb", [1, 4, 16])
@@ -140,27 +125,54 @@ def test_sweep_full(mb):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("mb", [64, 256, 1024, 4096])
-def test_sweep_sampled(mb):
+def test_sweep_full_large(mb, mode):
+    """The sweep's fp32 N(0, 0.02) weights at 64 MiB .. 4 GiB, 2048-byte
+    chunks, metadata from 10,000 seeded sample chunks: metadata and the whole
+    stream equal to the oracle's, exact decode."""
     cb = 2048
     x = W.ibp_gaussian(mb * (1 << 20) // 4, std=0.02, seed=0, device=DEV)
     nch = x.numel() * 4 // cb
     idx = W.sample_rows(nch, 10_000, seed=1, device=DEV)
     samples = x.view(nch, cb // 4)[idx].contiguous()
-    meta = I.build_meta(samples, cb, T=0.9, mode=0, ws=_ws(cb, 0, samples.shape[0]))
+    meta = I.build_meta(samples, cb, T=0.9, mode=mode, ws=_ws(cb, 0, samples.shape[0]))
+    mref = O.ibp_build_meta(_u8(samples), cb, T=0.9, mode=mode)
+    assert np.array_equal(_u8(meta), mref)
+    del samples
     st, y = _gpu_roundtrip(meta, x, cb)
     assert torch.equal(y.view(torch.int32), x.view(torch.int32))
     del y
-    mh = _u8(meta)
-    ng = (nch + 31) // 32
-    grp = st[128:128 + 8 * (ng + 1)].view(torch.int64).cpu().numpy()
-    off_pay = int(st[56:64].cpu().numpy().view(np.uint64)[0])
-    rng = np.random.default_rng(mb)
-    for g in list(rng.integers(0, ng, 8)) + [0, ng - 1]:
-        n_in = min(32, nch - 32 * g)
-        xg = x.view(torch.uint8)[32 * g * cb:(32 * g + n_in) * cb].cpu().numpy()
-        gb = O.ibp_encode_group(mh, xg, n_in)
-        assert np.array_equal(st[off_pay + grp[g] // 8: off_pay + grp[g + 1] // 8].cpu().numpy(), gb)
+    st_h = st.cpu().numpy()
+    del st
+    ibp_stream_equal(st_h, mref, _u8(x))
+
+
+@pytest.mark.parametrize("cb", [4, 20, 52, 300, 2060, 4092])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_chunk_sizes_not_multiple_of_16(cb, mode):
+    """Chunk sizes that are multiples of 4 bytes but not of 16 (the format
+    allows any multiple of 4): metadata from seeded sample chunks, the whole
+    stream with a ragged last chunk, and the decode, against the oracle."""
+    if mode == 1 and cb > 2048:
+        pytest.skip("the joint reading is built for chunks of up to 2048 bytes")
+    nch = 32 * 7 + 9
+    x = W.ibp_gaussian(nch * cb // 4 - 1, std=0.02, seed=cb, device=DEV)  # ragged last chunk
+    full = x.numel() * 4 // cb
+    idx = W.sample_rows(full, 150, seed=2, device=DEV)
+    samples = x[: full * (cb // 4)].view(full, cb // 4)[idx].contiguous()
+    ws = _ws(cb, 0, samples.shape[0])
+    meta = I.build_meta(samples, cb, T=0.9, mode=mode, ws=ws)
+    torch.cuda.synchronize()
+    assert I.status(ws) == 0
+    mref = O.ibp_build_meta(_u8(samples), cb, T=0.9, mode=mode)
+    assert np.array_equal(_u8(meta), mref)
+    st, y = _gpu_roundtrip(meta, x, cb)
+    ref = O.ibp_encode(mref, _u8(x))
+    assert np.array_equal(st.cpu().numpy(), ref)
+    assert torch.equal(y.view(torch.int32), x.view(torch.int32))
+    # chunks participate: smaller than the stream with every chunk raw
+    assert ref.size < O.lib().ora_ibp_stream_bytes_bound(cb, x.numel() * 4)
 
 
 def test_errors_reported():
@@ -213,8 +225,9 @@ def test_errors_reported():
 @pytest.mark.parametrize("cb", [512, 2048])
 def test_host_resident_input_and_streams(cb):
     """Pinned host tensors as encode input, encode output, decode input and
-    decode output (read and written in place by the kernels) give the same
-    bytes as the all-device path; pageable host memory is refused."""
+    decode output (read and written in place by the kernels) give the
+    oracle's stream and the exact input back; pageable host memory is
+    refused."""
     import ctypes as C
 
     rows = 3000 if cb == 512 else 1500
@@ -226,6 +239,8 @@ def test_host_resident_input_and_streams(cb):
     torch.cuda.synchronize()
     total = int(nb.item())
     ref = ref[:total].clone()
+    # the stream every placement must give is the oracle's
+    assert np.array_equal(ref.cpu().numpy(), O.ibp_encode(_u8(meta), _u8(x)))
     # host input
     xh = x.cpu().pin_memory()
     st, nb2 = I.compress(meta, xh, cb)

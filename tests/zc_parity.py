@@ -18,15 +18,27 @@ def finite_values(u16):
     return (u16[fin].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def check_plan(x_bits, seg_off, books_gpu, mu_gpu, sig_gpu):
+def _sum_abs(u16, step=1 << 24):
+    """Sum of |x| over the finite values, in pieces (large inputs)."""
+    tot = 0.0
+    for i in range(0, len(u16), step):
+        tot += float(np.abs(finite_values(u16[i:i + step])).sum())
+    return tot
+
+
+def check_plan(x_bits, seg_off, books_gpu, mu_gpu, sig_gpu, allow_near_ties=False):
     """Codebook parity for a plan computed on the GPU.
 
     The GPU sums each thread's 16 values as an fp32 tree (error at most 4 ulp
     of the sum of magnitudes) before accumulating exactly, so its mean and
     sigma may differ from the oracle's fp64 sums by that much.  Given the
     GPU's own (mu, sigma), the oracle's predictor must give the GPU's book
-    exactly; the oracle's book from its own statistics must agree too unless
-    the decision is a near-tie inside that error band (counted and returned).
+    exactly.  The oracle's book from its own statistics must agree too.  Only
+    where the caller builds near-ties on purpose (allow_near_ties) may it
+    differ, and then only inside the band those statistics' error allows:
+    every field that one book has and the other lacks must carry, at the
+    oracle's (mu, sigma), a mass within 1e-5 (relative) of the masses the
+    other book has in its place.  Returns the number of such segments.
     """
     nseg = len(books_gpu)
     seg = [0, len(x_bits)] if seg_off is None else list(seg_off)
@@ -36,18 +48,28 @@ def check_plan(x_bits, seg_off, books_gpu, mu_gpu, sig_gpu):
         cnt, s1, s2 = O.zc_stats(xs)
         mu_o, sg_o = O.zc_moments(cnt, s1, s2)
         if cnt:
-            v = finite_values(xs)
-            mean_abs = float(np.abs(v).mean())
+            mean_abs = _sum_abs(xs) / cnt
             ex2 = s2 / cnt
         else:
             mean_abs = ex2 = 0.0
         tol_mu = 8 * U * mean_abs + 1e-300
         assert abs(mu_gpu[s] - mu_o) <= tol_mu, (s, mu_gpu[s], mu_o)
-        tol_var = 8 * U * ex2 + 2 * abs(mu_o) * tol_mu + 2.0 ** -126
+        # groups whose squares could underflow fp32 are summed in fp64 on the
+        # GPU, so the only absolute term left is the fp32 subnormal spacing of
+        # the squares of a group kept in fp32 (2^-150 each)
+        tol_var = 8 * U * ex2 + 2 * abs(mu_o) * tol_mu + 2.0 ** -140
         assert abs(sig_gpu[s] ** 2 - sg_o ** 2) <= tol_var, (s, sig_gpu[s], sg_o)
         b_from_gpu_stats = O.zc_predict(float(mu_gpu[s]), float(sig_gpu[s]))
         assert np.array_equal(b_from_gpu_stats, books_gpu[s]), (s, b_from_gpu_stats, books_gpu[s])
-        if not np.array_equal(O.zc_predict(mu_o, sg_o), books_gpu[s]):
+        b_own = O.zc_predict(mu_o, sg_o)
+        if not np.array_equal(b_own, books_gpu[s]):
+            assert allow_near_ties, (s, b_own, books_gpu[s], mu_o, sg_o)
+            only_gpu = sorted(set(int(f) for f in books_gpu[s]) - set(int(f) for f in b_own))
+            only_own = sorted(set(int(f) for f in b_own) - set(int(f) for f in books_gpu[s]))
+            for a in only_gpu:
+                for b in only_own:
+                    ma, mb = O.zc_mass(mu_o, sg_o, a), O.zc_mass(mu_o, sg_o, b)
+                    assert abs(ma - mb) <= 1e-5 * max(ma, mb), (s, a, b, ma, mb)
             near_ties += 1
     return near_ties
 

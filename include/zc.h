@@ -78,6 +78,21 @@ const char* zc_strerror(int code);
 /* Library version as an integer (major*10000 + minor*100 + patch). */
 int zc_version(void);
 
+/* TEST ONLY -- for checking that the encoders' bounded waits end; the pages
+ * have no counterpart.  Every later zc_compress / ibp_compress call of this
+ * process (until switched off) leaves out the scan state of tile `tile` --
+ * the tile whose stream length or escape count the later tiles wait for: an
+ * 8192-slot ticket of the ZipCCL encoder, a tile of the IBP encoder (16 KB
+ * of input up to 512-byte chunks, 4096 groups of the offsets pass up to
+ * 2048-byte chunks, one group above) -- and limits every wait between thread
+ * blocks to `max_spins` polls (0: the normal limit, about one second).  The
+ * waits behind the missing state run out, the call sets ZC_ERR_TIMEOUT in
+ * its status word and returns with a stream that must not be used; nothing
+ * faults or hangs.  tile = UINT64_MAX with max_spins = 0 switches it off
+ * (the default).  Process-wide; not for use while other threads compress.
+ * Returns ZC_OK. */
+int zc_test_wait_fault(uint64_t tile, uint32_t max_spins);
+
 /* Read the status word of a workspace: synchronises the stream, copies the
  * word to *h_status (ZC_OK or a negative code).  Returns ZC_OK or ZC_ERR_CUDA. */
 int zc_status(const void* d_ws, zc_stream_t stream, int* h_status);
@@ -152,8 +167,10 @@ int zc_compress(zc_plan_t plan, const uint16_t* d_x, void* d_out,
  * (ZC_OK or a ZC_ERR_* code) once the kernel is done.  Enqueues one memset,
  * the encode kernel and a 4-byte device copy on `stream`.
  *
- * The first call on each device looks up the array's address (with that
- * device current); make it before any stream capture.  All calls on a device
+ * Each call made outside a stream capture looks up the array's address on
+ * the current device (a device reset reloads the library and may move it); a
+ * call during a capture uses the address the last such call found, so make
+ * one call on the device before any stream capture.  All calls on a device
  * share the one array: calls whose GPU work overlaps (other streams, other
  * threads) race and corrupt each other's streams, so order them on one
  * stream or with events. */
@@ -175,8 +192,10 @@ int zc_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_y,
 
 /* ======================================================== IBP
  *
- * Chunks are chunk_bytes long (multiple of 16, 16..4096); the last chunk of
- * an input may be shorter (a multiple of 4 bytes) and is stored raw.
+ * Chunks are chunk_bytes long (any multiple of 4, 4..4096: multiples of 16
+ * up to 2048 run on the TMA-pipelined kernels, the rest on word-granular
+ * ones); the last chunk of an input may be shorter (a multiple of 4 bytes)
+ * and is stored raw.
  */
 
 /* Size of an IBPM metadata blob: 64 + 2*chunk_bytes. */

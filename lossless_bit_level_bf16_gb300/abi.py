@@ -28,6 +28,7 @@ _vp, _u8p, _u64p, _dp = C.c_void_p, C.POINTER(C.c_uint8), C.POINTER(C.c_uint64),
 SIGNATURES = {
     "zc_strerror": (C.c_char_p, [C.c_int]),
     "zc_version": (C.c_int, []),
+    "zc_test_wait_fault": (C.c_int, [C.c_uint64, C.c_uint32]),
     "zc_status": (C.c_int, [_vp, _vp, C.POINTER(C.c_int)]),
     "zc_plan_create": (C.c_int, [C.c_uint64, _u64p, C.c_uint32, C.c_uint32, C.POINTER(_vp)]),
     "zc_plan_destroy": (None, [_vp]),

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <cstddef>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -41,6 +43,24 @@ int resident_blocks(const void* kernel, int threads, size_t smem) {
   std::lock_guard<std::mutex> g(mu);
   cache.push_back(Entry{kernel, dev, threads, smem, blocks});
   return blocks;
+}
+
+namespace {
+std::atomic<unsigned long long> g_fault_tile1{0};
+std::atomic<unsigned> g_fault_spins{0};
+}  // namespace
+
+cudaError_t arm_wait_fault(void* d_ws, cudaStream_t s) {
+  const unsigned long long f = g_fault_tile1.load();
+  const unsigned sp = g_fault_spins.load();
+  if (!f && !sp) return cudaSuccess;
+  struct {
+    unsigned long long fault_tile1;
+    unsigned max_spins, pad1;
+  } v{f, sp, 0};
+  static_assert(sizeof(v) == 16, "two fields of Ctrl");
+  return cudaMemcpyAsync(static_cast<char*>(d_ws) + offsetof(Ctrl, fault_tile1), &v, sizeof(v),
+                         cudaMemcpyHostToDevice, s);
 }
 
 }  // namespace lbb
@@ -99,6 +119,12 @@ const char* zc_strerror(int code) {
 
 int zc_version(void) { return 100; }
 
+int zc_test_wait_fault(uint64_t tile, uint32_t max_spins) {
+  lbb::g_fault_tile1.store(tile == UINT64_MAX ? 0ull : tile + 1);
+  lbb::g_fault_spins.store(max_spins);
+  return ZC_OK;
+}
+
 int zc_status(const void* d_ws, zc_stream_t stream, int* h_status) {
   if (!d_ws || !h_status) return ZC_ERR_ARG;
   int v = 0;
@@ -118,7 +144,6 @@ int zc_plan_create(uint64_t n, const uint64_t* h_seg_off, uint32_t nseg, uint32_
   *out_plan = nullptr;
   if (nseg == 0 || (!h_seg_off && nseg != 1)) return ZC_ERR_ARG;
   if (C < 1024u || C > 65536u || (C % 1024u) != 0) return ZC_ERR_ARG;
-  if ((C & (C - 1)) != 0) return ZC_ERR_UNSUPPORTED;  // GPU tiles need a power of two
   if (n > (1ull << 46)) return ZC_ERR_ARG;
   if (h_seg_off) {
     if (h_seg_off[0] != 0 || h_seg_off[nseg] != n) return ZC_ERR_ARG;
@@ -270,7 +295,9 @@ uint64_t ibp_meta_bytes(uint32_t chunk_bytes) {
   return lbb::kIbpmHeader + 2ull * chunk_bytes;
 }
 
-static bool ibp_chunk_ok(uint32_t cb) { return cb >= 16 && cb <= 4096 && (cb % 16) == 0; }
+// Any multiple of 4 bytes up to 4096: multiples of 16 up to 2048 take the
+// TMA-pipelined kernels, the others the word-granular ones.
+static bool ibp_chunk_ok(uint32_t cb) { return cb >= 4 && cb <= 4096 && (cb % 4) == 0; }
 
 size_t ibp_workspace_bytes(uint32_t cb, uint64_t n_bytes, uint64_t n_samples) {
   if (!ibp_chunk_ok(cb)) return 0;

@@ -26,7 +26,13 @@ struct Ctrl {
   int pad0;
   unsigned long long ticket;  // dynamic tile counter (ordered tile start)
   unsigned long long done;    // blocks finished (last one finalises)
-  unsigned long long spare[29];
+  // Wait-failure test switch (zero, i.e. off, unless zc_test_wait_fault armed
+  // it for the call): tile + 1 of the tile whose scan state is never
+  // published, and the number of polls each inter-block wait may take.
+  unsigned long long fault_tile1;
+  unsigned max_spins;
+  unsigned pad1;
+  unsigned long long spare[27];
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 constexpr size_t kCtrlBytes = 256;
@@ -205,6 +211,16 @@ constexpr unsigned long long kFlagInc = 2ull << 62;
 constexpr unsigned long long kValMask = (1ull << 62) - 1;
 constexpr unsigned kMaxSpins = 1u << 22;  // ~1 s with the back-off below
 
+// The poll limit of this call's inter-block waits, and whether `tile` may
+// publish its scan state (both read from the control block: see Ctrl).
+__device__ __forceinline__ unsigned wait_limit(const Ctrl* c) {
+  const unsigned v = c->max_spins;
+  return v ? v : kMaxSpins;
+}
+__device__ __forceinline__ bool may_publish(const Ctrl* c, unsigned long long tile) {
+  return c->fault_tile1 != tile + 1;
+}
+
 // Look-back with an adaptive window (states are published with relaxed
 // stores: they carry counts only, nothing else is read through them): the nearest 32 predecessors are read
 // first (one state per lane; usually one of them already holds an inclusive
@@ -253,16 +269,18 @@ __device__ __forceinline__ int lb_window(const unsigned long long* states, long 
 // D0 * 32 predecessors are read in the first round trip and D1 * 32 in each
 // further one; after FREE spins on a predecessor that has not published, the
 // warp sleeps between re-reads (doubling up to 512 ns) to spare L2 bandwidth.
+// `limit` bounds the polls of a predecessor that has not published; a tile
+// with `publish` false publishes nothing (the wait-failure test).
 template <int D0 = 1, int D1 = kLbDepth, unsigned FREE = 64>
 __device__ __forceinline__ unsigned long long lookback_warp_wide(
     unsigned long long* states, unsigned long long tile, unsigned long long aggregate,
-    bool* timed_out) {
+    bool* timed_out, unsigned limit = kMaxSpins, bool publish = true) {
   const int lane = threadIdx.x & (kWarp - 1);
   if (tile == 0) {
-    if (lane == 0) st_relaxed_u64(states, kFlagInc | aggregate);
+    if (lane == 0 && publish) st_relaxed_u64(states, kFlagInc | aggregate);
     return 0;
   }
-  if (lane == 0) st_relaxed_u64(states + tile, kFlagAgg | aggregate);
+  if (lane == 0 && publish) st_relaxed_u64(states + tile, kFlagAgg | aggregate);
   unsigned long long excl = 0;
   long long end = (long long)tile - 1;
   unsigned spins = 0, ns = 32;
@@ -271,7 +289,7 @@ __device__ __forceinline__ unsigned long long lookback_warp_wide(
     unsigned long long sum = 0;
     const int r = deep ? lb_window<D1>(states, end, &sum) : lb_window<D0>(states, end, &sum);
     if (r == kLbEmpty) {
-      if (++spins > kMaxSpins) {
+      if (++spins > limit) {
         to = true;
         break;
       }
@@ -288,10 +306,10 @@ __device__ __forceinline__ unsigned long long lookback_warp_wide(
   }
   if (to) {
     *timed_out = true;
-    if (lane == 0) st_relaxed_u64(states + tile, kFlagInc | aggregate);
+    if (lane == 0 && publish) st_relaxed_u64(states + tile, kFlagInc | aggregate);
     return 0;
   }
-  if (lane == 0) st_relaxed_u64(states + tile, kFlagInc | ((excl + aggregate) & kValMask));
+  if (lane == 0 && publish) st_relaxed_u64(states + tile, kFlagInc | ((excl + aggregate) & kValMask));
   return excl;
 }
 
@@ -387,7 +405,8 @@ template <int D>
 __device__ __forceinline__ unsigned long long lb2_lookback(const unsigned long long* states,
                                                            const unsigned long long* bwords,
                                                            unsigned long long t,
-                                                           bool* timed_out) {
+                                                           bool* timed_out,
+                                                           unsigned limit = kMaxSpins) {
   static_assert(32 * D >= (int)kLbBlock, "a window covers a block's tickets");
   if (t == 0) return 0;
   unsigned long long excl = 0, sum = 0;
@@ -400,7 +419,7 @@ __device__ __forceinline__ unsigned long long lb2_lookback(const unsigned long l
     int r;
     while ((r = lb2_window<D, false>(states, tend, blk * (long long)kLbBlock, &sum, &at)) ==
            kLbEmpty) {
-      if (++spins > kMaxSpins) {
+      if (++spins > limit) {
         *timed_out = true;
         return excl;
       }

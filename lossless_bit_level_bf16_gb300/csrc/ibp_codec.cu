@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_encode_kernel(IbpEncArgs 
     if (c0 + nch == A.nchunks && tail_bytes != cb) bits -= 8ull * (cb - tail_bytes);
     const unsigned long long padded = round_up_dev(bits, 128);
     // publish the aggregate now; the look-back below resolves it later
-    if (t == 0 && g > 0) st_relaxed_u64(A.states + g, kFlagAgg | padded);
+    if (t == 0 && g > 0 && may_publish(A.ctrl, g)) st_relaxed_u64(A.states + g, kFlagAgg | padded);
     if (t == 0) gbuf[0] = pword;  // the image is all zeros here (cleared at copy-out)
 
     // ---- phase 2: close up kept bits into the group image
@@ -183,7 +183,8 @@ __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_encode_kernel(IbpEncArgs 
     // ---- look-back for the group's bit offset
     if (warp == 0) {
       bool to = false;
-      const unsigned long long e = lookback_warp_wide(A.states, g, padded, &to);
+      const unsigned long long e = lookback_warp_wide(A.states, g, padded, &to, wait_limit(A.ctrl),
+                                                      may_publish(A.ctrl, g));
       if (lane == 0) {
         s_excl = e;
         if (to) set_status(A.ctrl, ZC_ERR_TIMEOUT);
@@ -445,6 +446,8 @@ cudaError_t ibp_launch_compress(const void* d_meta, uint32_t cb, const void* d_x
   A.ctrl = static_cast<Ctrl*>(d_ws);
   A.states = reinterpret_cast<unsigned long long*>(static_cast<char*>(d_ws) + kCtrlBytes);
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 8ull * A.ngroups, s);
+  if (e != cudaSuccess) return e;
+  e = arm_wait_fault(d_ws, s);
   if (e != cudaSuccess) return e;
   if (!x_host && ibp_pipe_supported(cb, true))
     return ibp_pipe_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap, d_out_bytes, d_ws, s);

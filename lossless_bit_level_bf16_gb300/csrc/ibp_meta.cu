@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(256) ibp_columns_kernel(
     const unsigned long long sb = sbq * kBlocksPerWarp + bi;
     const unsigned long long s = sb * 32ull + lane;
     const bool have = sb < Wn && s < N;
-    if (have && nw == kWordsPerWarp) {  // 16-byte aligned: W and w0 are multiples of 4
+    if (have && nw == kWordsPerWarp && (W & 3u) == 0) {  // 16-byte aligned: W and w0 multiples of 4
       const uint4 a = ld_nc_v4(samples + s * W + w0), b = ld_nc_v4(samples + s * W + w0 + 4);
       v[bi][0] = a.x; v[bi][1] = a.y; v[bi][2] = a.z; v[bi][3] = a.w;
       v[bi][4] = b.x; v[bi][5] = b.y; v[bi][6] = b.z; v[bi][7] = b.w;

@@ -463,7 +463,8 @@ __global__ void __launch_bounds__(kOffNT) ibp_offsets_kernel(OffArgs A) {
   const uint32_t excl_local = block_excl_scan<kOffNT>(local, s_wt, &total);
   if (warp == 0) {
     bool to = false;
-    const unsigned long long ex = lookback_warp_wide(A.states, tile, total, &to);
+    const unsigned long long ex = lookback_warp_wide(A.states, tile, total, &to, wait_limit(A.ctrl),
+                                                     may_publish(A.ctrl, tile));
     if (t == 0) {
       s_excl = ex;
       if (to) set_status(A.ctrl, ZC_ERR_TIMEOUT);
@@ -521,8 +522,11 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
   // the tile's input into stage s.
   uint32_t pf_pw = 0;
   unsigned long long pf_go = 0, pf_gend = 0;
+  bool run = ok;  // false: nothing to pack (bad metadata, or the call failed before)
+  // the largest legal stream of a group (every chunk raw), in bits
+  const unsigned long long max_group_bits = (32ull + 32ull * B + 127ull) / 128ull * 128ull;
   auto prefetch = [&](unsigned long long kk) {
-    const unsigned long long tile = ok ? blockIdx.x + kk * gridDim.x : A.ntiles;
+    const unsigned long long tile = run ? blockIdx.x + kk * gridDim.x : A.ntiles;
     if (tile >= A.ntiles) return;
     const unsigned long long g0 = tile * Q;
     const uint32_t nq = (uint32_t)((A.ngroups - g0) < Q ? (A.ngroups - g0) : Q);
@@ -531,7 +535,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
     pf_gend = grp[g0 + nq];
   };
   auto issue = [&](unsigned long long kk, uint32_t s) {
-    const unsigned long long tile = ok ? blockIdx.x + kk * gridDim.x : A.ntiles;
+    const unsigned long long tile = run ? blockIdx.x + kk * gridDim.x : A.ntiles;
     if (lane == 0) s_tile[s] = tile;
     if (tile >= A.ntiles) return;
     const unsigned long long g0 = tile * Q;
@@ -540,14 +544,22 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
     const unsigned long long go = pf_go;
     const unsigned long long base = __shfl_sync(kFull, go, 0);
     const bool raw = __ballot_sync(kFull, pw != 0) == 0;
+    // The offsets come from the scan pass through global memory: a tile whose
+    // span could not be its stream (offsets out of order, or longer than its
+    // groups stored raw) is not packed -- its sizes would index the image out
+    // of bounds -- and the call reports the inconsistency.
+    const unsigned long long span = pf_gend - base;
+    const bool bad = __any_sync(kFull, pf_gend < base || span > nq * max_group_bits ||
+                                           ((uint32_t)lane < nq && (go < base || go - base > span)));
     if ((uint32_t)lane < nq) {
       s_pw[s][lane] = pw;
-      s_gex[s][lane] = (uint32_t)(go - base);
+      s_gex[s][lane] = bad ? 0u : (uint32_t)(go - base);
     }
     if (lane == 0) {
-      s_base[s] = base;
-      s_agg[s] = (uint32_t)(pf_gend - base);
-      s_raw[s] = raw;
+      if (bad) set_status(A.ctrl, ZC_ERR_FORMAT);
+      s_base[s] = bad ? 0ull : base;
+      s_agg[s] = bad ? 0u : (uint32_t)span;  // nothing to write for a bad tile
+      s_raw[s] = bad ? 1 : raw;
       const unsigned long long b0 = tile * tile_raw;
       const unsigned long long tb = (A.n_bytes - b0) < tile_raw ? (A.n_bytes - b0) : tile_raw;
       const uint32_t b16 = (uint32_t)(tb & ~15ull);
@@ -564,6 +576,11 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
   if (t == 0)
     for (uint32_t s = 0; s < S; ++s) mbar_init(bars + s, 1);
   grid_dep_wait();  // the participation words and the group-offset table
+  // a call whose match or scan pass failed (a wait that ran out) packs
+  // nothing: its offsets cannot be trusted (one read, the same for the block)
+  if (t == 0) s_last = ok && get_status(A.ctrl) == 0;
+  __syncthreads();
+  run = s_last != 0;
   __syncthreads();
   if (warp == 0)
     for (uint32_t s = 0; s < S; ++s) {
@@ -839,6 +856,8 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
       prefetch_l2(1);
       if (mine) stage_in(bid, mstage, b_mfull);
     }
+    const unsigned lim = wait_limit(A.ctrl);
+    const unsigned long long fault1 = A.ctrl->fault_tile1;  // 0 unless a wait-failure test
     unsigned long long wave_base = 0;  // 128-bit units of the waves resolved so far
     for (uint32_t i = 0; i < mine + kWsLag; ++i) {
       if (i < mine) {
@@ -927,7 +946,7 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
         }
         s_cpw[i % (kWsLag + 1)][lane] = pw;
         units = __reduce_add_sync(kFull, units);
-        if (lane == 0) st_relaxed_u32(A.lens + tile, 0x80000000u | units);
+        if (lane == 0 && tile + 1 != fault1) st_relaxed_u32(A.lens + tile, 0x80000000u | units);
       }
       if (i + 1 == kWsLag) lens_fetch(0);
       if (i >= kWsLag) {
@@ -959,11 +978,13 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
             }
           }
           if (__all_sync(kFull, all)) break;
-          if (spins >= kMaxSpins) {
+          if (spins >= lim) {
             if (lane == 0) set_status(A.ctrl, ZC_ERR_TIMEOUT);
             break;
           }
-          if (get_status(A.ctrl) != 0) break;  // the call has failed: no more waiting
+          // the call has failed: no more waiting (one vote, so that the
+          // whole warp leaves the loop together)
+          if (__any_sync(kFull, get_status(A.ctrl) != 0)) break;
           __nanosleep(spins < 64 ? 32 : 256);
           for (uint32_t vi = lane; vi < nv4; vi += 32) lb[vi] = ld_relaxed_v4(A.lens + la0 + 4ull * vi);
           __syncwarp();
@@ -1612,6 +1633,8 @@ cudaError_t ibp_ws_compress(const void* d_meta, uint32_t cb, const void* d_x,
   // workspace: control block | one length word per tile (+ one vector of slack)
   e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 4ull * A.ntiles + 16, s);
   if (e != cudaSuccess) return e;
+  e = arm_wait_fault(d_ws, s);
+  if (e != cudaSuccess) return e;
   k<<<(unsigned)grid, kWsThreads, smem, s>>>(A);
   return cudaGetLastError();
 }
@@ -1633,6 +1656,8 @@ cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t cb, const void* d_x,
   unsigned long long* states = reinterpret_cast<unsigned long long*>(ws + kCtrlBytes);
   uint32_t* pw = reinterpret_cast<uint32_t*>(ws + kCtrlBytes + round_up(8ull * ntiles2, 256));
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 8ull * ntiles2, s);
+  if (e != cudaSuccess) return e;
+  e = arm_wait_fault(d_ws, s);
   if (e != cudaSuccess) return e;
   unsigned long long* grp =
       reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(d_out) + kIbp1Header);

@@ -20,6 +20,14 @@ constexpr uint32_t kZcAlign = 128;
 constexpr uint32_t kTileLanes = 8192;   // lanes (element slots) per encoder tile
 constexpr unsigned long long kZcLbBlock = 128;  // tiles per look-back block
 
+// Chunks of C slots (a multiple of 1024) that one encoder tile of kTileLanes
+// slots, starting at a multiple of kTileLanes, can touch: one when tiles and
+// chunks align, kTileLanes / C when chunks divide the tile, else up to two
+// partial chunks around the whole ones.
+__host__ __device__ constexpr uint32_t zc_chunks_per_tile(uint32_t C) {
+  return C % kTileLanes == 0 ? 1u : (kTileLanes % C == 0 ? kTileLanes / C : kTileLanes / C + 2u);
+}
+
 // ZipCCL encoder scratch after the control block: one look-back state per
 // tile, then one look-back word per block of kZcLbBlock tiles.
 constexpr unsigned long long zc_enc_blocks(unsigned long long ntiles) {
@@ -102,6 +110,11 @@ cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t chunk_bytes, const vo
 cudaError_t ibp_pipe_decompress(const void* d_meta, uint32_t chunk_bytes, const void* d_in,
                                 unsigned long long in_bytes, void* d_y,
                                 unsigned long long y_cap, void* d_ws, cudaStream_t s);
+
+// Wait-failure test switch (zc_test_wait_fault): when armed, writes the
+// fault tile and the poll limit into the control block of the workspace at
+// d_ws, after the launcher has cleared it; otherwise does nothing.
+cudaError_t arm_wait_fault(void* d_ws, cudaStream_t s);
 
 // Blocks of `kernel` resident per SM times SMs on the current device.
 int resident_blocks(const void* kernel, int threads, size_t smem);

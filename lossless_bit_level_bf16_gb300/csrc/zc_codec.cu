@@ -107,10 +107,13 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const ZcLayout& L = A.L;
   const uint32_t C = L.C, log2C = L.log2C;
+  // chunk sizes that are powers of two divide by shifts; the others (any
+  // multiple of 1024) by division, once per ticket and per 1024-slot step
+  const bool p2 = (C & (C - 1)) == 0;
   const unsigned long long S = L.slot_bytes;
-  const unsigned long long lanes_total = L.nchunks << log2C;
+  const unsigned long long lanes_total = L.nchunks * (unsigned long long)C;
   const unsigned long long ntiles = (lanes_total + kWTile - 1) / kWTile;
-  const uint32_t nct = C >= kWTile ? 1u : kWTile / C;  // chunks per ticket
+  const uint32_t nct = zc_chunks_per_tile(C);  // chunks a ticket can touch
   uint8_t* wring = dyn + (size_t)warp * (kStages * 2048u + nct * 1024u + 2 * kEscCap);  // input steps
   uint32_t* wlut = reinterpret_cast<uint32_t*>(wring + kStages * 2048u);
   uint8_t* const wst_base = wring + kStages * 2048u + nct * 1024u;  // two escape staging windows
@@ -125,9 +128,11 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   uint32_t p_run = 0, p_cs = 0, p_buf = 0;
   // a ticket's inclusive prefix (after a timeout: its own count, and nothing
   // for its block, so that no one waits)
+  const unsigned lim = wait_limit(A.ctrl);
+  const unsigned long long fault1 = A.ctrl->fault_tile1;  // 0 unless a wait-failure test
   auto publish_inc = [&](unsigned long long tl, unsigned long long excl, unsigned long long agg,
                          bool to) {
-    if (lane == 0) {
+    if (lane == 0 && tl + 1 != fault1) {
       if (to) {
         set_status(A.ctrl, ZC_ERR_TIMEOUT);
         st_relaxed_u64(A.states + tl, kFlagInc | agg);
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   };
   auto resolve = [&]() {
     bool to = false;
-    const unsigned long long excl = lb2_lookback<4>(A.states, A.bwords, p_tile, &to);
+    const unsigned long long excl = lb2_lookback<4>(A.states, A.bwords, p_tile, &to, lim);
     publish_inc(p_tile, excl, p_run, to);
     const unsigned long long dst = L.off_esc + excl;
     const uint8_t* pst = wst_base + p_buf * kEscCap;
@@ -148,9 +153,9 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
       for (uint32_t i = lane; i < p_run; i += 32) A.out[dst + i] = pst[i];
     }
     if (lane < (int)nct) {
-      const unsigned long long c = p_cfirst + lane;
-      const bool starts = C >= kWTile ? ((p_tlane0 & (C - 1)) == 0) : true;
-      if (c < L.nchunks && starts)
+      // chunks that start inside the ticket get their escape offset here
+      const unsigned long long c = p_cfirst + lane, cs = c * (unsigned long long)C;
+      if (c < L.nchunks && cs >= p_tlane0 && cs < p_tlane0 + kWTile)
         reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = excl + p_cs;
     }
     __syncwarp();
@@ -181,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
       break;
     }
     const unsigned long long tlane0 = tile * kWTile;
-    const unsigned long long cfirst = tlane0 >> log2C;
+    const unsigned long long cfirst = p2 ? (tlane0 >> log2C) : tlane0 / C;
+    const uint32_t r0 = (uint32_t)(tlane0 - cfirst * C);  // first slot's place in its chunk
     // chunk information, held by lane k for the ticket's chunk k
     unsigned long long ce0 = 0;
     uint32_t cval = 0;
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
           my_c1 = my_c0 + A.segs[my_seg].nchunks;
         }
         const ZcSegDev& r = A.segs[my_seg];
-        ce0 = r.elem_start + ((c - r.chunk_start) << log2C);
+        ce0 = r.elem_start + (c - r.chunk_start) * (unsigned long long)C;
         const unsigned long long end = r.elem_start + r.nelem;
         cval = (uint32_t)((end - ce0) < C ? (end - ce0) : C);
         cal = A.x_al16 && ((r.elem_start & 7ull) == 0);
@@ -228,7 +234,14 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     // are free of bank conflicts.  Other steps use plain per-lane loads.
     // With C >= 4096 the whole ticket lies in one chunk and the step's chunk
     // data need no shuffles.
-    const bool one = C >= kWTile;
+    const bool one = C % kWTile == 0;
+    // chunk (within the ticket) and slot (within the chunk) of step st's first slot
+    auto where = [&](uint32_t st, uint32_t& s0) -> int {
+      const uint32_t q = r0 + st * 1024u;
+      const uint32_t k = p2 ? (q >> log2C) : q / C;
+      s0 = q - k * C;
+      return (int)k;
+    };
     auto info = [&](uint32_t st, int& lct, unsigned long long& e0, uint32_t& vch, bool& al) {
       if (one) {
         lct = 0;
@@ -236,7 +249,8 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
         vch = t_val;
         al = t_al;
       } else {
-        lct = (int)((st * 1024u) >> log2C);
+        uint32_t s0_;
+        lct = where(st, s0_);
         e0 = __shfl_sync(kFull, ce0, lct);
         vch = __shfl_sync(kFull, cval, lct);
         al = __shfl_sync(kFull, cal, lct) != 0;
@@ -249,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
         uint32_t v_;
         bool a_;
         info(st, l_, e_, v_, a_);
-        const uint32_t s0 = (uint32_t)((tlane0 + st * 1024u) & (C - 1));
+        uint32_t s0;
+        where(st, s0);
         if (a_ && v_ >= s0 + 1024u) {
           uint8_t* slotbuf = wring + (st % kStages) * 2048u;
           const uint16_t* src = A.x + e_ + s0;
@@ -331,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
       uint32_t vch;
       bool al;
       info(st, lct, e0, vch, al);
-      const uint32_t s0 = (uint32_t)((tlane0 + st * 1024u) & (C - 1));
+      uint32_t s0;
+      where(st, s0);
       const uint32_t i0 = s0 + 32u * lane;
       const int valid = vch > i0 ? ((vch - i0) < 32u ? (int)(vch - i0) : 32) : 0;
       uint32_t w[16];
@@ -391,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     if (run <= kEscCap) {
       // publish this ticket's escape count now, resolve the previous ticket,
       // and keep this one pending in its window
-      if (lane == 0) lb2_publish_agg(A.states, A.bwords, tile, run);
+      if (lane == 0 && tile + 1 != fault1) lb2_publish_agg(A.states, A.bwords, tile, run);
       if (p_has) resolve();
       p_has = true;
       p_tile = tile;
@@ -408,9 +424,9 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     // ---- more escapes than a window holds: the look-back now, then the
     // ticket is classified again and its escapes written straight out
     bool to = false;
-    if (lane == 0) lb2_publish_agg(A.states, A.bwords, tile, run);
+    if (lane == 0 && tile + 1 != fault1) lb2_publish_agg(A.states, A.bwords, tile, run);
     __syncwarp();
-    const unsigned long long excl = lb2_lookback<4>(A.states, A.bwords, tile, &to);
+    const unsigned long long excl = lb2_lookback<4>(A.states, A.bwords, tile, &to, lim);
     publish_inc(tile, excl, run, to);
     const unsigned long long dst = L.off_esc + excl;
     if (dst + run > A.out_cap) {
@@ -425,7 +441,9 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
         uint32_t vch;
         bool al;
         info(st, lct, e0, vch, al);
-        const uint32_t i0 = (uint32_t)((tlane0 + st * 1024u) & (C - 1)) + 32u * lane;
+        uint32_t s0;
+        where(st, s0);
+        const uint32_t i0 = s0 + 32u * lane;
         const int valid = vch > i0 ? ((vch - i0) < 32u ? (int)(vch - i0) : 32) : 0;
         uint32_t w[16];
         lane_load(A.x + e0 + i0, valid, w);
@@ -440,9 +458,8 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
       }
     }
     if (lane < (int)nct) {
-      const unsigned long long c = cfirst + lane;
-      const bool starts = C >= kWTile ? ((tlane0 & (C - 1)) == 0) : true;
-      if (c < L.nchunks && starts)
+      const unsigned long long c = cfirst + lane, cs = c * (unsigned long long)C;
+      if (c < L.nchunks && cs >= tlane0 && cs < tlane0 + kWTile)
         reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = excl + cs_pos;
     }
     __syncwarp();  // the window is reused by the next ticket
@@ -543,8 +560,8 @@ __device__ bool parse_header(const uint8_t* in, unsigned long long in_bytes,
   h.off_static = rd_u64(in + 56);
   h.off_esc = rd_u64(in + 64);
   h.total = rd_u64(in + 72);
-  if (h.C < 1024u || h.C > 65536u || (h.C & (h.C - 1)) != 0 || h.nseg == 0) return false;
-  h.log2C = 31 - __clz(h.C);
+  if (h.C < 1024u || h.C > 65536u || (h.C % 1024u) != 0 || h.nseg == 0) return false;
+  h.log2C = 31 - __clz(h.C);  // used only when C is a power of two
   if (h.total > in_bytes) return false;
   const unsigned long long S = (unsigned long long)h.C * 11ull / 8ull;
   if (h.off_seg != kZcHeader) return false;
@@ -557,7 +574,7 @@ __device__ bool parse_header(const uint8_t* in, unsigned long long in_bytes,
   if (h.off_esc != h.off_static + h.nchunks * S) return false;
   if (h.off_esc > h.total || h.esc_total > h.total - h.off_esc) return false;
   if (h.total != h.off_esc + round_up_dev(h.esc_total, kZcAlign)) return false;
-  if (h.n > (h.nchunks << h.log2C)) return false;
+  if (h.n > h.nchunks * (unsigned long long)h.C) return false;
   if (h.n > y_cap) {
     err = ZC_ERR_CAPACITY;
     return false;
@@ -583,7 +600,7 @@ __device__ bool load_seg(const uint8_t* in, const DecHdr& h, uint32_t s, SegRec&
   r.R1 = (uint32_t)(bk >> 24);
   if (r.nelem > h.n || r.elem_start > h.n - r.nelem) return false;
   if (r.nchunks > h.nchunks || r.chunk_start > h.nchunks - r.nchunks) return false;
-  if (r.nchunks != ((r.nelem + h.C - 1) >> h.log2C)) return false;
+  if (r.nchunks != (r.nelem + h.C - 1) / h.C) return false;
   if (s == 0) return r.elem_start == 0 && r.chunk_start == 0;
   const uint8_t* q = p - kZcSegRec;
   return rd_u64(q) + rd_u64(q + 8) == r.elem_start && rd_u64(q + 16) + rd_u64(q + 24) == r.chunk_start;
@@ -707,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
       if (lane == 0) set_status(ctrl, ZC_ERR_FORMAT);
       continue;  // warp-uniform
     }
-    const unsigned long long e0 = r.elem_start + ((c - r.chunk_start) << h.log2C);
+    const unsigned long long e0 = r.elem_start + (c - r.chunk_start) * (unsigned long long)h.C;
     const unsigned long long vch_ll = r.elem_start + r.nelem - e0;
     const uint32_t vch = (uint32_t)(vch_ll < C ? vch_ll : C);
     const bool al = y_al16 && ((r.elem_start & 7ull) == 0);
@@ -805,9 +822,11 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   Ctrl* ctrl = static_cast<Ctrl*>(d_ws);
   unsigned long long* states =
       reinterpret_cast<unsigned long long*>(static_cast<char*>(d_ws) + kCtrlBytes);
-  const unsigned long long ntiles = ((L.nchunks << L.log2C) + kWTile - 1) / kWTile;
+  const unsigned long long ntiles = (L.nchunks * (unsigned long long)L.C + kWTile - 1) / kWTile;
   char* lb = static_cast<char*>(d_ws) + kCtrlBytes;
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + zc_enc_scratch_bytes(ntiles), s);
+  if (e != cudaSuccess) return e;
+  e = arm_wait_fault(d_ws, s);
   if (e != cudaSuccess) return e;
   EncArgs A;
   A.x = d_x;
@@ -820,7 +839,7 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   A.states = states;
   A.bwords = reinterpret_cast<unsigned long long*>(lb + (8 * ntiles + 15) / 16 * 16);
   A.x_al16 = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
-  const uint32_t nct = L.C >= kWTile ? 1u : kWTile / L.C;
+  const uint32_t nct = zc_chunks_per_tile(L.C);
   const size_t smem = (size_t)kEncWarps * (kStages * 2048u + nct * 1024u + 2 * kEscCap);
   e = cudaFuncSetAttribute(zc_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)

@@ -41,7 +41,9 @@ def test_host_only_calls(lib):
     assert lib.ibp_meta_bytes(512) == 64 + 1024
     assert lib.zc_decompress_workspace_bytes() == 256
     assert lib.ibp_workspace_bytes(512, 1 << 20, 0) >= 256
-    assert lib.ibp_workspace_bytes(12, 1 << 20, 0) == 0  # chunk size not supported
+    assert lib.ibp_workspace_bytes(12, 1 << 20, 0) >= 256  # any multiple of 4 bytes
+    assert lib.ibp_workspace_bytes(14, 1 << 20, 0) == 0  # not a multiple of 4
+    assert lib.ibp_workspace_bytes(4100, 1 << 20, 0) == 0  # above 4096
     assert lib.ibp_max_compressed_bytes(512, 4096) > 4096
 
 
@@ -51,8 +53,13 @@ def test_argument_checks_need_no_gpu(lib):
     assert lib.zc_plan_create(100, None, 1, 1000, ctypes.byref(h)) == abi.ZC_ERR_ARG
     assert lib.zc_plan_create(100, None, 1, 1 << 17, ctypes.byref(h)) == abi.ZC_ERR_ARG
     assert lib.zc_plan_create(100, None, 0, 4096, ctypes.byref(h)) == abi.ZC_ERR_ARG
-    # legal in the format (multiple of 1024) but not a power of two
-    assert lib.zc_plan_create(100, None, 1, 3072, ctypes.byref(h)) == abi.ZC_ERR_UNSUPPORTED
+    # any multiple of 1024 up to 65536, powers of two or not, passes the
+    # argument checks (without a GPU the plan's device table then fails)
+    for C in (1024, 3072, 5120, 9216, 64512, 65536):
+        rc = lib.zc_plan_create(100, None, 1, C, ctypes.byref(h))
+        assert rc in (abi.ZC_OK, abi.ZC_ERR_CUDA, abi.ZC_ERR_NOMEM), (C, rc)
+        if rc == abi.ZC_OK:
+            lib.zc_plan_destroy(h)
     # bad segment offsets
     so = (ctypes.c_uint64 * 3)(0, 60, 50)
     assert lib.zc_plan_create(50, so, 2, 4096, ctypes.byref(h)) == abi.ZC_ERR_ARG

@@ -29,14 +29,21 @@ static __device__ __align__(256) unsigned char g_zc_scratch[kStaticScratchBytes]
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// The array's device address on the current device, looked up once per
-// device (with that device current) and kept.
-int scratch_for_current_device(void** out) {
+// The array's device address on the current device.  Outside a stream
+// capture it is looked up on every call (with that device current): a device
+// reset reloads the library's module, and the array may then sit elsewhere.
+// During a capture the address the last such lookup found is used.
+int scratch_for_current_device(cudaStream_t s, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ZC_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return ZC_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();  // e.g. the legacy stream while another stream captures
+    cs = cudaStreamCaptureStatusActive;
+  }
   std::lock_guard<std::mutex> g(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (cs == cudaStreamCaptureStatusNone || !g_scratch_ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_zc_scratch) != cudaSuccess || !p) return ZC_ERR_CUDA;
     g_scratch_ptr[dev] = p;
@@ -57,10 +64,10 @@ extern "C" int zc_compress_static(zc_plan_t p, const uint16_t* d_x, void* d_out,
   if (!al(d_out, 16) || !al(d_x, 2) || !al(d_out_bytes, 8) || !al(d_status, 4)) return ZC_ERR_ARG;
   if (p->L.ntiles > kStaticMaxTiles) return ZC_ERR_CAPACITY;
   if (out_cap < p->L.off_esc) return ZC_ERR_CAPACITY;
-  void* scratch = nullptr;
-  const int rc = scratch_for_current_device(&scratch);
-  if (rc != ZC_OK) return rc;
   const cudaStream_t s = (cudaStream_t)stream;
+  void* scratch = nullptr;
+  const int rc = scratch_for_current_device(s, &scratch);
+  if (rc != ZC_OK) return rc;
   // the launcher clears the control block and the look-back words it uses
   cudaError_t e = lbb::zc_launch_compress(p->L, p->d_segs, d_x, d_out, out_cap,
                                           reinterpret_cast<unsigned long long*>(d_out_bytes),

@@ -2,12 +2,16 @@
 
 Collected last on purpose: the entry point's scratch is one array per device
 shared by every call, so it is checked after whatever the other tests left
-running on the device, as well as on its own in a fresh process.  Each case
-calls the new entry point twice in a row, on two different inputs, through
-the C ABI, and compares each stream byte for byte (the codec is exact, so the
-tolerance is zero) with zc_compress on the same input.
+running on the device, and (test_static_in_a_fresh_process) on its own in a
+new Python process whose first library call it is.  Each case calls the new
+entry point twice in a row, on two different inputs, through the C ABI, and
+compares each stream byte for byte (the codec is exact, so the tolerance is
+zero) with zc_compress on the same input.
 """
 import ctypes as C
+import os
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -86,3 +90,40 @@ def test_static_rejects_plans_beyond_its_scratch():
         assert rc == abi.ZC_ERR_CAPACITY
     finally:
         lib.zc_plan_destroy(h)
+
+
+def test_static_in_a_fresh_process():
+    """The two-input comparison again, in a new process where the first call
+    into the library is zc_compress_static (so its address lookup is the
+    process's first use of the array)."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = """
+import torch
+from lossless_bit_level_bf16_gb300 import abi, workloads as W, zipccl as Z
+lib = abi.load()
+n = 2 * 65536 + 333
+xs = [W.zc_gaussian(n, sigma=0.02, seed=21, device="cuda"),
+      W.zc_gaussian(n, sigma=0.3, seed=22, device="cuda")]
+plan = Z.Plan(n, None, 4096)
+plan.set_books([116, 117, 118, 119, 120, 121, 122])
+out = torch.zeros(plan.max_compressed_bytes, dtype=torch.uint8, device="cuda")
+nb = torch.zeros(1, dtype=torch.int64, device="cuda")
+status = torch.full((1,), 777, dtype=torch.int32, device="cuda")
+for x in xs:
+    rc = lib.zc_compress_static(plan._h, abi.ptr(x), abi.ptr(out), out.numel(), abi.ptr(nb),
+                                abi.ptr(status), abi.stream_handle(None))
+    assert rc == abi.ZC_OK, rc
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out[: int(nb.item())].clone()
+    ref, ref_nb = plan.compress(x)
+    torch.cuda.synchronize()
+    assert plan.status() == 0 and int(ref_nb.item()) == got.numel()
+    assert torch.equal(got, ref[: got.numel()])
+print("fresh-process-ok")
+"""
+    env = dict(os.environ)
+    env["PYTHONPATH"] = root + os.pathsep + env.get("PYTHONPATH", "")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and "fresh-process-ok" in r.stdout, r.stdout + r.stderr

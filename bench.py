@@ -14,8 +14,10 @@ events.  `e2e` repeats the step through host memory: pinned host inputs are
 copied in and the compressed streams copied out inside the timed region, the
 ZipCCL and IBP chains on two streams so that copies overlap kernels.
 
---impl reference times the bit-serial CPU oracle (the checker; single thread)
-on a bounded sample of the same workload.
+--impl reference times the bit-serial CPU oracle (the checker) on all host
+cores (independent oracle calls on disjoint pieces) over a bounded sample of
+the same workload; the GPU line's cpu_baseline carries that figure and the
+single-thread one.
 """
 from __future__ import annotations
 
@@ -146,6 +148,85 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
+class NvmlSampler:
+    """Clock and throttle-reason samples taken through NVML (the driver's
+    libnvidia-ml, read-only queries) every millisecond by a background
+    thread, so that even a timed region of a few milliseconds has samples.
+    Falls back to ClockSampler (nvidia-smi, 20 ms) when NVML is missing."""
+
+    HW_SLOWDOWN, SW_POWER_CAP, SW_THERMAL, HW_THERMAL = 0x8, 0x4, 0x20, 0x40
+
+    def __init__(self, device_index, period_s=0.001):
+        self.index = device_index
+        self.period = period_s
+        self.fallback = None
+        self.samples = []
+        self.max_mhz = None
+
+    def _open(self):
+        import ctypes as C
+        import torch
+        lib = C.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        u = str(getattr(torch.cuda.get_device_properties(self.index), "uuid", ""))
+        u = u if u.startswith("GPU-") else "GPU-" + u
+        h = C.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(u.encode(), C.byref(h)) != 0:
+            raise OSError("no NVML handle for " + u)
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = C.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, C.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        return lib, h, reasons
+
+    def __enter__(self):
+        import threading
+        try:
+            lib, h, reasons = self._open()
+        except (OSError, AttributeError):
+            self.fallback = ClockSampler(self.index).__enter__()
+            return self
+        import ctypes as C
+        self._stop = threading.Event()
+
+        def run():
+            clk, r = C.c_uint(), C.c_ulonglong()
+            while not self._stop.is_set():
+                if lib.nvmlDeviceGetClockInfo(h, 1, C.byref(clk)) == 0 and \
+                        reasons(h, C.byref(r)) == 0:
+                    self.samples.append((float(clk.value), int(r.value)))
+                time.sleep(self.period)
+        self._lib = lib
+        self._t = threading.Thread(target=run, daemon=True)
+        self._t.start()
+        time.sleep(0.005)  # the thread is sampling before the region starts
+        self.samples.clear()
+        return self
+
+    def __exit__(self, *a):
+        if self.fallback is not None:
+            return self.fallback.__exit__(*a)
+        self._stop.set()
+        self._t.join()
+
+    def summary(self):
+        if self.fallback is not None:
+            d = self.fallback.summary()
+            d["source"] = "nvidia-smi"
+            return d
+        mhz = [c for c, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        names = [(self.HW_SLOWDOWN, "hw_slowdown"), (self.HW_THERMAL, "hw_thermal_slowdown"),
+                 (self.SW_THERMAL, "sw_thermal_slowdown"), (self.SW_POWER_CAP, "sw_power_cap")]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in names if bits & b), "samples": len(mhz),
+                "source": "nvml, 1 ms"}
+
+
 def reduce_max(x: float) -> float:
     """Maximum of a float over all ranks (identity without a process group)."""
     import torch
@@ -208,15 +289,9 @@ class Workload:
         self.mode = 0
         self.unc_bytes = 2 * self.n + self.tbytes
         # kernels each op launches (cudaMemsetAsync of a control block aside)
-        self.kernels = {"zc_plan": ["zc_stats_kernel", "zc_predict_kernel"],
-                        "zc_compress": ["zc_encode_kernel"],
-                        "zc_decompress": ["zc_decode_kernel"],
-                        "ibp_build_meta": ["ibp_columns_kernel", "ibp_meta_kernel"],
-                        # one single-pass kernel for chunks of up to 512 bytes
-                        "ibp_compress": (["ibp_encode_ws_kernel"] if self.cb <= 512 else
-                                         ["ibp_match_kernel", "ibp_offsets_kernel",
-                                          "ibp_pack_kernel"]),
-                        "ibp_decompress": ["ibp_decode_pipe_kernel"]}
+        self.kernels = {op: kernels_of(op, self.cb) for op in
+                        ("zc_plan", "zc_compress", "zc_decompress", "ibp_build_meta",
+                         "ibp_compress", "ibp_decompress")}
         self.launches_per_step = sum(len(v) for v in self.kernels.values())
 
     def ops(self):
@@ -275,13 +350,29 @@ def gpu_arm(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize()
     all_evs = []
-    with ClockSampler(local_rank) as clk:
+    with NvmlSampler(local_rank) as clk:
         t0 = time.perf_counter()
         for _ in range(args.steps):
             all_evs.append(step(True))
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     barrier()
+    # the same step repeated for at least a second, with its own clock record
+    # (reported beside the K-step figure, which it does not replace)
+    sus_evs = []
+    with NvmlSampler(local_rank) as sclk:
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < args.sustain_s or len(sus_evs) < 3:
+            sus_evs.append(step(True))
+            if len(sus_evs) % 64 == 0:
+                sus_evs[-1][-1].synchronize()
+        torch.cuda.synchronize()
+        sus_wall = time.perf_counter() - t0
+    sus_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in sus_evs)
+    sustained = {"steps": len(sus_evs), "wall_s": round(sus_wall, 3), "ms_per_step": round(sus_ms, 4),
+                 "clocks": sclk.summary()}
+    if sustained["clocks"].get("sm_mhz"):
+        sustained["ms_x_mhz"] = round(sus_ms * sustained["clocks"]["sm_mhz"], 1)
     per_op = {name: [] for name, _ in ops}
     steps_ms = []
     for evs in all_evs:
@@ -341,8 +432,66 @@ def gpu_arm(args, rank, world, local_rank):
     e2e_max = reduce_max(e2e)
     h2d = hx.numel() * 2 + ht.numel() * 4 + hs.numel() * 4
     d2h = zsz + isz + 20
+    targets = target_ops(args, dev, flush, stream) if args.targets else {}
     return dict(wl=wl, per_op=per_op, ms=ms_max, ms_local=ms, wall=wall, clocks=clk.summary(),
-                e2e_ms=e2e_max, h2d=h2d, d2h=d2h, zsz=zsz, isz=isz)
+                e2e_ms=e2e_max, h2d=h2d, d2h=d2h, zsz=zsz, isz=isz, sustained=sustained,
+                targets=targets)
+
+
+# kernels each op launches, by codec and IBP chunk size
+def kernels_of(op, cb=512):
+    return {"zc_plan": ["zc_stats_kernel", "zc_predict_kernel"],
+            "zc_compress": ["zc_encode_kernel"],
+            "zc_decompress": ["zc_decode_kernel"],
+            "ibp_build_meta": ["ibp_columns_kernel", "ibp_meta_kernel"],
+            "ibp_compress": (["ibp_encode_ws_kernel"] if cb <= 512 else
+                             ["ibp_match_kernel", "ibp_offsets_kernel", "ibp_pack_kernel"]),
+            "ibp_decompress": ["ibp_decode_pipe_kernel"]}[op]
+
+
+TARGETS = [("zipccl", 1 << 30, 0, "zipccl bf16 N(0,0.01) 1 GiB, chunk 4096"),
+           ("ibp", 1 << 30, 0, "ibp fp32 N(0,0.02) 1 GiB, 2048-B chunks, per-position"),
+           ("ibp", 1 << 30, 1, "ibp fp32 N(0,0.02) 1 GiB, 2048-B chunks, joint")]
+
+
+def target_ops(args, dev, flush, stream):
+    """The workload list's >= 256 MB points where the roofline target applies,
+    timed op by op after the step (median of CUDA-event times, L2 flushed
+    before every launch): ZipCCL on the 1 GiB bf16 sweep point and IBP on the
+    1 GiB fp32 sweep point (2048-byte chunks, where chunks participate), in
+    both metadata modes.  Returns ops entries, each with its roofline."""
+    import torch
+
+    from lossless_bit_level_bf16_gb300 import abi
+    peak, peak_kind = _peaks()
+    out = {}
+    steps = max(5, min(args.steps, 20))
+    for kind, nbytes, mode, label in TARGETS:
+        ops, wss, unc, sbytes, check, nb, cb = _case(kind, nbytes, dev, mode)
+        ms = _time_ops(ops, flush, stream, 3, steps)
+        for ws in wss:
+            st = abi.status(ws)
+            if st != 0:
+                raise RuntimeError(f"{label}: device status {st}: {abi.strerror(st)}")
+        if not check():
+            raise RuntimeError(f"{label}: round trip differs")
+        comp = int(nb.item())
+        for name, t in ms.items():
+            if name == "ibp_build_meta":
+                continue  # 20 MB of samples: not a >= 256 MB op
+            alg = unc if name == "zc_plan" else unc + comp
+            ach = alg / (t * 1e-3) / 1e9
+            ks = kernels_of(name, cb)
+            out[f"{name} [{label}]"] = {
+                "ms": round(t, 4), "GBps_uncompressed": round(unc / (t * 1e-3) / 1e9, 1),
+                "ratio": round(unc / comp, 4), "kernels": ks, "launches_timed": steps,
+                "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+                             "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                             "frac": round(ach / peak, 4), "algorithmic_bytes_per_launch": alg,
+                             "traffic": measured_traffic(ks[0]) if len(ks) == 1 else None}}
+        del ops, wss, check, nb
+        torch.cuda.empty_cache()
+    return out
 
 
 def report_gpu(args, r, world):
@@ -407,7 +556,12 @@ def report_gpu(args, r, world):
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": r["clocks"],
+        "sustained": r["sustained"],
     }
+    if r["clocks"].get("sm_mhz"):
+        line["clocks"]["ms_x_mhz"] = round(r["ms"] * r["clocks"]["sm_mhz"], 1)
+    for name, d in r["targets"].items():
+        ops[name] = d
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
@@ -588,77 +742,136 @@ def sweep_arm(args):
 
 # ---------------------------------------------------------------- oracle arm
 
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            k = line.split(":")[0].strip().lower()
+            if k in ("model name", "cpu model"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+class OracleSample:
+    """The step's data on the host (the gradient-like buffer's 256 blocks and
+    the 1,000,000-row table with its 10,000 sample rows), and one pass of the
+    bit-serial oracle over part of it: ZipCCL encode + decode of `nblk`
+    blocks, IBP metadata + encode + decode of `rows` rows.  With threads > 1
+    the blocks and rows are cut into that many pieces (whole blocks; whole
+    groups of 32 rows) and each piece is an ordinary oracle call in a thread
+    of its own (ctypes releases the GIL), all pieces at once."""
+
+    def __init__(self):
+        import oracle as O
+        from lossless_bit_level_bf16_gb300 import workloads as W
+        O.build()
+        self.O = O
+        x, self.seg = W.zc_gradient(device="cpu")
+        self.xb = W.bf16_bits(x)
+        tab, idx = W.ibp_table(device="cpu")
+        self.tb = W.f32_bytes(tab)
+        self.sbytes = W.f32_bytes(tab[idx].contiguous())
+
+    def run(self, nblk, rows, threads=1):
+        import numpy as np
+        from concurrent.futures import ThreadPoolExecutor
+        O, B = self.O, 262144
+        nblk, rows = max(1, min(256, nblk)), max(32, min(1_000_000, rows))
+
+        def zc_piece(b0, b1):
+            st, _, _, _ = O.zc_encode(self.xb[b0 * B:b1 * B],
+                                      seg_off=[B * i for i in range(b1 - b0 + 1)], chunk_elems=4096)
+            rc, y = O.zc_decode(st)
+            assert rc == 0 and np.array_equal(y, self.xb[b0 * B:b1 * B])
+
+        def ibp_piece(meta, r0, r1):
+            xb = self.tb[r0 * 512:r1 * 512]
+            st = O.ibp_encode(meta, xb)
+            rc, y = O.ibp_decode(meta, st)
+            assert rc == 0 and np.array_equal(y, xb)
+
+        def cuts(n, k, unit=1):
+            k = max(1, min(k, n // unit))
+            e = [n * i // k // unit * unit for i in range(k)] + [n]
+            return [(e[i], e[i + 1]) for i in range(k) if e[i + 1] > e[i]]
+
+        with ThreadPoolExecutor(threads) as ex:
+            t0 = time.perf_counter()
+            list(ex.map(lambda c: zc_piece(*c), cuts(nblk, threads)))
+            tz = time.perf_counter() - t0
+            t0 = time.perf_counter()
+            meta = O.ibp_build_meta(self.sbytes, 512, T=0.9, mode=0)
+            tm = time.perf_counter() - t0
+            t0 = time.perf_counter()
+            list(ex.map(lambda c: ibp_piece(meta, *c), cuts(rows, threads, 32)))
+            ti = time.perf_counter() - t0
+        return nblk * B, tz, tm, rows, ti
+
+    def rate(self, seconds, threads):
+        """GB/s of the whole step's bytes (128 MiB ZipCCL + 512 MB IBP) at the
+        rates a pass sized to take about `seconds` measures."""
+        n_z, tz, tm, rows, ti = self.run(8, 25_000, threads)
+        scale = max(0.5, seconds) / max(tz + tm + ti, 1e-3)
+        if scale > 1.5:
+            n_z, tz, tm, rows, ti = self.run(int(8 * scale), int(25_000 * scale), threads)
+        zc_bytes, ibp_bytes = 2 * 256 * 262144, 1_000_000 * 512
+        step_s = zc_bytes / (n_z * 2 / tz) + ibp_bytes / (rows * 512 / ti) + tm
+        sample = (f"ZipCCL encode+decode of {n_z // 262144} of the 256 gradient blocks; IBP metadata "
+                  f"from the 10,000 sample rows + encode+decode of {rows} of the 1,000,000 table "
+                  f"rows; scaled to the step's 128 MiB + 512 MB")
+        return (zc_bytes + ibp_bytes) / step_s / 1e9, sample, tz + tm + ti
+
+
 def cpu_baseline(seconds=15.0):
-    """The bit-serial oracle on a bounded sample of the same workload, scaled
-    to the step's byte mix (ZipCCL : IBP = 128 MiB : 512 MB).  A small sample
-    measures the oracle's rates; a second one, sized from them to take about
-    `seconds`, gives the figure."""
-    import numpy as np
-
-    import oracle as O
-    from lossless_bit_level_bf16_gb300 import workloads as W
-    O.build()
-    sbytes = None
-
-    def sample(nblk, rows):
-        nonlocal sbytes
-        x, seg = W.zc_gradient(n_blocks=nblk, device="cpu")
-        xb = W.bf16_bits(x)
-        t0 = time.perf_counter()
-        st, _, _, _ = O.zc_encode(xb, seg_off=seg, chunk_elems=4096)
-        rc, y = O.zc_decode(st)
-        tz = time.perf_counter() - t0
-        assert rc == 0 and np.array_equal(y, xb)
-        tab, idx = W.ibp_table(rows=rows, device="cpu", n_samples=10_000)
-        tb = W.f32_bytes(tab)
-        if sbytes is None:
-            sbytes = W.f32_bytes(tab[idx].contiguous())
-        t0 = time.perf_counter()
-        meta = O.ibp_build_meta(sbytes, 512, T=0.9, mode=0)
-        tm = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        s2 = O.ibp_encode(meta, tb)
-        rc2, y2 = O.ibp_decode(meta, s2)
-        ti = time.perf_counter() - t0
-        assert rc2 == 0 and np.array_equal(y2, tb)
-        return xb.size, tz, tm, rows, ti
-
-    n_z, tz, tm, rows, ti = sample(8, 25_000)
-    scale = max(1.0, seconds) / max(tz + tm + ti, 1e-3)
-    if scale > 1.5:
-        n_z, tz, tm, rows, ti = sample(min(256, max(8, int(8 * scale))),
-                                       min(1_000_000, max(25_000, int(25_000 * scale))))
-    zc_rate = n_z * 2 / tz  # bytes/s
-    ibp_rate = rows * 512 / ti
-    zc_bytes, ibp_bytes = 2 * 256 * 262144, 1_000_000 * 512
-    step_s = zc_bytes / zc_rate + ibp_bytes / ibp_rate + tm
-    return {"value": round((zc_bytes + ibp_bytes) / step_s / 1e9, 4), "unit": "GB/s",
-            "cores": 1, "kind": "oracle",
-            "sample": f"ZipCCL encode+decode of {n_z} elements ({n_z // 262144} of the 256 "
-                      f"blocks); IBP metadata from 10,000 rows + encode+decode of {rows} rows; "
-                      f"scaled to the step's 128 MiB + 512 MB mix",
-            "sample_seconds": round(tz + tm + ti, 2)}
+    """The bit-serial oracle on the host cores: all cores (chunk-parallel:
+    independent oracle calls on disjoint whole blocks / groups of rows) and a
+    single thread, each on a bounded sample scaled to the step's byte mix."""
+    smp = OracleSample()
+    nproc = os.cpu_count() or 1
+    v1, sample1, s1 = smp.rate(seconds, 1)
+    vn, samplen, sn = smp.rate(seconds / 3, nproc)
+    return {"value": round(vn, 4), "unit": "GB/s", "cores": nproc, "kind": "oracle",
+            "sample": samplen + f"; {nproc} threads, one oracle call per piece",
+            "sample_seconds": round(sn, 2), "cpu_model": cpu_model(), "nproc": nproc,
+            "single_thread": {"value": round(v1, 4), "cores": 1, "sample": sample1,
+                              "sample_seconds": round(s1, 2)}}
 
 
 def reference_arm(args):
-    steps_s = []
+    """The oracle, as it stands, on all host cores: each step is one
+    chunk-parallel pass over a bounded sample of the workload, sized so the
+    whole --steps/--warmup run ends within a few minutes."""
+    smp = OracleSample()
+    nproc = os.cpu_count() or 1
+    per_step = min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup))
+    steps_s, vals = [], []
     last = None
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        # each step a bounded sample: the whole run ends within a few minutes
-        last = cpu_baseline(min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+        v, last, _ = smp.rate(per_step, nproc)
         if i >= args.warmup:
             steps_s.append(time.perf_counter() - t0)
-    v = last["value"]
+            vals.append(v)
+    v = round(statistics.mean(vals), 4)
     return {
         "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1000 * statistics.mean(steps_s), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded generators; a bounded sample per step)",
         "config": {"workload": WORKLOAD, "zc_chunk": 4096, "ibp_chunk_bytes": 512, "ibp_T": 0.9,
-                   "parallelism": "host cores"},
+                   "parallelism": f"host cores x{nproc}"},
         "impl": "reference",
-        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": last["sample"], "value": v},
+        "cpu_baseline": {"kind": "oracle", "cores": nproc, "sample": last, "value": v,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -680,6 +893,10 @@ def main():
     ap.add_argument("--sizes", default="", help="sweep sizes in MiB, comma separated")
     ap.add_argument("--ibp-mode", type=int, default=0, choices=[0, 1])
     ap.add_argument("--only", default="", help="sweep: time only these ops (comma separated)")
+    ap.add_argument("--no-targets", dest="targets", action="store_false",
+                    help="skip the 1 GiB target cases after the step")
+    ap.add_argument("--sustain-s", type=float, default=1.0,
+                    help="seconds of repeated steps for the sustained clock record")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

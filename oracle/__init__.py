@@ -74,6 +74,9 @@ def lib():
             "ora_ibp_decode": (C.c_int, [u8p, u8p, C.c_uint64, u8p, C.c_uint64, u64p]),
             "ora_ibp_encode_group": (C.c_int, [u8p, u8p, C.c_uint32, C.c_uint32, u8p,
                                                C.c_uint64, u64p]),
+            "ora_ibp_slot_read_bytes": (C.c_uint32, [u8p, C.c_int, C.c_uint32]),
+            "ora_ibp_slot_encode": (C.c_int, [u8p, u8p, C.c_uint32, u8p, C.POINTER(C.c_int)]),
+            "ora_ibp_slot_decode": (C.c_int, [u8p, u8p, C.c_uint32, C.c_int, u8p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -248,3 +251,78 @@ def ibp_encode_group(meta, x_chunks, nch, last_bytes=0):
                                     _p(out, C.c_uint8), cap, C.byref(bits))
     _chk(rc, "ibp_encode_group")
     return out[: bits.value // 8].copy()
+
+
+# ------------------------------------------------------------------ IBP slots
+
+def ibp_slot_read_bytes(meta, p, length):
+    meta = _u8(meta)
+    return lib().ora_ibp_slot_read_bytes(_p(meta, C.c_uint8), int(p), int(length))
+
+
+def _slot_ranges(nch, pieces):
+    pieces = max(1, min(pieces, nch))
+    e = [nch * i // pieces for i in range(pieces + 1)]
+    return [(e[i], e[i + 1]) for i in range(pieces) if e[i + 1] > e[i]]
+
+
+def ibp_slots_encode(meta, x, slots=None, threads=None):
+    """In-place slot form of the bytes x (a multiple of 4): returns (slots,
+    bitmask).  `slots` starts as a copy of x unless given (its bytes past a
+    compressed slot's body are left as they are); bitmask is uint32 words, bit
+    s % 32 of word s / 32 set when slot s is compressed.  Chunk ranges are
+    encoded in threads (one C call per chunk)."""
+    from concurrent.futures import ThreadPoolExecutor
+    meta, xb = _u8(meta), _u8(x)
+    cb = int(meta[8:12].view(np.uint32)[0])
+    n = xb.size
+    nch = (n + cb - 1) // cb
+    out = xb.copy() if slots is None else slots
+    bits = np.zeros(nch, np.uint8)
+    L = lib()
+    mp = _p(meta, C.c_uint8)
+
+    def run(r):
+        pv = C.c_int()
+        for s in range(*r):
+            ln = min(cb, n - s * cb)
+            ch = np.ascontiguousarray(xb[s * cb: s * cb + ln])
+            rc = L.ora_ibp_slot_encode(mp, _p(ch, C.c_uint8), ln,
+                                       _p(out[s * cb:], C.c_uint8), C.byref(pv))
+            _chk(rc, "ibp_slot_encode")
+            bits[s] = pv.value
+    with ThreadPoolExecutor(threads or min(32, os.cpu_count() or 1)) as ex:
+        list(ex.map(run, _slot_ranges(nch, 4 * (threads or min(32, os.cpu_count() or 1)))))
+    words = np.zeros((nch + 31) // 32, np.uint32)
+    for w in range(words.size):
+        b = bits[32 * w: 32 * w + 32]
+        words[w] = int(sum(int(v) << i for i, v in enumerate(b)))
+    return out, words
+
+
+def ibp_slots_gather(meta, slots, n_bytes, bitmask, idx):
+    """Chunks idx[0], idx[1], ... decoded from their slots: returns
+    (rows uint8 [len(idx), chunk_bytes] (a short last chunk's row is zero past
+    its length), bytes read from the slots)."""
+    meta, sl = _u8(meta), _u8(slots)
+    bitmask = np.ascontiguousarray(bitmask, np.uint32)
+    cb = int(meta[8:12].view(np.uint32)[0])
+    idx = np.asarray(idx, np.int64).reshape(-1)
+    rows = np.zeros((idx.size, cb), np.uint8)
+    L = lib()
+    mp = _p(meta, C.c_uint8)
+    read = 0
+    for i, s in enumerate(idx):
+        s = int(s)
+        ln = min(cb, n_bytes - s * cb)
+        p = int((int(bitmask[s // 32]) >> (s % 32)) & 1)
+        rb = L.ora_ibp_slot_read_bytes(mp, p, ln)
+        src = np.ascontiguousarray(sl[s * cb: s * cb + rb])  # only the part that is read
+        buf = np.zeros(cb, np.uint8)
+        buf[:rb] = src
+        row = np.zeros(cb, np.uint8)
+        _chk(L.ora_ibp_slot_decode(mp, _p(buf, C.c_uint8), ln, p, _p(row, C.c_uint8)),
+             "ibp_slot_decode")
+        rows[i, :ln] = row[:ln]
+        read += rb
+    return rows, read

@@ -771,3 +771,65 @@ int ora_ibp_decode(const uint8_t* meta, const uint8_t* in, uint64_t in_bytes,
   *n_out = n_bytes;
   return ORA_OK;
 }
+
+/* ---------------- IBP in-place slots ([IBP] Integrazione del Sistema) ---- */
+
+uint32_t ora_ibp_slot_read_bytes(const uint8_t* meta, int p, uint32_t len) {
+  const uint64_t B = (uint64_t)rd32(meta + 8) * 8u;
+  const uint64_t m = rd32(meta + 16);
+  return p ? (uint32_t)(4u * ((B - m + 31u) / 32u)) : len;
+}
+
+int ora_ibp_slot_encode(const uint8_t* meta, const uint8_t* chunk, uint32_t len,
+                        uint8_t* slot, int* p) {
+  if (!ibp_meta_ok(meta)) return ORA_E_ARG;
+  const uint32_t cb = rd32(meta + 8);
+  if (len == 0 || len > cb || (len % 4u) != 0) return ORA_E_ARG;
+  const uint64_t B = (uint64_t)cb * 8u;
+  const uint8_t* mask = meta + IBPM_HDR;
+  /* [IBP] step 2's predicate; a short chunk is kept raw */
+  *p = len == cb ? ora_ibp_chunk_p(meta, chunk) : 0;
+  if (!*p) {
+    memmove(slot, chunk, len);
+    return ORA_OK;
+  }
+  /* the kept bits, one at a time, into a scratch body, then the body's
+   * words over the start of the slot */
+  const uint32_t rb = ora_ibp_slot_read_bytes(meta, 1, cb);
+  uint8_t* body = (uint8_t*)calloc(rb ? rb : 1, 1);
+  if (!body) return ORA_E_ARG;
+  uint64_t q = 0;
+  for (uint64_t j = 0; j < B; ++j) {
+    if (get_bit(mask, j)) continue;
+    set_bit(body, q++, get_bit(chunk, j));
+  }
+  memcpy(slot, body, rb);
+  free(body);
+  return ORA_OK;
+}
+
+int ora_ibp_slot_decode(const uint8_t* meta, const uint8_t* slot, uint32_t len,
+                        int p, uint8_t* chunk) {
+  if (!ibp_meta_ok(meta)) return ORA_E_ARG;
+  const uint32_t cb = rd32(meta + 8);
+  if (len == 0 || len > cb || (len % 4u) != 0) return ORA_E_ARG;
+  if (!p) {
+    memmove(chunk, slot, len);
+    return ORA_OK;
+  }
+  if (len != cb || rd32(meta + 16) == 0) return ORA_E_FORMAT;
+  const uint64_t B = (uint64_t)cb * 8u;
+  const uint8_t* mask = meta + IBPM_HDR;
+  const uint8_t* bitval = meta + IBPM_HDR + cb;
+  uint8_t* out = (uint8_t*)calloc(cb, 1);
+  if (!out) return ORA_E_ARG;
+  uint64_t q = 0;
+  for (uint64_t j = 0; j < B; ++j) {
+    /* [IBP] step 3: Bitval at the invariant positions, kept bits in order */
+    if (get_bit(mask, j)) set_bit(out, j, get_bit(bitval, j));
+    else set_bit(out, j, get_bit(slot, q++));
+  }
+  memcpy(chunk, out, cb);
+  free(out);
+  return ORA_OK;
+}

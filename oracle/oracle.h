@@ -130,6 +130,32 @@ int ora_ibp_encode_group(const uint8_t* meta, const uint8_t* x, uint32_t nch,
                          uint32_t last_bytes, uint8_t* out, uint64_t cap,
                          uint64_t* bits);
 
+/* ---------------- IBP in-place slots ([IBP] Integrazione del Sistema) ------
+ *
+ * Tensors kept in host memory for transfer: chunk s of the input owns a fixed
+ * slot of chunk_bytes at slot_base + s*chunk_bytes (the last slot is as long
+ * as the last chunk).  When the chunk participates (the predicate of step 2)
+ * the slot starts with its body -- the B - m kept bits in ascending position
+ * order, zero bits up to a whole 32-bit word -- and the slot's later bytes are
+ * left as they were (compression in place); otherwise the slot holds the raw
+ * chunk.  A bitmask (bit s % 32 of 32-bit word s / 32) records which slots
+ * are compressed.  Reading a slot reads only its first
+ * ora_ibp_slot_read_bytes bytes. */
+
+/* Bytes of a slot that hold the chunk: 4*ceil((B - m)/32) when compressed,
+ * else len. */
+uint32_t ora_ibp_slot_read_bytes(const uint8_t* meta, int p, uint32_t len);
+
+/* Slot form of one chunk of len bytes (a multiple of 4, at most chunk_bytes):
+ * *p receives its participation bit; the slot's first read_bytes bytes are
+ * written, the rest of the slot is not touched. */
+int ora_ibp_slot_encode(const uint8_t* meta, const uint8_t* chunk, uint32_t len,
+                        uint8_t* slot, int* p);
+
+/* The chunk (len bytes) back from its slot and participation bit. */
+int ora_ibp_slot_decode(const uint8_t* meta, const uint8_t* slot, uint32_t len,
+                        int p, uint8_t* chunk);
+
 #ifdef __cplusplus
 }
 #endif

@@ -225,3 +225,82 @@ def test_degenerate_and_mismatch():
     bad[0] ^= 1
     assert O.ibp_decode(meta_none, bad)[0] == O.E_FORMAT
     assert O.ibp_decode(meta_none, st[:-16])[0] == O.E_FORMAT
+
+
+# ---------------------------------------------------------------- in-place slots
+# ([IBP] Integrazione del Sistema: tensors compressed in place in fixed-size
+# buffers, only the compressed part read, a GPU bitmask of compressed tensors)
+
+def _slot_case(cb, frac, nch, seed, tail=0):
+    rng = np.random.default_rng(seed)
+    B = 8 * cb
+    mask = (rng.uniform(size=B) < frac).astype(np.uint8)
+    bitval = rng.integers(0, 2, size=B).astype(np.uint8) & mask
+    meta = O.ibp_make_meta(cb, np.packbits(mask, bitorder="little"),
+                           np.packbits(bitval, bitorder="little"))
+    bits = rng.integers(0, 2, size=(nch, B)).astype(np.uint8)
+    force = rng.uniform(size=nch) < 0.6
+    bits[force] = np.where(mask.astype(bool), bitval, bits[force])
+    x = np.packbits(bits, axis=1, bitorder="little").reshape(-1)
+    return meta, x[: x.size - tail]
+
+
+@pytest.mark.parametrize("cb,frac,tail", [(64, 0.3, 0), (512, 0.12, 20), (20, 0.5, 0),
+                                          (48, 0.0, 8), (32, 1.0, 0), (2048, 0.02, 1024)])
+def test_slots_are_the_stream_bodies(cb, frac, tail):
+    """A slot's first bits are exactly the chunk's body in the IBP1 stream
+    (the layout pinned by the hand-derived golden stream): kept bits when the
+    participation bit is set, the raw chunk otherwise; the bitmask words are
+    the groups' participation words; a compressed slot is read for
+    4*ceil((B-m)/32) bytes and its bytes past that are left as they were."""
+    meta, x = _slot_case(cb, frac, 32 * 3 + 7, cb + int(frac * 100), tail)
+    n = x.size
+    nch = (n + cb - 1) // cb
+    m = int(meta[16:20].view(np.uint32)[0])
+    B = 8 * cb
+    slots, bm = O.ibp_slots_encode(meta, x, threads=3)
+    assert bm.size == (nch + 31) // 32
+    for g in range((nch + 31) // 32):
+        nin = min(32, nch - 32 * g)
+        last = n - (32 * g + nin - 1) * cb
+        pay = O.ibp_encode_group(meta, x[32 * g * cb: 32 * g * cb + (nin - 1) * cb + min(cb, last)],
+                                 nin, min(cb, last) if last < cb else 0)
+        pbits = np.unpackbits(pay, bitorder="little")
+        assert int(pay[:4].view(np.uint32)[0]) == int(bm[g])
+        q = 32
+        for t in range(nin):
+            s = 32 * g + t
+            ln = min(cb, n - s * cb)
+            p = (int(bm[g]) >> t) & 1
+            blen = (B - m) if p else 8 * ln
+            sb = np.unpackbits(slots[s * cb: s * cb + ln], bitorder="little")
+            assert np.array_equal(sb[:blen], pbits[q:q + blen]), (s, p)
+            rb = O.ibp_slot_read_bytes(meta, p, ln)
+            assert rb == (4 * ((B - m + 31) // 32) if p else ln)
+            if p:
+                assert not sb[blen:8 * rb].any()  # zero bits up to the word
+                assert np.array_equal(slots[s * cb + rb: s * cb + ln], x[s * cb + rb: s * cb + ln])
+            q += blen
+
+
+@pytest.mark.parametrize("cb,frac", [(64, 0.3), (512, 0.12), (20, 0.5), (32, 1.0), (16, 0.0)])
+def test_slots_gather_round_trip(cb, frac):
+    meta, x = _slot_case(cb, frac, 150, 7 + cb, tail=4 if cb > 4 else 0)
+    n = x.size
+    nch = (n + cb - 1) // cb
+    slots, bm = O.ibp_slots_encode(meta, x)
+    rng = np.random.default_rng(cb)
+    idx = np.concatenate([rng.integers(0, nch, 200), [nch - 1, 0, nch - 1]])
+    rows, read = O.ibp_slots_gather(meta, slots, n, bm, idx)
+    want_read = 0
+    for i, s in enumerate(idx):
+        ln = min(cb, n - s * cb)
+        assert np.array_equal(rows[i, :ln], x[s * cb: s * cb + ln]), s
+        p = (int(bm[s // 32]) >> (s % 32)) & 1
+        want_read += O.ibp_slot_read_bytes(meta, p, ln)
+    assert read == want_read
+    # reading a compressed slot reads less than the raw chunk exactly when
+    # m >= 32 (whole words dropped)
+    m = int(meta[16:20].view(np.uint32)[0])
+    if m >= 32 and bm.any():
+        assert read < sum(min(cb, n - s * cb) for s in idx)

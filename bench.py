@@ -678,6 +678,86 @@ def _case(kind, nbytes, dev, ibp_mode):
     return ops, (mws, iws, dws), 4 * n, ns * cb, check, nb, cb
 
 
+def slots_arm(args):
+    """IBP in-place slots on the 1,000,000 x 128 table (joint metadata, where
+    most rows are stored compressed): ibp_slots_compress from the device
+    table into pinned host slots, and ibp_slots_gather of 100,000 random rows
+    from them.  Beside it, the host link measured in the same run: the copy
+    engine (a pinned -> device copy of the whole table) and the same gather
+    kernel on raw slots (metadata without invariant bits: every slot a plain
+    row copy over the link).  GB/s of uncompressed bytes delivered; link GB/s
+    = bytes read from host memory / time."""
+    import torch
+
+    from lossless_bit_level_bf16_gb300 import abi, ibp as I, workloads as W
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    cb = 512
+    rows, idx = W.ibp_table(device=dev)
+    n = rows.numel() * 4
+    meta = I.build_meta(rows[idx].contiguous(), cb, T=0.9, mode=args.ibp_mode)
+    rnd = torch.randint(-2**31, 2**31 - 1, (10_000, cb // 4), dtype=torch.int32, device=dev)
+    meta_raw = I.build_meta(rnd, cb, T=1.0, mode=0)  # no position is invariant: m = 0
+    slots = torch.empty(rows.numel(), dtype=torch.float32).pin_memory()
+    slots_raw = torch.empty(rows.numel(), dtype=torch.float32).pin_memory()
+    bm = torch.zeros((n // cb + 31) // 32, dtype=torch.int32, device=dev)
+    bm_raw = torch.zeros_like(bm)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    gws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    K = 100_000
+    g = torch.Generator(device=dev).manual_seed(7)
+    pick = torch.randint(0, rows.shape[0], (K,), generator=g, device=dev)
+    out = torch.empty(K, cb // 4, dtype=torch.float32, device=dev)
+    rb = torch.zeros(1, dtype=torch.int64, device=dev)
+    rb_raw = torch.zeros(1, dtype=torch.int64, device=dev)
+    I.slots_compress(meta_raw, rows, cb, slots=slots_raw, bitmask=bm_raw, ws=ws)
+    dtab = torch.empty(rows.numel(), dtype=torch.float32, device=dev)
+    ops = [("ibp_slots_compress", lambda: I.slots_compress(meta, rows, cb, slots=slots, bitmask=bm,
+                                                           ws=ws)),
+           ("ibp_slots_gather", lambda: I.slots_gather(meta, slots, n, cb, bm, pick, out=out,
+                                                       read_bytes=rb, ws=gws)),
+           ("gather_raw_slots", lambda: I.slots_gather(meta_raw, slots_raw, n, cb, bm_raw, pick,
+                                                       out=out, read_bytes=rb_raw, ws=gws)),
+           ("dma_copy_table", lambda: dtab.copy_(slots_raw, non_blocking=True))]
+    ms = _time_ops(ops, flush, stream, max(3, args.warmup), args.steps)
+    for w in (ws, gws):
+        st = abi.status(w)
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {abi.strerror(st)}")
+    I.slots_gather(meta, slots, n, cb, bm, pick, out=out, read_bytes=rb, ws=gws)
+    torch.cuda.synchronize()
+    if not torch.equal(out.view(torch.int32), rows[pick].view(torch.int32)):
+        raise RuntimeError("gathered rows differ from the table")
+    import numpy as np
+    compressed = int(np.unpackbits(bm.cpu().numpy().view(np.uint8)).sum())
+    link = {"dma_pinned_to_device_GBps": round(n / (ms["dma_copy_table"] * 1e-3) / 1e9, 1),
+            "gather_raw_slots_link_GBps": round(int(rb_raw.item()) / (ms["gather_raw_slots"] * 1e-3)
+                                                / 1e9, 1)}
+    res = {}
+    for name in ("ibp_slots_compress", "ibp_slots_gather", "gather_raw_slots"):
+        t = ms[name]
+        if name == "ibp_slots_compress":
+            unc, host = n, None  # reads the device table, writes the host slots
+        else:
+            unc = K * cb
+            host = int((rb if name == "ibp_slots_gather" else rb_raw).item())
+        res[name] = {"ms": round(t, 4), "GBps_uncompressed": round(unc / (t * 1e-3) / 1e9, 1)}
+        if host is not None:
+            res[name]["host_bytes_read"] = host
+            res[name]["link_GBps"] = round(host / (t * 1e-3) / 1e9, 1)
+            res[name]["frac_of_raw_gather_link"] = round(
+                host / (t * 1e-3) / 1e9 / link["gather_raw_slots_link_GBps"], 4)
+    line = {"sweep": "table_slots", "bytes": n, "rows_gathered": K,
+            "ibp_mode": args.ibp_mode, "slots_compressed": compressed, "ops": res,
+            "host_link": link,
+            "speedup_vs_raw_gather": round(ms["gather_raw_slots"] / ms["ibp_slots_gather"], 4),
+            "config": {"chunk": cb, "warmup": args.warmup, "steps": args.steps,
+                       "slots": "pinned host memory", "l2": "flushed before every launch"}}
+    print(json.dumps(line), flush=True)
+
+
 def sweep_arm(args):
     """Per-op throughput, one JSON line per workload and size.
 
@@ -699,6 +779,8 @@ def sweep_arm(args):
     peak, peak_kind = _peaks()
     sizes = [int(float(v) * (1 << 20)) for v in args.sizes.split(",")] if args.sizes \
         else list(W.SWEEP_BYTES)
+    if args.codec == "table_slots":
+        return slots_arm(args)
     kinds = {"both": ["zipccl", "ibp"]}.get(args.codec, [args.codec])
     for kind in kinds:
         for nbytes in (sizes if kind in ("zipccl", "ibp", "ibp16") else [0]):
@@ -889,7 +971,7 @@ def main():
                     help="size sweep of both codecs instead of the step (one line per size)")
     ap.add_argument("--codec", default="both",
                     choices=["both", "zipccl", "ibp", "ibp16", "table", "table_host", "gradient",
-                             "moe"])
+                             "moe", "table_slots"])
     ap.add_argument("--sizes", default="", help="sweep sizes in MiB, comma separated")
     ap.add_argument("--ibp-mode", type=int, default=0, choices=[0, 1])
     ap.add_argument("--only", default="", help="sweep: time only these ops (comma separated)")

@@ -256,6 +256,52 @@ int ibp_decompress(const void* d_meta, uint32_t chunk_bytes, const void* d_in,
                    uint64_t in_bytes, void* d_y, uint64_t y_cap, void* d_ws,
                    size_t ws_bytes, zc_stream_t stream);
 
+/* ======================================================== IBP in-place slots
+ *
+ * [IBP] Integrazione del Sistema (PCIe transfer compression): tensors are
+ * compressed in CPU memory before they are transferred; a compressed tensor
+ * stays in place in a buffer of fixed size, of which only the compressed
+ * part is read, and a bitmask in GPU memory records which tensors are
+ * compressed.  Here a tensor is one chunk: chunk s of the data owns the slot
+ * of chunk_bytes at d_slots + s * chunk_bytes (the last slot is as long as
+ * the last chunk, a multiple of 4 bytes).  A compressed slot -- the chunk's
+ * participation bit of [IBP] step 2 is set -- starts with the chunk's body
+ * (its B - m kept bits in ascending position order, LSB first, zero bits up
+ * to a whole 32-bit word: 4*ceil((B - m)/32) bytes) and its later bytes are
+ * not written; every other slot holds the raw chunk.  Bit s % 32 of
+ * d_bitmask word s / 32 is set when slot s is compressed (the same bits as
+ * the IBP1 stream's group participation words).
+ */
+
+/* Write the slot form of the n_bytes (a multiple of 4) at d_x into d_slots
+ * (n_bytes long; d_x may be d_slots itself: compression in place, each chunk
+ * read whole before its slot is written; otherwise the two must not overlap)
+ * and the bitmask into d_bitmask (ceil(ceil(n_bytes/chunk_bytes)/32) words,
+ * device memory).  d_x and d_slots may be pinned host memory, read and
+ * written in place over the host link ([IBP] step 2: the GPU compresses
+ * through zero-copy access to CPU memory); other host memory returns
+ * ZC_ERR_ARG.  4-byte alignment.  d_ws: 256 bytes (status word).  One memset
+ * and one kernel; metadata made for another chunk size sets
+ * ZC_ERR_META_MISMATCH. */
+int ibp_slots_compress(const void* d_meta, uint32_t chunk_bytes, const void* d_x,
+                       uint64_t n_bytes, void* d_slots, uint32_t* d_bitmask,
+                       void* d_ws, size_t ws_bytes, zc_stream_t stream);
+
+/* Gather: row i of d_y (chunk_bytes each; a short last chunk fills only its
+ * length) receives chunk d_idx[i] (u64 slot indices, device memory, any
+ * order, repeats allowed), read from its slot -- only the slot's stored part
+ * -- and decoded ([IBP] step 3: a warp reads the segment from CPU memory into
+ * shared memory and puts the Bitval bits back).  d_slots may be pinned host
+ * memory; d_y device or pinned host memory.  *d_read_bytes (device, may be
+ * NULL) receives the bytes read from the slots.  An index past the last
+ * chunk sets ZC_ERR_ARG in the status word and its row is not written; a set
+ * bit on a slot that cannot hold a body (the short last one, or m = 0) sets
+ * ZC_ERR_FORMAT.  Up to two memsets and one kernel. */
+int ibp_slots_gather(const void* d_meta, uint32_t chunk_bytes, const void* d_slots,
+                     uint64_t n_bytes, const uint32_t* d_bitmask, const uint64_t* d_idx,
+                     uint64_t n_idx, void* d_y, uint64_t* d_read_bytes, void* d_ws,
+                     size_t ws_bytes, zc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

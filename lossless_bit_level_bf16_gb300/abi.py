@@ -50,6 +50,10 @@ SIGNATURES = {
                                C.c_size_t, _vp]),
     "ibp_decompress": (C.c_int, [_vp, C.c_uint32, _vp, C.c_uint64, _vp, C.c_uint64, _vp,
                                  C.c_size_t, _vp]),
+    "ibp_slots_compress": (C.c_int, [_vp, C.c_uint32, _vp, C.c_uint64, _vp, _vp, _vp, C.c_size_t,
+                                     _vp]),
+    "ibp_slots_gather": (C.c_int, [_vp, C.c_uint32, _vp, C.c_uint64, _vp, _vp, C.c_uint64, _vp,
+                                   _vp, _vp, C.c_size_t, _vp]),
 }
 
 

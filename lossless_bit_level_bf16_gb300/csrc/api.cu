@@ -370,4 +370,45 @@ int ibp_decompress(const void* d_meta, uint32_t cb, const void* d_in, uint64_t i
                                             (cudaStream_t)stream, in_host));
 }
 
+int ibp_slots_compress(const void* d_meta, uint32_t cb, const void* d_x, uint64_t n_bytes,
+                       void* d_slots, uint32_t* d_bitmask, void* d_ws, size_t ws_bytes,
+                       zc_stream_t stream) {
+  if (!d_meta || !d_slots || !d_bitmask || !d_ws || (!d_x && n_bytes) || !ibp_chunk_ok(cb) ||
+      (n_bytes % 4) != 0)
+    return ZC_ERR_ARG;
+  if (!aligned(d_meta, 16) || !aligned(d_x, 4) || !aligned(d_slots, 4) || !aligned(d_bitmask, 4) ||
+      !aligned(d_ws, 256))
+    return ZC_ERR_ARG;
+  if (ws_bytes < kCtrlBytes) return ZC_ERR_CAPACITY;
+  // the input is the slots themselves (compression in place) or apart from them
+  const char* xb = static_cast<const char*>(d_x);
+  const char* sb = static_cast<const char*>(d_slots);
+  if (xb != sb && xb < sb + n_bytes && sb < xb + n_bytes) return ZC_ERR_ARG;
+  bool x_host = false, s_host = false;
+  const void* sl = d_slots;
+  if (!reachable(&d_x, &x_host) || !reachable(&sl, &s_host)) return ZC_ERR_ARG;
+  if (xb == sb) d_x = sl;  // the same memory, by its device-side address
+  return cuda_rc(lbb::ibp_launch_slots_compress(d_meta, cb, d_x, n_bytes, const_cast<void*>(sl),
+                                                d_bitmask, d_ws, (cudaStream_t)stream));
+}
+
+int ibp_slots_gather(const void* d_meta, uint32_t cb, const void* d_slots, uint64_t n_bytes,
+                     const uint32_t* d_bitmask, const uint64_t* d_idx, uint64_t n_idx, void* d_y,
+                     uint64_t* d_read_bytes, void* d_ws, size_t ws_bytes, zc_stream_t stream) {
+  if (!d_meta || !d_slots || !d_bitmask || !d_ws || (!d_idx && n_idx) || (!d_y && n_idx) ||
+      !ibp_chunk_ok(cb) || (n_bytes % 4) != 0)
+    return ZC_ERR_ARG;
+  if (!aligned(d_meta, 16) || !aligned(d_slots, 4) || !aligned(d_bitmask, 4) ||
+      !aligned(d_idx, 8) || !aligned(d_y, 4) || !aligned(d_read_bytes, 8) || !aligned(d_ws, 256))
+    return ZC_ERR_ARG;
+  if (ws_bytes < kCtrlBytes) return ZC_ERR_CAPACITY;
+  bool s_host = false, y_host = false;
+  const void* yo = d_y;
+  if (!reachable(&d_slots, &s_host) || !reachable(&yo, &y_host)) return ZC_ERR_ARG;
+  return cuda_rc(lbb::ibp_launch_slots_gather(
+      d_meta, cb, d_slots, n_bytes, d_bitmask, reinterpret_cast<const unsigned long long*>(d_idx),
+      n_idx, const_cast<void*>(yo), reinterpret_cast<unsigned long long*>(d_read_bytes), d_ws,
+      (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -58,25 +58,6 @@ __device__ __forceinline__ uint32_t owned_word(int lane, int j) {
   return (uint32_t)(32 * j + lane);
 }
 
-// OR k (1..32) bits of v into the bit string at bit position pos.
-__device__ __forceinline__ void put_bits(uint32_t* buf, unsigned long long pos, uint32_t v,
-                                         uint32_t k) {
-  const uint32_t wi = (uint32_t)(pos >> 5), sh = (uint32_t)(pos & 31);
-  if (sh == 0 && k == 32) {
-    buf[wi] = v;  // the whole word belongs to this fragment
-    return;
-  }
-  atomicOr(buf + wi, v << sh);
-  if (sh + k > 32) atomicOr(buf + wi + 1, v >> (32 - sh));
-}
-
-__device__ __forceinline__ uint32_t get_bits(const uint32_t* buf, unsigned long long pos,
-                                             uint32_t k) {
-  const uint32_t wi = (uint32_t)(pos >> 5), sh = (uint32_t)(pos & 31);
-  const uint32_t v = __funnelshift_r(buf[wi], buf[wi + 1], sh);
-  return k >= 32 ? v : (v & ((1u << k) - 1u));
-}
-
 template <int VEC, int WPL, int CPW>
 __global__ void __launch_bounds__(32 * (32 / CPW)) ibp_encode_kernel(IbpEncArgs A) {
   constexpr int NT = 32 * (32 / CPW);

@@ -64,6 +64,28 @@ __device__ __forceinline__ uint32_t hd_expand(uint32_t x, uint32_t k, const uint
   return x & k;
 }
 
+// OR k (1..32) bits of v into the shared-memory bit string at bit position
+// pos (words the fragment shares with others take an atomic OR).
+__device__ __forceinline__ void put_bits(uint32_t* buf, unsigned long long pos, uint32_t v,
+                                         uint32_t k) {
+  const uint32_t wi = (uint32_t)(pos >> 5), sh = (uint32_t)(pos & 31);
+  if (sh == 0 && k == 32) {
+    buf[wi] = v;  // the whole word belongs to this fragment
+    return;
+  }
+  atomicOr(buf + wi, v << sh);
+  if (sh + k > 32) atomicOr(buf + wi + 1, v >> (32 - sh));
+}
+
+// k (1..32) bits of a bit string from bit position pos (the word after the
+// one holding pos must be readable).
+__device__ __forceinline__ uint32_t get_bits(const uint32_t* buf, unsigned long long pos,
+                                             uint32_t k) {
+  const uint32_t wi = (uint32_t)(pos >> 5), sh = (uint32_t)(pos & 31);
+  const uint32_t v = __funnelshift_r(buf[wi], buf[wi + 1], sh);
+  return k >= 32 ? v : (v & ((1u << k) - 1u));
+}
+
 // Per-word tables of one chunk layout, in shared memory:
 //   K[w]  keep mask (~Mask word)      V[w]  Bitval word (zero outside Mask)
 //   P[w]  kept bits in words < w      MV[i*W + w]  move masks of round i

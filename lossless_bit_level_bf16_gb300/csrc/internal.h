@@ -100,6 +100,18 @@ cudaError_t ibp_launch_decompress(const void* d_meta, uint32_t chunk_bytes,
                                   void* d_y, unsigned long long y_cap,
                                   void* d_ws, cudaStream_t s, bool in_host);
 
+// IBP in-place slots (ibp_slots.cu): the slot form of every chunk of d_x
+// (which may be d_slots itself) and the bitmask of compressed slots; the
+// gather of the chunks d_idx[0..n_idx) from their slots into rows of d_y.
+cudaError_t ibp_launch_slots_compress(const void* d_meta, uint32_t chunk_bytes, const void* d_x,
+                                      unsigned long long n_bytes, void* d_slots,
+                                      uint32_t* d_bitmask, void* d_ws, cudaStream_t s);
+cudaError_t ibp_launch_slots_gather(const void* d_meta, uint32_t chunk_bytes, const void* d_slots,
+                                    unsigned long long n_bytes, const uint32_t* d_bitmask,
+                                    const unsigned long long* d_idx, unsigned long long n_idx,
+                                    void* d_y, unsigned long long* d_read_bytes, void* d_ws,
+                                    cudaStream_t s);
+
 // TMA-pipelined IBP kernels (ibp_pipe.cu) for chunks of up to 2048 bytes;
 // the launchers above use them whenever ibp_pipe_supported says so.
 bool ibp_pipe_supported(uint32_t chunk_bytes, bool encode);

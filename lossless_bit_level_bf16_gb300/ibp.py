@@ -115,5 +115,57 @@ def decompress(meta: torch.Tensor, stream_bytes: torch.Tensor, n_bytes: int, chu
     return out
 
 
+def slots_compress(meta: torch.Tensor, x: torch.Tensor, chunk_bytes: int,
+                   slots: torch.Tensor | None = None, bitmask: torch.Tensor | None = None,
+                   ws: torch.Tensor | None = None, stream=None):
+    """ibp_slots_compress: the in-place slot form of ``x`` and the bitmask of
+    compressed slots.  ``slots`` defaults to ``x`` itself (compression in
+    place); either may be pinned host memory.  Returns (slots, bitmask int32
+    CUDA tensor)."""
+    lib = abi.load()
+    x = _reachable(x, "x")
+    slots = x if slots is None else _reachable(slots, "slots")
+    dev = meta.device
+    n_bytes = x.numel() * x.element_size()
+    nch = (n_bytes + chunk_bytes - 1) // chunk_bytes
+    if bitmask is None:
+        bitmask = torch.zeros(max(1, (nch + 31) // 32), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    abi.check(lib.ibp_slots_compress(abi.ptr(meta), chunk_bytes, abi.ptr(x), n_bytes,
+                                     abi.ptr(slots), abi.ptr(bitmask), abi.ptr(ws), ws.numel(),
+                                     abi.stream_handle(stream)), "ibp_slots_compress")
+    bitmask._lbb_ws = ws
+    return slots, bitmask
+
+
+def slots_gather(meta: torch.Tensor, slots: torch.Tensor, n_bytes: int, chunk_bytes: int,
+                 bitmask: torch.Tensor, idx: torch.Tensor, out: torch.Tensor | None = None,
+                 read_bytes: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                 stream=None, dtype=torch.float32):
+    """ibp_slots_gather: chunks ``idx`` (int64 CUDA tensor) decoded from their
+    slots into rows [len(idx), chunk_bytes] viewed as ``dtype`` (or into
+    ``out``).  Returns (rows, read_bytes int64[1])."""
+    lib = abi.load()
+    _reachable(slots, "slots")
+    idx = _dev_tensor(idx, "idx")
+    if idx.dtype != torch.int64:
+        raise ValueError("idx must be int64")
+    dev = meta.device
+    if out is None:
+        esize = torch.empty(0, dtype=dtype).element_size()
+        out = torch.zeros(idx.numel(), chunk_bytes // esize, dtype=dtype, device=dev)
+    if read_bytes is None:
+        read_bytes = torch.zeros(1, dtype=torch.int64, device=dev)
+    if ws is None:
+        ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    abi.check(lib.ibp_slots_gather(abi.ptr(meta), chunk_bytes, abi.ptr(slots), n_bytes,
+                                   abi.ptr(bitmask), abi.ptr(idx), idx.numel(), abi.ptr(out),
+                                   abi.ptr(read_bytes), abi.ptr(ws), ws.numel(),
+                                   abi.stream_handle(stream)), "ibp_slots_gather")
+    out._lbb_ws = ws
+    return out, read_bytes
+
+
 def status(ws: torch.Tensor, stream=None) -> int:
     return abi.status(ws, stream)

@@ -63,7 +63,7 @@ def lib():
                                         u8p, C.c_uint64, u64p, u8p, dp, dp]),
             "ora_zc_decode": (C.c_int, [u8p, C.c_uint64, u16p, C.c_uint64, u64p]),
             "ora_zc_encode_chunk": (C.c_int, [u16p, C.c_uint32, C.c_uint32, u8p, u8p, u8p,
-                                              C.POINTER(C.c_uint32)]),
+                                              C.POINTER(C.c_uint32), C.POINTER(C.c_int)]),
             "ora_ibp_meta_bytes": (C.c_uint64, [C.c_uint32]),
             "ora_fnv1a64": (C.c_uint64, [u8p, C.c_size_t]),
             "ora_ibp_build_meta": (C.c_int, [u8p, C.c_uint64, C.c_uint32, C.c_double, C.c_int, u8p]),
@@ -172,15 +172,18 @@ def zc_decode(stream, y_cap=None):
 
 
 def zc_encode_chunk(x, chunk_elems, book):
+    """Returns (slot, dynamic bytes, raw flag) of one chunk."""
     x = np.ascontiguousarray(x, dtype=np.uint16).reshape(-1)
     book = np.ascontiguousarray(book, dtype=np.uint8)
     slot = np.zeros(chunk_elems * 11 // 8, np.uint8)
     esc = np.zeros(chunk_elems, np.uint8)
     ne = C.c_uint32()
+    raw = C.c_int()
     rc = lib().ora_zc_encode_chunk(_p(x, C.c_uint16), x.size, chunk_elems, _p(book, C.c_uint8),
-                                   _p(slot, C.c_uint8), _p(esc, C.c_uint8), C.byref(ne))
+                                   _p(slot, C.c_uint8), _p(esc, C.c_uint8), C.byref(ne),
+                                   C.byref(raw))
     _chk(rc, "zc_encode_chunk")
-    return slot, esc[: ne.value].copy()
+    return slot, esc[: ne.value].copy(), bool(raw.value)
 
 
 # ------------------------------------------------------------------ IBP

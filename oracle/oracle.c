@@ -77,13 +77,20 @@ static double bf16_value(uint16_t v) {
  *    40 esc_bytes (all u64)  48 u8 book[7] ascending  55..63 zero
  *     region padded with zeros to a multiple of 128 bytes
  *   chunk escape-offset table at off_escoff: u64 x (nchunks+1), exclusive
- *     prefix of per-chunk escape counts; padded to 128 bytes
- *   static region at off_static: one slot of 11*C/8 bytes per chunk:
+ *     prefix of per-chunk dynamic byte counts (bits 62..0); bit 63 of entry c
+ *     (c < nchunks) set when chunk c is stored raw; padded to 128 bytes
+ *   static region at off_static: one slot of S = 11*C/8 bytes per chunk:
  *     [C sign+mantissa bytes][plane 0: C bits][plane 1][plane 2]
  *     bit i (LSB first within bytes) of plane k is bit k of element i's code
- *   escape region at off_esc: the 8-bit exponent fields of escaped elements,
- *     chunk by chunk, element order; zero padded to 128 bytes.
+ *   escape (dynamic) region at off_esc: per chunk, in chunk order, the 8-bit
+ *     exponent fields of its escaped elements (element order); zero padded to
+ *     128 bytes at the end.
  *   Elements past the end of a segment's last chunk: byte 0, code 0, no escape.
+ *   Raw fallback: a full chunk (L = C) with more escapes than the 5C/8 bytes
+ *     its raw form puts past the slot is stored raw: its 2C bytes (the bf16
+ *     values, little-endian) fill the slot first and their last 5C/8 bytes
+ *     are the chunk's dynamic part, so no full chunk takes more than 2C
+ *     bytes.  A segment's short last chunk is always coded.
  */
 
 #define ZC_MAGIC 0x3143435Au
@@ -224,7 +231,7 @@ static unsigned zc_code_of(unsigned e, const uint8_t book[7]) {
 
 int ora_zc_encode_chunk(const uint16_t* x, uint32_t L, uint32_t C,
                         const uint8_t book[7], uint8_t* slot, uint8_t* esc,
-                        uint32_t* n_esc) {
+                        uint32_t* n_esc, int* raw) {
   if (C < 1024u || (C % 1024u) != 0 || L > C) return ORA_E_ARG;
   uint64_t S = zc_slot_bytes(C);
   memset(slot, 0, S);
@@ -240,6 +247,18 @@ int ora_zc_encode_chunk(const uint16_t* x, uint32_t L, uint32_t C,
     unsigned code = zc_code_of(e, book);
     for (int k = 0; k < 3; ++k) set_bit(plane[k], i, (code >> k) & 1u);
     if (code == 0) esc[ne++] = (uint8_t)e;
+  }
+  /* raw fallback for a full chunk: fewer dynamic bytes than the escapes */
+  const uint64_t raw_bytes = 2ull * L;
+  const uint64_t raw_dyn = raw_bytes - S; /* 5C/8 when L = C */
+  *raw = L == C && raw_dyn < ne;
+  if (*raw) {
+    for (uint64_t b = 0; b < raw_bytes; ++b) {
+      const uint8_t byte = (uint8_t)(x[b / 2] >> (8 * (b % 2)));
+      if (b < S) slot[b] = byte;
+      else esc[b - S] = byte;
+    }
+    ne = (uint32_t)raw_dyn;
   }
   *n_esc = ne;
   return ORA_OK;
@@ -265,7 +284,7 @@ int ora_zc_encode(const uint16_t* x, uint64_t n, const uint64_t* seg_off,
   memset(out, 0, off_esc);
 
   uint8_t* slot = (uint8_t*)malloc(S);
-  uint8_t* esc = (uint8_t*)malloc(C);
+  uint8_t* esc = (uint8_t*)malloc(C);  /* escapes, or a raw chunk's remainder (< C) */
   if (!slot || !esc) {
     free(slot);
     free(esc);
@@ -302,8 +321,9 @@ int ora_zc_encode(const uint16_t* x, uint64_t n, const uint64_t* seg_off,
       uint64_t first = b + j * C;
       uint32_t L = (uint32_t)((e - first) < C ? (e - first) : C);
       uint32_t ne = 0;
-      ora_zc_encode_chunk(x + first, L, C, book, slot, esc, &ne);
-      wr64(out + off_escoff + 8u * chunk, esc_total);
+      int raw = 0;
+      ora_zc_encode_chunk(x + first, L, C, book, slot, esc, &ne, &raw);
+      wr64(out + off_escoff + 8u * chunk, esc_total | ((uint64_t)raw << 63));
       memcpy(out + off_static + chunk * S, slot, S);
       if (off_esc + esc_total + ne > cap) {
         free(slot);
@@ -382,9 +402,28 @@ int ora_zc_decode(const uint8_t* in, uint64_t in_bytes, uint16_t* y,
       uint64_t L = (b + len - first) < C ? (b + len - first) : C;
       const uint8_t* slot = in + off_static + chunk * S;
       const uint8_t* plane[3] = {slot + C, slot + C + C / 8, slot + C + 2 * (C / 8)};
-      uint64_t ep = rd64(in + off_escoff + 8u * chunk);
-      uint64_t ep_end = rd64(in + off_escoff + 8u * (chunk + 1));
+      const uint64_t e0 = rd64(in + off_escoff + 8u * chunk);
+      const uint64_t e1 = rd64(in + off_escoff + 8u * (chunk + 1));
+      const int raw = (int)(e0 >> 63);
+      uint64_t ep = e0 & ~(1ull << 63);
+      uint64_t ep_end = e1 & ~(1ull << 63);
+      if (chunk + 1 == nchunks && (e1 >> 63)) return ORA_E_FORMAT;
       if (ep > ep_end || ep_end > esc_total) return ORA_E_FORMAT;
+      if (raw) {
+        /* the raw fallback: 2C bytes, the slot's first, then the remainder */
+        const uint64_t rb = 2ull * L, rd = rb - S;
+        if (L != C || ep_end - ep != rd) return ORA_E_FORMAT;
+        for (uint64_t i = 0; i < L; ++i) {
+          uint16_t v = 0;
+          for (uint64_t h = 0; h < 2; ++h) {
+            const uint64_t bb = 2 * i + h;
+            const uint8_t byte = bb < S ? slot[bb] : in[off_esc + ep + (bb - S)];
+            v |= (uint16_t)((unsigned)byte << (8 * h));
+          }
+          y[first + i] = v;
+        }
+        continue;
+      }
       for (uint64_t i = 0; i < L; ++i) {
         unsigned smb = slot[i];
         unsigned code = 0;

@@ -86,11 +86,11 @@ int ora_zc_decode(const uint8_t* in, uint64_t in_bytes, uint16_t* y,
                   uint64_t y_cap, uint64_t* n_out);
 
 /* One chunk on its own: L real elements (L <= C), the static slot (11*C/8
- * bytes) and the chunk's escape bytes (at most L).  Used to check sampled
- * chunks of streams too large to re-encode whole. */
+ * bytes) and the chunk's dynamic bytes (escapes, or a raw chunk's last 5C/8
+ * bytes); *raw is set when the (full) chunk is stored raw. */
 int ora_zc_encode_chunk(const uint16_t* x, uint32_t L, uint32_t chunk_elems,
                         const uint8_t book[7], uint8_t* slot, uint8_t* esc,
-                        uint32_t* n_esc);
+                        uint32_t* n_esc, int* raw);
 
 /* ---------------- IBP invariant bit packing ---------------- */
 

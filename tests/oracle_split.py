@@ -64,7 +64,10 @@ def zc_stream_equal(stream, x_bits, chunk, book, pieces=None):
     assert int(h[0]) == n and int(h[1]) == nchunks, (h[0], h[1])
     off_seg, off_escoff, off_static, off_esc = (int(v) for v in h[3:7])
     assert off_esc == off_static + nchunks * S
-    eo = _u64(st, off_escoff, nchunks + 1).astype(np.int64)
+    # bit 63 of an entry marks a chunk stored raw; bits 62..0 are the offset
+    eo_all = _u64(st, off_escoff, nchunks + 1)
+    eo_raw = (eo_all >> np.uint64(63)).astype(np.int64)
+    eo = (eo_all & np.uint64((1 << 63) - 1)).astype(np.int64)
     if nchunks == 0:
         ref, _, _, _ = O.zc_encode(x, None, C, books=book)
         assert np.array_equal(st, ref)
@@ -82,9 +85,12 @@ def zc_stream_equal(stream, x_bits, chunk, book, pieces=None):
         if not np.array_equal(st[off_static + c0 * S: off_static + c1 * S],
                               ps[p_static: p_static + k * S]):
             bad.append("slots")
-        p_eo = _u64(ps, p_escoff, k + 1).astype(np.int64)
+        p_all = _u64(ps, p_escoff, k + 1)
+        p_eo = (p_all & np.uint64((1 << 63) - 1)).astype(np.int64)
         if not np.array_equal(eo[c0:c1 + 1] - eo[c0], p_eo):
             bad.append("escape offsets")
+        if not np.array_equal(eo_raw[c0:c1], (p_all[:k] >> np.uint64(63)).astype(np.int64)):
+            bad.append("raw-chunk flags")
         base = int(eo[c0])
         if not np.array_equal(st[off_esc + base: off_esc + base + p_n_esc],
                               ps[p_esc: p_esc + p_n_esc]):
@@ -101,7 +107,7 @@ def zc_stream_equal(stream, x_bits, chunk, book, pieces=None):
         assert head == bytes(st[:16]), "magic, version, header size, chunk, segments"
         assert pbook == bytes(st[off_seg + 48: off_seg + 55]) == bytes(book)
         esc += ne
-    assert int(eo[nchunks]) == esc and int(h[2]) == esc
+    assert int(eo[nchunks]) == esc and int(h[2]) == esc and eo_raw[nchunks] == 0
     total = O.zc_stream_bytes(n, None, C, esc)
     assert st.size == total and int(h[7]) == total, (st.size, total)
     rec = _u64(st, off_seg, 6)

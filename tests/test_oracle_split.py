@@ -27,6 +27,22 @@ def test_zc_split_accepts_oracle_stream(pieces):
     assert esc == int(ref[32:40].view(np.uint64)[0]) > 0
 
 
+def test_zc_split_with_raw_chunks():
+    rng = np.random.default_rng(8)
+    C = 1024
+    x = _bf16(rng.normal(0, 0.01, size=12 * C + 5))
+    x[3 * C:4 * C] = rng.integers(0, 65536, size=C).astype(np.uint16)  # stored raw
+    x[7 * C:8 * C] = 0x7FC0
+    book = np.arange(115, 122, dtype=np.uint8)
+    ref, _, _, _ = O.zc_encode(x, None, C, books=book)
+    zc_stream_equal(ref, x, C, book, pieces=5)
+    off_escoff = int(ref[48:56].view(np.uint64)[0])
+    bad = ref.copy()
+    bad[off_escoff + 8 * 3 + 7] ^= 0x80  # the raw flag of chunk 3
+    with pytest.raises(AssertionError):
+        zc_stream_equal(bad, x, C, book, pieces=5)
+
+
 def test_zc_split_rejects_any_changed_byte():
     rng = np.random.default_rng(5)
     C = 1024

@@ -34,6 +34,18 @@ def _bf16_round(f32):
 
 # ---------------------------------------------------------------- format pins
 
+def _dynamic_bytes(x, C, book):
+    """Dynamic-region bytes of a one-segment stream, chunk by chunk: the
+    escape count, or for a full chunk the raw form's remainder 5C/8 when that
+    is smaller (the raw fallback)."""
+    tot = 0
+    for c0 in range(0, x.size, C):
+        xc = x[c0:c0 + C]
+        ne = int(np.count_nonzero(~np.isin(_fields(xc), book)))
+        tot += min(ne, 5 * C // 8) if xc.size == C else ne
+    return tot
+
+
 def test_golden_tiny_stream():
     g = json.load(open(os.path.join(GOLD, "zc_tiny_stream.json")))
     x = np.array([int(h, 16) for h in g["input_u16_hex"]], np.uint16)
@@ -70,9 +82,8 @@ def test_bruteforce_every_bf16_pattern(C, bi):
         rc, y = O.zc_decode(st)
         assert rc == 0
         assert np.array_equal(y, x), "round trip must be bit-exact"
-        n_esc = int(np.count_nonzero(~np.isin(_fields(x), book)))
-        assert int(st[32:40].view(np.uint64)[0]) == n_esc
-        assert st.size == O.zc_stream_bytes(n, None, C, n_esc)
+        assert int(st[32:40].view(np.uint64)[0]) == _dynamic_bytes(x, C, book)
+        assert st.size == O.zc_stream_bytes(n, None, C, _dynamic_bytes(x, C, book))
 
 
 @pytest.mark.parametrize("C", [1024, 4096, 8192])
@@ -103,7 +114,8 @@ def test_chunk_entry_matches_stream():
     S = C * 11 // 8
     eo = st[off_escoff:off_escoff + 8 * 5].view(np.uint64)
     for c in range(4):
-        slot, esc = O.zc_encode_chunk(x[c * C:(c + 1) * C], C, book)
+        slot, esc, raw = O.zc_encode_chunk(x[c * C:(c + 1) * C], C, book)
+        assert not raw
         assert np.array_equal(slot, st[off_static + c * S: off_static + (c + 1) * S])
         assert np.array_equal(esc, st[off_esc + int(eo[c]): off_esc + int(eo[c + 1])])
 
@@ -333,3 +345,77 @@ def test_nonzero_mean_book_is_top7_of_scipy_masses(mu, sigma):
     assert gap > 1e-6, "case chosen away from a tie"
     want = np.sort(order[:7] + 1).astype(np.uint8)
     assert np.array_equal(O.zc_predict(mu, sigma), want)
+
+
+# ---------------------------------------------------------------- raw fallback
+
+@pytest.mark.parametrize("C", [1024, 3072, 4096])
+def test_raw_fallback_chunks(C):
+    """Full chunks whose escapes outnumber the raw form's remainder (5C/8
+    bytes) are stored raw: the bf16 values' bytes fill the slot, their last
+    5C/8 bytes are the chunk's dynamic part, bit 63 of its table entry is set;
+    such a chunk takes exactly 2C bytes.  A chunk with exactly 5C/8 escapes
+    stays coded, and so does the short last chunk, however many escapes it
+    has.  Mixed, the round trip stays exact."""
+    rng = np.random.default_rng(C)
+    book = np.arange(116, 123, dtype=np.uint8)
+    coded = _bf16_round(rng.normal(0, 0.01, size=C).astype(np.float32))
+    noise = rng.integers(0, 65536, size=C, dtype=np.uint32).astype(np.uint16)
+    edge = coded.copy()
+    S = 11 * C // 8
+    k = 5 * C // 8  # exactly as many escapes as the raw remainder: stays coded
+    edge[:k] = 0x7FC0
+    edge[k:] = np.where(np.isin(_fields(edge[k:]), book), edge[k:], 0x3C00 | (edge[k:] & 0x807F))
+    tail = noise[:300]  # short last chunk: coded whatever its escapes
+    x = np.concatenate([coded, noise, edge, noise[::-1], tail])
+    st, _, _, _ = O.zc_encode(x, chunk_elems=C, books=book)
+    rc, y = O.zc_decode(st)
+    assert rc == 0 and np.array_equal(y, x)
+    h = st[16:80].view(np.uint64)
+    off_escoff, off_static, off_esc = int(h[4]), int(h[5]), int(h[6])
+    eo = st[off_escoff:off_escoff + 8 * 6].view(np.uint64)
+    raw = [int(v) >> 63 for v in eo[:5]]
+    assert raw == [0, 1, 0, 1, 0] and int(eo[5]) >> 63 == 0
+    dyn = [int(eo[c + 1] & ~np.uint64(1 << 63)) - int(eo[c] & ~np.uint64(1 << 63)) for c in range(5)]
+    assert dyn[1] == dyn[3] == 5 * C // 8 and dyn[2] == k
+    assert dyn[4] == int(np.count_nonzero(~np.isin(_fields(tail), book))) > 0
+    for c in (1, 3):
+        xb = x[c * C:(c + 1) * C].view(np.uint8)
+        slot = st[off_static + c * S: off_static + (c + 1) * S]
+        assert np.array_equal(slot, xb[:S])
+        o = int(eo[c] & ~np.uint64(1 << 63))
+        assert np.array_equal(st[off_esc + o: off_esc + o + dyn[c]], xb[S:])
+    assert st.size == O.zc_stream_bytes(x.size, None, C, sum(dyn))
+    s2, d2, r2 = O.zc_encode_chunk(x[C:2 * C], C, book)
+    assert r2 and np.array_equal(s2, st[off_static + S: off_static + 2 * S]) and d2.size == 5 * C // 8
+
+
+def test_raw_fallback_bounds_expansion():
+    """Every value escaping (random bit patterns, a book none of them uses):
+    the stream is the raw bytes plus headers, tables and padding -- at most
+    19/16 of the input without the fallback, at most the input plus a few
+    hundred bytes with it."""
+    rng = np.random.default_rng(1)
+    C = 4096
+    x = rng.integers(0, 65536, size=40 * C + 17, dtype=np.uint32).astype(np.uint16)
+    x = np.where(np.isin(_fields(x), [0, 1, 2, 3, 4, 5, 6]), x | 0x0400, x).astype(np.uint16)
+    st, _, _, _ = O.zc_encode(x, chunk_elems=C, books=np.arange(7, dtype=np.uint8))
+    rc, y = O.zc_decode(st)
+    assert rc == 0 and np.array_equal(y, x)
+    fixed = O.zc_stream_bytes(x.size, None, C, 0)
+    assert st.size - fixed <= 40 * (5 * C // 8) + 17 + 128  # the 17-value tail is coded
+    assert st.size <= 2 * x.size + 11 * C // 8 + 1024
+
+
+def test_decode_rejects_bad_raw_flags():
+    rng = np.random.default_rng(4)
+    C = 1024
+    book = np.arange(116, 123, dtype=np.uint8)
+    x = np.concatenate([_bf16_round(rng.normal(0, 0.01, size=C).astype(np.float32)),
+                        rng.integers(0, 65536, size=C, dtype=np.uint32).astype(np.uint16)])
+    st, _, _, _ = O.zc_encode(x, chunk_elems=C, books=book)
+    off_escoff = int(st[48:56].view(np.uint64)[0])
+    for c in (0, 1, 2):  # flag a coded chunk, clear a raw one, flag the end entry
+        bad = st.copy()
+        bad[off_escoff + 8 * c + 7] ^= 0x80
+        assert O.zc_decode(bad)[0] == O.E_FORMAT, c

@@ -121,7 +121,9 @@ void zc_plan_destroy(zc_plan_t plan);
 /* Workspace bytes zc_plan and zc_compress need for this plan. */
 size_t zc_workspace_bytes(zc_plan_t plan);
 
-/* Upper bound of the stream size for this plan (every element escaped). */
+/* Upper bound of the stream size for this plan: the fixed part plus, per
+ * chunk, at most 5C/8 dynamic bytes (an incompressible full chunk is stored
+ * raw: 2C bytes in all) and one escape per element of a short last chunk. */
 uint64_t zc_max_compressed_bytes(zc_plan_t plan);
 
 /* Statistics and codebooks, [ZipCCL] 2.A: per segment, the count, sum and

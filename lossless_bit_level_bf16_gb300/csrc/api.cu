@@ -186,7 +186,8 @@ int zc_plan_create(uint64_t n, const uint64_t* h_seg_off, uint32_t nseg, uint32_
   }
   L.nchunks = chunks;
   L.nunits = units;
-  L.ntiles = (chunks * C + lbb::kTileLanes - 1) / lbb::kTileLanes;
+  const unsigned long long tl = lbb::zc_tile_slots(C);
+  L.ntiles = (chunks * C + tl - 1) / tl;
   L.slot_bytes = (unsigned long long)C * 11ull / 8ull;
   L.off_seg = lbb::kZcHeader;
   L.off_escoff = L.off_seg + lbb::round_up_dev((unsigned long long)lbb::kZcSegRec * nseg, lbb::kZcAlign);
@@ -221,7 +222,12 @@ size_t zc_workspace_bytes(zc_plan_t p) { return p ? zc_ws_bytes(p->L) : 0; }
 
 uint64_t zc_max_compressed_bytes(zc_plan_t p) {
   if (!p) return 0;
-  return p->L.off_esc + lbb::round_up_dev(p->L.n, lbb::kZcAlign);
+  // dynamic bytes: a full chunk at most 5C/8 (beyond that it is stored raw),
+  // a segment's short last chunk one escape per element
+  const unsigned long long C = p->L.C;
+  unsigned long long dyn = 0;
+  for (const lbb::ZcSegDev& r : p->h_segs) dyn += (r.nelem / C) * (5 * C / 8) + r.nelem % C;
+  return p->L.off_esc + lbb::round_up_dev(dyn, lbb::kZcAlign);
 }
 
 int zc_plan(zc_plan_t p, const uint16_t* d_x, void* d_ws, size_t ws_bytes, zc_stream_t stream) {

@@ -20,13 +20,20 @@ constexpr uint32_t kZcAlign = 128;
 constexpr uint32_t kTileLanes = 8192;   // lanes (element slots) per encoder tile
 constexpr unsigned long long kZcLbBlock = 128;  // tiles per look-back block
 
-// Chunks of C slots (a multiple of 1024) that one encoder tile of kTileLanes
-// slots, starting at a multiple of kTileLanes, can touch: one when tiles and
-// chunks align, kTileLanes / C when chunks divide the tile, else up to two
-// partial chunks around the whole ones.
-__host__ __device__ constexpr uint32_t zc_chunks_per_tile(uint32_t C) {
-  return C % kTileLanes == 0 ? 1u : (kTileLanes % C == 0 ? kTileLanes / C : kTileLanes / C + 2u);
+// Slots of one encoder tile (ticket) for chunks of C slots (a multiple of
+// 1024): whole chunks only, as many as fit in kTileLanes (one chunk when C is
+// larger), so that every chunk's escape count -- and with it the choice of
+// the raw form for an incompressible chunk -- is known inside one tile.
+// Powers of two up to kTileLanes give kTileLanes.
+__host__ __device__ constexpr uint32_t zc_tile_slots(uint32_t C) {
+  return C >= kTileLanes ? C : C * (kTileLanes / C);
 }
+__host__ __device__ constexpr uint32_t zc_chunks_per_tile(uint32_t C) {
+  return zc_tile_slots(C) / C;
+}
+
+// Bit 63 of a chunk's escape-offset table entry: the chunk is stored raw.
+constexpr unsigned long long kZcRawFlag = 1ull << 63;
 
 // ZipCCL encoder scratch after the control block: one look-back state per
 // tile, then one look-back word per block of kZcLbBlock tiles.

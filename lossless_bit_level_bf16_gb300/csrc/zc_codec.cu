@@ -112,8 +112,10 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   const bool p2 = (C & (C - 1)) == 0;
   const unsigned long long S = L.slot_bytes;
   const unsigned long long lanes_total = L.nchunks * (unsigned long long)C;
-  const unsigned long long ntiles = (lanes_total + kWTile - 1) / kWTile;
-  const uint32_t nct = zc_chunks_per_tile(C);  // chunks a ticket can touch
+  const uint32_t TL = zc_tile_slots(C);        // slots per ticket: whole chunks
+  const unsigned long long ntiles = (lanes_total + TL - 1) / TL;
+  const uint32_t nct = zc_chunks_per_tile(C);  // chunks per ticket
+  const uint32_t raw_dyn = 5u * C / 8u;        // dynamic bytes of a chunk stored raw
   uint8_t* wring = dyn + (size_t)warp * (kStages * 2048u + nct * 1024u + 2 * kEscCap);  // input steps
   uint32_t* wlut = reinterpret_cast<uint32_t*>(wring + kStages * 2048u);
   uint8_t* const wst_base = wring + kStages * 2048u + nct * 1024u;  // two escape staging windows
@@ -153,10 +155,8 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
       for (uint32_t i = lane; i < p_run; i += 32) A.out[dst + i] = pst[i];
     }
     if (lane < (int)nct) {
-      // chunks that start inside the ticket get their escape offset here
-      const unsigned long long c = p_cfirst + lane, cs = c * (unsigned long long)C;
-      if (c < L.nchunks && cs >= p_tlane0 && cs < p_tlane0 + kWTile)
-        reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = excl + p_cs;
+      const unsigned long long c = p_cfirst + lane;
+      if (c < L.nchunks) reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = excl + p_cs;
     }
     __syncwarp();
     p_has = false;
@@ -185,9 +185,8 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
       if (p_has) resolve();
       break;
     }
-    const unsigned long long tlane0 = tile * kWTile;
-    const unsigned long long cfirst = p2 ? (tlane0 >> log2C) : tlane0 / C;
-    const uint32_t r0 = (uint32_t)(tlane0 - cfirst * C);  // first slot's place in its chunk
+    const unsigned long long tlane0 = tile * TL;
+    const unsigned long long cfirst = tile * nct;  // tickets start at chunk starts
     // chunk information, held by lane k for the ticket's chunk k
     unsigned long long ce0 = 0;
     uint32_t cval = 0;
@@ -226,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     // 32-bit plane words; a step lies inside one chunk (C is a multiple of 1024)
     uint32_t run = 0, cs_pos = 0;  // escapes staged so far; chunk-start position (lane k)
     const uint32_t steps =
-        (uint32_t)((lanes_total - tlane0) < kWTile ? (lanes_total - tlane0) : kWTile) / 1024u;
+        (uint32_t)((lanes_total - tlane0) < TL ? (lanes_total - tlane0) : TL) / 1024u;
     // Step input: a full, 16-byte aligned step is copied into the warp's ring
     // with coalesced cp.async pieces (lane l copies 16-byte pieces l, l+32,
     // l+64, l+96), kAhead steps before it is used; each lane then reads its own
@@ -234,10 +233,10 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     // are free of bank conflicts.  Other steps use plain per-lane loads.
     // With C >= 4096 the whole ticket lies in one chunk and the step's chunk
     // data need no shuffles.
-    const bool one = C % kWTile == 0;
+    const bool one = nct == 1;
     // chunk (within the ticket) and slot (within the chunk) of step st's first slot
     auto where = [&](uint32_t st, uint32_t& s0) -> int {
-      const uint32_t q = r0 + st * 1024u;
+      const uint32_t q = st * 1024u;
       const uint32_t k = p2 ? (q >> log2C) : q / C;
       s0 = q - k * C;
       return (int)k;
@@ -402,9 +401,21 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
       run += tot;
     }
     __syncwarp();
+    // Chunk `lane` of the ticket: its escapes (to the next chunk's start or
+    // the ticket's end), whether it is stored raw (a full chunk with more
+    // escapes than the 5C/8 bytes its raw form puts past the slot), its
+    // dynamic bytes and their place within the ticket's.
     if (lane < (int)nct) cs_pos = s_cs[warp][lane];
+    const uint32_t nxt = __shfl_down_sync(kFull, cs_pos, 1);
+    const bool have_c = lane < (int)nct && cfirst + lane < L.nchunks;
+    const bool have_n = lane + 1 < (int)nct && cfirst + lane + 1 < L.nchunks;
+    const uint32_t cesc = have_c ? (have_n ? nxt : run) - cs_pos : 0u;
+    const bool craw = have_c && cval == C && cesc > raw_dyn;
+    uint32_t dtot;
+    const uint32_t dpos = warp_excl(craw ? raw_dyn : cesc, dtot);
+    const bool any_raw = __any_sync(kFull, craw);
 
-    if (run <= kEscCap) {
+    if (!any_raw && run <= kEscCap) {
       // publish this ticket's escape count now, resolve the previous ticket,
       // and keep this one pending in its window
       if (lane == 0 && tile + 1 != fault1) lb2_publish_agg(A.states, A.bwords, tile, run);
@@ -421,20 +432,19 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
       continue;
     }
     if (p_has) resolve();
-    // ---- more escapes than a window holds: the look-back now, then the
-    // ticket is classified again and its escapes written straight out
+    // ---- more escapes than a window holds, or a chunk stored raw: the
+    // look-back now, then the ticket is read again and its dynamic bytes
+    // (escapes, or a raw chunk's last 5C/8 bytes) written straight out
     bool to = false;
-    if (lane == 0 && tile + 1 != fault1) lb2_publish_agg(A.states, A.bwords, tile, run);
-    __syncwarp();
+    if (lane == 0 && tile + 1 != fault1) lb2_publish_agg(A.states, A.bwords, tile, dtot);
+    __syncwarp();  // also orders the slot stores above before the raw chunks' below
     const unsigned long long excl = lb2_lookback<4>(A.states, A.bwords, tile, &to, lim);
-    publish_inc(tile, excl, run, to);
+    publish_inc(tile, excl, dtot, to);
     const unsigned long long dst = L.off_esc + excl;
-    if (dst + run > A.out_cap) {
+    if (dst + dtot > A.out_cap) {
       if (lane == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
     } else {
-      // more escapes than the window holds: classify the ticket again and
-      // write its escape bytes straight to their place
-      uint32_t r2 = 0;
+      uint32_t r2 = 0;  // dynamic position within the ticket
       for (uint32_t st = 0; st < steps; ++st) {
         int lct;
         unsigned long long e0;
@@ -443,10 +453,29 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
         info(st, lct, e0, vch, al);
         uint32_t s0;
         where(st, s0);
+        const bool raw_c = __shfl_sync(kFull, craw, lct);
+        const uint32_t pos_c = __shfl_sync(kFull, dpos, lct);
+        if (s0 == 0) r2 = pos_c;
         const uint32_t i0 = s0 + 32u * lane;
         const int valid = vch > i0 ? ((vch - i0) < 32u ? (int)(vch - i0) : 32) : 0;
         uint32_t w[16];
         lane_load(A.x + e0 + i0, valid, w);
+        if (raw_c) {
+          // the lane's 32 values are raw bytes 2*i0 .. 2*i0+63 of the chunk,
+          // wholly in the slot or wholly past it (S is a multiple of 64)
+          const uint32_t b = 2u * i0;
+          if (b < S) {
+            uint8_t* sp = A.out + L.off_static + (cfirst + lct) * S + b;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              st_v4(sp + 16 * k, make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]));
+          } else {
+            uint8_t* dp = A.out + dst + pos_c + (b - (uint32_t)S);
+#pragma unroll
+            for (int k = 0; k < 64; ++k) dp[k] = (uint8_t)(w[k >> 2] >> (8 * (k & 3)));
+          }
+          continue;  // warp-uniform
+        }
         uint32_t acc[4];
         classify(w, wlut + (uint32_t)lct * 256u, valid, acc);
         const uint32_t esc = prmt(prmt(acc[0], acc[1], 0x7362), prmt(acc[2], acc[3], 0x7362), 0x7632);
@@ -457,11 +486,9 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
         r2 += tot;
       }
     }
-    if (lane < (int)nct) {
-      const unsigned long long c = cfirst + lane, cs = c * (unsigned long long)C;
-      if (c < L.nchunks && cs >= tlane0 && cs < tlane0 + kWTile)
-        reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = excl + cs_pos;
-    }
+    if (have_c)
+      reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[cfirst + lane] =
+          (excl + dpos) | (craw ? kZcRawFlag : 0ull);
     __syncwarp();  // the window is reused by the next ticket
   }
 
@@ -496,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   for (uint32_t s = lane; s < L.nseg; s += 32) {
     const ZcSegDev& r = A.segs[s];
     const volatile unsigned long long* ve = escoff;
-    const unsigned long long es = ve[r.chunk_start];
-    const unsigned long long ee = ve[r.chunk_start + r.nchunks];
+    const unsigned long long es = ve[r.chunk_start] & ~kZcRawFlag;
+    const unsigned long long ee = ve[r.chunk_start + r.nchunks] & ~kZcRawFlag;
     unsigned long long* rec =
         reinterpret_cast<unsigned long long*>(A.out + L.off_seg + (unsigned long long)kZcSegRec * s);
     unsigned long long bk = 0;
@@ -677,7 +704,8 @@ __global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
       if (s + 1 == h.nseg && (r.elem_start + r.nelem != h.n || r.chunk_start + r.nchunks != h.nchunks))
         set_status(ctrl, ZC_ERR_FORMAT);
     }
-    if (t == 0 && (rd_u64(escoff) != 0 || rd_u64(escoff + 8 * h.nchunks) != h.esc_total))
+    if (t == 0 && ((rd_u64(escoff) & ~kZcRawFlag) != 0 ||
+                   rd_u64(escoff + 8 * h.nchunks) != h.esc_total))
       set_status(ctrl, ZC_ERR_FORMAT);
   }
 
@@ -711,7 +739,8 @@ __global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
     uint32_t p0 = __ldg(reinterpret_cast<const unsigned short*>(pb));
     uint32_t p1 = __ldg(reinterpret_cast<const unsigned short*>(pb + (C >> 3)));
     uint32_t p2 = __ldg(reinterpret_cast<const unsigned short*>(pb + (C >> 2)));
-    const unsigned long long elo = n_lo, ehi = n_hi;
+    const bool craw = (n_lo & kZcRawFlag) != 0;  // the chunk is stored raw
+    const unsigned long long elo = n_lo & ~kZcRawFlag, ehi = n_hi & ~kZcRawFlag;
     const unsigned long long cn = c + 1;
     if (cn < c_end) {
       n_lo = rd_u64(escoff + 8 * cn);
@@ -728,6 +757,41 @@ __global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
     const unsigned long long vch_ll = r.elem_start + r.nelem - e0;
     const uint32_t vch = (uint32_t)(vch_ll < C ? vch_ll : C);
     const bool al = y_al16 && ((r.elem_start & 7ull) == 0);
+    if (craw) {
+      // a full chunk's 2C raw bytes: the slot, then its 5C/8 dynamic bytes
+      // (each 16-byte piece lies wholly in one: S is a multiple of 64)
+      if (vch != C || ehi - elo != 5ull * C / 8ull) {
+        if (lane == 0) set_status(ctrl, ZC_ERR_FORMAT);
+        continue;  // warp-uniform
+      }
+      for (uint32_t b = 16u * lane; b < 2u * C; b += 512u) {
+        uint4 v;
+        if (b < S) {
+          v = ld_nc_v4(slot + b);
+        } else {
+          const uint8_t* q = esc_base + elo + (b - S);
+          uint32_t u[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            u[k] = (uint32_t)q[4 * k] | ((uint32_t)q[4 * k + 1] << 8) |
+                   ((uint32_t)q[4 * k + 2] << 16) | ((uint32_t)q[4 * k + 3] << 24);
+          v = make_uint4(u[0], u[1], u[2], u[3]);
+        }
+        const unsigned long long elem = e0 + b / 2;
+        if (al) {
+          st_v4(y + elem, v);
+        } else {
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            y[elem + 2 * k] = (uint16_t)(u[k] & 0xFFFFu);
+            y[elem + 2 * k + 1] = (uint16_t)(u[k] >> 16);
+          }
+        }
+      }
+      __syncwarp();
+      continue;
+    }
     const unsigned long long ea = elo & ~15ull;  // staged window starts 16-byte aligned
     const bool staged = ehi - ea <= kWarpEscBytes;
     if (staged && ea + 16ull * lane < ehi)
@@ -822,7 +886,8 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   Ctrl* ctrl = static_cast<Ctrl*>(d_ws);
   unsigned long long* states =
       reinterpret_cast<unsigned long long*>(static_cast<char*>(d_ws) + kCtrlBytes);
-  const unsigned long long ntiles = (L.nchunks * (unsigned long long)L.C + kWTile - 1) / kWTile;
+  const unsigned long long tl = zc_tile_slots(L.C);
+  const unsigned long long ntiles = (L.nchunks * (unsigned long long)L.C + tl - 1) / tl;
   char* lb = static_cast<char*>(d_ws) + kCtrlBytes;
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + zc_enc_scratch_bytes(ntiles), s);
   if (e != cudaSuccess) return e;

@@ -174,6 +174,39 @@ def test_chunk_not_power_of_two(chunk):
     _check_full(allv.to(DEV).view(torch.bfloat16), None, chunk, [116, 117, 118, 119, 120, 121, 122])
 
 
+@pytest.mark.parametrize("chunk", [1024, 3072, 4096, 9216, 65536])
+def test_raw_fallback(chunk):
+    """Incompressible full chunks (random bit patterns, all-NaN runs) are
+    stored raw -- 2C bytes, bit 63 of the table entry -- next to coded chunks,
+    in several segments with ragged ends, in tickets that take the direct
+    path (raw chunks) and the staged one; with the plan's own books and with
+    a given book; stream equal to the oracle's, decode exact."""
+    g = torch.Generator().manual_seed(chunk)
+    lens = [chunk * 3 + 5, 7, chunk * 9, 2 * chunk - 3, 40_000]
+    parts = []
+    for i, L in enumerate(lens):
+        v = W.zc_gaussian(L, sigma=0.01, seed=60 + i)
+        bits = v.view(torch.int16)
+        for c0 in range(0, L, chunk):
+            if (c0 // chunk + i) % 3 == 1:  # every third chunk incompressible
+                n = min(chunk, L - c0)
+                bits[c0:c0 + n] = torch.randint(-32768, 32768, (n,), generator=g,
+                                                dtype=torch.int32).to(torch.int16)
+        if i == 3:
+            v[: min(L, chunk)] = float("nan")
+        parts.append(v)
+    x = torch.cat(parts).to(DEV)
+    seg = [0]
+    for L in lens:
+        seg.append(seg[-1] + L)
+    st, plan = _check_full(x, seg, chunk)
+    off_escoff = int(st[48:56].view(np.uint64)[0])
+    nch = int(st[24:32].view(np.uint64)[0])
+    flags = st[off_escoff:off_escoff + 8 * nch].view(np.uint64) >> np.uint64(63)
+    assert flags.sum() >= 5
+    _check_full(x, seg, chunk, [[116, 117, 118, 119, 120, 121, 122]] * len(lens))
+
+
 def test_degenerate_values():
     n = 10000
     # constant data (sigma = 0), all zeros, NaN / inf mixes, huge and tiny values
@@ -283,7 +316,7 @@ def test_output_capacity_reported():
     x = torch.full((50000,), float("nan"), dtype=torch.bfloat16, device=DEV)  # all escapes
     plan = Z.Plan(x.numel(), None, 4096)
     plan.fit(x)
-    fixed = plan.max_compressed_bytes - 50048
+    fixed = O.zc_stream_bytes(x.numel(), None, 4096, 0)  # everything but the dynamic bytes
     out = torch.zeros(fixed + 1000, dtype=torch.uint8, device=DEV)
     plan.compress(x, out=out)
     torch.cuda.synchronize()

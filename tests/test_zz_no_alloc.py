@@ -16,6 +16,7 @@ import sys
 import pytest
 import torch
 
+import oracle as O
 from lossless_bit_level_bf16_gb300 import abi, workloads as W, zipccl as Z
 
 pytestmark = pytest.mark.gpu
@@ -66,8 +67,8 @@ def test_static_status_reports_capacity():
     x[::7] = float("inf")  # every 7th element escapes
     plan = Z.Plan(n, None, 4096)
     plan.fit(x)
-    # room for the fixed part only: the escapes do not fit
-    plan_fixed = plan.max_compressed_bytes - ((n + 127) // 128) * 128
+    # room for the fixed part only (header, tables, slots): the escapes do not fit
+    plan_fixed = O.zc_stream_bytes(n, None, 4096, 0)
     out = torch.zeros(plan_fixed, dtype=torch.uint8, device=DEV)
     out_bytes = torch.zeros(1, dtype=torch.int64, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)

@@ -442,6 +442,7 @@ def gpu_arm(args, rank, world, local_rank):
 def kernels_of(op, cb=512):
     return {"zc_plan": ["zc_stats_kernel", "zc_predict_kernel"],
             "zc_compress": ["zc_encode_kernel"],
+            "zc_compress_fit": ["zc_encode_kernel", "zc_predict_kernel"],
             "zc_decompress": ["zc_decode_kernel"],
             "ibp_build_meta": ["ibp_columns_kernel", "ibp_meta_kernel"],
             "ibp_compress": (["ibp_encode_ws_kernel"] if cb <= 512 else
@@ -614,7 +615,9 @@ def _case(kind, nbytes, dev, ibp_mode):
         dws = torch.zeros(256, dtype=torch.uint8, device=dev)
         ops = [("zc_plan", lambda: plan.fit(x)),
                ("zc_compress", lambda: plan.compress(x, out=out, out_bytes=nb)),
-               ("zc_decompress", lambda: Z.decompress(out, out=y, in_bytes=out.numel(), ws=dws))]
+               ("zc_decompress", lambda: Z.decompress(out, out=y, in_bytes=out.numel(), ws=dws)),
+               # plan and encode from one read (the codebooks refit for the next call)
+               ("zc_compress_fit", lambda: plan.compress_fit(x, out=out, out_bytes=nb))]
         check = lambda: torch.equal(y.view(torch.int16), x.view(torch.int16))  # noqa: E731
         return ops, (plan.ws, dws), 2 * n, 0, check, nb, 4096
     if kind == "ibp16":

@@ -152,6 +152,21 @@ int zc_compress(zc_plan_t plan, const uint16_t* d_x, void* d_out,
                 uint64_t out_cap, uint64_t* d_out_bytes, void* d_ws,
                 size_t ws_bytes, zc_stream_t stream);
 
+/* zc_compress and the statistics of zc_plan from one read of d_x: the
+ * stream is the one zc_compress writes with the plan's codebooks as they are
+ * when the call starts; from the same loads the encoder sums each chunk's
+ * finite values and their squares, and a second kernel then replaces the
+ * plan's mu, sigma and codebooks with those of d_x ([ZipCCL] 2.A: the
+ * codebook comes from sigma, with no separate statistics pass) -- ready for
+ * the next call, as when consecutive tensors of a training run keep their
+ * distribution.  The sums are fp32 (sum, error) pairs of per-lane partial
+ * sums, so mu and sigma agree with zc_plan's to a few fp32 units in the last
+ * place and the codebooks are the same except at a near-tie.  Workspace:
+ * zc_workspace_bytes.  One memset, two kernels. */
+int zc_compress_fit(zc_plan_t plan, const uint16_t* d_x, void* d_out,
+                    uint64_t out_cap, uint64_t* d_out_bytes, void* d_ws,
+                    size_t ws_bytes, zc_stream_t stream);
+
 /* zc_compress without a workspace.  The ZipCCL pages have no counterpart:
  * this is an interface for callers that cannot allocate at the point where
  * they compress -- e.g. a communication library's progress thread, where a

@@ -39,6 +39,7 @@ SIGNATURES = {
     "zc_plan_info": (C.c_int, [_vp, _vp, _u8p, _dp]),
     "zc_compress": (C.c_int, [_vp, _vp, _vp, C.c_uint64, _vp, _vp, C.c_size_t, _vp]),
     "zc_compress_static": (C.c_int, [_vp, _vp, _vp, C.c_uint64, _vp, _vp, _vp]),
+    "zc_compress_fit": (C.c_int, [_vp, _vp, _vp, C.c_uint64, _vp, _vp, C.c_size_t, _vp]),
     "zc_decompress_workspace_bytes": (C.c_size_t, []),
     "zc_decompress": (C.c_int, [_vp, C.c_uint64, _vp, C.c_uint64, _vp, C.c_size_t, _vp]),
     "ibp_meta_bytes": (C.c_uint64, [C.c_uint32]),

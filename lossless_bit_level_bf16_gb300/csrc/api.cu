@@ -92,9 +92,13 @@ bool reachable(const void** p, bool* host) {
   return true;
 }
 
+// Workspace of a plan: the control block, then the statistics partials (one
+// per unit) or the encoder's look-back words followed by one statistics
+// partial per chunk (zc_compress_fit), whichever is larger.
 size_t zc_ws_bytes(const lbb::ZcLayout& L) {
   const unsigned long long a = L.nunits * sizeof(lbb::StatPartial);
-  const unsigned long long b = lbb::zc_enc_scratch_bytes(L.ntiles);
+  const unsigned long long b =
+      lbb::zc_fit_parts_offset(L.ntiles) - kCtrlBytes + L.nchunks * sizeof(lbb::StatPartial);
   return (size_t)lbb::round_up_dev(kCtrlBytes + std::max(a, b), 256);
 }
 
@@ -282,6 +286,18 @@ int zc_compress(zc_plan_t p, const uint16_t* d_x, void* d_out, uint64_t out_cap,
   return cuda_rc(lbb::zc_launch_compress(p->L, p->d_segs, d_x, d_out, out_cap,
                                          reinterpret_cast<unsigned long long*>(d_out_bytes), d_ws,
                                          (cudaStream_t)stream));
+}
+
+int zc_compress_fit(zc_plan_t p, const uint16_t* d_x, void* d_out, uint64_t out_cap,
+                    uint64_t* d_out_bytes, void* d_ws, size_t ws_bytes, zc_stream_t stream) {
+  if (!p || !d_out || !d_ws || (!d_x && p->L.n)) return ZC_ERR_ARG;
+  if (!aligned(d_out, 16) || !aligned(d_ws, 256) || !aligned(d_x, 2) || !aligned(d_out_bytes, 8))
+    return ZC_ERR_ARG;
+  if (ws_bytes < zc_ws_bytes(p->L)) return ZC_ERR_CAPACITY;
+  if (out_cap < p->L.off_esc) return ZC_ERR_CAPACITY;
+  return cuda_rc(lbb::zc_launch_compress(p->L, p->d_segs, d_x, d_out, out_cap,
+                                         reinterpret_cast<unsigned long long*>(d_out_bytes), d_ws,
+                                         (cudaStream_t)stream, true));
 }
 
 size_t zc_decompress_workspace_bytes(void) { return kCtrlBytes; }

@@ -44,6 +44,29 @@ __device__ __forceinline__ int get_status(const Ctrl* c) {
   return *reinterpret_cast<const volatile int*>(&c->status);
 }
 
+// ---------------------------------------------------------------- fp32 sums
+
+// The two bf16 values of a 32-bit word as fp32 (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Error-free transformation: hi + lo accumulates v exactly up to the rounding
+// of lo itself.
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float v) {
+  float s = __fadd_rn(hi, v);
+  float bb = __fsub_rn(s, hi);
+  float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(v, bb));
+  hi = s;
+  lo = __fadd_rn(lo, err);
+}
+
+// (a, b) += (a2, b2) for fp32 (sum, error) pairs: a takes the rounded sum of
+// the sums, b the error of that addition and the errors so far.
+__device__ __forceinline__ void pair_add(float& a, float& b, float a2, float b2) {
+  two_sum_acc(a, b, a2);
+  b = __fadd_rn(b, b2);
+}
+
 // ---------------------------------------------------------------- memory ops
 
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {

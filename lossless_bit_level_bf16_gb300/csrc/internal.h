@@ -73,11 +73,21 @@ inline unsigned long long round_up(unsigned long long v, unsigned long long a) {
 
 cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
                            const uint16_t* d_x, void* d_ws, cudaStream_t s);
+// fit: the encoder also sums each chunk's finite values (count, sum, sum of
+// squares) into partials after its scratch, and the predictor then replaces
+// the plan's statistics and codebooks from them (zc_compress_fit).
 cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
                                const uint16_t* d_x, void* d_out,
                                unsigned long long out_cap,
                                unsigned long long* d_out_bytes, void* d_ws,
-                               cudaStream_t s);
+                               cudaStream_t s, bool fit = false);
+// The predictor over per-chunk partials (the second launch of a fit).
+cudaError_t zc_launch_predict_chunks(const ZcLayout& L, ZcSegDev* d_segs,
+                                     const StatPartial* d_parts, cudaStream_t s);
+// Offset of the per-chunk statistics partials in an encoder workspace.
+constexpr unsigned long long zc_fit_parts_offset(unsigned long long ntiles) {
+  return 256 + (zc_enc_scratch_bytes(ntiles) + 15) / 16 * 16;
+}
 cudaError_t zc_launch_decompress(const void* d_in, unsigned long long in_bytes,
                                  uint16_t* d_y, unsigned long long y_cap,
                                  void* d_ws, cudaStream_t s);

@@ -47,6 +47,7 @@ struct EncArgs {
   Ctrl* ctrl;
   unsigned long long* states;  // look-back state per tile
   unsigned long long* bwords;  // look-back word per block of kLbBlock tiles
+  StatPartial* parts;          // zc_compress_fit: one statistics partial per chunk
   int x_al16;
 };
 
@@ -100,7 +101,13 @@ constexpr uint32_t kEscCap = 1024;                   // escape bytes a warp stag
 // 256-word lookup table per chunk of a ticket, kEscCap staged escape bytes.
 static_assert(kLbBlock == kZcLbBlock, "the scratch layout and the look-back agree");
 
-__global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
+// STATS (zc_compress_fit): each lane also sums its finite values and their
+// squares per step (four fp32 chains of eight values, then fp32 (sum, error)
+// pairs across steps; a step whose fp32 sums are not finite, or whose squares
+// may have underflowed, is summed in fp64), and the warp writes each chunk's
+// count and fp64 sums to A.parts when the chunk's last step is done.
+template <bool STATS>
+__global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncArgs A) {
   extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ int s_lseg[kEncWarps][kMaxLutSlots];
   __shared__ uint32_t s_cs[kEncWarps][kMaxLutSlots];  // escape position where a chunk starts
@@ -173,6 +180,10 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   __syncwarp();
   int my_seg = -1;  // segment cache of lanes < nct
   unsigned long long my_c0 = 0, my_c1 = 0;
+  // statistics of the chunk being classified (STATS only)
+  float st_hx = 0.f, st_lx = 0.f, st_hq = 0.f, st_lq = 0.f;
+  double st_dx = 0.0, st_dq = 0.0;
+  unsigned long long st_cnt = 0;
 
   // A ticket is taken only when the warp is ready to work on it: taking the
   // next one early delays its published escape count, which other warps'
@@ -367,6 +378,71 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
         lane_load(A.x + e0 + i0, valid, w);
       }
       const unsigned long long c = cfirst + lct;
+      if constexpr (STATS) {
+        float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {  // padding slots hold 0
+          const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
+          s1[j & 3] = __fadd_rn(__fadd_rn(s1[j & 3], lo), hi);
+          s2[j & 3] = __fmaf_rn(hi, hi, __fmaf_rn(lo, lo, s2[j & 3]));
+        }
+        const float t1 = __fadd_rn(__fadd_rn(s1[0], s1[1]), __fadd_rn(s1[2], s1[3]));
+        const float t2 = __fadd_rn(__fadd_rn(s2[0], s2[1]), __fadd_rn(s2[2], s2[3]));
+        bool fast = isfinite(t1) && isfinite(t2);
+        if (fast && t2 < 0x1p-96f) {  // squares may have lost bits: only if a value is not 0
+          uint32_t nz = 0;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) nz |= w[j] & 0x7FFF7FFFu;
+          fast = nz == 0;
+        }
+        if (fast) {
+          two_sum_acc(st_hx, st_lx, t1);
+          two_sum_acc(st_hq, st_lq, t2);
+          st_cnt += (unsigned long long)valid;
+        } else {  // an inf/NaN value, an fp32 overflow or underflow: fp64, finite values only
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
+            if (j < valid && ((bits >> 7) & 0xFFu) != 0xFFu) {
+              const double d = (double)__uint_as_float(bits << 16);
+              st_dx = __dadd_rn(st_dx, d);
+              st_dq = __dadd_rn(st_dq, __dmul_rn(d, d));
+              st_cnt += 1;
+            }
+          }
+        }
+        if (s0 + 1024u == C || st + 1 == steps) {  // the chunk's last step (warp-uniform)
+          float ax = st_hx, bx = st_lx, aq = st_hq, bq = st_lq;
+          unsigned long long n = st_cnt;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float ax2 = __shfl_down_sync(kFull, ax, o), bx2 = __shfl_down_sync(kFull, bx, o);
+            const float aq2 = __shfl_down_sync(kFull, aq, o), bq2 = __shfl_down_sync(kFull, bq, o);
+            pair_add(ax, bx, ax2, bx2);
+            pair_add(aq, bq, aq2, bq2);
+            n += __shfl_down_sync(kFull, n, o);
+          }
+          const bool fin =
+              __shfl_sync(kFull, isfinite(ax) && isfinite(bx) && isfinite(aq) && isfinite(bq), 0);
+          double r1, r2;
+          if (!fin || __any_sync(kFull, st_dx != 0.0 || st_dq != 0.0)) {
+            r1 = __dadd_rn(__dadd_rn((double)st_hx, (double)st_lx), st_dx);
+            r2 = __dadd_rn(__dadd_rn((double)st_hq, (double)st_lq), st_dq);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              r1 = __dadd_rn(r1, __shfl_down_sync(kFull, r1, o));
+              r2 = __dadd_rn(r2, __shfl_down_sync(kFull, r2, o));
+            }
+          } else {
+            r1 = __dadd_rn((double)ax, (double)bx);
+            r2 = __dadd_rn((double)aq, (double)bq);
+          }
+          if (lane == 0) A.parts[c] = StatPartial{n, r1, r2};
+          st_hx = st_lx = st_hq = st_lq = 0.f;
+          st_dx = st_dq = 0.0;
+          st_cnt = 0;
+        }
+      }
       uint32_t acc[4];
       classify(w, wlut + (uint32_t)lct * 256u, valid, acc);
       uint8_t* slot = A.out + L.off_static + c * S;
@@ -882,7 +958,7 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
                                const uint16_t* d_x, void* d_out,
                                unsigned long long out_cap,
                                unsigned long long* d_out_bytes, void* d_ws,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool fit) {
   Ctrl* ctrl = static_cast<Ctrl*>(d_ws);
   unsigned long long* states =
       reinterpret_cast<unsigned long long*>(static_cast<char*>(d_ws) + kCtrlBytes);
@@ -904,18 +980,24 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   A.states = states;
   A.bwords = reinterpret_cast<unsigned long long*>(lb + (8 * ntiles + 15) / 16 * 16);
   A.x_al16 = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
+  A.parts = fit ? reinterpret_cast<StatPartial*>(static_cast<char*>(d_ws) + zc_fit_parts_offset(ntiles))
+                : nullptr;
   const uint32_t nct = zc_chunks_per_tile(L.C);
   const size_t smem = (size_t)kEncWarps * (kStages * 2048u + nct * 1024u + 2 * kEscCap);
-  e = cudaFuncSetAttribute(zc_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto k = fit ? zc_encode_kernel<true> : zc_encode_kernel<false>;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(zc_encode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  const int res = resident_blocks((const void*)zc_encode_kernel, kThreads, smem);
+  const int res = resident_blocks((const void*)k, kThreads, smem);
   const unsigned long long need = (ntiles + kEncWarps - 1) / kEncWarps;
   unsigned long long grid = need < (unsigned long long)res ? need : (unsigned long long)res;
   if (grid == 0) grid = 1;
-  zc_encode_kernel<<<(unsigned)grid, kThreads, smem, s>>>(A);
-  return cudaGetLastError();
+  k<<<(unsigned)grid, kThreads, smem, s>>>(A);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !fit) return e;
+  // every chunk's partial is written before the predictor reads them
+  return zc_launch_predict_chunks(L, const_cast<ZcSegDev*>(d_segs), A.parts, s);
 }
 
 cudaError_t zc_launch_decompress(const void* d_in, unsigned long long in_bytes,

@@ -45,18 +45,6 @@ namespace {
 #endif
 constexpr int kStatBatch = LBB_STAT_BATCH;  // groups loaded before summing
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Error-free transformation: hi + lo accumulates v exactly up to the rounding
-// of lo itself.
-__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float v) {
-  float s = __fadd_rn(hi, v);
-  float bb = __fsub_rn(s, hi);
-  float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(v, bb));
-  hi = s;
-  lo = __fadd_rn(lo, err);
-}
 
 __device__ __forceinline__ int find_unit_segment(const ZcSegDev* segs, uint32_t nseg,
                                                  unsigned long long unit) {
@@ -84,12 +72,6 @@ __device__ __forceinline__ int find_unit_segment(const ZcSegDev* segs, uint32_t 
 // plan.
 constexpr int kStatWarps = kThreads / 32;
 
-// (a, b) += (a2, b2) for fp32 (sum, error) pairs: a takes the rounded sum of
-// the sums, b the error of that addition and the errors so far.
-__device__ __forceinline__ void pair_add(float& a, float& b, float a2, float b2) {
-  two_sum_acc(a, b, a2);
-  b = __fadd_rn(b, b2);
-}
 
 // The warp's loads run ahead of its sums through a ring of kStatRing batches
 // in shared memory (cp.async: each lane copies the 16-byte pieces it will sum
@@ -335,9 +317,11 @@ __device__ int field_of(double v) {
   return f > 254 ? 254 : (f < 0 ? 0 : f);
 }
 
+// parts: one partial per statistics unit (by_chunk = 0, after zc_stats_kernel)
+// or per chunk (by_chunk = 1, after the encoder that also sums).
 __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
     ZcSegDev* __restrict__ segs, uint32_t nseg, unsigned long long nunits,
-    const StatPartial* __restrict__ parts) {
+    const StatPartial* __restrict__ parts, int by_chunk) {
   __shared__ double s_r1[kThreads / 32], s_r2[kThreads / 32];
   __shared__ unsigned long long s_rc[kThreads / 32];
   __shared__ double s_mu, s_sigma;
@@ -351,8 +335,9 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
   const int t = threadIdx.x;
   const uint32_t sg = blockIdx.x;
   grid_dep_wait();  // the statistics partials
-  const unsigned long long u0 = segs[sg].unit_start;
-  const unsigned long long u1 = (sg + 1 < nseg) ? segs[sg + 1].unit_start : nunits;
+  const unsigned long long u0 = by_chunk ? segs[sg].chunk_start : segs[sg].unit_start;
+  const unsigned long long u1 = by_chunk ? u0 + segs[sg].nchunks
+                                         : ((sg + 1 < nseg) ? segs[sg + 1].unit_start : nunits);
   double a = 0.0, b = 0.0;
   unsigned long long c = 0;
   for (unsigned long long u = u0 + t; u < u1; u += kThreads) {
@@ -544,7 +529,13 @@ cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
   }
   return launch_dependent(zc_predict_kernel, L.nseg, kThreads, 0, s,
                           const_cast<ZcSegDev*>(d_segs), L.nseg, L.nunits,
-                          static_cast<const StatPartial*>(parts));
+                          static_cast<const StatPartial*>(parts), 0);
+}
+
+cudaError_t zc_launch_predict_chunks(const ZcLayout& L, ZcSegDev* d_segs,
+                                     const StatPartial* d_parts, cudaStream_t s) {
+  return launch_dependent(zc_predict_kernel, L.nseg, kThreads, 0, s, d_segs, L.nseg, L.nchunks,
+                          d_parts, 1);
 }
 
 }  // namespace lbb

@@ -111,6 +111,25 @@ class Plan:
                                        abi.stream_handle(stream)), "zc_compress")
         return out, out_bytes
 
+    def compress_fit(self, x: torch.Tensor, out: torch.Tensor | None = None,
+                     out_bytes: torch.Tensor | None = None, stream=None,
+                     ws: torch.Tensor | None = None):
+        """zc_compress_fit: encode with the current codebooks and, from the
+        same read, refit the plan's statistics and codebooks to ``x`` for the
+        next call.  Returns (out, out_bytes) like compress."""
+        x = _bits(x)
+        if x.numel() != self.n:
+            raise ValueError(f"plan is for {self.n} elements, tensor has {x.numel()}")
+        if out is None:
+            out = torch.empty(self.max_compressed_bytes, dtype=torch.uint8, device=self.device)
+        if out_bytes is None:
+            out_bytes = torch.zeros(1, dtype=torch.int64, device=self.device)
+        w = self.ws if ws is None else ws
+        abi.check(self.lib.zc_compress_fit(self._h, abi.ptr(x), abi.ptr(out), out.numel(),
+                                           abi.ptr(out_bytes), abi.ptr(w), w.numel(),
+                                           abi.stream_handle(stream)), "zc_compress_fit")
+        return out, out_bytes
+
     def compress_static(self, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
                         status: torch.Tensor | None = None, stream=None):
         """zc_compress_static: the caller passes every buffer (out, out_bytes

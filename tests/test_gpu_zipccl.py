@@ -207,6 +207,55 @@ def test_raw_fallback(chunk):
     _check_full(x, seg, chunk, [[116, 117, 118, 119, 120, 121, 122]] * len(lens))
 
 
+def _fit_cases():
+    x1 = W.zc_gaussian(1 << 20, sigma=0.02, seed=0, device=DEV)
+    yield "gaussian", x1, None, W.zc_gaussian(1 << 20, sigma=0.05, seed=1, device=DEV)
+    x, seg = W.zc_gradient(n_blocks=64, device=DEV)
+    y, _ = W.zc_gradient(n_blocks=64, seed=1, device=DEV)
+    yield "gradient", x, seg, y
+    lens = [0, 1, 7, 4095, 0, 4097, 12345, 3, 65536 + 5, 20000, 20000, 20000]
+    seg = [0]
+    for L in lens:
+        seg.append(seg[-1] + L)
+    parts = [W.zc_gaussian(L, sigma=[0.02, 1e-3, 3.0, 1e-5, 1e-30, 1e30][i % 6], seed=i, device=DEV)
+             for i, L in enumerate(lens)]
+    parts[9][::13] = float("inf")
+    parts[10][::17] = float("nan")
+    x = torch.cat(parts)
+    yield "ragged", x, seg, x.flip(0).contiguous()
+
+
+def test_compress_fit():
+    """zc_compress_fit: the stream is the oracle's for the codebooks in force
+    when the call starts; afterwards the plan's mean, sigma and codebooks are
+    those of the data (the oracle's fp64 statistics, within the fused sums'
+    rounding; the codebook equal to the oracle's own); the next call encodes
+    with them.  Includes empty, tiny, ragged segments, inf/NaN values and
+    values whose squares leave the fp32 range (summed in fp64)."""
+    for name, x, seg, y in _fit_cases():
+        nseg = 1 if seg is None else len(seg) - 1
+        plan = Z.Plan(x.numel(), seg, 4096)
+        first = [[116, 117, 118, 119, 120, 121, 122]] * nseg
+        plan.set_books(first)
+        xb, yb = _bits_np(x), _bits_np(y)
+        out, nb = plan.compress_fit(x)
+        torch.cuda.synchronize()
+        assert plan.status() == 0, name
+        check_stream_equal(out[: int(nb.item())].cpu().numpy(), xb, seg, 4096, first)
+        bk, mu, sg = plan.info()
+        check_plan(xb, seg, bk, mu, sg, rel=12)
+        out2, nb2 = plan.compress_fit(y)  # encodes with x's codebooks, refits to y
+        torch.cuda.synchronize()
+        assert plan.status() == 0, name
+        check_stream_equal(out2[: int(nb2.item())].cpu().numpy(), yb, seg, 4096, bk)
+        bk2, mu2, sg2 = plan.info()
+        check_plan(yb, seg, bk2, mu2, sg2, rel=12)
+        # the same books as the separate statistics pass, except at a near-tie
+        ref = Z.Plan(y.numel(), seg, 4096)
+        ref.fit(y)
+        assert np.array_equal(ref.info()[0], bk2), name
+
+
 def test_degenerate_values():
     n = 10000
     # constant data (sigma = 0), all zeros, NaN / inf mixes, huge and tiny values

@@ -26,12 +26,14 @@ def _sum_abs(u16, step=1 << 24):
     return tot
 
 
-def check_plan(x_bits, seg_off, books_gpu, mu_gpu, sig_gpu, allow_near_ties=False):
+def check_plan(x_bits, seg_off, books_gpu, mu_gpu, sig_gpu, allow_near_ties=False, rel=8):
     """Codebook parity for a plan computed on the GPU.
 
     The GPU sums each thread's 16 values as an fp32 tree (error at most 4 ulp
     of the sum of magnitudes) before accumulating exactly, so its mean and
-    sigma may differ from the oracle's fp64 sums by that much.  Given the
+    sigma may differ from the oracle's fp64 sums by that much (rel = 8 units
+    of fp32 rounding allowed; the encoder's fused sums of zc_compress_fit add
+    eight values per fp32 chain and then two levels, rel = 12).  Given the
     GPU's own (mu, sigma), the oracle's predictor must give the GPU's book
     exactly.  The oracle's book from its own statistics must agree too.  Only
     where the caller builds near-ties on purpose (allow_near_ties) may it
@@ -52,12 +54,12 @@ def check_plan(x_bits, seg_off, books_gpu, mu_gpu, sig_gpu, allow_near_ties=Fals
             ex2 = s2 / cnt
         else:
             mean_abs = ex2 = 0.0
-        tol_mu = 8 * U * mean_abs + 1e-300
+        tol_mu = rel * U * mean_abs + 1e-300
         assert abs(mu_gpu[s] - mu_o) <= tol_mu, (s, mu_gpu[s], mu_o)
         # groups whose squares could underflow fp32 are summed in fp64 on the
         # GPU, so the only absolute term left is the fp32 subnormal spacing of
         # the squares of a group kept in fp32 (2^-150 each)
-        tol_var = 8 * U * ex2 + 2 * abs(mu_o) * tol_mu + 2.0 ** -140
+        tol_var = rel * U * ex2 + 2 * abs(mu_o) * tol_mu + 2.0 ** -140
         assert abs(sig_gpu[s] ** 2 - sg_o ** 2) <= tol_var, (s, sig_gpu[s], sg_o)
         b_from_gpu_stats = O.zc_predict(float(mu_gpu[s]), float(sig_gpu[s]))
         assert np.array_equal(b_from_gpu_stats, books_gpu[s]), (s, b_from_gpu_stats, books_gpu[s])

@@ -93,6 +93,14 @@ int zc_version(void);
  * Returns ZC_OK. */
 int zc_test_wait_fault(uint64_t tile, uint32_t max_spins);
 
+/* TEST ONLY -- the pages have no counterpart.  ibp_compress of chunks up to
+ * 512 bytes normally runs one cooperative kernel (its blocks wait for each
+ * other's tile lengths, so the driver must place the whole grid at once); when
+ * the driver refuses that launch it takes the three-launch encode instead.
+ * enable = 0 makes every such call take the three-launch encode (so tests can
+ * check it), 1 restores the default.  Process-wide.  Returns ZC_OK. */
+int zc_test_ibp_single_pass(int enable);
+
 /* Read the status word of a workspace: synchronises the stream, copies the
  * word to *h_status (ZC_OK or a negative code).  Returns ZC_OK or ZC_ERR_CUDA. */
 int zc_status(const void* d_ws, zc_stream_t stream, int* h_status);
@@ -242,11 +250,12 @@ int ibp_build_meta(const void* d_samples, uint64_t n_samples,
  * d_out using the metadata at d_meta (its chunk size must be chunk_bytes;
  * checked on the device).  *d_out_bytes (device, may be NULL) receives the
  * stream size; a stream larger than out_cap sets ZC_ERR_CAPACITY and nothing
- * is written past out_cap.  For chunk_bytes <= 512: one memset and one
- * kernel that reads the input from device memory once (tiles are matched,
- * their stream lengths published in the workspace and their offsets resolved
- * a few tiles later, while the input is still in L2).  For chunk_bytes <=
- * 2048: one memset and three kernels (a read-only pass that decides every
+ * is written past out_cap.  For chunk_bytes <= 512 (multiples of 16): one
+ * memset and one cooperative kernel that reads the input from device memory
+ * once (tiles are matched, their stream lengths published in the workspace
+ * and their offsets resolved a few tiles later, while the input is still in
+ * L2); if the driver cannot place its whole grid at once, the three kernels
+ * below instead.  For chunk_bytes <= 2048: one memset and three kernels (a read-only pass that decides every
  * chunk's participation bit, a scan of the group lengths into the stream's
  * group-offset table, the packing pass); the workspace holds one
  * participation word per group between them.  Larger chunks: one memset and

@@ -29,6 +29,7 @@ SIGNATURES = {
     "zc_strerror": (C.c_char_p, [C.c_int]),
     "zc_version": (C.c_int, []),
     "zc_test_wait_fault": (C.c_int, [C.c_uint64, C.c_uint32]),
+    "zc_test_ibp_single_pass": (C.c_int, [C.c_int]),
     "zc_status": (C.c_int, [_vp, _vp, C.POINTER(C.c_int)]),
     "zc_plan_create": (C.c_int, [C.c_uint64, _u64p, C.c_uint32, C.c_uint32, C.POINTER(_vp)]),
     "zc_plan_destroy": (None, [_vp]),

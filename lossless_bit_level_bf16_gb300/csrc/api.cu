@@ -123,6 +123,11 @@ const char* zc_strerror(int code) {
 
 int zc_version(void) { return 100; }
 
+int zc_test_ibp_single_pass(int enable) {
+  lbb::ibp_set_single_pass(enable);
+  return ZC_OK;
+}
+
 int zc_test_wait_fault(uint64_t tile, uint32_t max_spins) {
   lbb::g_fault_tile1.store(tile == UINT64_MAX ? 0ull : tile + 1);
   lbb::g_fault_spins.store(max_spins);

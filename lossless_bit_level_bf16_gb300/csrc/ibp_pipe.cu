@@ -43,6 +43,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -1635,18 +1636,31 @@ cudaError_t ibp_ws_compress(const void* d_meta, uint32_t cb, const void* d_x,
   if (e != cudaSuccess) return e;
   e = arm_wait_fault(d_ws, s);
   if (e != cudaSuccess) return e;
-  k<<<(unsigned)grid, kWsThreads, smem, s>>>(A);
-  return cudaGetLastError();
+  // The blocks wait for lengths that every other block of the launch
+  // publishes: a cooperative launch makes the whole grid resident at once (or
+  // is refused, cudaErrorCooperativeLaunchTooLarge, e.g. on a GPU whose SMs
+  // are shared out), so no block ever waits for one that cannot start.
+  void* kargs[] = {&A};
+  return cudaLaunchCooperativeKernel((const void*)k, dim3((unsigned)grid), dim3(kWsThreads), kargs,
+                                     smem, s);
 }
 
+std::atomic<int> g_single_pass{1};  // 0: the three-launch encode for every chunk size (tests)
+
 }  // namespace
+
+void ibp_set_single_pass(int on) { g_single_pass.store(on ? 1 : 0); }
 
 bool ibp_pipe_supported(uint32_t cb, bool encode) { return cb <= 2048 && pick(cb, encode).ok; }
 
 cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t cb, const void* d_x,
                               unsigned long long n_bytes, void* d_out, unsigned long long out_cap,
                               unsigned long long* d_out_bytes, void* d_ws, cudaStream_t s) {
-  if (cb <= 512) return ibp_ws_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap, d_out_bytes, d_ws, s);
+  if (cb <= 512 && g_single_pass.load()) {
+    const cudaError_t e = ibp_ws_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap, d_out_bytes, d_ws, s);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    cudaGetLastError();  // the grid cannot be resident at once here: three launches instead
+  }
   const Geo g = pick(cb, true);
   const unsigned long long nchunks = (n_bytes + cb - 1) / cb, ngroups = (nchunks + 31) / 32;
   const unsigned long long ntiles2 = (ngroups + kOffNT * kOffIPT - 1) / (kOffNT * kOffIPT);

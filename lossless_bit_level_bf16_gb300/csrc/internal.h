@@ -132,6 +132,10 @@ cudaError_t ibp_launch_slots_gather(const void* d_meta, uint32_t chunk_bytes, co
 // TMA-pipelined IBP kernels (ibp_pipe.cu) for chunks of up to 2048 bytes;
 // the launchers above use them whenever ibp_pipe_supported says so.
 bool ibp_pipe_supported(uint32_t chunk_bytes, bool encode);
+// Test switch (zc_test_ibp_single_pass): 0 sends chunks of up to 512 bytes to
+// the three-launch encode, the path taken when the single-pass encoder's grid
+// cannot be resident at once.
+void ibp_set_single_pass(int on);
 cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t chunk_bytes, const void* d_x,
                               unsigned long long n_bytes, void* d_out,
                               unsigned long long out_cap, unsigned long long* d_out_bytes,

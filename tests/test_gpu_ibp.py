@@ -296,6 +296,28 @@ def test_bf16_weights(mode):
     assert total < xb.size
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_three_launch_encode_for_small_chunks(mode):
+    """The path the single-pass encoder falls back to when its grid cannot
+    be resident at once (three launches: match, offsets, pack) gives the
+    oracle's stream for 512-byte and smaller chunks too."""
+    lib = abi.load()
+    rows, idx = W.ibp_table(rows=150_000, cols=128, std=0.1, seed=4, device=DEV, n_samples=3000)
+    try:
+        lib.zc_test_ibp_single_pass(0)
+        for cb, x in ((512, rows.reshape(-1)), (256, rows.reshape(-1)[: 150_000 * 64 - 8]),
+                      (64, rows.reshape(-1)[:1_000_000])):
+            nch = x.numel() * 4 // cb
+            sidx = W.sample_rows(nch, 3000, seed=5, device=DEV)
+            meta = I.build_meta(x[: nch * (cb // 4)].view(nch, cb // 4)[sidx].contiguous(), cb,
+                                T=0.9, mode=mode)
+            st, y = _gpu_roundtrip(meta, x, cb)
+            assert np.array_equal(st.cpu().numpy(), O.ibp_encode(_u8(meta), _u8(x))), cb
+            assert torch.equal(y.view(torch.int32), x.view(torch.int32))
+    finally:
+        lib.zc_test_ibp_single_pass(1)
+
+
 def test_encode_next_to_another_stream():
     """The single-pass encoder's blocks wait for lengths that other blocks of
     the same launch publish.  Here its launches share the GPU with ZipCCL

@@ -400,10 +400,12 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
           two_sum_acc(st_hq, st_lq, t2);
           st_cnt += (unsigned long long)valid;
         } else {  // an inf/NaN value, an fp32 overflow or underflow: fp64, finite values only
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
-            if (j < valid && ((bits >> 7) & 0xFFu) != 0xFFu) {
+          // (rare: the lane's values are read again, one at a time)
+          const uint16_t* xs = A.x + e0 + s0 + 32u * lane;
+#pragma unroll 1
+          for (int j = 0; j < valid; ++j) {
+            const uint32_t bits = xs[j];
+            if (((bits >> 7) & 0xFFu) != 0xFFu) {
               const double d = (double)__uint_as_float(bits << 16);
               st_dx = __dadd_rn(st_dx, d);
               st_dq = __dadd_rn(st_dq, __dmul_rn(d, d));

@@ -60,25 +60,37 @@ def csrc_hash():
 
 
 def _traffic_table():
-    """Measured DRAM traffic per launch from the committed ncu summaries:
-    lines 'traffic <kernel> <sources sha1> <bytes per launch>' in profiles/*.md,
-    as {kernel: {sha1: bytes}} (a kernel may have lines from several captures)."""
+    """Measured DRAM traffic per launch from the committed ncu summaries, as
+    {kernel: {sha1: [(bytes per launch, uncompressed bytes, case), ...]}}.
+    Lines in profiles/*.md read 'traffic <kernel> <sources sha1> <bytes>
+    <uncompressed bytes of the captured launch> <case>', the case naming the
+    data and chunking the capture ran on (a kernel may have lines from several
+    captures)."""
     import glob
     out = {}
     for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         for line in open(f):
             parts = line.strip().strip("`").split()
-            if len(parts) == 4 and parts[0] == "traffic" and parts[3].isdigit():
-                out.setdefault(parts[1], {})[parts[2]] = int(parts[3])
+            if len(parts) == 6 and parts[0] == "traffic" and parts[3].isdigit() \
+                    and parts[4].isdigit():
+                out.setdefault(parts[1], {}).setdefault(parts[2], []).append(
+                    (int(parts[3]), int(parts[4]), parts[5]))
     return out
 
 
-def measured_traffic(kernel, table=None, sha=None):
-    """The kernel's DRAM bytes per launch measured on the current sources, or
-    None when no capture matches them."""
+def measured_traffic(kernel, case, unc, table=None, sha=None):
+    """The kernel's DRAM bytes for a launch over `unc` uncompressed bytes of
+    `case`, from a capture on the current sources: the captured figure, scaled
+    by unc / captured bytes when the sizes differ (traffic grows in proportion
+    with the input for these streaming kernels at a fixed data distribution
+    and chunking).  Returns (bytes, captured uncompressed bytes), or
+    (None, None) when no capture of that case matches the sources."""
     table = _traffic_table() if table is None else table
     sha = csrc_hash() if sha is None else sha
-    return table.get(kernel, {}).get(sha)
+    for nbytes, cap, c in table.get(kernel, {}).get(sha, []):
+        if c == case:
+            return (nbytes if cap == unc else round(nbytes * unc / cap)), cap
+    return None, None
 
 
 class ClockSampler:
@@ -293,6 +305,10 @@ class Workload:
                         ("zc_plan", "zc_compress", "zc_decompress", "ibp_build_meta",
                          "ibp_compress", "ibp_decompress")}
         self.launches_per_step = sum(len(v) for v in self.kernels.values())
+        # the data each op runs on, as named in the traffic lines of the profiles
+        self.case = {op: ("zc_gradient_c4096" if op.startswith("zc") else
+                          f"ibp_table_{self.cb}B_mode{self.mode}")
+                     for op in self.kernels}
 
     def ops(self):
         I, Z = self.I, self.Z
@@ -438,6 +454,13 @@ def gpu_arm(args, rank, world, local_rank):
                 targets=targets)
 
 
+def case_of(kind, cb, mode):
+    """The traffic lines' name for a size-sweep workload: ZipCCL on bf16
+    N(0, 0.01), chunk 4096; IBP on fp32 N(0, 0.02) in cb-byte chunks and
+    metadata mode `mode`."""
+    return "zc_gauss0.01_c4096" if kind == "zipccl" else f"ibp_gauss0.02_{cb}B_mode{mode}"
+
+
 # kernels each op launches, by codec and IBP chunk size
 def kernels_of(op, cb=512):
     return {"zc_plan": ["zc_stats_kernel", "zc_predict_kernel"],
@@ -483,13 +506,15 @@ def target_ops(args, dev, flush, stream):
             alg = unc if name == "zc_plan" else unc + comp
             ach = alg / (t * 1e-3) / 1e9
             ks = kernels_of(name, cb)
+            traffic, cap = measured_traffic(ks[0], case_of(kind, cb, mode), unc) \
+                if len(ks) == 1 else (None, None)
             out[f"{name} [{label}]"] = {
                 "ms": round(t, 4), "GBps_uncompressed": round(unc / (t * 1e-3) / 1e9, 1),
                 "ratio": round(unc / comp, 4), "kernels": ks, "launches_timed": steps,
                 "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak,
                              "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                              "frac": round(ach / peak, 4), "algorithmic_bytes_per_launch": alg,
-                             "traffic": measured_traffic(ks[0]) if len(ks) == 1 else None}}
+                             "traffic": traffic, "traffic_capture_bytes": cap}}
         del ops, wss, check, nb
         torch.cuda.empty_cache()
     return out
@@ -527,7 +552,7 @@ def report_gpu(args, r, world):
     dom = max(single, key=lambda k: statistics.mean(r["per_op"][k]))
     t_dom = statistics.mean(r["per_op"][dom])
     kname = wl.kernels[dom][0]
-    traffic = measured_traffic(kname)
+    traffic, cap = measured_traffic(kname, wl.case[dom], unc[dom])
     achieved = alg[dom] / (t_dom * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -552,7 +577,8 @@ def report_gpu(args, r, world):
         "roofline": {"bound": "hbm", "kernel": kname, "op": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "algorithmic_bytes_per_launch": alg[dom], "traffic": traffic},
+                     "algorithmic_bytes_per_launch": alg[dom], "traffic": traffic,
+                     "traffic_capture_bytes": cap},
         "e2e": {"value": round(unc_total / (r["e2e_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": wl.launches_per_step * args.steps,

@@ -27,13 +27,11 @@
 // pack; described at ibp_encode_ws_kernel); for larger chunks three launches
 // (match -> offsets -> pack, described at the encode kernels below), which
 // read the input twice.  Packing closes up the kept bits of a vector's 4 words into
-// one run of at most 128 bits and puts it into a shared-memory image of the
-// tile's stream (plain stores for the words the run covers alone, atomicOr
-// for a shared first or last word), which is then copied out with 16-byte
-// stores; a tile in which no chunk participates is copied straight from the
-// stage.  The image holds stream word j at image word j + 3: chunk bodies
-// start 32 bits after a 128-bit aligned group start, so a raw chunk that
-// follows raw chunks lands 16-byte aligned.
+// one run of at most 128 bits and ORs it into a shared-memory image of the
+// tile's stream (a shared atomicOr per word, with no choice between words a
+// run owns alone and words it shares), which is then copied out with 16-byte
+// stores and cleared; a tile in which no chunk participates is copied
+// straight from the stage.  The image holds stream word j at image word j.
 //
 // Decode, per tile: the tile's compressed bytes (its span taken from the
 // stream's group-offset table, checked first) are staged; one warp per group
@@ -166,12 +164,6 @@ __device__ __forceinline__ uint32_t vt_compress(const VecTab& v, uint32_t x, int
     return ((x >> v.MV[0][w]) & v.MV[1][w]) | (((x >> v.MV[2][w]) & v.MV[3][w]) << v.MV[4][w]);
   return hd_compress(x, v.K[w], &v.MV[0][w], 4);
 }
-// vt_compress for the three-run form (equal to the two-run form when the
-// keep masks have at most two runs: the third run's mask is then zero).
-__device__ __forceinline__ uint32_t vt_compress3(const VecTab& v, uint32_t x, int w) {
-  return ((x >> v.MV[0][w]) & v.MV[1][w]) | (((x >> v.MV[2][w]) & v.MV[3][w]) << v.MV[4][w]) |
-         (((x >> v.R3[0][w]) & v.R3[1][w]) << v.R3[2][w]);
-}
 // Inverse: the low kept-bit count of f spread out to the kept positions.
 __device__ __forceinline__ uint32_t vt_expand(const VecTab& v, uint32_t f, int w) {
   if (v.fast)
@@ -243,29 +235,133 @@ __device__ __forceinline__ void split4(const uint32_t u[4], const uint32_t k[4],
 }
 
 // OR the run o[0..3] (n <= 128 bits, LSB first, zero above n) into the image
-// at bit pos.  Words the run covers entirely belong to it alone.
-__device__ __forceinline__ void img_put(uint32_t* img, uint32_t pos, const uint32_t o[4],
-                                        uint32_t n) {
-  if (n == 0) return;
-  const uint32_t b = pos >> 5, sh = pos & 31;
-  if (sh == 0 && n == 128 && (b & 3) == 0) {
-    *reinterpret_cast<uint4*>(img + b) = make_uint4(o[0], o[1], o[2], o[3]);
-    return;
-  }
-  uint32_t w[5];
-  w[0] = o[0] << sh;
-  w[1] = __funnelshift_l(o[0], o[1], sh);
-  w[2] = __funnelshift_l(o[1], o[2], sh);
-  w[3] = __funnelshift_l(o[2], o[3], sh);
-  w[4] = sh ? (o[3] >> (32 - sh)) : 0u;
-  const uint32_t end = sh + n, nw = (end + 31) >> 5;
-  const bool tail_part = (end & 31) != 0;
+// at bit pos: one shared atomicOr for each of the 5 words from pos / 32 on,
+// with no choice per word (the image is zero before the tile; words past
+// the run take an OR of zero, and the image has slack for them past the
+// tile's last vector).
+__device__ __forceinline__ void img_or(uint32_t* img, uint32_t pos, const uint32_t o[4]) {
+  const uint32_t sh = pos & 31;
+  uint32_t* p = img + (pos >> 5);
+  atomicOr(p, o[0] << sh);
+  atomicOr(p + 1, __funnelshift_l(o[0], o[1], sh));
+  atomicOr(p + 2, __funnelshift_l(o[1], o[2], sh));
+  atomicOr(p + 3, __funnelshift_l(o[2], o[3], sh));
+  atomicOr(p + 4, __funnelshift_l(o[3], 0u, sh));
+}
+
+// Per-thread constants of the packing fast path, for the thread's vector
+// position when every keep mask of its 4 words has at most three runs of
+// ones.  Word j's field is ((x >> a0) & m0) | ((x >> d1) & M1) |
+// ((x >> d2) & M2): each later run is shifted straight to its place in the
+// field (d = the run's start minus the kept bits before it, M = its mask at
+// that place).  k0..k2: kept bits of words 0..2; n: of all four; Pr: kept
+// bits of the chunk before the vector.
+struct PackTab {
+  uint32_t a0[4], m0[4], d1[4], M1[4], d2[4], M2[4];
+  uint32_t k0, k1, k2, n, Pr;
+  bool ok, three;
+};
+
+// From a VecTab on which make_runs (and, for three runs, make_runs3) ran.
+__device__ __forceinline__ void make_packtab(const VecTab& v, PackTab& p) {
+  p.ok = v.fast || v.fast3;
+  p.three = !v.fast && v.fast3;
+  uint32_t k[4];
 #pragma unroll
-  for (uint32_t j = 0; j < 5; ++j) {
-    if (j < nw) {
-      const bool part = (j == 0 && sh != 0) || (j == nw - 1 && tail_part);
-      if (part) atomicOr(img + b + j, w[j]);
-      else img[b + j] = w[j];
+  for (int j = 0; j < 4; ++j) {
+    k[j] = __popc(v.K[j]);
+    p.a0[j] = v.MV[0][j];
+    p.m0[j] = v.MV[1][j];
+    const uint32_t m1 = v.MV[3][j], l0 = v.MV[4][j];  // l0 < 32 when there is a second run
+    p.d1[j] = m1 ? v.MV[2][j] - l0 : 0u;
+    p.M1[j] = m1 << l0;
+    const uint32_t m2 = p.three ? v.R3[1][j] : 0u, l01 = p.three ? v.R3[2][j] : 0u;
+    p.d2[j] = m2 ? v.R3[0][j] - l01 : 0u;
+    p.M2[j] = m2 << l01;
+  }
+  p.k0 = k[0];
+  p.k1 = k[1];
+  p.k2 = k[2];
+  p.n = k[0] + k[1] + k[2] + k[3];
+  p.Pr = v.Pr;
+}
+
+// x << s for s in 0..32 (0 at 32).
+__device__ __forceinline__ uint32_t shl32(uint32_t x, uint32_t s) { return __funnelshift_lc(0u, x, s); }
+
+// The kept bits of the 4 words x as one run o[0..3] (LSB first, zero above
+// p.n): fields concatenated from the last one down, each step a 128-bit
+// shift by the next field's length (clamped funnel shifts: no branches).
+template <bool THREE>
+__device__ __forceinline__ void pack_run(const PackTab& p, const uint4& d, uint32_t o[4]) {
+  const uint32_t x[4] = {d.x, d.y, d.z, d.w};
+  uint32_t f[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[j] = ((x[j] >> p.a0[j]) & p.m0[j]) | ((x[j] >> p.d1[j]) & p.M1[j]);
+    if (THREE) f[j] |= (x[j] >> p.d2[j]) & p.M2[j];
+  }
+  uint32_t o0 = f[3], o1, o2, o3;
+  o1 = __funnelshift_lc(o0, 0u, p.k2);
+  o0 = shl32(o0, p.k2) | f[2];
+  o2 = __funnelshift_lc(o1, 0u, p.k1);
+  o1 = __funnelshift_lc(o0, o1, p.k1);
+  o0 = shl32(o0, p.k1) | f[1];
+  o3 = __funnelshift_lc(o2, 0u, p.k0);
+  o2 = __funnelshift_lc(o1, o2, p.k0);
+  o1 = __funnelshift_lc(o0, o1, p.k0);
+  o0 = shl32(o0, p.k0) | f[0];
+  o[0] = o0;
+  o[1] = o1;
+  o[2] = o2;
+  o[3] = o3;
+}
+
+// Packs the staged tile's vectors v = t, t + NT, ... (< nvec) into the image
+// (fast path: REG positions, run-form keep masks).  E vectors per step: the
+// words and chunk offsets of all E are read before any is placed, so their
+// chains interleave (a placement's shared atomics would otherwise keep the
+// next vector's loads behind them).  spw / sgex: the tile's groups'
+// participation words and bit offsets, read once when the tile is one group
+// (ONEQ); r: the thread's vector position.
+template <bool THREE, bool ONEQ, int E, int NT>
+__device__ __forceinline__ void pack_fast(const PackTab& p, const uint32_t* sd, uint32_t nvec,
+                                          uint32_t twords, const uint32_t* spw,
+                                          const uint32_t* sgex, uint32_t lvpc, uint32_t r,
+                                          uint32_t B, uint32_t m, uint32_t* img, uint32_t t) {
+  const uint32_t pw1 = ONEQ ? spw[0] : 0u, gex1 = ONEQ ? sgex[0] + 32u : 0u;
+  const uint32_t rawpos = 128u * r;
+  for (uint32_t v0 = t; v0 < nvec; v0 += E * NT) {
+    uint4 d[E];
+    uint32_t off[E], in[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const uint32_t v = v0 + e * NT;
+      const uint32_t vv = v < nvec ? v : v0;  // a vector of the tile
+      const uint32_t c = vv >> lvpc, i5 = c & 31;
+      d[e] = *reinterpret_cast<const uint4*>(sd + 4 * vv);
+      const uint32_t pw = ONEQ ? pw1 : spw[c >> 5];
+      const uint32_t g = ONEQ ? gex1 : sgex[c >> 5] + 32u;
+      off[e] = g + i5 * B - (uint32_t)__popc(pw & ((1u << i5) - 1u)) * m;
+      in[e] = (pw >> i5) & 1u;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const uint32_t v = v0 + e * NT;
+      if (v >= nvec) continue;
+      uint32_t o[4];
+      if (in[e]) {
+        pack_run<THREE>(p, d[e], o);
+        off[e] += p.Pr;
+      } else {
+        const uint32_t wv = twords - 4 * v;  // >= 1; < 4 only for a short last vector
+        o[0] = d[e].x;
+        o[1] = wv > 1 ? d[e].y : 0u;
+        o[2] = wv > 2 ? d[e].z : 0u;
+        o[3] = wv > 3 ? d[e].w : 0u;
+        off[e] += rawpos;
+      }
+      img_or(img, off[e], o);
     }
   }
 }
@@ -510,10 +606,14 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
   const unsigned long long tile_raw = 32ull * Q * cb;
   const uint32_t gvec = 8 * W + 1;  // 16-byte vectors of a full group stored raw
 
-  VecTab vt;
+  const uint32_t r_own = (uint32_t)t & (A.vpc - 1);  // REG: every vector's position
+  PackTab pt{};
   if (REG) {
-    load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
-    make_runs(vt);
+    VecTab v0;
+    load_vectab(T, r_own, v0);
+    make_runs(v0);
+    make_runs3(v0);
+    make_packtab(v0, pt);
   }
   for (uint32_t i = t; i < A.img_words / 4; i += NT) img4[i] = make_uint4(0, 0, 0, 0);
 
@@ -639,23 +739,34 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
         }
       }
     } else {
-      if ((uint32_t)t < nq) img[3 + (s_gex[s][t] >> 5)] = s_pw[s][t];
-      // two vectors per thread per step: independent chains to interleave
-      for (uint32_t v0 = t; v0 < nvec; v0 += 2 * NT) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint32_t v = v0 + e * NT;
-          if (v >= nvec) continue;
+      // the group's participation word (atomic: a neighbouring run may OR a
+      // zero into the same word)
+      if ((uint32_t)t < nq) atomicOr(img + (s_gex[s][t] >> 5), s_pw[s][t]);
+      // run-form keep masks: constants in registers; otherwise the position's
+      // tables are read per vector
+      if (REG && pt.ok) {
+        const uint32_t* pw_ = s_pw[s];
+        const uint32_t* gx_ = s_gex[s];
+        if (pt.three) {
+          if (Q == 1) pack_fast<true, true, 2, NT>(pt, sd, nvec, twords, pw_, gx_, A.lvpc, r_own, B, m, img, t);
+          else pack_fast<true, false, 2, NT>(pt, sd, nvec, twords, pw_, gx_, A.lvpc, r_own, B, m, img, t);
+        } else {
+          if (Q == 1) pack_fast<false, true, 2, NT>(pt, sd, nvec, twords, pw_, gx_, A.lvpc, r_own, B, m, img, t);
+          else pack_fast<false, false, 2, NT>(pt, sd, nvec, twords, pw_, gx_, A.lvpc, r_own, B, m, img, t);
+        }
+      } else {
+        for (uint32_t v = t; v < nvec; v += NT) {
           uint32_t c, r;
           vec_pos<REG>(A, v, c, r);
           const uint32_t q = c >> 5, i = c & 31;
           const uint32_t pwq = s_pw[s][q];
-          if (!REG) load_vectab(T, r, vt);
+          VecTab vt;
+          load_vectab(T, r, vt);
           const uint4 d = *reinterpret_cast<const uint4*>(sd + 4 * v);
           const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
           const uint32_t off =
               s_gex[s][q] + 32u + i * B - (uint32_t)__popc(pwq & ((1u << i) - 1u)) * m;
-          uint32_t o[4], n, pos;
+          uint32_t o[4], pos;
           if ((pwq >> i) & 1u) {
             uint32_t f[4];
 #pragma unroll
@@ -663,30 +774,30 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
             uint32_t kk[4];
             kept_bits(vt, kk);
             cat4(f, kk, o);
-            n = kk[0] + kk[1] + kk[2] + kk[3];
             pos = off + vt.Pr;
           } else {
             const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
 #pragma unroll
             for (uint32_t w = 0; w < 4; ++w) o[w] = w < wv ? dw[w] : 0u;
-            n = 32u * wv;
             pos = off + 128u * r;
           }
-          img_put(img, 96u + pos, o, n);
+          img_or(img, pos, o);
         }
       }
       __syncthreads();
-      if (fits) {
-        for (uint32_t u0 = t; u0 < nv; u0 += 4 * NT) {
-          uint4 o[4];
+      // stream vector u is image vector u: copied out, and cleared for the
+      // next tile by the thread that read it
+      for (uint32_t u0 = t; u0 < nv; u0 += 4 * NT) {
+        uint4 o[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t u = u0 + e * NT;
-            if (u < nv) {
-              const uint4 x = img4[u + 1];
-              o[e] = make_uint4(img[4 * u + 3], x.x, x.y, x.z);
-            }
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t u = u0 + e * NT;
+          if (u < nv) {
+            o[e] = img4[u];
+            img4[u] = make_uint4(0, 0, 0, 0);
           }
+        }
+        if (fits) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const uint32_t u = u0 + e * NT;
@@ -695,12 +806,8 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
         }
       }
     }
-    __syncthreads();  // the stage (and the image) have been read
+    __syncthreads();  // the stage has been read, the image cleared
     if (warp == 0) issue(k + S, s);
-    if (!raw) {
-      for (uint32_t u = t; u <= nv; u += NT) img4[u] = make_uint4(0, 0, 0, 0);
-      __syncthreads();  // cleared before the next tile packs into it
-    }
   }
 
   // ---- last block: header and table end
@@ -1031,11 +1138,14 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
   } else {
     // ================================================= pack warps
     const uint32_t gvec = 8 * W + 1;  // 16-byte vectors of a full group stored raw
-    VecTab vt;
+    const uint32_t r_own = (uint32_t)t & (A.vpc - 1);  // REG: every vector's position
+    PackTab pt{};
     if (REG) {
-      load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
-      make_runs(vt);
-      make_runs3(vt);
+      VecTab v0;
+      load_vectab(T, r_own, v0);
+      make_runs(v0);
+      make_runs3(v0);
+      make_packtab(v0, pt);
     }
     if (t == 0)
       for (uint32_t s = 0; s < kWsStages && s < mine; ++s)
@@ -1096,64 +1206,70 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
           }
         }
       } else {
-        if ((uint32_t)t < nq) img[3 + (si.gex[t] >> 5)] = si.pw[t];
-        // Compiled for the general keep masks and for masks of at most three
-        // runs per word (16-bit data); a thread takes the one its vector
-        // position allows (the loop has no warp-wide operation).
-        auto pack_vectors = [&](auto three) {
-        constexpr bool THREE = decltype(three)::value;
-        // two vectors per thread per step: independent chains to interleave
-        for (uint32_t v0 = t; v0 < nvec; v0 += 2 * kWsPack) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const uint32_t v = v0 + e * kWsPack;
-            if (v >= nvec) continue;
+        if ((uint32_t)t < nq) atomicOr(img + (si.gex[t] >> 5), si.pw[t]);
+        // A thread whose vector position has run-form keep masks packs with
+        // its constants in registers; any other reads its position's tables
+        // per vector (the loops have no warp-wide operation).
+        if (REG && pt.ok) {
+          if (pt.three) {
+            if (Q == 1)
+              pack_fast<true, true, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, A.lvpc, r_own,
+                                                B, m, img, t);
+            else
+              pack_fast<true, false, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, A.lvpc, r_own,
+                                                 B, m, img, t);
+          } else {
+            if (Q == 1)
+              pack_fast<false, true, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, A.lvpc, r_own,
+                                                 B, m, img, t);
+            else
+              pack_fast<false, false, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, A.lvpc,
+                                                  r_own, B, m, img, t);
+          }
+        } else {
+          for (uint32_t v = t; v < nvec; v += kWsPack) {
             uint32_t c, r;
             vec_pos<REG>(A, v, c, r);
             const uint32_t q = c >> 5, i5 = c & 31;
             const uint32_t pwq = si.pw[q];
-            if (!REG) load_vectab(T, r, vt);
+            VecTab vt;
+            load_vectab(T, r, vt);
             const uint4 d = *reinterpret_cast<const uint4*>(sd + 4 * v);
             const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
             const uint32_t off =
                 si.gex[q] + 32u + i5 * B - (uint32_t)__popc(pwq & ((1u << i5) - 1u)) * m;
-            uint32_t o[4], n, pos;
+            uint32_t o[4], pos;
             if ((pwq >> i5) & 1u) {
               uint32_t f[4];
 #pragma unroll
-              for (int w = 0; w < 4; ++w) f[w] = THREE ? vt_compress3(vt, dw[w], w) : vt_compress(vt, dw[w], w);
+              for (int w = 0; w < 4; ++w) f[w] = vt_compress(vt, dw[w], w);
               uint32_t kk[4];
               kept_bits(vt, kk);
               cat4(f, kk, o);
-              n = kk[0] + kk[1] + kk[2] + kk[3];
               pos = off + vt.Pr;
             } else {
               const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
 #pragma unroll
               for (uint32_t w = 0; w < 4; ++w) o[w] = w < wv ? dw[w] : 0u;
-              n = 32u * wv;
               pos = off + 128u * r;
             }
-            img_put(img, 96u + pos, o, n);
+            img_or(img, pos, o);
           }
         }
-        };
-        if (REG && vt.fast3) pack_vectors(std::true_type{});
-        else pack_vectors(std::false_type{});
         named_bar(1, kWsPack);
-        if (fits) {
-          // stream vector u is image words 4 u + 3 .. 4 u + 6: a lane loads
-          // image vector u + 1 and takes word 4 u + 3 from the lane before it
-          for (uint32_t u0 = t; u0 - lane < nv; u0 += 4 * kWsPack) {
-            uint4 o[4];
+        // stream vector u is image vector u: copied out, and cleared for the
+        // next tile (the barrier at its top) by the thread that read it
+        for (uint32_t u0 = t; u0 < nv; u0 += 4 * kWsPack) {
+          uint4 o[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t u = u0 + e * kWsPack;
-              const uint4 x = u < nv ? img4[u + 1] : make_uint4(0, 0, 0, 0);
-              uint32_t prev = __shfl_up_sync(kFull, x.w, 1);
-              if (lane == 0) prev = u < nv ? img[4 * u + 3] : 0u;
-              o[e] = make_uint4(prev, x.x, x.y, x.z);
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t u = u0 + e * kWsPack;
+            if (u < nv) {
+              o[e] = img4[u];
+              img4[u] = make_uint4(0, 0, 0, 0);
             }
+          }
+          if (fits) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const uint32_t u = u0 + e * kWsPack;
@@ -1168,8 +1284,6 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
         if (j + kWsStages < mine)
           stage_in(tile + kWsStages * G, stages + (size_t)s * A.stage_bytes, b_sfull + s);
       }
-      if (!raw)  // cleared before the next tile (the barrier at its top)
-        for (uint32_t u = t; u <= nv; u += kWsPack) img4[u] = make_uint4(0, 0, 0, 0);
     }
   }
 

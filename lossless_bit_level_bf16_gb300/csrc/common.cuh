@@ -177,6 +177,26 @@ __device__ __forceinline__ unsigned long long l2_policy_keep() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+__device__ __forceinline__ unsigned long long l2_policy_first() {
+  unsigned long long p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// bulk_g2s with an L2 eviction-priority policy for the lines it reads.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                              unsigned long long* bar, unsigned long long pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+// st_v4 with an L2 eviction-priority policy.
+__device__ __forceinline__ void st_v4_hint(void* p, uint4 v, unsigned long long pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
 // Asks L2 to fetch a contiguous range (16-byte aligned, size a multiple of
 // 16); nothing waits for it.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes,

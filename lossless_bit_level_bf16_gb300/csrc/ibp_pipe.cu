@@ -70,6 +70,7 @@ struct PipeArgs {
   uint32_t cb, vpc, lvpc;  // chunk bytes, 16-byte vectors per chunk, log2 (REG)
   uint32_t Q, S, stage_bytes, img_words;
   uint32_t* lens;  // single-pass encode: every tile's published stream length
+  uint32_t lag;    // single-pass encode in pieces: waves between a group's match and its packing
 };
 
 // Mask tables of the 4 words at vector position r of a chunk.  When every
@@ -321,15 +322,19 @@ __device__ __forceinline__ void pack_run(const PackTab& p, const uint4& d, uint3
 // (fast path: REG positions, run-form keep masks).  E vectors per step: the
 // words and chunk offsets of all E are read before any is placed, so their
 // chains interleave (a placement's shared atomics would otherwise keep the
-// next vector's loads behind them).  spw / sgex: the tile's groups'
-// participation words and bit offsets, read once when the tile is one group
-// (ONEQ); r: the thread's vector position.
+// next vector's loads behind them).  Several groups (not ONEQ): spw / sgex
+// hold the groups' participation words and bit offsets.  One group (ONEQ):
+// pw1 is its participation word, the staged vectors belong to its chunks
+// cbase, cbase + 1, ..., and chunk c's body starts at image bit
+// g1 + c * B - (kept-bit savings of the chunks before it), g1 folding in
+// the group's first image bit and its 32 participation bits.  r: the
+// thread's vector position.
 template <bool THREE, bool ONEQ, int E, int NT>
 __device__ __forceinline__ void pack_fast(const PackTab& p, const uint32_t* sd, uint32_t nvec,
                                           uint32_t twords, const uint32_t* spw,
-                                          const uint32_t* sgex, uint32_t lvpc, uint32_t r,
-                                          uint32_t B, uint32_t m, uint32_t* img, uint32_t t) {
-  const uint32_t pw1 = ONEQ ? spw[0] : 0u, gex1 = ONEQ ? sgex[0] + 32u : 0u;
+                                          const uint32_t* sgex, uint32_t pw1, uint32_t g1,
+                                          uint32_t cbase, uint32_t lvpc, uint32_t r, uint32_t B,
+                                          uint32_t m, uint32_t* img, uint32_t t) {
   const uint32_t rawpos = 128u * r;
   for (uint32_t v0 = t; v0 < nvec; v0 += E * NT) {
     uint4 d[E];
@@ -338,10 +343,10 @@ __device__ __forceinline__ void pack_fast(const PackTab& p, const uint32_t* sd, 
     for (int e = 0; e < E; ++e) {
       const uint32_t v = v0 + e * NT;
       const uint32_t vv = v < nvec ? v : v0;  // a vector of the tile
-      const uint32_t c = vv >> lvpc, i5 = c & 31;
+      const uint32_t c = (ONEQ ? cbase : 0u) + (vv >> lvpc), i5 = c & 31;
       d[e] = *reinterpret_cast<const uint4*>(sd + 4 * vv);
       const uint32_t pw = ONEQ ? pw1 : spw[c >> 5];
-      const uint32_t g = ONEQ ? gex1 : sgex[c >> 5] + 32u;
+      const uint32_t g = ONEQ ? g1 : sgex[c >> 5] + 32u;
       off[e] = g + i5 * B - (uint32_t)__popc(pw & ((1u << i5) - 1u)) * m;
       in[e] = (pw >> i5) & 1u;
     }
@@ -747,12 +752,17 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
       if (REG && pt.ok) {
         const uint32_t* pw_ = s_pw[s];
         const uint32_t* gx_ = s_gex[s];
+        const uint32_t pw1 = pw_[0], g1 = gx_[0] + 32u;
         if (pt.three) {
-          if (Q == 1) pack_fast<true, true, 2, NT>(pt, sd, nvec, twords, pw_, gx_, A.lvpc, r_own, B, m, img, t);
-          else pack_fast<true, false, 2, NT>(pt, sd, nvec, twords, pw_, gx_, A.lvpc, r_own, B, m, img, t);
+          if (Q == 1)
+            pack_fast<true, true, 2, NT>(pt, sd, nvec, twords, pw_, gx_, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
+          else
+            pack_fast<true, false, 2, NT>(pt, sd, nvec, twords, pw_, gx_, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
         } else {
-          if (Q == 1) pack_fast<false, true, 2, NT>(pt, sd, nvec, twords, pw_, gx_, A.lvpc, r_own, B, m, img, t);
-          else pack_fast<false, false, 2, NT>(pt, sd, nvec, twords, pw_, gx_, A.lvpc, r_own, B, m, img, t);
+          if (Q == 1)
+            pack_fast<false, true, 2, NT>(pt, sd, nvec, twords, pw_, gx_, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
+          else
+            pack_fast<false, false, 2, NT>(pt, sd, nvec, twords, pw_, gx_, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
         }
       } else {
         for (uint32_t v = t; v < nvec; v += NT) {
@@ -852,6 +862,7 @@ constexpr int kWsPack = 128, kWsThreads = kWsPack + 32;
 constexpr uint32_t kWsLag = 3, kWsInfo = 2, kWsStages = 2;  // D = 3 waves (measured best)
 constexpr uint32_t kWsLensBytes = 2048;                  // a wave's lengths, padded
 constexpr unsigned kWsMaxGrid = kWsLensBytes / 4 - 8;    // 504 tiles per wave
+std::atomic<int> g_wsp_lag{2};  // waves between a group's match and its packing (pieces; 2 measured best)
 
 struct WsInfo {
   unsigned long long base;  // the tile's first stream bit, from the payload start
@@ -1211,20 +1222,21 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
         // its constants in registers; any other reads its position's tables
         // per vector (the loops have no warp-wide operation).
         if (REG && pt.ok) {
+          const uint32_t pw1 = si.pw[0], g1 = si.gex[0] + 32u;
           if (pt.three) {
             if (Q == 1)
-              pack_fast<true, true, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, A.lvpc, r_own,
-                                                B, m, img, t);
+              pack_fast<true, true, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, pw1, g1, 0u,
+                                                A.lvpc, r_own, B, m, img, t);
             else
-              pack_fast<true, false, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, A.lvpc, r_own,
-                                                 B, m, img, t);
+              pack_fast<true, false, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, pw1, g1, 0u,
+                                                 A.lvpc, r_own, B, m, img, t);
           } else {
             if (Q == 1)
-              pack_fast<false, true, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, A.lvpc, r_own,
-                                                 B, m, img, t);
+              pack_fast<false, true, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, pw1, g1, 0u,
+                                                 A.lvpc, r_own, B, m, img, t);
             else
-              pack_fast<false, false, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, A.lvpc,
-                                                  r_own, B, m, img, t);
+              pack_fast<false, false, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, pw1, g1, 0u,
+                                                  A.lvpc, r_own, B, m, img, t);
           }
         } else {
           for (uint32_t v = t; v < nvec; v += kWsPack) {
@@ -1300,6 +1312,420 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
   const unsigned long long pay = A.ngroups ? grp[A.ngroups] : 0ull;
   ibp_write_tail(A.meta, cb, m, A.n_bytes, A.nchunks, A.ngroups, A.dst, A.dst_cap, A.off_payload,
                  A.out_bytes, A.ctrl, pay, t, kWsThreads);
+}
+
+// ------------------------------------------ single-pass encode in pieces
+//
+// For chunks of 1024 and 2048 bytes a group is 32 or 64 KB of input, too
+// large to stage whole beside a match stage.  Here a block takes whole
+// groups (tile = group; block b owns groups b, b + G, ...) and moves each
+// through shared memory in pieces of 16 KB (cpp = 16 or 8 chunks, np = 2 or
+// 4 pieces per group).
+//   The control warp matches a group piece by piece from two stages (the
+//   next piece's copy in flight while it matches one), publishes the group's
+//   stream length after its last piece, and resolves the group of wave
+//   i - D (D = A.lag, 1..3) as the single-pass encoder above does.
+//   The pack warps take the pieces through two stages of their own.  A piece
+//   is packed into an image of its part of the group's stream, starting at
+//   the 16-byte vector that holds the piece's first bit; that vector already
+//   holds the previous piece's bits in it.  The full vectors are written
+//   out and the partial last one is moved to the front for the next piece.
+//   A group's stream is thus written by one block, in order, 16 bytes at a
+//   time: no block waits for another's output.
+constexpr int kWspPack = 128, kWspThreads = kWspPack + 32;
+constexpr uint32_t kWspPiece = 16384;  // input bytes per piece
+
+__host__ __device__ inline size_t wsp_smem_bytes(uint32_t cb, uint32_t stage_bytes,
+                                                 uint32_t img_words) {
+  return 4 * ibp_table_words(cb / 4) + 4ull * stage_bytes + 4ull * img_words +
+         2ull * kWsLensBytes + 8ull * (4 + 2 * kWsInfo);
+}
+
+// Bits below bit n (n <= 32).
+__device__ __forceinline__ uint32_t lowmask(uint32_t n) { return n >= 32 ? 0xFFFFFFFFu : (1u << n) - 1u; }
+
+template <int VPW>  // 16-byte vectors of a chunk per lane of a warp (vpc / 32)
+__global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs A) {
+  extern __shared__ __align__(128) uint8_t dyn[];
+  __shared__ uint32_t s_scr[kWspThreads / 32 + 4];
+  __shared__ WsInfo s_info[kWsInfo];
+  __shared__ uint32_t s_cpw[4];  // control warp: matched groups' participation words
+  __shared__ int s_last;
+  constexpr uint32_t vpc = 32 * VPW;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t cb = A.cb, W = cb / 4, B = 8 * cb;
+  const uint32_t cpp = kWspPiece / cb, np = 32 / cpp;  // chunks per piece, pieces per group
+  const uint32_t lag = A.lag;
+  const unsigned long long G = gridDim.x, bid = blockIdx.x;
+
+  uint32_t* tab = reinterpret_cast<uint32_t*>(dyn);
+  uint8_t* pstages = dyn + 4 * ibp_table_words(W);
+  uint8_t* mstages = pstages + 2ull * A.stage_bytes;
+  uint32_t* img = reinterpret_cast<uint32_t*>(mstages + 2ull * A.stage_bytes);
+  uint4* img4 = reinterpret_cast<uint4*>(img);
+  uint8_t* lensbuf = reinterpret_cast<uint8_t*>(img + A.img_words);
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(lensbuf + 2 * kWsLensBytes);
+  unsigned long long* b_sfull = bars;        // pack stages landed
+  unsigned long long* b_mfull = bars + 2;    // match stages landed
+  unsigned long long* b_ifull = bars + 4;    // slot handed over
+  unsigned long long* b_iempty = b_ifull + kWsInfo;  // slot read
+  unsigned long long* grp = reinterpret_cast<unsigned long long*>(A.dst + kIbp1Header);
+
+  IbpTables T;
+  if (!ibp_load_tables<kWspThreads>(A.meta, cb, tab, T, s_scr)) {  // the same in every block
+    if (t == 0) set_status(A.ctrl, ZC_ERR_META_MISMATCH);
+    return;
+  }
+  const uint32_t m = T.m;
+  const unsigned long long group_raw = 32ull * cb;
+  const unsigned long long tail_bytes = A.n_bytes - (A.nchunks ? (A.nchunks - 1) * cb : 0ull);
+  const bool short_tail = A.nchunks && tail_bytes != cb;
+  const uint32_t mine = bid < A.ntiles ? (uint32_t)((A.ntiles - bid + G - 1) / G) : 0u;
+  // input bytes of piece p of group g (0: no such piece)
+  auto piece_bytes = [&](unsigned long long g, uint32_t p) -> uint32_t {
+    const unsigned long long b0 = g * group_raw + (unsigned long long)p * kWspPiece;
+    if (b0 >= A.n_bytes) return 0u;
+    return (uint32_t)((A.n_bytes - b0) < kWspPiece ? (A.n_bytes - b0) : kWspPiece);
+  };
+  // one thread: copy this block's piece number seq (its group seq / np, piece
+  // seq % np) into a stage (its last 4..12 bytes with plain loads), with an
+  // L2 policy for the lines read: the match keeps them for the pack warps'
+  // second read, which lets them go
+  auto stage_piece = [&](uint32_t seq, uint8_t* st, unsigned long long* bar,
+                         unsigned long long pol) {
+    const uint32_t k = seq / np, p = seq % np;
+    if (k >= mine) return;
+    const unsigned long long g = bid + (unsigned long long)k * G;
+    const uint32_t tb = piece_bytes(g, p), b16 = tb & ~15u;
+    if (tb == 0) return;
+    const unsigned long long b0 = g * group_raw + (unsigned long long)p * kWspPiece;
+    for (uint32_t w = b16 / 4; w < tb / 4; ++w)
+      reinterpret_cast<uint32_t*>(st)[w] = __ldg(reinterpret_cast<const uint32_t*>(A.src + b0) + w);
+    if (b16 != tb) fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, b16);
+    if (b16) bulk_g2s_hint(st, A.src + b0, b16, bar, pol);
+  };
+  if (t == 0) {
+    for (uint32_t s = 0; s < 2; ++s) {
+      mbar_init(b_sfull + s, 1);
+      mbar_init(b_mfull + s, 1);
+    }
+    for (uint32_t k = 0; k < kWsInfo; ++k) {
+      mbar_init(b_ifull + k, 1);
+      mbar_init(b_iempty + k, 1);
+    }
+  }
+  for (uint32_t i = t; i < A.img_words / 4; i += kWspThreads) img4[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+
+  if (warp == kWspPack / 32) {
+    // ================================================= control warp
+    // lane l matches vector positions l, l + 32, ... of every chunk
+    uint32_t cK[VPW][4], cV[VPW][4];
+#pragma unroll
+    for (int k = 0; k < VPW; ++k)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        cK[k][q] = T.K[4 * (lane + 32 * k) + q];
+        cV[k][q] = T.V[4 * (lane + 32 * k) + q];
+      }
+    auto differs = [&](const uint32_t* sd, uint32_t c) -> uint32_t {
+      uint32_t x = 0;
+#pragma unroll
+      for (int k = 0; k < VPW; ++k) {
+        const uint4 d = *reinterpret_cast<const uint4*>(sd + 4 * (c * vpc + 32 * k + lane));
+        x |= ((d.x ^ cV[k][0]) & ~cK[k][0]) | ((d.y ^ cV[k][1]) & ~cK[k][1]) |
+             ((d.z ^ cV[k][2]) & ~cK[k][2]) | ((d.w ^ cV[k][3]) & ~cK[k][3]);
+      }
+      return x;
+    };
+    // lengths of the groups of wave w into lens buffer w & 1 (as in the
+    // single-pass encoder)
+    auto lens_fetch = [&](uint32_t w) {
+      if (w < mine) {
+        const unsigned long long wf = (unsigned long long)w * G, la0 = wf & ~3ull;
+        const uint32_t nw = (uint32_t)((A.ntiles - wf) < G ? (A.ntiles - wf) : G);
+        const uint32_t nv4 = (uint32_t)((wf + nw - la0 + 3) / 4);
+        uint8_t* lb = lensbuf + (w & 1u) * kWsLensBytes;
+        for (uint32_t vi = lane; vi < nv4; vi += 32) cp_async16(lb + 16u * vi, A.lens + la0 + 4ull * vi);
+      }
+      cp_async_commit();
+    };
+    const unsigned long long keep = l2_policy_keep();
+    if (lane == 0) {
+      stage_piece(0, mstages, b_mfull, keep);
+      stage_piece(1, mstages + A.stage_bytes, b_mfull + 1, keep);
+    }
+    const unsigned lim = wait_limit(A.ctrl);
+    const unsigned long long fault1 = A.ctrl->fault_tile1;  // 0 unless a wait-failure test
+    unsigned long long wave_base = 0;  // 128-bit units of the waves resolved so far
+    for (uint32_t i = 0; i < mine + lag; ++i) {
+      if (i < mine) {
+        // ---- match the group of wave i, piece by piece
+        const unsigned long long g = bid + (unsigned long long)i * G;
+        uint32_t bad = 0;  // the same in every lane
+        for (uint32_t p = 0; p < np; ++p) {
+          const uint32_t tb = piece_bytes(g, p);
+          if (tb == 0) break;
+          const uint32_t seq = i * np + p, ms = seq & 1u;
+          if (!mbar_wait(b_mfull + ms, (seq >> 1) & 1u)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+          const uint32_t* sd = reinterpret_cast<const uint32_t*>(mstages + (size_t)ms * A.stage_bytes);
+          const uint32_t nfull = tb / cb;  // a short last chunk never participates
+          uint32_t c = 0;
+          for (; c + 2 <= nfull; c += 2) {
+            const uint32_t x0 = differs(sd, c), x1 = differs(sd, c + 1);
+            if (__any_sync(kFull, x0 != 0)) bad |= 1u << (p * cpp + c);
+            if (__any_sync(kFull, x1 != 0)) bad |= 1u << (p * cpp + c + 1);
+          }
+          if (c < nfull && __any_sync(kFull, differs(sd, c) != 0)) bad |= 1u << (p * cpp + c);
+          __syncwarp();  // the match stage has been read
+          if (lane == 0) stage_piece(seq + 2, mstages + (size_t)ms * A.stage_bytes, b_mfull + ms, keep);
+        }
+        const unsigned long long c0 = 32ull * g;
+        const uint32_t nch = (uint32_t)((A.nchunks - c0) < 32 ? (A.nchunks - c0) : 32);
+        uint32_t valid = nch >= 32 ? kFull : ((1u << nch) - 1u);
+        if (short_tail && c0 + nch == A.nchunks) valid &= ~(1u << (nch - 1));
+        const uint32_t pw = m ? (~bad & valid) : 0u;
+        const uint32_t units = (uint32_t)(ibp_group_bits(g, pw, A.nchunks, tail_bytes, cb, m) >> 7);
+        if (lane == 0) {
+          s_cpw[i % (lag + 1)] = pw;
+          if (g + 1 != fault1) st_relaxed_u32(A.lens + g, 0x80000000u | units);
+        }
+      }
+      if (i + 1 == lag) lens_fetch(0);
+      if (i >= lag) {
+        // ---- resolve the group of wave j = i - D and hand it over
+        const uint32_t j = i - lag;
+        const unsigned long long wf = (unsigned long long)j * G, la0 = wf & ~3ull;
+        const uint32_t nw = (uint32_t)((A.ntiles - wf) < G ? (A.ntiles - wf) : G);
+        const uint32_t nv4 = (uint32_t)((wf + nw - la0 + 3) / 4);
+        uint4* lb = reinterpret_cast<uint4*>(lensbuf + (j & 1u) * kWsLensBytes);
+        cp_async_wait_all();
+        __syncwarp();
+        uint32_t pre = 0, tot = 0;
+        for (unsigned spins = 0;; ++spins) {
+          bool all = true;
+          pre = 0;
+          tot = 0;
+          for (uint32_t vi = lane; vi < nv4; vi += 32) {
+            const uint4 e4 = lb[vi];
+            const uint32_t e[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+            for (uint32_t q = 0; q < 4; ++q) {
+              const unsigned long long idx = la0 + 4ull * vi + q;  // group index
+              if (idx >= wf && idx < wf + nw) {
+                if (!(e[q] >> 31)) all = false;
+                const uint32_t u = e[q] & 0x7FFFFFFFu;
+                tot += u;
+                if (idx < wf + bid) pre += u;
+              }
+            }
+          }
+          if (__all_sync(kFull, all)) break;
+          if (spins >= lim) {
+            if (lane == 0) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+            break;
+          }
+          // the call has failed: no more waiting (one vote for the warp)
+          if (__any_sync(kFull, get_status(A.ctrl) != 0)) break;
+          __nanosleep(spins < 64 ? 32 : 256);
+          for (uint32_t vi = lane; vi < nv4; vi += 32) lb[vi] = ld_relaxed_v4(A.lens + la0 + 4ull * vi);
+          __syncwarp();
+        }
+        __syncwarp();  // lens buffer j & 1 has been read
+        lens_fetch(j + 1);
+        pre = __reduce_add_sync(kFull, pre);
+        tot = __reduce_add_sync(kFull, tot);
+        const unsigned long long base = (wave_base + pre) * 128ull;
+        wave_base += tot;
+        const unsigned long long g = bid + wf;
+        const uint32_t pw = s_cpw[j % (lag + 1)];
+        const uint32_t gb = (uint32_t)ibp_group_bits(g, pw, A.nchunks, tail_bytes, cb, m);
+        if (lane == 0) {
+          grp[g] = base;
+          if (g + 1 == A.ntiles) grp[A.ngroups] = base + gb;
+        }
+        // slot j % R, once the pack warps have read its previous contents
+        const uint32_t k = j % kWsInfo, f = j / kWsInfo;
+        if (f > 0 && !mbar_wait(b_iempty + k, (f - 1) & 1u)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+        if (lane == 0) {
+          WsInfo& si = s_info[k];
+          si.base = base;
+          si.pw[0] = pw;
+          si.gex[0] = 0;
+          si.agg = gb;
+          si.raw = pw == 0;
+          mbar_arrive(b_ifull + k);
+        }
+        __syncwarp();
+      }
+    }
+    cp_async_wait_all();
+  } else {
+    // ================================================= pack warps
+    const uint32_t r_own = (uint32_t)t & (vpc - 1);  // every vector's position
+    PackTab pt{};
+    {
+      VecTab v0;
+      load_vectab(T, r_own, v0);
+      make_runs(v0);
+      make_runs3(v0);
+      make_packtab(v0, pt);
+    }
+    const unsigned long long drop = l2_policy_first();
+    if (t == 0) {
+      stage_piece(0, pstages, b_sfull, drop);
+      stage_piece(1, pstages + A.stage_bytes, b_sfull + 1, drop);
+    }
+    uint32_t carry = 0;  // thread 0, raw groups: the previous piece's last input word
+    for (uint32_t j = 0; j < mine; ++j) {
+      const uint32_t k = j % kWsInfo;
+      if (!mbar_wait(b_ifull + k, (j / kWsInfo) & 1u)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+      const unsigned long long base = s_info[k].base;
+      const uint32_t pw = s_info[k].pw[0], agg = s_info[k].agg;
+      const bool raw = s_info[k].raw != 0;
+      named_bar(1, kWspPack);  // every pack thread has read the slot
+      if (t == 0) mbar_arrive(b_iempty + k);
+      const unsigned long long g = bid + (unsigned long long)j * G;
+      const unsigned long long dst0 = A.off_payload + (base >> 3);
+      const bool fits = dst0 + (agg >> 3) <= A.dst_cap;
+      if (!fits && t == 0) set_status(A.ctrl, ZC_ERR_CAPACITY);
+      carry = 0;  // a raw group's participation word
+      for (uint32_t p = 0; p < np; ++p) {
+        const uint32_t tb = piece_bytes(g, p);
+        if (tb == 0) break;
+        const bool last = p + 1 == np || piece_bytes(g, p + 1) == 0;
+        const uint32_t seq = j * np + p, s = seq & 1u;
+        if (!mbar_wait(b_sfull + s, (seq >> 1) & 1u)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+        const uint32_t* sd = reinterpret_cast<const uint32_t*>(pstages + (size_t)s * A.stage_bytes);
+        const uint32_t twords = tb / 4, nvec = (tb + 15) / 16;
+        const uint32_t c0 = p * cpp;  // the piece's first chunk in the group
+        if (raw) {
+          // [0][input words][zero padding]: output vector u of piece p is
+          // stream words 4096 p + 4 u .. + 3, i.e. the piece's input words
+          // 4 u - 1 .. 4 u + 2 (word -1: the previous piece's last word)
+          const uint32_t ibase = c0 * B;  // the piece's first 128-bit boundary
+          const uint32_t nfull = last ? (agg - ibase) >> 7 : kWspPiece / 16;
+          const unsigned long long dst = dst0 + (ibase >> 3);
+          for (uint32_t u0 = t; u0 - lane < nfull; u0 += 4 * kWspPack) {
+            uint4 o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t u = u0 + e * kWspPack;
+              uint4 x = make_uint4(0, 0, 0, 0);
+              if (u < nfull) {
+                if (4 * u + 3 < twords) {
+                  x = *reinterpret_cast<const uint4*>(sd + 4 * u);
+                } else {
+                  x.x = 4 * u < twords ? sd[4 * u] : 0u;
+                  x.y = 4 * u + 1 < twords ? sd[4 * u + 1] : 0u;
+                  x.z = 4 * u + 2 < twords ? sd[4 * u + 2] : 0u;
+                }
+              }
+              uint32_t prev = __shfl_up_sync(kFull, x.w, 1);
+              if (lane == 0)
+                prev = u == 0 ? carry : ((u < nfull && 4 * u - 1 < twords) ? sd[4 * u - 1] : 0u);
+              o[e] = make_uint4(prev, x.x, x.y, x.z);
+            }
+            if (fits) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const uint32_t u = u0 + e * kWspPack;
+                if (u < nfull) st_v4_hint(A.dst + dst + 16ull * u, o[e], drop);
+              }
+            }
+          }
+          if (t == 0) carry = sd[twords - 1];
+          named_bar(1, kWspPack);  // the stage has been read
+          if (t == 0) stage_piece(seq + 2, pstages + (size_t)s * A.stage_bytes, b_sfull + s, drop);
+        } else {
+          // bit P of the group's stream starts the piece; the image holds the
+          // stream from ibase = P rounded down to 128 bits
+          const uint32_t P = 32u + c0 * B - (uint32_t)__popc(pw & lowmask(c0)) * m;
+          const uint32_t ibase = P & ~127u;
+          const uint32_t Pn = last ? agg : 32u + (c0 + cpp) * B - (uint32_t)__popc(pw & lowmask(c0 + cpp)) * m;
+          const uint32_t nfull = (Pn - ibase) >> 7;  // vectors complete after this piece
+          if (p == 0 && t == 0) atomicOr(img, pw);  // the participation word
+          const uint32_t g1 = 32u - ibase;  // modulo 2^32: chunk starts relative to the image
+          if (pt.ok) {
+            if (pt.three)
+              pack_fast<true, true, 2, kWspPack>(pt, sd, nvec, twords, nullptr, nullptr, pw, g1, c0,
+                                                 A.lvpc, r_own, B, m, img, t);
+            else
+              pack_fast<false, true, 2, kWspPack>(pt, sd, nvec, twords, nullptr, nullptr, pw, g1, c0,
+                                                  A.lvpc, r_own, B, m, img, t);
+          } else {
+            for (uint32_t v = t; v < nvec; v += kWspPack) {
+              const uint32_t c = c0 + (v >> A.lvpc);
+              VecTab vt;
+              load_vectab(T, r_own, vt);
+              const uint4 d = *reinterpret_cast<const uint4*>(sd + 4 * v);
+              const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+              const uint32_t off = g1 + c * B - (uint32_t)__popc(pw & lowmask(c)) * m;
+              uint32_t o[4], pos;
+              if ((pw >> c) & 1u) {
+                uint32_t f[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) f[w] = vt_compress(vt, dw[w], w);
+                uint32_t kk[4];
+                kept_bits(vt, kk);
+                cat4(f, kk, o);
+                pos = off + vt.Pr;
+              } else {
+                const uint32_t wv = (twords - 4 * v) < 4u ? (twords - 4 * v) : 4u;
+#pragma unroll
+                for (uint32_t w = 0; w < 4; ++w) o[w] = w < wv ? dw[w] : 0u;
+                pos = off + 128u * r_own;
+              }
+              img_or(img, pos, o);
+            }
+          }
+          named_bar(1, kWspPack);  // the piece is in the image; the stage has been read
+          if (t == 0) stage_piece(seq + 2, pstages + (size_t)s * A.stage_bytes, b_sfull + s, drop);
+          const unsigned long long dst = dst0 + (ibase >> 3);
+          for (uint32_t u0 = t; u0 < nfull; u0 += 4 * kWspPack) {
+            uint4 o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t u = u0 + e * kWspPack;
+              if (u < nfull) {
+                o[e] = img4[u];
+                img4[u] = make_uint4(0, 0, 0, 0);
+              }
+            }
+            if (fits) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const uint32_t u = u0 + e * kWspPack;
+                if (u < nfull) st_v4_hint(A.dst + dst + 16ull * u, o[e], drop);
+              }
+            }
+          }
+          // the partial vector (the next piece's first) to the front: thread 0
+          // copied out vector 0 above, and no thread copies vector nfull
+          if (t == 0 && !last && nfull > 0) {
+            img4[0] = img4[nfull];
+            img4[nfull] = make_uint4(0, 0, 0, 0);
+          }
+          named_bar(1, kWspPack);  // the image is ready for the next piece
+        }
+      }
+    }
+  }
+
+  // ---- last block: header and table end
+  __syncthreads();
+  if (t == 0) {
+    __threadfence();
+    const unsigned long long dn = atomicAdd(&A.ctrl->done, 1ull);
+    s_last = (dn == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const unsigned long long pay = A.ngroups ? grp[A.ngroups] : 0ull;
+  ibp_write_tail(A.meta, cb, m, A.n_bytes, A.nchunks, A.ngroups, A.dst, A.dst_cap, A.off_payload,
+                 A.out_bytes, A.ctrl, pay, t, kWspThreads);
 }
 
 template <int NT, bool REG>
@@ -1759,19 +2185,71 @@ cudaError_t ibp_ws_compress(const void* d_meta, uint32_t cb, const void* d_x,
                                      smem, s);
 }
 
+// The single-pass encoder in pieces, for chunks of 1024 and 2048 bytes (a
+// group per tile, moved through shared memory 16 KB at a time).
+cudaError_t ibp_wsp_compress(const void* d_meta, uint32_t cb, const void* d_x,
+                             unsigned long long n_bytes, void* d_out, unsigned long long out_cap,
+                             unsigned long long* d_out_bytes, void* d_ws, cudaStream_t s) {
+  const unsigned long long nchunks = (n_bytes + cb - 1) / cb, ngroups = (nchunks + 31) / 32;
+  PipeArgs A{};
+  A.meta = static_cast<const uint8_t*>(d_meta);
+  A.src = static_cast<const uint8_t*>(d_x);
+  A.dst = static_cast<uint8_t*>(d_out);
+  A.dst_cap = out_cap;
+  A.n_bytes = n_bytes;
+  A.cb = cb;
+  A.nchunks = nchunks;
+  A.ngroups = ngroups;
+  A.ntiles = ngroups;
+  A.off_payload = kIbp1Header + round_up(8ull * (ngroups + 1), 128);
+  A.out_bytes = d_out_bytes;
+  A.ctrl = static_cast<Ctrl*>(d_ws);
+  A.lens = reinterpret_cast<uint32_t*>(static_cast<char*>(d_ws) + kCtrlBytes);
+  A.vpc = cb / 16;
+  A.lvpc = 0;
+  while ((1u << A.lvpc) < A.vpc) ++A.lvpc;
+  A.Q = 1;
+  A.S = 2;
+  A.stage_bytes = (uint32_t)(round_up(kWspPiece, 128) + kStageSlack);
+  A.img_words = kWspPiece / 4 + 16;
+  A.lag = g_wsp_lag.load();
+  const size_t smem = wsp_smem_bytes(cb, A.stage_bytes, A.img_words);
+  auto k = cb == 2048 ? ibp_encode_wsp_kernel<4> : ibp_encode_wsp_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  unsigned long long grid = (unsigned long long)resident_blocks((const void*)k, kWspThreads, smem);
+  if (grid > kWsMaxGrid) grid = kWsMaxGrid;
+  if (grid > A.ntiles) grid = A.ntiles;
+  if (grid == 0) grid = 1;
+  // workspace: control block | one length word per group (+ one vector of slack)
+  e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + 4ull * A.ntiles + 16, s);
+  if (e != cudaSuccess) return e;
+  e = arm_wait_fault(d_ws, s);
+  if (e != cudaSuccess) return e;
+  // blocks wait for every other block's group lengths: the whole grid must
+  // be resident at once (see ibp_ws_compress)
+  void* kargs[] = {&A};
+  return cudaLaunchCooperativeKernel((const void*)k, dim3((unsigned)grid), dim3(kWspThreads), kargs,
+                                     smem, s);
+}
+
 std::atomic<int> g_single_pass{1};  // 0: the three-launch encode for every chunk size (tests)
 
 }  // namespace
 
 void ibp_set_single_pass(int on) { g_single_pass.store(on ? 1 : 0); }
 
+void ibp_set_wsp_lag(int lag) { g_wsp_lag.store(lag < 1 ? 1 : (lag > 3 ? 3 : lag)); }
+
 bool ibp_pipe_supported(uint32_t cb, bool encode) { return cb <= 2048 && pick(cb, encode).ok; }
 
 cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t cb, const void* d_x,
                               unsigned long long n_bytes, void* d_out, unsigned long long out_cap,
                               unsigned long long* d_out_bytes, void* d_ws, cudaStream_t s) {
-  if (cb <= 512 && g_single_pass.load()) {
-    const cudaError_t e = ibp_ws_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap, d_out_bytes, d_ws, s);
+  if ((cb <= 512 || cb == 1024 || cb == 2048) && g_single_pass.load()) {
+    const cudaError_t e =
+        cb <= 512 ? ibp_ws_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap, d_out_bytes, d_ws, s)
+                  : ibp_wsp_compress(d_meta, cb, d_x, n_bytes, d_out, out_cap, d_out_bytes, d_ws, s);
     if (e != cudaErrorCooperativeLaunchTooLarge) return e;
     cudaGetLastError();  // the grid cannot be resident at once here: three launches instead
   }

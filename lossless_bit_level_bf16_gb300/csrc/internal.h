@@ -136,6 +136,9 @@ bool ibp_pipe_supported(uint32_t chunk_bytes, bool encode);
 // the three-launch encode, the path taken when the single-pass encoder's grid
 // cannot be resident at once.
 void ibp_set_single_pass(int on);
+// Waves between a group's match and its packing in the single-pass encoder
+// for 1024- and 2048-byte chunks (1..3; tests and measurements).
+void ibp_set_wsp_lag(int lag);
 cudaError_t ibp_pipe_compress(const void* d_meta, uint32_t chunk_bytes, const void* d_x,
                               unsigned long long n_bytes, void* d_out,
                               unsigned long long out_cap, unsigned long long* d_out_bytes,

@@ -57,7 +57,7 @@ def test_meta_table_rows(mode):
     assert (mode == 0 and m >= 512) or (mode == 1 and 400 <= m <= 640)
 
 
-@pytest.mark.parametrize("cb", [16, 48, 64, 512, 1040, 2048, 4096])
+@pytest.mark.parametrize("cb", [16, 48, 64, 512, 1024, 1040, 2048, 4096])
 @pytest.mark.parametrize("frac", [0.0, 0.12, 0.5, 1.0])
 def test_random_masks(cb, frac):
     rng = np.random.default_rng(cb * 10 + int(frac * 100))
@@ -270,14 +270,15 @@ def test_host_resident_input_and_streams(cb):
     assert rc == abi.ZC_ERR_ARG
 
 
+@pytest.mark.parametrize("cb", [512, 2048])
 @pytest.mark.parametrize("mode", [0, 1])
-def test_bf16_weights(mode):
-    """IBP on 16-bit data: bf16 N(0, 0.02) weights in 512-byte chunks (256
-    values).  The codec sees bytes; metadata and stream must equal the
-    oracle's, the round trip must be exact, and the sign/exponent bits that
-    the weights share make the stream smaller than the input."""
-    cb = 512
-    x16 = W.zc_gaussian(256 * 1000 + 128, sigma=0.02, seed=21, device=DEV)  # ragged last chunk
+def test_bf16_weights(mode, cb):
+    """IBP on 16-bit data: bf16 N(0, 0.02) weights in 512- and 2048-byte
+    chunks (256 and 1024 values; keep masks of three runs per word).  The
+    codec sees bytes; metadata and stream must equal the oracle's, the round
+    trip must be exact, and the sign/exponent bits that the weights share
+    make the stream smaller than the input."""
+    x16 = W.zc_gaussian((cb // 2) * 1000 + 128, sigma=0.02, seed=21, device=DEV)  # ragged last chunk
     xb = W.bf16_bits(x16).view("uint8")
     x32 = x16.view(torch.int32).view(torch.float32)
     idx = W.sample_rows(x32.numel() * 4 // cb, 600, seed=2, device=DEV)
@@ -297,16 +298,17 @@ def test_bf16_weights(mode):
 
 
 @pytest.mark.parametrize("mode", [0, 1])
-def test_three_launch_encode_for_small_chunks(mode):
-    """The path the single-pass encoder falls back to when its grid cannot
+def test_three_launch_encode(mode):
+    """The path the single-pass encoders fall back to when their grid cannot
     be resident at once (three launches: match, offsets, pack) gives the
-    oracle's stream for 512-byte and smaller chunks too."""
+    oracle's stream for the chunk sizes the single-pass encoders take."""
     lib = abi.load()
     rows, idx = W.ibp_table(rows=150_000, cols=128, std=0.1, seed=4, device=DEV, n_samples=3000)
     try:
         lib.zc_test_ibp_single_pass(0)
         for cb, x in ((512, rows.reshape(-1)), (256, rows.reshape(-1)[: 150_000 * 64 - 8]),
-                      (64, rows.reshape(-1)[:1_000_000])):
+                      (64, rows.reshape(-1)[:1_000_000]), (1024, rows.reshape(-1)[:-40]),
+                      (2048, rows.reshape(-1)[: 100_000 * 128 + 12])):
             nch = x.numel() * 4 // cb
             sidx = W.sample_rows(nch, 3000, seed=5, device=DEV)
             meta = I.build_meta(x[: nch * (cb // 4)].view(nch, cb // 4)[sidx].contiguous(), cb,

@@ -54,11 +54,13 @@ def test_zipccl_wait_runs_out(lib, tile):
     assert np.array_equal(st, ref)
 
 
-@pytest.mark.parametrize("cb,mb,tile", [(512, 3, 7), (512, 3, 0), (1024, 130, 0), (4096, 3, 3)])
-def test_ibp_wait_runs_out(lib, cb, mb, tile):
-    """512-byte chunks: the single-pass encoder (tiles of 16 KB); 1024: the
-    offsets pass (tiles of 4096 groups, so 130 MiB gives two); 4096: the
-    group-by-group encoder."""
+@pytest.mark.parametrize("cb,mb,tile,single", [(512, 3, 7, 1), (512, 3, 0, 1), (2048, 9, 5, 1),
+                                               (1024, 130, 0, 0), (4096, 3, 3, 1)])
+def test_ibp_wait_runs_out(lib, cb, mb, tile, single):
+    """512-byte chunks: the single-pass encoder (tiles of 16 KB); 2048: the
+    single-pass encoder in pieces (a group per tile); 1024 with the single
+    pass switched off: the offsets pass of the three-launch encode (tiles of
+    4096 groups, so 130 MiB gives two); 4096: the group-by-group encoder."""
     x = W.ibp_gaussian(mb * (1 << 20) // 4, std=0.02, seed=3, device=DEV)
     nch = x.numel() * 4 // cb
     idx = W.sample_rows(nch, 2000, seed=1, device=DEV)
@@ -67,11 +69,15 @@ def test_ibp_wait_runs_out(lib, cb, mb, tile):
                         mode=1 if cb <= 2048 else 0)
     n_bytes = x.numel() * 4
     ws = torch.empty(I.workspace_bytes(cb, n_bytes, 0), dtype=torch.uint8, device=DEV)
-    lib.zc_test_wait_fault(tile, 2000)
-    I.compress(meta, x, cb, ws=ws)
-    torch.cuda.synchronize()
-    assert I.status(ws) == abi.ZC_ERR_TIMEOUT
-    lib.zc_test_wait_fault(OFF, 0)
+    lib.zc_test_ibp_single_pass(single)
+    try:
+        lib.zc_test_wait_fault(tile, 2000)
+        I.compress(meta, x, cb, ws=ws)
+        torch.cuda.synchronize()
+        assert I.status(ws) == abi.ZC_ERR_TIMEOUT
+        lib.zc_test_wait_fault(OFF, 0)
+    finally:
+        lib.zc_test_ibp_single_pass(1)
     st, nb = I.compress(meta, x, cb, ws=ws)
     torch.cuda.synchronize()
     assert I.status(ws) == 0

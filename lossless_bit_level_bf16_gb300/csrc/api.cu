@@ -94,12 +94,10 @@ bool reachable(const void** p, bool* host) {
 
 // Workspace of a plan: the control block, then the statistics partials (one
 // per unit) or the encoder's look-back words followed by one statistics
-// partial per chunk (zc_compress_fit), whichever is larger.
+// partial per chunk (zc_compress_fit), whichever is larger; then the
+// predictor's per-block totals and one block counter per segment.
 size_t zc_ws_bytes(const lbb::ZcLayout& L) {
-  const unsigned long long a = L.nunits * sizeof(lbb::StatPartial);
-  const unsigned long long b =
-      lbb::zc_fit_parts_offset(L.ntiles) - kCtrlBytes + L.nchunks * sizeof(lbb::StatPartial);
-  return (size_t)lbb::round_up_dev(kCtrlBytes + std::max(a, b), 256);
+  return (size_t)lbb::round_up_dev(lbb::zc_cnt_offset(L) + 4ull * L.nseg, 256);
 }
 
 }  // namespace
@@ -179,7 +177,7 @@ int zc_plan_create(uint64_t n, const uint64_t* h_seg_off, uint32_t nseg, uint32_
     delete p;
     return ZC_ERR_NOMEM;
   }
-  unsigned long long chunks = 0, units = 0;
+  unsigned long long chunks = 0, units = 0, max_units = 0, max_chunks = 0;
   for (uint32_t s = 0; s < nseg; ++s) {
     const unsigned long long b = h_seg_off ? h_seg_off[s] : 0;
     const unsigned long long e = h_seg_off ? h_seg_off[s + 1] : n;
@@ -192,9 +190,13 @@ int zc_plan_create(uint64_t n, const uint64_t* h_seg_off, uint32_t nseg, uint32_
     r.unit_start = units;
     chunks += r.nchunks;
     units += (r.nelem + U - 1) / U;
+    max_units = std::max(max_units, (r.nelem + U - 1) / U);
+    max_chunks = std::max(max_chunks, r.nchunks);
   }
   L.nchunks = chunks;
   L.nunits = units;
+  L.kred_u = lbb::zc_red_blocks(max_units);
+  L.kred_c = lbb::zc_red_blocks(max_chunks);
   const unsigned long long tl = lbb::zc_tile_slots(C);
   L.ntiles = (chunks * C + tl - 1) / tl;
   L.slot_bytes = (unsigned long long)C * 11ull / 8ull;

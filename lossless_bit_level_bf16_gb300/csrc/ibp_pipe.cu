@@ -22,11 +22,12 @@
 // registers for the whole kernel (REG); otherwise they are read from shared
 // memory per vector.
 //
-// Encode: for chunks of up to 512 bytes, one launch that reads the input from
-// DRAM once (a control warp matches and resolves offsets, four pack warps
-// pack; described at ibp_encode_ws_kernel); for larger chunks three launches
-// (match -> offsets -> pack, described at the encode kernels below), which
-// read the input twice.  Packing closes up the kept bits of a vector's 4 words into
+// Encode: for chunks of up to 512 bytes, and of 1024 and 2048 bytes, one
+// launch (a control warp matches and resolves offsets, four pack warps pack;
+// described at ibp_encode_ws_kernel and ibp_encode_wsp_kernel); for other
+// chunk sizes, and when a single-pass grid cannot be resident at once, three
+// launches (match -> offsets -> pack, described at the encode kernels below),
+// which read the input twice.  Packing closes up the kept bits of a vector's 4 words into
 // one run of at most 128 bits and ORs it into a shared-memory image of the
 // tile's stream (a shared atomicOr per word, with no choice between words a
 // run owns alone and words it shares), which is then copied out with 16-byte

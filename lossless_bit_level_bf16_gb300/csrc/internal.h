@@ -59,7 +59,16 @@ struct ZcLayout {
   uint32_t nseg, C, log2C, U;  // U: elements per statistics unit
   unsigned long long off_seg, off_escoff, off_static, off_esc;
   unsigned long long slot_bytes;
+  // predictor blocks per segment over unit partials (plan) and over chunk
+  // partials (fit): each block adds a fixed range of at most 1024 partials
+  uint32_t kred_u, kred_c;
 };
+
+// Predictor blocks per segment for `maxparts` partials in the largest segment.
+inline uint32_t zc_red_blocks(unsigned long long maxparts) {
+  const unsigned long long k = (maxparts + 1023) / 1024;
+  return k < 1 ? 1u : (k > 128 ? 128u : (uint32_t)k);
+}
 
 // One partial of the statistics pass (one unit of U elements).
 struct StatPartial {
@@ -83,10 +92,21 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
                                cudaStream_t s, bool fit = false);
 // The predictor over per-chunk partials (the second launch of a fit).
 cudaError_t zc_launch_predict_chunks(const ZcLayout& L, ZcSegDev* d_segs,
-                                     const StatPartial* d_parts, cudaStream_t s);
+                                     const StatPartial* d_parts, void* d_ws, cudaStream_t s);
 // Offset of the per-chunk statistics partials in an encoder workspace.
 constexpr unsigned long long zc_fit_parts_offset(unsigned long long ntiles) {
   return 256 + (zc_enc_scratch_bytes(ntiles) + 15) / 16 * 16;
+}
+// The predictor's per-block totals (nseg * max(kred_u, kred_c) partials) and
+// one block counter per segment follow the partials of the plan or the fit.
+inline unsigned long long zc_red_offset(const ZcLayout& L) {
+  const unsigned long long a = 256 + L.nunits * sizeof(StatPartial);
+  const unsigned long long b = zc_fit_parts_offset(L.ntiles) + L.nchunks * sizeof(StatPartial);
+  return round_up(a > b ? a : b, 256);
+}
+inline unsigned long long zc_cnt_offset(const ZcLayout& L) {
+  const unsigned long long k = L.kred_u > L.kred_c ? L.kred_u : L.kred_c;
+  return round_up(zc_red_offset(L) + (unsigned long long)L.nseg * k * sizeof(StatPartial), 256);
 }
 cudaError_t zc_launch_decompress(const void* d_in, unsigned long long in_bytes,
                                  uint16_t* d_y, unsigned long long y_cap,

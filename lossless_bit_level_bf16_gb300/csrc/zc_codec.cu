@@ -968,6 +968,8 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   const unsigned long long ntiles = (L.nchunks * (unsigned long long)L.C + tl - 1) / tl;
   char* lb = static_cast<char*>(d_ws) + kCtrlBytes;
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + zc_enc_scratch_bytes(ntiles), s);
+  if (e == cudaSuccess && fit && L.kred_c > 1)  // the predictor's block counters
+    e = cudaMemsetAsync(static_cast<char*>(d_ws) + zc_cnt_offset(L), 0, 4ull * L.nseg, s);
   if (e != cudaSuccess) return e;
   e = arm_wait_fault(d_ws, s);
   if (e != cudaSuccess) return e;
@@ -999,7 +1001,7 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   e = cudaGetLastError();
   if (e != cudaSuccess || !fit) return e;
   // every chunk's partial is written before the predictor reads them
-  return zc_launch_predict_chunks(L, const_cast<ZcSegDev*>(d_segs), A.parts, s);
+  return zc_launch_predict_chunks(L, const_cast<ZcSegDev*>(d_segs), A.parts, d_ws, s);
 }
 
 cudaError_t zc_launch_decompress(const void* d_in, unsigned long long in_bytes,

@@ -319,9 +319,15 @@ __device__ int field_of(double v) {
 
 // parts: one partial per statistics unit (by_chunk = 0, after zc_stats_kernel)
 // or per chunk (by_chunk = 1, after the encoder that also sums).
+// K blocks per segment (block k of segment s is block s * K + k): block k
+// adds the fixed range k of the segment's partials; with K > 1 it files its
+// totals and the segment's last block to finish (a counter per segment,
+// zeroed by the launcher) adds the K totals in index order and goes on with
+// the codebook.  The sums depend only on the plan, not on which block is last.
 __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
     ZcSegDev* __restrict__ segs, uint32_t nseg, unsigned long long nunits,
-    const StatPartial* __restrict__ parts, int by_chunk) {
+    const StatPartial* __restrict__ parts, int by_chunk, uint32_t K, StatPartial* red,
+    uint32_t* cnt) {
   __shared__ double s_r1[kThreads / 32], s_r2[kThreads / 32];
   __shared__ unsigned long long s_rc[kThreads / 32];
   __shared__ double s_mu, s_sigma;
@@ -332,12 +338,16 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
   __shared__ int s_ok;
   __shared__ float s_emf[256], s_epf[256], s_m7f, s_m8f;
   __shared__ uint32_t s_keyf[256];
+  __shared__ int s_lastblk;
   const int t = threadIdx.x;
-  const uint32_t sg = blockIdx.x;
+  const uint32_t sg = blockIdx.x / K, kb = blockIdx.x % K;
   grid_dep_wait();  // the statistics partials
-  const unsigned long long u0 = by_chunk ? segs[sg].chunk_start : segs[sg].unit_start;
-  const unsigned long long u1 = by_chunk ? u0 + segs[sg].nchunks
-                                         : ((sg + 1 < nseg) ? segs[sg + 1].unit_start : nunits);
+  const unsigned long long s0 = by_chunk ? segs[sg].chunk_start : segs[sg].unit_start;
+  const unsigned long long s1e = by_chunk ? s0 + segs[sg].nchunks
+                                          : ((sg + 1 < nseg) ? segs[sg + 1].unit_start : nunits);
+  const unsigned long long per = (s1e - s0 + K - 1) / K;
+  const unsigned long long u0 = s0 + per * kb < s1e ? s0 + per * kb : s1e;
+  const unsigned long long u1 = u0 + per < s1e ? u0 + per : s1e;
   double a = 0.0, b = 0.0;
   unsigned long long c = 0;
   for (unsigned long long u = u0 + t; u < u1; u += kThreads) {
@@ -365,6 +375,27 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
       s2 = __dadd_rn(s2, s_r2[w]);
       n += s_rc[w];
     }
+    s_lastblk = 1;
+    if (K > 1) {
+      StatPartial& mine = red[(unsigned long long)sg * K + kb];
+      mine.cnt = n;
+      mine.s1 = s1;
+      mine.s2 = s2;
+      __threadfence();
+      s_lastblk = atomicAdd(cnt + sg, 1u) == K - 1;
+      if (s_lastblk) {
+        __threadfence();
+        s1 = 0.0;
+        s2 = 0.0;
+        n = 0;
+        for (uint32_t j = 0; j < K; ++j) {
+          const StatPartial* r = red + (unsigned long long)sg * K + j;
+          s1 = __dadd_rn(s1, __ldcg(&r->s1));
+          s2 = __dadd_rn(s2, __ldcg(&r->s2));
+          n += __ldcg(&r->cnt);
+        }
+      }
+    }
     double mu = 0.0, sigma = 0.0;
     if (n) {
       mu = __ddiv_rn(s1, (double)n);
@@ -376,6 +407,7 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
     s_is = sigma > 0.0 ? __drcp_rn(__dmul_rn(sigma, 1.4142135623730951)) : 0.0;  // 1/(sigma sqrt 2)
   }
   __syncthreads();
+  if (!s_lastblk) return;  // another block of the segment finishes it
   const double mu = s_mu, sigma = s_sigma;
   unsigned char* book = segs[sg].book;
   if (!(sigma > 0.0)) {
@@ -512,10 +544,27 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
 
 }  // namespace
 
+namespace {
+// The predictor over L's segments, K blocks per segment.
+cudaError_t launch_predict(const ZcLayout& L, ZcSegDev* d_segs, unsigned long long nparts,
+                           const StatPartial* parts, int by_chunk, uint32_t K, void* d_ws,
+                           cudaStream_t s) {
+  StatPartial* red = reinterpret_cast<StatPartial*>(static_cast<char*>(d_ws) + zc_red_offset(L));
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(static_cast<char*>(d_ws) + zc_cnt_offset(L));
+  return launch_dependent(zc_predict_kernel, L.nseg * K, kThreads, 0, s, d_segs, L.nseg, nparts,
+                          parts, by_chunk, K, red, cnt);
+}
+}  // namespace
+
 cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
                            const uint16_t* d_x, void* d_ws, cudaStream_t s) {
   StatPartial* parts = reinterpret_cast<StatPartial*>(static_cast<char*>(d_ws) + kCtrlBytes);
   const int al = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
+  if (L.kred_u > 1) {  // the predictor's block counters
+    const cudaError_t e =
+        cudaMemsetAsync(static_cast<char*>(d_ws) + zc_cnt_offset(L), 0, 4ull * L.nseg, s);
+    if (e != cudaSuccess) return e;
+  }
   if (L.nunits) {
     cudaError_t e = cudaFuncSetAttribute(zc_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kStatSmem);
@@ -527,15 +576,12 @@ cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  return launch_dependent(zc_predict_kernel, L.nseg, kThreads, 0, s,
-                          const_cast<ZcSegDev*>(d_segs), L.nseg, L.nunits,
-                          static_cast<const StatPartial*>(parts), 0);
+  return launch_predict(L, const_cast<ZcSegDev*>(d_segs), L.nunits, parts, 0, L.kred_u, d_ws, s);
 }
 
 cudaError_t zc_launch_predict_chunks(const ZcLayout& L, ZcSegDev* d_segs,
-                                     const StatPartial* d_parts, cudaStream_t s) {
-  return launch_dependent(zc_predict_kernel, L.nseg, kThreads, 0, s, d_segs, L.nseg, L.nchunks,
-                          d_parts, 1);
+                                     const StatPartial* d_parts, void* d_ws, cudaStream_t s) {
+  return launch_predict(L, d_segs, L.nchunks, d_parts, 1, L.kred_c, d_ws, s);
 }
 
 }  // namespace lbb

@@ -10,8 +10,9 @@
 //   zc_stats_kernel    one warp per statistics unit (U elements inside one
 //                      segment): count, sum and sum of squares of the finite
 //                      values.  HBM-bound: 2 bytes read per element.
-//   zc_predict_kernel  one block per segment: adds the unit partials in a
-//                      fixed order, forms mu and sigma, evaluates the Gaussian
+//   zc_predict_kernel  K blocks per segment add fixed ranges of the unit
+//                      partials; the segment's last block adds their totals
+//                      in a fixed order, forms mu and sigma, evaluates the Gaussian
 //                      mass of the exponent fields and keeps the 7 largest.
 //                      fp64 is slow on this part, so each field edge's erfc
 //                      ranking is done in fp32 unless the 7th and 8th masses

@@ -469,6 +469,7 @@ def kernels_of(op, cb=512):
             "zc_decompress": ["zc_decode_kernel"],
             "ibp_build_meta": ["ibp_columns_kernel", "ibp_meta_kernel"],
             "ibp_compress": (["ibp_encode_ws_kernel"] if cb <= 512 else
+                             ["ibp_encode_wsp_kernel"] if cb in (1024, 2048) else
                              ["ibp_match_kernel", "ibp_offsets_kernel", "ibp_pack_kernel"]),
             "ibp_decompress": ["ibp_decode_pipe_kernel"]}[op]
 

@@ -102,7 +102,8 @@ constexpr uint32_t kEscCap = 1024;                   // escape bytes a warp stag
 static_assert(kLbBlock == kZcLbBlock, "the scratch layout and the look-back agree");
 
 // STATS (zc_compress_fit): each lane also sums its finite values and their
-// squares per step (four fp32 chains of eight values, then fp32 (sum, error)
+// squares per step (four fp32 chains of eight values, in packed fp32x2
+// operations, then fp32 (sum, error)
 // pairs across steps; a step whose fp32 sums are not finite, or whose squares
 // may have underflowed, is summed in fp64), and the warp writes each chunk's
 // count and fp64 sums to A.parts when the chunk's last step is done.
@@ -379,15 +380,19 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
       }
       const unsigned long long c = cfirst + lct;
       if constexpr (STATS) {
-        float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+        // four fp32 chains of eight values: the low and the high value of the
+        // even and of the odd words, two chains per packed fp32x2 operation
+        unsigned long long s1[2] = {0ull, 0ull}, s2[2] = {0ull, 0ull};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {  // padding slots hold 0
-          const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
-          s1[j & 3] = __fadd_rn(__fadd_rn(s1[j & 3], lo), hi);
-          s2[j & 3] = __fmaf_rn(hi, hi, __fmaf_rn(lo, lo, s2[j & 3]));
+          const unsigned long long v = f2_pack(bf16_lo(w[j]), bf16_hi(w[j]));
+          s1[j & 1] = f2_add(s1[j & 1], v);
+          s2[j & 1] = f2_fma(v, v, s2[j & 1]);
         }
-        const float t1 = __fadd_rn(__fadd_rn(s1[0], s1[1]), __fadd_rn(s1[2], s1[3]));
-        const float t2 = __fadd_rn(__fadd_rn(s2[0], s2[1]), __fadd_rn(s2[2], s2[3]));
+        const float2 a0 = f2_unpack(s1[0]), a1 = f2_unpack(s1[1]);
+        const float2 q0 = f2_unpack(s2[0]), q1 = f2_unpack(s2[1]);
+        const float t1 = __fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y));
+        const float t2 = __fadd_rn(__fadd_rn(q0.x, q0.y), __fadd_rn(q1.x, q1.y));
         bool fast = isfinite(t1) && isfinite(t2);
         if (fast && t2 < 0x1p-96f) {  // squares may have lost bits: only if a value is not 0
           uint32_t nz = 0;

@@ -1335,11 +1335,12 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
 //   time: no block waits for another's output.
 constexpr int kWspPack = 128, kWspThreads = kWspPack + 32;
 constexpr uint32_t kWspPiece = 16384;  // input bytes per piece
+constexpr uint32_t kWspMS = 2, kWspPS = 2;  // match stages, pack stages
 
 __host__ __device__ inline size_t wsp_smem_bytes(uint32_t cb, uint32_t stage_bytes,
                                                  uint32_t img_words) {
-  return 4 * ibp_table_words(cb / 4) + 4ull * stage_bytes + 4ull * img_words +
-         2ull * kWsLensBytes + 8ull * (4 + 2 * kWsInfo);
+  return 4 * ibp_table_words(cb / 4) + (size_t)(kWspMS + kWspPS) * stage_bytes +
+         4ull * img_words + 2ull * kWsLensBytes + 8ull * (kWspMS + kWspPS + 2 * kWsInfo);
 }
 
 // Bits below bit n (n <= 32).
@@ -1361,14 +1362,14 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
 
   uint32_t* tab = reinterpret_cast<uint32_t*>(dyn);
   uint8_t* pstages = dyn + 4 * ibp_table_words(W);
-  uint8_t* mstages = pstages + 2ull * A.stage_bytes;
-  uint32_t* img = reinterpret_cast<uint32_t*>(mstages + 2ull * A.stage_bytes);
+  uint8_t* mstages = pstages + (size_t)kWspPS * A.stage_bytes;
+  uint32_t* img = reinterpret_cast<uint32_t*>(mstages + (size_t)kWspMS * A.stage_bytes);
   uint4* img4 = reinterpret_cast<uint4*>(img);
   uint8_t* lensbuf = reinterpret_cast<uint8_t*>(img + A.img_words);
   unsigned long long* bars = reinterpret_cast<unsigned long long*>(lensbuf + 2 * kWsLensBytes);
-  unsigned long long* b_sfull = bars;        // pack stages landed
-  unsigned long long* b_mfull = bars + 2;    // match stages landed
-  unsigned long long* b_ifull = bars + 4;    // slot handed over
+  unsigned long long* b_sfull = bars;                    // pack stages landed
+  unsigned long long* b_mfull = bars + kWspPS;           // match stages landed
+  unsigned long long* b_ifull = b_mfull + kWspMS;        // slot handed over
   unsigned long long* b_iempty = b_ifull + kWsInfo;  // slot read
   unsigned long long* grp = reinterpret_cast<unsigned long long*>(A.dst + kIbp1Header);
 
@@ -1407,10 +1408,8 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
     if (b16) bulk_g2s_hint(st, A.src + b0, b16, bar, pol);
   };
   if (t == 0) {
-    for (uint32_t s = 0; s < 2; ++s) {
-      mbar_init(b_sfull + s, 1);
-      mbar_init(b_mfull + s, 1);
-    }
+    for (uint32_t s = 0; s < kWspPS; ++s) mbar_init(b_sfull + s, 1);
+    for (uint32_t s = 0; s < kWspMS; ++s) mbar_init(b_mfull + s, 1);
     for (uint32_t k = 0; k < kWsInfo; ++k) {
       mbar_init(b_ifull + k, 1);
       mbar_init(b_iempty + k, 1);
@@ -1453,10 +1452,9 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
       cp_async_commit();
     };
     const unsigned long long keep = l2_policy_keep();
-    if (lane == 0) {
-      stage_piece(0, mstages, b_mfull, keep);
-      stage_piece(1, mstages + A.stage_bytes, b_mfull + 1, keep);
-    }
+    if (lane == 0)
+      for (uint32_t s = 0; s < kWspMS; ++s)
+        stage_piece(s, mstages + (size_t)s * A.stage_bytes, b_mfull + s, keep);
     const unsigned lim = wait_limit(A.ctrl);
     const unsigned long long fault1 = A.ctrl->fault_tile1;  // 0 unless a wait-failure test
     unsigned long long wave_base = 0;  // 128-bit units of the waves resolved so far
@@ -1468,8 +1466,8 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
         for (uint32_t p = 0; p < np; ++p) {
           const uint32_t tb = piece_bytes(g, p);
           if (tb == 0) break;
-          const uint32_t seq = i * np + p, ms = seq & 1u;
-          if (!mbar_wait(b_mfull + ms, (seq >> 1) & 1u)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+          const uint32_t seq = i * np + p, ms = seq % kWspMS;
+          if (!mbar_wait(b_mfull + ms, (seq / kWspMS) & 1u)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
           const uint32_t* sd = reinterpret_cast<const uint32_t*>(mstages + (size_t)ms * A.stage_bytes);
           const uint32_t nfull = tb / cb;  // a short last chunk never participates
           uint32_t c = 0;
@@ -1480,7 +1478,8 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
           }
           if (c < nfull && __any_sync(kFull, differs(sd, c) != 0)) bad |= 1u << (p * cpp + c);
           __syncwarp();  // the match stage has been read
-          if (lane == 0) stage_piece(seq + 2, mstages + (size_t)ms * A.stage_bytes, b_mfull + ms, keep);
+          if (lane == 0)
+            stage_piece(seq + kWspMS, mstages + (size_t)ms * A.stage_bytes, b_mfull + ms, keep);
         }
         const unsigned long long c0 = 32ull * g;
         const uint32_t nch = (uint32_t)((A.nchunks - c0) < 32 ? (A.nchunks - c0) : 32);
@@ -1574,10 +1573,9 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
       make_packtab(v0, pt);
     }
     const unsigned long long drop = l2_policy_first();
-    if (t == 0) {
-      stage_piece(0, pstages, b_sfull, drop);
-      stage_piece(1, pstages + A.stage_bytes, b_sfull + 1, drop);
-    }
+    if (t == 0)
+      for (uint32_t s = 0; s < kWspPS; ++s)
+        stage_piece(s, pstages + (size_t)s * A.stage_bytes, b_sfull + s, drop);
     uint32_t carry = 0;  // thread 0, raw groups: the previous piece's last input word
     for (uint32_t j = 0; j < mine; ++j) {
       const uint32_t k = j % kWsInfo;
@@ -1596,8 +1594,8 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
         const uint32_t tb = piece_bytes(g, p);
         if (tb == 0) break;
         const bool last = p + 1 == np || piece_bytes(g, p + 1) == 0;
-        const uint32_t seq = j * np + p, s = seq & 1u;
-        if (!mbar_wait(b_sfull + s, (seq >> 1) & 1u)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
+        const uint32_t seq = j * np + p, s = seq % kWspPS;
+        if (!mbar_wait(b_sfull + s, (seq / kWspPS) & 1u)) set_status(A.ctrl, ZC_ERR_TIMEOUT);
         const uint32_t* sd = reinterpret_cast<const uint32_t*>(pstages + (size_t)s * A.stage_bytes);
         const uint32_t twords = tb / 4, nvec = (tb + 15) / 16;
         const uint32_t c0 = p * cpp;  // the piece's first chunk in the group
@@ -1638,7 +1636,7 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
           }
           if (t == 0) carry = sd[twords - 1];
           named_bar(1, kWspPack);  // the stage has been read
-          if (t == 0) stage_piece(seq + 2, pstages + (size_t)s * A.stage_bytes, b_sfull + s, drop);
+          if (t == 0) stage_piece(seq + kWspPS, pstages + (size_t)s * A.stage_bytes, b_sfull + s, drop);
         } else {
           // bit P of the group's stream starts the piece; the image holds the
           // stream from ibase = P rounded down to 128 bits
@@ -1682,7 +1680,7 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
             }
           }
           named_bar(1, kWspPack);  // the piece is in the image; the stage has been read
-          if (t == 0) stage_piece(seq + 2, pstages + (size_t)s * A.stage_bytes, b_sfull + s, drop);
+          if (t == 0) stage_piece(seq + kWspPS, pstages + (size_t)s * A.stage_bytes, b_sfull + s, drop);
           const unsigned long long dst = dst0 + (ibase >> 3);
           for (uint32_t u0 = t; u0 < nfull; u0 += 4 * kWspPack) {
             uint4 o[4];

@@ -288,6 +288,19 @@ __device__ __forceinline__ void make_packtab(const VecTab& v, PackTab& p) {
   p.Pr = v.Pr;
 }
 
+// Bits below bit n (n <= 32).
+__device__ __forceinline__ uint32_t lowmask(uint32_t n) { return n >= 32 ? 0xFFFFFFFFu : (1u << n) - 1u; }
+
+// A group's chunk table for the packing: entry c is chunk c's first bit in
+// the group's stream, from the group's first bit g (g + 32 + c * B minus the
+// kept-bit savings of the participating chunks before it), shifted left by
+// one, with the chunk's participation bit below.  Filled by threads 0..31.
+__device__ __forceinline__ void fill_chunk_table(uint32_t* coff, uint32_t t, uint32_t pw, uint32_t g,
+                                                 uint32_t B, uint32_t m) {
+  if (t < 32)
+    coff[t] = ((g + 32u + t * B - (uint32_t)__popc(pw & lowmask(t)) * m) << 1) | ((pw >> t) & 1u);
+}
+
 // x << s for s in 0..32 (0 at 32).
 __device__ __forceinline__ uint32_t shl32(uint32_t x, uint32_t s) { return __funnelshift_lc(0u, x, s); }
 
@@ -323,19 +336,20 @@ __device__ __forceinline__ void pack_run(const PackTab& p, const uint4& d, uint3
 // (fast path: REG positions, run-form keep masks).  E vectors per step: the
 // words and chunk offsets of all E are read before any is placed, so their
 // chains interleave (a placement's shared atomics would otherwise keep the
-// next vector's loads behind them).  Several groups (not ONEQ): spw / sgex
-// hold the groups' participation words and bit offsets.  One group (ONEQ):
-// pw1 is its participation word, the staged vectors belong to its chunks
-// cbase, cbase + 1, ..., and chunk c's body starts at image bit
+// next vector's loads behind them).  MODE 0 (several groups): spw / sgex
+// hold the groups' participation words and bit offsets.  MODE 1 (one
+// group): pw1 is its participation word, the staged vectors belong to its
+// chunks cbase, cbase + 1, ..., and chunk c's body starts at image bit
 // g1 + c * B - (kept-bit savings of the chunks before it), g1 folding in
-// the group's first image bit and its 32 participation bits.  r: the
-// thread's vector position.
-template <bool THREE, bool ONEQ, int E, int NT>
+// the group's first image bit and its 32 participation bits.  MODE 2 (one
+// group, table): chunk c's entry in coff (fill_chunk_table) gives its first
+// bit, plus g1.  r: the thread's vector position.
+template <bool THREE, int MODE, int E, int NT>
 __device__ __forceinline__ void pack_fast(const PackTab& p, const uint32_t* sd, uint32_t nvec,
                                           uint32_t twords, const uint32_t* spw,
-                                          const uint32_t* sgex, uint32_t pw1, uint32_t g1,
-                                          uint32_t cbase, uint32_t lvpc, uint32_t r, uint32_t B,
-                                          uint32_t m, uint32_t* img, uint32_t t) {
+                                          const uint32_t* sgex, const uint32_t* coff, uint32_t pw1,
+                                          uint32_t g1, uint32_t cbase, uint32_t lvpc, uint32_t r,
+                                          uint32_t B, uint32_t m, uint32_t* img, uint32_t t) {
   const uint32_t rawpos = 128u * r;
   for (uint32_t v0 = t; v0 < nvec; v0 += E * NT) {
     uint4 d[E];
@@ -344,12 +358,18 @@ __device__ __forceinline__ void pack_fast(const PackTab& p, const uint32_t* sd, 
     for (int e = 0; e < E; ++e) {
       const uint32_t v = v0 + e * NT;
       const uint32_t vv = v < nvec ? v : v0;  // a vector of the tile
-      const uint32_t c = (ONEQ ? cbase : 0u) + (vv >> lvpc), i5 = c & 31;
+      const uint32_t c = (MODE ? cbase : 0u) + (vv >> lvpc), i5 = c & 31;
       d[e] = *reinterpret_cast<const uint4*>(sd + 4 * vv);
-      const uint32_t pw = ONEQ ? pw1 : spw[c >> 5];
-      const uint32_t g = ONEQ ? g1 : sgex[c >> 5] + 32u;
-      off[e] = g + i5 * B - (uint32_t)__popc(pw & ((1u << i5) - 1u)) * m;
-      in[e] = (pw >> i5) & 1u;
+      if (MODE == 2) {
+        const uint32_t ce = coff[c];
+        off[e] = (ce >> 1) + g1;
+        in[e] = ce & 1u;
+      } else {
+        const uint32_t pw = MODE ? pw1 : spw[c >> 5];
+        const uint32_t g = MODE ? g1 : sgex[c >> 5] + 32u;
+        off[e] = g + i5 * B - (uint32_t)__popc(pw & ((1u << i5) - 1u)) * m;
+        in[e] = (pw >> i5) & 1u;
+      }
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -756,14 +776,14 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
         const uint32_t pw1 = pw_[0], g1 = gx_[0] + 32u;
         if (pt.three) {
           if (Q == 1)
-            pack_fast<true, true, 2, NT>(pt, sd, nvec, twords, pw_, gx_, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
+            pack_fast<true, 1, 2, NT>(pt, sd, nvec, twords, pw_, gx_, nullptr, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
           else
-            pack_fast<true, false, 2, NT>(pt, sd, nvec, twords, pw_, gx_, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
+            pack_fast<true, 0, 2, NT>(pt, sd, nvec, twords, pw_, gx_, nullptr, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
         } else {
           if (Q == 1)
-            pack_fast<false, true, 2, NT>(pt, sd, nvec, twords, pw_, gx_, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
+            pack_fast<false, 1, 2, NT>(pt, sd, nvec, twords, pw_, gx_, nullptr, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
           else
-            pack_fast<false, false, 2, NT>(pt, sd, nvec, twords, pw_, gx_, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
+            pack_fast<false, 0, 2, NT>(pt, sd, nvec, twords, pw_, gx_, nullptr, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
         }
       } else {
         for (uint32_t v = t; v < nvec; v += NT) {
@@ -885,6 +905,7 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
   __shared__ uint32_t s_scr[kWsThreads / 32 + 4];
   __shared__ WsInfo s_info[kWsInfo];
   __shared__ uint32_t s_cpw[kWsLag + 1][kMaxQ];  // control warp: matched tiles' words
+  __shared__ uint32_t s_coff[32];                 // pack warps: a one-group tile's chunk table
   __shared__ int s_last;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t cb = A.cb, W = cb / 4, B = 8 * cb, Q = A.Q;
@@ -1167,7 +1188,9 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
       bool ok = mbar_wait(b_sfull + s, (j / kWsStages) & 1u);
       ok = mbar_wait(b_ifull + k, (j / kWsInfo) & 1u) && ok;
       if (!ok) set_status(A.ctrl, ZC_ERR_TIMEOUT);
-      named_bar(1, kWsPack);  // the previous tile's image is cleared
+      if (Q == 1 && !s_info[k].raw)  // one group: its chunk table (the previous tile is done with it)
+        fill_chunk_table(s_coff, (uint32_t)t, s_info[k].pw[0], s_info[k].gex[0], B, m);
+      named_bar(1, kWsPack);  // the previous tile's image is cleared, the chunk table filled
       const WsInfo& si = s_info[k];
       const uint32_t* sd = reinterpret_cast<const uint32_t*>(stages + (size_t)s * A.stage_bytes);
       const unsigned long long tile = bid + (unsigned long long)j * G, g0 = tile * Q;
@@ -1223,21 +1246,21 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
         // its constants in registers; any other reads its position's tables
         // per vector (the loops have no warp-wide operation).
         if (REG && pt.ok) {
-          const uint32_t pw1 = si.pw[0], g1 = si.gex[0] + 32u;
+          // one group: chunk offsets from the table filled at the tile's start
           if (pt.three) {
             if (Q == 1)
-              pack_fast<true, true, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, pw1, g1, 0u,
-                                                A.lvpc, r_own, B, m, img, t);
+              pack_fast<true, 2, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, s_coff, 0u, 0u,
+                                             0u, A.lvpc, r_own, B, m, img, t);
             else
-              pack_fast<true, false, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, pw1, g1, 0u,
-                                                 A.lvpc, r_own, B, m, img, t);
+              pack_fast<true, 0, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, nullptr, 0u, 0u,
+                                             0u, A.lvpc, r_own, B, m, img, t);
           } else {
             if (Q == 1)
-              pack_fast<false, true, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, pw1, g1, 0u,
-                                                 A.lvpc, r_own, B, m, img, t);
+              pack_fast<false, 2, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, s_coff, 0u, 0u,
+                                              0u, A.lvpc, r_own, B, m, img, t);
             else
-              pack_fast<false, false, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, pw1, g1, 0u,
-                                                  A.lvpc, r_own, B, m, img, t);
+              pack_fast<false, 0, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, nullptr, 0u, 0u,
+                                              0u, A.lvpc, r_own, B, m, img, t);
           }
         } else {
           for (uint32_t v = t; v < nvec; v += kWsPack) {
@@ -1343,15 +1366,13 @@ __host__ __device__ inline size_t wsp_smem_bytes(uint32_t cb, uint32_t stage_byt
          4ull * img_words + 2ull * kWsLensBytes + 8ull * (kWspMS + kWspPS + 2 * kWsInfo);
 }
 
-// Bits below bit n (n <= 32).
-__device__ __forceinline__ uint32_t lowmask(uint32_t n) { return n >= 32 ? 0xFFFFFFFFu : (1u << n) - 1u; }
-
 template <int VPW>  // 16-byte vectors of a chunk per lane of a warp (vpc / 32)
 __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs A) {
   extern __shared__ __align__(128) uint8_t dyn[];
   __shared__ uint32_t s_scr[kWspThreads / 32 + 4];
   __shared__ WsInfo s_info[kWsInfo];
   __shared__ uint32_t s_cpw[4];  // control warp: matched groups' participation words
+  __shared__ uint32_t s_coff[32];  // pack warps: the group's chunk table
   __shared__ int s_last;
   constexpr uint32_t vpc = 32 * VPW;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -1583,7 +1604,9 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
       const unsigned long long base = s_info[k].base;
       const uint32_t pw = s_info[k].pw[0], agg = s_info[k].agg;
       const bool raw = s_info[k].raw != 0;
-      named_bar(1, kWspPack);  // every pack thread has read the slot
+      // the group's chunk table (every pack thread is past the previous group)
+      if (!raw) fill_chunk_table(s_coff, (uint32_t)t, pw, 0u, B, m);
+      named_bar(1, kWspPack);  // every pack thread has read the slot; the table is filled
       if (t == 0) mbar_arrive(b_iempty + k);
       const unsigned long long g = bid + (unsigned long long)j * G;
       const unsigned long long dst0 = A.off_payload + (base >> 3);
@@ -1647,12 +1670,13 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
           if (p == 0 && t == 0) atomicOr(img, pw);  // the participation word
           const uint32_t g1 = 32u - ibase;  // modulo 2^32: chunk starts relative to the image
           if (pt.ok) {
+            // chunk c's first bit relative to the image: its table entry - ibase
             if (pt.three)
-              pack_fast<true, true, 2, kWspPack>(pt, sd, nvec, twords, nullptr, nullptr, pw, g1, c0,
-                                                 A.lvpc, r_own, B, m, img, t);
+              pack_fast<true, 2, 2, kWspPack>(pt, sd, nvec, twords, nullptr, nullptr, s_coff, pw,
+                                              0u - ibase, c0, A.lvpc, r_own, B, m, img, t);
             else
-              pack_fast<false, true, 2, kWspPack>(pt, sd, nvec, twords, nullptr, nullptr, pw, g1, c0,
-                                                  A.lvpc, r_own, B, m, img, t);
+              pack_fast<false, 2, 2, kWspPack>(pt, sd, nvec, twords, nullptr, nullptr, s_coff, pw,
+                                               0u - ibase, c0, A.lvpc, r_own, B, m, img, t);
           } else {
             for (uint32_t v = t; v < nvec; v += kWspPack) {
               const uint32_t c = c0 + (v >> A.lvpc);

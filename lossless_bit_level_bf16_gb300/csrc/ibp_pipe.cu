@@ -261,13 +261,14 @@ __device__ __forceinline__ void img_or(uint32_t* img, uint32_t pos, const uint32
 struct PackTab {
   uint32_t a0[4], m0[4], d1[4], M1[4], d2[4], M2[4];
   uint32_t k0, k1, k2, n, Pr;
-  bool ok, three;
+  bool ok, three, low;  // low: every word's first run starts at bit 0
 };
 
 // From a VecTab on which make_runs (and, for three runs, make_runs3) ran.
 __device__ __forceinline__ void make_packtab(const VecTab& v, PackTab& p) {
   p.ok = v.fast || v.fast3;
   p.three = !v.fast && v.fast3;
+  p.low = v.MV[0][0] == 0 && v.MV[0][1] == 0 && v.MV[0][2] == 0 && v.MV[0][3] == 0;
   uint32_t k[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -307,13 +308,13 @@ __device__ __forceinline__ uint32_t shl32(uint32_t x, uint32_t s) { return __fun
 // The kept bits of the 4 words x as one run o[0..3] (LSB first, zero above
 // p.n): fields concatenated from the last one down, each step a 128-bit
 // shift by the next field's length (clamped funnel shifts: no branches).
-template <bool THREE>
+template <bool THREE, bool LOW>
 __device__ __forceinline__ void pack_run(const PackTab& p, const uint4& d, uint32_t o[4]) {
   const uint32_t x[4] = {d.x, d.y, d.z, d.w};
   uint32_t f[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    f[j] = ((x[j] >> p.a0[j]) & p.m0[j]) | ((x[j] >> p.d1[j]) & p.M1[j]);
+    f[j] = ((LOW ? x[j] : x[j] >> p.a0[j]) & p.m0[j]) | ((x[j] >> p.d1[j]) & p.M1[j]);
     if (THREE) f[j] |= (x[j] >> p.d2[j]) & p.M2[j];
   }
   uint32_t o0 = f[3], o1, o2, o3;
@@ -344,7 +345,7 @@ __device__ __forceinline__ void pack_run(const PackTab& p, const uint4& d, uint3
 // the group's first image bit and its 32 participation bits.  MODE 2 (one
 // group, table): chunk c's entry in coff (fill_chunk_table) gives its first
 // bit, plus g1.  r: the thread's vector position.
-template <bool THREE, int MODE, int E, int NT>
+template <bool THREE, bool LOW, int MODE, int E, int NT>
 __device__ __forceinline__ void pack_fast(const PackTab& p, const uint32_t* sd, uint32_t nvec,
                                           uint32_t twords, const uint32_t* spw,
                                           const uint32_t* sgex, const uint32_t* coff, uint32_t pw1,
@@ -377,7 +378,7 @@ __device__ __forceinline__ void pack_fast(const PackTab& p, const uint32_t* sd, 
       if (v >= nvec) continue;
       uint32_t o[4];
       if (in[e]) {
-        pack_run<THREE>(p, d[e], o);
+        pack_run<THREE, LOW>(p, d[e], o);
         off[e] += p.Pr;
       } else {
         const uint32_t wv = twords - 4 * v;  // >= 1; < 4 only for a short last vector
@@ -389,6 +390,30 @@ __device__ __forceinline__ void pack_fast(const PackTab& p, const uint32_t* sd, 
       }
       img_or(img, off[e], o);
     }
+  }
+}
+
+// pack_fast in the form the thread's run constants allow.
+template <int MODE, int E, int NT>
+__device__ __forceinline__ void pack_any(const PackTab& p, const uint32_t* sd, uint32_t nvec,
+                                         uint32_t twords, const uint32_t* spw, const uint32_t* sgex,
+                                         const uint32_t* coff, uint32_t pw1, uint32_t g1,
+                                         uint32_t cbase, uint32_t lvpc, uint32_t r, uint32_t B,
+                                         uint32_t m, uint32_t* img, uint32_t t) {
+  if (p.three) {
+    if (p.low)
+      pack_fast<true, true, MODE, E, NT>(p, sd, nvec, twords, spw, sgex, coff, pw1, g1, cbase, lvpc,
+                                         r, B, m, img, t);
+    else
+      pack_fast<true, false, MODE, E, NT>(p, sd, nvec, twords, spw, sgex, coff, pw1, g1, cbase,
+                                          lvpc, r, B, m, img, t);
+  } else {
+    if (p.low)
+      pack_fast<false, true, MODE, E, NT>(p, sd, nvec, twords, spw, sgex, coff, pw1, g1, cbase,
+                                          lvpc, r, B, m, img, t);
+    else
+      pack_fast<false, false, MODE, E, NT>(p, sd, nvec, twords, spw, sgex, coff, pw1, g1, cbase,
+                                           lvpc, r, B, m, img, t);
   }
 }
 
@@ -774,17 +799,10 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_pack_kernel(PipeArgs A) {
         const uint32_t* pw_ = s_pw[s];
         const uint32_t* gx_ = s_gex[s];
         const uint32_t pw1 = pw_[0], g1 = gx_[0] + 32u;
-        if (pt.three) {
-          if (Q == 1)
-            pack_fast<true, 1, 2, NT>(pt, sd, nvec, twords, pw_, gx_, nullptr, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
-          else
-            pack_fast<true, 0, 2, NT>(pt, sd, nvec, twords, pw_, gx_, nullptr, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
-        } else {
-          if (Q == 1)
-            pack_fast<false, 1, 2, NT>(pt, sd, nvec, twords, pw_, gx_, nullptr, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
-          else
-            pack_fast<false, 0, 2, NT>(pt, sd, nvec, twords, pw_, gx_, nullptr, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
-        }
+        if (Q == 1)
+          pack_any<1, 2, NT>(pt, sd, nvec, twords, pw_, gx_, nullptr, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
+        else
+          pack_any<0, 2, NT>(pt, sd, nvec, twords, pw_, gx_, nullptr, pw1, g1, 0u, A.lvpc, r_own, B, m, img, t);
       } else {
         for (uint32_t v = t; v < nvec; v += NT) {
           uint32_t c, r;
@@ -1247,21 +1265,12 @@ __global__ void __launch_bounds__(kWsThreads, 3) ibp_encode_ws_kernel(PipeArgs A
         // per vector (the loops have no warp-wide operation).
         if (REG && pt.ok) {
           // one group: chunk offsets from the table filled at the tile's start
-          if (pt.three) {
-            if (Q == 1)
-              pack_fast<true, 2, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, s_coff, 0u, 0u,
-                                             0u, A.lvpc, r_own, B, m, img, t);
-            else
-              pack_fast<true, 0, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, nullptr, 0u, 0u,
-                                             0u, A.lvpc, r_own, B, m, img, t);
-          } else {
-            if (Q == 1)
-              pack_fast<false, 2, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, s_coff, 0u, 0u,
-                                              0u, A.lvpc, r_own, B, m, img, t);
-            else
-              pack_fast<false, 0, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, nullptr, 0u, 0u,
-                                              0u, A.lvpc, r_own, B, m, img, t);
-          }
+          if (Q == 1)
+            pack_any<2, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, s_coff, 0u, 0u, 0u, A.lvpc,
+                                    r_own, B, m, img, t);
+          else
+            pack_any<0, 4, kWsPack>(pt, sd, nvec, twords, si.pw, si.gex, nullptr, 0u, 0u, 0u, A.lvpc,
+                                    r_own, B, m, img, t);
         } else {
           for (uint32_t v = t; v < nvec; v += kWsPack) {
             uint32_t c, r;
@@ -1671,12 +1680,8 @@ __global__ void __launch_bounds__(kWspThreads, 2) ibp_encode_wsp_kernel(PipeArgs
           const uint32_t g1 = 32u - ibase;  // modulo 2^32: chunk starts relative to the image
           if (pt.ok) {
             // chunk c's first bit relative to the image: its table entry - ibase
-            if (pt.three)
-              pack_fast<true, 2, 2, kWspPack>(pt, sd, nvec, twords, nullptr, nullptr, s_coff, pw,
-                                              0u - ibase, c0, A.lvpc, r_own, B, m, img, t);
-            else
-              pack_fast<false, 2, 2, kWspPack>(pt, sd, nvec, twords, nullptr, nullptr, s_coff, pw,
-                                               0u - ibase, c0, A.lvpc, r_own, B, m, img, t);
+            pack_any<2, 2, kWspPack>(pt, sd, nvec, twords, nullptr, nullptr, s_coff, pw, 0u - ibase,
+                                     c0, A.lvpc, r_own, B, m, img, t);
           } else {
             for (uint32_t v = t; v < nvec; v += kWspPack) {
               const uint32_t c = c0 + (v >> A.lvpc);

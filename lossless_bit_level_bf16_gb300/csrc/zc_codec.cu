@@ -756,6 +756,7 @@ __global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
     unsigned long long y_cap, Ctrl* ctrl, int y_al16) {
   __shared__ uint32_t s_nib[256];
   __shared__ __align__(16) uint8_t s_esc[kDecWarps][kWarpEscBytes + 16];
+  __shared__ __align__(16) uint8_t s_ex[kDecWarps][32 * 16];  // a lane's 16 exponent bytes
   __shared__ DecHdr s_h;
   __shared__ int s_ok;
 
@@ -910,21 +911,24 @@ __global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
       uint32_t E0 = prmt(r.R0, r.R1, cA), E1 = prmt(r.R0, r.R1, cA >> 16);
       uint32_t E2 = prmt(r.R0, r.R1, cB), E3 = prmt(r.R0, r.R1, cB >> 16);
       if (esc && base + ne <= ehi) {
+        // the lane's exponent bytes go through its own 16 bytes of shared
+        // memory: each escaped one is one byte store
+        uint4* mine = reinterpret_cast<uint4*>(s_ex[warp] + 16 * lane);
+        *mine = make_uint4(E0, E1, E2, E3);
+        uint8_t* mb = reinterpret_cast<uint8_t*>(mine);
         uint32_t m = esc;
         unsigned long long pos = base;
         while (m) {
           const int i = __ffs(m) - 1;
           m &= m - 1;
-          const uint32_t e = staged ? wesc[pos - ea] : esc_base[pos];
+          mb[i] = staged ? wesc[pos - ea] : esc_base[pos];
           ++pos;
-          const uint32_t sh = (uint32_t)(i & 3) * 8u;
-          const uint32_t keep = ~(0xFFu << sh), ins = e << sh;
-          const int q = i >> 2;
-          if (q == 0) E0 = (E0 & keep) | ins;
-          else if (q == 1) E1 = (E1 & keep) | ins;
-          else if (q == 2) E2 = (E2 & keep) | ins;
-          else E3 = (E3 & keep) | ins;
         }
+        const uint4 v = *mine;
+        E0 = v.x;
+        E1 = v.y;
+        E2 = v.z;
+        E3 = v.w;
       }
       if (valid) {
         uint32_t o[8];

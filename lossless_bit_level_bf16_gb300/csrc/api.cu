@@ -92,6 +92,18 @@ bool reachable(const void** p, bool* host) {
   return true;
 }
 
+// The classification tables of the codebooks in p->h_segs, after the segment
+// records on the device.
+int upload_luts(zc_plan_s* p) {
+  std::vector<uint32_t> luts(256ull * p->L.nseg);
+  for (uint32_t s = 0; s < p->L.nseg; ++s)
+    for (uint32_t e = 0; e < 256; ++e) luts[256ull * s + e] = lbb::zc_lut_entry(p->h_segs[s].book, e);
+  return cudaMemcpy(lbb::zc_seg_luts(p->d_segs, p->L.nseg), luts.data(), 4ull * luts.size(),
+                    cudaMemcpyHostToDevice) == cudaSuccess
+             ? ZC_OK
+             : ZC_ERR_CUDA;
+}
+
 // Workspace of a plan: the control block, then the statistics partials (one
 // per unit) or the encoder's look-back words followed by one statistics
 // partial per chunk (zc_compress_fit), whichever is larger; then the
@@ -209,12 +221,14 @@ int zc_plan_create(uint64_t n, const uint64_t* h_seg_off, uint32_t nseg, uint32_
     return ZC_ERR_ARG;
   }
   cudaGetDevice(&p->device);
-  if (cudaMalloc(&p->d_segs, sizeof(lbb::ZcSegDev) * nseg) != cudaSuccess) {
+  // segment records, then each segment's classification table
+  if (cudaMalloc(&p->d_segs, (sizeof(lbb::ZcSegDev) + 1024) * nseg) != cudaSuccess) {
     delete p;
     return ZC_ERR_NOMEM;
   }
   if (cudaMemcpy(p->d_segs, p->h_segs.data(), sizeof(lbb::ZcSegDev) * nseg,
-                 cudaMemcpyHostToDevice) != cudaSuccess) {
+                 cudaMemcpyHostToDevice) != cudaSuccess ||
+      upload_luts(p) != ZC_OK) {
     cudaFree(p->d_segs);
     delete p;
     return ZC_ERR_CUDA;
@@ -261,9 +275,12 @@ int zc_plan_set_books(zc_plan_t p, const uint8_t* h_books) {
   for (uint32_t s = 0; s < p->L.nseg; ++s) {
     std::memcpy(segs[s].book, h_books + 7 * s, 7);
     segs[s].book[7] = 0;
+    std::memcpy(p->h_segs[s].book, segs[s].book, 8);
   }
-  return cuda_rc(cudaMemcpy(p->d_segs, segs.data(), sizeof(lbb::ZcSegDev) * p->L.nseg,
-                            cudaMemcpyHostToDevice));
+  if (cudaMemcpy(p->d_segs, segs.data(), sizeof(lbb::ZcSegDev) * p->L.nseg,
+                 cudaMemcpyHostToDevice) != cudaSuccess)
+    return ZC_ERR_CUDA;
+  return upload_luts(p);
 }
 
 int zc_plan_info(zc_plan_t p, zc_stream_t stream, uint8_t* h_books, double* h_mu_sigma) {

@@ -54,6 +54,26 @@ struct ZcSegDev {
 };
 static_assert(sizeof(ZcSegDev) == 64, "segment record is 64 bytes");
 
+// The encoder's 256-entry classification table of a segment (entry e for
+// exponent field e): the 3-bit code's bits at bits 0, 8 and 16, or bit 24
+// for an escape.  Shifting an entry left by the element's index (0..7) drops
+// its bits into four per-plane bytes.  A plan keeps each segment's table
+// after its segment records, in the same device allocation (zc_seg_luts),
+// written wherever the codebook is set.
+__host__ __device__ inline uint32_t zc_lut_entry(const unsigned char* book, uint32_t e) {
+  uint32_t code = 0;
+  for (int j = 0; j < 7; ++j)
+    if (book[j] == e) code = (uint32_t)j + 1;
+  if (code == 0) return 1u << 24;
+  return (code & 1u) | (((code >> 1) & 1u) << 8) | (((code >> 2) & 1u) << 16);
+}
+__host__ __device__ inline uint32_t* zc_seg_luts(ZcSegDev* segs, uint32_t nseg) {
+  return reinterpret_cast<uint32_t*>(segs + nseg);
+}
+__host__ __device__ inline const uint32_t* zc_seg_luts(const ZcSegDev* segs, uint32_t nseg) {
+  return reinterpret_cast<const uint32_t*>(segs + nseg);
+}
+
 struct ZcLayout {
   unsigned long long n, nchunks, ntiles, nunits;
   uint32_t nseg, C, log2C, U;  // U: elements per statistics unit

@@ -68,18 +68,6 @@ __device__ __forceinline__ int find_chunk_segment(const ZcSegDev* segs, uint32_t
   return lo;
 }
 
-// Entry of the encode lookup table: bit 0/8/16 = bit 0/1/2 of the 3-bit code,
-// bit 24 = escape.  Shifting an entry left by the element's index (0..7)
-// drops its bits into four per-plane bytes.
-__device__ __forceinline__ uint32_t lut_entry(const unsigned char* book, uint32_t e) {
-  uint32_t code = 0;
-#pragma unroll
-  for (int j = 0; j < 7; ++j)
-    if (book[j] == e) code = (uint32_t)j + 1;
-  if (code == 0) return 1u << 24;
-  return (code & 1u) | (((code >> 1) & 1u) << 8) | (((code >> 2) & 1u) << 16);
-}
-
 __device__ __forceinline__ uint32_t sm4(uint32_t w0, uint32_t w1) {
   // sign+mantissa bytes of 4 consecutive bf16 held in w0, w1
   return (prmt(w0, w1, 0x7531) & 0x80808080u) | (prmt(w0, w1, 0x6420) & 0x7F7F7F7Fu);
@@ -226,7 +214,9 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
     for (uint32_t k = 0; k < nct; ++k) {
       const int sg = __shfl_sync(kFull, cseg, (int)k);
       if (sg >= 0 && s_lseg[warp][k] != sg) {
-        for (uint32_t e = lane; e < 256u; e += 32u) wlut[k * 256u + e] = lut_entry(A.segs[sg].book, e);
+        // the segment's table, kept by the plan
+        const uint32_t* src = zc_seg_luts(A.segs, L.nseg) + 256u * (uint32_t)sg;
+        for (uint32_t e = lane; e < 256u; e += 32u) wlut[k * 256u + e] = __ldg(src + e);
         __syncwarp();
         if (lane == 0) s_lseg[warp][k] = sg;
       }
@@ -338,11 +328,14 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
       st4[b4 + (1u ^ sw)] = make_uint4(w[4], w[5], w[6], w[7]);
       st4[b4 + (2u ^ sw)] = make_uint4(w[8], w[9], w[10], w[11]);
       st4[b4 + (3u ^ sw)] = make_uint4(w[12], w[13], w[14], w[15]);
-      const uint16_t* h = reinterpret_cast<const uint16_t*>(slotbuf);
+      // value i of the lane sits at half-word 32 * lane + (i ^ 8 * sw): its
+      // 16-byte piece i >> 3 was stored at piece (i >> 3) ^ sw
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(slotbuf) + 32u * lane;
+      const uint32_t sw8 = sw << 3;
       while (esc) {
         const uint32_t i = (uint32_t)__ffs(esc) - 1u;
         esc &= esc - 1;
-        const uint32_t hv = h[(b4 + ((i >> 3) ^ sw)) * 8u + (i & 7u)];
+        const uint32_t hv = h[i ^ sw8];
         if (pos < cap) dst[pos] = (uint8_t)((hv >> 7) & 0xFFu);
         ++pos;
       }

@@ -340,6 +340,7 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
   __shared__ float s_emf[256], s_epf[256], s_m7f, s_m8f;
   __shared__ uint32_t s_keyf[256];
   __shared__ int s_lastblk;
+  __shared__ unsigned char s_book[8];
   const int t = threadIdx.x;
   const uint32_t sg = blockIdx.x / K, kb = blockIdx.x % K;
   grid_dep_wait();  // the statistics partials
@@ -410,16 +411,26 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
   __syncthreads();
   if (!s_lastblk) return;  // another block of the segment finishes it
   const double mu = s_mu, sigma = s_sigma;
-  unsigned char* book = segs[sg].book;
+  // the codebook is built in s_book, then written with the segment's
+  // classification table (publish_book)
+  static_assert(kThreads == 256, "one thread per table entry");
+  auto publish_book = [&]() {
+    __syncthreads();
+    if (t < 8) segs[sg].book[t] = s_book[t];
+    zc_seg_luts(segs, nseg)[256u * sg + (uint32_t)t] = zc_lut_entry(s_book, (uint32_t)t);
+    if (t == 0) {
+      segs[sg].mu = mu;
+      segs[sg].sigma = sigma;
+    }
+  };
   if (!(sigma > 0.0)) {
     if (t == 0) {
       int lo = field_of(mu) - 3;
       lo = lo < 0 ? 0 : (lo > 248 ? 248 : lo);
-      for (int j = 0; j < 7; ++j) book[j] = (unsigned char)(lo + j);
-      book[7] = 0;
-      segs[sg].mu = mu;
-      segs[sg].sigma = sigma;
+      for (int j = 0; j < 7; ++j) s_book[j] = (unsigned char)(lo + j);
+      s_book[7] = 0;
     }
+    publish_book();
     return;
   }
   // Fast ranking in fp32.  Edge terms with erfcf of the fp64 argument rounded
@@ -534,13 +545,10 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
   if (take) {
     int pos = 0;
     for (int g = 1; g < t; ++g) pos += s_take[g];
-    book[pos] = (unsigned char)t;
+    s_book[pos] = (unsigned char)t;
   }
-  if (t == 0) {
-    book[7] = 0;
-    segs[sg].mu = mu;
-    segs[sg].sigma = sigma;
-  }
+  if (t == 0) s_book[7] = 0;
+  publish_book();
 }
 
 }  // namespace

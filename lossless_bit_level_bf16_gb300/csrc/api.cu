@@ -221,14 +221,27 @@ int zc_plan_create(uint64_t n, const uint64_t* h_seg_off, uint32_t nseg, uint32_
     return ZC_ERR_ARG;
   }
   cudaGetDevice(&p->device);
-  // segment records, then each segment's classification table
-  if (cudaMalloc(&p->d_segs, (sizeof(lbb::ZcSegDev) + 1024) * nseg) != cudaSuccess) {
+  // segment records, each segment's classification table, the segment of
+  // every chunk
+  if (cudaMalloc(&p->d_segs, (sizeof(lbb::ZcSegDev) + 1024) * nseg + 4ull * chunks) != cudaSuccess) {
     delete p;
     return ZC_ERR_NOMEM;
   }
+  std::vector<uint32_t> cseg;
+  try {
+    cseg.resize(chunks);
+  } catch (...) {
+    cudaFree(p->d_segs);
+    delete p;
+    return ZC_ERR_NOMEM;
+  }
+  for (uint32_t s = 0; s < nseg; ++s)
+    for (unsigned long long c = 0; c < p->h_segs[s].nchunks; ++c) cseg[p->h_segs[s].chunk_start + c] = s;
   if (cudaMemcpy(p->d_segs, p->h_segs.data(), sizeof(lbb::ZcSegDev) * nseg,
                  cudaMemcpyHostToDevice) != cudaSuccess ||
-      upload_luts(p) != ZC_OK) {
+      upload_luts(p) != ZC_OK ||
+      (chunks && cudaMemcpy(lbb::zc_chunk_seg(p->d_segs, nseg), cseg.data(), 4ull * chunks,
+                            cudaMemcpyHostToDevice) != cudaSuccess)) {
     cudaFree(p->d_segs);
     delete p;
     return ZC_ERR_CUDA;

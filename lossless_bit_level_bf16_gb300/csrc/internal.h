@@ -73,6 +73,13 @@ __host__ __device__ inline uint32_t* zc_seg_luts(ZcSegDev* segs, uint32_t nseg) 
 __host__ __device__ inline const uint32_t* zc_seg_luts(const ZcSegDev* segs, uint32_t nseg) {
   return reinterpret_cast<const uint32_t*>(segs + nseg);
 }
+// After the tables: the segment of every chunk (one word per chunk).
+__host__ __device__ inline uint32_t* zc_chunk_seg(ZcSegDev* segs, uint32_t nseg) {
+  return zc_seg_luts(segs, nseg) + 256ull * nseg;
+}
+__host__ __device__ inline const uint32_t* zc_chunk_seg(const ZcSegDev* segs, uint32_t nseg) {
+  return zc_seg_luts(segs, nseg) + 256ull * nseg;
+}
 
 struct ZcLayout {
   unsigned long long n, nchunks, ntiles, nunits;

@@ -51,23 +51,6 @@ struct EncArgs {
   int x_al16;
 };
 
-// Largest segment index whose chunk_start <= c (segments with no chunks are
-// skipped because a later one starts at the same chunk).
-__device__ __forceinline__ int find_chunk_segment(const ZcSegDev* segs, uint32_t nseg,
-                                                  unsigned long long c, unsigned long long nchunks) {
-  // segments of equal size: the proportional guess is the answer (one load)
-  uint32_t g = (uint32_t)(((double)c * (double)nseg) / (double)nchunks);
-  if (g >= nseg) g = nseg - 1;
-  if (segs[g].chunk_start <= c && c - segs[g].chunk_start < segs[g].nchunks) return (int)g;
-  int lo = 0, hi = (int)nseg - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (segs[mid].chunk_start <= c) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
 __device__ __forceinline__ uint32_t sm4(uint32_t w0, uint32_t w1) {
   // sign+mantissa bytes of 4 consecutive bf16 held in w0, w1
   return (prmt(w0, w1, 0x7531) & 0x80808080u) | (prmt(w0, w1, 0x6420) & 0x7F7F7F7Fu);
@@ -195,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
       const unsigned long long c = cfirst + lane;
       if (c < L.nchunks) {
         if (my_seg < 0 || c < my_c0 || c >= my_c1) {
-          my_seg = find_chunk_segment(A.segs, L.nseg, c, L.nchunks);
+          my_seg = (int)__ldg(zc_chunk_seg(A.segs, L.nseg) + c);  // the plan's chunk index
           my_c0 = A.segs[my_seg].chunk_start;
           my_c1 = my_c0 + A.segs[my_seg].nchunks;
         }

@@ -259,6 +259,13 @@ __device__ __forceinline__ void grid_dep_launch() {
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
   return __byte_perm(a, b, s);
 }
+// prmt.b32 in its default mode, where bit 3 of a selector nibble replicates
+// the selected byte's sign bit over the output byte.
+__device__ __forceinline__ uint32_t prmt_sx(uint32_t a, uint32_t b, uint32_t s) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(s));
+  return r;
+}
 
 // ---------------------------------------------------------------- warp sums
 

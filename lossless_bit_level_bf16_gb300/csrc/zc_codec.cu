@@ -692,10 +692,13 @@ __device__ bool load_seg(const uint8_t* in, const DecHdr& h, uint32_t s, SegRec&
   return rd_u64(q) + rd_u64(q + 8) == r.elem_start && rd_u64(q + 16) + rd_u64(q + 24) == r.chunk_start;
 }
 
-__device__ __forceinline__ uint32_t out_word(uint32_t S, uint32_t E, uint32_t sel) {
-  // two bf16 from (sign+mantissa byte, exponent byte) pairs
-  const uint32_t T = prmt(S, E, sel);  // [s0, e0, s1, e1]
-  return (T & 0x007F007Fu) | ((T >> 1) & 0x7F807F80u) | ((T << 8) & 0x80008000u);
+// Two bf16 from (sign+mantissa byte, exponent byte) pairs: selP takes each
+// sign+mantissa byte twice, the second time with its sign replicated over
+// the byte (selector bit 3), so that masking leaves the sign at bit 15 and
+// the mantissa at bits 0..6; selQ puts each exponent byte at bits 8..15 of
+// its half (zeros from the second operand elsewhere), one shift down.
+__device__ __forceinline__ uint32_t out_word(uint32_t S, uint32_t E, uint32_t selP, uint32_t selQ) {
+  return (prmt_sx(S, E, selP) & 0x807F807Fu) | (prmt(E, 0u, selQ) >> 1);
 }
 
 constexpr uint32_t kWarpEscBytes = 512;  // escape bytes a warp stages per chunk
@@ -908,14 +911,14 @@ __global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
       }
       if (valid) {
         uint32_t o[8];
-        o[0] = out_word(smv.x, E0, 0x5140);
-        o[1] = out_word(smv.x, E0, 0x7362);
-        o[2] = out_word(smv.y, E1, 0x5140);
-        o[3] = out_word(smv.y, E1, 0x7362);
-        o[4] = out_word(smv.z, E2, 0x5140);
-        o[5] = out_word(smv.z, E2, 0x7362);
-        o[6] = out_word(smv.w, E3, 0x5140);
-        o[7] = out_word(smv.w, E3, 0x7362);
+        o[0] = out_word(smv.x, E0, 0x9180, 0x1404);
+        o[1] = out_word(smv.x, E0, 0xB3A2, 0x3424);
+        o[2] = out_word(smv.y, E1, 0x9180, 0x1404);
+        o[3] = out_word(smv.y, E1, 0xB3A2, 0x3424);
+        o[4] = out_word(smv.z, E2, 0x9180, 0x1404);
+        o[5] = out_word(smv.z, E2, 0xB3A2, 0x3424);
+        o[6] = out_word(smv.w, E3, 0x9180, 0x1404);
+        o[7] = out_word(smv.w, E3, 0xB3A2, 0x3424);
         const unsigned long long elem = e0 + i0;
         if (valid == 16 && al) {
           st_v4(y + elem, make_uint4(o[0], o[1], o[2], o[3]));

@@ -83,8 +83,9 @@ int zc_version(void);
  * process (until switched off) leaves out the scan state of tile `tile` --
  * the tile whose stream length or escape count the later tiles wait for: an
  * 8192-slot ticket of the ZipCCL encoder, a tile of the IBP encoder (16 KB
- * of input up to 512-byte chunks, 4096 groups of the offsets pass up to
- * 2048-byte chunks, one group above) -- and limits every wait between thread
+ * of input up to 512-byte chunks, one group at 1024 and 2048 bytes, 4096
+ * groups of the offsets pass for the other chunk sizes up to 2048 bytes and
+ * in the three-launch encode, one group above) -- and limits every wait between thread
  * blocks to `max_spins` polls (0: the normal limit, about one second).  The
  * waits behind the missing state run out, the call sets ZC_ERR_TIMEOUT in
  * its status word and returns with a stream that must not be used; nothing
@@ -94,9 +95,10 @@ int zc_version(void);
 int zc_test_wait_fault(uint64_t tile, uint32_t max_spins);
 
 /* TEST ONLY -- the pages have no counterpart.  ibp_compress of chunks up to
- * 512 bytes normally runs one cooperative kernel (its blocks wait for each
- * other's tile lengths, so the driver must place the whole grid at once); when
- * the driver refuses that launch it takes the three-launch encode instead.
+ * 512 bytes, and of 1024 and 2048 bytes, normally runs one cooperative kernel
+ * (its blocks wait for each other's tile lengths, so the driver must place
+ * the whole grid at once); when the driver refuses that launch it takes the
+ * three-launch encode instead.
  * enable = 0 makes every such call take the three-launch encode (so tests can
  * check it), 1 restores the default.  Process-wide.  Returns ZC_OK. */
 int zc_test_ibp_single_pass(int enable);
@@ -255,7 +257,10 @@ int ibp_build_meta(const void* d_samples, uint64_t n_samples,
  * once (tiles are matched, their stream lengths published in the workspace
  * and their offsets resolved a few tiles later, while the input is still in
  * L2); if the driver cannot place its whole grid at once, the three kernels
- * below instead.  For chunk_bytes <= 2048: one memset and three kernels (a read-only pass that decides every
+ * below instead.  For chunk_bytes 1024 and 2048 the same, with a whole group
+ * per tile moved through shared memory 16 KB at a time (the workspace holds
+ * one stream length per group).  For the other chunk_bytes <= 2048: one
+ * memset and three kernels (a read-only pass that decides every
  * chunk's participation bit, a scan of the group lengths into the stream's
  * group-offset table, the packing pass); the workspace holds one
  * participation word per group between them.  Larger chunks: one memset and

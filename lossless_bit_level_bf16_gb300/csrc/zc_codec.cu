@@ -48,6 +48,7 @@ struct EncArgs {
   unsigned long long* states;  // look-back state per tile
   unsigned long long* bwords;  // look-back word per block of kLbBlock tiles
   StatPartial* parts;          // zc_compress_fit: one statistics partial per chunk
+  uint32_t* red_cnt;           // zc_compress_fit: the predictor's block counters, zeroed here
   int x_al16;
 };
 
@@ -86,6 +87,9 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const ZcLayout& L = A.L;
   const uint32_t C = L.C, log2C = L.log2C;
+  // the predictor that follows a fit reads these only once this kernel is done
+  if (STATS && A.red_cnt && blockIdx.x == 0)
+    for (uint32_t i = (uint32_t)t; i < L.nseg; i += kThreads) A.red_cnt[i] = 0;
   // chunk sizes that are powers of two divide by shifts; the others (any
   // multiple of 1024) by division, once per ticket and per 1024-slot step
   const bool p2 = (C & (C - 1)) == 0;
@@ -956,8 +960,6 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   const unsigned long long ntiles = (L.nchunks * (unsigned long long)L.C + tl - 1) / tl;
   char* lb = static_cast<char*>(d_ws) + kCtrlBytes;
   cudaError_t e = cudaMemsetAsync(d_ws, 0, kCtrlBytes + zc_enc_scratch_bytes(ntiles), s);
-  if (e == cudaSuccess && fit && L.kred_c > 1)  // the predictor's block counters
-    e = cudaMemsetAsync(static_cast<char*>(d_ws) + zc_cnt_offset(L), 0, 4ull * L.nseg, s);
   if (e != cudaSuccess) return e;
   e = arm_wait_fault(d_ws, s);
   if (e != cudaSuccess) return e;
@@ -974,6 +976,9 @@ cudaError_t zc_launch_compress(const ZcLayout& L, const ZcSegDev* d_segs,
   A.x_al16 = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
   A.parts = fit ? reinterpret_cast<StatPartial*>(static_cast<char*>(d_ws) + zc_fit_parts_offset(ntiles))
                 : nullptr;
+  A.red_cnt = fit && L.kred_c > 1
+                  ? reinterpret_cast<uint32_t*>(static_cast<char*>(d_ws) + zc_cnt_offset(L))
+                  : nullptr;
   const uint32_t nct = zc_chunks_per_tile(L.C);
   const size_t smem = (size_t)kEncWarps * (kStages * 2048u + nct * 1024u + 2 * kEscCap);
   auto k = fit ? zc_encode_kernel<true> : zc_encode_kernel<false>;

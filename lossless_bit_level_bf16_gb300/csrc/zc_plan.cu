@@ -83,11 +83,17 @@ constexpr int kStatRing = 3;
 constexpr uint32_t kStatSlotVecs = kStatBatch * 2 * 32;  // 16-byte pieces per batch
 constexpr size_t kStatSmem = (size_t)kStatWarps * kStatRing * kStatSlotVecs * 16;
 
+// red_cnt (not null when the predictor takes several blocks per segment):
+// the predictor's per-segment block counters, zeroed here by block 0 (the
+// predictor reads them only once this kernel has finished).
 __global__ void __launch_bounds__(kThreads, 2) zc_stats_kernel(
     const uint16_t* __restrict__ x, const ZcSegDev* __restrict__ segs, uint32_t nseg,
-    uint32_t U, unsigned long long nunits, StatPartial* __restrict__ parts, int x_al16) {
+    uint32_t U, unsigned long long nunits, StatPartial* __restrict__ parts, int x_al16,
+    uint32_t* red_cnt) {
   extern __shared__ uint4 s_ring[];
   const int lane = threadIdx.x & 31;
+  if (red_cnt && blockIdx.x == 0)
+    for (uint32_t i = threadIdx.x; i < nseg; i += blockDim.x) red_cnt[i] = 0;
   uint4* ring = s_ring + (size_t)(threadIdx.x >> 5) * kStatRing * kStatSlotVecs;
   grid_dep_launch();  // the predictor may be scheduled as blocks finish
   unsigned long long ub;
@@ -569,11 +575,8 @@ cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
                            const uint16_t* d_x, void* d_ws, cudaStream_t s) {
   StatPartial* parts = reinterpret_cast<StatPartial*>(static_cast<char*>(d_ws) + kCtrlBytes);
   const int al = (reinterpret_cast<uintptr_t>(d_x) & 15u) == 0;
-  if (L.kred_u > 1) {  // the predictor's block counters
-    const cudaError_t e =
-        cudaMemsetAsync(static_cast<char*>(d_ws) + zc_cnt_offset(L), 0, 4ull * L.nseg, s);
-    if (e != cudaSuccess) return e;
-  }
+  uint32_t* red_cnt =
+      L.kred_u > 1 ? reinterpret_cast<uint32_t*>(static_cast<char*>(d_ws) + zc_cnt_offset(L)) : nullptr;
   if (L.nunits) {
     cudaError_t e = cudaFuncSetAttribute(zc_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kStatSmem);
@@ -581,7 +584,8 @@ cudaError_t zc_launch_plan(const ZcLayout& L, const ZcSegDev* d_segs,
     const int res = resident_blocks((const void*)zc_stats_kernel, kThreads, kStatSmem);
     const unsigned long long need = (L.nunits + kStatWarps - 1) / kStatWarps;
     const unsigned grid = (unsigned)(need < (unsigned long long)res ? need : (unsigned long long)res);
-    zc_stats_kernel<<<grid, kThreads, kStatSmem, s>>>(d_x, d_segs, L.nseg, L.U, L.nunits, parts, al);
+    zc_stats_kernel<<<grid, kThreads, kStatSmem, s>>>(d_x, d_segs, L.nseg, L.U, L.nunits, parts, al,
+                                                      red_cnt);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

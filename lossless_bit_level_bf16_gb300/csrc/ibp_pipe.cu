@@ -166,19 +166,6 @@ __device__ __forceinline__ uint32_t vt_compress(const VecTab& v, uint32_t x, int
     return ((x >> v.MV[0][w]) & v.MV[1][w]) | (((x >> v.MV[2][w]) & v.MV[3][w]) << v.MV[4][w]);
   return hd_compress(x, v.K[w], &v.MV[0][w], 4);
 }
-// Inverse: the low kept-bit count of f spread out to the kept positions.
-__device__ __forceinline__ uint32_t vt_expand(const VecTab& v, uint32_t f, int w) {
-  if (v.fast)
-    return ((f & v.MV[1][w]) << v.MV[0][w]) | (((f >> v.MV[4][w]) & v.MV[3][w]) << v.MV[2][w]);
-  return hd_expand(f, v.K[w], &v.MV[0][w], 4);
-}
-
-// vt_expand for the three-run form.
-__device__ __forceinline__ uint32_t vt_expand3(const VecTab& v, uint32_t f, int w) {
-  return ((f & v.MV[1][w]) << v.MV[0][w]) | (((f >> v.MV[4][w]) & v.MV[3][w]) << v.MV[2][w]) |
-         (((f >> v.R3[2][w]) & v.R3[1][w]) << v.R3[0][w]);
-}
-
 // Kept bits per word of the vector (recomputed: cheaper than registers).
 __device__ __forceinline__ void kept_bits(const VecTab& v, uint32_t k[4]) {
 #pragma unroll
@@ -300,6 +287,44 @@ __device__ __forceinline__ void fill_chunk_table(uint32_t* coff, uint32_t t, uin
                                                  uint32_t B, uint32_t m) {
   if (t < 32)
     coff[t] = ((g + 32u + t * B - (uint32_t)__popc(pw & lowmask(t)) * m) << 1) | ((pw >> t) & 1u);
+}
+
+// Per-thread constants of the decoder's fast path, for the thread's vector
+// position when every keep mask of its 4 words has at most three runs of
+// ones: word w's field is the km[w] low bits read c_w bits into the vector's
+// run (c_0 = 0, then c1, c2, c3), and expands to ((f << a0) & M0) |
+// ((f << e1) & M1) | ((f << e2) & M2) (each run's mask already at its place
+// in the word), ORed with Bitval V.
+struct UnpackTab {
+  uint32_t km[4], c1, c2, c3;
+  uint32_t a0[4], M0[4], e1[4], M1[4], e2[4], M2[4], V[4];
+  uint32_t Pr;
+  bool ok, three;
+};
+
+// From a VecTab on which make_runs and make_runs3 ran.
+__device__ __forceinline__ void make_unpacktab(const VecTab& v, UnpackTab& u) {
+  u.ok = v.fast || v.fast3;
+  u.three = !v.fast && v.fast3;
+  uint32_t k[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    k[j] = __popc(v.K[j]);
+    u.km[j] = lowmask(k[j]);
+    u.a0[j] = v.MV[0][j];
+    u.M0[j] = v.MV[1][j] << v.MV[0][j];
+    const uint32_t m1 = v.MV[3][j], l0 = v.MV[4][j];
+    u.e1[j] = m1 ? v.MV[2][j] - l0 : 0u;
+    u.M1[j] = m1 << v.MV[2][j];
+    const uint32_t m2 = u.three ? v.R3[1][j] : 0u, l01 = u.three ? v.R3[2][j] : 0u;
+    u.e2[j] = m2 ? v.R3[0][j] - l01 : 0u;
+    u.M2[j] = m2 ? m2 << v.R3[0][j] : 0u;
+    u.V[j] = v.V[j];
+  }
+  u.c1 = k[0];
+  u.c2 = k[0] + k[1];
+  u.c3 = k[0] + k[1] + k[2];
+  u.Pr = v.Pr;
 }
 
 // x << s for s in 0..32 (0 at 32).
@@ -1797,11 +1822,13 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
   const unsigned long long* grp = reinterpret_cast<const unsigned long long*>(A.src + kIbp1Header);
   const uint32_t cap = A.stage_bytes - kStageSlack;
 
-  VecTab vt;
+  UnpackTab ut{};
   if (REG) {
-    load_vectab(T, (uint32_t)t & (A.vpc - 1), vt);
-    make_runs(vt);
-    make_runs3(vt);
+    VecTab v0;
+    load_vectab(T, (uint32_t)t & (A.vpc - 1), v0);
+    make_runs(v0);
+    make_runs3(v0);
+    make_unpacktab(v0, ut);
   }
 
   // warp 0: the span of this block's kk-th tile.  prefetch() loads its
@@ -1955,23 +1982,24 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
         const uint32_t q = c >> 5, i = c & 31;
         if (s_gbad[bf][q]) continue;
         live[e] = true;
-        if (!REG) load_vectab(T, r, vt);
         const uint32_t off = s_off[bf][q][i];
         uint32_t u[4];
         if ((s_pw[bf][q] >> i) & 1u) {
-          if (REG && (THREE ? (vt.fast || vt.fast3) : vt.fast)) {
+          if (REG && ut.ok) {
             // each word's field read at its own bit offset, expanded from runs
-            uint32_t pos = off + vt.Pr;
+            const uint32_t p0 = off + ut.Pr;
+            const uint32_t cw[4] = {0u, ut.c1, ut.c2, ut.c3};
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-              const uint32_t kw = __popc(vt.K[w]);
-              const uint32_t a = pos >> 5, sh = pos & 31;
-              uint32_t f = __funnelshift_r(sd[a], sd[a + 1], sh);
-              f &= kw >= 32 ? 0xFFFFFFFFu : ((1u << kw) - 1u);
-              o[e][w] = (THREE ? vt_expand3(vt, f, w) : vt_expand(vt, f, w)) | vt.V[w];
-              pos += kw;
+              const uint32_t pos = p0 + cw[w], a = pos >> 5, sh = pos & 31;
+              const uint32_t f = __funnelshift_r(sd[a], sd[a + 1], sh) & ut.km[w];
+              uint32_t x = ((f << ut.a0[w]) & ut.M0[w]) | ((f << ut.e1[w]) & ut.M1[w]);
+              if (THREE) x |= (f << ut.e2[w]) & ut.M2[w];
+              o[e][w] = x | ut.V[w];
             }
           } else {
+            VecTab vt;
+            load_vectab(T, r, vt);
             win128(sd, off + vt.Pr, u);
             uint32_t f[4];
             uint32_t kk[4];
@@ -2008,7 +2036,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ibp_decode_pipe_kernel(PipeArgs 
     if (warp == 0) issue(k + S, s);
   }
   };
-  if (__syncthreads_or(REG && vt.fast3 ? 1 : 0)) tiles(std::true_type{});
+  if (__syncthreads_or(REG && ut.three ? 1 : 0)) tiles(std::true_type{});
   else tiles(std::false_type{});
 }
 

@@ -329,8 +329,9 @@ __device__ int field_of(double v) {
 // K blocks per segment (block k of segment s is block s * K + k): block k
 // adds the fixed range k of the segment's partials; with K > 1 it files its
 // totals and the segment's last block to finish (a counter per segment,
-// zeroed by the launcher) adds the K totals in index order and goes on with
-// the codebook.  The sums depend only on the plan, not on which block is last.
+// zeroed by the kernel that wrote the partials) adds the K totals with the same fixed tree
+// as a range of partials and goes on with the codebook.  The sums depend
+// only on the plan, not on which block is last.
 __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
     ZcSegDev* __restrict__ segs, uint32_t nseg, unsigned long long nunits,
     const StatPartial* __restrict__ parts, int by_chunk, uint32_t K, StatPartial* red,
@@ -356,33 +357,48 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
   const unsigned long long per = (s1e - s0 + K - 1) / K;
   const unsigned long long u0 = s0 + per * kb < s1e ? s0 + per * kb : s1e;
   const unsigned long long u1 = u0 + per < s1e ? u0 + per : s1e;
-  double a = 0.0, b = 0.0;
-  unsigned long long c = 0;
-  for (unsigned long long u = u0 + t; u < u1; u += kThreads) {
-    a = __dadd_rn(a, parts[u].s1);
-    b = __dadd_rn(b, parts[u].s2);
-    c += parts[u].cnt;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = __dadd_rn(a, __shfl_down_sync(kFull, a, o));
-    b = __dadd_rn(b, __shfl_down_sync(kFull, b, o));
-    c += __shfl_down_sync(kFull, c, o);
-  }
-  if ((t & 31) == 0) {
-    s_r1[t >> 5] = a;
-    s_r2[t >> 5] = b;
-    s_rc[t >> 5] = c;
-  }
-  __syncthreads();
-  if (t == 0) {
-    double s1 = 0.0, s2 = 0.0;
-    unsigned long long n = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
-      s1 = __dadd_rn(s1, s_r1[w]);
-      s2 = __dadd_rn(s2, s_r2[w]);
-      n += s_rc[w];
+  // The block's sum of partials lo .. hi - 1: thread t adds lo + t,
+  // lo + t + 256, ... in index order, then a fixed shuffle tree per warp and
+  // the 8 warp sums in order; thread 0 gets the totals.
+  auto block_sum = [&](const StatPartial* p, unsigned long long lo, unsigned long long hi,
+                       double* r1, double* r2, unsigned long long* rc) {
+    double a = 0.0, b = 0.0;
+    unsigned long long c = 0;
+#pragma unroll 4
+    for (unsigned long long u = lo + t; u < hi; u += kThreads) {
+      a = __dadd_rn(a, __ldcg(&p[u].s1));
+      b = __dadd_rn(b, __ldcg(&p[u].s2));
+      c += __ldcg(&p[u].cnt);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a = __dadd_rn(a, __shfl_down_sync(kFull, a, o));
+      b = __dadd_rn(b, __shfl_down_sync(kFull, b, o));
+      c += __shfl_down_sync(kFull, c, o);
+    }
+    if ((t & 31) == 0) {
+      s_r1[t >> 5] = a;
+      s_r2[t >> 5] = b;
+      s_rc[t >> 5] = c;
+    }
+    __syncthreads();
+    if (t == 0) {
+      double s1 = 0.0, s2 = 0.0;
+      unsigned long long n = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        s1 = __dadd_rn(s1, s_r1[w]);
+        s2 = __dadd_rn(s2, s_r2[w]);
+        n += s_rc[w];
+      }
+      *r1 = s1;
+      *r2 = s2;
+      *rc = n;
+    }
+  };
+  double s1 = 0.0, s2 = 0.0;
+  unsigned long long n = 0;
+  block_sum(parts, u0, u1, &s1, &s2, &n);
+  if (t == 0) {
     s_lastblk = 1;
     if (K > 1) {
       StatPartial& mine = red[(unsigned long long)sg * K + kb];
@@ -391,19 +407,17 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
       mine.s2 = s2;
       __threadfence();
       s_lastblk = atomicAdd(cnt + sg, 1u) == K - 1;
-      if (s_lastblk) {
-        __threadfence();
-        s1 = 0.0;
-        s2 = 0.0;
-        n = 0;
-        for (uint32_t j = 0; j < K; ++j) {
-          const StatPartial* r = red + (unsigned long long)sg * K + j;
-          s1 = __dadd_rn(s1, __ldcg(&r->s1));
-          s2 = __dadd_rn(s2, __ldcg(&r->s2));
-          n += __ldcg(&r->cnt);
-        }
-      }
     }
+  }
+  __syncthreads();
+  if (!s_lastblk) return;  // another block of the segment finishes it
+  if (K > 1) {
+    // the segment's K block totals, read from L2 by the whole block and
+    // added in the same fixed order whichever block is last
+    __threadfence();
+    block_sum(red + (unsigned long long)sg * K, 0, K, &s1, &s2, &n);
+  }
+  if (t == 0) {
     double mu = 0.0, sigma = 0.0;
     if (n) {
       mu = __ddiv_rn(s1, (double)n);
@@ -415,7 +429,6 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
     s_is = sigma > 0.0 ? __drcp_rn(__dmul_rn(sigma, 1.4142135623730951)) : 0.0;  // 1/(sigma sqrt 2)
   }
   __syncthreads();
-  if (!s_lastblk) return;  // another block of the segment finishes it
   const double mu = s_mu, sigma = s_sigma;
   // the codebook is built in s_book, then written with the segment's
   // classification table (publish_book)

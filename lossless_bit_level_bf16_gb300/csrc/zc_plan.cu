@@ -23,8 +23,10 @@
 //                      ranked as integers (their fp64 bit patterns).
 //
 // Arithmetic of the statistics pass: the 16 values a thread holds are summed
-// (and their squares, exact in fp32 for bf16 inputs) as an fp32 tree (error
-// at most 4 units in the last place of the sum of magnitudes), the tree sums
+// (and their squares, exact in fp32 for bf16 inputs) with four fp32
+// additions on every value's path, run as packed fp32x2 operations on the
+// pairs of values that share a word (error at most 4 units in the last place
+// of the sum of magnitudes, as for a 16-leaf tree), the group sums
 // are accumulated as unevaluated fp32 pairs (error-free two-sum), the pairs
 // of a unit's lanes are added as pairs too, and only the unit's total is
 // formed in fp64 (an fp64 tree when a pair overflows fp32).  A
@@ -42,7 +44,7 @@ namespace lbb {
 namespace {
 
 #ifndef LBB_STAT_BATCH
-#define LBB_STAT_BATCH 4
+#define LBB_STAT_BATCH 2
 #endif
 constexpr int kStatBatch = LBB_STAT_BATCH;  // groups loaded before summing
 
@@ -77,7 +79,8 @@ constexpr int kStatWarps = kThreads / 32;
 // The warp's loads run ahead of its sums through a ring of kStatRing batches
 // in shared memory (cp.async: each lane copies the 16-byte pieces it will sum
 // itself, so the warp needs no synchronization), over its whole range of
-// units.  Units of a segment that does not start 16-byte aligned, and the
+// units.  Batches of 2 KB (two steps) in a 3-slot ring: 6 KB per warp, three
+// blocks per SM.  Units of a segment that does not start 16-byte aligned, and the
 // pieces at a unit's ragged end, are read with per-element loads when summed.
 constexpr int kStatRing = 3;
 constexpr uint32_t kStatSlotVecs = kStatBatch * 2 * 32;  // 16-byte pieces per batch
@@ -86,7 +89,7 @@ constexpr size_t kStatSmem = (size_t)kStatWarps * kStatRing * kStatSlotVecs * 16
 // red_cnt (not null when the predictor takes several blocks per segment):
 // the predictor's per-segment block counters, zeroed here by block 0 (the
 // predictor reads them only once this kernel has finished).
-__global__ void __launch_bounds__(kThreads, 2) zc_stats_kernel(
+__global__ void __launch_bounds__(kThreads, 3) zc_stats_kernel(
     const uint16_t* __restrict__ x, const ZcSegDev* __restrict__ segs, uint32_t nseg,
     uint32_t U, unsigned long long nunits, StatPartial* __restrict__ parts, int x_al16,
     uint32_t* red_cnt) {
@@ -204,23 +207,21 @@ __global__ void __launch_bounds__(kThreads, 2) zc_stats_kernel(
     for (int g = 0; g < kStatBatch; ++g) {
       const int valid = vh[g][0] + vh[g][1];
       if (valid == 0) continue;
-      float v[16];
+      // word j's two values as one fp32x2 pair; pairs j and j + 4 are added
+      // first, then the four sums in a tree, then the pair's two halves: every
+      // value goes through four additions, as in a 16-leaf tree
+      unsigned long long p1[4], p2[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        v[2 * j] = bf16_lo(w[g][j]);
-        v[2 * j + 1] = bf16_hi(w[g][j]);
+      for (int j = 0; j < 4; ++j) {
+        const unsigned long long a = f2_pack(bf16_lo(w[g][j]), bf16_hi(w[g][j]));
+        const unsigned long long b = f2_pack(bf16_lo(w[g][j + 4]), bf16_hi(w[g][j + 4]));
+        p1[j] = f2_add(a, b);
+        p2[j] = f2_fma(b, b, f2_mul(a, a));  // squares exact (bf16), one rounding each add
       }
-      float q[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) q[j] = __fmul_rn(v[j], v[j]);
-#pragma unroll
-      for (int st = 1; st < 16; st <<= 1) {
-#pragma unroll
-        for (int j = 0; j < 16; j += 2 * st) {
-          v[j] = __fadd_rn(v[j], v[j + st]);
-          q[j] = __fadd_rn(q[j], q[j + st]);
-        }
-      }
+      p1[0] = f2_add(f2_add(p1[0], p1[1]), f2_add(p1[2], p1[3]));
+      p2[0] = f2_add(f2_add(p2[0], p2[1]), f2_add(p2[2], p2[3]));
+      const float2 h1 = f2_unpack(p1[0]), h2 = f2_unpack(p2[0]);
+      float v[1] = {__fadd_rn(h1.x, h1.y)}, q[1] = {__fadd_rn(h2.x, h2.y)};
       // Squares below 2^-126 lose bits in fp32 (below 2^-149 they vanish):
       // when the group's sum of squares is under 2^-96 and a value is not
       // zero, the loss could exceed the fp32 rounding bound, so the group

@@ -231,18 +231,17 @@ __global__ void __launch_bounds__(kMetaThreads) ibp_meta_kernel(
   }
   if (mode == 0) {
     __syncthreads();
-    for (uint32_t w = t; w < W; w += kMetaThreads) {
-      uint32_t mk = 0, bv = 0;
-      for (int b = 0; b < 32; ++b) {
-        const unsigned long long o = ones[32u * w + b];
-        const unsigned long long agree = o > N - o ? o : N - o;
-        if (agree >= k) {
-          mk |= 1u << b;
-          if (o >= k) bv |= 1u << b;
-        }
+    // lane b of a warp decides position 32 w + b of word w; the warp's two
+    // votes are the word's Mask and Bitval
+    for (uint32_t j0 = (uint32_t)t & ~31u; j0 < B; j0 += kMetaThreads) {
+      const unsigned long long o = ones[j0 + (t & 31)];
+      const unsigned long long agree = o > N - o ? o : N - o;
+      const uint32_t mk = __ballot_sync(kFull, agree >= k);
+      const uint32_t bv = __ballot_sync(kFull, agree >= k && o >= k);
+      if ((t & 31) == 0) {
+        smask[j0 >> 5] = mk;
+        sbitv[j0 >> 5] = bv;
       }
-      smask[w] = mk;
-      sbitv[w] = bv;
     }
   } else {
     // candidates sorted by (agreement descending, position ascending)
@@ -295,22 +294,27 @@ __global__ void __launch_bounds__(kMetaThreads) ibp_meta_kernel(
   }
   const uint32_t m = block_sum_1024(pc, red);
   if (t == 0) {
-    unsigned long long h = 0xcbf29ce484222325ull;
-    const unsigned long long prime = 0x100000001b3ull;
-    for (int i = 0; i < 4; ++i) {
-      h ^= (chunk_bytes >> (8 * i)) & 0xFFu;
-      h *= prime;
-    }
-    for (uint32_t w = 0; w < W; ++w)
-      for (int i = 0; i < 4; ++i) {
-        h ^= (smask[w] >> (8 * i)) & 0xFFu;
-        h *= prime;
-      }
-    for (uint32_t w = 0; w < W; ++w)
-      for (int i = 0; i < 4; ++i) {
-        h ^= (sbitv[w] >> (8 * i)) & 0xFFu;
-        h *= prime;
-      }
+    // FNV-1a-64 over the chunk size (4 bytes, little-endian), Mask and
+    // Bitval.  The prime is 2^40 + 435, so h * prime = h * 435 + (h << 40):
+    // in 32-bit halves the low half's chain per byte is one XOR and one
+    // widening multiply, and the high half follows beside it.
+    uint32_t lo = 0x84222325u, hi = 0xcbf29ce4u;  // the offset basis
+    auto step = [&](uint32_t byte) {
+      lo ^= byte;
+      const unsigned long long p = (unsigned long long)lo * 435ull;
+      hi = hi * 435u + (uint32_t)(p >> 32) + (lo << 8);
+      lo = (uint32_t)p;
+    };
+    auto word = [&](uint32_t v) {
+      step(v & 0xFFu);
+      step((v >> 8) & 0xFFu);
+      step((v >> 16) & 0xFFu);
+      step(v >> 24);
+    };
+    word(chunk_bytes);
+    for (uint32_t w = 0; w < W; ++w) word(smask[w]);
+    for (uint32_t w = 0; w < W; ++w) word(sbitv[w]);
+    const unsigned long long h = ((unsigned long long)hi << 32) | lo;
     unsigned long long* hd = reinterpret_cast<unsigned long long*>(meta);
     hd[0] = (unsigned long long)kIbpmMagic | (1ull << 32) | ((unsigned long long)kIbpmHeader << 48);
     hd[1] = (unsigned long long)chunk_bytes | ((unsigned long long)B << 32);

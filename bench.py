@@ -409,35 +409,48 @@ def gpu_arm(args, rank, world, local_rank):
     hz = torch.empty(zsz, dtype=torch.uint8, pin_memory=True)
     hi = torch.empty(isz, dtype=torch.uint8, pin_memory=True)
     h_status = torch.empty(5 * 4, dtype=torch.uint8, pin_memory=True)
-    # the two codecs' chains (copy in, plan/meta, encode, decode, copy out)
-    # run on two streams, so one codec's copies overlap the other's kernels
-    zs, ist = torch.cuda.Stream(), torch.cuda.Stream()
-    zops, iops = ops[:3], ops[3:]
+    # The two codecs' chains (copy in, plan/meta, encode, decode, copy out)
+    # run on two streams, so one codec's copies overlap the other's kernels.
+    # The table goes over the host-to-device link first (the IBP chain is the
+    # longer one), the ZipCCL input after it; each codec's stream goes back
+    # on a stream of its own as soon as it is encoded, while it is decoded.
+    zs, ist, zos, ios = (torch.cuda.Stream() for _ in range(4))
+    zops, iops = dict(ops[:3]), dict(ops[3:])
     e2e_ms = []
     for it in range(args.warmup + args.steps):
         flush.add_(1)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        t_in, z_enc, i_enc = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
         a.record(stream)
-        zs.wait_event(a)
         ist.wait_event(a)
-        with torch.cuda.stream(zs):
-            wl.x.copy_(hx, non_blocking=True)
-            for _, fn in zops:
-                fn()
-            hz.copy_(wl.zout[:zsz], non_blocking=True)
-            for j, ws in enumerate((wl.plan.ws, wl.zdws)):
-                h_status[4 * j:4 * j + 4].copy_(ws[:4], non_blocking=True)
         with torch.cuda.stream(ist):
             wl.table.copy_(ht, non_blocking=True)
             wl.samples.copy_(hs, non_blocking=True)
-            for _, fn in iops:
-                fn()
-            hi.copy_(wl.iout[:isz], non_blocking=True)
+            t_in.record(ist)
+            iops["ibp_build_meta"]()
+            iops["ibp_compress"]()
+            i_enc.record(ist)
+            iops["ibp_decompress"]()
             for j, ws in enumerate((wl.mws, wl.iws, wl.idws)):
                 h_status[8 + 4 * j:12 + 4 * j].copy_(ws[:4], non_blocking=True)
-        stream.wait_stream(zs)
-        stream.wait_stream(ist)
+        ios.wait_event(i_enc)
+        with torch.cuda.stream(ios):
+            hi.copy_(wl.iout[:isz], non_blocking=True)
+        zs.wait_event(t_in)
+        with torch.cuda.stream(zs):
+            wl.x.copy_(hx, non_blocking=True)
+            zops["zc_plan"]()
+            zops["zc_compress"]()
+            z_enc.record(zs)
+            zops["zc_decompress"]()
+            for j, ws in enumerate((wl.plan.ws, wl.zdws)):
+                h_status[4 * j:4 * j + 4].copy_(ws[:4], non_blocking=True)
+        zos.wait_event(z_enc)
+        with torch.cuda.stream(zos):
+            hz.copy_(wl.zout[:zsz], non_blocking=True)
+        for st_ in (zs, ist, zos, ios):
+            stream.wait_stream(st_)
         b.record(stream)
         b.synchronize()
         if it >= args.warmup:

@@ -734,7 +734,7 @@ __device__ bool find_seg_checked(const uint8_t* in, const DecHdr& h, unsigned lo
 // step; no block
 // barrier after the header is read.  The chunk's escape bytes are staged in
 // the warp's shared-memory window when they fit (one 16-byte load per lane).
-__global__ void __launch_bounds__(kThreads, 4) zc_decode_kernel(
+__global__ void __launch_bounds__(kThreads, 3) zc_decode_kernel(
     const uint8_t* __restrict__ in, unsigned long long in_bytes, uint16_t* __restrict__ y,
     unsigned long long y_cap, Ctrl* ctrl, int y_al16) {
   __shared__ uint32_t s_nib[256];

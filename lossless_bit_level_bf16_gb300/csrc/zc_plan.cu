@@ -351,10 +351,11 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
   __shared__ unsigned char s_book[8];
   const int t = threadIdx.x;
   const uint32_t sg = blockIdx.x / K, kb = blockIdx.x % K;
-  grid_dep_wait();  // the statistics partials
+  // the segment's range of partials (fields fixed when the plan was made)
   const unsigned long long s0 = by_chunk ? segs[sg].chunk_start : segs[sg].unit_start;
   const unsigned long long s1e = by_chunk ? s0 + segs[sg].nchunks
                                           : ((sg + 1 < nseg) ? segs[sg + 1].unit_start : nunits);
+  grid_dep_wait();  // the statistics partials
   const unsigned long long per = (s1e - s0 + K - 1) / K;
   const unsigned long long u0 = s0 + per * kb < s1e ? s0 + per * kb : s1e;
   const unsigned long long u1 = u0 + per < s1e ? u0 + per : s1e;
@@ -463,7 +464,7 @@ __global__ void __launch_bounds__(kThreads) zc_predict_kernel(
   // whose exact masses are largest are the fp32 top 7, whatever the rounding
   // of an fp64 evaluation; the book is their set, in ascending order.
   if (t >= 1 && t <= 255) {
-    const double e = ldexp(1.0, t - 127), is = s_is;
+    const double e = __longlong_as_double((long long)(t - 127 + 1023) << 52), is = s_is;  // 2^(t-127)
     s_emf[t] = erfcf((float)__dmul_rn(__dsub_rn(e, mu), is));
     s_epf[t] = erfcf((float)__dmul_rn(__dadd_rn(e, mu), is));
   }

@@ -59,10 +59,33 @@ def csrc_hash():
     return h.hexdigest()[:12]
 
 
+def kernel_hash(kernel):
+    """sha1 (12 hex digits) over the CUDA source file that defines `kernel`
+    and every header the sources share (csrc/*.cuh, csrc/*.h, include/zc.h):
+    a committed traffic figure is used only while the kernel's own sources
+    are the ones it measured (an edit to another kernel's file leaves it
+    valid)."""
+    import glob
+    import hashlib
+    import re
+    csrc = os.path.join(ROOT, "lossless_bit_level_bf16_gb300", "csrc")
+    pat = re.compile(r"__global__[^;{]*?\b" + re.escape(kernel) + r"\s*\(", re.S)
+    tus = [p for p in sorted(glob.glob(os.path.join(csrc, "*.cu"))) if pat.search(open(p).read())]
+    if len(tus) != 1:
+        raise KeyError(f"{kernel}: defined in {len(tus)} source files")
+    heads = sorted(glob.glob(os.path.join(csrc, "*.cuh")) + glob.glob(os.path.join(csrc, "*.h")))
+    heads.append(os.path.join(ROOT, "include", "zc.h"))
+    h = hashlib.sha1()
+    for path in tus + heads:
+        h.update(os.path.basename(path).encode())
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:12]
+
+
 def _traffic_table():
     """Measured DRAM traffic per launch from the committed ncu summaries, as
     {kernel: {sha1: [(bytes per launch, uncompressed bytes, case), ...]}}.
-    Lines in profiles/*.md read 'traffic <kernel> <sources sha1> <bytes>
+    Lines in profiles/*.md read 'traffic <kernel> <kernel_hash> <bytes>
     <uncompressed bytes of the captured launch> <case>', the case naming the
     data and chunking the capture ran on (a kernel may have lines from several
     captures)."""
@@ -86,7 +109,7 @@ def measured_traffic(kernel, case, unc, table=None, sha=None):
     and chunking).  Returns (bytes, captured uncompressed bytes), or
     (None, None) when no capture of that case matches the sources."""
     table = _traffic_table() if table is None else table
-    sha = csrc_hash() if sha is None else sha
+    sha = kernel_hash(kernel) if sha is None else sha
     for nbytes, cap, c in table.get(kernel, {}).get(sha, []):
         if c == case:
             return (nbytes if cap == unc else round(nbytes * unc / cap)), cap

@@ -37,6 +37,8 @@
 // plan: the partition into units and every reduction order are fixed.
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -143,6 +145,13 @@ __global__ void __launch_bounds__(kThreads, 3) zc_stats_kernel(
   };
   auto issue = [&](const Cursor& c, int slot) {
     if (!c.al) return;
+    if (c.hi - c.base >= kStatBatch * 512ull) {  // the whole batch: no test per piece
+      uint4* dst = ring + (size_t)slot * kStatSlotVecs + lane;
+      const uint16_t* src = x + c.base + 8ull * lane;
+#pragma unroll
+      for (int p = 0; p < 2 * kStatBatch; ++p) cp_async16(dst + 32 * p, src + 256 * p);
+      return;
+    }
 #pragma unroll
     for (int g = 0; g < kStatBatch; ++g)
 #pragma unroll
@@ -179,79 +188,91 @@ __global__ void __launch_bounds__(kThreads, 3) zc_stats_kernel(
     cp_async_commit();
     islot = islot + 1 == kStatRing ? 0 : islot + 1;
     cp_async_wait_group<kStatRing - 1>();  // this lane's pieces of the batch
-    uint32_t w[kStatBatch][8];
-    int vh[kStatBatch][2];
+    // The batch, compiled twice: FULL (the unit is 16-byte aligned and the
+    // batch lies wholly inside it, every piece in the ring: no test per
+    // piece) and the general form (pieces past the unit's end count 0
+    // values, pieces of an unaligned unit are read one value at a time).
+    auto batch = [&](auto full_tag) {
+      constexpr bool FULL = decltype(full_tag)::value;
+      uint32_t w[kStatBatch][8];
+      int vh[kStatBatch][2];
 #pragma unroll
-    for (int g = 0; g < kStatBatch; ++g) {
+      for (int g = 0; g < kStatBatch; ++g) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const unsigned long long e0 = cc.base + g * 512ull + 256ull * h + 8ull * lane;
-        const unsigned long long rem = e0 < cc.hi ? cc.hi - e0 : 0ull;
-        const int v = rem < 8 ? (int)rem : 8;
-        vh[g][h] = v;
-        if (v == 8 && cc.al) {
-          const uint4 a4 = ring[(size_t)cslot * kStatSlotVecs + (2 * g + h) * 32 + lane];
-          w[g][4 * h] = a4.x; w[g][4 * h + 1] = a4.y; w[g][4 * h + 2] = a4.z; w[g][4 * h + 3] = a4.w;
+        for (int h = 0; h < 2; ++h) {
+          const unsigned long long e0 = cc.base + g * 512ull + 256ull * h + 8ull * lane;
+          int v = 8;
+          if (!FULL) {
+            const unsigned long long rem = e0 < cc.hi ? cc.hi - e0 : 0ull;
+            v = rem < 8 ? (int)rem : 8;
+          }
+          vh[g][h] = v;
+          if (FULL || (v == 8 && cc.al)) {
+            const uint4 a4 = ring[(size_t)cslot * kStatSlotVecs + (2 * g + h) * 32 + lane];
+            w[g][4 * h] = a4.x; w[g][4 * h + 1] = a4.y; w[g][4 * h + 2] = a4.z; w[g][4 * h + 3] = a4.w;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t l = (2 * j < v) ? (uint32_t)__ldg(x + e0 + 2 * j) : 0u;
+              const uint32_t hh = (2 * j + 1 < v) ? (uint32_t)__ldg(x + e0 + 2 * j + 1) : 0u;
+              w[g][4 * h + j] = l | (hh << 16);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kStatBatch; ++g) {
+        const int valid = FULL ? 16 : vh[g][0] + vh[g][1];
+        if (!FULL && valid == 0) continue;
+        // word j's two values as one fp32x2 pair; pairs j and j + 4 are added
+        // first, then the four sums in a tree, then the pair's two halves:
+        // every value goes through four additions, as in a 16-leaf tree
+        unsigned long long p1[4], p2[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const unsigned long long a = f2_pack(bf16_lo(w[g][j]), bf16_hi(w[g][j]));
+          const unsigned long long b = f2_pack(bf16_lo(w[g][j + 4]), bf16_hi(w[g][j + 4]));
+          p1[j] = f2_add(a, b);
+          p2[j] = f2_fma(b, b, f2_mul(a, a));  // squares exact (bf16), one rounding each add
+        }
+        p1[0] = f2_add(f2_add(p1[0], p1[1]), f2_add(p1[2], p1[3]));
+        p2[0] = f2_add(f2_add(p2[0], p2[1]), f2_add(p2[2], p2[3]));
+        const float2 h1 = f2_unpack(p1[0]), h2 = f2_unpack(p2[0]);
+        const float sv = __fadd_rn(h1.x, h1.y), sq = __fadd_rn(h2.x, h2.y);
+        // Squares below 2^-126 lose bits in fp32 (below 2^-149 they vanish):
+        // when the group's sum of squares is under 2^-96 and a value is not
+        // zero, the loss could exceed the fp32 rounding bound, so the group
+        // goes to fp64 like a non-finite one.
+        bool fast = isfinite(sv) && isfinite(sq);
+        if (fast && sq < 0x1p-96f) {
+          uint32_t nz = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) nz |= w[g][j] & 0x7FFF7FFFu;
+          fast = nz == 0;
+        }
+        if (fast) {
+          two_sum_acc(hx, lx, sv);
+          two_sum_acc(hq, lq, sq);
+          cnt += (unsigned long long)valid;
         } else {
+          // an inf/NaN input, an fp32 overflow or underflow: redo these
+          // values in fp64
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t l = (2 * j < v) ? (uint32_t)__ldg(x + e0 + 2 * j) : 0u;
-            const uint32_t hh = (2 * j + 1 < v) ? (uint32_t)__ldg(x + e0 + 2 * j + 1) : 0u;
-            w[g][4 * h + j] = l | (hh << 16);
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t bits = (j & 1) ? (w[g][j >> 1] >> 16) : (w[g][j >> 1] & 0xFFFFu);
+            if ((j & 7) < vh[g][j >> 3] && ((bits >> 7) & 0xFFu) != 0xFFu) {
+              const double d = (double)__uint_as_float(bits << 16);
+              dx = __dadd_rn(dx, d);
+              dq = __dadd_rn(dq, __dmul_rn(d, d));
+              cnt += 1;
+            }
           }
         }
       }
-    }
+    };
+    if (cc.al && cc.hi - cc.base >= kStatBatch * 512ull) batch(std::true_type{});
+    else batch(std::false_type{});
     cslot = cslot + 1 == kStatRing ? 0 : cslot + 1;
-#pragma unroll
-    for (int g = 0; g < kStatBatch; ++g) {
-      const int valid = vh[g][0] + vh[g][1];
-      if (valid == 0) continue;
-      // word j's two values as one fp32x2 pair; pairs j and j + 4 are added
-      // first, then the four sums in a tree, then the pair's two halves: every
-      // value goes through four additions, as in a 16-leaf tree
-      unsigned long long p1[4], p2[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const unsigned long long a = f2_pack(bf16_lo(w[g][j]), bf16_hi(w[g][j]));
-        const unsigned long long b = f2_pack(bf16_lo(w[g][j + 4]), bf16_hi(w[g][j + 4]));
-        p1[j] = f2_add(a, b);
-        p2[j] = f2_fma(b, b, f2_mul(a, a));  // squares exact (bf16), one rounding each add
-      }
-      p1[0] = f2_add(f2_add(p1[0], p1[1]), f2_add(p1[2], p1[3]));
-      p2[0] = f2_add(f2_add(p2[0], p2[1]), f2_add(p2[2], p2[3]));
-      const float2 h1 = f2_unpack(p1[0]), h2 = f2_unpack(p2[0]);
-      float v[1] = {__fadd_rn(h1.x, h1.y)}, q[1] = {__fadd_rn(h2.x, h2.y)};
-      // Squares below 2^-126 lose bits in fp32 (below 2^-149 they vanish):
-      // when the group's sum of squares is under 2^-96 and a value is not
-      // zero, the loss could exceed the fp32 rounding bound, so the group
-      // goes to fp64 like a non-finite one.
-      bool fast = isfinite(v[0]) && isfinite(q[0]);
-      if (fast && q[0] < 0x1p-96f) {
-        uint32_t nz = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) nz |= w[g][j] & 0x7FFF7FFFu;
-        fast = nz == 0;
-      }
-      if (fast) {
-        two_sum_acc(hx, lx, v[0]);
-        two_sum_acc(hq, lq, q[0]);
-        cnt += (unsigned long long)valid;
-      } else {
-        // an inf/NaN input, an fp32 overflow or underflow: redo these values
-        // in fp64
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t bits = (j & 1) ? (w[g][j >> 1] >> 16) : (w[g][j >> 1] & 0xFFFFu);
-          if ((j & 7) < vh[g][j >> 3] && ((bits >> 7) & 0xFFu) != 0xFFu) {
-            const double d = (double)__uint_as_float(bits << 16);
-            dx = __dadd_rn(dx, d);
-            dq = __dadd_rn(dq, __dmul_rn(d, d));
-            cnt += 1;
-          }
-        }
-      }
-    }
     if (cc.base + kStatBatch * 512ull >= cc.hi) {
       // the unit's last batch: lanes' fp32 pairs, fp64 if a pair overflows or
       // fp64 sums exist

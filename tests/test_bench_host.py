@@ -5,6 +5,8 @@ import glob
 import os
 import re
 
+import pytest
+
 import bench
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -88,6 +90,20 @@ def test_source_hash_covers_every_cuda_source():
     assert any(s.endswith(".cu") for s in srcs) and any(s.endswith(".cuh") for s in srcs)
     h = bench.csrc_hash()
     assert re.fullmatch(r"[0-9a-f]{12}", h) and h == bench.csrc_hash()
+
+
+def test_kernel_hash_follows_the_kernels_own_sources():
+    """A kernel's hash covers its own source file and the shared headers:
+    kernels of one file share it, kernels of different files differ, and a
+    name no source defines is refused."""
+    ws, dec = bench.kernel_hash("ibp_encode_ws_kernel"), bench.kernel_hash("ibp_decode_pipe_kernel")
+    zenc, zdec = bench.kernel_hash("zc_encode_kernel"), bench.kernel_hash("zc_decode_kernel")
+    stats = bench.kernel_hash("zc_stats_kernel")
+    assert all(re.fullmatch(r"[0-9a-f]{12}", h) for h in (ws, dec, zenc, zdec, stats))
+    assert ws == dec and zenc == zdec
+    assert len({ws, zenc, stats}) == 3
+    with pytest.raises(KeyError):
+        bench.kernel_hash("no_such_kernel")
 
 
 def test_peaks_come_from_the_measured_file():

@@ -78,11 +78,15 @@ static_assert(kLbBlock == kZcLbBlock, "the scratch layout and the look-back agre
 // operations, then fp32 (sum, error)
 // pairs across steps; a step whose fp32 sums are not finite, or whose squares
 // may have underflowed, is summed in fp64), and the warp writes each chunk's
-// count and fp64 sums to A.parts when the chunk's last step is done.
+// count and fp64 sums to A.parts when the chunk's last step is done.  The
+// lane's rare fp64 sums live in shared memory (s_stdx, s_stdq) and its count
+// in 32 bits (a chunk has at most 65536 values), so that both forms of the
+// kernel run at three blocks per SM.
 template <bool STATS>
-__global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncArgs A) {
+__global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ int s_lseg[kEncWarps][kMaxLutSlots];
+  __shared__ double s_stdx[STATS ? kEncWarps : 1][32], s_stdq[STATS ? kEncWarps : 1][32];
   __shared__ uint32_t s_cs[kEncWarps][kMaxLutSlots];  // escape position where a chunk starts
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const ZcLayout& L = A.L;
@@ -158,8 +162,11 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
   unsigned long long my_c0 = 0, my_c1 = 0;
   // statistics of the chunk being classified (STATS only)
   float st_hx = 0.f, st_lx = 0.f, st_hq = 0.f, st_lq = 0.f;
-  double st_dx = 0.0, st_dq = 0.0;
-  unsigned long long st_cnt = 0;
+  uint32_t st_cnt = 0;  // values of the chunk summed so far (a chunk has at most 65536)
+  if constexpr (STATS) {
+    s_stdx[warp][lane] = 0.0;
+    s_stdq[warp][lane] = 0.0;
+  }
 
   // A ticket is taken only when the warp is ready to work on it: taking the
   // next one early delays its published escape count, which other warps'
@@ -383,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
         if (fast) {
           two_sum_acc(st_hx, st_lx, t1);
           two_sum_acc(st_hq, st_lq, t2);
-          st_cnt += (unsigned long long)valid;
+          st_cnt += (uint32_t)valid;
         } else {  // an inf/NaN value, an fp32 overflow or underflow: fp64, finite values only
           // (rare: the lane's values are read again, one at a time)
           const uint16_t* xs = A.x + e0 + s0 + 32u * lane;
@@ -392,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
             const uint32_t bits = xs[j];
             if (((bits >> 7) & 0xFFu) != 0xFFu) {
               const double d = (double)__uint_as_float(bits << 16);
-              st_dx = __dadd_rn(st_dx, d);
-              st_dq = __dadd_rn(st_dq, __dmul_rn(d, d));
+              s_stdx[warp][lane] = __dadd_rn(s_stdx[warp][lane], d);
+              s_stdq[warp][lane] = __dadd_rn(s_stdq[warp][lane], __dmul_rn(d, d));
               st_cnt += 1;
             }
           }
@@ -401,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
         if (s0 + 1024u == C || st + 1 == steps) {  // the chunk's last step (warp-uniform)
           float ax = st_hx, bx = st_lx, aq = st_hq, bq = st_lq;
           unsigned long long n = st_cnt;
+          const double st_dx = s_stdx[warp][lane], st_dq = s_stdq[warp][lane];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
             const float ax2 = __shfl_down_sync(kFull, ax, o), bx2 = __shfl_down_sync(kFull, bx, o);
@@ -426,7 +434,8 @@ __global__ void __launch_bounds__(kThreads, STATS ? 2 : 3) zc_encode_kernel(EncA
           }
           if (lane == 0) A.parts[c] = StatPartial{n, r1, r2};
           st_hx = st_lx = st_hq = st_lq = 0.f;
-          st_dx = st_dq = 0.0;
+          s_stdx[warp][lane] = 0.0;
+          s_stdq[warp][lane] = 0.0;
           st_cnt = 0;
         }
       }

@@ -88,6 +88,10 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   __shared__ int s_lseg[kEncWarps][kMaxLutSlots];
   __shared__ double s_stdx[STATS ? kEncWarps : 1][32], s_stdq[STATS ? kEncWarps : 1][32];
   __shared__ uint32_t s_cs[kEncWarps][kMaxLutSlots];  // escape position where a chunk starts
+  // the pending (previous) ticket of each warp: its index, first chunk, escape
+  // count, staging window, and its chunks' escape starts (lanes < chunks per ticket)
+  __shared__ unsigned long long s_ptile[kEncWarps], s_pcfirst[kEncWarps];
+  __shared__ uint32_t s_prun[kEncWarps], s_pbuf[kEncWarps], s_pcs[kEncWarps][kMaxLutSlots];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const ZcLayout& L = A.L;
   const uint32_t C = L.C, log2C = L.log2C;
@@ -113,8 +117,6 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
   // have published), so the warp never waits on the look-back with its
   // slots still to write.
   bool p_has = false;
-  unsigned long long p_tile = 0, p_tlane0 = 0, p_cfirst = 0;
-  uint32_t p_run = 0, p_cs = 0, p_buf = 0;
   // a ticket's inclusive prefix (after a timeout: its own count, and nothing
   // for its block, so that no one waits)
   const unsigned lim = wait_limit(A.ctrl);
@@ -131,6 +133,8 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     }
   };
   auto resolve = [&]() {
+    const unsigned long long p_tile = s_ptile[warp], p_cfirst = s_pcfirst[warp];
+    const uint32_t p_run = s_prun[warp], p_buf = s_pbuf[warp];
     bool to = false;
     const unsigned long long excl = lb2_lookback<4>(A.states, A.bwords, p_tile, &to, lim);
     publish_inc(p_tile, excl, p_run, to);
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     }
     if (lane < (int)nct) {
       const unsigned long long c = p_cfirst + lane;
-      if (c < L.nchunks) reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = excl + p_cs;
+      if (c < L.nchunks) reinterpret_cast<unsigned long long*>(A.out + L.off_escoff)[c] = excl + s_pcs[warp][lane];
     }
     __syncwarp();
     p_has = false;
@@ -493,12 +497,14 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
       if (lane == 0 && tile + 1 != fault1) lb2_publish_agg(A.states, A.bwords, tile, run);
       if (p_has) resolve();
       p_has = true;
-      p_tile = tile;
-      p_tlane0 = tlane0;
-      p_cfirst = cfirst;
-      p_run = run;
-      p_cs = cs_pos;
-      p_buf = buf;
+      if (lane == 0) {
+        s_ptile[warp] = tile;
+        s_pcfirst[warp] = cfirst;
+        s_prun[warp] = run;
+        s_pbuf[warp] = buf;
+      }
+      if (lane < kMaxLutSlots) s_pcs[warp][lane] = cs_pos;
+      __syncwarp();
       buf ^= 1u;
       wst = wst_base + buf * kEscCap;
       continue;

@@ -106,6 +106,22 @@ def test_kernel_hash_follows_the_kernels_own_sources():
         bench.kernel_hash("no_such_kernel")
 
 
+def test_every_bench_kernel_has_one_defining_source():
+    """Each kernel the bench names for an op is defined in exactly one CUDA
+    source file, so its traffic figures are keyed by that file's hash; and
+    every committed traffic line names such a kernel."""
+    names = set()
+    for op in ("zc_plan", "zc_compress", "zc_compress_fit", "zc_decompress", "ibp_build_meta",
+               "ibp_decompress"):
+        names.update(bench.kernels_of(op))
+    for cb in (512, 1024, 2048, 1536):
+        names.update(bench.kernels_of("ibp_compress", cb))
+    for k in sorted(names):
+        assert re.fullmatch(r"[0-9a-f]{12}", bench.kernel_hash(k)), k
+    for k in bench._traffic_table():
+        assert k in names, k
+
+
 def test_peaks_come_from_the_measured_file():
     peak, kind = bench._peaks()
     if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")):

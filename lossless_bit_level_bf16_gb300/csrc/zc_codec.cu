@@ -208,18 +208,6 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
     const unsigned long long t_e0 = __shfl_sync(kFull, ce0, 0);
     const uint32_t t_val = __shfl_sync(kFull, cval, 0);
     const bool t_al = __shfl_sync(kFull, cal, 0) != 0;
-    // lookup tables of the ticket's chunks (rebuilt only when the segment changes)
-    for (uint32_t k = 0; k < nct; ++k) {
-      const int sg = __shfl_sync(kFull, cseg, (int)k);
-      if (sg >= 0 && s_lseg[warp][k] != sg) {
-        // the segment's table, kept by the plan
-        const uint32_t* src = zc_seg_luts(A.segs, L.nseg) + 256u * (uint32_t)sg;
-        for (uint32_t e = lane; e < 256u; e += 32u) wlut[k * 256u + e] = __ldg(src + e);
-        __syncwarp();
-        if (lane == 0) s_lseg[warp][k] = sg;
-      }
-    }
-    __syncwarp();
 
     // ---- steps of 1024 slots, 32 consecutive slots per lane: a lane builds whole
     // 32-bit plane words; a step lies inside one chunk (C is a multiple of 1024)
@@ -341,6 +329,19 @@ __global__ void __launch_bounds__(kThreads, 3) zc_encode_kernel(EncArgs A) {
 
 #pragma unroll
     for (uint32_t k = 0; k < kAhead; ++k) issue(k);
+    // lookup tables of the ticket's chunks (rebuilt only when the segment
+    // changes), copied while the first step's input is on its way
+    for (uint32_t k = 0; k < nct; ++k) {
+      const int sg = __shfl_sync(kFull, cseg, (int)k);
+      if (sg >= 0 && s_lseg[warp][k] != sg) {
+        // the segment's table, kept by the plan
+        const uint32_t* src = zc_seg_luts(A.segs, L.nseg) + 256u * (uint32_t)sg;
+        for (uint32_t e = lane; e < 256u; e += 32u) wlut[k * 256u + e] = __ldg(src + e);
+        __syncwarp();
+        if (lane == 0) s_lseg[warp][k] = sg;
+      }
+    }
+    __syncwarp();
     for (uint32_t st = 0; st < steps; ++st) {
       issue(st + kAhead);
       int lct;
